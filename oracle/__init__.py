@@ -1,0 +1,207 @@
+"""ctypes front end of the fp64 CPU oracle (``mog_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  It never touches the CUDA
+library and the CUDA library never touches it.
+
+Every function takes bf16 data as ``uint16`` bit patterns and returns numpy arrays.
+Summaries are returned as a dict with keys ``cl_n, cl_mu, cl_var, cl_vbar, sub_n,
+sub_mu, sub_var, sub_vbar`` (counts int32, the rest float64, shapes ``[C]``,
+``[C, d]``, ``[C*L]``, ``[C*L, d]``).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mog_oracle.c")
+_LIB = os.path.join(_HERE, "libmog_oracle.so")
+
+_i64 = C.c_int64
+_dbl = C.c_double
+_p = C.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp contraction off, OpenMP on)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call([
+            "gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fopenmp",
+            "-o", tmp, _SRC, "-lm",
+        ])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        l = C.CDLL(_LIB)
+        for name in ("ora_assign", "ora_lloyd", "ora_stats", "ora_build", "ora_select",
+                     "ora_decode", "ora_dense"):
+            getattr(l, name).restype = C.c_int
+        _lib = l
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_p)
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 inputs are uint16 bit patterns")
+    return a
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise RuntimeError(f"oracle {name} failed with code {rc}")
+
+
+def tau_of(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def assign(x: np.ndarray, cent: np.ndarray, rows=None) -> np.ndarray:
+    """Nearest centroid (canonical fp64 distance, lowest index on ties) of x[rows]."""
+    x = _u16(x)
+    d = x.shape[1]
+    rows = np.arange(x.shape[0], dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    cent = np.ascontiguousarray(cent, np.float64)
+    out = np.empty(rows.shape[0], np.int32)
+    _check(lib().ora_assign(_ptr(x), _i64(d), _ptr(rows), _i64(rows.shape[0]), _ptr(cent),
+                            _i64(cent.shape[0]), _i64(d), _ptr(out)), "assign")
+    return out
+
+
+def lloyd(x: np.ndarray, k: int, iters: int, rows=None, history: bool = False):
+    """Lloyd's algorithm with strided seeding.  Returns (cent, assign, steps, hist)."""
+    x = _u16(x)
+    d = x.shape[1]
+    rows = np.arange(x.shape[0], dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    cent = np.empty((k, d), np.float64)
+    asg = np.empty(rows.shape[0], np.int32)
+    hist = np.zeros((iters, k, d), np.float64) if history else None
+    steps = np.zeros(1, np.int64)
+    _check(lib().ora_lloyd(_ptr(x), _i64(d), _ptr(rows), _i64(rows.shape[0]), _i64(k), _i64(d),
+                           _i64(iters), _ptr(cent), _ptr(asg), _ptr(hist), _ptr(steps)), "lloyd")
+    s = int(steps[0])
+    return cent, asg, s, (hist[:s] if history else None)
+
+
+def _summ_buffers(Cn: int, L: int, d: int):
+    return dict(
+        cl_n=np.zeros(Cn, np.int32), cl_mu=np.zeros((Cn, d)), cl_var=np.zeros((Cn, d)),
+        cl_vbar=np.zeros((Cn, d)), sub_n=np.zeros(Cn * L, np.int32),
+        sub_mu=np.zeros((Cn * L, d)), sub_var=np.zeros((Cn * L, d)), sub_vbar=np.zeros((Cn * L, d)),
+    )
+
+
+def _summ_args(s):
+    return [_ptr(s[k]) for k in ("cl_n", "cl_mu", "cl_var", "cl_vbar", "sub_n", "sub_mu",
+                                 "sub_var", "sub_vbar")]
+
+
+def stats(K: np.ndarray, V: np.ndarray, perm: np.ndarray, sub_off: np.ndarray, Cn: int, L: int):
+    """Gaussian summaries of a given (cluster, subcluster) partition."""
+    K, V = _u16(K), _u16(V)
+    d = K.shape[1]
+    perm = np.ascontiguousarray(perm, np.int32)
+    sub_off = np.ascontiguousarray(sub_off, np.int32)
+    s = _summ_buffers(Cn, L, d)
+    _check(lib().ora_stats(_ptr(K), _ptr(V), _i64(d), _i64(d), _ptr(perm), _ptr(sub_off),
+                           _i64(Cn), _i64(L), *_summ_args(s)), "stats")
+    return s
+
+
+def build_unit(K: np.ndarray, V: np.ndarray, n_build: int, S: int, R: int, Cn: int, L: int,
+               T1: int = 10, T2: int = 10):
+    """The full two-level build of one KV head.  Returns a dict with ``perm``,
+    ``sub_off``, ``l1_assign``, ``steps`` and the summaries."""
+    K, V = _u16(K), _u16(V)
+    d = K.shape[1]
+    nm = max(0, n_build - R - S)
+    s = _summ_buffers(Cn, L, d)
+    perm = np.zeros(max(nm, 1), np.int32)
+    sub_off = np.zeros(Cn * L + 1, np.int32)
+    l1 = np.zeros(max(nm, 1), np.int32)
+    steps = np.zeros(2, np.int64)
+    _check(lib().ora_build(_ptr(K), _ptr(V), _i64(d), _i64(n_build), _i64(d), _i64(S), _i64(R),
+                           _i64(Cn), _i64(L), _i64(T1), _i64(T2), _ptr(perm), _ptr(sub_off),
+                           *_summ_args(s), _ptr(l1), _ptr(steps)), "build")
+    s.update(perm=perm[:nm], sub_off=sub_off, l1_assign=l1[:nm], steps=(int(steps[0]), int(steps[1])),
+             C=Cn, L=L, n_build=n_build, S=S, R=R)
+    return s
+
+
+def select(q: np.ndarray, summ: dict, top_c: int, top_s: int, score_mode: int = 0):
+    """Cluster and subcluster selection of one query head.
+    Returns (sel_c[top_c], sel_s[top_c, top_s], cscore[C], sscore[top_c, L])."""
+    q = _u16(q)
+    d = q.shape[0]
+    Cn, L = summ["C"], summ["L"]
+    sel_c = np.zeros(max(top_c, 1), np.int32)
+    sel_s = np.zeros(max(top_c * top_s, 1), np.int32)
+    cs = np.zeros(max(Cn, 1))
+    ss = np.zeros(max(top_c * L, 1))
+    _check(lib().ora_select(_ptr(q), _i64(d), _dbl(tau_of(d)), _i64(Cn), _i64(L),
+                            _ptr(summ["cl_n"]), _ptr(summ["cl_mu"]), _ptr(summ["cl_var"]),
+                            _ptr(summ["sub_n"]), _ptr(summ["sub_mu"]), _ptr(summ["sub_var"]),
+                            _i64(top_c), _i64(top_s), C.c_int(score_mode), _ptr(sel_c),
+                            _ptr(sel_s), _ptr(cs), _ptr(ss)), "select")
+    return (sel_c[:top_c], sel_s[:top_c * top_s].reshape(top_c, top_s), cs[:Cn],
+            ss[:top_c * L].reshape(top_c, L))
+
+
+def decode(K: np.ndarray, V: np.ndarray, n_now: int, q: np.ndarray, summ: dict,
+           sel_c: np.ndarray, sel_s: np.ndarray, residual: bool = True):
+    """Exact + residual output of one query head for a given selection.
+    Returns (out[d], diag = (m, den, n_exact))."""
+    K, V, q = _u16(K), _u16(V), _u16(q)
+    d = K.shape[1]
+    sel_c = np.ascontiguousarray(sel_c, np.int32).reshape(-1)
+    tc = sel_c.shape[0]
+    sel_s = np.ascontiguousarray(sel_s, np.int32).reshape(-1)
+    ts = sel_s.shape[0] // tc if tc else 0
+    out = np.zeros(d)
+    diag = np.zeros(3)
+    perm = np.ascontiguousarray(summ["perm"], np.int32)
+    if perm.size == 0:
+        perm = np.zeros(1, np.int32)
+    _check(lib().ora_decode(_ptr(K), _ptr(V), _i64(d), _i64(d), _i64(n_now), _i64(summ["n_build"]),
+                            _i64(summ["S"]), _i64(summ["R"]), _ptr(q), _dbl(tau_of(d)),
+                            _i64(summ["C"]), _i64(summ["L"]), _ptr(perm), _ptr(summ["sub_off"]),
+                            *_summ_args(summ), _ptr(sel_c if tc else np.zeros(1, np.int32)),
+                            _ptr(sel_s if sel_s.size else np.zeros(1, np.int32)), _i64(tc),
+                            _i64(ts), C.c_int(1 if residual else 0), _ptr(out), _ptr(diag)),
+           "decode")
+    return out, diag
+
+
+def dense(K: np.ndarray, V: np.ndarray, n: int, q: np.ndarray) -> np.ndarray:
+    """Exact softmax attention of one query head over keys [0, n)."""
+    K, V, q = _u16(K), _u16(V), _u16(q)
+    d = K.shape[1]
+    out = np.zeros(d)
+    _check(lib().ora_dense(_ptr(K), _ptr(V), _i64(d), _i64(d), _i64(n), _ptr(q), _dbl(tau_of(d)),
+                           _ptr(out)), "dense")
+    return out
+
+
+def mog_head(K, V, n_now, q, summ, top_c, top_s, score_mode=0, residual=True):
+    """Selection then decode for one query head (the oracle's whole decode step)."""
+    sel_c, sel_s, _, _ = select(q, summ, top_c, top_s, score_mode)
+    out, diag = decode(K, V, n_now, q, summ, sel_c, sel_s, residual)
+    return out, sel_c, sel_s, diag

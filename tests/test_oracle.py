@@ -1,0 +1,365 @@
+"""Pins of the fp64 CPU oracle against facts that do not come from the oracle itself:
+library routines (scipy's k-means and distances, numpy statistics, scipy's softmax),
+closed forms (the Gaussian moment generating function), exactness cases the method
+guarantees, and invariants.  No GPU is used.
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy.cluster.vq import kmeans2
+from scipy.spatial.distance import cdist
+from scipy.special import logsumexp, softmax
+
+from serving_mog_decode_gb300 import workloads as wl
+
+D = 128
+TAU = 1.0 / math.sqrt(D)
+
+
+def f64(h):
+    return wl.from_bf16(h).astype(np.float64)
+
+
+def dense_ref(K, V, n, q):
+    """Softmax attention written with scipy/numpy, independent of the oracle."""
+    logits = TAU * (f64(K[:n]) @ f64(q))
+    return softmax(logits) @ f64(V[:n])
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def planted(n, M=16, sigma=0.5, seed=0, d=D):
+    g = np.random.default_rng(seed)
+    c = g.standard_normal((M, d))
+    z = g.integers(0, M, n)
+    K = wl.to_bf16(c[z] + sigma * g.standard_normal((n, d)))
+    V = wl.to_bf16(g.standard_normal((n, d)))
+    q = wl.to_bf16(0.5 * c[0] + 0.5 * g.standard_normal(d))
+    return K, V, q
+
+
+# ----------------------------------------------------------------------------- inputs
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(3).standard_normal(100000) * 10.0 ** np.random.default_rng(4).integers(-8, 8, 100000)
+    ours = wl.to_bf16(x)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_generator_is_deterministic_and_planted():
+    w = wl.WORKLOADS["tiny-4k"]
+    K1, V1, q1 = wl.make_unit(w)
+    K2, V2, q2 = wl.make_unit(w)
+    assert np.array_equal(K1, K2) and np.array_equal(V1, V2) and np.array_equal(q1, q2)
+    k = f64(K1)
+    assert np.allclose(np.linalg.norm(k[:4], axis=1), 8.0, rtol=1e-2)  # sinks 8*u
+    u = wl.UnitDraw(w, 0, 0, w.n)
+    resid = k[4:] - u.centres[u.z[4:]]
+    assert abs(resid.std() - 0.5) < 0.01                       # sigma 0.5 around centres
+    assert abs(f64(V1).std() - 1.0) < 0.01
+
+
+# ----------------------------------------------------------------------------- k-means
+
+def test_assign_matches_scipy_cdist():
+    g = np.random.default_rng(1)
+    X = wl.to_bf16(g.standard_normal((3000, D)))
+    cent = g.standard_normal((37, D))
+    ref = np.argmin(cdist(f64(X), cent, "sqeuclidean"), axis=1)
+    from oracle import assign
+    assert np.array_equal(assign(X, cent), ref)
+
+
+def test_assign_ties_take_lowest_index(ora):
+    g = np.random.default_rng(2)
+    X = wl.to_bf16(g.standard_normal((200, D)))
+    base = g.standard_normal((5, D))
+    cent = np.concatenate([base, base[::-1]])       # every centroid duplicated
+    a = ora.assign(X, cent)
+    assert a.max() < 5                              # the lower copy always wins
+    assert np.array_equal(a, np.argmin(cdist(f64(X), base, "sqeuclidean"), axis=1))
+    # a key equidistant from two centroids goes to the lower index
+    c2 = np.stack([np.full(D, 1.0), np.full(D, -1.0)])
+    assert ora.assign(wl.to_bf16(np.zeros((1, D))), c2)[0] == 0
+    assert ora.assign(wl.to_bf16(np.zeros((1, D))), c2[::-1].copy())[0] == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 10])
+def test_lloyd_matches_scipy_kmeans2(ora, T):
+    K, _, _ = planted(2000, M=24, sigma=0.8, seed=5)
+    k = 12
+    cent, asg, steps, hist = ora.lloyd(K, k, T, history=True)
+    X = f64(K)
+    init = X[(np.arange(k) * X.shape[0]) // k]                 # strided seeding
+    assert np.array_equal(hist[0], init)
+    # scipy runs `iter` assign+update rounds; our label after `steps` assignment steps is
+    # scipy's label with iter=steps (same centroid history), and the centroids used by
+    # our last step are scipy's code book after steps-1 updates.
+    cb, lab = kmeans2(X, init.copy(), iter=steps, minit="matrix", missing="warn")
+    assert np.array_equal(asg, lab)
+    if steps >= 2:
+        cb_prev, _ = kmeans2(X, init.copy(), iter=steps - 1, minit="matrix", missing="warn")
+        assert np.allclose(cent, cb_prev, rtol=0, atol=1e-12)
+    if steps < T:   # early stop only at a fixed point
+        assert np.array_equal(ora.assign(K, cb), asg)
+
+
+def test_lloyd_objective_never_increases(ora):
+    K, _, _ = planted(3000, M=40, sigma=0.7, seed=6)
+    _, _, steps, hist = ora.lloyd(K, 20, 10, history=True)
+    X = f64(K)
+    obj = [cdist(X, h, "sqeuclidean").min(axis=1).sum() for h in hist]
+    assert steps >= 3
+    assert all(b <= a * (1 + 1e-12) for a, b in zip(obj, obj[1:]))
+
+
+def test_lloyd_more_centroids_than_points(ora):
+    K, _, _ = planted(5, M=5, seed=7)
+    cent, asg, steps, _ = ora.lloyd(K, 8, 3)
+    # seeds repeat members; duplicates tie and the lower index keeps the member
+    assert sorted(asg.tolist()) == sorted(set(asg.tolist()))   # each member its own cluster
+    assert np.array_equal(f64(K)[:, :], cent[asg])
+
+
+# ----------------------------------------------------------------------------- statistics
+
+def test_stats_match_numpy_and_identities(ora):
+    g = np.random.default_rng(8)
+    n, Cn, L = 1500, 7, 5
+    K = wl.to_bf16(g.standard_normal((n, D)) * 2 + 1)
+    V = wl.to_bf16(g.standard_normal((n, D)))
+    lab = g.integers(0, Cn * L, n)
+    lab[lab == 3] = 4                                     # group 3 stays empty
+    perm = np.argsort(lab, kind="stable").astype(np.int32)
+    sub_off = np.searchsorted(lab[perm], np.arange(Cn * L + 1)).astype(np.int32)
+    s = ora.stats(K, V, perm, sub_off, Cn, L)
+    X, Y = f64(K), f64(V)
+    for grp in range(Cn * L):
+        m = lab == grp
+        assert s["sub_n"][grp] == m.sum()
+        if m.sum() == 0:
+            assert not s["sub_mu"][grp].any() and not s["sub_var"][grp].any()
+            continue
+        np.testing.assert_allclose(s["sub_mu"][grp], X[m].mean(0), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(s["sub_var"][grp], X[m].var(0), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(s["sub_vbar"][grp], Y[m].mean(0), rtol=1e-12, atol=1e-12)
+    for c in range(Cn):
+        m = (lab // L) == c
+        sl = slice(c * L, (c + 1) * L)
+        ns = s["sub_n"][sl].astype(np.float64)
+        assert s["cl_n"][c] == m.sum() == ns.sum()
+        np.testing.assert_allclose(s["cl_mu"][c], X[m].mean(0), rtol=1e-12, atol=1e-12)
+        # count-weighted sub means give the cluster mean; law of total variance
+        np.testing.assert_allclose((ns[:, None] * s["sub_mu"][sl]).sum(0) / ns.sum(), s["cl_mu"][c],
+                                   atol=1e-12)
+        within = (ns[:, None] * s["sub_var"][sl]).sum(0) / ns.sum()
+        between = (ns[:, None] * (s["sub_mu"][sl] - s["cl_mu"][c]) ** 2).sum(0) / ns.sum()
+        np.testing.assert_allclose(s["cl_var"][c], within + between, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(s["cl_vbar"][c], Y[m].mean(0), rtol=1e-12, atol=1e-12)
+
+
+def test_build_partition_is_consistent(ora):
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    S, R, Cn, L = w.n_sink, w.n_recent, w.n_clusters, w.n_sub
+    b = ora.build_unit(K, V, w.n, S, R, Cn, L)
+    nm = w.n - S - R
+    perm, off, a1 = b["perm"], b["sub_off"], b["l1_assign"]
+    assert np.array_equal(np.sort(perm), np.arange(S, S + nm))           # mid region only
+    assert off[0] == 0 and off[-1] == nm and np.all(np.diff(off) >= 0)
+    # clusters are the first-level labels; positions ascend inside every subcluster
+    for c in range(Cn):
+        seg = perm[off[c * L]:off[(c + 1) * L]]
+        assert np.all(a1[seg - S] == c)
+        for l in range(L):
+            sub = perm[off[c * L + l]:off[c * L + l + 1]]
+            assert np.all(np.diff(sub) > 0)
+    # the first level is scipy's k-means from the same strided seeds
+    X = f64(K[S:S + nm])
+    init = X[(np.arange(Cn) * nm) // Cn]
+    s1 = b["steps"][0]
+    _, lab = kmeans2(X, init, iter=s1, minit="matrix", missing="warn")
+    assert np.array_equal(a1, lab)
+    # the second level of every cluster is scipy's k-means on its members
+    for c in range(0, Cn, 7):
+        seg = np.sort(perm[off[c * L]:off[(c + 1) * L]])
+        if seg.size == 0:
+            continue
+        Xc = f64(K[seg])
+        init2 = Xc[(np.arange(L) * seg.size) // L]
+        sub_of = np.empty(seg.size, np.int64)
+        for l in range(L):
+            sub_of[np.isin(seg, perm[off[c * L + l]:off[c * L + l + 1]])] = l
+        # run scipy until it reproduces (it has no early stop; 10 steps at most)
+        ok = any(np.array_equal(kmeans2(Xc, init2.copy(), iter=t, minit="matrix", missing="warn")[1], sub_of)
+                 for t in range(1, 11))
+        assert ok
+
+
+# ----------------------------------------------------------------------------- estimator
+
+def _single_group(ora, K, V):
+    """Everything in one cluster / one subcluster, no anchors."""
+    n = K.shape[0]
+    return ora.build_unit(K, V, n, 0, 0, 1, 1, 1, 1)
+
+
+def test_log_mass_is_gaussian_mgf(ora):
+    """For keys drawn from N(mu, diag s^2), sum_i exp(tau q.k_i) -> n exp(tau q.mu +
+    tau^2 sum q_j^2 s_j^2 / 2): the residual exponent must match the empirical log-sum."""
+    g = np.random.default_rng(11)
+    n = 200000
+    mu = g.standard_normal(D)
+    s = g.uniform(0.2, 1.2, D)
+    K = wl.to_bf16(mu + s * g.standard_normal((n, D)))
+    V = wl.to_bf16(g.standard_normal((n, D)))
+    q = wl.to_bf16(0.6 * g.standard_normal(D) / s)
+    summ = _single_group(ora, K, V)
+    out, diag = ora.decode(K, V, n, q, summ, np.array([-1], np.int32), np.array([[-1]], np.int32))
+    e_s = diag[0]                       # no exact keys: m is the residual exponent itself
+    emp = logsumexp(TAU * (f64(K) @ f64(q)))
+    qq = f64(q)
+    half = 0.5 * TAU ** 2 * np.sum(qq ** 2 * summ["cl_var"][0])
+    assert half > 0.1                   # the variance term matters at this scale
+    assert abs(e_s - emp) < 0.02 * half + 5e-3   # sampling error ~1.5e-3
+    np.testing.assert_allclose(out, summ["cl_vbar"][0], atol=1e-12)   # lone group: out = vbar
+
+
+def test_log_mass_two_point_group(ora):
+    """Two keys mu +- delta e_j: population variance delta^2 in dimension j only; the
+    exact log-sum is ln(2 cosh(tau q_j delta)) + tau q.mu; the Gaussian exponent replaces
+    ln cosh(x) by x^2/2, so the gap is ln cosh(x) - x^2/2 = -x^4/12 + x^6/45 - ..."""
+    mu = np.zeros(D)
+    mu[:4] = [1.0, -2.0, 0.5, 3.0]
+    K = np.stack([mu, mu]).copy()
+    K[0, 5] += 0.25
+    K[1, 5] -= 0.25
+    Kb = wl.to_bf16(K)
+    V = wl.to_bf16(np.random.default_rng(0).standard_normal((2, D)))
+    q = np.zeros(D)
+    q[:4] = [0.5, 0.25, -1.0, 2.0]
+    q[5] = 2.0
+    qb = wl.to_bf16(q)
+    summ = _single_group(ora, Kb, V)
+    _, diag = ora.decode(Kb, V, 2, qb, summ, np.array([-1], np.int32), np.array([[-1]], np.int32))
+    x = TAU * 2.0 * 0.25
+    exact = math.log(2 * math.cosh(x)) + TAU * float(f64(qb) @ mu)
+    assert abs((exact - diag[0]) - (math.log(math.cosh(x)) - x * x / 2)) < 1e-14
+    assert abs(math.log(math.cosh(x)) - x * x / 2 + x ** 4 / 12) < x ** 6 / 40
+
+
+def test_all_selected_equals_dense(ora):
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    b = ora.build_unit(K, V, w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    out, sel_c, sel_s, diag = ora.mog_head(K, V, w.n, q[0], b, w.n_clusters, w.n_sub)
+    nonempty = int((b["cl_n"] > 0).sum())
+    assert (sel_c >= 0).sum() == nonempty
+    assert diag[2] == w.n
+    ref = dense_ref(K, V, w.n, q[0])
+    assert rel_l2(out, ref) < 1e-12
+    assert rel_l2(ora.dense(K, V, w.n, q[0]), ref) < 1e-12
+
+
+def test_singleton_subclusters_make_residual_exact(ora):
+    K, V, q = planted(300, M=6, seed=12)
+    Cn, L = 4, 300            # L >= any cluster size: every member becomes its own subcluster
+    b = ora.build_unit(K, V, 300, 2, 10, Cn, L, 10, 3)
+    assert b["sub_n"].max() == 1
+    assert np.all(b["sub_var"] == 0)
+    out, _, _, diag = ora.mog_head(K, V, 300, q, b, Cn, 0)   # all clusters, no subclusters
+    assert diag[2] == 12                                      # only the anchors are exact
+    assert rel_l2(out, dense_ref(K, V, 300, q)) < 1e-12
+
+
+def test_duplicate_keys_make_residual_exact(ora):
+    g = np.random.default_rng(13)
+    distinct = g.standard_normal((16, D)) * 2
+    Kd = np.repeat(distinct, 8, axis=0)              # position p holds vector p // 8
+    K = wl.to_bf16(Kd)
+    V = wl.to_bf16(g.standard_normal((128, D)))
+    q = wl.to_bf16(0.3 * distinct[3] + 0.3 * g.standard_normal(D))
+    b = ora.build_unit(K, V, 128, 0, 0, 16, 3)
+    assert np.all(b["cl_n"] == 8) and np.all(b["cl_var"] == 0)
+    out, _, _, diag = ora.mog_head(K, V, 128, q, b, 0, 0)    # nothing selected
+    assert diag[2] == 0
+    assert rel_l2(out, dense_ref(K, V, 128, q)) < 1e-12
+
+
+def test_short_context_is_all_anchors(ora):
+    K, V, q = planted(200, seed=14)
+    b = ora.build_unit(K, V, 200, 4, 196, 3, 2)
+    assert b["perm"].size == 0 and np.all(b["cl_n"] == 0)
+    out, _, _, diag = ora.mog_head(K, V, 200, q, b, 3, 2)
+    assert diag[2] == 200
+    assert rel_l2(out, dense_ref(K, V, 200, q)) < 1e-12
+
+
+def test_appended_keys_join_recent_anchors(ora):
+    K, V, q = planted(600, seed=15)
+    b = ora.build_unit(K, V, 500, 4, 32, 8, 4)
+    out, _, _, diag = ora.mog_head(K, V, 600, q, b, 8, 4)   # all selected
+    assert diag[2] == 600
+    assert rel_l2(out, dense_ref(K, V, 600, q)) < 1e-12
+
+
+def test_tiny_sweep_is_a_convex_combination(ora):
+    K, V, q = planted(64, M=5, seed=16)
+    b = ora.build_unit(K, V, 64, 2, 6, 8, 4)
+    Y = f64(V)
+    allv = np.concatenate([Y, b["cl_vbar"], b["sub_vbar"]])
+    lo, hi = allv.min(0) - 1e-12, allv.max(0) + 1e-12
+    ref = dense_ref(K, V, 64, q)
+    for tc in range(0, 9):
+        for ts in range(0, 5):
+            out, sel_c, sel_s, diag = ora.mog_head(K, V, 64, q, b, tc, ts)
+            assert diag[1] > 0 and np.all(out >= lo) and np.all(out <= hi)
+            assert (sel_c >= 0).sum() == min(tc, int((b["cl_n"] > 0).sum()))
+            if tc == 8 and ts == 4:
+                assert rel_l2(out, ref) < 1e-12
+
+
+def test_selection_order_and_variance_term(ora):
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    b = ora.build_unit(K, V, w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    sel_c, sel_s, cs, ss = ora.select(q[0], b, 10, 6)
+    order = np.lexsort((np.arange(cs.size), -cs))
+    order = [i for i in order if b["cl_n"][i] > 0]
+    assert np.array_equal(sel_c, order[:10])
+    for i, c in enumerate(sel_c):
+        sc = ss[i]
+        o = [l for l in np.lexsort((np.arange(sc.size), -sc)) if b["sub_n"][c * w.n_sub + l] > 0]
+        assert np.array_equal(sel_s[i][:len(o[:6])], o[:6])
+    # two groups that differ only in spread along q: the wider one carries more mass
+    g = np.random.default_rng(17)
+    base = np.zeros((64, D))
+    narrow = base + 0.05 * g.standard_normal((64, D))
+    wide = base + 1.0 * g.standard_normal((64, D))
+    Kx = wl.to_bf16(np.concatenate([narrow, wide]))
+    Vx = wl.to_bf16(g.standard_normal((128, D)))
+    bx = ora.build_unit(Kx, Vx, 128, 0, 0, 2, 1)
+    if bx["cl_n"][0] == 64 and bx["cl_n"][1] == 64:
+        qx = wl.to_bf16(np.full(D, 1.0))
+        sc, _, cs2, _ = ora.select(qx, bx, 1, 0)
+        wide_id = int(np.argmax(bx["cl_var"].sum(1)))
+        assert sc[0] == wide_id
+        _, _, cs1, _ = ora.select(qx, bx, 1, 0, score_mode=1)
+        assert abs((cs2 - cs1)[wide_id] - (math.log(64) + 0.5 * TAU ** 2 * bx["cl_var"][wide_id].sum())) < 1e-9
+
+
+def test_residual_reduces_error_on_planted_data(ora):
+    """The page reports that adding the residual cuts the error of top-cluster-only
+    attention; on planted-centre data it must at least reduce it."""
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    b = ora.build_unit(K, V, w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    ref = dense_ref(K, V, w.n, q[0])
+    mog, _, _, _ = ora.mog_head(K, V, w.n, q[0], b, w.top_c, w.top_s)
+    top, _, _, _ = ora.mog_head(K, V, w.n, q[0], b, w.top_c, w.top_s, residual=False)
+    assert rel_l2(mog, ref) < rel_l2(top, ref)
