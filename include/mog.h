@@ -1,0 +1,242 @@
+/*
+ * mog.h -- C ABI of libmog: Mixture-of-Gaussians (MoG) decode attention on one GPU
+ * (NVIDIA GB300, sm_103a).
+ *
+ * What the library computes, and where the pages state it:
+ *   [IA] "Iceberg Attention: Sublinear Long-Context Decoding with Mixture-of-Gaussians",
+ *        Abstract: after prefill, each head's keys are split into O(sqrt N) clusters and
+ *        O(log N) subclusters per cluster, each group summarised by a Gaussian; at decode
+ *        the query is scored against the summaries, the best clusters/subclusters are
+ *        attended exactly, the rest is approximated from the groups' means and variances.
+ *   [RC] newx.sg paper page on retrieval-completion attention, Abstract: sink and tail
+ *        anchors are attended exactly together with the retrieved keys; the estimated
+ *        numerator and denominator of the rest are added in the unnormalised domain and
+ *        one normalisation follows.
+ * Residual form of this library (consistent with [IA]'s "means and variances"): an
+ * unselected group s (count n_s, key mean mu_s, per-dimension population variance
+ * sigma2_s, value mean vbar_s) adds den_s = n_s * exp(tau q.mu_s + tau^2/2 *
+ * sum_j q_j^2 sigma2_sj - m) to the denominator and den_s * vbar_s to the numerator,
+ * tau = 1/sqrt(d), m the running maximum.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are device pointers, *_host host pointers.  The caller owns all
+ *    memory (KV cache, queries, outputs, the build arena, scratch).  The library never
+ *    allocates device memory; a handle is a small host structure.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
+ *    device work is enqueued on it; no entry point synchronises the host unless it says so.
+ *  - bf16 data are IEEE bfloat16 bit patterns (uint16).  KV caches are [B][H_kv][n_cap][d]
+ *    with element strides given in mog_kv; d must be 128 and rows contiguous.
+ *  - Return value: MOG_OK or a mog_status error.  Argument errors are detected before any
+ *    work is enqueued.  Errors detected on the device are recorded in the handle's status
+ *    word and reported by mog_sync_status.
+ */
+#ifndef MOG_H
+#define MOG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOG_OK = 0,
+    MOG_ERR_INVALID_ARG = 1,     /* null pointer, negative size, bad flag */
+    MOG_ERR_SHAPE = 2,           /* unsupported shape (d != 128, G > 16, ...) */
+    MOG_ERR_ARENA_TOO_SMALL = 3, /* caller buffer smaller than the size query returned */
+    MOG_ERR_CUDA = 4,            /* a CUDA runtime call failed (see mog_last_error) */
+    MOG_ERR_DEVICE_CHECK = 5,    /* a device-side check failed (see mog_sync_status) */
+    MOG_ERR_TIMEOUT = 6,         /* reserved: a bounded device wait gave up */
+    MOG_ERR_NOT_IMPLEMENTED = 7,
+    MOG_ERR_CAPACITY = 8         /* appending past n_cap */
+} mog_status;
+
+/*
+ * Build and decode parameters.  All counts are per KV head ("unit" = (b, h_kv)).
+ *  n_clusters, n_sub : C and L; 0 selects round(sqrt(N_b)) and ceil(log2(N_b)) from each
+ *                      sequence's build length N_b ([IA]: O(sqrt N) x O(log N)).
+ *  top_c, top_s      : clusters selected per query head, subclusters selected inside each
+ *                      selected cluster ([IA]).  top_c*G <= 256, L <= 32.
+ *  n_sink, n_recent  : anchors S and R; positions [0,S) and [N_b-R, N) are never clustered
+ *                      and always attended exactly ([RC]).
+ *  iters_l1, iters_l2: Lloyd assignment steps per level (0 selects 10); a level stops
+ *                      early once a step changes no assignment.
+ *  score_mode        : 0 = log-mass score ln n + tau q.mu + tau^2/2 sum q^2 sigma2 (the
+ *                      residual's own exponent); 1 = tau q.mu only.
+ *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
+ *  flags             : must be 0.
+ */
+typedef struct mog_params {
+    int32_t batch, h_kv, h_q, d;
+    int32_t n_cap;
+    int32_t n_clusters, n_sub;
+    int32_t top_c, top_s;
+    int32_t n_sink, n_recent;
+    int32_t iters_l1, iters_l2;
+    int32_t score_mode;
+    int32_t residual;
+    int32_t flags;
+} mog_params;
+
+/* A bf16 KV cache in device memory.  Element (b, h, n, j) of K is
+ * k[b*stride_b + h*stride_h + n*stride_n + j]; V uses the same strides.  stride_n >= d,
+ * all strides multiples of 8 elements (16-byte aligned rows), base pointers 16-byte
+ * aligned.  mog_append writes into this cache. */
+typedef struct mog_kv {
+    void *k;
+    void *v;
+    int64_t stride_b, stride_h, stride_n;
+} mog_kv;
+
+typedef struct mog_handle mog_handle;
+
+/* Byte offsets (into the arena) of the handle's device arrays, for inspection by tests.
+ * u = b*h_kv + h indexes units. */
+typedef struct mog_layout {
+    int32_t units, c_max, l_max, n_cap, d, group, top_c, top_s;
+    int64_t unit_info;  /* int32 [units][8]: C_u, L_u, N_build, N_mid, S, recent_lo, b, 0 */
+    int64_t n_now;      /* int32 [batch]: current length of each sequence */
+    int64_t perm;       /* int32 [units][n_cap]: mid positions ordered (cluster, sub, position) */
+    int64_t sub_off;    /* int32 [units][sub_off_stride]: offsets into perm, C_u*L_u+1 used */
+    int64_t sub_off_stride;
+    int64_t cl_n;       /* int32 [units][c_max] */
+    int64_t cl_ms;      /* f32   [units][c_max][2][d]: mean, variance */
+    int64_t cl_vbar;    /* f32   [units][c_max][d] */
+    int64_t sub_n;      /* int32 [units][c_max*l_max], group c*L_u + l */
+    int64_t sub_ms;     /* f32   [units][c_max*l_max][2][d] */
+    int64_t sub_vbar;   /* f32   [units][c_max*l_max][d] */
+    int64_t l1_assign;  /* int32 [units][n_cap]: final first-level cluster of mid key S+i */
+    int64_t status;     /* int32 [8]: device status word, check counters */
+    int64_t l1_steps;   /* int32 [units]: assignment steps taken by the first level */
+    int64_t fallback;   /* int32 [units][iters_l1]: rows decided by the exact fp64 fallback */
+} mog_layout;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char *mog_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread's calls into the library. */
+const char *mog_last_error(void);
+
+/*
+ * Size of the device arena mog_build needs for these parameters and build lengths.
+ * lengths_host: int32[batch] build lengths N_b (1 <= N_b <= n_cap).
+ */
+int mog_arena_bytes(const mog_params *p, const int32_t *lengths_host, size_t *bytes);
+
+/*
+ * MoG build ([IA], "after prefill ... partitions the keys"): for every unit, first-level
+ * Lloyd k-means of the mid keys [S, N_b - R) into C_u clusters, second-level k-means of
+ * each cluster into L_u subclusters, then count, key mean, per-dimension population
+ * variance and value mean of every cluster and subcluster.  Enqueued on `stream`; no host
+ * synchronisation.
+ *  kv           : the cache (read; must outlive the handle)
+ *  lengths_dev  : int32[batch] N_b on the device; lengths_host the same values on the host
+ *  arena_dev    : caller-owned device buffer of at least mog_arena_bytes() bytes, 256-byte
+ *                 aligned; it holds every summary and all decode workspace and must
+ *                 outlive the handle
+ *  out          : receives a new handle (free it with mog_destroy)
+ */
+int mog_build(const mog_kv *kv, const int32_t *lengths_dev, const int32_t *lengths_host,
+              const mog_params *p, void *arena_dev, size_t arena_bytes, void *stream,
+              mog_handle **out);
+
+/*
+ * MoG decode step ([IA], "scored against these compact representations ... attended
+ * exactly ... approximated from the means and variances"; [RC]): per query head, score the
+ * clusters, take the top top_c, score their subclusters, take the top top_s in each,
+ * attend exactly to the members of the selected subclusters plus the anchors, add the
+ * Gaussian residual of every unselected non-empty group, normalise once.
+ *  q_dev   : bf16 [batch][h_q][d]; query head g*G + i belongs to KV head g
+ *  out_dev : f32 [batch][h_q][d]
+ * Calls on one handle must not overlap on the GPU (they share the arena's workspace).
+ */
+int mog_decode(mog_handle *h, const void *q_dev, float *out_dev, void *stream);
+
+/*
+ * mog_decode with the selection exposed, for parity tests.  sel layout: int32
+ * [batch][h_q][top_c + top_c*top_s]: the selected cluster ids in rank order, then for
+ * the i-th selected cluster its top_s subcluster indices (0..L_u-1) in rank order; -1
+ * pads missing entries.  sel_in_dev (may be NULL) replaces the library's own selection;
+ * sel_out_dev (may be NULL) receives the selection used.
+ */
+int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev, const int32_t *sel_in_dev,
+                  int32_t *sel_out_dev, void *stream);
+
+/*
+ * Append one decode token per sequence: k_new_dev, v_new_dev bf16 [batch][h_kv][d] are
+ * written at position n_now[b] of the cache, then n_now[b] += 1.  Appended keys join the
+ * recent anchors; summaries are unchanged.  MOG_ERR_CAPACITY if a sequence would exceed
+ * n_cap (checked on the host from the build lengths and the number of appends).
+ */
+int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void *stream);
+
+/* Copy the arena layout of a handle. */
+int mog_get_layout(const mog_handle *h, mog_layout *out);
+
+/* Synchronise `stream`, then read the device status word: MOG_OK or the recorded error. */
+int mog_sync_status(mog_handle *h, void *stream);
+
+/* Split factor (partial results per unit) of the decode's exact-attention kernel. */
+int mog_decode_splits(const mog_handle *h, int32_t *splits);
+
+/* Free the host structure of a handle (not the caller's arena or cache).  NULL is a no-op. */
+void mog_destroy(mog_handle *h);
+
+/*
+ * Full-scan exact decode attention, the comparison path ([IA]: the full KV scan that MoG
+ * avoids): for every query head, softmax(tau q.K^T) V over keys [0, N_b).  Query head
+ * (b, g*G + i) reads KV head (b, g).
+ *  lengths_dev : int32[batch] on the device; n_max >= every length (sizes the launch)
+ *  q_dev       : bf16 [batch][h_q][d];  out_dev: f32 [batch][h_q][d]
+ *  scratch_dev : device buffer of at least dense_decode_scratch_bytes() bytes (partial
+ *                results of the split scan); no initial contents needed
+ */
+int dense_decode_scratch_bytes(int32_t batch, int32_t h_kv, int32_t h_q, int32_t d,
+                               int32_t n_max, size_t *bytes);
+int dense_decode(const mog_kv *kv, const int32_t *lengths_dev, int32_t n_max, int32_t batch,
+                 int32_t h_kv, int32_t h_q, int32_t d, const void *q_dev, float *out_dev,
+                 void *scratch_dev, size_t scratch_bytes, void *stream);
+
+/*
+ * Test export of one first-level k-means assignment step ([IA]'s partition, computed by
+ * a Lloyd step): for each of the n rows x_i (bf16, row stride ld elements),
+ * assign_out_dev[i] = argmin_c sum_j (x_ij - cent_cj)^2 with the lowest index on ties,
+ * decided exactly as the fp64 sum of rounded squares in index order.  The same kernels
+ * as mog_build's first level.  cent_dev: f32 [k][d].  scratch_dev: at least
+ * mog_kmeans_assign_scratch_bytes() bytes.  fallback_rows_host (may be NULL) receives the
+ * number of rows the exact fallback decided (this synchronises the stream).
+ */
+int mog_kmeans_assign_scratch_bytes(int32_t n, int32_t k, int32_t d, size_t *bytes);
+int mog_kmeans_assign(const void *x_dev, int64_t ld, int32_t n, const float *cent_dev,
+                      int32_t k, int32_t d, int32_t *assign_out_dev, void *scratch_dev,
+                      size_t scratch_bytes, void *stream, int32_t *fallback_rows_host);
+
+/*
+ * Test export of one second-level assignment step: n_seg segments, segment s holding
+ * rows rows_dev[seg_off[s] .. seg_off[s+1]) of x, assigned among its own k centroids
+ * cent_dev[s][k][d] (f32), same decision rule as above.  The same kernel as mog_build's
+ * second level.  k <= 32.
+ */
+int mog_kmeans_assign_segments(const void *x_dev, int64_t ld, const int32_t *rows_dev,
+                               const int32_t *seg_off_dev, int32_t n_seg, const float *cent_dev,
+                               int32_t k, int32_t d, int32_t *assign_out_dev, void *stream);
+
+/*
+ * mog_build with the partition given instead of clustered: perm_dev int32 [units][n_cap]
+ * lists each unit's mid positions ordered by (cluster, subcluster, position) and
+ * sub_off_dev int32 [units][sub_off_stride] the offsets (C_u*L_u+1 used, relative to the
+ * unit's perm row).  Only the summaries are computed.  For parity tests.
+ */
+int mog_sub_off_stride(const mog_params *p, const int32_t *lengths_host, int64_t *stride);
+int mog_build_from_partition(const mog_kv *kv, const int32_t *lengths_dev,
+                             const int32_t *lengths_host, const mog_params *p,
+                             const int32_t *perm_dev, const int32_t *sub_off_dev,
+                             void *arena_dev, size_t arena_bytes, void *stream,
+                             mog_handle **out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOG_H */
