@@ -1,0 +1,548 @@
+// api.cu -- the C ABI of libmog (declared in mog.h): argument validation, the arena
+// layout, and the launch sequences.  No entry point allocates device memory.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace mog;
+
+struct mog_handle {
+    Plan plan;
+    Dev dev;
+    mog_kv kv;
+    char *arena;
+    std::vector<int32_t> lengths;
+    std::vector<int32_t> info;  // host copy of unit_info
+    int appended;
+};
+
+static thread_local char g_err[256] = "";
+
+static int cuda_fail(cudaError_t e, const char *where) {
+    snprintf(g_err, sizeof g_err, "%s: %s", where, cudaGetErrorString(e));
+    return MOG_ERR_CUDA;
+}
+#define CK(call)                                              \
+    do {                                                      \
+        cudaError_t e_ = (call);                              \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call);   \
+    } while (0)
+
+namespace mog {
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
+static int isqrt_round(int64_t n) {
+    int64_t c = (int64_t)sqrt((double)n);
+    while (c * c > n) --c;
+    while ((c + 1) * (c + 1) <= n) ++c;
+    return (int)(n - c * c > c ? c + 1 : c);  // round(sqrt(n)); a tie cannot occur
+}
+static int ceil_log2(int64_t n) {
+    int l = 0;
+    while (((int64_t)1 << l) < n) ++l;
+    return l;
+}
+
+void unit_clusters(const mog_params *p, int n, int *C, int *L) {
+    *C = std::max(1, p->n_clusters > 0 ? p->n_clusters : isqrt_round(n));
+    *L = std::max(1, p->n_sub > 0 ? p->n_sub : ceil_log2(n));
+}
+
+static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
+
+int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
+    if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
+    if (p->flags != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
+        p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
+        p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
+        (p->score_mode != 0 && p->score_mode != 1) || (p->residual != 0 && p->residual != 1))
+        return MOG_ERR_INVALID_ARG;
+    if (p->d != MOG_D || p->h_q % p->h_kv != 0 || p->h_q / p->h_kv > MOG_MAX_G)
+        return MOG_ERR_SHAPE;
+    Plan &P = *pl;
+    memset(&P, 0, sizeof P);
+    P.batch = p->batch;
+    P.h_kv = p->h_kv;
+    P.h_q = p->h_q;
+    P.G = p->h_q / p->h_kv;
+    P.d = p->d;
+    P.n_cap = p->n_cap;
+    P.units = p->batch * p->h_kv;
+    P.tc = p->top_c;
+    P.ts = p->top_s;
+    P.T1 = p->iters_l1 > 0 ? p->iters_l1 : 10;
+    P.T2 = p->iters_l2 > 0 ? p->iters_l2 : 10;
+    P.score_mode = p->score_mode;
+    P.residual = p->residual;
+    P.c_max = P.l_max = 1;
+    P.n_mid_max = 0;
+    for (int b = 0; b < p->batch; ++b) {
+        const int n = lengths_host[b];
+        if (n < 1 || n > p->n_cap) return MOG_ERR_SHAPE;
+        int C, L;
+        unit_clusters(p, n, &C, &L);
+        P.c_max = std::max(P.c_max, C);
+        P.l_max = std::max(P.l_max, L);
+        P.n_mid_max = std::max(P.n_mid_max, std::max(0, n - p->n_recent - p->n_sink));
+    }
+    if (P.l_max > MOG_MAX_L || P.c_max > MAX_C || P.ts > MOG_MAX_L) return MOG_ERR_SHAPE;
+    if (P.G * P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
+    const int tcc = std::max(P.tc, 1);
+    const int p1_min = (int)ceil_div64(P.c_max, 64);
+    const int p1_cap = std::min(64, 1024 / tcc);
+    if (p1_min > p1_cap) return MOG_ERR_SHAPE;  // c_max too large for this top_c
+    const int sms = num_sms();
+    P.P1 = std::min(p1_cap, std::max(p1_min, (int)ceil_div64(2 * sms, P.units)));
+    P.P1 = std::max(1, std::min(P.P1, P.c_max));
+    P.P = std::max(1, std::min(MAX_SPLITS, (int)ceil_div64(2 * sms, P.units)));
+    P.nchunks = std::max(1, (int)ceil_div64(P.n_mid_max, SORT_CHUNK));
+    P.sub_off_stride = (P.c_max * P.l_max + 1 + 3) & ~3;
+    const int64_t U = P.units, G = P.G, cm = P.c_max, lm = P.l_max, nc = P.n_cap;
+    const int64_t SW = P.tc + P.tc * P.ts;
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t r = o;
+        o += al(std::max<int64_t>(bytes, 4));
+        return r;
+    };
+    P.o_status = take(64);
+    P.o_unit_info = take(4 * U * UI_STRIDE);
+    P.o_n_now = take(4 * P.batch);
+    P.o_perm = take(4 * U * nc);
+    P.o_sub_off = take(4 * U * P.sub_off_stride);
+    P.o_cl_n = take(4 * U * cm);
+    P.o_cl_ms = take(4 * U * cm * 2 * MOG_D);
+    P.o_cl_vbar = take(4 * U * cm * MOG_D);
+    P.o_sub_n = take(4 * U * cm * lm);
+    P.o_sub_ms = take(4 * U * cm * lm * 2 * MOG_D);
+    P.o_sub_vbar = take(4 * U * cm * lm * MOG_D);
+    P.o_l1_assign = take(4 * U * nc);
+    P.o_l1_steps = take(4 * U);
+    P.o_cent = take(4 * U * cm * MOG_D);
+    P.o_permA = take(4 * U * nc);
+    P.o_changed = take(4 * U * P.T1);
+    P.o_fb_list = take(4 * U * nc);
+    P.o_fb_cnt = take(4 * U * P.T1);
+    P.o_hist = take(4 * U * P.nchunks * cm);
+    P.o_offs = take(4 * U * P.nchunks * cm);
+    P.o_ctot = take(4 * U * cm);
+    P.o_coff = take(4 * U * (cm + 1));
+    P.o_sub_assign = take(4 * U * nc);
+    P.o_cscore = take(4 * U * 2 * G * cm);
+    P.o_subscore = take(4 * U * MOG_MAX_UNION * G * MOG_MAX_L);
+    P.o_partials = take(4 * U * MAX_SPLITS * G * (MOG_D + 2));
+    P.o_cselmask = take(4 * U * cm);
+    P.o_uhm = take(4 * U * MOG_MAX_UNION);
+    P.o_subres = take(4 * U * MOG_MAX_UNION * MOG_MAX_L);
+    P.o_rowmask = take(4 * U * nc);
+    P.o_ucl = take(4 * U * MOG_MAX_UNION);
+    P.o_ucount = take(4 * U);
+    P.o_sel = take(4 * U * G * std::max<int64_t>(SW, 1));
+    P.o_slotcnt = take(4 * U * MOG_MAX_UNION);
+    P.o_rowpos = take(4 * U * nc);
+    P.o_counters = take(4 * U * 4);
+    P.o_cand_s = take(4 * U * P.P1 * G * tcc);
+    P.o_cand_i = take(4 * U * P.P1 * G * tcc);
+    P.total = o;
+    return MOG_OK;
+}
+
+Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
+    Dev d;
+    memset(&d, 0, sizeof d);
+    char *a = static_cast<char *>(arena);
+    d.K = static_cast<const uint16_t *>(kv->k);
+    d.V = static_cast<const uint16_t *>(kv->v);
+    d.Kw = static_cast<uint16_t *>(kv->k);
+    d.Vw = static_cast<uint16_t *>(kv->v);
+    d.sb = kv->stride_b;
+    d.sh = kv->stride_h;
+    d.sn = kv->stride_n;
+    d.batch = P.batch;
+    d.h_kv = P.h_kv;
+    d.G = P.G;
+    d.units = P.units;
+    d.n_cap = P.n_cap;
+    d.c_max = P.c_max;
+    d.l_max = P.l_max;
+    d.tc = P.tc;
+    d.ts = P.ts;
+    d.T1 = P.T1;
+    d.T2 = P.T2;
+    d.score_mode = P.score_mode;
+    d.residual = P.residual;
+    d.P = P.P;
+    d.P1 = P.P1;
+    d.nchunks = P.nchunks;
+    d.sub_off_stride = P.sub_off_stride;
+    d.tau = (float)(1.0 / sqrt((double)P.d));
+#define PTR(name, T) d.name = reinterpret_cast<T *>(a + P.o_##name)
+    PTR(unit_info, int);
+    PTR(n_now, int);
+    PTR(perm, int);
+    PTR(sub_off, int);
+    PTR(cl_n, int);
+    PTR(sub_n, int);
+    PTR(l1_assign, int);
+    PTR(status, int);
+    PTR(l1_steps, int);
+    PTR(cl_ms, float);
+    PTR(cl_vbar, float);
+    PTR(sub_ms, float);
+    PTR(sub_vbar, float);
+    PTR(cent, float);
+    PTR(permA, int);
+    PTR(changed, int);
+    PTR(fb_list, int);
+    PTR(fb_cnt, int);
+    PTR(hist, int);
+    PTR(offs, int);
+    PTR(ctot, int);
+    PTR(coff, int);
+    PTR(sub_assign, int);
+    PTR(cscore, float);
+    PTR(subscore, float);
+    PTR(partials, float);
+    PTR(cselmask, uint32_t);
+    PTR(uhm, uint32_t);
+    PTR(subres, uint32_t);
+    PTR(rowmask, uint32_t);
+    PTR(ucl, int);
+    PTR(ucount, int);
+    PTR(sel, int);
+    PTR(slotcnt, int);
+    PTR(rowpos, int);
+    PTR(counters, unsigned);
+    PTR(cand_s, float);
+    PTR(cand_i, int);
+#undef PTR
+    return d;
+}
+
+}  // namespace mog
+
+// Partition sanity check for mog_build_from_partition: offsets monotone and complete,
+// positions inside the unit's mid region.  Bad input sets the status word; the
+// statistics kernel then skips the unit.
+__global__ void k_check_partition(Dev dv) {
+    const int u = blockIdx.x;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int C = ui[UI_C], L = ui[UI_L], nm = ui[UI_NMID], S = ui[UI_S];
+    const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride;
+    const int *pm = dv.perm + (size_t)u * dv.n_cap;
+    bool bad = false;
+    for (int g = threadIdx.x; g < C * L; g += blockDim.x)
+        if (so[g] > so[g + 1]) bad = true;
+    if (threadIdx.x == 0 && (so[0] != 0 || so[C * L] != nm)) bad = true;
+    for (int i = threadIdx.x; i < nm; i += blockDim.x)
+        if (pm[i] < S || pm[i] >= S + nm) bad = true;
+    if (bad) flag_error(dv.status, ST_BAD_INDEX);
+}
+
+// ------------------------------------------------------------------------------- ABI
+
+static const char *kNames[] = {"MOG_OK", "MOG_ERR_INVALID_ARG", "MOG_ERR_SHAPE",
+                               "MOG_ERR_ARENA_TOO_SMALL", "MOG_ERR_CUDA", "MOG_ERR_DEVICE_CHECK",
+                               "MOG_ERR_TIMEOUT", "MOG_ERR_NOT_IMPLEMENTED", "MOG_ERR_CAPACITY"};
+
+extern "C" const char *mog_status_string(int status) {
+    if (status < 0 || status >= (int)(sizeof kNames / sizeof kNames[0])) return "MOG_UNKNOWN_STATUS";
+    return kNames[status];
+}
+
+extern "C" const char *mog_last_error(void) { return g_err; }
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+static int check_kv(const mog_kv *kv, int batch, int h_kv, int n_cap) {
+    if (!kv || !kv->k || !kv->v) return MOG_ERR_INVALID_ARG;
+    if (!aligned16(kv->k) || !aligned16(kv->v)) return MOG_ERR_INVALID_ARG;
+    if (kv->stride_n < MOG_D || kv->stride_b < 0 || kv->stride_h < 0) return MOG_ERR_SHAPE;
+    if ((kv->stride_n | kv->stride_b | kv->stride_h) & 7) return MOG_ERR_SHAPE;
+    (void)batch;
+    (void)h_kv;
+    (void)n_cap;
+    return MOG_OK;
+}
+
+extern "C" int mog_arena_bytes(const mog_params *p, const int32_t *lengths_host, size_t *bytes) {
+    if (!bytes) return MOG_ERR_INVALID_ARG;
+    Plan pl;
+    int st = make_plan(p, lengths_host, &pl);
+    if (st != MOG_OK) return st;
+    *bytes = (size_t)pl.total;
+    return MOG_OK;
+}
+
+static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
+                        const int32_t *lengths_host, const mog_params *p, void *arena,
+                        size_t arena_bytes, cudaStream_t s, mog_handle **out, mog_handle **hh) {
+    if (!out || !lengths_dev || !arena) return MOG_ERR_INVALID_ARG;
+    *out = nullptr;
+    Plan pl;
+    int st = make_plan(p, lengths_host, &pl);
+    if (st != MOG_OK) return st;
+    if ((st = check_kv(kv, p->batch, p->h_kv, p->n_cap)) != MOG_OK) return st;
+    if (((uintptr_t)arena & 255) != 0) return MOG_ERR_INVALID_ARG;
+    if (arena_bytes < (size_t)pl.total) return MOG_ERR_ARENA_TOO_SMALL;
+    mog_handle *h = new mog_handle;
+    h->plan = pl;
+    h->kv = *kv;
+    h->arena = static_cast<char *>(arena);
+    h->dev = make_dev(pl, arena, kv);
+    h->lengths.assign(lengths_host, lengths_host + p->batch);
+    h->appended = 0;
+    h->info.assign((size_t)pl.units * UI_STRIDE, 0);
+    for (int u = 0; u < pl.units; ++u) {
+        const int b = u / p->h_kv, n = lengths_host[b];
+        int C, L;
+        unit_clusters(p, n, &C, &L);
+        int32_t *r = &h->info[(size_t)u * UI_STRIDE];
+        r[UI_C] = C;
+        r[UI_L] = L;
+        r[UI_NBUILD] = n;
+        r[UI_NMID] = std::max(0, n - p->n_recent - p->n_sink);
+        r[UI_S] = p->n_sink;
+        r[UI_RLO] = std::max(p->n_sink, n - p->n_recent);
+        r[UI_B] = b;
+    }
+    char *a = h->arena;
+    cudaError_t e;
+#define CKH(call)                                  \
+    do {                                           \
+        if ((e = (call)) != cudaSuccess) {         \
+            delete h;                              \
+            return cuda_fail(e, #call);            \
+        }                                          \
+    } while (0)
+    CKH(cudaMemcpyAsync(a + pl.o_unit_info, h->info.data(), h->info.size() * 4,
+                        cudaMemcpyHostToDevice, s));
+    CKH(cudaMemcpyAsync(a + pl.o_n_now, lengths_dev, 4 * (size_t)pl.batch, cudaMemcpyDeviceToDevice, s));
+    CKH(cudaMemsetAsync(a + pl.o_status, 0, 64, s));
+    CKH(cudaMemsetAsync(a + pl.o_changed, 0, 4 * (size_t)pl.units * pl.T1, s));
+    CKH(cudaMemsetAsync(a + pl.o_fb_cnt, 0, 4 * (size_t)pl.units * pl.T1, s));
+    CKH(cudaMemsetAsync(a + pl.o_counters, 0, 16 * (size_t)pl.units, s));
+    CKH(cudaMemsetAsync(a + pl.o_coff, 0, 4 * (size_t)pl.units * (pl.c_max + 1), s));
+    CKH(cudaMemsetAsync(a + pl.o_l1_assign, 0xff, 4 * (size_t)pl.units * pl.n_cap, s));
+    CKH(cudaMemsetAsync(a + pl.o_l1_steps, 0, 4 * (size_t)pl.units, s));
+    CKH(cudaMemsetAsync(a + pl.o_ucount, 0, 4 * (size_t)pl.units, s));
+#undef CKH
+    *hh = h;
+    return MOG_OK;
+}
+
+extern "C" int mog_build(const mog_kv *kv, const int32_t *lengths_dev, const int32_t *lengths_host,
+                         const mog_params *p, void *arena_dev, size_t arena_bytes, void *stream,
+                         mog_handle **out) {
+    mog_handle *h = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = common_build(kv, lengths_dev, lengths_host, p, arena_dev, arena_bytes, s, out, &h);
+    if (st != MOG_OK) return st;
+    cudaError_t e = launch_build(h->dev, h->plan, s);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "mog_build launch");
+    }
+    *out = h;
+    return MOG_OK;
+}
+
+extern "C" int mog_sub_off_stride(const mog_params *p, const int32_t *lengths_host, int64_t *stride) {
+    if (!stride) return MOG_ERR_INVALID_ARG;
+    Plan pl;
+    int st = make_plan(p, lengths_host, &pl);
+    if (st != MOG_OK) return st;
+    *stride = pl.sub_off_stride;
+    return MOG_OK;
+}
+
+extern "C" int mog_build_from_partition(const mog_kv *kv, const int32_t *lengths_dev,
+                                        const int32_t *lengths_host, const mog_params *p,
+                                        const int32_t *perm_dev, const int32_t *sub_off_dev,
+                                        void *arena_dev, size_t arena_bytes, void *stream,
+                                        mog_handle **out) {
+    if (!perm_dev || !sub_off_dev) return MOG_ERR_INVALID_ARG;
+    mog_handle *h = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = common_build(kv, lengths_dev, lengths_host, p, arena_dev, arena_bytes, s, out, &h);
+    if (st != MOG_OK) return st;
+    const Plan &pl = h->plan;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(h->arena + pl.o_perm, perm_dev, 4 * (size_t)pl.units * pl.n_cap,
+                             cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->arena + pl.o_sub_off, sub_off_dev,
+                             4 * (size_t)pl.units * pl.sub_off_stride, cudaMemcpyDeviceToDevice,
+                             s)) != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "mog_build_from_partition copy");
+    }
+    k_check_partition<<<pl.units, 256, 0, s>>>(h->dev);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = launch_stats_only(h->dev, pl, s);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "mog_build_from_partition launch");
+    }
+    *out = h;
+    return MOG_OK;
+}
+
+extern "C" int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev,
+                             const int32_t *sel_in_dev, int32_t *sel_out_dev, void *stream) {
+    if (!h || !q_dev || !out_dev) return MOG_ERR_INVALID_ARG;
+    if (!aligned16(q_dev) || !aligned16(out_dev)) return MOG_ERR_INVALID_ARG;
+    cudaError_t e = launch_decode(h->dev, h->plan, q_dev, out_dev, sel_in_dev, sel_out_dev,
+                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "mog_decode launch");
+    return MOG_OK;
+}
+
+extern "C" int mog_decode(mog_handle *h, const void *q_dev, float *out_dev, void *stream) {
+    return mog_decode_ex(h, q_dev, out_dev, nullptr, nullptr, stream);
+}
+
+extern "C" int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void *stream) {
+    if (!h || !k_new_dev || !v_new_dev) return MOG_ERR_INVALID_ARG;
+    if (!aligned16(k_new_dev) || !aligned16(v_new_dev)) return MOG_ERR_INVALID_ARG;
+    const int nmax = *std::max_element(h->lengths.begin(), h->lengths.end());
+    if ((int64_t)nmax + h->appended + 1 > h->plan.n_cap) return MOG_ERR_CAPACITY;
+    cudaError_t e = launch_append(h->dev, h->plan, k_new_dev, v_new_dev, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "mog_append launch");
+    h->appended += 1;
+    return MOG_OK;
+}
+
+extern "C" int mog_get_layout(const mog_handle *h, mog_layout *o) {
+    if (!h || !o) return MOG_ERR_INVALID_ARG;
+    const Plan &P = h->plan;
+    memset(o, 0, sizeof *o);
+    o->units = P.units;
+    o->c_max = P.c_max;
+    o->l_max = P.l_max;
+    o->n_cap = P.n_cap;
+    o->d = P.d;
+    o->group = P.G;
+    o->top_c = P.tc;
+    o->top_s = P.ts;
+    o->unit_info = P.o_unit_info;
+    o->n_now = P.o_n_now;
+    o->perm = P.o_perm;
+    o->sub_off = P.o_sub_off;
+    o->sub_off_stride = P.sub_off_stride;
+    o->cl_n = P.o_cl_n;
+    o->cl_ms = P.o_cl_ms;
+    o->cl_vbar = P.o_cl_vbar;
+    o->sub_n = P.o_sub_n;
+    o->sub_ms = P.o_sub_ms;
+    o->sub_vbar = P.o_sub_vbar;
+    o->l1_assign = P.o_l1_assign;
+    o->status = P.o_status;
+    o->l1_steps = P.o_l1_steps;
+    o->fallback = P.o_fb_cnt;
+    return MOG_OK;
+}
+
+extern "C" int mog_sync_status(mog_handle *h, void *stream) {
+    if (!h) return MOG_ERR_INVALID_ARG;
+    CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    int st = 0;
+    CK(cudaMemcpy(&st, h->arena + h->plan.o_status, 4, cudaMemcpyDeviceToHost));
+    return st ? MOG_ERR_DEVICE_CHECK : MOG_OK;
+}
+
+extern "C" int mog_decode_splits(const mog_handle *h, int32_t *splits) {
+    if (!h || !splits) return MOG_ERR_INVALID_ARG;
+    *splits = h->plan.P;
+    return MOG_OK;
+}
+
+extern "C" void mog_destroy(mog_handle *h) { delete h; }
+
+// ---------------------------------------------------------------------- dense_decode
+
+extern "C" int dense_decode_scratch_bytes(int32_t batch, int32_t h_kv, int32_t h_q, int32_t d,
+                                          int32_t n_max, size_t *bytes) {
+    if (!bytes || batch <= 0 || h_kv <= 0 || h_q <= 0 || n_max <= 0) return MOG_ERR_INVALID_ARG;
+    if (d != MOG_D || h_q % h_kv != 0 || h_q / h_kv > MOG_MAX_G) return MOG_ERR_SHAPE;
+    const int units = batch * h_kv, G = h_q / h_kv;
+    *bytes = (size_t)units * dense_splits(units, n_max) * G * (MOG_D + 2) * sizeof(float);
+    return MOG_OK;
+}
+
+extern "C" int dense_decode(const mog_kv *kv, const int32_t *lengths_dev, int32_t n_max,
+                            int32_t batch, int32_t h_kv, int32_t h_q, int32_t d, const void *q_dev,
+                            float *out_dev, void *scratch_dev, size_t scratch_bytes, void *stream) {
+    size_t need = 0;
+    int st = dense_decode_scratch_bytes(batch, h_kv, h_q, d, n_max, &need);
+    if (st != MOG_OK) return st;
+    if ((st = check_kv(kv, batch, h_kv, n_max)) != MOG_OK) return st;
+    if (!lengths_dev || !q_dev || !out_dev || !scratch_dev) return MOG_ERR_INVALID_ARG;
+    if (!aligned16(q_dev) || !aligned16(out_dev) || !aligned16(scratch_dev)) return MOG_ERR_INVALID_ARG;
+    if (scratch_bytes < need) return MOG_ERR_ARENA_TOO_SMALL;
+    const int units = batch * h_kv;
+    cudaError_t e = launch_dense(static_cast<const uint16_t *>(kv->k), static_cast<const uint16_t *>(kv->v),
+                                 kv->stride_b, kv->stride_h, kv->stride_n, lengths_dev, n_max, batch,
+                                 h_kv, h_q / h_kv, q_dev, out_dev, static_cast<float *>(scratch_dev),
+                                 dense_splits(units, n_max), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dense_decode launch");
+    return MOG_OK;
+}
+
+// ----------------------------------------------------------------- parity exports
+
+extern "C" int mog_kmeans_assign_scratch_bytes(int32_t n, int32_t k, int32_t d, size_t *bytes) {
+    if (!bytes || n < 0 || k <= 0) return MOG_ERR_INVALID_ARG;
+    if (d != MOG_D) return MOG_ERR_SHAPE;
+    *bytes = 256 + 4 * (size_t)std::max(n, 1);
+    return MOG_OK;
+}
+
+extern "C" int mog_kmeans_assign(const void *x_dev, int64_t ld, int32_t n, const float *cent_dev,
+                                 int32_t k, int32_t d, int32_t *assign_out_dev, void *scratch_dev,
+                                 size_t scratch_bytes, void *stream, int32_t *fallback_rows_host) {
+    size_t need = 0;
+    int st = mog_kmeans_assign_scratch_bytes(n, k, d, &need);
+    if (st != MOG_OK) return st;
+    if (!x_dev || !cent_dev || !assign_out_dev || !scratch_dev) return MOG_ERR_INVALID_ARG;
+    if (!aligned16(x_dev) || !aligned16(cent_dev) || ld < MOG_D || (ld & 7)) return MOG_ERR_SHAPE;
+    if (scratch_bytes < need) return MOG_ERR_ARENA_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int *sc = static_cast<int *>(scratch_dev);
+    CK(cudaMemsetAsync(sc, 0, 256, s));
+    CK(launch_assign_l1(static_cast<const uint16_t *>(x_dev), ld, n, cent_dev, k, assign_out_dev,
+                        sc, sc + 64, sc + 32, s));
+    if (fallback_rows_host) {
+        CK(cudaMemcpyAsync(fallback_rows_host, sc + 32, 4, cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+    }
+    return MOG_OK;
+}
+
+extern "C" int mog_kmeans_assign_segments(const void *x_dev, int64_t ld, const int32_t *rows_dev,
+                                          const int32_t *seg_off_dev, int32_t n_seg,
+                                          const float *cent_dev, int32_t k, int32_t d,
+                                          int32_t *assign_out_dev, void *stream) {
+    if (!x_dev || !rows_dev || !seg_off_dev || !cent_dev || !assign_out_dev || n_seg < 0)
+        return MOG_ERR_INVALID_ARG;
+    if (d != MOG_D || k <= 0 || k > MOG_MAX_L || ld < MOG_D || (ld & 7) || !aligned16(x_dev))
+        return MOG_ERR_SHAPE;
+    CK(launch_assign_segments(static_cast<const uint16_t *>(x_dev), ld, rows_dev, seg_off_dev, n_seg,
+                              cent_dev, k, assign_out_dev, static_cast<cudaStream_t>(stream)));
+    return MOG_OK;
+}

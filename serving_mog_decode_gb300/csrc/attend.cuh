@@ -1,0 +1,250 @@
+// attend.cuh -- split-KV online-softmax attention over 64-row tiles of a bf16 KV cache,
+// shared by the full-scan kernel and the MoG exact-attention kernel.
+//
+// One CTA = 4 warps.  Rows (keys) are copied into shared memory with 16-byte cp.async,
+// three stages deep, in a layout whose 16-byte chunks are XOR-swizzled by (row & 7) so
+// that ldmatrix reads are bank-conflict free.  Warp w owns rows 16w..16w+15 of every
+// tile and keeps its own running (max, sum, output) for the G query heads of the KV head,
+// which sit in the M dimension of an m16n8k16 bf16 mma (rows >= G stay masked).
+//  - logits S = Q K^T: A = Q (bf16, exact), B = K tile, fp32 accumulate;
+//  - weights P = 2^(S*tau*log2e - m), split into bf16 hi + lo parts (16-bit precision)
+//    so the P V product (fp32 accumulate) keeps ~2^-17 relative weight error;
+//  - a per-row head mask removes heads for which a row is not selected (logit -inf).
+#pragma once
+
+#include "common.cuh"
+
+namespace mog {
+
+constexpr int AT_WARPS = 4;
+constexpr int AT_THREADS = AT_WARPS * 32;
+constexpr int AT_ROWS = 64;
+constexpr int AT_STAGES = 3;
+constexpr int AT_ROW_BYTES = MOG_D * 2;               // 256
+constexpr int AT_TILE_BYTES = AT_ROWS * AT_ROW_BYTES;  // 16 KB (K or V)
+constexpr int AT_STAGE_BYTES = 2 * AT_TILE_BYTES + AT_ROWS * 4;
+constexpr int AT_SMEM = AT_STAGES * AT_STAGE_BYTES;
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct WarpAcc {
+    float o[16][4];  // output fragment: 16 dim tiles of 8, rows lane/4 and lane/4 + 8
+    float m[2];      // running max (log2 domain) of rows lane/4, lane/4 + 8
+    float l[2];      // this lane's share of the running sum
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[t][e] = 0.f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+    }
+};
+
+// Q as mma A fragments for the 8 k-steps of d = 128; heads >= G are zero.
+__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[8][4], const uint16_t *q, int G) {
+    const int lane = threadIdx.x & 31;
+    const int h0 = lane >> 2, h1 = h0 + 8, c = (lane & 3) * 2;
+    const uint32_t *q0 = reinterpret_cast<const uint32_t *>(q + h0 * MOG_D);
+    const uint32_t *q1 = reinterpret_cast<const uint32_t *>(q + h1 * MOG_D);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const int k0 = ks * 16 + c;
+        qa[ks][0] = h0 < G ? q0[k0 / 2] : 0u;
+        qa[ks][1] = h1 < G ? q1[k0 / 2] : 0u;
+        qa[ks][2] = h0 < G ? q0[(k0 + 8) / 2] : 0u;
+        qa[ks][3] = h1 < G ? q1[(k0 + 8) / 2] : 0u;
+    }
+}
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return (uint32_t)(row * AT_ROW_BYTES + ((chunk ^ (row & 7)) << 4));
+}
+
+// Issue the copies of one tile: rows r < nrows come from krow/vrow(pos(r)); others are
+// zero-filled with mask 0.  `posf(r, &pos, &mask)` supplies row positions.
+template <typename RowFn>
+__device__ __forceinline__ void issue_tile(uint8_t *stage, int nrows, const uint16_t *kbase,
+                                           const uint16_t *vbase, int64_t sn, RowFn posf) {
+    uint32_t *smask = reinterpret_cast<uint32_t *>(stage + 2 * AT_TILE_BYTES);
+    const uint32_t sk = smem_u32(stage), sv = sk + AT_TILE_BYTES;
+    const int tid = threadIdx.x;
+    // each thread: rows tid/16 + 8i, chunk tid%16
+    const int ch = tid & 15;
+#pragma unroll
+    for (int i = 0; i < AT_ROWS / 8; ++i) {
+        const int r = (tid >> 4) + 8 * i;
+        int64_t pos = 0;
+        uint32_t mk = 0;
+        const bool ok = r < nrows;
+        if (ok) posf(r, pos, mk);
+        const uint16_t *ks = kbase + (ok ? pos * sn : 0) + ch * 8;
+        const uint16_t *vs = vbase + (ok ? pos * sn : 0) + ch * 8;
+        cp_async16(sk + swz(r, ch), ks, ok ? 16 : 0);
+        cp_async16(sv + swz(r, ch), vs, ok ? 16 : 0);
+        if (ch == 0) smask[r] = ok ? mk : 0u;
+    }
+}
+
+// Consume one tile (already in shared memory) into this warp's accumulator.
+__device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[8][4],
+                                             const uint8_t *stage, float scale2) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t sk = smem_u32(stage), sv = sk + AT_TILE_BYTES;
+    const uint32_t *smask = reinterpret_cast<const uint32_t *>(stage + 2 * AT_TILE_BYTES);
+    const int rbase = w * 16;
+    float s[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[t][e] = 0.f;
+    {
+        const int mat = lane >> 3, r8 = lane & 7;
+        const int key = rbase + (mat >> 1) * 8 + r8;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(sk + swz(key, 2 * ks + (mat & 1)), b0, b1, b2, b3);
+            mma_bf16(s[0], qa[ks], b0, b1);
+            mma_bf16(s[1], qa[ks], b2, b3);
+        }
+    }
+    const int h0 = lane >> 2, h1 = h0 + 8;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int key = rbase + t * 8 + (lane & 3) * 2 + e;
+            const uint32_t mk = smask[key];
+            s[t][e] = ((mk >> h0) & 1u) ? s[t][e] * scale2 : -INFINITY;
+            s[t][e + 2] = ((mk >> h1) & 1u) ? s[t][e + 2] * scale2 : -INFINITY;
+            mx0 = fmaxf(mx0, s[t][e]);
+            mx1 = fmaxf(mx1, s[t][e + 2]);
+        }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
+    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(acc.m[0] - mn0);
+    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(acc.m[1] - mn1);
+    acc.m[0] = mn0;
+    acc.m[1] = mn1;
+    float p[2][4];
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            p[t][e] = mn0 == -INFINITY ? 0.f : exp2f(s[t][e] - mn0);
+            p[t][e + 2] = mn1 == -INFINITY ? 0.f : exp2f(s[t][e + 2] - mn1);
+            ps0 += p[t][e];
+            ps1 += p[t][e + 2];
+        }
+    acc.l[0] = acc.l[0] * al0 + ps0;
+    acc.l[1] = acc.l[1] * al1 + ps1;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        acc.o[t][0] *= al0;
+        acc.o[t][1] *= al0;
+        acc.o[t][2] *= al1;
+        acc.o[t][3] *= al1;
+    }
+    uint32_t ahi[4], alo[4];
+    {
+        const float v[4][2] = {{p[0][0], p[0][1]}, {p[0][2], p[0][3]}, {p[1][0], p[1][1]},
+                               {p[1][2], p[1][3]}};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t hb = pack_bf2(v[i][0], v[i][1]);
+            ahi[i] = hb;
+            const float r0 = v[i][0] - bf_lo(hb), r1 = v[i][1] - bf_hi(hb);
+            alo[i] = pack_bf2(r0, r1);
+        }
+    }
+    {
+        const int mat = lane >> 3, r8 = lane & 7;
+        const int key = rbase + (mat & 1) * 8 + r8;
+#pragma unroll
+        for (int dt = 0; dt < 16; dt += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(sv + swz(key, dt + (mat >> 1)), b0, b1, b2, b3);
+            mma_bf16(acc.o[dt], ahi, b0, b1);
+            mma_bf16(acc.o[dt], alo, b0, b1);
+            mma_bf16(acc.o[dt + 1], ahi, b2, b3);
+            mma_bf16(acc.o[dt + 1], alo, b2, b3);
+        }
+    }
+}
+
+// Partial result layout: per head, [0] = m (log2 domain), [1] = l, [2..2+d) = acc.
+constexpr int PART_W = MOG_D + 2;
+
+// Write this warp's state for heads < G into st[w][g][PART_W] (shared memory).
+__device__ __forceinline__ void warp_state_out(const WarpAcc &acc, float *st, int G) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float l0 = acc.l[0], l1 = acc.l[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int h0 = lane >> 2, h1 = h0 + 8, c = (lane & 3) * 2;
+    float *b = st + (size_t)w * G * PART_W;
+    if (h0 < G) {
+        float *r = b + h0 * PART_W;
+        if ((lane & 3) == 0) {
+            r[0] = acc.m[0];
+            r[1] = l0;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            r[2 + t * 8 + c] = acc.o[t][0];
+            r[2 + t * 8 + c + 1] = acc.o[t][1];
+        }
+    }
+    if (h1 < G) {
+        float *r = b + h1 * PART_W;
+        if ((lane & 3) == 0) {
+            r[0] = acc.m[1];
+            r[1] = l1;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            r[2 + t * 8 + c] = acc.o[t][2];
+            r[2 + t * 8 + c + 1] = acc.o[t][3];
+        }
+    }
+}
+
+// Merge n states st[i][g][PART_W] (stride per state = G*PART_W floats) into dst[g][PART_W].
+// Called by all threads of the CTA; shared or global sources.
+__device__ __forceinline__ void merge_states(const float *st, int n, int G, float *dst,
+                                             bool cg_loads) {
+    for (int e = threadIdx.x; e < G * MOG_D; e += blockDim.x) {
+        const int g = e / MOG_D, j = e % MOG_D;
+        float m = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+            const float *r = st + ((size_t)i * G + g) * PART_W;
+            m = fmaxf(m, cg_loads ? __ldcg(r) : r[0]);
+        }
+        float l = 0.f, a = 0.f;
+        if (m != -INFINITY) {
+            for (int i = 0; i < n; ++i) {
+                const float *r = st + ((size_t)i * G + g) * PART_W;
+                const float mi = cg_loads ? __ldcg(r) : r[0];
+                if (mi == -INFINITY) continue;
+                const float sc = exp2f(mi - m);
+                l += sc * (cg_loads ? __ldcg(r + 1) : r[1]);
+                a += sc * (cg_loads ? __ldcg(r + 2 + j) : r[2 + j]);
+            }
+        }
+        float *o = dst + (size_t)g * PART_W;
+        if (j == 0) {
+            o[0] = m;
+            o[1] = l;
+        }
+        o[2 + j] = a;
+    }
+}
+
+}  // namespace mog

@@ -1,0 +1,104 @@
+// dense.cu -- full-scan exact decode attention, the comparison path: every query head
+// attends to all N_b keys of its KV head (softmax(tau q.K^T) V, tau = 1/sqrt(d)).
+// "Iceberg Attention: Sublinear Long-Context Decoding with Mixture-of-Gaussians",
+// Abstract: decoding over a long context normally scans the whole KV cache; this is that
+// scan.  Split-KV: each (KV head, split) CTA streams a contiguous key range through the
+// attention engine and writes a partial (max, sum, acc); a second kernel merges them.
+#include "attend.cuh"
+#include "internal.h"
+
+namespace mog {
+
+struct DenseArgs {
+    const uint16_t *K, *V;
+    int64_t sb, sh, sn;
+    const int32_t *lengths;
+    int h_kv, G, splits;
+    const uint16_t *q;
+    float *out, *part;  // part: [units][splits][G][PART_W]
+    float scale2;
+};
+
+__global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    const int u = blockIdx.y, p = blockIdx.x;
+    const int b = u / a.h_kv, h = u % a.h_kv;
+    const int n = a.lengths[b];
+    // contiguous split of [0, n) into `splits` ranges of whole tiles
+    const int64_t ntile = ceil_div64(n, AT_ROWS);
+    const int64_t t0 = ntile * p / a.splits, t1 = ntile * (p + 1) / a.splits;
+    const int64_t lo = t0 * AT_ROWS, hi = min((int64_t)n, t1 * AT_ROWS);
+    const int nt = (int)(t1 - t0);
+    const uint16_t *kb = a.K + b * a.sb + h * a.sh;
+    const uint16_t *vb = a.V + b * a.sb + h * a.sh;
+    const uint32_t allm = a.G >= 32 ? 0xffffffffu : ((1u << a.G) - 1u);
+    uint32_t qa[8][4];
+    load_q_frags(qa, a.q + ((int64_t)b * a.h_kv * a.G + (int64_t)h * a.G) * MOG_D, a.G);
+    WarpAcc acc;
+    acc.init();
+    auto issue = [&](int t) {
+        const int64_t r0 = lo + (int64_t)t * AT_ROWS;
+        const int nr = (int)min((int64_t)AT_ROWS, hi - r0);
+        issue_tile(dsm + (t % AT_STAGES) * AT_STAGE_BYTES, nr, kb, vb, a.sn,
+                   [&](int r, int64_t &pos, uint32_t &mk) {
+                       pos = r0 + r;
+                       mk = allm;
+                   });
+    };
+#pragma unroll
+    for (int s = 0; s < AT_STAGES - 1; ++s) {
+        if (s < nt) issue(s);
+        cp_async_commit();
+    }
+    for (int t = 0; t < nt; ++t) {
+        cp_async_wait<AT_STAGES - 2>();
+        __syncthreads();
+        if (t + AT_STAGES - 1 < nt) issue(t + AT_STAGES - 1);
+        cp_async_commit();
+        compute_tile(acc, qa, dsm + (t % AT_STAGES) * AT_STAGE_BYTES, a.scale2);
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    float *st = reinterpret_cast<float *>(dsm);
+    warp_state_out(acc, st, a.G);
+    __syncthreads();
+    merge_states(st, AT_WARPS, a.G, a.part + ((int64_t)u * a.splits + p) * a.G * PART_W, false);
+}
+
+__global__ void k_dense_merge(DenseArgs a) {
+    extern __shared__ __align__(16) float mg[];
+    const int u = blockIdx.x;
+    merge_states(a.part + (int64_t)u * a.splits * a.G * PART_W, a.splits, a.G, mg, true);
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.G * MOG_D; e += blockDim.x) {
+        const int g = e / MOG_D, j = e % MOG_D;
+        const float l = mg[g * PART_W + 1];
+        a.out[((int64_t)u * a.G + g) * MOG_D + j] = l > 0.f ? mg[g * PART_W + 2 + j] / l : 0.f;
+    }
+}
+
+int dense_splits(int units, int n_max) {
+    // enough CTAs for two per SM, no split shorter than 8 tiles
+    const int want = (int)ceil_div64(2 * num_sms(), units);
+    const int64_t bl = ceil_div64(n_max, 8 * AT_ROWS);
+    const int by_len = bl < 1 ? 1 : (int)bl;
+    return max(1, min(want, by_len));
+}
+
+cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64_t sh,
+                         int64_t sn, const int32_t *lengths, int n_max, int batch, int h_kv,
+                         int G, const void *q, float *out, float *scratch, int splits,
+                         cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute((const void *)k_dense_split,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    if (e != cudaSuccess) return e;
+    DenseArgs a{K, V, sb, sh, sn, lengths, h_kv, G, splits,
+                static_cast<const uint16_t *>(q), out, scratch,
+                (float)(LOG2E / sqrt((double)MOG_D))};
+    const int U = batch * h_kv;
+    k_dense_split<<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
+    k_dense_merge<<<U, 256, G * PART_W * sizeof(float), s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace mog

@@ -1,0 +1,89 @@
+// internal.h -- host/device shared structures of libmog (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mog.h"
+
+namespace mog {
+
+// per-unit table, int32 x 8 (mirrors mog_layout.unit_info)
+enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
+
+constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
+constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
+constexpr int MAX_C = 4096;        // clusters per unit supported
+
+// Typed view of an arena, passed by value to every kernel.
+struct Dev {
+    // cache
+    const uint16_t *K, *V;
+    uint16_t *Kw, *Vw;  // writable views (append)
+    int64_t sb, sh, sn;
+    // shape
+    int batch, h_kv, G, units, n_cap, c_max, l_max, tc, ts, T1, T2, score_mode, residual;
+    int P, P1, nchunks;
+    int64_t sub_off_stride;
+    float tau;
+    // persistent
+    int *unit_info, *n_now, *perm, *sub_off, *cl_n, *sub_n, *l1_assign, *status, *l1_steps;
+    float *cl_ms, *cl_vbar, *sub_ms, *sub_vbar;
+    // build workspace
+    float *cent;
+    int *permA, *changed, *fb_list, *fb_cnt, *hist, *offs, *ctot, *coff, *sub_assign;
+    // decode workspace
+    float *cscore, *subscore, *partials;
+    uint32_t *cselmask, *uhm, *subres, *rowmask;
+    int *ucl, *ucount, *sel, *slotcnt, *rowpos;
+    unsigned *counters;
+    float *cand_s;  // [units][P1][G][tc] per-slice top clusters
+    int *cand_i;
+
+    __host__ __device__ const uint16_t *krow(int b, int h, int64_t pos) const {
+        return K + b * sb + h * sh + pos * sn;
+    }
+    __host__ __device__ const uint16_t *vrow(int b, int h, int64_t pos) const {
+        return V + b * sb + h * sh + pos * sn;
+    }
+};
+
+// Host-side plan: sizes and byte offsets of every array in the arena.
+struct Plan {
+    int batch, h_kv, h_q, G, d, n_cap, units, c_max, l_max, tc, ts, T1, T2;
+    int score_mode, residual, P, P1, nchunks, n_mid_max;
+    int64_t sub_off_stride;
+    int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
+        o_sub_vbar, o_l1_assign, o_status, o_l1_steps;
+    int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
+        o_sub_assign;
+    int64_t o_cscore, o_subscore, o_partials, o_cselmask, o_uhm, o_subres, o_rowmask, o_ucl,
+        o_ucount, o_sel, o_slotcnt, o_rowpos, o_counters, o_cand_s, o_cand_i;
+    int64_t total;
+};
+
+int num_sms();
+int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl);
+Dev make_dev(const Plan &pl, void *arena, const mog_kv *kv);
+void unit_clusters(const mog_params *p, int n, int *C, int *L);
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s);
+cudaError_t launch_stats_only(const Dev &dv, const Plan &pl, cudaStream_t s);
+cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *out,
+                          const int32_t *sel_in, int32_t *sel_out, cudaStream_t s);
+cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
+                          cudaStream_t s);
+cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64_t sh,
+                         int64_t sn, const int32_t *lengths, int n_max, int batch, int h_kv,
+                         int G, const void *q, float *out, float *scratch, int splits,
+                         cudaStream_t s);
+int dense_splits(int units, int n_max);
+cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
+                             int32_t *assign, int *changed, int *fb_list, int *fb_cnt,
+                             cudaStream_t s);
+cudaError_t launch_assign_segments(const uint16_t *x, int64_t ld, const int32_t *rows,
+                                   const int32_t *seg_off, int n_seg, const float *cent, int k,
+                                   int32_t *assign, cudaStream_t s);
+
+}  // namespace mog

@@ -1,0 +1,788 @@
+// kmeans.cu -- the MoG build: two-level Lloyd k-means over each KV head's mid-region keys
+// and the Gaussian summaries of every cluster and subcluster.
+//
+// Source: "Iceberg Attention: Sublinear Long-Context Decoding with Mixture-of-Gaussians",
+// Abstract (after prefill the keys of each head are partitioned hierarchically into
+// O(sqrt N) clusters and O(log N) subclusters per cluster, each represented by a
+// Gaussian).  The pages name no clustering algorithm; this library uses Lloyd's
+// algorithm with strided seeding (centroid j starts at member floor(j*n/k) in position
+// order), at most T assignment steps, a mean update between steps, an early stop when a
+// step changes nothing, and empty clusters keeping their centroid.
+//
+// Assignment decision.  The nearest centroid is defined by D(x,c) = sum_j (x_j - c_j)^2
+// evaluated in fp64 in index order, lowest index on ties.  The kernels compute D in fp32
+// (difference, then fused square-accumulate: |D32 - D| <= (d+2) 2^-24 D since every term
+// is non-negative) and keep the winner only when the runner-up is separated by more than
+// that bound on both values (with a safety factor); every other row is recomputed with
+// the exact fp64 rule.  The result therefore equals the fp64 rule bit for bit.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mog {
+
+// relative error bound of the fp32 distance, with a safety factor of ~3 over (d+2)*2^-24
+constexpr float kCertRel = 2.5e-5f;
+
+__device__ __forceinline__ bool certified(float b1, float b2) {
+    // true minimum is b1's centroid for every rounding within the bound
+    return b2 - b1 > kCertRel * (b1 + b2);
+}
+
+// exact rule: fp64, index order, no contraction
+__device__ __forceinline__ double exact_dist(const uint16_t *x, const float *c) {
+    double acc = 0.0;
+    for (int j = 0; j < MOG_D; ++j) {
+        double diff = __dsub_rn((double)bf1(x[j]), (double)c[j]);
+        acc = __dadd_rn(acc, __dmul_rn(diff, diff));
+    }
+    return acc;
+}
+
+// converged before or at step t: some step 1..t changed nothing
+__device__ __forceinline__ bool converged_by(const int *changed, int t) {
+    for (int s = 1; s <= t; ++s)
+        if (changed[s] == 0) return true;
+    return false;
+}
+
+// ------------------------------------------------------------------------------------
+// First-level assignment.  One CTA: 64 rows x all centroids, 256 threads, each thread a
+// 4 x 4 register tile of (row, centroid) distances; rows and centroid tiles are staged
+// transposed in shared memory as fp32.
+// ------------------------------------------------------------------------------------
+struct AssignJob {
+    const uint16_t *K;
+    int64_t sb, sh, sn;
+    int h_kv;
+    const int *unit_info;  // null: a single unit of n_single rows at K, row stride sn
+    int n_single, k_single;
+    const float *cent;
+    int64_t cent_ustride;
+    int *assign;
+    int64_t assign_ustride;
+    int *changed;  // [unit][T]
+    int *fb_list;  // [unit][fb_ustride]
+    int64_t fb_ustride;
+    int *fb_cnt;  // [unit][T]
+    int t, T;
+};
+
+constexpr int AS_ROWS = 64, AS_CENT = 64, AS_THREADS = 256, AS_PAD = 68;
+constexpr size_t AS_SMEM = 2 * MOG_D * AS_PAD * sizeof(float);
+
+__device__ __forceinline__ void job_unit(const AssignJob &jb, int u, const uint16_t *&x,
+                                         int &n, int &k) {
+    if (jb.unit_info) {
+        const int *ui = jb.unit_info + u * UI_STRIDE;
+        int b = ui[UI_B], h = u % jb.h_kv;
+        n = ui[UI_NMID];
+        k = ui[UI_C];
+        x = jb.K + b * jb.sb + h * jb.sh + (int64_t)ui[UI_S] * jb.sn;
+    } else {
+        n = jb.n_single;
+        k = jb.k_single;
+        x = jb.K;
+    }
+}
+
+__global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
+    extern __shared__ __align__(16) float as_smem[];
+    float *Xs = as_smem;                  // [d][AS_PAD], rows
+    float *Cs = as_smem + MOG_D * AS_PAD;  // [d][AS_PAD], centroids
+    __shared__ int s_changed, s_base;
+    __shared__ int s_unc[AS_ROWS];
+    const int u = blockIdx.y;
+    const int *chg = jb.changed + (int64_t)u * jb.T;
+    if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
+    const uint16_t *x;
+    int n, k;
+    job_unit(jb, u, x, n, k);
+    const int r0 = blockIdx.x * AS_ROWS;
+    if (r0 >= n || k <= 0) return;
+    const float *cent = jb.cent + u * jb.cent_ustride;
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    if (tid == 0) s_changed = 0;
+
+    // rows -> Xs[j][r] (fp32), 16-byte loads of 8 bf16
+    for (int e = tid; e < AS_ROWS * 16; e += AS_THREADS) {
+        int r = e >> 4, ch = e & 15;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (r0 + r < n) w = *reinterpret_cast<const uint4 *>(x + (int64_t)(r0 + r) * jb.sn + ch * 8);
+        uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            Xs[(ch * 8 + 2 * q) * AS_PAD + r] = bf_lo(ws[q]);
+            Xs[(ch * 8 + 2 * q + 1) * AS_PAD + r] = bf_hi(ws[q]);
+        }
+    }
+    float b1[4], b2[4];
+    int i1[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        b1[a] = INFINITY;
+        b2[a] = INFINITY;
+        i1[a] = 0x7fffffff;
+    }
+    for (int c0 = 0; c0 < k; c0 += AS_CENT) {
+        __syncthreads();
+        for (int e = tid; e < AS_CENT * 32; e += AS_THREADS) {
+            int c = e >> 5, j4 = e & 31;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c0 + c < k) v = *reinterpret_cast<const float4 *>(cent + (int64_t)(c0 + c) * MOG_D + j4 * 4);
+            Cs[(j4 * 4 + 0) * AS_PAD + c] = v.x;
+            Cs[(j4 * 4 + 1) * AS_PAD + c] = v.y;
+            Cs[(j4 * 4 + 2) * AS_PAD + c] = v.z;
+            Cs[(j4 * 4 + 3) * AS_PAD + c] = v.w;
+        }
+        __syncthreads();
+        float acc[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int bq = 0; bq < 4; ++bq) acc[a][bq] = 0.f;
+#pragma unroll 4
+        for (int j = 0; j < MOG_D; ++j) {
+            float4 xv = *reinterpret_cast<const float4 *>(Xs + j * AS_PAD + ty * 4);
+            float4 cv = *reinterpret_cast<const float4 *>(Cs + j * AS_PAD + tx * 4);
+            float xa[4] = {xv.x, xv.y, xv.z, xv.w}, ca[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int bq = 0; bq < 4; ++bq) {
+                    float df = __fsub_rn(xa[a], ca[bq]);
+                    acc[a][bq] = __fmaf_rn(df, df, acc[a][bq]);
+                }
+        }
+#pragma unroll
+        for (int bq = 0; bq < 4; ++bq) {
+            int c = c0 + tx * 4 + bq;
+            if (c >= k) break;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                float dd = acc[a][bq];
+                if (dd < b1[a]) {
+                    b2[a] = b1[a];
+                    b1[a] = dd;
+                    i1[a] = c;
+                } else if (dd < b2[a]) {
+                    b2[a] = dd;
+                }
+            }
+        }
+    }
+    // merge the 16 threads that share each row (lanes with equal ty in a half-warp)
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+            float ob1 = __shfl_xor_sync(0xffffffffu, b1[a], o);
+            float ob2 = __shfl_xor_sync(0xffffffffu, b2[a], o);
+            int oi1 = __shfl_xor_sync(0xffffffffu, i1[a], o);
+            if (ob1 < b1[a] || (ob1 == b1[a] && oi1 < i1[a])) {
+                b2[a] = fminf(ob2, b1[a]);
+                b1[a] = ob1;
+                i1[a] = oi1;
+            } else {
+                b2[a] = fminf(b2[a], ob1);
+            }
+        }
+    }
+    int my_changed = 0;
+    if (tx == 0) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            int r = r0 + ty * 4 + a;
+            s_unc[ty * 4 + a] = 0;
+            if (r >= n) continue;
+            int *dst = jb.assign + u * jb.assign_ustride + r;
+            if (k == 1 || certified(b1[a], b2[a])) {
+                int old = *dst;
+                if (old != i1[a]) {
+                    *dst = i1[a];
+                    ++my_changed;
+                }
+            } else {
+                s_unc[ty * 4 + a] = 1;
+            }
+        }
+        if (my_changed) atomicAdd(&s_changed, my_changed);
+    }
+    __syncthreads();
+    // uncertified rows: one contiguous block of the fallback list per CTA
+    if (tid < 32) {
+        int f0 = s_unc[tid], f1 = s_unc[tid + 32];
+        int cnt = __popc(__ballot_sync(0xffffffffu, f0)) + __popc(__ballot_sync(0xffffffffu, f1));
+        if (tid == 0) s_base = cnt ? atomicAdd(jb.fb_cnt + u * jb.T + jb.t, cnt) : 0;
+        __syncwarp();
+        int base = s_base;
+        uint32_t m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
+        int *fl = jb.fb_list + u * jb.fb_ustride;
+        if (f0) fl[base + __popc(m0 & lanemask_lt())] = r0 + tid;
+        if (f1) fl[base + __popc(m0) + __popc(m1 & lanemask_lt())] = r0 + 32 + tid;
+        if (tid == 0 && s_changed) atomicAdd(jb.changed + u * jb.T + jb.t, s_changed);
+    }
+}
+
+// Rows the fp32 pass could not certify: one warp per row, lanes over centroids, the exact
+// fp64 rule; lowest index on ties.
+__global__ void k_assign_fallback(AssignJob jb) {
+    const int u = blockIdx.y;
+    const int *chg = jb.changed + (int64_t)u * jb.T;
+    if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
+    const uint16_t *x;
+    int n, k;
+    job_unit(jb, u, x, n, k);
+    const int cnt = jb.fb_cnt[u * jb.T + jb.t];
+    const float *cent = jb.cent + u * jb.cent_ustride;
+    const int lane = threadIdx.x & 31;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int e = warp; e < cnt; e += nwarps) {
+        int r = jb.fb_list[u * jb.fb_ustride + e];
+        const uint16_t *xr = x + (int64_t)r * jb.sn;
+        double best = INFINITY;
+        int bi = 0x7fffffff;
+        for (int c = lane; c < k; c += 32) {
+            double dd = exact_dist(xr, cent + (int64_t)c * MOG_D);
+            if (dd < best) {
+                best = dd;
+                bi = c;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            double ob = __shfl_xor_sync(0xffffffffu, best, o);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ob < best || (ob == best && oi < bi)) {
+                best = ob;
+                bi = oi;
+            }
+        }
+        if (lane == 0) {
+            int *dst = jb.assign + u * jb.assign_ustride + r;
+            if (*dst != bi) {
+                *dst = bi;
+                atomicAdd(jb.changed + u * jb.T + jb.t, 1);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Stable counting sort of the first-level assignment: per-chunk histograms, a column
+// scan over chunks, a scan over clusters, then one warp per chunk scatters its rows in
+// order (ranks inside a warp from __match_any_sync).  perm lists positions S + i.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ bool l1_skip(const Dev &dv, int u, int t) {
+    return t >= 1 && converged_by(dv.changed + (int64_t)u * dv.T1, t);
+}
+
+__global__ void k_sort_hist(Dev dv, int t) {
+    extern __shared__ int hs[];
+    const int u = blockIdx.y, chunk = blockIdx.x;
+    if (l1_skip(dv, u, t)) return;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int n = ui[UI_NMID], C = ui[UI_C];
+    const int lo = chunk * SORT_CHUNK;
+    if (lo >= n) return;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) hs[c] = 0;
+    __syncthreads();
+    const int *a = dv.l1_assign + (int64_t)u * dv.n_cap;
+    for (int i = lo + threadIdx.x; i < min(n, lo + SORT_CHUNK); i += blockDim.x) atomicAdd(&hs[a[i]], 1);
+    __syncthreads();
+    int *h = dv.hist + ((int64_t)u * dv.nchunks + chunk) * dv.c_max;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) h[c] = hs[c];
+}
+
+__global__ void k_sort_colscan(Dev dv, int t) {
+    const int u = blockIdx.y;
+    if (l1_skip(dv, u, t)) return;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int n = ui[UI_NMID], C = ui[UI_C];
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    const int nch = (int)ceil_div64(n, SORT_CHUNK);
+    const int *h = dv.hist + (int64_t)u * dv.nchunks * dv.c_max + c;
+    int *o = dv.offs + (int64_t)u * dv.nchunks * dv.c_max + c;
+    int run = 0;
+    for (int k = 0; k < nch; ++k) {
+        o[(int64_t)k * dv.c_max] = run;
+        run += h[(int64_t)k * dv.c_max];
+    }
+    dv.ctot[(int64_t)u * dv.c_max + c] = run;
+}
+
+// exclusive scan of the cluster totals: coff[u][0..C]
+__global__ void k_sort_base(Dev dv, int t) {
+    __shared__ int wsum[32];
+    const int u = blockIdx.x;
+    if (l1_skip(dv, u, t)) return;
+    const int C = dv.unit_info[u * UI_STRIDE + UI_C];
+    const int *tot = dv.ctot + (int64_t)u * dv.c_max;
+    int *co = dv.coff + (int64_t)u * (dv.c_max + 1);
+    const int per = (int)ceil_div64(C, blockDim.x);
+    const int c0 = threadIdx.x * per;
+    int s = 0;
+    for (int c = c0; c < min(C, c0 + per); ++c) s += tot[c];
+    // block exclusive scan of s
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int v = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;
+        int inc2 = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, inc2, o);
+            if (lane >= o) inc2 += y;
+        }
+        wsum[lane] = inc2 - v;
+    }
+    __syncthreads();
+    int run = wsum[w] + incl - s;
+    for (int c = c0; c < min(C, c0 + per); ++c) {
+        co[c] = run;
+        run += tot[c];
+    }
+    if (c0 < C && c0 + per >= C) co[C] = run;
+    if (C == 0 && threadIdx.x == 0) co[0] = 0;
+}
+
+__global__ void k_sort_scatter(Dev dv, int t) {
+    extern __shared__ int cnt[];
+    const int u = blockIdx.y, chunk = blockIdx.x;
+    if (l1_skip(dv, u, t)) return;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int n = ui[UI_NMID], C = ui[UI_C], S = ui[UI_S];
+    const int lo = chunk * SORT_CHUNK;
+    if (lo >= n) return;
+    const int lane = threadIdx.x;
+    for (int c = lane; c < C; c += 32) cnt[c] = 0;
+    __syncwarp();
+    const int *a = dv.l1_assign + (int64_t)u * dv.n_cap;
+    const int *o = dv.offs + ((int64_t)u * dv.nchunks + chunk) * dv.c_max;
+    const int *co = dv.coff + (int64_t)u * (dv.c_max + 1);
+    int *perm = dv.permA + (int64_t)u * dv.n_cap;
+    const int hi = min(n, lo + SORT_CHUNK);
+    for (int i0 = lo; i0 < hi; i0 += 32) {
+        int i = i0 + lane;
+        bool valid = i < hi;
+        int c = valid ? a[i] : -1;
+        uint32_t grp = __match_any_sync(0xffffffffu, c);
+        int rank = __popc(grp & lanemask_lt());
+        if (valid) {
+            int pos = co[c] + o[c] + cnt[c] + rank;
+            perm[pos] = S + i;
+        }
+        __syncwarp();
+        if (valid && rank == 0) cnt[c] += __popc(grp);
+        __syncwarp();
+    }
+}
+
+// Centroid update: fp32 Kahan mean of the members in sorted (position) order; 8 warps
+// each sum a contiguous slice, combined in warp order.  Empty clusters keep the centroid.
+__global__ void __launch_bounds__(256) k_l1_update(Dev dv, int t) {
+    __shared__ float ps[8][MOG_D];
+    __shared__ float pc[8][MOG_D];
+    const int u = blockIdx.y, c = blockIdx.x;
+    if (l1_skip(dv, u, t)) return;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    if (c >= ui[UI_C]) return;
+    const int b = ui[UI_B], h = u % dv.h_kv;
+    const int *co = dv.coff + (int64_t)u * (dv.c_max + 1);
+    const int lo = co[c], n = co[c + 1] - lo;
+    if (n == 0) return;
+    const int *perm = dv.permA + (int64_t)u * dv.n_cap + lo;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = (int)((int64_t)w * n / 8), m1 = (int)((int64_t)(w + 1) * n / 8);
+    Kahan acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q].init();
+    for (int m = m0; m < m1; ++m) {
+        const uint16_t *row = dv.krow(b, h, perm[m]);
+        uint2 wv = *reinterpret_cast<const uint2 *>(row + lane * 4);
+        acc[0].add(bf_lo(wv.x));
+        acc[1].add(bf_hi(wv.x));
+        acc[2].add(bf_lo(wv.y));
+        acc[3].add(bf_hi(wv.y));
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        ps[w][lane * 4 + q] = acc[q].s;
+        pc[w][lane * 4 + q] = acc[q].c;
+    }
+    __syncthreads();
+    if (threadIdx.x < MOG_D) {
+        Kahan tot;
+        tot.init();
+        for (int ww = 0; ww < 8; ++ww) {
+            tot.add(ps[ww][threadIdx.x]);
+            tot.add(-pc[ww][threadIdx.x]);
+        }
+        dv.cent[((int64_t)u * dv.c_max + c) * MOG_D + threadIdx.x] = tot.s / (float)n;
+    }
+}
+
+__global__ void k_l1_init(Dev dv) {
+    const int u = blockIdx.y, c = blockIdx.x;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int C = ui[UI_C], n = ui[UI_NMID];
+    if (c >= C || n == 0) return;
+    const int b = ui[UI_B], h = u % dv.h_kv;
+    const int64_t pos = ui[UI_S] + (int64_t)c * n / C;
+    const uint16_t *row = dv.krow(b, h, pos);
+    for (int j = threadIdx.x; j < MOG_D; j += blockDim.x)
+        dv.cent[((int64_t)u * dv.c_max + c) * MOG_D + j] = bf1(row[j]);
+}
+
+// ------------------------------------------------------------------------------------
+// Second level + summaries, one CTA per (unit, cluster).
+// ------------------------------------------------------------------------------------
+
+// One assignment of row x (bf16, 128) among k centroids cs[k][d] in shared memory.
+__device__ __forceinline__ int assign_small(const uint16_t *x, const float *cs, int k) {
+    uint32_t w[64];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        uint4 v = *reinterpret_cast<const uint4 *>(x + q * 8);
+        w[4 * q] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
+    }
+    float b1 = INFINITY, b2 = INFINITY;
+    int i1 = 0;
+    for (int l = 0; l < k; ++l) {
+        const float *c = cs + l * MOG_D;
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 64; ++q) {
+            float d0 = __fsub_rn(bf_lo(w[q]), c[2 * q]);
+            acc = __fmaf_rn(d0, d0, acc);
+            float d1 = __fsub_rn(bf_hi(w[q]), c[2 * q + 1]);
+            acc = __fmaf_rn(d1, d1, acc);
+        }
+        if (acc < b1) {
+            b2 = b1;
+            b1 = acc;
+            i1 = l;
+        } else if (acc < b2) {
+            b2 = acc;
+        }
+    }
+    if (k == 1 || certified(b1, b2)) return i1;
+    double best = INFINITY;
+    int bi = 0;
+    for (int l = 0; l < k; ++l) {
+        double dd = exact_dist(x, cs + l * MOG_D);
+        if (dd < best) {
+            best = dd;
+            bi = l;
+        }
+    }
+    return bi;
+}
+
+struct SegJob {  // standalone segmented assignment (parity export)
+    const uint16_t *x;
+    int64_t ld;
+    const int32_t *rows, *seg_off;
+    const float *cent;
+    int k;
+    int32_t *assign;
+};
+
+constexpr int L2_THREADS = 256;
+
+__global__ void __launch_bounds__(L2_THREADS) k_assign_segments(SegJob jb) {
+    __shared__ __align__(16) float cs[MOG_MAX_L * MOG_D];
+    const int s = blockIdx.x;
+    const int lo = jb.seg_off[s], hi = jb.seg_off[s + 1];
+    for (int e = threadIdx.x; e < jb.k * MOG_D; e += blockDim.x)
+        cs[e] = jb.cent[(int64_t)s * jb.k * MOG_D + e];
+    __syncthreads();
+    for (int m = lo + threadIdx.x; m < hi; m += blockDim.x)
+        jb.assign[m] = assign_small(jb.x + (int64_t)jb.rows[m] * jb.ld, cs, jb.k);
+}
+
+__global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) {
+    extern __shared__ __align__(16) float l2s[];
+    float *cs = l2s;                          // [L][d] centroids
+    float *ks = cs + MOG_MAX_L * MOG_D;       // [L][d] Kahan sums
+    float *kc = ks + MOG_MAX_L * MOG_D;       // [L][d] Kahan compensation
+    __shared__ int cnt[MOG_MAX_L], pref[MOG_MAX_L + 1], fill[MOG_MAX_L];
+    __shared__ int s_changed;
+    const int u = blockIdx.y, c = blockIdx.x;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int C = ui[UI_C], L = ui[UI_L];
+    if (c >= C) return;
+    if (!do_kmeans && *(volatile const int *)dv.status != 0) return;  // rejected partition
+    const int b = ui[UI_B], h = u % dv.h_kv;
+    const int tid = threadIdx.x;
+    int *so = dv.sub_off + u * dv.sub_off_stride;
+    int *permF = dv.perm + (int64_t)u * dv.n_cap;
+    int lo, n;
+    if (do_kmeans) {
+        const int *co = dv.coff + (int64_t)u * (dv.c_max + 1);
+        lo = co[c];
+        n = co[c + 1] - lo;
+        if (c == 0 && tid == 0) {  // record the first-level step count
+            int steps = dv.T1;
+            const int *chg = dv.changed + (int64_t)u * dv.T1;
+            for (int s = 1; s < dv.T1; ++s)
+                if (chg[s] == 0) { steps = s + 1; break; }
+            dv.l1_steps[u] = ui[UI_NMID] > 0 ? steps : 0;
+        }
+    } else {
+        lo = so[c * L];
+        n = so[(c + 1) * L] - lo;
+    }
+    if (do_kmeans) {
+        const int *pA = dv.permA + (int64_t)u * dv.n_cap + lo;
+        int *sa = dv.sub_assign + (int64_t)u * dv.n_cap + lo;
+        if (n > 0) {
+            for (int e = tid; e < L * MOG_D; e += blockDim.x) {
+                int l = e / MOG_D, j = e % MOG_D;
+                cs[e] = bf1(dv.krow(b, h, pA[(int64_t)l * n / L])[j]);
+            }
+            for (int m = tid; m < n; m += blockDim.x) sa[m] = -1;
+        }
+        for (int t = 0; t < dv.T2 && n > 0; ++t) {
+            if (tid == 0) s_changed = 0;
+            __syncthreads();
+            int my = 0;
+            for (int m = tid; m < n; m += blockDim.x) {
+                int a = assign_small(dv.krow(b, h, pA[m]), cs, L);
+                if (a != sa[m]) {
+                    sa[m] = a;
+                    ++my;
+                }
+            }
+            if (my) atomicAdd(&s_changed, my);
+            __syncthreads();
+            if (t > 0 && s_changed == 0) break;
+            if (t + 1 == dv.T2) break;
+            // update: thread j owns dimension j, members in position order
+            if (tid < MOG_D) {
+                for (int l = 0; l < L; ++l) {
+                    ks[l * MOG_D + tid] = 0.f;
+                    kc[l * MOG_D + tid] = 0.f;
+                }
+                for (int m = 0; m < n; ++m) {
+                    int a = sa[m];
+                    float v = bf1(dv.krow(b, h, pA[m])[tid]);
+                    float y = __fsub_rn(v, kc[a * MOG_D + tid]);
+                    float s0 = ks[a * MOG_D + tid];
+                    float tt = __fadd_rn(s0, y);
+                    kc[a * MOG_D + tid] = __fsub_rn(__fsub_rn(tt, s0), y);
+                    ks[a * MOG_D + tid] = tt;
+                }
+            }
+            if (tid < MOG_MAX_L) cnt[tid] = 0;
+            __syncthreads();
+            for (int m = tid; m < n; m += blockDim.x) atomicAdd(&cnt[sa[m]], 1);
+            __syncthreads();
+            if (tid < MOG_D)
+                for (int l = 0; l < L; ++l)
+                    if (cnt[l] > 0) cs[l * MOG_D + tid] = ks[l * MOG_D + tid] / (float)cnt[l];
+            __syncthreads();
+        }
+        // final order: (subcluster, position), stable
+        if (tid < MOG_MAX_L) cnt[tid] = 0;
+        __syncthreads();
+        for (int m = tid; m < n; m += blockDim.x) atomicAdd(&cnt[sa[m]], 1);
+        __syncthreads();
+        if (tid == 0) {
+            pref[0] = 0;
+            for (int l = 0; l < L; ++l) pref[l + 1] = pref[l] + cnt[l];
+            for (int l = 0; l < L; ++l) {
+                so[c * L + l] = lo + pref[l];
+                fill[l] = 0;
+            }
+            if (c == C - 1) so[C * L] = lo + n;
+        }
+        __syncthreads();
+        if (tid < 32) {
+            for (int m0 = 0; m0 < n; m0 += 32) {
+                int m = m0 + tid;
+                bool valid = m < n;
+                int a = valid ? sa[m] : -1;
+                uint32_t grp = __match_any_sync(0xffffffffu, a);
+                int rank = __popc(grp & lanemask_lt());
+                if (valid) permF[lo + pref[a] + fill[a] + rank] = pA[m];
+                __syncwarp();
+                if (valid && rank == 0) fill[a] += __popc(grp);
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+    }
+    // ---------------- summaries: thread j < d on K, thread d + j on V -----------------
+    const int *pf = permF + lo;
+    const int j = tid & (MOG_D - 1);
+    const bool isV = tid >= MOG_D;
+    const int64_t cg = (int64_t)u * dv.c_max + c;
+    Kahan tot;
+    tot.init();
+    for (int l = 0; l < L; ++l) {
+        const int g0 = so[c * L + l] - lo, g1 = so[c * L + l + 1] - lo;
+        const int64_t sg = (int64_t)u * dv.c_max * dv.l_max + (int64_t)c * L + l;
+        Kahan s;
+        s.init();
+        for (int m = g0; m < g1; ++m) {
+            const uint16_t *row = isV ? dv.vrow(b, h, pf[m]) : dv.krow(b, h, pf[m]);
+            float v = bf1(row[j]);
+            s.add(v);
+            tot.add(v);
+        }
+        const int ng = g1 - g0;
+        const float mean = ng > 0 ? s.s / (float)ng : 0.f;
+        if (isV) {
+            dv.sub_vbar[sg * MOG_D + j] = mean;
+        } else {
+            dv.sub_ms[sg * 2 * MOG_D + j] = mean;
+            Kahan q;
+            q.init();
+            for (int m = g0; m < g1; ++m) {
+                float df = __fsub_rn(bf1(dv.krow(b, h, pf[m])[j]), mean);
+                q.add(__fmul_rn(df, df));
+            }
+            dv.sub_ms[sg * 2 * MOG_D + MOG_D + j] = ng > 0 ? q.s / (float)ng : 0.f;
+            if (j == 0) dv.sub_n[sg] = ng;
+        }
+    }
+    const float cmean = n > 0 ? tot.s / (float)n : 0.f;
+    if (isV) {
+        dv.cl_vbar[cg * MOG_D + j] = cmean;
+        // cluster variance (keys), computed by the V threads in parallel with the K threads
+        Kahan s;
+        s.init();
+        for (int m = 0; m < n; ++m) s.add(bf1(dv.krow(b, h, pf[m])[j]));
+        const float km = n > 0 ? s.s / (float)n : 0.f;
+        Kahan q;
+        q.init();
+        for (int m = 0; m < n; ++m) {
+            float df = __fsub_rn(bf1(dv.krow(b, h, pf[m])[j]), km);
+            q.add(__fmul_rn(df, df));
+        }
+        dv.cl_ms[cg * 2 * MOG_D + MOG_D + j] = n > 0 ? q.s / (float)n : 0.f;
+    } else {
+        dv.cl_ms[cg * 2 * MOG_D + j] = cmean;
+        if (j == 0) dv.cl_n[cg] = n;
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// launchers
+// ------------------------------------------------------------------------------------
+static AssignJob build_job(const Dev &dv, int t) {
+    AssignJob jb;
+    jb.K = dv.K;
+    jb.sb = dv.sb;
+    jb.sh = dv.sh;
+    jb.sn = dv.sn;
+    jb.h_kv = dv.h_kv;
+    jb.unit_info = dv.unit_info;
+    jb.n_single = 0;
+    jb.k_single = 0;
+    jb.cent = dv.cent;
+    jb.cent_ustride = (int64_t)dv.c_max * MOG_D;
+    jb.assign = dv.l1_assign;
+    jb.assign_ustride = dv.n_cap;
+    jb.changed = dv.changed;
+    jb.fb_list = dv.fb_list;
+    jb.fb_ustride = dv.n_cap;
+    jb.fb_cnt = dv.fb_cnt;
+    jb.t = t;
+    jb.T = dv.T1;
+    return jb;
+}
+
+static cudaError_t set_smem(const void *fn, size_t bytes) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+static size_t l2_smem() { return 3 * MOG_MAX_L * MOG_D * sizeof(float); }
+
+cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = set_smem((const void *)k_assign_l1, AS_SMEM)) != cudaSuccess) return e;
+    if ((e = set_smem((const void *)k_l2_stats, l2_smem())) != cudaSuccess) return e;
+    if ((e = set_smem((const void *)k_sort_hist, pl.c_max * sizeof(int))) != cudaSuccess) return e;
+    if ((e = set_smem((const void *)k_sort_scatter, pl.c_max * sizeof(int))) != cudaSuccess) return e;
+    const int U = pl.units;
+    if (pl.n_mid_max > 0) {
+        k_l1_init<<<dim3(pl.c_max, U), 128, 0, s>>>(dv);
+        const int rblocks = (int)ceil_div64(pl.n_mid_max, AS_ROWS);
+        for (int t = 0; t < pl.T1; ++t) {
+            AssignJob jb = build_job(dv, t);
+            k_assign_l1<<<dim3(rblocks, U), AS_THREADS, AS_SMEM, s>>>(jb);
+            k_assign_fallback<<<dim3(16, U), 256, 0, s>>>(jb);
+            k_sort_hist<<<dim3(pl.nchunks, U), 256, pl.c_max * sizeof(int), s>>>(dv, t);
+            k_sort_colscan<<<dim3((int)ceil_div64(pl.c_max, 128), U), 128, 0, s>>>(dv, t);
+            k_sort_base<<<U, 1024, 0, s>>>(dv, t);
+            k_sort_scatter<<<dim3(pl.nchunks, U), 32, pl.c_max * sizeof(int), s>>>(dv, t);
+            if (t + 1 < pl.T1) k_l1_update<<<dim3(pl.c_max, U), 256, 0, s>>>(dv, t);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    }
+    k_l2_stats<<<dim3(pl.c_max, U), L2_THREADS, l2_smem(), s>>>(dv, 1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats_only(const Dev &dv, const Plan &pl, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = set_smem((const void *)k_l2_stats, l2_smem())) != cudaSuccess) return e;
+    k_l2_stats<<<dim3(pl.c_max, pl.units), L2_THREADS, l2_smem(), s>>>(dv, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
+                             int32_t *assign, int *changed, int *fb_list, int *fb_cnt,
+                             cudaStream_t s) {
+    cudaError_t e;
+    if ((e = set_smem((const void *)k_assign_l1, AS_SMEM)) != cudaSuccess) return e;
+    AssignJob jb;
+    jb.K = x;
+    jb.sb = jb.sh = 0;
+    jb.sn = ld;
+    jb.h_kv = 1;
+    jb.unit_info = nullptr;
+    jb.n_single = n;
+    jb.k_single = k;
+    jb.cent = cent;
+    jb.cent_ustride = 0;
+    jb.assign = assign;
+    jb.assign_ustride = 0;
+    jb.changed = changed;
+    jb.fb_list = fb_list;
+    jb.fb_ustride = 0;
+    jb.fb_cnt = fb_cnt;
+    jb.t = 0;
+    jb.T = 1;
+    if (n > 0) {
+        k_assign_l1<<<dim3((int)ceil_div64(n, AS_ROWS), 1), AS_THREADS, AS_SMEM, s>>>(jb);
+        k_assign_fallback<<<dim3(16, 1), 256, 0, s>>>(jb);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_assign_segments(const uint16_t *x, int64_t ld, const int32_t *rows,
+                                   const int32_t *seg_off, int n_seg, const float *cent, int k,
+                                   int32_t *assign, cudaStream_t s) {
+    SegJob jb{x, ld, rows, seg_off, cent, k, assign};
+    if (n_seg > 0) k_assign_segments<<<n_seg, L2_THREADS, 0, s>>>(jb);
+    return cudaGetLastError();
+}
+
+}  // namespace mog
