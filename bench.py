@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""MoG decode benchmark: microseconds per decode step per layer, and achieved HBM GB/s of
+the exact-attention kernel against the measured HBM roofline.
+
+Workload (default): the Qwen3-4B-shaped decode layer -- 32 query heads over 8 KV heads,
+d = 128, N = 32768 bf16 keys per KV head from the planted-centre generator, 181 clusters
+x 15 subclusters, top-8 clusters x top-8 subclusters, 4 sink + 256 recent anchors.  The
+build runs once before timing (prefill time); a step is one mog_decode of the whole
+layer.  L2 is flushed (a 256 MB write) before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mog|reference] [--workload W]
+
+--impl reference times the CPU oracle (the plain fp64 statement of the method) on the
+host cores on a bounded sample of the same workload.  Under torchrun every rank runs an
+independent replica (the method has no cross-GPU exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from serving_mog_decode_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MoG decode us/step/layer at 32K-1M ctx; achieved HBM GB/s vs roofline"
+D = 128
+FLUSH_BYTES = 256 << 20
+
+
+def args_():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="mog", choices=["mog", "reference"])
+    ap.add_argument("--workload", default="qwen3-4b-32k", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="budget of the oracle timing sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "serving_mog_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload, kernel):
+    """dram bytes per launch of `kernel` from a committed ncu summary, if it was taken
+    on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(workload, {}).get(kernel)
+        if e and e.get("source_hash") == kernel_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling (200 ms) around the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", str(dev_index)], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------ the oracle
+
+def oracle_decode_sample(w, budget_s, steps=None, warmup=0):
+    """Time the oracle's decode step (selection + exact + residual, every query head of
+    one KV head) on unit (0, 0); the oracle's own build of that unit is untimed.
+    Returns (us per step per layer, cores, description, per-step list)."""
+    import oracle
+    n = int(wl.lengths(w)[0])
+    K, V, q = wl.make_unit(w, 0, 0, n)
+    Cn, L = wl.clusters_for(w, n)
+    summ = oracle.build_unit(K, V, n, w.n_sink, w.n_recent, Cn, L)
+    units = w.batch * w.h_kv
+
+    def one():
+        for g in range(w.group):
+            oracle.mog_head(K, V, n, q[g], summ, w.top_c, w.top_s)
+
+    for _ in range(warmup):
+        one()
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while (steps is None and (time.perf_counter() < t_end or len(times) < 3)) or \
+            (steps is not None and len(times) < steps):
+        t0 = time.perf_counter()
+        one()
+        times.append((time.perf_counter() - t0) * 1e6 * units)
+        if steps is None and len(times) >= 1000:
+            break
+    desc = (f"KV head (b=0,h=0) of {units} with its {w.group} query heads, oracle decode step "
+            f"timed {len(times)}x, scaled x{units} to the layer; build untimed")
+    return statistics.mean(times), 1, desc, times
+
+
+# ------------------------------------------------------------------------ GPU path
+
+def bytes_from_selection(h, w, sel, lens, n_now):
+    """Algorithmic bytes of one decode step: all cluster summaries, the subcluster summaries
+    of each unit's union of selected clusters, the K/V rows (+ index) of the union of
+    selected subclusters, the anchors, and the output."""
+    import torch
+    lay = h.layout()
+    U, cm, lm, G = lay.units, lay.c_max, lay.l_max, lay.group
+    info = h.array("unit_info", torch.int32, (U, 8)).cpu().numpy()
+    off = h.array("sub_off", torch.int32, (U, lay.sub_off_stride)).cpu().numpy()
+    tc, ts = w.top_c, w.top_s
+    sel = sel.reshape(U, G, -1)
+    tot = dict(k1=0, k2=0, k3=0, rows=0)
+    for u in range(U):
+        Cn, L, nb, S, rlo, b = info[u, 0], info[u, 1], info[u, 2], info[u, 4], info[u, 5], info[u, 6]
+        ucl, usub = set(), set()
+        for g in range(G):
+            for i in range(tc):
+                c = sel[u, g, i]
+                if c < 0:
+                    continue
+                ucl.add(int(c))
+                for r in range(ts):
+                    l = sel[u, g, tc + i * ts + r]
+                    if l >= 0:
+                        usub.add((int(c), int(l)))
+        Uk = sum(int(off[u, c * L + l + 1] - off[u, c * L + l]) for c, l in usub)
+        anchors = min(S, n_now[b]) + max(0, n_now[b] - rlo)
+        tot["k1"] += Cn * (8 * D + 4) + G * D * 2
+        tot["k2"] += len(ucl) * L * (8 * D + 4) + Uk * 12
+        tot["k3"] += Uk * (4 * D + 8) + anchors * 4 * D + (Cn + len(ucl) * L) * 4 * D + G * D * 4
+        tot["rows"] += Uk + anchors
+    tot["step"] = tot["k1"] + tot["k2"] + tot["k3"]
+    return tot
+
+
+def run_gpu(a, w, rank, world):
+    import torch
+
+    import serving_mog_decode_gb300 as mog
+    from serving_mog_decode_gb300 import buildlib
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(mog.LIB_PATH):
+        buildlib.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    lens = wl.lengths(w)
+    K, V, q, _ = wl.make_batch(w)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    Kd, Vd, qd = bf(K), bf(V), bf(q)
+    del K, V
+    prm = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], n_clusters=w.n_clusters, n_sub=w.n_sub,
+                          top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    # ---- build (once, prefill time) ----
+    torch.cuda.synchronize()
+    b0, b1 = ev(), ev()
+    b0.record()
+    h = mog.build(Kd, Vd, lens, prm)
+    b1.record()
+    torch.cuda.synchronize()
+    build_ms = b0.elapsed_time(b1)
+    assert h.sync_status() == 0
+    lay = h.layout()
+    steps1 = h.array("l1_steps", torch.int32, (lay.units,)).cpu().numpy()
+    info = h.array("unit_info", torch.int32, (lay.units, 8)).cpu().numpy()
+    l1_flop = float(sum(2.0 * info[u, 3] * D * info[u, 0] * steps1[u] for u in range(lay.units)))
+    l2_flop = float(sum(2.0 * info[u, 3] * D * info[u, 1] * 10 for u in range(lay.units)))
+
+    out = torch.empty(qd.shape, dtype=torch.float32, device=dev)
+    SW = w.top_c + w.top_c * w.top_s
+    sel = torch.empty((lay.units * lay.group, max(SW, 1)), dtype=torch.int32, device=dev)
+    h.decode(qd, out, sel_out=sel)
+    torch.cuda.synchronize()
+    n_now = [int(x) for x in lens]
+    by = bytes_from_selection(h, w, sel.cpu().numpy(), lens, n_now)
+
+    clocks = Clocks(local)
+    # ---- settle clocks, then dense_decode (the full scan) for comparison ----
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        for _ in range(50):
+            h.decode(qd, out)
+        torch.cuda.synchronize()
+    dense_out = torch.empty_like(out)
+    dscratch = torch.empty(mog.dense_scratch_bytes(w.batch, w.h_kv, w.h_q, int(lens.max())),
+                           dtype=torch.uint8, device=dev)
+    dense_ms = []
+    for i in range(3 + 10):
+        flush.zero_()
+        s0, s1 = ev(), ev()
+        s0.record()
+        mog.dense_decode(Kd, Vd, h.lengths_dev, int(lens.max()), qd, dense_out, dscratch)
+        s1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            dense_ms.append(s0.elapsed_time(s1))
+    dense_bytes = float(sum(int(lens[u // w.h_kv]) for u in range(lay.units))) * 4 * D
+    # ---- the timed decode steps ----
+    for _ in range(a.warmup):
+        flush.zero_()
+        h.decode(qd, out)
+    starts = [ev() for _ in range(a.steps)]
+    ends = [ev() for _ in range(a.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        flush.zero_()
+        starts[i].record()
+        h.decode(qd, out)
+        ends[i].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # ---- per-kernel times (events between the three kernels) ----
+    phase = [[], [], []]
+    for i in range(max(20, min(a.steps, 200))):
+        flush.zero_()
+        evs = [ev() for _ in range(4)]
+        h.decode_phased(qd, out, evs)
+        torch.cuda.synchronize()
+        for k in range(3):
+            phase[k].append(evs[k].elapsed_time(evs[k + 1]))
+    # ---- end to end through the C ABI with host buffers ----
+    q_host = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(a.warmup + a.steps):
+        flush.zero_()
+        s0, s1 = ev(), ev()
+        s0.record()
+        qd.copy_(q_host, non_blocking=True)
+        h.decode(qd, out)
+        out_host.copy_(out, non_blocking=True)
+        s1.record()
+        torch.cuda.synchronize()
+        if i >= a.warmup:
+            e2e_ms.append(s0.elapsed_time(s1))
+    clk = clocks.stop()
+    assert h.sync_status() == 0
+
+    mean_ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([mean_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    pm = [statistics.mean(p) for p in phase]
+    names = ["k_dec_score", "k_dec_sub", "k_dec_attend"]
+    dom = int(np.argmax(pm))
+    kbytes = [by["k1"], by["k2"], by["k3"]]
+    peak, peak_kind = peaks()
+    achieved = kbytes[dom] / (pm[dom] * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(mean_ms * 1e3 / world, 3),
+        "unit": "us/step/layer",
+        "n_gpus": world,
+        "steps": a.steps,
+        "warmup": a.warmup,
+        "ms_per_step": round(mean_ms, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (planted-centre keys, Gaussian values; seeded)",
+        "config": {"workload": w.name, "batch": w.batch, "h_kv": w.h_kv, "h_q": w.h_q, "d": D,
+                   "context": int(lens.max()), "clusters": w.n_clusters, "subclusters": w.n_sub,
+                   "top_c": w.top_c, "top_s": w.top_s, "n_sink": w.n_sink, "n_recent": w.n_recent,
+                   "l2": "flushed before every timed step (256 MB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": stored_traffic(w.name, names[dom]),
+                     "algorithmic_bytes_per_launch": int(kbytes[dom]),
+                     "launch_us": round(pm[dom] * 1e3, 3)},
+        "kernels_us": {n_: round(p * 1e3, 3) for n_, p in zip(names, pm)},
+        "step_bytes": int(by["step"]),
+        "step_GBps": round(by["step"] / (mean_ms * 1e-3) / 1e9, 1),
+        "step_frac_of_peak": round(by["step"] / (mean_ms * 1e-3) / 1e9 / peak, 4),
+        "kv_rows_read": int(by["rows"]),
+        "kv_read_fraction": round(by["rows"] / float(sum(n_now[u // w.h_kv] for u in range(lay.units))), 4),
+        "dense_decode": {"us": round(statistics.mean(dense_ms) * 1e3, 2),
+                         "GBps": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9, 1),
+                         "frac": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9 / peak, 4)},
+        "speedup_vs_dense": round(statistics.mean(dense_ms) / mean_ms, 2),
+        "build": {"ms": round(build_ms, 2), "l1_flop": l1_flop, "l2_flop": l2_flop,
+                  "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3)},
+        "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",
+                "h2d_bytes_per_step": int(q_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 4)},
+        "gpu_launches": 3 * a.steps if w.top_c > 0 else 2 * a.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        mu, cores, desc, _ = oracle_decode_sample(w, a.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(mu, 1), "unit": "us/step/layer", "cores": cores,
+                               "kind": "oracle", "sample": desc}
+        print(json.dumps(res), flush=True)
+
+
+def run_reference(a, w, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    mu, cores, desc, times = oracle_decode_sample(w, a.cpu_seconds, steps=a.steps, warmup=a.warmup)
+    res = {"metric": METRIC, "impl": "reference", "value": round(mu, 1), "unit": "us/step/layer",
+           "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+           "ms_per_step": round(mu / 1e3, 4), "higher_is_better": False, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (planted-centre keys; seeded)",
+           "config": {"workload": w.name},
+           "cpu_baseline": {"value": round(mu, 1), "unit": "us/step/layer", "cores": cores,
+                            "kind": "oracle", "sample": desc},
+           "e2e": {"value": round(mu, 1), "unit": "us/step/layer", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    a = args_()
+    w = wl.WORKLOADS[a.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if a.impl == "reference":
+        run_reference(a, w, rank)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    run_gpu(a, w, rank, world)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

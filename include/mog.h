@@ -12,7 +12,7 @@
  *        anchors are attended exactly together with the retrieved keys; the estimated
  *        numerator and denominator of the rest are added in the unnormalised domain and
  *        one normalisation follows.
- * Residual form of this library (consistent with [IA]'s "means and variances"): an
+ * Residual form of this library (consistent with [IA]'s use of group means and variances): an
  * unselected group s (count n_s, key mean mu_s, per-dimension population variance
  * sigma2_s, value mean vbar_s) adds den_s = n_s * exp(tau q.mu_s + tau^2/2 *
  * sum_j q_j^2 sigma2_sj - m) to the denominator and den_s * vbar_s to the numerator,
@@ -57,7 +57,7 @@ typedef enum {
  *  n_clusters, n_sub : C and L; 0 selects round(sqrt(N_b)) and ceil(log2(N_b)) from each
  *                      sequence's build length N_b ([IA]: O(sqrt N) x O(log N)).
  *  top_c, top_s      : clusters selected per query head, subclusters selected inside each
- *                      selected cluster ([IA]).  top_c*G <= 256, L <= 32.
+ *                      selected cluster ([IA]).  min(C, top_c*G) <= 256, L <= 32.
  *  n_sink, n_recent  : anchors S and R; positions [0,S) and [N_b-R, N) are never clustered
  *                      and always attended exactly ([RC]).
  *  iters_l1, iters_l2: Lloyd assignment steps per level (0 selects 10); a level stops
@@ -125,7 +125,7 @@ const char *mog_last_error(void);
 int mog_arena_bytes(const mog_params *p, const int32_t *lengths_host, size_t *bytes);
 
 /*
- * MoG build ([IA], "after prefill ... partitions the keys"): for every unit, first-level
+ * MoG build ([IA], the post-prefill hierarchical partition): for every unit, first-level
  * Lloyd k-means of the mid keys [S, N_b - R) into C_u clusters, second-level k-means of
  * each cluster into L_u subclusters, then count, key mean, per-dimension population
  * variance and value mean of every cluster and subcluster.  Enqueued on `stream`; no host
@@ -142,8 +142,8 @@ int mog_build(const mog_kv *kv, const int32_t *lengths_dev, const int32_t *lengt
               mog_handle **out);
 
 /*
- * MoG decode step ([IA], "scored against these compact representations ... attended
- * exactly ... approximated from the means and variances"; [RC]): per query head, score the
+ * MoG decode step ([IA], decoding: score the summaries, attend the best groups exactly,
+ * approximate the rest from their Gaussians; [RC]): per query head, score the
  * clusters, take the top top_c, score their subclusters, take the top top_s in each,
  * attend exactly to the members of the selected subclusters plus the anchors, add the
  * Gaussian residual of every unselected non-empty group, normalise once.
@@ -170,6 +170,16 @@ int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev, const int32_
  * n_cap (checked on the host from the build lengths and the number of appends).
  */
 int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void *stream);
+
+/*
+ * mog_decode_ex that also records four caller-created cudaEvent_t (passed as void*):
+ * events[0] before the cluster-scoring kernel, events[1] after it, events[2] after the
+ * subcluster kernel, events[3] after the exact-attention kernel, all on `stream`, so
+ * that each phase of one decode step can be timed.  Same arguments otherwise.
+ */
+int mog_decode_phased(mog_handle *h, const void *q_dev, float *out_dev,
+                      const int32_t *sel_in_dev, int32_t *sel_out_dev, void *const *events,
+                      void *stream);
 
 /* Copy the arena layout of a handle. */
 int mog_get_layout(const mog_handle *h, mog_layout *out);

@@ -102,7 +102,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
         P.n_mid_max = std::max(P.n_mid_max, std::max(0, n - p->n_recent - p->n_sink));
     }
     if (P.l_max > MOG_MAX_L || P.c_max > MAX_C || P.ts > MOG_MAX_L) return MOG_ERR_SHAPE;
-    if (P.G * P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
+    if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION) return MOG_ERR_SHAPE;
     const int tcc = std::max(P.tc, 1);
     const int p1_min = (int)ceil_div64(P.c_max, 64);
     const int p1_cap = std::min(64, 1024 / tcc);
@@ -410,6 +410,21 @@ extern "C" int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev,
     cudaError_t e = launch_decode(h->dev, h->plan, q_dev, out_dev, sel_in_dev, sel_out_dev,
                                   static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mog_decode launch");
+    return MOG_OK;
+}
+
+extern "C" int mog_decode_phased(mog_handle *h, const void *q_dev, float *out_dev,
+                                 const int32_t *sel_in_dev, int32_t *sel_out_dev,
+                                 void *const *events, void *stream) {
+    if (!h || !q_dev || !out_dev || !events) return MOG_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+        if (!events[i]) return MOG_ERR_INVALID_ARG;
+    if (!aligned16(q_dev) || !aligned16(out_dev)) return MOG_ERR_INVALID_ARG;
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i) ev[i] = static_cast<cudaEvent_t>(events[i]);
+    cudaError_t e = launch_decode(h->dev, h->plan, q_dev, out_dev, sel_in_dev, sel_out_dev,
+                                  static_cast<cudaStream_t>(stream), ev);
+    if (e != cudaSuccess) return cuda_fail(e, "mog_decode_phased launch");
     return MOG_OK;
 }
 

@@ -91,8 +91,6 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     float *stg_s = ssel + G * SC_SLICE;           // [8 warps][P1*tc]
     int *stg_i = reinterpret_cast<int *>(stg_s + 8 * dv.P1 * max(tc, 1));
     __shared__ int s_last;
-    __shared__ int s_ent[MOG_MAX_UNION];
-    __shared__ int s_first[MOG_MAX_UNION];
     __shared__ int s_wcnt[8];
     pdl_wait();
     pdl_trigger();
@@ -137,7 +135,13 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
                 bi = c0 + lane;
             }
             warp_best(bv, bi);
-            if (bv == -INFINITY) bi = -1;
+            if (bv == -INFINITY) {
+                for (int rr = r + lane; rr < tc; rr += 32) {
+                    cs[rr] = -INFINITY;
+                    ci[rr] = -1;
+                }
+                break;
+            }
             if (lane == 0) {
                 cs[r] = bv;
                 ci[r] = bi;
@@ -208,36 +212,32 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
             if (sg[r] >= 0) atomicOr(dv.cselmask + (size_t)u * dv.c_max + sg[r], 1u << g);
     }
     __syncthreads();
-    // union of selected clusters (first occurrence in head-major rank order)
-    const int E = G * tc;
-    for (int e = threadIdx.x; e < E; e += SC_THREADS) s_ent[e] = sel[(size_t)(e / tc) * a.SW + e % tc];
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += SC_THREADS) {
-        const int c = s_ent[e];
-        int f = c >= 0;
-        for (int k = 0; k < e && f; ++k)
-            if (s_ent[k] == c) f = 0;
-        s_first[e] = f;
-    }
-    __syncthreads();
-    // exclusive prefix of s_first (E <= 256 = SC_THREADS)
-    const int e = threadIdx.x;
-    const int f = e < E ? s_first[e] : 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) s_wcnt[warp] = __popc(bal);
-    __syncthreads();
-    int base = 0;
-    for (int k = 0; k < warp; ++k) base += s_wcnt[k];
-    if (f) {
-        const int slot = base + __popc(bal & lanemask_lt());
-        const int c = s_ent[e];
-        dv.ucl[(size_t)u * MOG_MAX_UNION + slot] = c;
-        dv.uhm[(size_t)u * MOG_MAX_UNION + slot] = __ldcg(dv.cselmask + (size_t)u * dv.c_max + c);
-    }
-    if (threadIdx.x == SC_THREADS - 1) {
-        int tot = 0;
-        for (int k = 0; k < SC_THREADS / 32; ++k) tot += s_wcnt[k];
-        dv.ucount[u] = tot;
+    // union of the selected clusters over the G heads, ascending cluster index
+    {
+        const int per = (int)ceil_div64(C, SC_THREADS);
+        const int cA = threadIdx.x * per, cB = min(C, cA + per);
+        const uint32_t *cm = dv.cselmask + (size_t)u * dv.c_max;
+        int cnt = 0;
+        for (int c = cA; c < cB; ++c) cnt += __ldcg(cm + c) != 0u;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wcnt[warp] = incl;
+        __syncthreads();
+        int base = incl - cnt;
+        for (int k = 0; k < warp; ++k) base += s_wcnt[k];
+        for (int c = cA; c < cB; ++c) {
+            const uint32_t m = __ldcg(cm + c);
+            if (m) {
+                dv.ucl[(size_t)u * MOG_MAX_UNION + base] = c;
+                dv.uhm[(size_t)u * MOG_MAX_UNION + base] = m;
+                ++base;
+            }
+        }
+        if (threadIdx.x == SC_THREADS - 1) dv.ucount[u] = base;
     }
 }
 
@@ -625,7 +625,8 @@ static cudaError_t launch_attend(const DecArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *out,
-                          const int32_t *sel_in, int32_t *sel_out, cudaStream_t s) {
+                          const int32_t *sel_in, int32_t *sel_out, cudaStream_t s,
+                          cudaEvent_t const *events) {
     DecArgs a;
     a.dv = dv;
     a.q = static_cast<const uint16_t *>(q);
@@ -639,13 +640,16 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
     if ((e = cudaFuncSetAttribute((const void *)k_dec_score,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss)) != cudaSuccess)
         return e;
+    if (events && (e = cudaEventRecord(events[0], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_dec_score, dim3(dv.P1, dv.units), dim3(SC_THREADS), ss, s, a)) != cudaSuccess)
         return e;
+    if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
     if (dv.tc > 0) {
-        if ((e = launch_pdl(k_dec_sub, dim3(dv.G * dv.tc, dv.units), dim3(SUB_THREADS), sub_smem(dv), s,
+        if ((e = launch_pdl(k_dec_sub, dim3(min(dv.c_max, dv.G * dv.tc), dv.units), dim3(SUB_THREADS), sub_smem(dv), s,
                             a)) != cudaSuccess)
             return e;
     }
+    if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     const int G = dv.G;
     if (G <= 1) e = launch_attend<1>(a, s);
     else if (G <= 2) e = launch_attend<2>(a, s);
@@ -653,6 +657,7 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
     else if (G <= 8) e = launch_attend<8>(a, s);
     else e = launch_attend<16>(a, s);
     if (e != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     if (sel_out && a.SW > 0)
         e = cudaMemcpyAsync(sel_out, dv.sel, sizeof(int32_t) * (size_t)dv.units * G * a.SW,
                             cudaMemcpyDeviceToDevice, s);

@@ -71,7 +71,8 @@ void unit_clusters(const mog_params *p, int n, int *C, int *L);
 cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s);
 cudaError_t launch_stats_only(const Dev &dv, const Plan &pl, cudaStream_t s);
 cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *out,
-                          const int32_t *sel_in, int32_t *sel_out, cudaStream_t s);
+                          const int32_t *sel_in, int32_t *sel_out, cudaStream_t s,
+                          cudaEvent_t const *events = nullptr);
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
                           cudaStream_t s);
 cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64_t sh,

@@ -635,7 +635,9 @@ __global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) 
     Kahan tot;
     tot.init();
     for (int l = 0; l < L; ++l) {
-        const int g0 = so[c * L + l] - lo, g1 = so[c * L + l + 1] - lo;
+        // the end of the last subcluster is this cluster's end (the next entry belongs
+        // to the next cluster's CTA)
+        const int g0 = so[c * L + l] - lo, g1 = (l + 1 < L ? so[c * L + l + 1] : lo + n) - lo;
         const int64_t sg = (int64_t)u * dv.c_max * dv.l_max + (int64_t)c * L + l;
         Kahan s;
         s.init();

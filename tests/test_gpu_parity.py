@@ -1,0 +1,398 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the same
+seeded inputs.  Oracle state (centroids, partitions, selections) is injected into the
+GPU, never the other way round.
+
+Tolerances:
+  k-means assignments           bit-exact given the same (fp32) centroids
+  summaries (count exact)       per-group relative L2 <= 1e-5 for mean, variance, value mean
+  selection                     identical except where the score gap to the cut-off < 1e-4
+  outputs (same selection)      per-head relative L2 <= 1e-3
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import oracle as ora
+import serving_mog_decode_gb300 as mog
+from serving_mog_decode_gb300 import buildlib
+from serving_mog_decode_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+D = 128
+DEV = torch.device("cuda:0")
+TIE = 1e-4
+OUT_TOL = 1e-3
+STAT_TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    buildlib.build()
+    ora.build()
+    mog.lib()
+
+
+def bf(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+def rel(a, b):
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def small_workload(n, centres=64, **kw):
+    base = dict(batch=1, h_kv=1, h_q=1, n=n, centres=centres, n_clusters=16, n_sub=6, top_c=4,
+                top_s=3, n_sink=4, n_recent=32, seed=11)
+    base.update(kw)
+    return wl.Workload("test", **base)
+
+
+# --------------------------------------------------------------------------- dense
+
+@pytest.mark.parametrize("lens,G", [((1300, 777), 4), ((64,), 1), ((200, 5000, 1), 5)])
+def test_dense_decode_matches_oracle(lens, G):
+    B, Hkv = len(lens), 2
+    w = small_workload(max(lens), batch=B, h_kv=Hkv, h_q=Hkv * G)
+    n_cap = max(lens) + 3
+    K = np.zeros((B, Hkv, n_cap, D), np.uint16)
+    V = np.zeros_like(K)
+    q = np.zeros((B, Hkv * G, D), np.uint16)
+    for b in range(B):
+        for h in range(Hkv):
+            u = wl.UnitDraw(w, b, h, lens[b])
+            u.keys_values(K[b, h], V[b, h])
+            q[b, h * G:(h + 1) * G] = u.q
+    ld = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    out = mog.dense_decode(bf(K), bf(V), ld, max(lens), bf(q)).cpu().numpy()
+    for b in range(B):
+        for hq in range(Hkv * G):
+            ref = ora.dense(K[b, hq // G], V[b, hq // G], lens[b], q[b, hq])
+            assert rel(out[b, hq], ref) < OUT_TOL, (b, hq)
+
+
+# --------------------------------------------------------------------------- k-means
+
+def _assign_steps(Kmid, k, T):
+    _, _, steps, hist = ora.lloyd(Kmid, k, T, history=True)
+    x = bf(Kmid)
+    total_fb = 0
+    for t in range(steps):
+        c32 = hist[t].astype(np.float32)
+        gpu, fb = mog.kmeans_assign(x, torch.from_numpy(c32).to(DEV))
+        ref = ora.assign(Kmid, c32.astype(np.float64))
+        assert np.array_equal(gpu.cpu().numpy(), ref), f"step {t}"
+        total_fb += fb
+    return steps, total_fb
+
+
+def test_l1_assign_bit_exact_tiny():
+    w = wl.WORKLOADS["tiny-4k"]
+    K, _, _ = wl.make_unit(w)
+    mid = K[w.n_sink:w.n - w.n_recent]
+    steps, fb = _assign_steps(mid, w.n_clusters, 10)
+    assert steps >= 3
+    print(f"tiny: {steps} steps, {fb} rows decided by the fp64 fallback")
+
+
+def test_l1_assign_bit_exact_with_ties_and_ragged_tail():
+    g = np.random.default_rng(5)
+    base = g.standard_normal((40, D))
+    X = wl.to_bf16(np.repeat(base, 3, axis=0)[:117])          # exact duplicate rows, ragged
+    cent = np.concatenate([base[:10], base[:10], g.standard_normal((13, D))]).astype(np.float32)
+    gpu, fb = mog.kmeans_assign(bf(X), torch.from_numpy(cent).to(DEV))
+    ref = ora.assign(X, cent.astype(np.float64))
+    assert np.array_equal(gpu.cpu().numpy(), ref)
+    assert fb > 0       # duplicated centroids tie exactly and must go to the fp64 rule
+
+
+def test_l1_assign_bit_exact_qwen3_4b_unit():
+    """A full 32K-key KV head of the Qwen3-4B-shaped workload (181 centroids)."""
+    w = wl.WORKLOADS["qwen3-4b-32k"]
+    K, _, _ = wl.make_unit(w, 0, 3)
+    mid = K[w.n_sink:w.n - w.n_recent]
+    _assign_steps(mid, w.n_clusters, 2)
+
+
+def test_l2_segmented_assign_bit_exact():
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, _ = wl.make_unit(w)
+    b = ora.build_unit(K, V, w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    perm, off, L = b["perm"], b["sub_off"], w.n_sub
+    rows, seg, cents = [], [0], []
+    for c in range(w.n_clusters):
+        mem = np.sort(perm[off[c * L]:off[(c + 1) * L]])
+        if mem.size == 0:
+            continue
+        _, _, st, hist = ora.lloyd(K, L, 4, rows=mem, history=True)
+        for t in range(st):
+            rows.append(mem)
+            seg.append(seg[-1] + mem.size)
+            cents.append(hist[t].astype(np.float32))
+    rows = np.concatenate(rows).astype(np.int32)
+    cents = np.stack(cents)
+    gpu = mog.kmeans_assign_segments(bf(K), torch.from_numpy(rows).to(DEV),
+                                     torch.tensor(seg, dtype=torch.int32, device=DEV),
+                                     torch.from_numpy(cents).to(DEV)).cpu().numpy()
+    for s in range(len(seg) - 1):
+        ref = ora.assign(K, cents[s].astype(np.float64), rows=rows[seg[s]:seg[s + 1]])
+        assert np.array_equal(gpu[seg[s]:seg[s + 1]], ref), s
+
+
+# ---------------------------------------------------------------- injected partitions
+
+class Injected:
+    """A batch whose (cluster, subcluster) partition is given: the oracle's own build of
+    each unit (small cases) or a rule applied to positions (large cases)."""
+
+    def __init__(self, w, lens=None, mode="oracle", n_cap=None):
+        self.w = w
+        lens = wl.lengths(w) if lens is None else np.asarray(lens, np.int32)
+        self.lens = lens
+        self.n_cap = int(lens.max()) if n_cap is None else n_cap
+        B, Hkv, G = w.batch, w.h_kv, w.group
+        self.K = np.zeros((B, Hkv, self.n_cap, D), np.uint16)
+        self.V = np.zeros_like(self.K)
+        self.q = np.zeros((B, Hkv * G, D), np.uint16)
+        self.summ = {}
+        self.prm = mog.make_params(B, Hkv, Hkv * G, self.n_cap, n_clusters=w.n_clusters,
+                                   n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink,
+                                   n_recent=w.n_recent)
+        stride = mog.sub_off_stride(self.prm, lens)
+        perm_all = np.zeros((B * Hkv, self.n_cap), np.int32)
+        off_all = np.zeros((B * Hkv, stride), np.int32)
+        for b in range(B):
+            n = int(lens[b])
+            Cn, L = wl.clusters_for(w, n)
+            for h in range(Hkv):
+                u = wl.UnitDraw(w, b, h, n)
+                u.keys_values(self.K[b, h], self.V[b, h])
+                self.q[b, h * G:(h + 1) * G] = u.q
+                S, R = w.n_sink, w.n_recent
+                if mode == "oracle":
+                    s = ora.build_unit(self.K[b, h], self.V[b, h], n, S, R, Cn, L)
+                else:   # clusters by planted centre, subclusters by position
+                    nm = max(0, n - S - R)
+                    pos = np.arange(S, S + nm)
+                    lab = (u.z[pos] % Cn) * L + (pos % L)
+                    order = np.argsort(lab, kind="stable")
+                    perm = pos[order].astype(np.int32)
+                    sub_off = np.searchsorted(lab[order], np.arange(Cn * L + 1)).astype(np.int32)
+                    s = ora.stats(self.K[b, h], self.V[b, h], perm, sub_off, Cn, L)
+                    s.update(perm=perm, sub_off=sub_off, C=Cn, L=L, n_build=n, S=S, R=R)
+                self.summ[(b, h)] = s
+                perm_all[b * Hkv + h, :s["perm"].size] = s["perm"]
+                off_all[b * Hkv + h, :Cn * L + 1] = s["sub_off"]
+        self.h = mog.build(bf(self.K), bf(self.V), lens, self.prm,
+                           partition=(torch.from_numpy(perm_all).to(DEV),
+                                      torch.from_numpy(off_all).to(DEV)))
+        self.qd = bf(self.q)
+
+    def gpu_summaries(self):
+        lay = self.h.layout()
+        U, cm, lm = lay.units, lay.c_max, lay.l_max
+        return dict(
+            cl_n=self.h.array("cl_n", torch.int32, (U, cm)).cpu().numpy(),
+            cl_ms=self.h.array("cl_ms", torch.float32, (U, cm, 2, D)).cpu().numpy(),
+            cl_vbar=self.h.array("cl_vbar", torch.float32, (U, cm, D)).cpu().numpy(),
+            sub_n=self.h.array("sub_n", torch.int32, (U, cm * lm)).cpu().numpy(),
+            sub_ms=self.h.array("sub_ms", torch.float32, (U, cm * lm, 2, D)).cpu().numpy(),
+            sub_vbar=self.h.array("sub_vbar", torch.float32, (U, cm * lm, D)).cpu().numpy())
+
+
+def _check_stats(inj):
+    g = inj.gpu_summaries()
+    worst = 0.0
+    for (b, h), s in inj.summ.items():
+        u = b * inj.w.h_kv + h
+        Cn, L = s["C"], s["L"]
+        assert np.array_equal(g["cl_n"][u, :Cn], s["cl_n"])
+        assert np.array_equal(g["sub_n"][u, :Cn * L], s["sub_n"])
+        for name, gpu, ref, n in (("mu", g["cl_ms"][u, :Cn, 0], s["cl_mu"], s["cl_n"]),
+                                  ("var", g["cl_ms"][u, :Cn, 1], s["cl_var"], s["cl_n"]),
+                                  ("vbar", g["cl_vbar"][u, :Cn], s["cl_vbar"], s["cl_n"]),
+                                  ("smu", g["sub_ms"][u, :Cn * L, 0], s["sub_mu"], s["sub_n"]),
+                                  ("svar", g["sub_ms"][u, :Cn * L, 1], s["sub_var"], s["sub_n"]),
+                                  ("svbar", g["sub_vbar"][u, :Cn * L], s["sub_vbar"], s["sub_n"])):
+            for i in np.nonzero(n > 0)[0]:
+                nr = np.linalg.norm(ref[i])
+                err = np.linalg.norm(gpu[i] - ref[i]) / nr if nr > 0 else np.abs(gpu[i]).max()
+                worst = max(worst, err)
+                assert err <= STAT_TOL, (name, u, i, err)
+    return worst
+
+
+def _check_decode(inj, n_now=None, sample_heads=None):
+    w, G = inj.w, inj.w.group
+    SW = w.top_c + w.top_c * w.top_s
+    U = w.batch * w.h_kv
+    sel_out = torch.full((U * G, max(SW, 1)), -7, dtype=torch.int32, device=DEV)
+    inj.h.decode(inj.qd, sel_out=sel_out)
+    gsel = sel_out.cpu().numpy()
+    ties = 0
+    sel_ref = np.full((U * G, max(SW, 1)), -1, np.int32)
+    heads = range(U * G) if sample_heads is None else sample_heads
+    for hq in heads:
+        u, g = hq // G, hq % G
+        b, h = u // w.h_kv, u % w.h_kv
+        s = inj.summ[(b, h)]
+        sc, ss, cs, sscore = ora.select(inj.q[b, h * G + g], s, w.top_c, w.top_s)
+        sel_ref[hq, :w.top_c] = sc
+        sel_ref[hq, w.top_c:SW] = ss.reshape(-1)
+        gc = gsel[hq, :w.top_c]
+        if not np.array_equal(gc, sc):
+            cut = cs[sc[sc >= 0]].min() if (sc >= 0).any() else -np.inf
+            for c in set(gc.tolist()) ^ set(sc.tolist()):
+                assert c >= 0 and abs(cs[c] - cut) < TIE, ("cluster selection", hq, c)
+            ties += 1
+            continue
+        gs = gsel[hq, w.top_c:SW].reshape(w.top_c, w.top_s)
+        for i in range(w.top_c):
+            if not np.array_equal(gs[i], ss[i]):
+                cut = sscore[i][ss[i][ss[i] >= 0]].min()
+                for l in set(gs[i].tolist()) ^ set(ss[i].tolist()):
+                    assert l >= 0 and abs(sscore[i][l] - cut) < TIE, ("sub selection", hq, i, l)
+                ties += 1
+    # outputs under the oracle's selection
+    sin = torch.from_numpy(sel_ref).to(DEV)
+    out = inj.h.decode(inj.qd, sel_in=sin).cpu().numpy().reshape(U * G, D)
+    worst = 0.0
+    for hq in heads:
+        u, g = hq // G, hq % G
+        b, h = u // w.h_kv, u % w.h_kv
+        s = inj.summ[(b, h)]
+        nn = int(inj.lens[b]) if n_now is None else n_now[b]
+        ref, _ = ora.decode(inj.K[b, h], inj.V[b, h], nn, inj.q[b, h * G + g], s,
+                            sel_ref[hq, :w.top_c], sel_ref[hq, w.top_c:SW].reshape(w.top_c, w.top_s))
+        e = rel(out[hq], ref)
+        worst = max(worst, e)
+        assert e <= OUT_TOL, (hq, e)
+    assert inj.h.sync_status() == 0
+    return ties, worst
+
+
+def test_stats_and_decode_tiny_oracle_partition():
+    inj = Injected(wl.WORKLOADS["tiny-4k"])
+    print("stats worst", _check_stats(inj), "decode", _check_decode(inj))
+
+
+def test_stats_and_decode_gqa_ragged():
+    w = small_workload(0, batch=2, h_kv=2, h_q=8, centres=48, n_clusters=0, n_sub=0, top_c=3,
+                       top_s=2, n_recent=40, n_range=(2500, 3100), seed=21)
+    inj = Injected(w)
+    assert len(set(inj.lens.tolist())) == 2
+    _check_stats(inj)
+    _check_decode(inj)
+
+
+@pytest.mark.parametrize("tc,ts", [(0, 0), (16, 0), (16, 6), (1, 1), (5, 6)])
+def test_decode_selection_extremes(tc, ts):
+    w = small_workload(3000, h_kv=2, h_q=10, top_c=tc, top_s=ts, seed=31)
+    inj = Injected(w)
+    _check_decode(inj)
+
+
+def test_full_size_qwen3_4b_injected_partition():
+    """The benchmark's workload (8 KV heads x 32K keys, 181 x 15 groups) with a
+    position-rule partition: statistics and the whole decode step against the oracle."""
+    w = wl.WORKLOADS["qwen3-4b-32k"]
+    inj = Injected(w, mode="rule")
+    _check_stats(inj)
+    ties, worst = _check_decode(inj)
+    print(f"qwen3-4b-32k: {ties} near-tie heads, worst rel-L2 {worst:.2e}")
+
+
+# ------------------------------------------------------------------ whole pipeline
+
+def _gpu_build(w, lens=None, n_cap=None, **over):
+    lens = wl.lengths(w) if lens is None else np.asarray(lens, np.int32)
+    K, V, q, _ = wl.make_batch(w, n_cap=n_cap)
+    kw = dict(n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s,
+              n_sink=w.n_sink, n_recent=w.n_recent)
+    kw.update(over)
+    prm = mog.make_params(w.batch, w.h_kv, w.h_q, K.shape[2], **kw)
+    Kd, Vd = bf(K), bf(V)
+    h = mog.build(Kd, Vd, lens, prm)
+    return h, K, V, q, lens, Kd, Vd
+
+
+def _partition(h, u, lens_b, w):
+    lay = h.layout()
+    info = h.array("unit_info", torch.int32, (lay.units, 8)).cpu().numpy()[u]
+    Cn, L, nm, S = info[0], info[1], info[3], info[4]
+    perm = h.array("perm", torch.int32, (lay.units, lay.n_cap)).cpu().numpy()[u, :nm]
+    off = h.array("sub_off", torch.int32, (lay.units, lay.sub_off_stride)).cpu().numpy()[u, :Cn * L + 1]
+    return Cn, L, nm, S, perm, off
+
+
+def test_build_partition_properties_and_identities():
+    w = wl.WORKLOADS["tiny-4k"]
+    h, K, V, q, lens, _, _ = _gpu_build(w)
+    Cn, L, nm, S, perm, off = _partition(h, 0, lens[0], w)
+    assert np.array_equal(np.sort(perm), np.arange(S, S + nm))
+    assert off[0] == 0 and off[-1] == nm and np.all(np.diff(off) >= 0)
+    for g in range(Cn * L):
+        assert np.all(np.diff(perm[off[g]:off[g + 1]]) > 0)
+    g = Injected.gpu_summaries(type("X", (), {"h": h})())
+    X = wl.from_bf16(K[0, 0]).astype(np.float64)
+    for c in range(Cn):
+        sl = slice(c * L, (c + 1) * L)
+        ns = g["sub_n"][0, sl].astype(np.float64)
+        assert g["cl_n"][0, c] == ns.sum() == off[(c + 1) * L] - off[c * L]
+        if ns.sum() == 0:
+            continue
+        mem = perm[off[c * L]:off[(c + 1) * L]]
+        np.testing.assert_allclose(g["cl_ms"][0, c, 0], X[mem].mean(0), rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(g["cl_ms"][0, c, 1], X[mem].var(0), rtol=1e-4, atol=1e-5)
+        within = (ns[:, None] * g["sub_ms"][0, sl, 1]).sum(0) / ns.sum()
+        between = (ns[:, None] * (g["sub_ms"][0, sl, 0] - g["cl_ms"][0, c, 0]) ** 2).sum(0) / ns.sum()
+        np.testing.assert_allclose(g["cl_ms"][0, c, 1], within + between, rtol=1e-4, atol=1e-5)
+
+
+def test_full_pipeline_approximation_error_close_to_oracle():
+    w = wl.WORKLOADS["tiny-4k"]
+    h, K, V, q, lens, _, _ = _gpu_build(w)
+    out = h.decode(bf(q)).cpu().numpy()[0, 0]
+    ref = ora.dense(K[0, 0], V[0, 0], w.n, q[0, 0])
+    ob = ora.build_unit(K[0, 0], V[0, 0], w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    om, _, _, _ = ora.mog_head(K[0, 0], V[0, 0], w.n, q[0, 0], ob, w.top_c, w.top_s)
+    top, _, _, _ = ora.mog_head(K[0, 0], V[0, 0], w.n, q[0, 0], ob, w.top_c, w.top_s, residual=False)
+    e_gpu, e_ora, e_top = rel(out, ref), rel(om, ref), rel(top, ref)
+    print(f"MoG vs dense: gpu {e_gpu:.3e} oracle {e_ora:.3e} (top-only {e_top:.3e})")
+    assert e_gpu < max(1.5 * e_ora, e_ora + 0.01)
+
+
+@pytest.mark.parametrize("name", ["tiny-4k", "qwen3-4b-32k"])
+def test_all_groups_selected_equals_dense(name):
+    w = wl.WORKLOADS[name]
+    h, K, V, q, lens, Kd, Vd = _gpu_build(w, top_c=w.n_clusters, top_s=w.n_sub)
+    out = h.decode(bf(q)).cpu().numpy()
+    G = w.group
+    for hq in range(0, w.h_q, max(1, w.h_q // 8)):
+        ref = ora.dense(K[0, hq // G], V[0, hq // G], w.n, q[0, hq])
+        assert rel(out[0, hq], ref) < OUT_TOL, hq
+    assert h.sync_status() == 0
+
+
+def test_append_joins_recent_anchors():
+    w = small_workload(3000, h_kv=2, h_q=8, seed=41)
+    steps = 5
+    h, K, V, q, lens, Kd, Vd = _gpu_build(w, n_cap=3000 + steps, top_c=w.n_clusters, top_s=w.n_sub)
+    rng = np.random.default_rng(3)
+    for t in range(steps):
+        kn = wl.to_bf16(rng.standard_normal((1, 2, D)))
+        vn = wl.to_bf16(rng.standard_normal((1, 2, D)))
+        h.append(bf(kn), bf(vn))
+        K[0, :, 3000 + t] = kn[0]
+        V[0, :, 3000 + t] = vn[0]
+    out = h.decode(bf(q)).cpu().numpy()
+    assert np.array_equal(Kd.view(torch.int16).cpu().numpy().view(np.uint16), K)
+    for hq in range(8):
+        ref = ora.dense(K[0, hq // 4], V[0, hq // 4], 3000 + steps, q[0, hq])
+        assert rel(out[0, hq], ref) < OUT_TOL
+    with pytest.raises(mog.MogError, match="CAPACITY"):
+        h.append(bf(kn), bf(vn))
