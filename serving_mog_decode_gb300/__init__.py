@@ -183,6 +183,9 @@ class Handle:
 
     def decode_phased(self, q, out, events, sel_out=None, stream=None):
         """Decode with four torch.cuda.Event objects recorded around the three kernels."""
+        for e in events:       # torch creates the CUDA event on first record
+            if not e.cuda_event:
+                e.record()
         arr = (C.c_void_p * 4)(*[e.cuda_event for e in events])
         _check(lib().mog_decode_phased(self._h, _ptr(q), _ptr(out), None, _ptr(sel_out), arr,
                                        _stream(stream)), "mog_decode_phased")
