@@ -37,6 +37,8 @@ from serving_mog_decode_gb300 import workloads as wl  # noqa: E402
 METRIC = "MoG decode us/step/layer at 32K-1M ctx; achieved HBM GB/s vs roofline"
 D = 128
 FLUSH_BYTES = 256 << 20
+CUSHION_CYCLES = 200_000   # GPU-side spin before each timed step (~0.1 ms): the host
+                           # finishes enqueueing the step before the start event is reached
 
 
 def args_():
@@ -112,7 +114,7 @@ class Clocks:
         sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
@@ -251,6 +253,7 @@ def run_gpu(a, w, rank, world):
     dense_ms = []
     for i in range(3 + 10):
         flush.zero_()
+        torch.cuda._sleep(CUSHION_CYCLES)
         s0, s1 = ev(), ev()
         s0.record()
         mog.dense_decode(Kd, Vd, h.lengths_dev, int(lens.max()), qd, dense_out, dscratch)
@@ -270,6 +273,7 @@ def run_gpu(a, w, rank, world):
     torch.cuda.synchronize()
     for i in range(a.steps):
         flush.zero_()
+        torch.cuda._sleep(CUSHION_CYCLES)
         starts[i].record()
         h.decode(qd, out)
         ends[i].record()
@@ -281,6 +285,7 @@ def run_gpu(a, w, rank, world):
     phase = [[], [], []]
     for i in range(max(20, min(a.steps, 200))):
         flush.zero_()
+        torch.cuda._sleep(CUSHION_CYCLES)
         evs = [ev() for _ in range(4)]
         h.decode_phased(qd, out, evs)
         torch.cuda.synchronize()

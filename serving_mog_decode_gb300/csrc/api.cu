@@ -6,6 +6,9 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
+#include <set>
+#include <tuple>
 #include <vector>
 
 #include "common.cuh"
@@ -45,6 +48,20 @@ int num_sms() {
         return 152;
     }
     return n;
+}
+
+cudaError_t ensure_smem(const void *fn, size_t bytes) {
+    static std::mutex mu;
+    static std::set<std::tuple<const void *, int, size_t>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_tuple(fn, dev, bytes);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
 }
 
 static int isqrt_round(int64_t n) {
@@ -155,6 +172,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_ucount = take(4 * U);
     P.o_sel = take(4 * U * G * std::max<int64_t>(SW, 1));
     P.o_slotcnt = take(4 * U * MOG_MAX_UNION);
+    P.o_slotcoff = take(4 * U * MOG_MAX_UNION);
     P.o_rowpos = take(4 * U * nc);
     P.o_counters = take(4 * U * 4);
     P.o_cand_s = take(4 * U * P.P1 * G * tcc);
@@ -227,6 +245,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     PTR(ucount, int);
     PTR(sel, int);
     PTR(slotcnt, int);
+    PTR(slotcoff, int);
     PTR(rowpos, int);
     PTR(counters, unsigned);
     PTR(cand_s, float);

@@ -177,8 +177,10 @@ __device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[
     }
 }
 
-// Partial result layout: per head, [0] = m (log2 domain), [1] = l, [2..2+d) = acc.
-constexpr int PART_W = MOG_D + 2;
+// Partial result layout: per head, [0] = m (log2 domain), [1] = l, [2], [3] unused,
+// [4 .. 4+d) = acc; 528 bytes, so that every partial is a whole number of 16-byte chunks.
+constexpr int PART_W = MOG_D + 4;
+constexpr int PART_ACC = 4;
 
 // Write this warp's state for heads < G into st[w][g][PART_W] (shared memory).
 __device__ __forceinline__ void warp_state_out(const WarpAcc &acc, float *st, int G) {
@@ -198,8 +200,8 @@ __device__ __forceinline__ void warp_state_out(const WarpAcc &acc, float *st, in
         }
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-            r[2 + t * 8 + c] = acc.o[t][0];
-            r[2 + t * 8 + c + 1] = acc.o[t][1];
+            r[PART_ACC + t * 8 + c] = acc.o[t][0];
+            r[PART_ACC + t * 8 + c + 1] = acc.o[t][1];
         }
     }
     if (h1 < G) {
@@ -210,32 +212,27 @@ __device__ __forceinline__ void warp_state_out(const WarpAcc &acc, float *st, in
         }
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-            r[2 + t * 8 + c] = acc.o[t][2];
-            r[2 + t * 8 + c + 1] = acc.o[t][3];
+            r[PART_ACC + t * 8 + c] = acc.o[t][2];
+            r[PART_ACC + t * 8 + c + 1] = acc.o[t][3];
         }
     }
 }
 
-// Merge n states st[i][g][PART_W] (stride per state = G*PART_W floats) into dst[g][PART_W].
-// Called by all threads of the CTA; shared or global sources.
-__device__ __forceinline__ void merge_states(const float *st, int n, int G, float *dst,
-                                             bool cg_loads) {
+// Merge n states st[i][g][PART_W] held in shared memory (stride per state G*PART_W
+// floats) into dst[g][PART_W] (shared or global).  Called by all threads of the CTA.
+__device__ __forceinline__ void merge_states(const float *st, int n, int G, float *dst) {
     for (int e = threadIdx.x; e < G * MOG_D; e += blockDim.x) {
         const int g = e / MOG_D, j = e % MOG_D;
         float m = -INFINITY;
-        for (int i = 0; i < n; ++i) {
-            const float *r = st + ((size_t)i * G + g) * PART_W;
-            m = fmaxf(m, cg_loads ? __ldcg(r) : r[0]);
-        }
+        for (int i = 0; i < n; ++i) m = fmaxf(m, st[((size_t)i * G + g) * PART_W]);
         float l = 0.f, a = 0.f;
         if (m != -INFINITY) {
             for (int i = 0; i < n; ++i) {
                 const float *r = st + ((size_t)i * G + g) * PART_W;
-                const float mi = cg_loads ? __ldcg(r) : r[0];
-                if (mi == -INFINITY) continue;
-                const float sc = exp2f(mi - m);
-                l += sc * (cg_loads ? __ldcg(r + 1) : r[1]);
-                a += sc * (cg_loads ? __ldcg(r + 2 + j) : r[2 + j]);
+                if (r[0] == -INFINITY) continue;
+                const float sc = exp2f(r[0] - m);
+                l += sc * r[1];
+                a += sc * r[PART_ACC + j];
             }
         }
         float *o = dst + (size_t)g * PART_W;
@@ -243,7 +240,71 @@ __device__ __forceinline__ void merge_states(const float *st, int n, int G, floa
             o[0] = m;
             o[1] = l;
         }
-        o[2 + j] = a;
+        o[PART_ACC + j] = a;
+    }
+}
+
+// Merge n partials part[i][g][PART_W] from global memory and write the normalised
+// result out[g][d] (= acc / l).  The partials are staged into shared memory `sm`
+// (sm_floats floats, >= G*PART_W + G*(n_chunk+2)) with cp.async, all copies of a chunk in
+// flight at once, and folded into a running (max, sum, acc) per head.
+__device__ __forceinline__ void merge_global_out(const float *part, int n, int G, float *sm,
+                                                 int sm_floats, float *out) {
+    const int per = G * PART_W;
+    int ch = (sm_floats - 3 * MOG_MAX_G) / (per + G);
+    ch = ch < 1 ? 1 : ch;
+    float *stage = sm;                        // [ch][G][PART_W]
+    float *sS = stage + (size_t)ch * per;     // [ch][G] per-partial scales
+    float *sM = sS + (size_t)ch * G;          // [G] running max
+    float *sL = sM + MOG_MAX_G;               // [G] running sum
+    float *sA = sL + MOG_MAX_G;               // [G] rescale of the running acc
+    if (threadIdx.x < (unsigned)G) {
+        sM[threadIdx.x] = -INFINITY;
+        sL[threadIdx.x] = 0.f;
+    }
+    float acc[MOG_MAX_G * MOG_D / 128];  // elements e = tid + k*blockDim, blockDim >= 128
+    const int ept = (G * MOG_D + blockDim.x - 1) / blockDim.x;
+    for (int k = 0; k < ept; ++k) acc[k] = 0.f;
+    for (int c0 = 0; c0 < n; c0 += ch) {
+        const int cnt = min(ch, n - c0);
+        const int q4 = cnt * per / 4;
+        const float *src = part + (size_t)c0 * per;
+        for (int q = threadIdx.x; q < q4; q += blockDim.x) cp_async16(smem_u32(stage + 4 * q), src + 4 * q, 16);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        if (threadIdx.x < (unsigned)G) {
+            const int g = threadIdx.x;
+            float mn = sM[g];
+            for (int i = 0; i < cnt; ++i) mn = fmaxf(mn, stage[(size_t)i * per + g * PART_W]);
+            float lsum = 0.f;
+            for (int i = 0; i < cnt; ++i) {
+                const float mi = stage[(size_t)i * per + g * PART_W];
+                const float sc = (mi == -INFINITY) ? 0.f : exp2f(mi - mn);
+                sS[i * G + g] = sc;
+                lsum += sc * stage[(size_t)i * per + g * PART_W + 1];
+            }
+            const float so = (sM[g] == -INFINITY) ? 0.f : exp2f(sM[g] - mn);
+            sA[g] = so;
+            sL[g] = sL[g] * so + lsum;
+            sM[g] = mn;
+        }
+        __syncthreads();
+        for (int k = 0; k < ept; ++k) {
+            const int e = threadIdx.x + k * blockDim.x;
+            if (e >= G * MOG_D) break;
+            const int g = e / MOG_D, j = e % MOG_D;
+            float a = acc[k] * sA[g];
+            for (int i = 0; i < cnt; ++i) a += sS[i * G + g] * stage[(size_t)i * per + g * PART_W + PART_ACC + j];
+            acc[k] = a;
+        }
+        __syncthreads();
+    }
+    for (int k = 0; k < ept; ++k) {
+        const int e = threadIdx.x + k * blockDim.x;
+        if (e >= G * MOG_D) break;
+        const int g = e / MOG_D;
+        out[e] = sL[g] > 0.f ? acc[k] / sL[g] : 0.f;
     }
 }
 

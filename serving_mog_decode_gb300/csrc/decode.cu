@@ -81,6 +81,11 @@ __device__ __forceinline__ void warp_best(float &v, int &i) {
 
 constexpr int SC_THREADS = 256;
 constexpr int SC_SLICE = 64;  // clusters per score CTA at most (two per lane)
+constexpr int SC_PER_WARP = SC_SLICE / (SC_THREADS / 32);
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
+}
 
 __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     extern __shared__ __align__(16) float scs[];
@@ -99,22 +104,45 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     const int C = ui[UI_C];
     const int c0 = (int)((int64_t)C * p / dv.P1), c1 = (int)((int64_t)C * (p + 1) / dv.P1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // summaries of this warp's clusters, loaded before the weights are ready
+    float4 mu[SC_PER_WARP], va[SC_PER_WARP];
+    int nn[SC_PER_WARP];
+#pragma unroll
+    for (int k = 0; k < SC_PER_WARP; ++k) {
+        const int c = c0 + warp + 8 * k;
+        nn[k] = 0;
+        if (c < c1) {
+            const float *ms = dv.cl_ms + ((size_t)u * dv.c_max + c) * 2 * MOG_D;
+            mu[k] = *reinterpret_cast<const float4 *>(ms + lane * 4);
+            va[k] = *reinterpret_cast<const float4 *>(ms + MOG_D + lane * 4);
+            nn[k] = dv.cl_n[(size_t)u * dv.c_max + c];
+        }
+    }
     load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
     __syncthreads();
-    float res[MOG_MAX_G], sl[MOG_MAX_G];
     float *cres = dv.cscore + (size_t)u * 2 * G * dv.c_max;  // [0][g][c] selection, [1][g][c] residual
-    for (int c = c0 + warp; c < c1; c += SC_THREADS / 32) {
-        const int n = dv.cl_n[(size_t)u * dv.c_max + c];
-        group_scores(dv.cl_ms + ((size_t)u * dv.c_max + c) * 2 * MOG_D, n, w, G, dv.score_mode,
-                     res, sl);
-        if (lane == 0) {
-            for (int g = 0; g < G; ++g) {
-                cres[(size_t)g * dv.c_max + c] = sl[g];
-                cres[((size_t)G + g) * dv.c_max + c] = res[g];
-                ssel[g * SC_SLICE + (c - c0)] = sl[g];
+#pragma unroll
+    for (int k = 0; k < SC_PER_WARP; ++k) {
+        const int c = c0 + warp + 8 * k;
+        if (c >= c1) break;
+        const int n = nn[k];
+        const float ln = n > 0 ? logf((float)n) : 0.f;
+        for (int g = 0; g < G; ++g) {
+            const float4 wm = *reinterpret_cast<const float4 *>(w + g * 2 * MOG_D + lane * 4);
+            const float4 wv = *reinterpret_cast<const float4 *>(w + g * 2 * MOG_D + MOG_D + lane * 4);
+            float dm = wm.x * mu[k].x + wm.y * mu[k].y + wm.z * mu[k].z + wm.w * mu[k].w;
+            float dq = wv.x * va[k].x + wv.y * va[k].y + wv.z * va[k].z + wv.w * va[k].w;
+            dm = warp_sum(dm);
+            dq = warp_sum(dq);
+            const float r = n > 0 ? ln + dm + dq : -INFINITY;
+            const float sl = dv.score_mode == 0 ? r : (n > 0 ? dm : -INFINITY);
+            if (lane == 0) {
+                cres[(size_t)g * dv.c_max + c] = sl;
+                cres[((size_t)G + g) * dv.c_max + c] = r;
+                ssel[g * SC_SLICE + (c - c0)] = sl;
             }
-            dv.cselmask[(size_t)u * dv.c_max + c] = 0u;
         }
+        if (lane == 0) dv.cselmask[(size_t)u * dv.c_max + c] = 0u;
     }
     __syncthreads();
     // local top-tc of this slice, per head
@@ -122,8 +150,8 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     for (int g = warp; g < G && tc > 0; g += SC_THREADS / 32) {
         float v0 = lane < ns ? ssel[g * SC_SLICE + lane] : -INFINITY;
         float v1 = lane + 32 < ns ? ssel[g * SC_SLICE + lane + 32] : -INFINITY;
-        float *cs = a.cand_s + (((size_t)u * dv.P1 + p) * G + g) * tc;
-        int *ci = a.cand_i + (((size_t)u * dv.P1 + p) * G + g) * tc;
+        float *cs = a.cand_s + (((size_t)u * G + g) * dv.P1 + p) * tc;
+        int *ci = a.cand_i + (((size_t)u * G + g) * dv.P1 + p) * tc;
         for (int r = 0; r < tc; ++r) {
             float bv;
             int bi;
@@ -160,7 +188,7 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     if (!s_last) return;
     __threadfence();
     if (threadIdx.x == 0) dv.counters[u * 4 + 0] = 0u;
-    // ---- last CTA of the unit: merge the candidate lists (sorted, P1 of them) ----
+    // ---- last CTA of the unit: merge the P1 sorted candidate lists of every head ----
     int *sel = dv.sel + (size_t)u * G * a.SW;
     const int ncand = dv.P1 * tc;
     for (int g = warp; g < G; g += SC_THREADS / 32) {
@@ -177,12 +205,13 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
         } else {
             float *ss = stg_s + warp * ncand;
             int *sx = stg_i + warp * ncand;
+            const size_t base = ((size_t)u * G + g) * ncand;
             for (int e = lane; e < ncand; e += 32) {
-                const int pp = e / tc, r = e % tc;
-                const size_t off = (((size_t)u * dv.P1 + pp) * G + g) * tc + r;
-                ss[e] = __ldcg(a.cand_s + off);
-                sx[e] = __ldcg(a.cand_i + off);
+                cp_async4(smem_u32(ss + e), a.cand_s + base + e);
+                cp_async4(smem_u32(sx + e), a.cand_i + base + e);
             }
+            cp_async_commit();
+            cp_async_wait<0>();
             __syncwarp();
             // lane k walks lists k and k+32
             int p0 = 0, p1 = 0;
@@ -203,8 +232,8 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
                 warp_best(bv, bi);
                 if (bv == -INFINITY) break;
                 if (lane == 0) sg[r] = bi;
-                if (!takeb && ia == bi && va == bv) ++p0;
-                else if (takeb && ib == bi && vb == bv) ++p1;
+                if (!takeb && ia == bi) ++p0;
+                else if (takeb && ib == bi) ++p1;
             }
         }
         __syncwarp();
@@ -252,6 +281,8 @@ __global__ void __launch_bounds__(SUB_THREADS) k_dec_sub(DecArgs a) {
     float *ssel = sres + G * MOG_MAX_L;    // [G][32]
     __shared__ uint32_t smask[MOG_MAX_L];
     __shared__ int spref[MOG_MAX_L + 1];
+    __shared__ int sso[MOG_MAX_L + 1];
+    __shared__ int snn[MOG_MAX_L];
     pdl_wait();
     pdl_trigger();
     const int u = blockIdx.y, j = blockIdx.x;
@@ -261,14 +292,16 @@ __global__ void __launch_bounds__(SUB_THREADS) k_dec_sub(DecArgs a) {
     const int c = dv.ucl[(size_t)u * MOG_MAX_UNION + j];
     const uint32_t hm = dv.uhm[(size_t)u * MOG_MAX_UNION + j];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
-    if (threadIdx.x < MOG_MAX_L) smask[threadIdx.x] = 0u;
-    __syncthreads();
+    const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
     const size_t g0 = (size_t)u * dv.c_max * dv.l_max + (size_t)c * L;
+    if (threadIdx.x <= (unsigned)L) sso[threadIdx.x] = so[threadIdx.x];
+    if (threadIdx.x < (unsigned)L) snn[threadIdx.x] = dv.sub_n[g0 + threadIdx.x];
+    if (threadIdx.x < MOG_MAX_L) smask[threadIdx.x] = 0u;
+    load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
+    __syncthreads();
     float res[MOG_MAX_G], sl[MOG_MAX_G];
     for (int l = warp; l < L; l += SUB_THREADS / 32) {
-        const int n = dv.sub_n[g0 + l];
-        group_scores(dv.sub_ms + (g0 + l) * 2 * MOG_D, n, w, G, dv.score_mode, res, sl);
+        group_scores(dv.sub_ms + (g0 + l) * 2 * MOG_D, snn[l], w, G, dv.score_mode, res, sl);
         if (lane == 0)
             for (int g = 0; g < G; ++g) {
                 sres[g * MOG_MAX_L + l] = res[g];
@@ -280,8 +313,7 @@ __global__ void __launch_bounds__(SUB_THREADS) k_dec_sub(DecArgs a) {
     for (int g = warp; g < G; g += SUB_THREADS / 32) {
         if (!((hm >> g) & 1u)) continue;
         int *sg = selu + (size_t)g * a.SW;
-        // rank of c in this head's cluster list
-        int rk = -1;
+        int rk = -1;  // rank of c in this head's cluster list
         for (int r0 = 0; r0 < dv.tc; r0 += 32) {
             const int r = r0 + lane;
             const uint32_t b = __ballot_sync(0xffffffffu, r < dv.tc && sg[r] == c);
@@ -296,7 +328,7 @@ __global__ void __launch_bounds__(SUB_THREADS) k_dec_sub(DecArgs a) {
             const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + dv.tc + rk * dv.ts;
             for (int r = lane; r < dv.ts; r += 32) {
                 const int l = si[r];
-                const bool ok = l >= 0 && l < L && dv.sub_n[g0 + l] > 0;
+                const bool ok = l >= 0 && l < L && snn[l] > 0;
                 subs[r] = ok ? l : -1;
                 if (ok) atomicOr(&smask[l], 1u << g);
             }
@@ -316,32 +348,29 @@ __global__ void __launch_bounds__(SUB_THREADS) k_dec_sub(DecArgs a) {
         }
     }
     __syncthreads();
-    const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride;
-    if (threadIdx.x < L) {
+    if (threadIdx.x < (unsigned)L) {
         const int l = threadIdx.x;
-        const int n = dv.sub_n[g0 + l];
-        dv.subres[((size_t)u * MOG_MAX_UNION + j) * MOG_MAX_L + l] = n > 0 ? (hm & ~smask[l]) : 0u;
+        dv.subres[((size_t)u * MOG_MAX_UNION + j) * MOG_MAX_L + l] = snn[l] > 0 ? (hm & ~smask[l]) : 0u;
         for (int g = 0; g < G; ++g)
             dv.subscore[(((size_t)u * MOG_MAX_UNION + j) * G + g) * MOG_MAX_L + l] = sres[g * MOG_MAX_L + l];
     }
     if (threadIdx.x == 0) {
         spref[0] = 0;
-        for (int l = 0; l < L; ++l)
-            spref[l + 1] = spref[l] + (smask[l] ? so[c * L + l + 1] - so[c * L + l] : 0);
+        for (int l = 0; l < L; ++l) spref[l + 1] = spref[l] + (smask[l] ? sso[l + 1] - sso[l] : 0);
         dv.slotcnt[(size_t)u * MOG_MAX_UNION + j] = spref[L];
+        dv.slotcoff[(size_t)u * MOG_MAX_UNION + j] = sso[0];
     }
     __syncthreads();
-    const int coff = so[c * L];
+    // compacted rows of the selected subclusters, one flat parallel pass
+    const int tot = spref[L];
     const int *perm = dv.perm + (size_t)u * dv.n_cap;
-    int *rp = dv.rowpos + (size_t)u * dv.n_cap + coff;
-    uint32_t *rm = dv.rowmask + (size_t)u * dv.n_cap + coff;
-    for (int l = 0; l < L; ++l) {
-        if (!smask[l]) continue;
-        const int lo = so[c * L + l], n = so[c * L + l + 1] - lo;
-        for (int i = threadIdx.x; i < n; i += SUB_THREADS) {
-            rp[spref[l] + i] = perm[lo + i];
-            rm[spref[l] + i] = smask[l];
-        }
+    int *rp = dv.rowpos + (size_t)u * dv.n_cap + sso[0];
+    uint32_t *rm = dv.rowmask + (size_t)u * dv.n_cap + sso[0];
+    for (int i = threadIdx.x; i < tot; i += SUB_THREADS) {
+        int l = 0;
+        while (spref[l + 1] <= i) ++l;
+        rp[i] = perm[sso[l] + (i - spref[l])];
+        rm[i] = smask[l];
     }
 }
 
@@ -354,9 +383,9 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     const int G = dv.G;
     __shared__ int spre[MOG_MAX_UNION + 1];
     __shared__ int scoff[MOG_MAX_UNION];
+    __shared__ int sucl[MOG_MAX_UNION];
     __shared__ int spos[SUPER];
     __shared__ uint32_t smk[SUPER];
-    __shared__ float smax[AT_WARPS][MOG_MAX_G];
     __shared__ int s_last;
     pdl_wait();
     pdl_trigger();
@@ -370,16 +399,16 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     const int Uc = dv.ucount[u];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
-    // slot prefix (serial over <= 256 slots, by warp 0 with a warp scan per 32)
-    if (warp == 0) {
+    if (warp == 0) {  // slot prefix over <= 256 slots
         int run = n_anchor;
         for (int j0 = 0; j0 < Uc; j0 += 32) {
             const int j = j0 + lane;
             int cnt = 0;
             if (j < Uc) {
-                cnt = dv.slotcnt[(size_t)u * MOG_MAX_UNION + j];
-                scoff[j] = dv.sub_off[(size_t)u * dv.sub_off_stride +
-                                      dv.ucl[(size_t)u * MOG_MAX_UNION + j] * L];
+                const size_t sj = (size_t)u * MOG_MAX_UNION + j;
+                cnt = dv.slotcnt[sj];
+                scoff[j] = dv.slotcoff[sj];
+                sucl[j] = dv.ucl[sj];
             }
             int incl = cnt;
 #pragma unroll
@@ -404,8 +433,12 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     WarpAcc acc;
     acc.init();
     const float scale2 = dv.tau * LOG2E;
-    for (int sbase = r0; sbase < r1; sbase += SUPER) {
-        const int ns = min(SUPER, r1 - sbase);
+    float *stB = reinterpret_cast<float *>(asm_ + AT_SMEM);        // [AT_WARPS][G][PART_W]
+    float *stA = stB - AT_WARPS * G * PART_W;                      // aliases the tile area
+
+    int sbase = r0, ns = 0, nt = 0;
+    auto resolve = [&]() {
+        ns = min(SUPER, r1 - sbase);
         for (int t = tid; t < ns; t += AT_THREADS) {
             const int i = sbase + t;
             int pos;
@@ -433,20 +466,99 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
             smk[t] = mk;
         }
         __syncthreads();
-        const int nt = (int)ceil_div64(ns, AT_ROWS);
-        auto issue = [&](int t) {
-            const int rb = t * AT_ROWS;
-            issue_tile(asm_ + (t % AT_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, ns - rb), kb, vb, dv.sn,
-                       [&](int r, int64_t &pos, uint32_t &mk) {
-                           pos = spos[rb + r];
-                           mk = smk[rb + r];
-                       });
-        };
+        nt = (int)ceil_div64(ns, AT_ROWS);
+    };
+    auto issue = [&](int t) {
+        const int rb = t * AT_ROWS;
+        issue_tile(asm_ + (t % AT_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, ns - rb), kb, vb, dv.sn,
+                   [&](int r, int64_t &pos, uint32_t &mk) {
+                       pos = spos[rb + r];
+                       mk = smk[rb + r];
+                   });
+    };
+    auto prologue = [&]() {
 #pragma unroll
         for (int s = 0; s < AT_STAGES - 1; ++s) {
             if (s < nt) issue(s);
             cp_async_commit();
         }
+    };
+    if (sbase < r1) {
+        resolve();
+        prologue();
+    }
+    // ---------- Gaussian residual of this CTA's slice of unselected groups ----------
+    // (runs while the first tiles are in flight; per-warp online softmax over items)
+    {
+        const int I = Uc * L;
+        const int cA = (int)((int64_t)C * p / P), cB = (int)((int64_t)C * (p + 1) / P);
+        const int iA = (int)((int64_t)I * p / P), iB = (int)((int64_t)I * (p + 1) / P);
+        const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
+        const int ncl = dv.residual ? cB - cA : 0, nsub = dv.residual ? iB - iA : 0;
+        float M[GT], racc[GT][4], rl[GT];
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+            M[g] = -INFINITY;
+            rl[g] = 0.f;
+            racc[g][0] = racc[g][1] = racc[g][2] = racc[g][3] = 0.f;
+        }
+        for (int e = warp; e < ncl + nsub; e += AT_WARPS) {
+            uint32_t need;
+            const float *ex;
+            size_t stride;
+            const float *vbar;
+            if (e < ncl) {
+                const int c = cA + e;
+                need = dv.cl_n[(size_t)u * dv.c_max + c] > 0
+                           ? (allm & ~__ldcg(dv.cselmask + (size_t)u * dv.c_max + c)) : 0u;
+                ex = cres + c;
+                stride = dv.c_max;
+                vbar = dv.cl_vbar + ((size_t)u * dv.c_max + c) * MOG_D;
+            } else {
+                const int it = iA + (e - ncl), jj = it / L, l = it % L;
+                need = dv.subres[((size_t)u * MOG_MAX_UNION + jj) * MOG_MAX_L + l];
+                ex = dv.subscore + (((size_t)u * MOG_MAX_UNION + jj) * G) * MOG_MAX_L + l;
+                stride = MOG_MAX_L;
+                vbar = dv.sub_vbar + ((size_t)u * dv.c_max * dv.l_max + (size_t)sucl[jj] * L + l) * MOG_D;
+            }
+            const float4 v = *reinterpret_cast<const float4 *>(vbar + lane * 4);
+            float exv[GT];
+#pragma unroll
+            for (int g = 0; g < GT; ++g) exv[g] = (g < G && ((need >> g) & 1u)) ? ex[g * stride] * LOG2E : -INFINITY;
+#pragma unroll
+            for (int g = 0; g < GT; ++g) {
+                if (exv[g] == -INFINITY) continue;
+                if (exv[g] > M[g]) {
+                    const float sc = exp2f(M[g] - exv[g]);
+                    rl[g] *= sc;
+                    racc[g][0] *= sc;
+                    racc[g][1] *= sc;
+                    racc[g][2] *= sc;
+                    racc[g][3] *= sc;
+                    M[g] = exv[g];
+                }
+                const float wgt = exp2f(exv[g] - M[g]);
+                rl[g] += wgt;
+                racc[g][0] += wgt * v.x;
+                racc[g][1] += wgt * v.y;
+                racc[g][2] += wgt * v.z;
+                racc[g][3] += wgt * v.w;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+            if (g >= G) break;
+            float *r = stB + ((size_t)warp * G + g) * PART_W;
+            if (lane == 0) {
+                r[0] = M[g];
+                r[1] = rl[g];
+            }
+            *reinterpret_cast<float4 *>(r + PART_ACC + lane * 4) =
+                make_float4(racc[g][0], racc[g][1], racc[g][2], racc[g][3]);
+        }
+    }
+    // ---------------------------- exact rows, tile pipeline ----------------------------
+    while (sbase < r1) {
         for (int t = 0; t < nt; ++t) {
             cp_async_wait<AT_STAGES - 2>();
             __syncthreads();
@@ -456,106 +568,16 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
         }
         cp_async_wait<0>();
         __syncthreads();
+        sbase += SUPER;
+        if (sbase < r1) {
+            resolve();
+            prologue();
+        }
     }
-    float *stA = reinterpret_cast<float *>(asm_);       // [AT_WARPS][G][PART_W] exact
-    float *stB = stA + AT_WARPS * G * PART_W;            // [AT_WARPS][G][PART_W] residual
     warp_state_out(acc, stA, G);
-    // ---------------- Gaussian residual of a slice of the unselected groups ----------
-    const int I = Uc * L;
-    const int cA = (int)((int64_t)C * p / P), cB = (int)((int64_t)C * (p + 1) / P);
-    const int iA = (int)((int64_t)I * p / P), iB = (int)((int64_t)I * (p + 1) / P);
-    const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
-    float mloc[GT];
-#pragma unroll
-    for (int g = 0; g < GT; ++g) mloc[g] = -INFINITY;
-    const int ncl = dv.residual ? cB - cA : 0, nsub = dv.residual ? iB - iA : 0;
-    // pass 1: per-head maximum exponent over this CTA's items
-    for (int e = tid; e < ncl + nsub; e += AT_THREADS) {
-        uint32_t need;
-        const float *ex;
-        size_t stride;
-        if (e < ncl) {
-            const int c = cA + e;
-            need = dv.cl_n[(size_t)u * dv.c_max + c] > 0
-                       ? (allm & ~__ldcg(dv.cselmask + (size_t)u * dv.c_max + c)) : 0u;
-            ex = cres + c;
-            stride = dv.c_max;
-        } else {
-            const int it = iA + (e - ncl), jj = it / L, l = it % L;
-            need = dv.subres[((size_t)u * MOG_MAX_UNION + jj) * MOG_MAX_L + l];
-            ex = dv.subscore + (((size_t)u * MOG_MAX_UNION + jj) * G) * MOG_MAX_L + l;
-            stride = MOG_MAX_L;
-        }
-#pragma unroll
-        for (int g = 0; g < GT; ++g)
-            if (g < G && ((need >> g) & 1u)) mloc[g] = fmaxf(mloc[g], ex[g * stride] * LOG2E);
-    }
-#pragma unroll
-    for (int g = 0; g < GT; ++g) {
-        const float m = warp_max(mloc[g]);
-        if (lane == 0 && g < G) smax[warp][g] = m;
-    }
-    __syncthreads();
-    float M[GT], racc[GT][4], rl[GT];
-#pragma unroll
-    for (int g = 0; g < GT; ++g) {
-        M[g] = -INFINITY;
-        if (g < G)
-            for (int w2 = 0; w2 < AT_WARPS; ++w2) M[g] = fmaxf(M[g], smax[w2][g]);
-        rl[g] = 0.f;
-        racc[g][0] = racc[g][1] = racc[g][2] = racc[g][3] = 0.f;
-    }
-    // pass 2: one warp per item, lane owns 4 dimensions
-    for (int e = warp; e < ncl + nsub; e += AT_WARPS) {
-        uint32_t need;
-        const float *ex;
-        size_t stride;
-        const float *vbar;
-        if (e < ncl) {
-            const int c = cA + e;
-            need = dv.cl_n[(size_t)u * dv.c_max + c] > 0
-                       ? (allm & ~__ldcg(dv.cselmask + (size_t)u * dv.c_max + c)) : 0u;
-            ex = cres + c;
-            stride = dv.c_max;
-            vbar = dv.cl_vbar + ((size_t)u * dv.c_max + c) * MOG_D;
-        } else {
-            const int it = iA + (e - ncl), jj = it / L, l = it % L;
-            need = dv.subres[((size_t)u * MOG_MAX_UNION + jj) * MOG_MAX_L + l];
-            ex = dv.subscore + (((size_t)u * MOG_MAX_UNION + jj) * G) * MOG_MAX_L + l;
-            stride = MOG_MAX_L;
-            const int c = dv.ucl[(size_t)u * MOG_MAX_UNION + jj];
-            vbar = dv.sub_vbar + ((size_t)u * dv.c_max * dv.l_max + (size_t)c * L + l) * MOG_D;
-        }
-        if (!need) continue;
-        const float4 v = *reinterpret_cast<const float4 *>(vbar + lane * 4);
-#pragma unroll
-        for (int g = 0; g < GT; ++g) {
-            if (g < G && ((need >> g) & 1u)) {
-                const float wgt = exp2f(ex[g * stride] * LOG2E - M[g]);
-                rl[g] += wgt;
-                racc[g][0] += wgt * v.x;
-                racc[g][1] += wgt * v.y;
-                racc[g][2] += wgt * v.z;
-                racc[g][3] += wgt * v.w;
-            }
-        }
-    }
-#pragma unroll
-    for (int g = 0; g < GT; ++g) {
-        if (g >= G) break;
-        float *r = stB + ((size_t)warp * G + g) * PART_W;
-        if (lane == 0) {
-            r[0] = rl[g] > 0.f ? M[g] : -INFINITY;
-            r[1] = rl[g];
-        }
-        r[2 + lane * 4 + 0] = racc[g][0];
-        r[2 + lane * 4 + 1] = racc[g][1];
-        r[2 + lane * 4 + 2] = racc[g][2];
-        r[2 + lane * 4 + 3] = racc[g][3];
-    }
     __syncthreads();
     float *part = dv.partials + ((size_t)u * MAX_SPLITS + p) * G * PART_W;
-    merge_states(stA, 2 * AT_WARPS, G, part, false);
+    merge_states(stA, 2 * AT_WARPS, G, part);  // stA and stB are contiguous
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -566,16 +588,11 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     if (!s_last) return;
     __threadfence();
     if (tid == 0) dv.counters[u * 4 + 1] = 0u;
-    float *mg = stA;  // [G][PART_W]
-    merge_states(dv.partials + (size_t)u * MAX_SPLITS * G * PART_W, P, G, mg, true);
-    __syncthreads();
-    for (int e = tid; e < G * MOG_D; e += AT_THREADS) {
-        const int g = e / MOG_D, j = e % MOG_D;
-        const float l = mg[g * PART_W + 1];
-        a.out[((size_t)u * G + g) * MOG_D + j] = l > 0.f ? mg[g * PART_W + 2 + j] / l : 0.f;
-    }
+    merge_global_out(dv.partials + (size_t)u * MAX_SPLITS * G * PART_W, P, G,
+                     reinterpret_cast<float *>(asm_), AT_SMEM / 4, a.out + (size_t)u * G * MOG_D);
 }
 
+// Append one token per sequence at position n_now[b], then advance n_now[b].
 __global__ void k_append(Dev dv, const uint16_t *kn, const uint16_t *vn) {
     const int b = blockIdx.x;
     const int pos = dv.n_now[b];
@@ -618,10 +635,10 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 
 template <int GT>
 static cudaError_t launch_attend(const DecArgs &a, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute((const void *)k_dec_attend<GT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    const size_t sm = AT_SMEM + sizeof(float) * AT_WARPS * a.dv.G * PART_W;
+    cudaError_t e = ensure_smem((const void *)k_dec_attend<GT>, sm);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_dec_attend<GT>, dim3(a.dv.P, a.dv.units), dim3(AT_THREADS), AT_SMEM, s, a);
+    return launch_pdl(k_dec_attend<GT>, dim3(a.dv.P, a.dv.units), dim3(AT_THREADS), sm, s, a);
 }
 
 cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *out,
@@ -637,9 +654,7 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
     a.cand_i = dv.cand_i;
     cudaError_t e;
     const size_t ss = score_smem(dv);
-    if ((e = cudaFuncSetAttribute((const void *)k_dec_score,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss)) != cudaSuccess)
-        return e;
+    if ((e = ensure_smem((const void *)k_dec_score, ss)) != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[0], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_dec_score, dim3(dv.P1, dv.units), dim3(SC_THREADS), ss, s, a)) != cudaSuccess)
         return e;

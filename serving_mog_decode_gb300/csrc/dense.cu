@@ -62,19 +62,17 @@ __global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
     float *st = reinterpret_cast<float *>(dsm);
     warp_state_out(acc, st, a.G);
     __syncthreads();
-    merge_states(st, AT_WARPS, a.G, a.part + ((int64_t)u * a.splits + p) * a.G * PART_W, false);
+    merge_states(st, AT_WARPS, a.G, a.part + ((int64_t)u * a.splits + p) * a.G * PART_W);
 }
 
-__global__ void k_dense_merge(DenseArgs a) {
+constexpr int MERGE_THREADS = 256;
+constexpr int MERGE_SMEM = 96 * 1024;
+
+__global__ void __launch_bounds__(MERGE_THREADS) k_dense_merge(DenseArgs a) {
     extern __shared__ __align__(16) float mg[];
     const int u = blockIdx.x;
-    merge_states(a.part + (int64_t)u * a.splits * a.G * PART_W, a.splits, a.G, mg, true);
-    __syncthreads();
-    for (int e = threadIdx.x; e < a.G * MOG_D; e += blockDim.x) {
-        const int g = e / MOG_D, j = e % MOG_D;
-        const float l = mg[g * PART_W + 1];
-        a.out[((int64_t)u * a.G + g) * MOG_D + j] = l > 0.f ? mg[g * PART_W + 2 + j] / l : 0.f;
-    }
+    merge_global_out(a.part + (int64_t)u * a.splits * a.G * PART_W, a.splits, a.G, mg,
+                     MERGE_SMEM / 4, a.out + (int64_t)u * a.G * MOG_D);
 }
 
 int dense_splits(int units, int n_max) {
@@ -89,15 +87,15 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
                          int64_t sn, const int32_t *lengths, int n_max, int batch, int h_kv,
                          int G, const void *q, float *out, float *scratch, int splits,
                          cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute((const void *)k_dense_split,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    cudaError_t e = ensure_smem((const void *)k_dense_split, AT_SMEM);
+    if (e == cudaSuccess) e = ensure_smem((const void *)k_dense_merge, MERGE_SMEM);
     if (e != cudaSuccess) return e;
     DenseArgs a{K, V, sb, sh, sn, lengths, h_kv, G, splits,
                 static_cast<const uint16_t *>(q), out, scratch,
                 (float)(LOG2E / sqrt((double)MOG_D))};
     const int U = batch * h_kv;
     k_dense_split<<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
-    k_dense_merge<<<U, 256, G * PART_W * sizeof(float), s>>>(a);
+    k_dense_merge<<<U, MERGE_THREADS, MERGE_SMEM, s>>>(a);
     return cudaGetLastError();
 }
 

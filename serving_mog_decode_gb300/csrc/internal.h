@@ -35,7 +35,7 @@ struct Dev {
     // decode workspace
     float *cscore, *subscore, *partials;
     uint32_t *cselmask, *uhm, *subres, *rowmask;
-    int *ucl, *ucount, *sel, *slotcnt, *rowpos;
+    int *ucl, *ucount, *sel, *slotcnt, *slotcoff, *rowpos;
     unsigned *counters;
     float *cand_s;  // [units][P1][G][tc] per-slice top clusters
     int *cand_i;
@@ -58,11 +58,13 @@ struct Plan {
     int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
         o_sub_assign;
     int64_t o_cscore, o_subscore, o_partials, o_cselmask, o_uhm, o_subres, o_rowmask, o_ucl,
-        o_ucount, o_sel, o_slotcnt, o_rowpos, o_counters, o_cand_s, o_cand_i;
+        o_ucount, o_sel, o_slotcnt, o_slotcoff, o_rowpos, o_counters, o_cand_s, o_cand_i;
     int64_t total;
 };
 
 int num_sms();
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (function, device, size)
+cudaError_t ensure_smem(const void *fn, size_t bytes);
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl);
 Dev make_dev(const Plan &pl, void *arena, const mog_kv *kv);
 void unit_clusters(const mog_params *p, int n, int *C, int *L);

@@ -710,9 +710,7 @@ static AssignJob build_job(const Dev &dv, int t) {
     return jb;
 }
 
-static cudaError_t set_smem(const void *fn, size_t bytes) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
+static cudaError_t set_smem(const void *fn, size_t bytes) { return ensure_smem(fn, bytes); }
 
 static size_t l2_smem() { return 3 * MOG_MAX_L * MOG_D * sizeof(float); }
 
