@@ -119,14 +119,11 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
         P.n_mid_max = std::max(P.n_mid_max, std::max(0, n - p->n_recent - p->n_sink));
     }
     if (P.l_max > MOG_MAX_L || P.c_max > MAX_C || P.ts > MOG_MAX_L) return MOG_ERR_SHAPE;
-    if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION) return MOG_ERR_SHAPE;
+    if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION || P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
     const int tcc = std::max(P.tc, 1);
-    const int p1_min = (int)ceil_div64(P.c_max, 64);
-    const int p1_cap = std::min(64, 1024 / tcc);
-    if (p1_min > p1_cap) return MOG_ERR_SHAPE;  // c_max too large for this top_c
+    P.P1 = (int)ceil_div64(P.c_max, 64);  // 64-cluster scoring slices
+    if (sub_smem_bytes(P.G, P.c_max, P.tc) > 200 * 1024) return MOG_ERR_SHAPE;  // candidate lists
     const int sms = num_sms();
-    P.P1 = std::min(p1_cap, std::max(p1_min, (int)ceil_div64(2 * sms, P.units)));
-    P.P1 = std::max(1, std::min(P.P1, P.c_max));
     P.P = std::max(1, std::min(MAX_SPLITS, (int)ceil_div64(2 * sms, P.units)));
     P.nchunks = std::max(1, (int)ceil_div64(P.n_mid_max, SORT_CHUNK));
     P.sub_off_stride = (P.c_max * P.l_max + 1 + 3) & ~3;
@@ -163,7 +160,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_sub_assign = take(4 * U * nc);
     P.o_cscore = take(4 * U * 2 * G * cm);
     P.o_subscore = take(4 * U * MOG_MAX_UNION * G * MOG_MAX_L);
-    P.o_partials = take(4 * U * MAX_SPLITS * G * (MOG_D + 2));
+    P.o_partials = take(4 * U * PART_SLOTS * G * (MOG_D + 4));
     P.o_cselmask = take(4 * U * cm);
     P.o_uhm = take(4 * U * MOG_MAX_UNION);
     P.o_subres = take(4 * U * MOG_MAX_UNION * MOG_MAX_L);
@@ -515,7 +512,7 @@ extern "C" int dense_decode_scratch_bytes(int32_t batch, int32_t h_kv, int32_t h
     if (!bytes || batch <= 0 || h_kv <= 0 || h_q <= 0 || n_max <= 0) return MOG_ERR_INVALID_ARG;
     if (d != MOG_D || h_q % h_kv != 0 || h_q / h_kv > MOG_MAX_G) return MOG_ERR_SHAPE;
     const int units = batch * h_kv, G = h_q / h_kv;
-    *bytes = (size_t)units * dense_splits(units, n_max) * G * (MOG_D + 2) * sizeof(float);
+    *bytes = (size_t)units * dense_splits(units, n_max) * G * (MOG_D + 4) * sizeof(float);
     return MOG_OK;
 }
 

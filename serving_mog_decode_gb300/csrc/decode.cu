@@ -35,219 +35,219 @@ struct DecArgs {
     int *cand_i;
 };
 
-// per-head score weights: w[g][0..d) = tau q, w[g][d..2d) = tau^2/2 q^2
-__device__ __forceinline__ void load_weights(float *w, const uint16_t *q, int G, float tau) {
-    for (int e = threadIdx.x; e < G * MOG_D; e += blockDim.x) {
-        const int g = e / MOG_D, j = e % MOG_D;
-        const float qv = bf1(q[(size_t)g * MOG_D + j]);
-        w[g * 2 * MOG_D + j] = tau * qv;
-        w[g * 2 * MOG_D + MOG_D + j] = 0.5f * tau * tau * qv * qv;
+// per-head score weights, float4-chunked: w[g][k] (k < 32) holds tau*q over dims 4k..4k+3,
+// w[g][32 + k] holds tau^2/2 * q^2 over the same dims
+__device__ __forceinline__ void load_weights(float4 *w, const uint16_t *q, int G, float tau) {
+    for (int e = threadIdx.x; e < G * 32; e += blockDim.x) {
+        const int g = e / 32, k = e % 32;
+        const uint2 raw = *reinterpret_cast<const uint2 *>(q + (size_t)g * MOG_D + 4 * k);
+        const float q0 = bf_lo(raw.x), q1 = bf_hi(raw.x), q2 = bf_lo(raw.y), q3 = bf_hi(raw.y);
+        w[g * 64 + k] = make_float4(tau * q0, tau * q1, tau * q2, tau * q3);
+        const float t2 = 0.5f * tau * tau;
+        w[g * 64 + 32 + k] = make_float4(t2 * q0 * q0, t2 * q1 * q1, t2 * q2 * q2, t2 * q3 * q3);
     }
 }
 
-// warp-cooperative: scores of one group (summary ms[2d]) for heads g < G.
-// Returns through res[g], sel[g] on every lane.
-__device__ __forceinline__ void group_scores(const float *ms, int n, const float *w, int G,
-                                             int mode, float *res, float *sel) {
-    const int lane = threadIdx.x & 31;
-    const float4 mu = *reinterpret_cast<const float4 *>(ms + lane * 4);
-    const float4 va = *reinterpret_cast<const float4 *>(ms + MOG_D + lane * 4);
-    const float ln = n > 0 ? logf((float)n) : 0.f;
-    for (int g = 0; g < G; ++g) {
-        const float4 wm = *reinterpret_cast<const float4 *>(w + g * 2 * MOG_D + lane * 4);
-        const float4 wv = *reinterpret_cast<const float4 *>(w + g * 2 * MOG_D + MOG_D + lane * 4);
-        float dm = wm.x * mu.x + wm.y * mu.y + wm.z * mu.z + wm.w * mu.w;
-        float dq = wv.x * va.x + wv.y * va.y + wv.z * va.z + wv.w * va.w;
-        dm = warp_sum(dm);
-        dq = warp_sum(dq);
-        const float r = n > 0 ? ln + dm + dq : -INFINITY;
-        res[g] = r;
-        sel[g] = mode == 0 ? r : (n > 0 ? dm : -INFINITY);
-    }
-}
-
-// warp argmax over (value desc, index asc); returns the winner on every lane
-__device__ __forceinline__ void warp_best(float &v, int &i) {
+// Scores of one group by 4 cooperating lanes (lanes 4i..4i+3 of a warp): lane part q reads
+// the float4 chunks k = q + 4i of the mean and of the variance.  Returns, on all 4 lanes,
+// the log-mass exponent res[g] (the residual's) and the selection score sel[g].
+template <int GT>
+__device__ __forceinline__ void quad_scores(const float *ms, int n, bool valid, const float4 *w,
+                                            int G, int mode, float (&res)[GT], float (&sel)[GT]) {
+    const int q = threadIdx.x & 3;
+    float4 mu[8], va[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-        if (ranks_before(ov, oi, v, i)) {
-            v = ov;
-            i = oi;
+    for (int i = 0; i < 8; ++i) {
+        if (valid) {
+            mu[i] = *reinterpret_cast<const float4 *>(ms + 4 * (q + 4 * i));
+            va[i] = *reinterpret_cast<const float4 *>(ms + MOG_D + 4 * (q + 4 * i));
+        } else {
+            mu[i] = va[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    const float ln = n > 0 ? logf((float)n) : 0.f;
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+        if (g >= G) break;
+        float dm = 0.f, dq = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 a = w[g * 64 + q + 4 * i], b = w[g * 64 + 32 + q + 4 * i];
+            dm += a.x * mu[i].x + a.y * mu[i].y + a.z * mu[i].z + a.w * mu[i].w;
+            dq += b.x * va[i].x + b.y * va[i].y + b.z * va[i].z + b.w * va[i].w;
+        }
+        dm += __shfl_xor_sync(0xffffffffu, dm, 1);
+        dm += __shfl_xor_sync(0xffffffffu, dm, 2);
+        dq += __shfl_xor_sync(0xffffffffu, dq, 1);
+        dq += __shfl_xor_sync(0xffffffffu, dq, 2);
+        const bool ok = valid && n > 0;
+        res[g] = ok ? ln + dm + dq : -INFINITY;
+        sel[g] = !ok ? -INFINITY : (mode == 0 ? res[g] : dm);
+    }
 }
-
-constexpr int SC_THREADS = 256;
-constexpr int SC_SLICE = 64;  // clusters per score CTA at most (two per lane)
-constexpr int SC_PER_WARP = SC_SLICE / (SC_THREADS / 32);
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
 }
 
+constexpr int SC_THREADS = 256;
+constexpr int SC_SLICE = 64;  // clusters per scoring CTA: 4 lanes each
+
+// K1: grid (ceil(c_max/64), units).  Scores of a 64-cluster slice for all G heads; the
+// slice's top-tc per head (rank counting, score desc then index asc) as a sorted candidate
+// list cand[u][g][slice][tc].
+template <int GT>
 __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
-    extern __shared__ __align__(16) float scs[];
     const Dev &dv = a.dv;
     const int G = dv.G, tc = dv.tc;
-    float *w = scs;                               // [G][2d]
-    float *ssel = w + G * 2 * MOG_D;              // [G][SC_SLICE]
-    float *stg_s = ssel + G * SC_SLICE;           // [8 warps][P1*tc]
-    int *stg_i = reinterpret_cast<int *>(stg_s + 8 * dv.P1 * max(tc, 1));
-    __shared__ int s_last;
-    __shared__ int s_wcnt[8];
+    __shared__ float4 w[GT * 64];
+    __shared__ float ssel[GT][SC_SLICE];
     pdl_wait();
     pdl_trigger();
     const int u = blockIdx.y, p = blockIdx.x;
-    const int *ui = dv.unit_info + u * UI_STRIDE;
-    const int C = ui[UI_C];
-    const int c0 = (int)((int64_t)C * p / dv.P1), c1 = (int)((int64_t)C * (p + 1) / dv.P1);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // summaries of this warp's clusters, loaded before the weights are ready
-    float4 mu[SC_PER_WARP], va[SC_PER_WARP];
-    int nn[SC_PER_WARP];
-#pragma unroll
-    for (int k = 0; k < SC_PER_WARP; ++k) {
-        const int c = c0 + warp + 8 * k;
-        nn[k] = 0;
-        if (c < c1) {
-            const float *ms = dv.cl_ms + ((size_t)u * dv.c_max + c) * 2 * MOG_D;
-            mu[k] = *reinterpret_cast<const float4 *>(ms + lane * 4);
-            va[k] = *reinterpret_cast<const float4 *>(ms + MOG_D + lane * 4);
-            nn[k] = dv.cl_n[(size_t)u * dv.c_max + c];
-        }
-    }
+    const int C = dv.unit_info[u * UI_STRIDE + UI_C];
+    const int c0 = p * SC_SLICE, ns = max(0, min(SC_SLICE, C - c0));
+    const int cl = threadIdx.x >> 2, q4 = threadIdx.x & 3;
+    const int c = c0 + cl;
+    const bool valid = cl < ns;
+    const float *ms = dv.cl_ms + ((size_t)u * dv.c_max + (valid ? c : 0)) * 2 * MOG_D;
+    const int n = valid ? dv.cl_n[(size_t)u * dv.c_max + c] : 0;
     load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
     __syncthreads();
+    float res[GT], sl[GT];
+    quad_scores<GT>(ms, n, valid, w, G, dv.score_mode, res, sl);
     float *cres = dv.cscore + (size_t)u * 2 * G * dv.c_max;  // [0][g][c] selection, [1][g][c] residual
+    if (valid && q4 == 0) {
 #pragma unroll
-    for (int k = 0; k < SC_PER_WARP; ++k) {
-        const int c = c0 + warp + 8 * k;
-        if (c >= c1) break;
-        const int n = nn[k];
-        const float ln = n > 0 ? logf((float)n) : 0.f;
-        for (int g = 0; g < G; ++g) {
-            const float4 wm = *reinterpret_cast<const float4 *>(w + g * 2 * MOG_D + lane * 4);
-            const float4 wv = *reinterpret_cast<const float4 *>(w + g * 2 * MOG_D + MOG_D + lane * 4);
-            float dm = wm.x * mu[k].x + wm.y * mu[k].y + wm.z * mu[k].z + wm.w * mu[k].w;
-            float dq = wv.x * va[k].x + wv.y * va[k].y + wv.z * va[k].z + wv.w * va[k].w;
-            dm = warp_sum(dm);
-            dq = warp_sum(dq);
-            const float r = n > 0 ? ln + dm + dq : -INFINITY;
-            const float sl = dv.score_mode == 0 ? r : (n > 0 ? dm : -INFINITY);
-            if (lane == 0) {
-                cres[(size_t)g * dv.c_max + c] = sl;
-                cres[((size_t)G + g) * dv.c_max + c] = r;
-                ssel[g * SC_SLICE + (c - c0)] = sl;
-            }
-        }
-        if (lane == 0) dv.cselmask[(size_t)u * dv.c_max + c] = 0u;
-    }
-    __syncthreads();
-    // local top-tc of this slice, per head
-    const int ns = c1 - c0;
-    for (int g = warp; g < G && tc > 0; g += SC_THREADS / 32) {
-        float v0 = lane < ns ? ssel[g * SC_SLICE + lane] : -INFINITY;
-        float v1 = lane + 32 < ns ? ssel[g * SC_SLICE + lane + 32] : -INFINITY;
-        float *cs = a.cand_s + (((size_t)u * G + g) * dv.P1 + p) * tc;
-        int *ci = a.cand_i + (((size_t)u * G + g) * dv.P1 + p) * tc;
-        for (int r = 0; r < tc; ++r) {
-            float bv;
-            int bi;
-            if (ranks_before(v1, c0 + lane + 32, v0, c0 + lane)) {
-                bv = v1;
-                bi = c0 + lane + 32;
-            } else {
-                bv = v0;
-                bi = c0 + lane;
-            }
-            warp_best(bv, bi);
-            if (bv == -INFINITY) {
-                for (int rr = r + lane; rr < tc; rr += 32) {
-                    cs[rr] = -INFINITY;
-                    ci[rr] = -1;
-                }
-                break;
-            }
-            if (lane == 0) {
-                cs[r] = bv;
-                ci[r] = bi;
-            }
-            if (bi == c0 + lane) v0 = -INFINITY;
-            if (bi == c0 + lane + 32) v1 = -INFINITY;
+        for (int g = 0; g < GT; ++g) {
+            if (g >= G) break;
+            cres[(size_t)g * dv.c_max + c] = sl[g];
+            cres[((size_t)G + g) * dv.c_max + c] = res[g];
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned t = atomicAdd(dv.counters + u * 4 + 0, 1u);
-        s_last = (t == (unsigned)dv.P1 - 1);
+    if (q4 == 0) {
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+            if (g < G) ssel[g][cl] = valid ? sl[g] : -INFINITY;
     }
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x == 0) dv.counters[u * 4 + 0] = 0u;
-    // ---- last CTA of the unit: merge the P1 sorted candidate lists of every head ----
-    int *sel = dv.sel + (size_t)u * G * a.SW;
-    const int ncand = dv.P1 * tc;
-    for (int g = warp; g < G; g += SC_THREADS / 32) {
-        int *sg = sel + (size_t)g * a.SW;
-        for (int e = lane; e < a.SW; e += 32) sg[e] = -1;
-        __syncwarp();
-        if (tc == 0) continue;
+    if (tc == 0) return;
+    const int P1 = gridDim.x;
+    const int span = max(SC_SLICE, tc);
+    for (int e = threadIdx.x; e < G * span; e += SC_THREADS) {
+        const int g = e / span, i = e % span;
+        float *cs = a.cand_s + (((size_t)u * G + g) * P1 + p) * tc;
+        int *ci = a.cand_i + (((size_t)u * G + g) * P1 + p) * tc;
+        if (i < ns) {
+            const float v = ssel[g][i];
+            int rank = 0;
+            for (int k = 0; k < ns; ++k) rank += ranks_before(ssel[g][k], k, v, i);
+            if (rank < tc) {
+                cs[rank] = v;
+                ci[rank] = v == -INFINITY ? -1 : c0 + i;
+            }
+        } else if (i < tc) {
+            cs[i] = -INFINITY;
+            ci[i] = -1;
+        }
+    }
+}
+
+constexpr int SB_THREADS = 256;
+constexpr int SB_CHUNK = 32;  // residual items staged per pass
+
+// K2: grid (max(1, min(c_max, G*tc)), units).  Every CTA merges the per-slice candidate
+// lists into each head's top-tc clusters (or takes the caller's selection), forms the union
+// over the G heads (ascending cluster index) and takes union slot j: subcluster scores,
+// top-ts per head that selected the cluster, the compacted exact rows, and the Gaussian
+// residual partial of (a) the unselected subclusters of its cluster and (b) a slice of the
+// clusters that some head did not select.
+template <int GT>
+__global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
+    extern __shared__ __align__(16) uint8_t sbm[];
+    const Dev &dv = a.dv;
+    const int G = dv.G, tc = dv.tc, ts = dv.ts;
+    const int u = blockIdx.y, j = blockIdx.x;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int C = ui[UI_C], L = ui[UI_L];
+    const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
+    const int NC = P1 * tc;  // candidates per head
+    // dynamic shared memory
+    float *cand_s = reinterpret_cast<float *>(sbm);                 // [G][NC]
+    int *cand_i = reinterpret_cast<int *>(cand_s + (size_t)G * NC);  // [G][NC]
+    uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + (size_t)G * NC);  // [c_max]
+    float *vst = reinterpret_cast<float *>(cselm + ((dv.c_max + 3) & ~3));   // [SB_CHUNK][d]
+    __shared__ float4 w[GT * 64];
+    __shared__ int selc[GT][MOG_MAX_UNION];
+    __shared__ float sres[GT][MOG_MAX_L];
+    __shared__ float ssl[GT][MOG_MAX_L];
+    __shared__ uint32_t smask[MOG_MAX_L];
+    __shared__ int sso[MOG_MAX_L + 1], snn[MOG_MAX_L], spref[MOG_MAX_L + 1];
+    __shared__ float iex[SB_CHUNK][GT];
+    __shared__ uint32_t ineed[SB_CHUNK];
+    __shared__ int s_wcnt[SB_THREADS / 32], s_cj, s_uc;
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
+    // ---- 1. every head's top-tc clusters ----
+    for (int e = tid; e < G * MOG_MAX_UNION; e += SB_THREADS) selc[e / MOG_MAX_UNION][e % MOG_MAX_UNION] = -1;
+    for (int e = tid; e < C; e += SB_THREADS) cselm[e] = 0u;
+    if (tc > 0 && !a.sel_in) {
+        const size_t base = (size_t)u * G * NC;
+        for (int e = tid; e < G * NC; e += SB_THREADS) {
+            cp_async4(smem_u32(cand_s + e), a.cand_s + base + e);
+            cp_async4(smem_u32(cand_i + e), a.cand_i + base + e);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (tc > 0) {
         if (a.sel_in) {
-            const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW;
-            for (int r = lane; r < tc; r += 32) {
-                const int c = si[r];
-                sg[r] = (c >= 0 && c < C && dv.cl_n[(size_t)u * dv.c_max + c] > 0) ? c : -1;
+            for (int e = tid; e < G * tc; e += SB_THREADS) {
+                const int g = e / tc, r = e % tc;
+                const int c = a.sel_in[((size_t)u * G + g) * a.SW + r];
+                selc[g][r] = (c >= 0 && c < C && dv.cl_n[(size_t)u * dv.c_max + c] > 0) ? c : -1;
             }
         } else {
-            float *ss = stg_s + warp * ncand;
-            int *sx = stg_i + warp * ncand;
-            const size_t base = ((size_t)u * G + g) * ncand;
-            for (int e = lane; e < ncand; e += 32) {
-                cp_async4(smem_u32(ss + e), a.cand_s + base + e);
-                cp_async4(smem_u32(sx + e), a.cand_i + base + e);
-            }
-            cp_async_commit();
-            cp_async_wait<0>();
-            __syncwarp();
-            // lane k walks lists k and k+32
-            int p0 = 0, p1 = 0;
-            for (int r = 0; r < tc; ++r) {
-                float va = -INFINITY, vb = -INFINITY;
-                int ia = 0x7fffffff, ib = 0x7fffffff;
-                if (lane < dv.P1 && p0 < tc && sx[lane * tc + p0] >= 0) {
-                    va = ss[lane * tc + p0];
-                    ia = sx[lane * tc + p0];
+            // element (g, list p, position r): its rank over all lists of head g is r plus,
+            // for every other list, the length of that list's prefix ranking before it
+            for (int e = tid; e < G * NC; e += SB_THREADS) {
+                const int g = e / NC, pr = e % NC, pl = pr / tc, r = pr % tc;
+                const float *cs = cand_s + (size_t)g * NC;
+                const int *ci = cand_i + (size_t)g * NC;
+                const int x = ci[pr];
+                if (x < 0) continue;
+                const float v = cs[pr];
+                int rank = r;
+                for (int q = 0; q < P1 && rank < tc; ++q) {
+                    if (q == pl) continue;
+                    int lo = 0, hi = tc;  // first position not ranking before (v, x)
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        const int xm = ci[q * tc + mid];
+                        if (xm >= 0 && ranks_before(cs[q * tc + mid], xm, v, x)) lo = mid + 1;
+                        else hi = mid;
+                    }
+                    rank += lo;
                 }
-                if (lane + 32 < dv.P1 && p1 < tc && sx[(lane + 32) * tc + p1] >= 0) {
-                    vb = ss[(lane + 32) * tc + p1];
-                    ib = sx[(lane + 32) * tc + p1];
-                }
-                const bool takeb = ranks_before(vb, ib, va, ia);
-                float bv = takeb ? vb : va;
-                int bi = takeb ? ib : ia;
-                warp_best(bv, bi);
-                if (bv == -INFINITY) break;
-                if (lane == 0) sg[r] = bi;
-                if (!takeb && ia == bi) ++p0;
-                else if (takeb && ib == bi) ++p1;
+                if (rank < tc) selc[g][rank] = x;
             }
         }
-        __syncwarp();
-        for (int r = lane; r < tc; r += 32)
-            if (sg[r] >= 0) atomicOr(dv.cselmask + (size_t)u * dv.c_max + sg[r], 1u << g);
     }
     __syncthreads();
-    // union of the selected clusters over the G heads, ascending cluster index
+    for (int e = tid; e < G * tc; e += SB_THREADS) {
+        const int c = selc[e / tc][e % tc];
+        if (c >= 0) atomicOr(&cselm[c], 1u << (e / tc));
+    }
+    __syncthreads();
+    // ---- 2. union over the heads, ascending; this CTA's slot ----
     {
-        const int per = (int)ceil_div64(C, SC_THREADS);
-        const int cA = threadIdx.x * per, cB = min(C, cA + per);
-        const uint32_t *cm = dv.cselmask + (size_t)u * dv.c_max;
+        const int per = (int)ceil_div64(C, SB_THREADS);
+        const int cA = tid * per, cB = min(C, cA + per);
         int cnt = 0;
-        for (int c = cA; c < cB; ++c) cnt += __ldcg(cm + c) != 0u;
+        for (int c = cA; c < cB; ++c) cnt += cselm[c] != 0u;
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -258,124 +258,226 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
         __syncthreads();
         int base = incl - cnt;
         for (int k = 0; k < warp; ++k) base += s_wcnt[k];
-        for (int c = cA; c < cB; ++c) {
-            const uint32_t m = __ldcg(cm + c);
-            if (m) {
-                dv.ucl[(size_t)u * MOG_MAX_UNION + base] = c;
-                dv.uhm[(size_t)u * MOG_MAX_UNION + base] = m;
-                ++base;
-            }
-        }
-        if (threadIdx.x == SC_THREADS - 1) dv.ucount[u] = base;
-    }
-}
-
-constexpr int SUB_THREADS = 128;
-
-__global__ void __launch_bounds__(SUB_THREADS) k_dec_sub(DecArgs a) {
-    extern __shared__ __align__(16) float sbs[];
-    const Dev &dv = a.dv;
-    const int G = dv.G;
-    float *w = sbs;                        // [G][2d]
-    float *sres = w + G * 2 * MOG_D;       // [G][32]
-    float *ssel = sres + G * MOG_MAX_L;    // [G][32]
-    __shared__ uint32_t smask[MOG_MAX_L];
-    __shared__ int spref[MOG_MAX_L + 1];
-    __shared__ int sso[MOG_MAX_L + 1];
-    __shared__ int snn[MOG_MAX_L];
-    pdl_wait();
-    pdl_trigger();
-    const int u = blockIdx.y, j = blockIdx.x;
-    if (j >= dv.ucount[u]) return;
-    const int *ui = dv.unit_info + u * UI_STRIDE;
-    const int L = ui[UI_L];
-    const int c = dv.ucl[(size_t)u * MOG_MAX_UNION + j];
-    const uint32_t hm = dv.uhm[(size_t)u * MOG_MAX_UNION + j];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
-    const size_t g0 = (size_t)u * dv.c_max * dv.l_max + (size_t)c * L;
-    if (threadIdx.x <= (unsigned)L) sso[threadIdx.x] = so[threadIdx.x];
-    if (threadIdx.x < (unsigned)L) snn[threadIdx.x] = dv.sub_n[g0 + threadIdx.x];
-    if (threadIdx.x < MOG_MAX_L) smask[threadIdx.x] = 0u;
-    load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
-    __syncthreads();
-    float res[MOG_MAX_G], sl[MOG_MAX_G];
-    for (int l = warp; l < L; l += SUB_THREADS / 32) {
-        group_scores(dv.sub_ms + (g0 + l) * 2 * MOG_D, snn[l], w, G, dv.score_mode, res, sl);
-        if (lane == 0)
-            for (int g = 0; g < G; ++g) {
-                sres[g * MOG_MAX_L + l] = res[g];
-                ssel[g * MOG_MAX_L + l] = sl[g];
-            }
-    }
-    __syncthreads();
-    int *selu = dv.sel + (size_t)u * G * a.SW;
-    for (int g = warp; g < G; g += SUB_THREADS / 32) {
-        if (!((hm >> g) & 1u)) continue;
-        int *sg = selu + (size_t)g * a.SW;
-        int rk = -1;  // rank of c in this head's cluster list
-        for (int r0 = 0; r0 < dv.tc; r0 += 32) {
-            const int r = r0 + lane;
-            const uint32_t b = __ballot_sync(0xffffffffu, r < dv.tc && sg[r] == c);
-            if (b) {
-                rk = r0 + __ffs(b) - 1;
-                break;
-            }
-        }
-        if (rk < 0) continue;
-        int *subs = sg + dv.tc + rk * dv.ts;
-        if (a.sel_in) {
-            const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + dv.tc + rk * dv.ts;
-            for (int r = lane; r < dv.ts; r += 32) {
-                const int l = si[r];
-                const bool ok = l >= 0 && l < L && snn[l] > 0;
-                subs[r] = ok ? l : -1;
-                if (ok) atomicOr(&smask[l], 1u << g);
-            }
-        } else {
-            float v = lane < L ? ssel[g * MOG_MAX_L + lane] : -INFINITY;
-            for (int r = 0; r < dv.ts; ++r) {
-                float bv = v;
-                int bi = lane;
-                warp_best(bv, bi);
-                if (bv == -INFINITY) break;
-                if (lane == 0) {
-                    subs[r] = bi;
-                    atomicOr(&smask[bi], 1u << g);
+        if (tid == SB_THREADS - 1) s_uc = base + cnt;
+        if (j >= base && j < base + cnt) {
+            int k = base;
+            for (int c = cA; c < cB; ++c)
+                if (cselm[c]) {
+                    if (k == j) s_cj = c;
+                    ++k;
                 }
-                if (bi == lane) v = -INFINITY;
-            }
         }
     }
     __syncthreads();
-    if (threadIdx.x < (unsigned)L) {
-        const int l = threadIdx.x;
-        dv.subres[((size_t)u * MOG_MAX_UNION + j) * MOG_MAX_L + l] = snn[l] > 0 ? (hm & ~smask[l]) : 0u;
-        for (int g = 0; g < G; ++g)
-            dv.subscore[(((size_t)u * MOG_MAX_UNION + j) * G + g) * MOG_MAX_L + l] = sres[g * MOG_MAX_L + l];
+    const int Uc = s_uc;
+    const int R = max(Uc, 1);
+    if (j >= R) return;
+    const bool has_slot = j < Uc;
+    const int c = has_slot ? s_cj : 0;
+    const uint32_t hm = has_slot ? cselm[c] : 0u;
+    int *selu = dv.sel + (size_t)u * G * a.SW;
+    if (j == 0) {
+        if (tid == 0) dv.ucount[u] = Uc;
+        for (int e = tid; e < G * tc; e += SB_THREADS) {
+            const int g = e / tc, r = e % tc;
+            selu[(size_t)g * a.SW + r] = selc[g][r];
+            if (selc[g][r] < 0)
+                for (int k = 0; k < ts; ++k) selu[(size_t)g * a.SW + tc + r * ts + k] = -1;
+        }
     }
-    if (threadIdx.x == 0) {
-        spref[0] = 0;
-        for (int l = 0; l < L; ++l) spref[l + 1] = spref[l] + (smask[l] ? sso[l + 1] - sso[l] : 0);
-        dv.slotcnt[(size_t)u * MOG_MAX_UNION + j] = spref[L];
-        dv.slotcoff[(size_t)u * MOG_MAX_UNION + j] = sso[0];
+    // ---- 3. subcluster scores of the slot's cluster ----
+    const size_t g0 = (size_t)u * dv.c_max * dv.l_max + (size_t)c * L;
+    const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
+    if (has_slot) {
+        if (tid <= L) sso[tid] = so[tid];
+        if (tid < L) snn[tid] = dv.sub_n[g0 + tid];
+        if (tid < MOG_MAX_L) smask[tid] = 0u;
+        load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
+        __syncthreads();
+        const int l = tid >> 2;
+        const bool valid = l < L;
+        float res[GT], sl[GT];
+        quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D, valid ? snn[l] : 0, valid,
+                        w, G, dv.score_mode, res, sl);
+        if (valid && (tid & 3) == 0) {
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+                if (g < G) {
+                    sres[g][l] = res[g];
+                    ssl[g][l] = sl[g];
+                }
+        }
+        __syncthreads();
+        // top-ts per head that selected c (rank counting over <= 32 subclusters)
+        for (int g = warp; g < G; g += SB_THREADS / 32) {
+            if (!((hm >> g) & 1u)) continue;
+            int rk = -1;
+            for (int r = 0; r < tc; ++r)
+                if (selc[g][r] == c) { rk = r; break; }
+            if (rk < 0) continue;
+            int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
+            if (a.sel_in) {
+                const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + tc + (size_t)rk * ts;
+                for (int r = lane; r < ts; r += 32) {
+                    const int l2 = si[r];
+                    const bool ok = l2 >= 0 && l2 < L && snn[l2] > 0;
+                    subs[r] = ok ? l2 : -1;
+                    if (ok) atomicOr(&smask[l2], 1u << g);
+                }
+            } else {
+                for (int r = lane; r < ts; r += 32) subs[r] = -1;
+                __syncwarp();
+                const float v = lane < L ? ssl[g][lane] : -INFINITY;
+                int rank = 0;
+                for (int k = 0; k < L; ++k) rank += ranks_before(ssl[g][k], k, v, lane);
+                if (lane < L && v != -INFINITY && rank < ts) {
+                    subs[rank] = lane;
+                    atomicOr(&smask[lane], 1u << g);
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            spref[0] = 0;
+            for (int k = 0; k < L; ++k) spref[k + 1] = spref[k] + (smask[k] ? sso[k + 1] - sso[k] : 0);
+            dv.slotcnt[(size_t)u * MOG_MAX_UNION + j] = spref[L];
+            dv.slotcoff[(size_t)u * MOG_MAX_UNION + j] = sso[0];
+        }
+        __syncthreads();
+        // compacted exact rows, one flat parallel pass
+        const int tot = spref[L];
+        const int *perm = dv.perm + (size_t)u * dv.n_cap;
+        int *rp = dv.rowpos + (size_t)u * dv.n_cap + sso[0];
+        uint32_t *rm = dv.rowmask + (size_t)u * dv.n_cap + sso[0];
+        for (int i = tid; i < tot; i += SB_THREADS) {
+            int k = 0;
+            while (spref[k + 1] <= i) ++k;
+            rp[i] = perm[sso[k] + (i - spref[k])];
+            rm[i] = smask[k];
+        }
     }
-    __syncthreads();
-    // compacted rows of the selected subclusters, one flat parallel pass
-    const int tot = spref[L];
-    const int *perm = dv.perm + (size_t)u * dv.n_cap;
-    int *rp = dv.rowpos + (size_t)u * dv.n_cap + sso[0];
-    uint32_t *rm = dv.rowmask + (size_t)u * dv.n_cap + sso[0];
-    for (int i = threadIdx.x; i < tot; i += SUB_THREADS) {
-        int l = 0;
-        while (spref[l + 1] <= i) ++l;
-        rp[i] = perm[sso[l] + (i - spref[l])];
-        rm[i] = smask[l];
+    // ---- 4. Gaussian residual partial ----
+    // items: unselected subclusters of the slot's cluster (heads that selected it), then the
+    // clusters [j*C/R, (j+1)*C/R) for the heads that did not select them
+    const int nsub = (dv.residual && has_slot) ? L : 0;
+    const int cA = (int)((int64_t)C * j / R), cB = (int)((int64_t)C * (j + 1) / R);
+    const int ncl = dv.residual ? cB - cA : 0;
+    const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
+    // thread (g, quad) accumulates dims 4*quad..4*quad+3 of head g
+    const int rg = tid >> 5, rq = tid & 31;
+    float m_run = -INFINITY, l_run = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < nsub + ncl; i0 += SB_CHUNK) {
+        const int cnt = min(SB_CHUNK, nsub + ncl - i0);
+        __syncthreads();
+        for (int e = tid; e < cnt * 32; e += SB_THREADS) {  // value means, 16 B per thread
+            const int it = i0 + e / 32, k = e % 32;
+            const float *vb = it < nsub ? dv.sub_vbar + (g0 + it) * MOG_D
+                                        : dv.cl_vbar + ((size_t)u * dv.c_max + cA + (it - nsub)) * MOG_D;
+            cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * k), vb + 4 * k, 16);
+        }
+        cp_async_commit();
+        for (int e = tid; e < cnt; e += SB_THREADS) {
+            const int it = i0 + e;
+            uint32_t need;
+            if (it < nsub) {
+                need = snn[it] > 0 ? (hm & ~smask[it]) : 0u;
+                for (int g = 0; g < G && g < GT; ++g) iex[e][g] = sres[g][it];
+            } else {
+                const int cc = cA + (it - nsub);
+                need = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~cselm[cc]) : 0u;
+                for (int g = 0; g < G && g < GT; ++g) iex[e][g] = cres[(size_t)g * dv.c_max + cc];
+            }
+            ineed[e] = need;
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+        if (rg < G) {
+            for (int e = 0; e < cnt; ++e) {
+                if (!((ineed[e] >> rg) & 1u)) continue;
+                const float ex = iex[e][rg] * LOG2E;
+                if (ex > m_run) {
+                    const float sc = exp2f(m_run - ex);
+                    l_run *= sc;
+                    acc.x *= sc;
+                    acc.y *= sc;
+                    acc.z *= sc;
+                    acc.w *= sc;
+                    m_run = ex;
+                }
+                const float wgt = exp2f(ex - m_run);
+                const float4 v = *reinterpret_cast<const float4 *>(vst + (size_t)e * MOG_D + 4 * rq);
+                l_run += wgt;
+                acc.x += wgt * v.x;
+                acc.y += wgt * v.y;
+                acc.z += wgt * v.z;
+                acc.w += wgt * v.w;
+            }
+        }
+    }
+    // heads beyond the 8 warps: loop (G <= 16)
+    float *rp2 = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS + j) * G * PART_W;
+    if (rg < G) {
+        float *r = rp2 + (size_t)rg * PART_W;
+        if (rq == 0) {
+            r[0] = m_run;
+            r[1] = l_run;
+        }
+        *reinterpret_cast<float4 *>(r + PART_ACC + 4 * rq) = acc;
+    }
+    if (G > SB_THREADS / 32) {  // second pass for heads 8..15
+        for (int g2 = 8 + rg; g2 < G; g2 += 8) {
+            float m2 = -INFINITY, l2 = 0.f;
+            float4 a2 = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i0 = 0; i0 < nsub + ncl; ++i0) {
+                uint32_t need;
+                float exv;
+                const float *vb;
+                if (i0 < nsub) {
+                    need = snn[i0] > 0 ? (hm & ~smask[i0]) : 0u;
+                    exv = sres[g2 < GT ? g2 : 0][i0];
+                    vb = dv.sub_vbar + (g0 + i0) * MOG_D;
+                } else {
+                    const int cc = cA + (i0 - nsub);
+                    need = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~cselm[cc]) : 0u;
+                    exv = cres[(size_t)g2 * dv.c_max + cc];
+                    vb = dv.cl_vbar + ((size_t)u * dv.c_max + cc) * MOG_D;
+                }
+                if (!((need >> g2) & 1u)) continue;
+                const float ex = exv * LOG2E;
+                if (ex > m2) {
+                    const float sc = exp2f(m2 - ex);
+                    l2 *= sc;
+                    a2.x *= sc;
+                    a2.y *= sc;
+                    a2.z *= sc;
+                    a2.w *= sc;
+                    m2 = ex;
+                }
+                const float wgt = exp2f(ex - m2);
+                const float4 v = *reinterpret_cast<const float4 *>(vb + 4 * rq);
+                l2 += wgt;
+                a2.x += wgt * v.x;
+                a2.y += wgt * v.y;
+                a2.z += wgt * v.z;
+                a2.w += wgt * v.w;
+            }
+            float *r = rp2 + (size_t)g2 * PART_W;
+            if (rq == 0) {
+                r[0] = m2;
+                r[1] = l2;
+            }
+            *reinterpret_cast<float4 *>(r + PART_ACC + 4 * rq) = a2;
+        }
     }
 }
 
 constexpr int SUPER = 256;  // rows resolved per pass
+constexpr int RB = 8;       // residual partials staged per pass in the attention kernel
 
+// K3: grid (P, units).  Rows [p*T/P, (p+1)*T/P) of the unit's exact list (anchors first),
+// plus residual partials [p*R/P, (p+1)*R/P) from k_dec_sub, into one partial; the last CTA
+// of the unit merges the P partials and normalises once.
 template <int GT>
 __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     extern __shared__ __align__(128) uint8_t asm_[];
@@ -383,7 +485,6 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     const int G = dv.G;
     __shared__ int spre[MOG_MAX_UNION + 1];
     __shared__ int scoff[MOG_MAX_UNION];
-    __shared__ int sucl[MOG_MAX_UNION];
     __shared__ int spos[SUPER];
     __shared__ uint32_t smk[SUPER];
     __shared__ int s_last;
@@ -391,14 +492,26 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     pdl_trigger();
     const int u = blockIdx.y, p = blockIdx.x, P = dv.P;
     const int *ui = dv.unit_info + u * UI_STRIDE;
-    const int b = ui[UI_B], h = u % dv.h_kv, C = ui[UI_C], L = ui[UI_L];
+    const int b = ui[UI_B], h = u % dv.h_kv;
     const int S = ui[UI_S], rlo = ui[UI_RLO];
     const int nnow = dv.n_now[b];
     const int s_cnt = min(S, nnow), r_cnt = max(0, nnow - rlo);
     const int n_anchor = s_cnt + r_cnt;
-    const int Uc = dv.ucount[u];
+    const int Uc = dv.tc > 0 ? dv.ucount[u] : 0;
+    const int R = max(Uc, 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
+    float *stA = reinterpret_cast<float *>(asm_ + AT_SMEM);   // [AT_WARPS + RB][G][PART_W]
+    float *stR = stA + (size_t)AT_WARPS * G * PART_W;
+    // residual partials of this CTA: fetch now, merge at the end
+    const int ra = (int)((int64_t)R * p / P), rb = (int)((int64_t)R * (p + 1) / P);
+    const float *rsrc = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS) * G * PART_W;
+    {
+        const int cnt = min(RB, rb - ra);
+        for (int q = tid; q < cnt * G * PART_W / 4; q += AT_THREADS)
+            cp_async16(smem_u32(stR + 4 * q), rsrc + (size_t)ra * G * PART_W + 4 * q, 16);
+        cp_async_commit();
+    }
     if (warp == 0) {  // slot prefix over <= 256 slots
         int run = n_anchor;
         for (int j0 = 0; j0 < Uc; j0 += 32) {
@@ -408,7 +521,6 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
                 const size_t sj = (size_t)u * MOG_MAX_UNION + j;
                 cnt = dv.slotcnt[sj];
                 scoff[j] = dv.slotcoff[sj];
-                sucl[j] = dv.ucl[sj];
             }
             int incl = cnt;
 #pragma unroll
@@ -433,9 +545,6 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     WarpAcc acc;
     acc.init();
     const float scale2 = dv.tau * LOG2E;
-    float *stB = reinterpret_cast<float *>(asm_ + AT_SMEM);        // [AT_WARPS][G][PART_W]
-    float *stA = stB - AT_WARPS * G * PART_W;                      // aliases the tile area
-
     int sbase = r0, ns = 0, nt = 0;
     auto resolve = [&]() {
         ns = min(SUPER, r1 - sbase);
@@ -469,96 +578,20 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
         nt = (int)ceil_div64(ns, AT_ROWS);
     };
     auto issue = [&](int t) {
-        const int rb = t * AT_ROWS;
-        issue_tile(asm_ + (t % AT_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, ns - rb), kb, vb, dv.sn,
+        const int rbs = t * AT_ROWS;
+        issue_tile(asm_ + (t % AT_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, ns - rbs), kb, vb, dv.sn,
                    [&](int r, int64_t &pos, uint32_t &mk) {
-                       pos = spos[rb + r];
-                       mk = smk[rb + r];
+                       pos = spos[rbs + r];
+                       mk = smk[rbs + r];
                    });
     };
-    auto prologue = [&]() {
+    while (sbase < r1) {
+        resolve();
 #pragma unroll
         for (int s = 0; s < AT_STAGES - 1; ++s) {
             if (s < nt) issue(s);
             cp_async_commit();
         }
-    };
-    if (sbase < r1) {
-        resolve();
-        prologue();
-    }
-    // ---------- Gaussian residual of this CTA's slice of unselected groups ----------
-    // (runs while the first tiles are in flight; per-warp online softmax over items)
-    {
-        const int I = Uc * L;
-        const int cA = (int)((int64_t)C * p / P), cB = (int)((int64_t)C * (p + 1) / P);
-        const int iA = (int)((int64_t)I * p / P), iB = (int)((int64_t)I * (p + 1) / P);
-        const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
-        const int ncl = dv.residual ? cB - cA : 0, nsub = dv.residual ? iB - iA : 0;
-        float M[GT], racc[GT][4], rl[GT];
-#pragma unroll
-        for (int g = 0; g < GT; ++g) {
-            M[g] = -INFINITY;
-            rl[g] = 0.f;
-            racc[g][0] = racc[g][1] = racc[g][2] = racc[g][3] = 0.f;
-        }
-        for (int e = warp; e < ncl + nsub; e += AT_WARPS) {
-            uint32_t need;
-            const float *ex;
-            size_t stride;
-            const float *vbar;
-            if (e < ncl) {
-                const int c = cA + e;
-                need = dv.cl_n[(size_t)u * dv.c_max + c] > 0
-                           ? (allm & ~__ldcg(dv.cselmask + (size_t)u * dv.c_max + c)) : 0u;
-                ex = cres + c;
-                stride = dv.c_max;
-                vbar = dv.cl_vbar + ((size_t)u * dv.c_max + c) * MOG_D;
-            } else {
-                const int it = iA + (e - ncl), jj = it / L, l = it % L;
-                need = dv.subres[((size_t)u * MOG_MAX_UNION + jj) * MOG_MAX_L + l];
-                ex = dv.subscore + (((size_t)u * MOG_MAX_UNION + jj) * G) * MOG_MAX_L + l;
-                stride = MOG_MAX_L;
-                vbar = dv.sub_vbar + ((size_t)u * dv.c_max * dv.l_max + (size_t)sucl[jj] * L + l) * MOG_D;
-            }
-            const float4 v = *reinterpret_cast<const float4 *>(vbar + lane * 4);
-            float exv[GT];
-#pragma unroll
-            for (int g = 0; g < GT; ++g) exv[g] = (g < G && ((need >> g) & 1u)) ? ex[g * stride] * LOG2E : -INFINITY;
-#pragma unroll
-            for (int g = 0; g < GT; ++g) {
-                if (exv[g] == -INFINITY) continue;
-                if (exv[g] > M[g]) {
-                    const float sc = exp2f(M[g] - exv[g]);
-                    rl[g] *= sc;
-                    racc[g][0] *= sc;
-                    racc[g][1] *= sc;
-                    racc[g][2] *= sc;
-                    racc[g][3] *= sc;
-                    M[g] = exv[g];
-                }
-                const float wgt = exp2f(exv[g] - M[g]);
-                rl[g] += wgt;
-                racc[g][0] += wgt * v.x;
-                racc[g][1] += wgt * v.y;
-                racc[g][2] += wgt * v.z;
-                racc[g][3] += wgt * v.w;
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < GT; ++g) {
-            if (g >= G) break;
-            float *r = stB + ((size_t)warp * G + g) * PART_W;
-            if (lane == 0) {
-                r[0] = M[g];
-                r[1] = rl[g];
-            }
-            *reinterpret_cast<float4 *>(r + PART_ACC + lane * 4) =
-                make_float4(racc[g][0], racc[g][1], racc[g][2], racc[g][3]);
-        }
-    }
-    // ---------------------------- exact rows, tile pipeline ----------------------------
-    while (sbase < r1) {
         for (int t = 0; t < nt; ++t) {
             cp_async_wait<AT_STAGES - 2>();
             __syncthreads();
@@ -569,15 +602,32 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
         cp_async_wait<0>();
         __syncthreads();
         sbase += SUPER;
-        if (sbase < r1) {
-            resolve();
-            prologue();
-        }
     }
+    cp_async_wait<0>();
     warp_state_out(acc, stA, G);
     __syncthreads();
-    float *part = dv.partials + ((size_t)u * MAX_SPLITS + p) * G * PART_W;
-    merge_states(stA, 2 * AT_WARPS, G, part);  // stA and stB are contiguous
+    float *part = dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W;
+    const int nres = max(0, min(RB, rb - ra));
+    if (rb - ra <= RB) {
+        merge_states(stA, AT_WARPS + nres, G, part);  // stA and stR are contiguous
+    } else {
+        // more residual partials than one stage: fold them in RB at a time through the
+        // (now free) tile area: run[0] holds the running state, run[1..] the staged chunk
+        float *run = reinterpret_cast<float *>(asm_);
+        float *tmp = run + (size_t)(1 + RB) * G * PART_W;
+        merge_states(stA, AT_WARPS + nres, G, tmp);
+        for (int k0 = ra + RB; k0 < rb; k0 += RB) {
+            __syncthreads();
+            for (int q = tid; q < G * PART_W; q += AT_THREADS) run[q] = tmp[q];
+            const int cnt = min(RB, rb - k0);
+            for (int q = tid; q < cnt * G * PART_W / 4; q += AT_THREADS)
+                cp_async16(smem_u32(run + (size_t)G * PART_W + 4 * q), rsrc + (size_t)k0 * G * PART_W + 4 * q, 16);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncthreads();
+            merge_states(run, 1 + cnt, G, k0 + RB >= rb ? part : tmp);
+        }
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -588,7 +638,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     if (!s_last) return;
     __threadfence();
     if (tid == 0) dv.counters[u * 4 + 1] = 0u;
-    merge_global_out(dv.partials + (size_t)u * MAX_SPLITS * G * PART_W, P, G,
+    merge_global_out(dv.partials + (size_t)u * PART_SLOTS * G * PART_W, P, G,
                      reinterpret_cast<float *>(asm_), AT_SMEM / 4, a.out + (size_t)u * G * MOG_D);
 }
 
@@ -609,14 +659,6 @@ __global__ void k_append(Dev dv, const uint16_t *kn, const uint16_t *vn) {
 }
 
 // ------------------------------------------------------------------------------------
-static size_t score_smem(const Dev &dv) {
-    return sizeof(float) * ((size_t)dv.G * 2 * MOG_D + (size_t)dv.G * SC_SLICE) +
-           (sizeof(float) + sizeof(int)) * 8 * (size_t)dv.P1 * (size_t)max(dv.tc, 1);
-}
-static size_t sub_smem(const Dev &dv) {
-    return sizeof(float) * ((size_t)dv.G * 2 * MOG_D + 2 * (size_t)dv.G * MOG_MAX_L);
-}
-
 template <typename K>
 static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               const DecArgs &a) {
@@ -633,12 +675,33 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+size_t sub_smem_bytes(int G, int c_max, int tc) {
+    const int P1 = (int)ceil_div64(c_max, SC_SLICE);
+    return sizeof(float) * 2 * (size_t)G * P1 * tc + sizeof(uint32_t) * ((c_max + 3) & ~3) +
+           sizeof(float) * SB_CHUNK * MOG_D;
+}
+
 template <int GT>
-static cudaError_t launch_attend(const DecArgs &a, cudaStream_t s) {
-    const size_t sm = AT_SMEM + sizeof(float) * AT_WARPS * a.dv.G * PART_W;
-    cudaError_t e = ensure_smem((const void *)k_dec_attend<GT>, sm);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k_dec_attend<GT>, dim3(a.dv.P, a.dv.units), dim3(AT_THREADS), sm, s, a);
+static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t const *events) {
+    const Dev &dv = a.dv;
+    cudaError_t e;
+    if (events && (e = cudaEventRecord(events[0], s)) != cudaSuccess) return e;
+    const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
+    if ((e = launch_pdl(k_dec_score<GT>, dim3(P1, dv.units), dim3(SC_THREADS), 0, s, a)) != cudaSuccess)
+        return e;
+    if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
+    const size_t sm2 = sub_smem_bytes(dv.G, dv.c_max, dv.tc);
+    if ((e = ensure_smem((const void *)k_dec_sub<GT>, sm2)) != cudaSuccess) return e;
+    const int nslot = max(1, min(dv.c_max, dv.G * dv.tc));
+    if ((e = launch_pdl(k_dec_sub<GT>, dim3(nslot, dv.units), dim3(SB_THREADS), sm2, s, a)) != cudaSuccess)
+        return e;
+    if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
+    const size_t sm3 = AT_SMEM + sizeof(float) * (AT_WARPS + RB) * dv.G * PART_W;
+    if ((e = ensure_smem((const void *)k_dec_attend<GT>, sm3)) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_dec_attend<GT>, dim3(dv.P, dv.units), dim3(AT_THREADS), sm3, s, a)) != cudaSuccess)
+        return e;
+    if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
+    return cudaSuccess;
 }
 
 cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *out,
@@ -652,27 +715,14 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
     a.SW = dv.tc + dv.tc * dv.ts;
     a.cand_s = dv.cand_s;
     a.cand_i = dv.cand_i;
-    cudaError_t e;
-    const size_t ss = score_smem(dv);
-    if ((e = ensure_smem((const void *)k_dec_score, ss)) != cudaSuccess) return e;
-    if (events && (e = cudaEventRecord(events[0], s)) != cudaSuccess) return e;
-    if ((e = launch_pdl(k_dec_score, dim3(dv.P1, dv.units), dim3(SC_THREADS), ss, s, a)) != cudaSuccess)
-        return e;
-    if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
-    if (dv.tc > 0) {
-        if ((e = launch_pdl(k_dec_sub, dim3(min(dv.c_max, dv.G * dv.tc), dv.units), dim3(SUB_THREADS), sub_smem(dv), s,
-                            a)) != cudaSuccess)
-            return e;
-    }
-    if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     const int G = dv.G;
-    if (G <= 1) e = launch_attend<1>(a, s);
-    else if (G <= 2) e = launch_attend<2>(a, s);
-    else if (G <= 4) e = launch_attend<4>(a, s);
-    else if (G <= 8) e = launch_attend<8>(a, s);
-    else e = launch_attend<16>(a, s);
+    cudaError_t e;
+    if (G <= 1) e = launch_steps<1>(a, s, events);
+    else if (G <= 2) e = launch_steps<2>(a, s, events);
+    else if (G <= 4) e = launch_steps<4>(a, s, events);
+    else if (G <= 8) e = launch_steps<8>(a, s, events);
+    else e = launch_steps<16>(a, s, events);
     if (e != cudaSuccess) return e;
-    if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     if (sel_out && a.SW > 0)
         e = cudaMemcpyAsync(sel_out, dv.sel, sizeof(int32_t) * (size_t)dv.units * G * a.SW,
                             cudaMemcpyDeviceToDevice, s);
