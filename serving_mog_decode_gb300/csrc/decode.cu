@@ -172,11 +172,13 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
     const int C = ui[UI_C], L = ui[UI_L];
     const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
     const int NC = P1 * tc;  // candidates per head
-    // dynamic shared memory
-    float *cand_s = reinterpret_cast<float *>(sbm);                 // [G][NC]
-    int *cand_i = reinterpret_cast<int *>(cand_s + (size_t)G * NC);  // [G][NC]
-    uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + (size_t)G * NC);  // [c_max]
-    float *vst = reinterpret_cast<float *>(cselm + ((dv.c_max + 3) & ~3));   // [SB_CHUNK][d]
+    // dynamic shared memory; every region starts on a 16-byte boundary (the staged value
+    // means are read and written 16 bytes at a time)
+    const size_t ncw = ((size_t)G * NC + 3) & ~(size_t)3;
+    float *cand_s = reinterpret_cast<float *>(sbm);                  // [G][NC]
+    int *cand_i = reinterpret_cast<int *>(cand_s + ncw);              // [G][NC]
+    uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + ncw);     // [c_max]
+    float *vst = reinterpret_cast<float *>(cselm + ((dv.c_max + 3) & ~3));  // [SB_CHUNK][d]
     __shared__ float4 w[GT * 64];
     __shared__ int selc[GT][MOG_MAX_UNION];
     __shared__ float sres[GT][MOG_MAX_L];
@@ -677,7 +679,8 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
 
 size_t sub_smem_bytes(int G, int c_max, int tc) {
     const int P1 = (int)ceil_div64(c_max, SC_SLICE);
-    return sizeof(float) * 2 * (size_t)G * P1 * tc + sizeof(uint32_t) * ((c_max + 3) & ~3) +
+    const size_t ncw = ((size_t)G * P1 * tc + 3) & ~(size_t)3;  // 16-byte multiples
+    return sizeof(float) * 2 * ncw + sizeof(uint32_t) * ((c_max + 3) & ~3) +
            sizeof(float) * SB_CHUNK * MOG_D;
 }
 

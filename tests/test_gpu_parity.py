@@ -396,3 +396,20 @@ def test_append_joins_recent_anchors():
         assert rel(out[0, hq], ref) < OUT_TOL
     with pytest.raises(mog.MogError, match="CAPACITY"):
         h.append(bf(kn), bf(vn))
+
+
+def test_many_units_many_slots_per_split():
+    """256 KV heads (2 splits each) with up to 24 selected clusters: every attention CTA
+    folds more residual partials than one staging pass holds."""
+    w = small_workload(1200, batch=16, h_kv=16, h_q=16, centres=24, n_clusters=36, n_sub=4,
+                       top_c=24, top_s=2, n_recent=16, seed=51)
+    inj = Injected(w)
+    assert inj.h.splits() * 8 < 24
+    _check_decode(inj, sample_heads=range(0, 256, 7))
+
+
+def test_sixteen_query_heads_per_kv_head():
+    w = small_workload(2500, h_kv=1, h_q=16, top_c=5, top_s=3, seed=61)
+    inj = Injected(w)
+    _check_stats(inj)
+    _check_decode(inj)
