@@ -121,7 +121,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (P.l_max > MOG_MAX_L || P.c_max > MAX_C || P.ts > MOG_MAX_L) return MOG_ERR_SHAPE;
     if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION || P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
     const int tcc = std::max(P.tc, 1);
-    P.P1 = (int)ceil_div64(P.c_max, 64);  // 64-cluster scoring slices
+    P.P1 = (int)ceil_div64(P.c_max, 32);  // 32-cluster scoring slices
     if (sub_smem_bytes(P.G, P.c_max, P.tc) > 200 * 1024) return MOG_ERR_SHAPE;  // candidate lists
     const int sms = num_sms();
     P.P = std::max(1, std::min(MAX_SPLITS, (int)ceil_div64(2 * sms, P.units)));
@@ -358,6 +358,9 @@ static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
     CKH(cudaMemsetAsync(a + pl.o_l1_assign, 0xff, 4 * (size_t)pl.units * pl.n_cap, s));
     CKH(cudaMemsetAsync(a + pl.o_l1_steps, 0, 4 * (size_t)pl.units, s));
     CKH(cudaMemsetAsync(a + pl.o_ucount, 0, 4 * (size_t)pl.units, s));
+    // groups beyond a unit's C / L keep count 0 (the decode scores every c < c_max)
+    CKH(cudaMemsetAsync(a + pl.o_cl_n, 0, 4 * (size_t)pl.units * pl.c_max, s));
+    CKH(cudaMemsetAsync(a + pl.o_sub_n, 0, 4 * (size_t)pl.units * pl.c_max * pl.l_max, s));
 #undef CKH
     *hh = h;
     return MOG_OK;

@@ -90,32 +90,60 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
 }
 
-constexpr int SC_THREADS = 256;
-constexpr int SC_SLICE = 64;  // clusters per scoring CTA: 4 lanes each
+// Running (max, sum, acc) of a softmax-weighted sum over 4 output dimensions, log2 domain.
+struct OnlineAcc {
+    float m, l;
+    float4 a;
+    __device__ __forceinline__ void init() {
+        m = -INFINITY;
+        l = 0.f;
+        a = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __device__ __forceinline__ void absorb(float ex, const float *v4) {
+        if (ex > m) {
+            const float sc = exp2f(m - ex);
+            l *= sc;
+            a.x *= sc;
+            a.y *= sc;
+            a.z *= sc;
+            a.w *= sc;
+            m = ex;
+        }
+        const float wgt = exp2f(ex - m);
+        const float4 v = *reinterpret_cast<const float4 *>(v4);
+        l += wgt;
+        a.x += wgt * v.x;
+        a.y += wgt * v.y;
+        a.z += wgt * v.z;
+        a.w += wgt * v.w;
+    }
+};
 
-// K1: grid (ceil(c_max/64), units).  Scores of a 64-cluster slice for all G heads; the
-// slice's top-tc per head (rank counting, score desc then index asc) as a sorted candidate
-// list cand[u][g][slice][tc].
+constexpr int SC_SLICE = 32;                 // clusters per scoring CTA
+constexpr int SC_THREADS = 4 * SC_SLICE;     // 4 lanes per cluster
+
+// K1: grid (ceil(c_max/32), units).  Scores of a 32-cluster slice for all G heads (clusters
+// beyond a unit's C have count 0 and score -inf); the slice's top-tc per head (rank
+// counting, score desc then index asc) as a sorted candidate list cand[u][g][slice][tc].
 template <int GT>
 __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     const Dev &dv = a.dv;
     const int G = dv.G, tc = dv.tc;
     __shared__ float4 w[GT * 64];
     __shared__ float ssel[GT][SC_SLICE];
-    pdl_wait();
-    pdl_trigger();
     const int u = blockIdx.y, p = blockIdx.x;
-    const int C = dv.unit_info[u * UI_STRIDE + UI_C];
-    const int c0 = p * SC_SLICE, ns = max(0, min(SC_SLICE, C - c0));
     const int cl = threadIdx.x >> 2, q4 = threadIdx.x & 3;
-    const int c = c0 + cl;
-    const bool valid = cl < ns;
+    const int c = p * SC_SLICE + cl;
+    const bool valid = c < dv.c_max;
+    // everything read here is written before the decode step starts
     const float *ms = dv.cl_ms + ((size_t)u * dv.c_max + (valid ? c : 0)) * 2 * MOG_D;
     const int n = valid ? dv.cl_n[(size_t)u * dv.c_max + c] : 0;
     load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
     __syncthreads();
     float res[GT], sl[GT];
     quad_scores<GT>(ms, n, valid, w, G, dv.score_mode, res, sl);
+    pdl_wait();  // the previous step's readers of cscore/cand are done
+    pdl_trigger();
     float *cres = dv.cscore + (size_t)u * 2 * G * dv.c_max;  // [0][g][c] selection, [1][g][c] residual
     if (valid && q4 == 0) {
 #pragma unroll
@@ -132,16 +160,17 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     }
     __syncthreads();
     if (tc == 0) return;
-    const int P1 = gridDim.x;
+    const int P1 = gridDim.x, c0 = p * SC_SLICE;
     const int span = max(SC_SLICE, tc);
     for (int e = threadIdx.x; e < G * span; e += SC_THREADS) {
         const int g = e / span, i = e % span;
         float *cs = a.cand_s + (((size_t)u * G + g) * P1 + p) * tc;
         int *ci = a.cand_i + (((size_t)u * G + g) * P1 + p) * tc;
-        if (i < ns) {
+        if (i < SC_SLICE) {
             const float v = ssel[g][i];
             int rank = 0;
-            for (int k = 0; k < ns; ++k) rank += ranks_before(ssel[g][k], k, v, i);
+#pragma unroll 8
+            for (int k = 0; k < SC_SLICE; ++k) rank += ranks_before(ssel[g][k], k, v, i);
             if (rank < tc) {
                 cs[rank] = v;
                 ci[rank] = v == -INFINITY ? -1 : c0 + i;
@@ -154,7 +183,7 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
 }
 
 constexpr int SB_THREADS = 256;
-constexpr int SB_CHUNK = 32;  // residual items staged per pass
+constexpr int SB_CHUNK = 32;  // cluster residual items staged per pass
 
 // K2: grid (max(1, min(c_max, G*tc)), units).  Every CTA merges the per-slice candidate
 // lists into each head's top-tc clusters (or takes the caller's selection), forms the union
@@ -172,13 +201,13 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
     const int C = ui[UI_C], L = ui[UI_L];
     const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
     const int NC = P1 * tc;  // candidates per head
-    // dynamic shared memory; every region starts on a 16-byte boundary (the staged value
-    // means are read and written 16 bytes at a time)
+    // dynamic shared memory, every region 16-byte aligned
     const size_t ncw = ((size_t)G * NC + 3) & ~(size_t)3;
-    float *cand_s = reinterpret_cast<float *>(sbm);                  // [G][NC]
-    int *cand_i = reinterpret_cast<int *>(cand_s + ncw);              // [G][NC]
-    uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + ncw);     // [c_max]
-    float *vst = reinterpret_cast<float *>(cselm + ((dv.c_max + 3) & ~3));  // [SB_CHUNK][d]
+    float *cand_s = reinterpret_cast<float *>(sbm);                        // [G][NC]
+    int *cand_i = reinterpret_cast<int *>(cand_s + ncw);                    // [G][NC]
+    uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + ncw);           // [c_max]
+    float *vst = reinterpret_cast<float *>(cselm + ((dv.c_max + 3) & ~3));  // [32 + SB_CHUNK][d]
+    float *vcl = vst + (size_t)MOG_MAX_L * MOG_D;
     __shared__ float4 w[GT * 64];
     __shared__ int selc[GT][MOG_MAX_UNION];
     __shared__ float sres[GT][MOG_MAX_L];
@@ -188,13 +217,16 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
     __shared__ float iex[SB_CHUNK][GT];
     __shared__ uint32_t ineed[SB_CHUNK];
     __shared__ int s_wcnt[SB_THREADS / 32], s_cj, s_uc;
-    pdl_wait();
-    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
-    // ---- 1. every head's top-tc clusters ----
+    // ---- 0. before the dependency: weights, cleared tables ----
+    load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
     for (int e = tid; e < G * MOG_MAX_UNION; e += SB_THREADS) selc[e / MOG_MAX_UNION][e % MOG_MAX_UNION] = -1;
     for (int e = tid; e < C; e += SB_THREADS) cselm[e] = 0u;
+    if (tid < MOG_MAX_L) smask[tid] = 0u;
+    pdl_wait();
+    pdl_trigger();
+    // ---- 1. every head's top-tc clusters ----
     if (tc > 0 && !a.sel_in) {
         const size_t base = (size_t)u * G * NC;
         for (int e = tid; e < G * NC; e += SB_THREADS) {
@@ -209,8 +241,8 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
         if (a.sel_in) {
             for (int e = tid; e < G * tc; e += SB_THREADS) {
                 const int g = e / tc, r = e % tc;
-                const int c = a.sel_in[((size_t)u * G + g) * a.SW + r];
-                selc[g][r] = (c >= 0 && c < C && dv.cl_n[(size_t)u * dv.c_max + c] > 0) ? c : -1;
+                const int cc = a.sel_in[((size_t)u * G + g) * a.SW + r];
+                selc[g][r] = (cc >= 0 && cc < C && dv.cl_n[(size_t)u * dv.c_max + cc] > 0) ? cc : -1;
             }
         } else {
             // element (g, list p, position r): its rank over all lists of head g is r plus,
@@ -240,8 +272,8 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
     }
     __syncthreads();
     for (int e = tid; e < G * tc; e += SB_THREADS) {
-        const int c = selc[e / tc][e % tc];
-        if (c >= 0) atomicOr(&cselm[c], 1u << (e / tc));
+        const int cc = selc[e / tc][e % tc];
+        if (cc >= 0) atomicOr(&cselm[cc], 1u << (e / tc));
     }
     __syncthreads();
     // ---- 2. union over the heads, ascending; this CTA's slot ----
@@ -249,7 +281,7 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
         const int per = (int)ceil_div64(C, SB_THREADS);
         const int cA = tid * per, cB = min(C, cA + per);
         int cnt = 0;
-        for (int c = cA; c < cB; ++c) cnt += cselm[c] != 0u;
+        for (int cc = cA; cc < cB; ++cc) cnt += cselm[cc] != 0u;
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -263,9 +295,9 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
         if (tid == SB_THREADS - 1) s_uc = base + cnt;
         if (j >= base && j < base + cnt) {
             int k = base;
-            for (int c = cA; c < cB; ++c)
-                if (cselm[c]) {
-                    if (k == j) s_cj = c;
+            for (int cc = cA; cc < cB; ++cc)
+                if (cselm[cc]) {
+                    if (k == j) s_cj = cc;
                     ++k;
                 }
         }
@@ -287,20 +319,44 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
                 for (int k = 0; k < ts; ++k) selu[(size_t)g * a.SW + tc + r * ts + k] = -1;
         }
     }
-    // ---- 3. subcluster scores of the slot's cluster ----
+    // ---- 3. one batch of loads: subcluster summaries and value means, the first chunk of
+    //         the cluster residual slice ----
     const size_t g0 = (size_t)u * dv.c_max * dv.l_max + (size_t)c * L;
     const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
+    const int nsub = (dv.residual && has_slot) ? L : 0;
+    const int cA = (int)((int64_t)C * j / R), cB = (int)((int64_t)C * (j + 1) / R);
+    const int ncl = dv.residual ? cB - cA : 0;
+    const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
+    auto stage_clusters = [&](int k0) {  // cluster items k0 .. k0 + SB_CHUNK of the slice
+        const int cnt = min(SB_CHUNK, ncl - k0);
+        for (int e = tid; e < cnt * 32; e += SB_THREADS) {
+            const int cc = cA + k0 + e / 32, k = e % 32;
+            cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * k),
+                       dv.cl_vbar + ((size_t)u * dv.c_max + cc) * MOG_D + 4 * k, 16);
+        }
+        cp_async_commit();
+        for (int e = tid; e < cnt; e += SB_THREADS) {
+            const int cc = cA + k0 + e;
+            ineed[e] = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~cselm[cc]) : 0u;
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+                if (g < G) iex[e][g] = cres[(size_t)g * dv.c_max + cc];
+        }
+    };
+    if (nsub > 0)
+        for (int e = tid; e < L * 32; e += SB_THREADS)
+            cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
+                       dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
+    if (ncl > 0) stage_clusters(0);
+    else cp_async_commit();
     if (has_slot) {
         if (tid <= L) sso[tid] = so[tid];
         if (tid < L) snn[tid] = dv.sub_n[g0 + tid];
-        if (tid < MOG_MAX_L) smask[tid] = 0u;
-        load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
-        __syncthreads();
         const int l = tid >> 2;
         const bool valid = l < L;
         float res[GT], sl[GT];
-        quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D, valid ? snn[l] : 0, valid,
-                        w, G, dv.score_mode, res, sl);
+        quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D,
+                        valid ? dv.sub_n[g0 + l] : 0, valid, w, G, dv.score_mode, res, sl);
         if (valid && (tid & 3) == 0) {
 #pragma unroll
             for (int g = 0; g < GT; ++g)
@@ -309,8 +365,10 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
                     ssl[g][l] = sl[g];
                 }
         }
-        __syncthreads();
-        // top-ts per head that selected c (rank counting over <= 32 subclusters)
+    }
+    __syncthreads();
+    // ---- 4. top-ts subclusters per head that selected c; compacted exact rows ----
+    if (has_slot) {
         for (int g = warp; g < G; g += SB_THREADS / 32) {
             if (!((hm >> g) & 1u)) continue;
             int rk = -1;
@@ -339,14 +397,22 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
             }
         }
         __syncthreads();
-        if (tid == 0) {
-            spref[0] = 0;
-            for (int k = 0; k < L; ++k) spref[k + 1] = spref[k] + (smask[k] ? sso[k + 1] - sso[k] : 0);
-            dv.slotcnt[(size_t)u * MOG_MAX_UNION + j] = spref[L];
-            dv.slotcoff[(size_t)u * MOG_MAX_UNION + j] = sso[0];
+        if (warp == 0) {  // prefix of the selected subclusters' sizes
+            const int cnt = lane < L && smask[lane] ? sso[lane + 1] - sso[lane] : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane < L) spref[lane + 1] = incl;
+            if (lane == 0) {
+                spref[0] = 0;
+                dv.slotcoff[(size_t)u * MOG_MAX_UNION + j] = sso[0];
+            }
+            if (lane == L - 1) dv.slotcnt[(size_t)u * MOG_MAX_UNION + j] = incl;
         }
         __syncthreads();
-        // compacted exact rows, one flat parallel pass
         const int tot = spref[L];
         const int *perm = dv.perm + (size_t)u * dv.n_cap;
         int *rp = dv.rowpos + (size_t)u * dv.n_cap + sso[0];
@@ -358,124 +424,52 @@ __global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
             rm[i] = smask[k];
         }
     }
-    // ---- 4. Gaussian residual partial ----
-    // items: unselected subclusters of the slot's cluster (heads that selected it), then the
-    // clusters [j*C/R, (j+1)*C/R) for the heads that did not select them
-    const int nsub = (dv.residual && has_slot) ? L : 0;
-    const int cA = (int)((int64_t)C * j / R), cB = (int)((int64_t)C * (j + 1) / R);
-    const int ncl = dv.residual ? cB - cA : 0;
-    const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
-    // thread (g, quad) accumulates dims 4*quad..4*quad+3 of head g
-    const int rg = tid >> 5, rq = tid & 31;
-    float m_run = -INFINITY, l_run = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < nsub + ncl; i0 += SB_CHUNK) {
-        const int cnt = min(SB_CHUNK, nsub + ncl - i0);
-        __syncthreads();
-        for (int e = tid; e < cnt * 32; e += SB_THREADS) {  // value means, 16 B per thread
-            const int it = i0 + e / 32, k = e % 32;
-            const float *vb = it < nsub ? dv.sub_vbar + (g0 + it) * MOG_D
-                                        : dv.cl_vbar + ((size_t)u * dv.c_max + cA + (it - nsub)) * MOG_D;
-            cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * k), vb + 4 * k, 16);
+    // ---- 5. Gaussian residual partial: thread (g, quad) owns dims 4*quad..+3 of head
+    //         g = warp and, when G > 8, also of head warp + 8 ----
+    const int rq = tid & 31;
+    OnlineAcc st[2];
+    st[0].init();
+    st[1].init();
+    const int hA = warp, hB = warp + SB_THREADS / 32;
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int l = 0; l < nsub; ++l) {
+        if (snn[l] <= 0) continue;
+        const uint32_t need = hm & ~smask[l];
+        const float *vrow = vst + (size_t)l * MOG_D + 4 * rq;
+        if (hA < G && ((need >> hA) & 1u)) st[0].absorb(sres[hA][l] * LOG2E, vrow);
+        if (hB < G && ((need >> hB) & 1u)) st[1].absorb(sres[hB][l] * LOG2E, vrow);
+    }
+    for (int k0 = 0; k0 < ncl; k0 += SB_CHUNK) {
+        if (k0 > 0) {  // further chunks of the cluster slice (large C, few slots)
+            __syncthreads();
+            stage_clusters(k0);
+            cp_async_wait<0>();
+            __syncthreads();
         }
-        cp_async_commit();
-        for (int e = tid; e < cnt; e += SB_THREADS) {
-            const int it = i0 + e;
-            uint32_t need;
-            if (it < nsub) {
-                need = snn[it] > 0 ? (hm & ~smask[it]) : 0u;
-                for (int g = 0; g < G && g < GT; ++g) iex[e][g] = sres[g][it];
-            } else {
-                const int cc = cA + (it - nsub);
-                need = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~cselm[cc]) : 0u;
-                for (int g = 0; g < G && g < GT; ++g) iex[e][g] = cres[(size_t)g * dv.c_max + cc];
-            }
-            ineed[e] = need;
-        }
-        cp_async_wait<0>();
-        __syncthreads();
-        if (rg < G) {
-            for (int e = 0; e < cnt; ++e) {
-                if (!((ineed[e] >> rg) & 1u)) continue;
-                const float ex = iex[e][rg] * LOG2E;
-                if (ex > m_run) {
-                    const float sc = exp2f(m_run - ex);
-                    l_run *= sc;
-                    acc.x *= sc;
-                    acc.y *= sc;
-                    acc.z *= sc;
-                    acc.w *= sc;
-                    m_run = ex;
-                }
-                const float wgt = exp2f(ex - m_run);
-                const float4 v = *reinterpret_cast<const float4 *>(vst + (size_t)e * MOG_D + 4 * rq);
-                l_run += wgt;
-                acc.x += wgt * v.x;
-                acc.y += wgt * v.y;
-                acc.z += wgt * v.z;
-                acc.w += wgt * v.w;
-            }
+        const int cnt = min(SB_CHUNK, ncl - k0);
+        for (int e = 0; e < cnt; ++e) {
+            const float *vrow = vcl + (size_t)e * MOG_D + 4 * rq;
+            if (hA < G && ((ineed[e] >> hA) & 1u)) st[0].absorb(iex[e][hA] * LOG2E, vrow);
+            if (hB < G && ((ineed[e] >> hB) & 1u)) st[1].absorb(iex[e][hB < GT ? hB : 0] * LOG2E, vrow);
         }
     }
-    // heads beyond the 8 warps: loop (G <= 16)
-    float *rp2 = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS + j) * G * PART_W;
-    if (rg < G) {
-        float *r = rp2 + (size_t)rg * PART_W;
+    float *rbase = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS + j) * G * PART_W;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int g = k == 0 ? hA : hB;
+        if (g >= G) continue;
+        float *r = rbase + (size_t)g * PART_W;
         if (rq == 0) {
-            r[0] = m_run;
-            r[1] = l_run;
+            r[0] = st[k].m;
+            r[1] = st[k].l;
         }
-        *reinterpret_cast<float4 *>(r + PART_ACC + 4 * rq) = acc;
-    }
-    if (G > SB_THREADS / 32) {  // second pass for heads 8..15
-        for (int g2 = 8 + rg; g2 < G; g2 += 8) {
-            float m2 = -INFINITY, l2 = 0.f;
-            float4 a2 = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int i0 = 0; i0 < nsub + ncl; ++i0) {
-                uint32_t need;
-                float exv;
-                const float *vb;
-                if (i0 < nsub) {
-                    need = snn[i0] > 0 ? (hm & ~smask[i0]) : 0u;
-                    exv = sres[g2 < GT ? g2 : 0][i0];
-                    vb = dv.sub_vbar + (g0 + i0) * MOG_D;
-                } else {
-                    const int cc = cA + (i0 - nsub);
-                    need = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~cselm[cc]) : 0u;
-                    exv = cres[(size_t)g2 * dv.c_max + cc];
-                    vb = dv.cl_vbar + ((size_t)u * dv.c_max + cc) * MOG_D;
-                }
-                if (!((need >> g2) & 1u)) continue;
-                const float ex = exv * LOG2E;
-                if (ex > m2) {
-                    const float sc = exp2f(m2 - ex);
-                    l2 *= sc;
-                    a2.x *= sc;
-                    a2.y *= sc;
-                    a2.z *= sc;
-                    a2.w *= sc;
-                    m2 = ex;
-                }
-                const float wgt = exp2f(ex - m2);
-                const float4 v = *reinterpret_cast<const float4 *>(vb + 4 * rq);
-                l2 += wgt;
-                a2.x += wgt * v.x;
-                a2.y += wgt * v.y;
-                a2.z += wgt * v.z;
-                a2.w += wgt * v.w;
-            }
-            float *r = rp2 + (size_t)g2 * PART_W;
-            if (rq == 0) {
-                r[0] = m2;
-                r[1] = l2;
-            }
-            *reinterpret_cast<float4 *>(r + PART_ACC + 4 * rq) = a2;
-        }
+        *reinterpret_cast<float4 *>(r + PART_ACC + 4 * rq) = st[k].a;
     }
 }
 
 constexpr int SUPER = 256;  // rows resolved per pass
-constexpr int RB = 8;       // residual partials staged per pass in the attention kernel
+constexpr int RB = 2;       // residual partials staged per pass in the attention kernel
 
 // K3: grid (P, units).  Rows [p*T/P, (p+1)*T/P) of the unit's exact list (anchors first),
 // plus residual partials [p*R/P, (p+1)*R/P) from k_dec_sub, into one partial; the last CTA
@@ -490,8 +484,6 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     __shared__ int spos[SUPER];
     __shared__ uint32_t smk[SUPER];
     __shared__ int s_last;
-    pdl_wait();
-    pdl_trigger();
     const int u = blockIdx.y, p = blockIdx.x, P = dv.P;
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int b = ui[UI_B], h = u % dv.h_kv;
@@ -499,12 +491,18 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     const int nnow = dv.n_now[b];
     const int s_cnt = min(S, nnow), r_cnt = max(0, nnow - rlo);
     const int n_anchor = s_cnt + r_cnt;
-    const int Uc = dv.tc > 0 ? dv.ucount[u] : 0;
-    const int R = max(Uc, 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
-    float *stA = reinterpret_cast<float *>(asm_ + AT_SMEM);   // [AT_WARPS + RB][G][PART_W]
-    float *stR = stA + (size_t)AT_WARPS * G * PART_W;
+    uint32_t qa[8][4];
+    load_q_frags(qa, a.q + (size_t)u * G * MOG_D, G);
+    pdl_wait();  // below: outputs of the subcluster kernel
+    pdl_trigger();
+    const int Uc = dv.tc > 0 ? dv.ucount[u] : 0;
+    const int R = max(Uc, 1);
+    // shared memory: [tiles (AT_SMEM)][RB staged residual partials]; after the tile loop
+    // the warp states go right before the staged partials, at the end of the tile area
+    float *stR = reinterpret_cast<float *>(asm_ + AT_SMEM);
+    float *stA = stR - (size_t)AT_WARPS * G * PART_W;
     // residual partials of this CTA: fetch now, merge at the end
     const int ra = (int)((int64_t)R * p / P), rb = (int)((int64_t)R * (p + 1) / P);
     const float *rsrc = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS) * G * PART_W;
@@ -542,8 +540,6 @@ __global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
     const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
     const int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
     const uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
-    uint32_t qa[8][4];
-    load_q_frags(qa, a.q + (size_t)u * G * MOG_D, G);
     WarpAcc acc;
     acc.init();
     const float scale2 = dv.tau * LOG2E;
@@ -681,7 +677,7 @@ size_t sub_smem_bytes(int G, int c_max, int tc) {
     const int P1 = (int)ceil_div64(c_max, SC_SLICE);
     const size_t ncw = ((size_t)G * P1 * tc + 3) & ~(size_t)3;  // 16-byte multiples
     return sizeof(float) * 2 * ncw + sizeof(uint32_t) * ((c_max + 3) & ~3) +
-           sizeof(float) * SB_CHUNK * MOG_D;
+           sizeof(float) * (MOG_MAX_L + SB_CHUNK) * MOG_D;  // value means staged
 }
 
 template <int GT>
@@ -699,7 +695,7 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
     if ((e = launch_pdl(k_dec_sub<GT>, dim3(nslot, dv.units), dim3(SB_THREADS), sm2, s, a)) != cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
-    const size_t sm3 = AT_SMEM + sizeof(float) * (AT_WARPS + RB) * dv.G * PART_W;
+    const size_t sm3 = AT_SMEM + sizeof(float) * RB * dv.G * PART_W;
     if ((e = ensure_smem((const void *)k_dec_attend<GT>, sm3)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_dec_attend<GT>, dim3(dv.P, dv.units), dim3(AT_THREADS), sm3, s, a)) != cudaSuccess)
         return e;
