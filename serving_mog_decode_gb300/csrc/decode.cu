@@ -20,6 +20,8 @@
 //               first) through the attention engine, the Gaussian residual terms of a
 //               slice of the unselected groups, one partial per CTA; the last CTA of the
 //               unit merges the partials and normalises once.
+#include <algorithm>
+
 #include "attend.cuh"
 #include "internal.h"
 
@@ -182,462 +184,418 @@ __global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
     }
 }
 
-constexpr int SB_THREADS = 256;
-constexpr int SB_CHUNK = 32;  // cluster residual items staged per pass
+constexpr int SL_STAGES = 2;                  // tile buffers of the slot kernel
+constexpr int SL_SPLIT = 2;                   // CTAs per union slot (halves of its rows)
+constexpr int SL_ANCHOR = 2;                  // anchor CTAs per unit
+constexpr int SL_CHUNK = 32;                  // cluster residual items staged per pass
+constexpr int SUPER = 256;                    // row positions resolved per pass
+constexpr int SL_AREA = SL_STAGES * AT_STAGE_BYTES;  // 66 KB: selection / tiles / residual
 
-// K2: grid (max(1, min(c_max, G*tc)), units).  Every CTA merges the per-slice candidate
-// lists into each head's top-tc clusters (or takes the caller's selection), forms the union
-// over the G heads (ascending cluster index) and takes union slot j: subcluster scores,
-// top-ts per head that selected the cluster, the compacted exact rows, and the Gaussian
-// residual partial of (a) the unselected subclusters of its cluster and (b) a slice of the
-// clusters that some head did not select.
+// Bytes of the slot kernel's phase-shared area (selection tables, then tiles, then the
+// residual staging); the selection (G*tc ints) follows it.
+__host__ __device__ inline size_t slot_area_bytes(int G, int c_max, int tc) {
+    const int P1 = (int)ceil_div64(c_max, SC_SLICE);
+    const size_t ncw = ((size_t)G * P1 * tc + 3) & ~(size_t)3;
+    const size_t sel = sizeof(float) * 2 * ncw + sizeof(uint32_t) * ((c_max + 3) & ~3);
+    const size_t res = sizeof(float) * ((size_t)(AT_WARPS + 1) * G * PART_W + (MOG_MAX_L + SL_CHUNK) * MOG_D);
+    size_t m = sel > res ? sel : res;
+    m = m > (size_t)SL_AREA ? m : (size_t)SL_AREA;
+    return (m + 15) & ~(size_t)15;
+}
+
+size_t slot_smem_bytes(int G, int c_max, int tc) {
+    return slot_area_bytes(G, c_max, tc) + sizeof(int) * (((size_t)G * tc + 3) & ~(size_t)3);
+}
+
+// Attention over `nrows` rows whose positions/masks come from `resolve(i0, n)` (filling
+// spos/smk for rows i0..i0+n), SUPER rows at a time, two tile buffers.
+template <typename Resolve>
+__device__ __forceinline__ void slot_rows(WarpAcc &acc, const uint32_t (&qa)[8][4], uint8_t *area,
+                                          int nrows, const uint16_t *kb, const uint16_t *vb,
+                                          int64_t sn, int *spos, uint32_t *smk, float scale2,
+                                          Resolve resolve) {
+    for (int sb = 0; sb < nrows; sb += SUPER) {
+        const int ns = min(SUPER, nrows - sb);
+        resolve(sb, ns);
+        __syncthreads();
+        const int nt = (int)ceil_div64(ns, AT_ROWS);
+        auto issue = [&](int t) {
+            const int rb = t * AT_ROWS;
+            issue_tile(area + (t % SL_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, ns - rb), kb, vb, sn,
+                       [&](int r, int64_t &pos, uint32_t &mk) {
+                           pos = spos[rb + r];
+                           mk = smk[rb + r];
+                       });
+        };
+        issue(0);
+        cp_async_commit();
+        if (nt > 1) issue(1);
+        cp_async_commit();
+        for (int t = 0; t < nt; ++t) {
+            cp_async_wait<1>();
+            __syncthreads();
+            compute_tile(acc, qa, area + (t % SL_STAGES) * AT_STAGE_BYTES, scale2);
+            __syncthreads();
+            if (t + 2 < nt) issue(t + 2);
+            cp_async_commit();
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+    }
+}
+
+// K2: grid (SL_ANCHOR + SL_SPLIT * min(c_max, G*tc), units).
+//  - CTAs a < SL_ANCHOR attend to the anchor rows (sinks, recent and appended keys); they
+//    need nothing from the scoring kernel and run ahead of it.
+//  - CTA SL_ANCHOR + SL_SPLIT*j + part merges the per-slice candidate lists into every
+//    head's top-tc clusters (or takes the caller's selection), forms the union over the G
+//    heads (ascending cluster index) and takes union slot j: subcluster scores, top-ts per
+//    head that selected the cluster, then attention over `part`'s half of the members of
+//    the selected subclusters; part 0 adds the Gaussian residual of the unselected
+//    subclusters of that cluster and of a slice of the clusters some head did not select.
+//  Every CTA writes one partial (max, sum, acc); the last CTA of the unit merges them
+//  and normalises once.
 template <int GT>
-__global__ void __launch_bounds__(SB_THREADS) k_dec_sub(DecArgs a) {
-    extern __shared__ __align__(16) uint8_t sbm[];
+__global__ void __launch_bounds__(AT_THREADS) k_dec_slot(DecArgs a) {
+    extern __shared__ __align__(128) uint8_t area[];
     const Dev &dv = a.dv;
     const int G = dv.G, tc = dv.tc, ts = dv.ts;
-    const int u = blockIdx.y, j = blockIdx.x;
-    const int *ui = dv.unit_info + u * UI_STRIDE;
-    const int C = ui[UI_C], L = ui[UI_L];
-    const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
-    const int NC = P1 * tc;  // candidates per head
-    // dynamic shared memory, every region 16-byte aligned
-    const size_t ncw = ((size_t)G * NC + 3) & ~(size_t)3;
-    float *cand_s = reinterpret_cast<float *>(sbm);                        // [G][NC]
-    int *cand_i = reinterpret_cast<int *>(cand_s + ncw);                    // [G][NC]
-    uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + ncw);           // [c_max]
-    float *vst = reinterpret_cast<float *>(cselm + ((dv.c_max + 3) & ~3));  // [32 + SB_CHUNK][d]
-    float *vcl = vst + (size_t)MOG_MAX_L * MOG_D;
     __shared__ float4 w[GT * 64];
-    __shared__ int selc[GT][MOG_MAX_UNION];
     __shared__ float sres[GT][MOG_MAX_L];
     __shared__ float ssl[GT][MOG_MAX_L];
     __shared__ uint32_t smask[MOG_MAX_L];
     __shared__ int sso[MOG_MAX_L + 1], snn[MOG_MAX_L], spref[MOG_MAX_L + 1];
-    __shared__ float iex[SB_CHUNK][GT];
-    __shared__ uint32_t ineed[SB_CHUNK];
-    __shared__ int s_wcnt[SB_THREADS / 32], s_cj, s_uc;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
-    // ---- 0. before the dependency: weights, cleared tables ----
-    load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
-    for (int e = tid; e < G * MOG_MAX_UNION; e += SB_THREADS) selc[e / MOG_MAX_UNION][e % MOG_MAX_UNION] = -1;
-    for (int e = tid; e < C; e += SB_THREADS) cselm[e] = 0u;
-    if (tid < MOG_MAX_L) smask[tid] = 0u;
-    pdl_wait();
-    pdl_trigger();
-    // ---- 1. every head's top-tc clusters ----
-    if (tc > 0 && !a.sel_in) {
-        const size_t base = (size_t)u * G * NC;
-        for (int e = tid; e < G * NC; e += SB_THREADS) {
-            cp_async4(smem_u32(cand_s + e), a.cand_s + base + e);
-            cp_async4(smem_u32(cand_i + e), a.cand_i + base + e);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (tc > 0) {
-        if (a.sel_in) {
-            for (int e = tid; e < G * tc; e += SB_THREADS) {
-                const int g = e / tc, r = e % tc;
-                const int cc = a.sel_in[((size_t)u * G + g) * a.SW + r];
-                selc[g][r] = (cc >= 0 && cc < C && dv.cl_n[(size_t)u * dv.c_max + cc] > 0) ? cc : -1;
-            }
-        } else {
-            // element (g, list p, position r): its rank over all lists of head g is r plus,
-            // for every other list, the length of that list's prefix ranking before it
-            for (int e = tid; e < G * NC; e += SB_THREADS) {
-                const int g = e / NC, pr = e % NC, pl = pr / tc, r = pr % tc;
-                const float *cs = cand_s + (size_t)g * NC;
-                const int *ci = cand_i + (size_t)g * NC;
-                const int x = ci[pr];
-                if (x < 0) continue;
-                const float v = cs[pr];
-                int rank = r;
-                for (int q = 0; q < P1 && rank < tc; ++q) {
-                    if (q == pl) continue;
-                    int lo = 0, hi = tc;  // first position not ranking before (v, x)
-                    while (lo < hi) {
-                        const int mid = (lo + hi) >> 1;
-                        const int xm = ci[q * tc + mid];
-                        if (xm >= 0 && ranks_before(cs[q * tc + mid], xm, v, x)) lo = mid + 1;
-                        else hi = mid;
-                    }
-                    rank += lo;
-                }
-                if (rank < tc) selc[g][rank] = x;
-            }
-        }
-    }
-    __syncthreads();
-    for (int e = tid; e < G * tc; e += SB_THREADS) {
-        const int cc = selc[e / tc][e % tc];
-        if (cc >= 0) atomicOr(&cselm[cc], 1u << (e / tc));
-    }
-    __syncthreads();
-    // ---- 2. union over the heads, ascending; this CTA's slot ----
-    {
-        const int per = (int)ceil_div64(C, SB_THREADS);
-        const int cA = tid * per, cB = min(C, cA + per);
-        int cnt = 0;
-        for (int cc = cA; cc < cB; ++cc) cnt += cselm[cc] != 0u;
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) s_wcnt[warp] = incl;
-        __syncthreads();
-        int base = incl - cnt;
-        for (int k = 0; k < warp; ++k) base += s_wcnt[k];
-        if (tid == SB_THREADS - 1) s_uc = base + cnt;
-        if (j >= base && j < base + cnt) {
-            int k = base;
-            for (int cc = cA; cc < cB; ++cc)
-                if (cselm[cc]) {
-                    if (k == j) s_cj = cc;
-                    ++k;
-                }
-        }
-    }
-    __syncthreads();
-    const int Uc = s_uc;
-    const int R = max(Uc, 1);
-    if (j >= R) return;
-    const bool has_slot = j < Uc;
-    const int c = has_slot ? s_cj : 0;
-    const uint32_t hm = has_slot ? cselm[c] : 0u;
-    int *selu = dv.sel + (size_t)u * G * a.SW;
-    if (j == 0) {
-        if (tid == 0) dv.ucount[u] = Uc;
-        for (int e = tid; e < G * tc; e += SB_THREADS) {
-            const int g = e / tc, r = e % tc;
-            selu[(size_t)g * a.SW + r] = selc[g][r];
-            if (selc[g][r] < 0)
-                for (int k = 0; k < ts; ++k) selu[(size_t)g * a.SW + tc + r * ts + k] = -1;
-        }
-    }
-    // ---- 3. one batch of loads: subcluster summaries and value means, the first chunk of
-    //         the cluster residual slice ----
-    const size_t g0 = (size_t)u * dv.c_max * dv.l_max + (size_t)c * L;
-    const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
-    const int nsub = (dv.residual && has_slot) ? L : 0;
-    const int cA = (int)((int64_t)C * j / R), cB = (int)((int64_t)C * (j + 1) / R);
-    const int ncl = dv.residual ? cB - cA : 0;
-    const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
-    auto stage_clusters = [&](int k0) {  // cluster items k0 .. k0 + SB_CHUNK of the slice
-        const int cnt = min(SB_CHUNK, ncl - k0);
-        for (int e = tid; e < cnt * 32; e += SB_THREADS) {
-            const int cc = cA + k0 + e / 32, k = e % 32;
-            cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * k),
-                       dv.cl_vbar + ((size_t)u * dv.c_max + cc) * MOG_D + 4 * k, 16);
-        }
-        cp_async_commit();
-        for (int e = tid; e < cnt; e += SB_THREADS) {
-            const int cc = cA + k0 + e;
-            ineed[e] = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~cselm[cc]) : 0u;
-#pragma unroll
-            for (int g = 0; g < GT; ++g)
-                if (g < G) iex[e][g] = cres[(size_t)g * dv.c_max + cc];
-        }
-    };
-    if (nsub > 0)
-        for (int e = tid; e < L * 32; e += SB_THREADS)
-            cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
-                       dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
-    if (ncl > 0) stage_clusters(0);
-    else cp_async_commit();
-    if (has_slot) {
-        if (tid <= L) sso[tid] = so[tid];
-        if (tid < L) snn[tid] = dv.sub_n[g0 + tid];
-        const int l = tid >> 2;
-        const bool valid = l < L;
-        float res[GT], sl[GT];
-        quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D,
-                        valid ? dv.sub_n[g0 + l] : 0, valid, w, G, dv.score_mode, res, sl);
-        if (valid && (tid & 3) == 0) {
-#pragma unroll
-            for (int g = 0; g < GT; ++g)
-                if (g < G) {
-                    sres[g][l] = res[g];
-                    ssl[g][l] = sl[g];
-                }
-        }
-    }
-    __syncthreads();
-    // ---- 4. top-ts subclusters per head that selected c; compacted exact rows ----
-    if (has_slot) {
-        for (int g = warp; g < G; g += SB_THREADS / 32) {
-            if (!((hm >> g) & 1u)) continue;
-            int rk = -1;
-            for (int r = 0; r < tc; ++r)
-                if (selc[g][r] == c) { rk = r; break; }
-            if (rk < 0) continue;
-            int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
-            if (a.sel_in) {
-                const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + tc + (size_t)rk * ts;
-                for (int r = lane; r < ts; r += 32) {
-                    const int l2 = si[r];
-                    const bool ok = l2 >= 0 && l2 < L && snn[l2] > 0;
-                    subs[r] = ok ? l2 : -1;
-                    if (ok) atomicOr(&smask[l2], 1u << g);
-                }
-            } else {
-                for (int r = lane; r < ts; r += 32) subs[r] = -1;
-                __syncwarp();
-                const float v = lane < L ? ssl[g][lane] : -INFINITY;
-                int rank = 0;
-                for (int k = 0; k < L; ++k) rank += ranks_before(ssl[g][k], k, v, lane);
-                if (lane < L && v != -INFINITY && rank < ts) {
-                    subs[rank] = lane;
-                    atomicOr(&smask[lane], 1u << g);
-                }
-            }
-        }
-        __syncthreads();
-        if (warp == 0) {  // prefix of the selected subclusters' sizes
-            const int cnt = lane < L && smask[lane] ? sso[lane + 1] - sso[lane] : 0;
-            int incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane < L) spref[lane + 1] = incl;
-            if (lane == 0) {
-                spref[0] = 0;
-                dv.slotcoff[(size_t)u * MOG_MAX_UNION + j] = sso[0];
-            }
-            if (lane == L - 1) dv.slotcnt[(size_t)u * MOG_MAX_UNION + j] = incl;
-        }
-        __syncthreads();
-        const int tot = spref[L];
-        const int *perm = dv.perm + (size_t)u * dv.n_cap;
-        int *rp = dv.rowpos + (size_t)u * dv.n_cap + sso[0];
-        uint32_t *rm = dv.rowmask + (size_t)u * dv.n_cap + sso[0];
-        for (int i = tid; i < tot; i += SB_THREADS) {
-            int k = 0;
-            while (spref[k + 1] <= i) ++k;
-            rp[i] = perm[sso[k] + (i - spref[k])];
-            rm[i] = smask[k];
-        }
-    }
-    // ---- 5. Gaussian residual partial: thread (g, quad) owns dims 4*quad..+3 of head
-    //         g = warp and, when G > 8, also of head warp + 8 ----
-    const int rq = tid & 31;
-    OnlineAcc st[2];
-    st[0].init();
-    st[1].init();
-    const int hA = warp, hB = warp + SB_THREADS / 32;
-    cp_async_wait<0>();
-    __syncthreads();
-    for (int l = 0; l < nsub; ++l) {
-        if (snn[l] <= 0) continue;
-        const uint32_t need = hm & ~smask[l];
-        const float *vrow = vst + (size_t)l * MOG_D + 4 * rq;
-        if (hA < G && ((need >> hA) & 1u)) st[0].absorb(sres[hA][l] * LOG2E, vrow);
-        if (hB < G && ((need >> hB) & 1u)) st[1].absorb(sres[hB][l] * LOG2E, vrow);
-    }
-    for (int k0 = 0; k0 < ncl; k0 += SB_CHUNK) {
-        if (k0 > 0) {  // further chunks of the cluster slice (large C, few slots)
-            __syncthreads();
-            stage_clusters(k0);
-            cp_async_wait<0>();
-            __syncthreads();
-        }
-        const int cnt = min(SB_CHUNK, ncl - k0);
-        for (int e = 0; e < cnt; ++e) {
-            const float *vrow = vcl + (size_t)e * MOG_D + 4 * rq;
-            if (hA < G && ((ineed[e] >> hA) & 1u)) st[0].absorb(iex[e][hA] * LOG2E, vrow);
-            if (hB < G && ((ineed[e] >> hB) & 1u)) st[1].absorb(iex[e][hB < GT ? hB : 0] * LOG2E, vrow);
-        }
-    }
-    float *rbase = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS + j) * G * PART_W;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int g = k == 0 ? hA : hB;
-        if (g >= G) continue;
-        float *r = rbase + (size_t)g * PART_W;
-        if (rq == 0) {
-            r[0] = st[k].m;
-            r[1] = st[k].l;
-        }
-        *reinterpret_cast<float4 *>(r + PART_ACC + 4 * rq) = st[k].a;
-    }
-}
-
-constexpr int SUPER = 256;  // rows resolved per pass
-constexpr int RB = 2;       // residual partials staged per pass in the attention kernel
-
-// K3: grid (P, units).  Rows [p*T/P, (p+1)*T/P) of the unit's exact list (anchors first),
-// plus residual partials [p*R/P, (p+1)*R/P) from k_dec_sub, into one partial; the last CTA
-// of the unit merges the P partials and normalises once.
-template <int GT>
-__global__ void __launch_bounds__(AT_THREADS) k_dec_attend(DecArgs a) {
-    extern __shared__ __align__(128) uint8_t asm_[];
-    const Dev &dv = a.dv;
-    const int G = dv.G;
-    __shared__ int spre[MOG_MAX_UNION + 1];
-    __shared__ int scoff[MOG_MAX_UNION];
     __shared__ int spos[SUPER];
     __shared__ uint32_t smk[SUPER];
-    __shared__ int s_last;
-    const int u = blockIdx.y, p = blockIdx.x, P = dv.P;
-    const int *ui = dv.unit_info + u * UI_STRIDE;
-    const int b = ui[UI_B], h = u % dv.h_kv;
-    const int S = ui[UI_S], rlo = ui[UI_RLO];
-    const int nnow = dv.n_now[b];
-    const int s_cnt = min(S, nnow), r_cnt = max(0, nnow - rlo);
-    const int n_anchor = s_cnt + r_cnt;
+    __shared__ float iex[SL_CHUNK][GT];
+    __shared__ uint32_t ineed[SL_CHUNK];
+    __shared__ int s_wcnt[AT_WARPS], s_cj, s_uc, s_last;
+    const int u = blockIdx.y, r = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int b = ui[UI_B], h = u % dv.h_kv, C = ui[UI_C], L = ui[UI_L];
+    const int S = ui[UI_S], rlo = ui[UI_RLO];
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
+    const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
+    const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
+    const float scale2 = dv.tau * LOG2E;
     uint32_t qa[8][4];
     load_q_frags(qa, a.q + (size_t)u * G * MOG_D, G);
-    pdl_wait();  // below: outputs of the subcluster kernel
-    pdl_trigger();
-    const int Uc = dv.tc > 0 ? dv.ucount[u] : 0;
-    const int R = max(Uc, 1);
-    // shared memory: [tiles (AT_SMEM)][RB staged residual partials]; after the tile loop
-    // the warp states go right before the staged partials, at the end of the tile area
-    float *stR = reinterpret_cast<float *>(asm_ + AT_SMEM);
-    float *stA = stR - (size_t)AT_WARPS * G * PART_W;
-    // residual partials of this CTA: fetch now, merge at the end
-    const int ra = (int)((int64_t)R * p / P), rb = (int)((int64_t)R * (p + 1) / P);
-    const float *rsrc = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS) * G * PART_W;
-    {
-        const int cnt = min(RB, rb - ra);
-        for (int q = tid; q < cnt * G * PART_W / 4; q += AT_THREADS)
-            cp_async16(smem_u32(stR + 4 * q), rsrc + (size_t)ra * G * PART_W + 4 * q, 16);
-        cp_async_commit();
-    }
-    if (warp == 0) {  // slot prefix over <= 256 slots
-        int run = n_anchor;
-        for (int j0 = 0; j0 < Uc; j0 += 32) {
-            const int j = j0 + lane;
-            int cnt = 0;
-            if (j < Uc) {
-                const size_t sj = (size_t)u * MOG_MAX_UNION + j;
-                cnt = dv.slotcnt[sj];
-                scoff[j] = dv.slotcoff[sj];
+    WarpAcc acc;
+    acc.init();
+    float *states = reinterpret_cast<float *>(area);  // after the tiles: [AT_WARPS + 1][G][PART_W]
+    float *part_out;
+    bool has_res = false;
+    if (r < SL_ANCHOR) {
+        // ------------------------------- anchors ---------------------------------------
+        pdl_trigger();
+        const int nnow = dv.n_now[b];
+        const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
+        const int i0 = (int)((int64_t)n_anchor * r / SL_ANCHOR), i1 = (int)((int64_t)n_anchor * (r + 1) / SL_ANCHOR);
+        slot_rows(acc, qa, area, i1 - i0, kb, vb, dv.sn, spos, smk, scale2, [&](int sb, int ns) {
+            for (int t = tid; t < ns; t += AT_THREADS) {
+                const int i = i0 + sb + t;
+                spos[t] = i < s_cnt ? i : rlo + (i - s_cnt);
+                smk[t] = allm;
             }
+        });
+        part_out = dv.partials + ((size_t)u * PART_SLOTS + r) * G * PART_W;
+    } else {
+        // ------------------------------- a union slot -----------------------------------
+        const int j = (r - SL_ANCHOR) / SL_SPLIT, part = (r - SL_ANCHOR) % SL_SPLIT;
+        const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
+        const int NC = P1 * tc;
+        const size_t ncw = ((size_t)G * NC + 3) & ~(size_t)3;
+        float *cand_s = reinterpret_cast<float *>(area);                       // [G][NC]
+        int *cand_i = reinterpret_cast<int *>(cand_s + ncw);                    // [G][NC]
+        uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + ncw);           // [c_max]
+        // the selection itself outlives the shared area (tiles reuse it): tail region
+        int *selc = reinterpret_cast<int *>(area + slot_area_bytes(G, dv.c_max, tc));  // [G][tc]
+        load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
+        for (int e = tid; e < G * tc; e += AT_THREADS) selc[e] = -1;
+        for (int e = tid; e < C; e += AT_THREADS) cselm[e] = 0u;
+        if (tid < MOG_MAX_L) smask[tid] = 0u;
+        pdl_wait();  // candidate lists of the scoring kernel
+        pdl_trigger();
+        if (tc > 0 && !a.sel_in) {
+            const size_t base = (size_t)u * G * NC;
+            for (int e = tid; e < G * NC; e += AT_THREADS) {
+                cp_async4(smem_u32(cand_s + e), a.cand_s + base + e);
+                cp_async4(smem_u32(cand_i + e), a.cand_i + base + e);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        if (tc > 0) {
+            if (a.sel_in) {
+                for (int e = tid; e < G * tc; e += AT_THREADS) {
+                    const int g = e / tc, rr = e % tc;
+                    const int cc = a.sel_in[((size_t)u * G + g) * a.SW + rr];
+                    selc[g * tc + rr] =
+                        (cc >= 0 && cc < C && dv.cl_n[(size_t)u * dv.c_max + cc] > 0) ? cc : -1;
+                }
+            } else {
+                // element (g, list p, position r): its rank over all lists of head g is r
+                // plus, for every other list, the length of that list's prefix ranking
+                // before it
+                for (int e = tid; e < G * NC; e += AT_THREADS) {
+                    const int g = e / NC, pr = e % NC, pl = pr / tc, rr = pr % tc;
+                    const float *cs = cand_s + (size_t)g * NC;
+                    const int *ci = cand_i + (size_t)g * NC;
+                    const int x = ci[pr];
+                    if (x < 0) continue;
+                    const float v = cs[pr];
+                    int rank = rr;
+                    for (int q = 0; q < P1 && rank < tc; ++q) {
+                        if (q == pl) continue;
+                        int lo = 0, hi = tc;  // first position not ranking before (v, x)
+                        while (lo < hi) {
+                            const int mid = (lo + hi) >> 1;
+                            const int xm = ci[q * tc + mid];
+                            if (xm >= 0 && ranks_before(cs[q * tc + mid], xm, v, x)) lo = mid + 1;
+                            else hi = mid;
+                        }
+                        rank += lo;
+                    }
+                    if (rank < tc) selc[g * tc + rank] = x;
+                }
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < G * tc; e += AT_THREADS) {
+            const int cc = selc[(e / tc) * tc + e % tc];
+            if (cc >= 0) atomicOr(&cselm[cc], 1u << (e / tc));
+        }
+        __syncthreads();
+        {  // union over the heads, ascending; this CTA's slot
+            const int per = (int)ceil_div64(C, AT_THREADS);
+            const int cA = tid * per, cB = min(C, cA + per);
+            int cnt = 0;
+            for (int cc = cA; cc < cB; ++cc) cnt += cselm[cc] != 0u;
             int incl = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            if (j < Uc) spre[j] = run + incl - cnt;
-            run += __shfl_sync(0xffffffffu, incl, 31);
+            if (lane == 31) s_wcnt[warp] = incl;
+            __syncthreads();
+            int base = incl - cnt;
+            for (int k = 0; k < warp; ++k) base += s_wcnt[k];
+            if (tid == AT_THREADS - 1) s_uc = base + cnt;
+            if (j >= base && j < base + cnt) {
+                int k = base;
+                for (int cc = cA; cc < cB; ++cc)
+                    if (cselm[cc]) {
+                        if (k == j) s_cj = cc;
+                        ++k;
+                    }
+            }
         }
-        if (lane == 0) spre[Uc] = run;
-    }
-    __syncthreads();
-    const int T = spre[Uc];
-    const int r0 = (int)((int64_t)T * p / P), r1 = (int)((int64_t)T * (p + 1) / P);
-    const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
-    const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
-    const int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
-    const uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
-    WarpAcc acc;
-    acc.init();
-    const float scale2 = dv.tau * LOG2E;
-    int sbase = r0, ns = 0, nt = 0;
-    auto resolve = [&]() {
-        ns = min(SUPER, r1 - sbase);
-        for (int t = tid; t < ns; t += AT_THREADS) {
-            const int i = sbase + t;
-            int pos;
-            uint32_t mk;
-            if (i < n_anchor) {
-                pos = i < s_cnt ? i : rlo + (i - s_cnt);
-                mk = allm;
-            } else {
-                int lo = 0, hi = Uc - 1;  // last slot with spre[slot] <= i
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (spre[mid] <= i) lo = mid;
-                    else hi = mid - 1;
+        __syncthreads();
+        const int Uc = s_uc, R = max(Uc, 1);
+        part_out = nullptr;
+        if (j < R) {
+            part_out = dv.partials + ((size_t)u * PART_SLOTS + r) * G * PART_W;
+            const bool has_slot = j < Uc;
+            const int c = has_slot ? s_cj : 0;
+            const uint32_t hm = has_slot ? cselm[c] : 0u;
+            int *selu = dv.sel + (size_t)u * G * a.SW;
+            if (j == 0 && part == 0) {
+                if (tid == 0) dv.ucount[u] = Uc;
+                for (int e = tid; e < G * tc; e += AT_THREADS) {
+                    const int g = e / tc, rr = e % tc;
+                    const int cc = selc[g * tc + rr];
+                    selu[(size_t)g * a.SW + rr] = cc;
+                    if (cc < 0)
+                        for (int k = 0; k < ts; ++k) selu[(size_t)g * a.SW + tc + rr * ts + k] = -1;
                 }
-                const int k = scoff[lo] + (i - spre[lo]);
-                pos = rowpos[k];
-                mk = rowmask[k];
             }
-            if ((unsigned)pos >= (unsigned)dv.n_cap) {  // corrupt row list: flag, skip
-                flag_error(dv.status, ST_BAD_INDEX);
-                pos = 0;
-                mk = 0u;
-            }
-            spos[t] = pos;
-            smk[t] = mk;
-        }
-        __syncthreads();
-        nt = (int)ceil_div64(ns, AT_ROWS);
-    };
-    auto issue = [&](int t) {
-        const int rbs = t * AT_ROWS;
-        issue_tile(asm_ + (t % AT_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, ns - rbs), kb, vb, dv.sn,
-                   [&](int r, int64_t &pos, uint32_t &mk) {
-                       pos = spos[rbs + r];
-                       mk = smk[rbs + r];
-                   });
-    };
-    while (sbase < r1) {
-        resolve();
+            const size_t g0 = (size_t)u * dv.c_max * dv.l_max + (size_t)c * L;
+            const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
+            int nrows = 0, row0 = 0;
+            if (has_slot) {
+                if (tid <= L) sso[tid] = so[tid];
+                if (tid < L) snn[tid] = dv.sub_n[g0 + tid];
+                const int l = tid >> 2;
+                const bool valid = l < L;
+                float res[GT], sl[GT];
+                quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D,
+                                valid ? dv.sub_n[g0 + l] : 0, valid, w, G, dv.score_mode, res, sl);
+                if (valid && (tid & 3) == 0) {
 #pragma unroll
-        for (int s = 0; s < AT_STAGES - 1; ++s) {
-            if (s < nt) issue(s);
-            cp_async_commit();
+                    for (int g = 0; g < GT; ++g)
+                        if (g < G) {
+                            sres[g][l] = res[g];
+                            ssl[g][l] = sl[g];
+                        }
+                }
+                __syncthreads();
+                for (int g = warp; g < G; g += AT_WARPS) {  // top-ts of each head that chose c
+                    if (!((hm >> g) & 1u)) continue;
+                    int rk = -1;
+                    for (int rr = 0; rr < tc; ++rr)
+                        if (selc[g * tc + rr] == c) { rk = rr; break; }
+                    if (rk < 0) continue;
+                    int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
+                    if (a.sel_in) {
+                        const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + tc + (size_t)rk * ts;
+                        for (int rr = lane; rr < ts; rr += 32) {
+                            const int l2 = si[rr];
+                            const bool ok = l2 >= 0 && l2 < L && snn[l2] > 0;
+                            if (part == 0) subs[rr] = ok ? l2 : -1;
+                            if (ok) atomicOr(&smask[l2], 1u << g);
+                        }
+                    } else {
+                        if (part == 0)
+                            for (int rr = lane; rr < ts; rr += 32) subs[rr] = -1;
+                        __syncwarp();
+                        const float v = lane < L ? ssl[g][lane] : -INFINITY;
+                        int rank = 0;
+                        for (int k = 0; k < L; ++k) rank += ranks_before(ssl[g][k], k, v, lane);
+                        if (lane < L && v != -INFINITY && rank < ts) {
+                            if (part == 0) subs[rank] = lane;
+                            atomicOr(&smask[lane], 1u << g);
+                        }
+                    }
+                }
+                __syncthreads();
+                if (warp == 0) {  // prefix of the selected subclusters' sizes
+                    const int cnt = lane < L && smask[lane] ? sso[lane + 1] - sso[lane] : 0;
+                    int incl = cnt;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (lane < L) spref[lane + 1] = incl;
+                    if (lane == 0) spref[0] = 0;
+                }
+                __syncthreads();
+                const int T = spref[L];
+                row0 = (int)((int64_t)T * part / SL_SPLIT);
+                nrows = (int)((int64_t)T * (part + 1) / SL_SPLIT) - row0;
+            }
+            // ---------------- exact rows of this half ----------------
+            const int *perm = dv.perm + (size_t)u * dv.n_cap;
+            slot_rows(acc, qa, area, nrows, kb, vb, dv.sn, spos, smk, scale2, [&](int sb, int ns) {
+                for (int t = tid; t < ns; t += AT_THREADS) {
+                    const int i = row0 + sb + t;
+                    int k = 0;
+                    while (spref[k + 1] <= i) ++k;
+                    int pos = perm[sso[k] + (i - spref[k])];
+                    uint32_t mk = smask[k];
+                    if ((unsigned)pos >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
+                        flag_error(dv.status, ST_BAD_INDEX);
+                        pos = 0;
+                        mk = 0u;
+                    }
+                    spos[t] = pos;
+                    smk[t] = mk;
+                }
+            });
+            // ---------------- Gaussian residual (part 0) ----------------
+            if (part == 0 && dv.residual) {
+                has_res = true;
+                float *vst = states + (size_t)(AT_WARPS + 1) * G * PART_W;  // [32 + SL_CHUNK][d]
+                float *vcl = vst + (size_t)MOG_MAX_L * MOG_D;
+                const int nsub = has_slot ? L : 0;
+                const int cA = (int)((int64_t)C * j / R), cB = (int)((int64_t)C * (j + 1) / R);
+                const int ncl = cB - cA;
+                const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
+                auto stage_clusters = [&](int k0) {
+                    const int cnt = min(SL_CHUNK, ncl - k0);
+                    for (int e = tid; e < cnt * 32; e += AT_THREADS) {
+                        const int cc = cA + k0 + e / 32, k = e % 32;
+                        cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * k),
+                                   dv.cl_vbar + ((size_t)u * dv.c_max + cc) * MOG_D + 4 * k, 16);
+                    }
+                    cp_async_commit();
+                    for (int e = tid; e < cnt; e += AT_THREADS) {
+                        const int cc = cA + k0 + e;
+                        uint32_t chose = 0u;  // heads that selected cc
+                        for (int q = 0; q < G * tc; ++q)
+                            if (selc[q] == cc) chose |= 1u << (q / tc);
+                        ineed[e] = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~chose) : 0u;
+#pragma unroll
+                        for (int g = 0; g < GT; ++g)
+                            if (g < G) iex[e][g] = cres[(size_t)g * dv.c_max + cc];
+                    }
+                };
+                for (int e = tid; e < nsub * 32; e += AT_THREADS)
+                    cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
+                               dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
+                if (ncl > 0) stage_clusters(0);
+                else cp_async_commit();
+                cp_async_wait<0>();
+                __syncthreads();
+                // thread (warp, lane) owns dims 4*lane..+3 of heads warp, warp + 4, ...
+                OnlineAcc st[MOG_MAX_G / AT_WARPS];
+#pragma unroll
+                for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) st[k].init();
+                for (int l = 0; l < nsub; ++l) {
+                    if (snn[l] <= 0) continue;
+                    const uint32_t need = hm & ~smask[l];
+                    const float *vrow = vst + (size_t)l * MOG_D + 4 * lane;
+#pragma unroll
+                    for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) {
+                        const int g = warp + AT_WARPS * k;
+                        if (g < G && ((need >> g) & 1u)) st[k].absorb(sres[g < GT ? g : 0][l] * LOG2E, vrow);
+                    }
+                }
+                for (int k0 = 0; k0 < ncl; k0 += SL_CHUNK) {
+                    if (k0 > 0) {
+                        __syncthreads();
+                        stage_clusters(k0);
+                        cp_async_wait<0>();
+                        __syncthreads();
+                    }
+                    const int cnt = min(SL_CHUNK, ncl - k0);
+                    for (int e = 0; e < cnt; ++e) {
+                        const float *vrow = vcl + (size_t)e * MOG_D + 4 * lane;
+#pragma unroll
+                        for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) {
+                            const int g = warp + AT_WARPS * k;
+                            if (g < G && ((ineed[e] >> g) & 1u)) st[k].absorb(iex[e][g < GT ? g : 0] * LOG2E, vrow);
+                        }
+                    }
+                }
+                float *rs = states + (size_t)AT_WARPS * G * PART_W;  // state AT_WARPS
+#pragma unroll
+                for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) {
+                    const int g = warp + AT_WARPS * k;
+                    if (g >= G) continue;
+                    float *o = rs + (size_t)g * PART_W;
+                    if (lane == 0) {
+                        o[0] = st[k].m;
+                        o[1] = st[k].l;
+                    }
+                    *reinterpret_cast<float4 *>(o + PART_ACC + 4 * lane) = st[k].a;
+                }
+            }
         }
-        for (int t = 0; t < nt; ++t) {
-            cp_async_wait<AT_STAGES - 2>();
-            __syncthreads();
-            if (t + AT_STAGES - 1 < nt) issue(t + AT_STAGES - 1);
-            cp_async_commit();
-            compute_tile(acc, qa, asm_ + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
-        }
-        cp_async_wait<0>();
-        __syncthreads();
-        sbase += SUPER;
     }
-    cp_async_wait<0>();
-    warp_state_out(acc, stA, G);
-    __syncthreads();
-    float *part = dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W;
-    const int nres = max(0, min(RB, rb - ra));
-    if (rb - ra <= RB) {
-        merge_states(stA, AT_WARPS + nres, G, part);  // stA and stR are contiguous
-    } else {
-        // more residual partials than one stage: fold them in RB at a time through the
-        // (now free) tile area: run[0] holds the running state, run[1..] the staged chunk
-        float *run = reinterpret_cast<float *>(asm_);
-        float *tmp = run + (size_t)(1 + RB) * G * PART_W;
-        merge_states(stA, AT_WARPS + nres, G, tmp);
-        for (int k0 = ra + RB; k0 < rb; k0 += RB) {
-            __syncthreads();
-            for (int q = tid; q < G * PART_W; q += AT_THREADS) run[q] = tmp[q];
-            const int cnt = min(RB, rb - k0);
-            for (int q = tid; q < cnt * G * PART_W / 4; q += AT_THREADS)
-                cp_async16(smem_u32(run + (size_t)G * PART_W + 4 * q), rsrc + (size_t)k0 * G * PART_W + 4 * q, 16);
-            cp_async_commit();
-            cp_async_wait<0>();
-            __syncthreads();
-            merge_states(run, 1 + cnt, G, k0 + RB >= rb ? part : tmp);
-        }
+    // ------------------- this CTA's partial; the unit's last CTA merges ------------------
+    if (part_out) {
+        warp_state_out(acc, states, G);
+        __syncthreads();
+        merge_states(states, AT_WARPS + (has_res ? 1 : 0), G, part_out);
     }
     __threadfence();
     __syncthreads();
     if (tid == 0) {
         const unsigned t = atomicAdd(dv.counters + u * 4 + 1, 1u);
-        s_last = (t == (unsigned)P - 1);
+        s_last = (t == gridDim.x - 1);
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
     if (tid == 0) dv.counters[u * 4 + 1] = 0u;
-    merge_global_out(dv.partials + (size_t)u * PART_SLOTS * G * PART_W, P, G,
-                     reinterpret_cast<float *>(asm_), AT_SMEM / 4, a.out + (size_t)u * G * MOG_D);
+    const int Uc = dv.tc > 0 ? __ldcg(dv.ucount + u) : 0;
+    const int nparts = SL_ANCHOR + SL_SPLIT * max(Uc, 1);
+    merge_global_out(dv.partials + (size_t)u * PART_SLOTS * G * PART_W, nparts, G,
+                     reinterpret_cast<float *>(area), SL_AREA / 4, a.out + (size_t)u * G * MOG_D);
 }
 
 // Append one token per sequence at position n_now[b], then advance n_now[b].
@@ -673,13 +631,6 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cuda
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-size_t sub_smem_bytes(int G, int c_max, int tc) {
-    const int P1 = (int)ceil_div64(c_max, SC_SLICE);
-    const size_t ncw = ((size_t)G * P1 * tc + 3) & ~(size_t)3;  // 16-byte multiples
-    return sizeof(float) * 2 * ncw + sizeof(uint32_t) * ((c_max + 3) & ~3) +
-           sizeof(float) * (MOG_MAX_L + SB_CHUNK) * MOG_D;  // value means staged
-}
-
 template <int GT>
 static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t const *events) {
     const Dev &dv = a.dv;
@@ -689,16 +640,13 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
     if ((e = launch_pdl(k_dec_score<GT>, dim3(P1, dv.units), dim3(SC_THREADS), 0, s, a)) != cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
-    const size_t sm2 = sub_smem_bytes(dv.G, dv.c_max, dv.tc);
-    if ((e = ensure_smem((const void *)k_dec_sub<GT>, sm2)) != cudaSuccess) return e;
+    const size_t sm = slot_smem_bytes(dv.G, dv.c_max, dv.tc);
+    if ((e = ensure_smem((const void *)k_dec_slot<GT>, sm)) != cudaSuccess) return e;
     const int nslot = max(1, min(dv.c_max, dv.G * dv.tc));
-    if ((e = launch_pdl(k_dec_sub<GT>, dim3(nslot, dv.units), dim3(SB_THREADS), sm2, s, a)) != cudaSuccess)
+    if ((e = launch_pdl(k_dec_slot<GT>, dim3(SL_ANCHOR + SL_SPLIT * nslot, dv.units), dim3(AT_THREADS), sm, s,
+                        a)) != cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
-    const size_t sm3 = AT_SMEM + sizeof(float) * RB * dv.G * PART_W;
-    if ((e = ensure_smem((const void *)k_dec_attend<GT>, sm3)) != cudaSuccess) return e;
-    if ((e = launch_pdl(k_dec_attend<GT>, dim3(dv.P, dv.units), dim3(AT_THREADS), sm3, s, a)) != cudaSuccess)
-        return e;
     if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     return cudaSuccess;
 }

@@ -13,7 +13,7 @@ enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
 
 constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
 constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
-constexpr int PART_SLOTS = MAX_SPLITS + 256;  // + residual partials (one per union slot)
+constexpr int PART_SLOTS = 4 + 2 * 256;  // partials per unit: anchor CTAs + 2 per union slot
 constexpr int MAX_C = 4096;        // clusters per unit supported
 
 // Typed view of an arena, passed by value to every kernel.
@@ -83,7 +83,7 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
                          int G, const void *q, float *out, float *scratch, int splits,
                          cudaStream_t s);
 int dense_splits(int units, int n_max);
-size_t sub_smem_bytes(int G, int c_max, int tc);
+size_t slot_smem_bytes(int G, int c_max, int tc);
 cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
                              int32_t *assign, int *changed, int *fb_list, int *fb_cnt,
                              cudaStream_t s);
