@@ -84,6 +84,14 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// wait until at most n (runtime, 0..3) cp.async groups are pending
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+    if (n <= 0) cp_async_wait<0>();
+    else if (n == 1) cp_async_wait<1>();
+    else if (n == 2) cp_async_wait<2>();
+    else cp_async_wait<3>();
+}
+
 // read-only 16-byte global load, not kept in L1
 __device__ __forceinline__ uint4 ldg_nc16(const void *p) {
     uint4 r;

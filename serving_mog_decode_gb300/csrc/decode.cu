@@ -8,19 +8,24 @@
 // (sink/tail anchors attended exactly; exact and estimated numerator and denominator
 // added in the unnormalised domain, one normalisation).
 //
-//  k_dec_score  (units x P1 CTAs): log-mass score of every cluster for the G query heads
-//               of a KV head, s = ln n + tau q.mu + tau^2/2 sum_j q_j^2 var_j; each CTA
-//               keeps the top-tc of its slice; the last CTA of a unit merges them
-//               (score descending, index ascending), records the selection and the union
-//               of selected clusters over the G heads.
-//  k_dec_sub    (units x G*tc CTAs): one union cluster per CTA: subcluster scores, top-ts
-//               per head that selected the cluster, residual masks of the rest, and the
-//               compacted list of rows (positions, head masks) to attend exactly.
-//  k_dec_attend (units x P CTAs): rows [p*T/P, (p+1)*T/P) of the unit's exact list (anchors
-//               first) through the attention engine, the Gaussian residual terms of a
-//               slice of the unselected groups, one partial per CTA; the last CTA of the
-//               unit merges the partials and normalises once.
+// One kernel per decode step: a thread-block cluster of CS CTAs per KV head ("unit"),
+// all hand-offs in distributed shared memory behind cluster barriers:
+//  P1  CTA k scores its slice of clusters for the G query heads of the unit,
+//      s = ln n + tau q.mu + tau^2/2 sum_j q_j^2 var_j, and keeps its slice's top-tc per head;
+//  P2  every CTA reads all slices' candidates, derives each head's top-tc clusters (score
+//      descending, index ascending) and their union over the heads (ascending index);
+//  P3  CTA k takes union slots k, k+CS, ...: subcluster scores, top-ts per head that chose
+//      the cluster, the member rows of the chosen subclusters (written to a row list), and
+//      the Gaussian residual of the unselected subclusters and of its own slice clusters;
+//  P4  the unit's exact rows (anchors, then the slots' rows) are split evenly over the CS
+//      CTAs and attended (mma.sync engine), giving one partial (max, sum, acc) per CTA;
+//  P5  CTA k merges a slice of the output over all partials and normalises once.
+#include <cooperative_groups.h>
+
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "attend.cuh"
 #include "internal.h"
@@ -121,481 +126,537 @@ struct OnlineAcc {
     }
 };
 
-constexpr int SC_SLICE = 32;                 // clusters per scoring CTA
-constexpr int SC_THREADS = 4 * SC_SLICE;     // 4 lanes per cluster
+constexpr int MD_THREADS = AT_THREADS;  // 4 warps (the attention engine's geometry)
+constexpr int SUPER = 256;                // row positions resolved per pass
+constexpr int RCH = 32;                   // slice clusters staged per residual pass
 
-// K1: grid (ceil(c_max/32), units).  Scores of a 32-cluster slice for all G heads (clusters
-// beyond a unit's C have count 0 and score -inf); the slice's top-tc per head (rank
-// counting, score desc then index asc) as a sorted candidate list cand[u][g][slice][tc].
+// Shared-memory layout of the decode kernel (byte offsets, 16-byte aligned).
+struct MdLay {
+    int CS, SL, NSLOT, SPC, stages;
+    int cand_s, cand_i, pub_cnt, pub_coff, pub_state;                // read by other CTAs
+    int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl, ucoff, pre;  // local
+    int sres, ssl, snn, sso, spref, smask, wst, rst, spos, smk, area;
+    int total;
+};
+
+__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int stages) {
+    MdLay m;
+    int o = 0;
+    auto take = [&](int bytes, int align) {
+        o = (o + align - 1) & ~(align - 1);
+        const int r = o;
+        o += bytes;
+        return r;
+    };
+    const int tcc = tc > 0 ? tc : 1;
+    m.CS = CS;
+    m.SL = (c_max + CS - 1) / CS;
+    m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
+    m.SPC = (m.NSLOT + CS - 1) / CS;
+    m.stages = stages;
+    m.cand_s = take(4 * G * tcc, 16);
+    m.cand_i = take(4 * G * tcc, 16);
+    m.pub_cnt = take(4 * m.SPC, 16);
+    m.pub_coff = take(4 * m.SPC, 16);
+    m.pub_state = take(4 * G * PART_W, 16);
+    m.w = take(16 * 64 * G, 16);
+    m.csl = take(4 * G * m.SL, 16);
+    m.crs = take(4 * G * m.SL, 16);
+    m.cnn = take(4 * m.SL, 16);
+    m.allc_s = take(4 * CS * G * tcc, 16);
+    m.allc_i = take(4 * CS * G * tcc, 16);
+    m.selc = take(4 * G * tcc, 16);
+    m.bm = take(4 * ((c_max + 31) / 32), 16);
+    m.ucl = take(4 * m.NSLOT, 16);
+    m.ucoff = take(4 * m.NSLOT, 16);
+    m.pre = take(4 * (m.NSLOT + 1), 16);
+    m.sres = take(4 * m.SPC * G * MOG_MAX_L, 16);
+    m.ssl = take(4 * m.SPC * G * MOG_MAX_L, 16);
+    m.snn = take(4 * m.SPC * MOG_MAX_L, 16);
+    m.sso = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
+    m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
+    m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
+    m.wst = take(4 * AT_WARPS * G * PART_W, 16);
+    m.rst = take(4 * G * PART_W, 16);  // right after wst: 5 contiguous states
+    m.spos = take(4 * SUPER, 16);
+    m.smk = take(4 * SUPER, 16);
+    const int tiles = stages * AT_STAGE_BYTES;
+    const int resb = (m.SPC * l_max + RCH) * MOG_D * 4;
+    m.area = take(tiles > resb ? tiles : resb, 128);
+    m.total = (o + 15) & ~15;
+    return m;
+}
+
 template <int GT>
-__global__ void __launch_bounds__(SC_THREADS) k_dec_score(DecArgs a) {
+__global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
+    namespace cg = cooperative_groups;
+    extern __shared__ __align__(128) uint8_t sm[];
+    cg::cluster_group cluster = cg::this_cluster();
     const Dev &dv = a.dv;
-    const int G = dv.G, tc = dv.tc;
-    __shared__ float4 w[GT * 64];
-    __shared__ float ssel[GT][SC_SLICE];
-    const int u = blockIdx.y, p = blockIdx.x;
-    const int cl = threadIdx.x >> 2, q4 = threadIdx.x & 3;
-    const int c = p * SC_SLICE + cl;
-    const bool valid = c < dv.c_max;
-    // everything read here is written before the decode step starts
-    const float *ms = dv.cl_ms + ((size_t)u * dv.c_max + (valid ? c : 0)) * 2 * MOG_D;
-    const int n = valid ? dv.cl_n[(size_t)u * dv.c_max + c] : 0;
-    load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
-    __syncthreads();
-    float res[GT], sl[GT];
-    quad_scores<GT>(ms, n, valid, w, G, dv.score_mode, res, sl);
-    pdl_wait();  // the previous step's readers of cscore/cand are done
-    pdl_trigger();
-    float *cres = dv.cscore + (size_t)u * 2 * G * dv.c_max;  // [0][g][c] selection, [1][g][c] residual
-    if (valid && q4 == 0) {
-#pragma unroll
-        for (int g = 0; g < GT; ++g) {
-            if (g >= G) break;
-            cres[(size_t)g * dv.c_max + c] = sl[g];
-            cres[((size_t)G + g) * dv.c_max + c] = res[g];
-        }
-    }
-    if (q4 == 0) {
-#pragma unroll
-        for (int g = 0; g < GT; ++g)
-            if (g < G) ssel[g][cl] = valid ? sl[g] : -INFINITY;
-    }
-    __syncthreads();
-    if (tc == 0) return;
-    const int P1 = gridDim.x, c0 = p * SC_SLICE;
-    const int span = max(SC_SLICE, tc);
-    for (int e = threadIdx.x; e < G * span; e += SC_THREADS) {
-        const int g = e / span, i = e % span;
-        float *cs = a.cand_s + (((size_t)u * G + g) * P1 + p) * tc;
-        int *ci = a.cand_i + (((size_t)u * G + g) * P1 + p) * tc;
-        if (i < SC_SLICE) {
-            const float v = ssel[g][i];
-            int rank = 0;
-#pragma unroll 8
-            for (int k = 0; k < SC_SLICE; ++k) rank += ranks_before(ssel[g][k], k, v, i);
-            if (rank < tc) {
-                cs[rank] = v;
-                ci[rank] = v == -INFINITY ? -1 : c0 + i;
-            }
-        } else if (i < tc) {
-            cs[i] = -INFINITY;
-            ci[i] = -1;
-        }
-    }
-}
-
-constexpr int SL_STAGES = 2;                  // tile buffers of the slot kernel
-constexpr int SL_SPLIT = 2;                   // CTAs per union slot (halves of its rows)
-constexpr int SL_ANCHOR = 2;                  // anchor CTAs per unit
-constexpr int SL_CHUNK = 32;                  // cluster residual items staged per pass
-constexpr int SUPER = 256;                    // row positions resolved per pass
-constexpr int SL_AREA = SL_STAGES * AT_STAGE_BYTES;  // 66 KB: selection / tiles / residual
-
-// Bytes of the slot kernel's phase-shared area (selection tables, then tiles, then the
-// residual staging); the selection (G*tc ints) follows it.
-__host__ __device__ inline size_t slot_area_bytes(int G, int c_max, int tc) {
-    const int P1 = (int)ceil_div64(c_max, SC_SLICE);
-    const size_t ncw = ((size_t)G * P1 * tc + 3) & ~(size_t)3;
-    const size_t sel = sizeof(float) * 2 * ncw + sizeof(uint32_t) * ((c_max + 3) & ~3);
-    const size_t res = sizeof(float) * ((size_t)(AT_WARPS + 1) * G * PART_W + (MOG_MAX_L + SL_CHUNK) * MOG_D);
-    size_t m = sel > res ? sel : res;
-    m = m > (size_t)SL_AREA ? m : (size_t)SL_AREA;
-    return (m + 15) & ~(size_t)15;
-}
-
-size_t slot_smem_bytes(int G, int c_max, int tc) {
-    return slot_area_bytes(G, c_max, tc) + sizeof(int) * (((size_t)G * tc + 3) & ~(size_t)3);
-}
-
-// Attention over `nrows` rows whose positions/masks come from `resolve(i0, n)` (filling
-// spos/smk for rows i0..i0+n), SUPER rows at a time, two tile buffers.
-template <typename Resolve>
-__device__ __forceinline__ void slot_rows(WarpAcc &acc, const uint32_t (&qa)[8][4], uint8_t *area,
-                                          int nrows, const uint16_t *kb, const uint16_t *vb,
-                                          int64_t sn, int *spos, uint32_t *smk, float scale2,
-                                          Resolve resolve) {
-    for (int sb = 0; sb < nrows; sb += SUPER) {
-        const int ns = min(SUPER, nrows - sb);
-        resolve(sb, ns);
-        __syncthreads();
-        const int nt = (int)ceil_div64(ns, AT_ROWS);
-        auto issue = [&](int t) {
-            const int rb = t * AT_ROWS;
-            issue_tile(area + (t % SL_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, ns - rb), kb, vb, sn,
-                       [&](int r, int64_t &pos, uint32_t &mk) {
-                           pos = spos[rb + r];
-                           mk = smk[rb + r];
-                       });
-        };
-        issue(0);
-        cp_async_commit();
-        if (nt > 1) issue(1);
-        cp_async_commit();
-        for (int t = 0; t < nt; ++t) {
-            cp_async_wait<1>();
-            __syncthreads();
-            compute_tile(acc, qa, area + (t % SL_STAGES) * AT_STAGE_BYTES, scale2);
-            __syncthreads();
-            if (t + 2 < nt) issue(t + 2);
-            cp_async_commit();
-        }
-        cp_async_wait<0>();
-        __syncthreads();
-    }
-}
-
-// K2: grid (SL_ANCHOR + SL_SPLIT * min(c_max, G*tc), units).
-//  - CTAs a < SL_ANCHOR attend to the anchor rows (sinks, recent and appended keys); they
-//    need nothing from the scoring kernel and run ahead of it.
-//  - CTA SL_ANCHOR + SL_SPLIT*j + part merges the per-slice candidate lists into every
-//    head's top-tc clusters (or takes the caller's selection), forms the union over the G
-//    heads (ascending cluster index) and takes union slot j: subcluster scores, top-ts per
-//    head that selected the cluster, then attention over `part`'s half of the members of
-//    the selected subclusters; part 0 adds the Gaussian residual of the unselected
-//    subclusters of that cluster and of a slice of the clusters some head did not select.
-//  Every CTA writes one partial (max, sum, acc); the last CTA of the unit merges them
-//  and normalises once.
-template <int GT>
-__global__ void __launch_bounds__(AT_THREADS) k_dec_slot(DecArgs a) {
-    extern __shared__ __align__(128) uint8_t area[];
-    const Dev &dv = a.dv;
-    const int G = dv.G, tc = dv.tc, ts = dv.ts;
-    __shared__ float4 w[GT * 64];
-    __shared__ float sres[GT][MOG_MAX_L];
-    __shared__ float ssl[GT][MOG_MAX_L];
-    __shared__ uint32_t smask[MOG_MAX_L];
-    __shared__ int sso[MOG_MAX_L + 1], snn[MOG_MAX_L], spref[MOG_MAX_L + 1];
-    __shared__ int spos[SUPER];
-    __shared__ uint32_t smk[SUPER];
-    __shared__ float iex[SL_CHUNK][GT];
-    __shared__ uint32_t ineed[SL_CHUNK];
-    __shared__ int s_wcnt[AT_WARPS], s_cj, s_uc, s_last;
-    const int u = blockIdx.y, r = blockIdx.x;
+    const int G = dv.G, tc = dv.tc, ts = dv.ts, tcc = max(tc, 1);
+    const int CS = m.CS, k = (int)cluster.block_rank();
+    const int u = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float *cand_s = reinterpret_cast<float *>(sm + m.cand_s);
+    int *cand_i = reinterpret_cast<int *>(sm + m.cand_i);
+    int *pub_cnt = reinterpret_cast<int *>(sm + m.pub_cnt);
+    int *pub_coff = reinterpret_cast<int *>(sm + m.pub_coff);
+    float *pub_state = reinterpret_cast<float *>(sm + m.pub_state);
+    float4 *w = reinterpret_cast<float4 *>(sm + m.w);
+    float *csl = reinterpret_cast<float *>(sm + m.csl);
+    float *crs = reinterpret_cast<float *>(sm + m.crs);
+    int *cnn = reinterpret_cast<int *>(sm + m.cnn);
+    float *allc_s = reinterpret_cast<float *>(sm + m.allc_s);
+    int *allc_i = reinterpret_cast<int *>(sm + m.allc_i);
+    int *selc = reinterpret_cast<int *>(sm + m.selc);
+    uint32_t *bm = reinterpret_cast<uint32_t *>(sm + m.bm);
+    int *ucl = reinterpret_cast<int *>(sm + m.ucl);
+    int *ucoff = reinterpret_cast<int *>(sm + m.ucoff);
+    int *pre = reinterpret_cast<int *>(sm + m.pre);
+    float *sres = reinterpret_cast<float *>(sm + m.sres);
+    float *ssl = reinterpret_cast<float *>(sm + m.ssl);
+    int *snn = reinterpret_cast<int *>(sm + m.snn);
+    int *sso = reinterpret_cast<int *>(sm + m.sso);
+    int *spref = reinterpret_cast<int *>(sm + m.spref);
+    uint32_t *smask = reinterpret_cast<uint32_t *>(sm + m.smask);
+    float *wst = reinterpret_cast<float *>(sm + m.wst);
+    float *rst = reinterpret_cast<float *>(sm + m.rst);
+    int *spos = reinterpret_cast<int *>(sm + m.spos);
+    uint32_t *smk = reinterpret_cast<uint32_t *>(sm + m.smk);
+    uint8_t *area = sm + m.area;
+    __shared__ int s_wsum[AT_WARPS], s_uc;
+
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int b = ui[UI_B], h = u % dv.h_kv, C = ui[UI_C], L = ui[UI_L];
     const int S = ui[UI_S], rlo = ui[UI_RLO];
+    const int nnow = dv.n_now[b];
+    const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
-    const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
-    const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
-    const float scale2 = dv.tau * LOG2E;
+    const size_t ug = (size_t)u * dv.c_max;               // cluster index base
+    const size_t usg = (size_t)u * dv.c_max * dv.l_max;   // subcluster index base
+    const uint16_t *qg = a.q + (size_t)u * G * MOG_D;
+    int *selu = dv.sel + (size_t)u * G * a.SW;
+
+    // ------------------------------------------------------------ P0: query, weights
     uint32_t qa[8][4];
-    load_q_frags(qa, a.q + (size_t)u * G * MOG_D, G);
-    WarpAcc acc;
-    acc.init();
-    float *states = reinterpret_cast<float *>(area);  // after the tiles: [AT_WARPS + 1][G][PART_W]
-    float *part_out;
-    bool has_res = false;
-    if (r < SL_ANCHOR) {
-        // ------------------------------- anchors ---------------------------------------
-        pdl_trigger();
-        const int nnow = dv.n_now[b];
-        const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
-        const int i0 = (int)((int64_t)n_anchor * r / SL_ANCHOR), i1 = (int)((int64_t)n_anchor * (r + 1) / SL_ANCHOR);
-        slot_rows(acc, qa, area, i1 - i0, kb, vb, dv.sn, spos, smk, scale2, [&](int sb, int ns) {
-            for (int t = tid; t < ns; t += AT_THREADS) {
-                const int i = i0 + sb + t;
-                spos[t] = i < s_cnt ? i : rlo + (i - s_cnt);
-                smk[t] = allm;
-            }
-        });
-        part_out = dv.partials + ((size_t)u * PART_SLOTS + r) * G * PART_W;
-    } else {
-        // ------------------------------- a union slot -----------------------------------
-        const int j = (r - SL_ANCHOR) / SL_SPLIT, part = (r - SL_ANCHOR) % SL_SPLIT;
-        const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
-        const int NC = P1 * tc;
-        const size_t ncw = ((size_t)G * NC + 3) & ~(size_t)3;
-        float *cand_s = reinterpret_cast<float *>(area);                       // [G][NC]
-        int *cand_i = reinterpret_cast<int *>(cand_s + ncw);                    // [G][NC]
-        uint32_t *cselm = reinterpret_cast<uint32_t *>(cand_i + ncw);           // [c_max]
-        // the selection itself outlives the shared area (tiles reuse it): tail region
-        int *selc = reinterpret_cast<int *>(area + slot_area_bytes(G, dv.c_max, tc));  // [G][tc]
-        load_weights(w, a.q + (size_t)u * G * MOG_D, G, dv.tau);
-        for (int e = tid; e < G * tc; e += AT_THREADS) selc[e] = -1;
-        for (int e = tid; e < C; e += AT_THREADS) cselm[e] = 0u;
-        if (tid < MOG_MAX_L) smask[tid] = 0u;
-        pdl_wait();  // candidate lists of the scoring kernel
-        pdl_trigger();
-        if (tc > 0 && !a.sel_in) {
-            const size_t base = (size_t)u * G * NC;
-            for (int e = tid; e < G * NC; e += AT_THREADS) {
-                cp_async4(smem_u32(cand_s + e), a.cand_s + base + e);
-                cp_async4(smem_u32(cand_i + e), a.cand_i + base + e);
-            }
-            cp_async_commit();
-            cp_async_wait<0>();
+    load_q_frags(qa, qg, G);
+    load_weights(w, qg, G, dv.tau);
+    pdl_wait();
+    pdl_trigger();
+    __syncthreads();
+
+    // ------------------------------------------------- P1: score this CTA's clusters
+    const int c0 = k * m.SL;
+    const int ns = max(0, min(C - c0, m.SL));
+    for (int base = 0; base < ns; base += MD_THREADS / 4) {
+        const int cl = base + (tid >> 2);
+        const bool valid = cl < ns;
+        const int c = c0 + (valid ? cl : 0);
+        const int n = valid ? dv.cl_n[ug + c] : 0;
+        float res[GT], sl[GT];
+        quad_scores<GT>(dv.cl_ms + (ug + c) * 2 * MOG_D, n, valid, w, G, dv.score_mode, res, sl);
+        if (valid && (tid & 3) == 0) {
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+                if (g < G) {
+                    csl[g * m.SL + cl] = sl[g];
+                    crs[g * m.SL + cl] = res[g];
+                }
+            cnn[cl] = n;
         }
-        __syncthreads();
-        if (tc > 0) {
-            if (a.sel_in) {
-                for (int e = tid; e < G * tc; e += AT_THREADS) {
-                    const int g = e / tc, rr = e % tc;
-                    const int cc = a.sel_in[((size_t)u * G + g) * a.SW + rr];
-                    selc[g * tc + rr] =
-                        (cc >= 0 && cc < C && dv.cl_n[(size_t)u * dv.c_max + cc] > 0) ? cc : -1;
+    }
+    __syncthreads();
+    if (tc > 0) {  // this slice's top-tc per head, sorted, as (score, cluster) with -1 padding
+        const int span = max(ns, tc);
+        for (int e = tid; e < G * span; e += MD_THREADS) {
+            const int g = e / span, i = e % span;
+            if (i < ns) {
+                const float v = csl[g * m.SL + i];
+                int rank = 0;
+                for (int kk = 0; kk < ns; ++kk) rank += ranks_before(csl[g * m.SL + kk], kk, v, i);
+                if (rank < tc) {
+                    cand_s[g * tc + rank] = v;
+                    cand_i[g * tc + rank] = v == -INFINITY ? -1 : c0 + i;
                 }
             } else {
-                // element (g, list p, position r): its rank over all lists of head g is r
-                // plus, for every other list, the length of that list's prefix ranking
-                // before it
-                for (int e = tid; e < G * NC; e += AT_THREADS) {
-                    const int g = e / NC, pr = e % NC, pl = pr / tc, rr = pr % tc;
-                    const float *cs = cand_s + (size_t)g * NC;
-                    const int *ci = cand_i + (size_t)g * NC;
-                    const int x = ci[pr];
-                    if (x < 0) continue;
-                    const float v = cs[pr];
-                    int rank = rr;
-                    for (int q = 0; q < P1 && rank < tc; ++q) {
-                        if (q == pl) continue;
-                        int lo = 0, hi = tc;  // first position not ranking before (v, x)
-                        while (lo < hi) {
-                            const int mid = (lo + hi) >> 1;
-                            const int xm = ci[q * tc + mid];
-                            if (xm >= 0 && ranks_before(cs[q * tc + mid], xm, v, x)) lo = mid + 1;
-                            else hi = mid;
-                        }
-                        rank += lo;
+                cand_s[g * tc + i] = -INFINITY;
+                cand_i[g * tc + i] = -1;
+            }
+        }
+    }
+    for (int e = tid; e < G * tcc; e += MD_THREADS) selc[e] = -1;
+    for (int e = tid; e < (dv.c_max + 31) / 32; e += MD_THREADS) bm[e] = 0u;
+    cluster.sync();  // S1: candidates of every slice are published
+
+    // ------------------------------------------------------- P2: selection and union
+    if (tc > 0) {
+        if (a.sel_in) {
+            for (int e = tid; e < G * tc; e += MD_THREADS) {
+                const int g = e / tc, r = e % tc;
+                const int cc = a.sel_in[((size_t)u * G + g) * a.SW + r];
+                selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
+            }
+        } else {
+            for (int e = tid; e < CS * G * tc; e += MD_THREADS) {  // gather [g][src][r]
+                const int src = e / (G * tc), rem = e % (G * tc), g = rem / tc, r = rem % tc;
+                const float *rs = cluster.map_shared_rank(cand_s, src);
+                const int *ri = cluster.map_shared_rank(cand_i, src);
+                allc_s[(g * CS + src) * tc + r] = rs[rem];
+                allc_i[(g * CS + src) * tc + r] = ri[rem];
+            }
+            __syncthreads();
+            // element (g, list p, position r): rank over all lists of head g = r plus, for
+            // every other list, the length of its prefix that ranks before the element
+            for (int e = tid; e < G * CS * tc; e += MD_THREADS) {
+                const int g = e / (CS * tc), pr = e % (CS * tc), pl = pr / tc, r = pr % tc;
+                const float *cs = allc_s + (size_t)g * CS * tc;
+                const int *ci = allc_i + (size_t)g * CS * tc;
+                const int x = ci[pr];
+                if (x < 0) continue;
+                const float v = cs[pr];
+                int rank = r;
+                for (int q = 0; q < CS && rank < tc; ++q) {
+                    if (q == pl) continue;
+                    int lo = 0, hi = tc;
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        const int xm = ci[q * tc + mid];
+                        if (xm >= 0 && ranks_before(cs[q * tc + mid], xm, v, x)) lo = mid + 1;
+                        else hi = mid;
                     }
-                    if (rank < tc) selc[g * tc + rank] = x;
+                    rank += lo;
+                }
+                if (rank < tc) selc[g * tc + rank] = x;
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < G * tc; e += MD_THREADS)
+        if (selc[e] >= 0) atomicOr(&bm[selc[e] >> 5], 1u << (selc[e] & 31));
+    __syncthreads();
+    {  // union = set bits of bm, ascending: ucl[0 .. Uc)
+        const int nw = (dv.c_max + 31) / 32;
+        const int per = (nw + MD_THREADS - 1) / MD_THREADS;
+        const int w0 = tid * per, w1 = min(nw, w0 + per);
+        int cnt = 0;
+        for (int i = w0; i < w1; ++i) cnt += __popc(bm[i]);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int base = incl - cnt;
+        for (int kk = 0; kk < warp; ++kk) base += s_wsum[kk];
+        if (tid == MD_THREADS - 1) s_uc = base + cnt;
+        for (int i = w0; i < w1; ++i) {
+            uint32_t bits = bm[i];
+            while (bits) {
+                const int bit = __ffs(bits) - 1;
+                bits &= bits - 1;
+                ucl[base++] = i * 32 + bit;
+            }
+        }
+    }
+    __syncthreads();
+    const int Uc = s_uc;
+    if (k == 0) {  // the cluster part of the exported selection
+        for (int e = tid; e < G * tc; e += MD_THREADS) {
+            const int g = e / tc, r = e % tc;
+            selu[(size_t)g * a.SW + r] = selc[e];
+            if (selc[e] < 0)
+                for (int kk = 0; kk < ts; ++kk) selu[(size_t)g * a.SW + tc + r * ts + kk] = -1;
+        }
+    }
+
+    // ----------------------------------------- P3: this CTA's union slots, residual
+    const int nmy = Uc > k ? (Uc - k + CS - 1) / CS : 0;  // slots k, k+CS, ...
+    const bool resid = dv.residual != 0;
+    float *vst = reinterpret_cast<float *>(area);           // [SPC*l_max][d] subcluster means
+    float *vcl = vst + (size_t)m.SPC * dv.l_max * MOG_D;    // [RCH][d] slice cluster means
+    for (int s = 0; s < nmy; ++s) {
+        const int c = ucl[k + s * CS];
+        const size_t g0 = usg + (size_t)c * L;
+        const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
+        if (tid <= L) sso[s * (MOG_MAX_L + 1) + tid] = so[tid];
+        if (tid < L) snn[s * MOG_MAX_L + tid] = dv.sub_n[g0 + tid];
+        if (resid)
+            for (int e = tid; e < L * 32; e += MD_THREADS)
+                cp_async16(smem_u32(vst + ((size_t)s * dv.l_max + e / 32) * MOG_D + 4 * (e % 32)),
+                           dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
+        const int l = tid >> 2;
+        const bool valid = l < L;
+        float res[GT], sl[GT];
+        quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D, valid ? dv.sub_n[g0 + l] : 0,
+                        valid, w, G, dv.score_mode, res, sl);
+        if (valid && (tid & 3) == 0) {
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+                if (g < G) {
+                    sres[(s * G + g) * MOG_MAX_L + l] = res[g];
+                    ssl[(s * G + g) * MOG_MAX_L + l] = sl[g];
+                }
+        }
+        if (tid < MOG_MAX_L) smask[s * MOG_MAX_L + tid] = 0u;
+    }
+    // slice clusters that some head did not select: value means, first chunk
+    auto need_cluster = [&](int cl) -> uint32_t {
+        const int c = c0 + cl;
+        if (cnn[cl] <= 0) return 0u;
+        uint32_t chose = 0u;
+        for (int q = 0; q < G * tc; ++q)
+            if (selc[q] == c) chose |= 1u << (q / tc);
+        return allm & ~chose;
+    };
+    auto stage_slice = [&](int k0) {
+        const int cnt = min(RCH, ns - k0);
+        for (int e = tid; e < cnt * 32; e += MD_THREADS)
+            cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
+                       dv.cl_vbar + (ug + c0 + k0 + e / 32) * MOG_D + 4 * (e % 32), 16);
+    };
+    if (resid && ns > 0) stage_slice(0);
+    cp_async_commit();
+    __syncthreads();
+    // top-ts subclusters of every head that chose a slot's cluster
+    for (int e = warp; e < nmy * G; e += AT_WARPS) {
+        const int s = e / G, g = e % G;
+        const int c = ucl[k + s * CS];
+        int rk = -1;
+        for (int r = 0; r < tc; ++r)
+            if (selc[g * tc + r] == c) { rk = r; break; }
+        if (rk < 0) continue;
+        int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
+        const int *nn = snn + s * MOG_MAX_L;
+        if (a.sel_in) {
+            const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + tc + (size_t)rk * ts;
+            for (int r = lane; r < ts; r += 32) {
+                const int l2 = si[r];
+                const bool ok = l2 >= 0 && l2 < L && nn[l2] > 0;
+                subs[r] = ok ? l2 : -1;
+                if (ok) atomicOr(&smask[s * MOG_MAX_L + l2], 1u << g);
+            }
+        } else {
+            for (int r = lane; r < ts; r += 32) subs[r] = -1;
+            __syncwarp();
+            const float *sc = ssl + (s * G + g) * MOG_MAX_L;
+            const float v = lane < L ? sc[lane] : -INFINITY;
+            int rank = 0;
+            for (int kk = 0; kk < L; ++kk) rank += ranks_before(sc[kk], kk, v, lane);
+            if (lane < L && v != -INFINITY && rank < ts) {
+                subs[rank] = lane;
+                atomicOr(&smask[s * MOG_MAX_L + lane], 1u << g);
+            }
+        }
+    }
+    __syncthreads();
+    for (int s = warp; s < nmy; s += AT_WARPS) {  // prefix of the chosen subclusters' sizes
+        const int *so = sso + s * (MOG_MAX_L + 1);
+        const int cnt = lane < L && smask[s * MOG_MAX_L + lane] ? so[lane + 1] - so[lane] : 0;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane < L) spref[s * (MOG_MAX_L + 1) + lane + 1] = incl;
+        if (lane == 0) {
+            spref[s * (MOG_MAX_L + 1)] = 0;
+            pub_coff[s] = so[0];
+        }
+        if (lane == L - 1) pub_cnt[s] = incl;
+    }
+    __syncthreads();
+    {  // member rows of the chosen subclusters -> the unit's row list (perm order)
+        const int *perm = dv.perm + (size_t)u * dv.n_cap;
+        int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
+        uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
+        for (int s = 0; s < nmy; ++s) {
+            const int *sp = spref + s * (MOG_MAX_L + 1);
+            const int *so = sso + s * (MOG_MAX_L + 1);
+            const int tot = sp[L];
+            for (int i = tid; i < tot; i += MD_THREADS) {
+                int kk = 0;
+                while (sp[kk + 1] <= i) ++kk;
+                rowpos[so[0] + i] = perm[so[kk] + (i - sp[kk])];
+                rowmask[so[0] + i] = smask[s * MOG_MAX_L + kk];
+            }
+        }
+    }
+    // Gaussian residual: thread (warp, lane) owns dims 4*lane..+3 of heads warp, warp+4, ..
+    {
+        OnlineAcc st[MOG_MAX_G / AT_WARPS];
+#pragma unroll
+        for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) st[kk].init();
+        if (resid) {
+            cp_async_wait<0>();
+            __syncthreads();
+            for (int s = 0; s < nmy; ++s) {
+                const int c = ucl[k + s * CS];
+                uint32_t hm = 0u;
+                for (int q = 0; q < G * tc; ++q)
+                    if (selc[q] == c) hm |= 1u << (q / tc);
+                for (int l = 0; l < L; ++l) {
+                    if (snn[s * MOG_MAX_L + l] <= 0) continue;
+                    const uint32_t need = hm & ~smask[s * MOG_MAX_L + l];
+                    const float *vrow = vst + ((size_t)s * dv.l_max + l) * MOG_D + 4 * lane;
+#pragma unroll
+                    for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) {
+                        const int g = warp + AT_WARPS * kk;
+                        if (g < G && ((need >> g) & 1u))
+                            st[kk].absorb(sres[(s * G + g) * MOG_MAX_L + l] * LOG2E, vrow);
+                    }
+                }
+            }
+            for (int k0 = 0; k0 < ns; k0 += RCH) {
+                if (k0 > 0) {
+                    __syncthreads();
+                    stage_slice(k0);
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    __syncthreads();
+                }
+                const int cnt = min(RCH, ns - k0);
+                for (int e = 0; e < cnt; ++e) {
+                    const uint32_t need = need_cluster(k0 + e);
+                    const float *vrow = vcl + (size_t)e * MOG_D + 4 * lane;
+#pragma unroll
+                    for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) {
+                        const int g = warp + AT_WARPS * kk;
+                        if (g < G && ((need >> g) & 1u)) st[kk].absorb(crs[g * m.SL + k0 + e] * LOG2E, vrow);
+                    }
                 }
             }
         }
-        __syncthreads();
-        for (int e = tid; e < G * tc; e += AT_THREADS) {
-            const int cc = selc[(e / tc) * tc + e % tc];
-            if (cc >= 0) atomicOr(&cselm[cc], 1u << (e / tc));
+#pragma unroll
+        for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) {
+            const int g = warp + AT_WARPS * kk;
+            if (g >= G) continue;
+            float *o = rst + (size_t)g * PART_W;
+            if (lane == 0) {
+                o[0] = st[kk].m;
+                o[1] = st[kk].l;
+            }
+            *reinterpret_cast<float4 *>(o + PART_ACC + 4 * lane) = st[kk].a;
         }
-        __syncthreads();
-        {  // union over the heads, ascending; this CTA's slot
-            const int per = (int)ceil_div64(C, AT_THREADS);
-            const int cA = tid * per, cB = min(C, cA + per);
+    }
+    cp_async_wait<0>();
+    cluster.sync();  // S2: row lists (global) and their counts (shared) are published
+
+    // -------------------------------------------- P4: exact rows, split evenly
+    if (warp == 0) {  // slot prefix from the owners' counts
+        int run = n_anchor;
+        for (int j0 = 0; j0 < Uc; j0 += 32) {
+            const int j = j0 + lane;
             int cnt = 0;
-            for (int cc = cA; cc < cB; ++cc) cnt += cselm[cc] != 0u;
+            if (j < Uc) {
+                const int own = j % CS, s = j / CS;
+                cnt = cluster.map_shared_rank(pub_cnt, own)[s];
+                ucoff[j] = cluster.map_shared_rank(pub_coff, own)[s];
+            }
             int incl = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            if (lane == 31) s_wcnt[warp] = incl;
+            if (j < Uc) pre[j] = run + incl - cnt;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) pre[Uc] = run;
+    }
+    __syncthreads();
+    const int T = pre[Uc];
+    const int r0 = (int)((int64_t)T * k / CS), r1 = (int)((int64_t)T * (k + 1) / CS);
+    const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
+    const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
+    const int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
+    const uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
+    WarpAcc acc;
+    acc.init();
+    const float scale2 = dv.tau * LOG2E;
+    const int NSTG = m.stages;
+    for (int sb = r0; sb < r1; sb += SUPER) {
+        const int nrow = min(SUPER, r1 - sb);
+        for (int t = tid; t < nrow; t += MD_THREADS) {
+            const int i = sb + t;
+            int pos;
+            uint32_t mk;
+            if (i < n_anchor) {
+                pos = i < s_cnt ? i : rlo + (i - s_cnt);
+                mk = allm;
+            } else {
+                int lo = 0, hi = Uc - 1;  // last slot with pre[slot] <= i
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (pre[mid] <= i) lo = mid;
+                    else hi = mid - 1;
+                }
+                const int kk = ucoff[lo] + (i - pre[lo]);
+                pos = __ldcg(rowpos + kk);
+                mk = __ldcg(rowmask + kk);
+            }
+            if ((unsigned)pos >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
+                flag_error(dv.status, ST_BAD_INDEX);
+                pos = 0;
+                mk = 0u;
+            }
+            spos[t] = pos;
+            smk[t] = mk;
+        }
+        __syncthreads();
+        const int nt = (int)ceil_div64(nrow, AT_ROWS);
+        auto issue = [&](int t) {
+            const int rb = t * AT_ROWS;
+            issue_tile(area + (t % NSTG) * AT_STAGE_BYTES, min(AT_ROWS, nrow - rb), kb, vb, dv.sn,
+                       [&](int r, int64_t &pos, uint32_t &mk) {
+                           pos = spos[rb + r];
+                           mk = smk[rb + r];
+                       });
+        };
+        for (int s = 0; s < NSTG - 1; ++s) {
+            if (s < nt) issue(s);
+            cp_async_commit();
+        }
+        for (int t = 0; t < nt; ++t) {
+            cp_async_wait_dyn(NSTG - 2);
             __syncthreads();
-            int base = incl - cnt;
-            for (int k = 0; k < warp; ++k) base += s_wcnt[k];
-            if (tid == AT_THREADS - 1) s_uc = base + cnt;
-            if (j >= base && j < base + cnt) {
-                int k = base;
-                for (int cc = cA; cc < cB; ++cc)
-                    if (cselm[cc]) {
-                        if (k == j) s_cj = cc;
-                        ++k;
-                    }
-            }
+            if (t + NSTG - 1 < nt) issue(t + NSTG - 1);
+            cp_async_commit();
+            compute_tile(acc, qa, area + (t % NSTG) * AT_STAGE_BYTES, scale2);
         }
+        cp_async_wait<0>();
         __syncthreads();
-        const int Uc = s_uc, R = max(Uc, 1);
-        part_out = nullptr;
-        if (j < R) {
-            part_out = dv.partials + ((size_t)u * PART_SLOTS + r) * G * PART_W;
-            const bool has_slot = j < Uc;
-            const int c = has_slot ? s_cj : 0;
-            const uint32_t hm = has_slot ? cselm[c] : 0u;
-            int *selu = dv.sel + (size_t)u * G * a.SW;
-            if (j == 0 && part == 0) {
-                if (tid == 0) dv.ucount[u] = Uc;
-                for (int e = tid; e < G * tc; e += AT_THREADS) {
-                    const int g = e / tc, rr = e % tc;
-                    const int cc = selc[g * tc + rr];
-                    selu[(size_t)g * a.SW + rr] = cc;
-                    if (cc < 0)
-                        for (int k = 0; k < ts; ++k) selu[(size_t)g * a.SW + tc + rr * ts + k] = -1;
+    }
+    warp_state_out(acc, wst, G);
+    __syncthreads();
+    merge_states(wst, AT_WARPS + 1, G, pub_state);  // wst and rst are contiguous
+    cluster.sync();  // S3: every CTA's partial is published
+
+    // ------------------------------------- P5: this CTA's slice of the output
+    {
+        const int tot = G * MOG_D;
+        const int e0 = (int)((int64_t)tot * k / CS), e1 = (int)((int64_t)tot * (k + 1) / CS);
+        for (int e = e0 + tid; e < e1; e += MD_THREADS) {
+            const int g = e / MOG_D, j = e % MOG_D;
+            float M = -INFINITY;
+            for (int src = 0; src < CS; ++src)
+                M = fmaxf(M, cluster.map_shared_rank(pub_state, src)[g * PART_W]);
+            float lsum = 0.f, asum = 0.f;
+            if (M != -INFINITY)
+                for (int src = 0; src < CS; ++src) {
+                    const float *ps = cluster.map_shared_rank(pub_state, src) + g * PART_W;
+                    const float mi = ps[0];
+                    if (mi == -INFINITY) continue;
+                    const float sc = exp2f(mi - M);
+                    lsum += sc * ps[1];
+                    asum += sc * ps[PART_ACC + j];
                 }
-            }
-            const size_t g0 = (size_t)u * dv.c_max * dv.l_max + (size_t)c * L;
-            const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
-            int nrows = 0, row0 = 0;
-            if (has_slot) {
-                if (tid <= L) sso[tid] = so[tid];
-                if (tid < L) snn[tid] = dv.sub_n[g0 + tid];
-                const int l = tid >> 2;
-                const bool valid = l < L;
-                float res[GT], sl[GT];
-                quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D,
-                                valid ? dv.sub_n[g0 + l] : 0, valid, w, G, dv.score_mode, res, sl);
-                if (valid && (tid & 3) == 0) {
-#pragma unroll
-                    for (int g = 0; g < GT; ++g)
-                        if (g < G) {
-                            sres[g][l] = res[g];
-                            ssl[g][l] = sl[g];
-                        }
-                }
-                __syncthreads();
-                for (int g = warp; g < G; g += AT_WARPS) {  // top-ts of each head that chose c
-                    if (!((hm >> g) & 1u)) continue;
-                    int rk = -1;
-                    for (int rr = 0; rr < tc; ++rr)
-                        if (selc[g * tc + rr] == c) { rk = rr; break; }
-                    if (rk < 0) continue;
-                    int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
-                    if (a.sel_in) {
-                        const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + tc + (size_t)rk * ts;
-                        for (int rr = lane; rr < ts; rr += 32) {
-                            const int l2 = si[rr];
-                            const bool ok = l2 >= 0 && l2 < L && snn[l2] > 0;
-                            if (part == 0) subs[rr] = ok ? l2 : -1;
-                            if (ok) atomicOr(&smask[l2], 1u << g);
-                        }
-                    } else {
-                        if (part == 0)
-                            for (int rr = lane; rr < ts; rr += 32) subs[rr] = -1;
-                        __syncwarp();
-                        const float v = lane < L ? ssl[g][lane] : -INFINITY;
-                        int rank = 0;
-                        for (int k = 0; k < L; ++k) rank += ranks_before(ssl[g][k], k, v, lane);
-                        if (lane < L && v != -INFINITY && rank < ts) {
-                            if (part == 0) subs[rank] = lane;
-                            atomicOr(&smask[lane], 1u << g);
-                        }
-                    }
-                }
-                __syncthreads();
-                if (warp == 0) {  // prefix of the selected subclusters' sizes
-                    const int cnt = lane < L && smask[lane] ? sso[lane + 1] - sso[lane] : 0;
-                    int incl = cnt;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    if (lane < L) spref[lane + 1] = incl;
-                    if (lane == 0) spref[0] = 0;
-                }
-                __syncthreads();
-                const int T = spref[L];
-                row0 = (int)((int64_t)T * part / SL_SPLIT);
-                nrows = (int)((int64_t)T * (part + 1) / SL_SPLIT) - row0;
-            }
-            // ---------------- exact rows of this half ----------------
-            const int *perm = dv.perm + (size_t)u * dv.n_cap;
-            slot_rows(acc, qa, area, nrows, kb, vb, dv.sn, spos, smk, scale2, [&](int sb, int ns) {
-                for (int t = tid; t < ns; t += AT_THREADS) {
-                    const int i = row0 + sb + t;
-                    int k = 0;
-                    while (spref[k + 1] <= i) ++k;
-                    int pos = perm[sso[k] + (i - spref[k])];
-                    uint32_t mk = smask[k];
-                    if ((unsigned)pos >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
-                        flag_error(dv.status, ST_BAD_INDEX);
-                        pos = 0;
-                        mk = 0u;
-                    }
-                    spos[t] = pos;
-                    smk[t] = mk;
-                }
-            });
-            // ---------------- Gaussian residual (part 0) ----------------
-            if (part == 0 && dv.residual) {
-                has_res = true;
-                float *vst = states + (size_t)(AT_WARPS + 1) * G * PART_W;  // [32 + SL_CHUNK][d]
-                float *vcl = vst + (size_t)MOG_MAX_L * MOG_D;
-                const int nsub = has_slot ? L : 0;
-                const int cA = (int)((int64_t)C * j / R), cB = (int)((int64_t)C * (j + 1) / R);
-                const int ncl = cB - cA;
-                const float *cres = dv.cscore + ((size_t)u * 2 + 1) * G * dv.c_max;
-                auto stage_clusters = [&](int k0) {
-                    const int cnt = min(SL_CHUNK, ncl - k0);
-                    for (int e = tid; e < cnt * 32; e += AT_THREADS) {
-                        const int cc = cA + k0 + e / 32, k = e % 32;
-                        cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * k),
-                                   dv.cl_vbar + ((size_t)u * dv.c_max + cc) * MOG_D + 4 * k, 16);
-                    }
-                    cp_async_commit();
-                    for (int e = tid; e < cnt; e += AT_THREADS) {
-                        const int cc = cA + k0 + e;
-                        uint32_t chose = 0u;  // heads that selected cc
-                        for (int q = 0; q < G * tc; ++q)
-                            if (selc[q] == cc) chose |= 1u << (q / tc);
-                        ineed[e] = dv.cl_n[(size_t)u * dv.c_max + cc] > 0 ? (allm & ~chose) : 0u;
-#pragma unroll
-                        for (int g = 0; g < GT; ++g)
-                            if (g < G) iex[e][g] = cres[(size_t)g * dv.c_max + cc];
-                    }
-                };
-                for (int e = tid; e < nsub * 32; e += AT_THREADS)
-                    cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
-                               dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
-                if (ncl > 0) stage_clusters(0);
-                else cp_async_commit();
-                cp_async_wait<0>();
-                __syncthreads();
-                // thread (warp, lane) owns dims 4*lane..+3 of heads warp, warp + 4, ...
-                OnlineAcc st[MOG_MAX_G / AT_WARPS];
-#pragma unroll
-                for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) st[k].init();
-                for (int l = 0; l < nsub; ++l) {
-                    if (snn[l] <= 0) continue;
-                    const uint32_t need = hm & ~smask[l];
-                    const float *vrow = vst + (size_t)l * MOG_D + 4 * lane;
-#pragma unroll
-                    for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) {
-                        const int g = warp + AT_WARPS * k;
-                        if (g < G && ((need >> g) & 1u)) st[k].absorb(sres[g < GT ? g : 0][l] * LOG2E, vrow);
-                    }
-                }
-                for (int k0 = 0; k0 < ncl; k0 += SL_CHUNK) {
-                    if (k0 > 0) {
-                        __syncthreads();
-                        stage_clusters(k0);
-                        cp_async_wait<0>();
-                        __syncthreads();
-                    }
-                    const int cnt = min(SL_CHUNK, ncl - k0);
-                    for (int e = 0; e < cnt; ++e) {
-                        const float *vrow = vcl + (size_t)e * MOG_D + 4 * lane;
-#pragma unroll
-                        for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) {
-                            const int g = warp + AT_WARPS * k;
-                            if (g < G && ((ineed[e] >> g) & 1u)) st[k].absorb(iex[e][g < GT ? g : 0] * LOG2E, vrow);
-                        }
-                    }
-                }
-                float *rs = states + (size_t)AT_WARPS * G * PART_W;  // state AT_WARPS
-#pragma unroll
-                for (int k = 0; k < MOG_MAX_G / AT_WARPS; ++k) {
-                    const int g = warp + AT_WARPS * k;
-                    if (g >= G) continue;
-                    float *o = rs + (size_t)g * PART_W;
-                    if (lane == 0) {
-                        o[0] = st[k].m;
-                        o[1] = st[k].l;
-                    }
-                    *reinterpret_cast<float4 *>(o + PART_ACC + 4 * lane) = st[k].a;
-                }
-            }
+            a.out[(size_t)u * G * MOG_D + e] = lsum > 0.f ? asum / lsum : 0.f;
         }
     }
-    // ------------------- this CTA's partial; the unit's last CTA merges ------------------
-    if (part_out) {
-        warp_state_out(acc, states, G);
-        __syncthreads();
-        merge_states(states, AT_WARPS + (has_res ? 1 : 0), G, part_out);
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned t = atomicAdd(dv.counters + u * 4 + 1, 1u);
-        s_last = (t == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (tid == 0) dv.counters[u * 4 + 1] = 0u;
-    const int Uc = dv.tc > 0 ? __ldcg(dv.ucount + u) : 0;
-    const int nparts = SL_ANCHOR + SL_SPLIT * max(Uc, 1);
-    merge_global_out(dv.partials + (size_t)u * PART_SLOTS * G * PART_W, nparts, G,
-                     reinterpret_cast<float *>(area), SL_AREA / 4, a.out + (size_t)u * G * MOG_D);
+    cluster.sync();  // S4: keep this CTA's shared memory alive for the other readers
 }
 
 // Append one token per sequence at position n_now[b], then advance n_now[b].
@@ -616,38 +677,97 @@ __global__ void k_append(Dev dv, const uint16_t *kn, const uint16_t *vn) {
 
 // ------------------------------------------------------------------------------------
 template <typename K>
-static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              const DecArgs &a) {
+static cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cs,
+                             const DecArgs &a, const MdLay &m) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = cs;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, a, m);
+}
+
+// Cluster size (CTAs per unit) and pipeline depth for a decode launch: the largest cluster
+// (<= 16) such that every unit's cluster is resident at once, four tile stages when the
+// launch fits one CTA per SM.
+template <int GT>
+static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
+    const void *fn = (const void *)k_mog_decode<GT>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    const int sms = num_sms();
+    for (int cs = 16; cs >= 1; cs >>= 1) {
+        if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;
+        const int stages = (int64_t)cs * dv.units <= sms ? 4 : 2;
+        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, stages);
+        if (m.total > 227 * 1024) continue;
+        if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs, dv.units);
+        cfg.blockDim = dim3(MD_THREADS);
+        cfg.dynamicSmemBytes = m.total;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = cs;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int ncl = 0;
+        e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (ncl >= dv.units || cs == 1) {
+            *cs_out = cs;
+            *m_out = m;
+            return cudaSuccess;
+        }
+    }
+    return cudaErrorInvalidConfiguration;
 }
 
 template <int GT>
 static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t const *events) {
     const Dev &dv = a.dv;
     cudaError_t e;
+    // the shape depends only on the plan: cache it per (units, G, tc, c_max, l_max)
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int, int>, std::pair<int, MdLay>> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, dv.units, dv.G, dv.tc, dv.c_max, dv.l_max);
+    int cs;
+    MdLay m;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it == cache.end()) {
+            if ((e = pick_shape<GT>(dv, &cs, &m)) != cudaSuccess) return e;
+            cache[key] = std::make_pair(cs, m);
+        } else {
+            cs = it->second.first;
+            m = it->second.second;
+        }
+    }
+    if ((e = ensure_smem((const void *)k_mog_decode<GT>, (size_t)m.total)) != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[0], s)) != cudaSuccess) return e;
-    const int P1 = (int)ceil_div64(dv.c_max, SC_SLICE);
-    if ((e = launch_pdl(k_dec_score<GT>, dim3(P1, dv.units), dim3(SC_THREADS), 0, s, a)) != cudaSuccess)
+    if ((e = launch_ex(k_mog_decode<GT>, dim3(cs, dv.units), dim3(MD_THREADS), m.total, s, cs, a, m)) !=
+        cudaSuccess)
         return e;
-    if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
-    const size_t sm = slot_smem_bytes(dv.G, dv.c_max, dv.tc);
-    if ((e = ensure_smem((const void *)k_dec_slot<GT>, sm)) != cudaSuccess) return e;
-    const int nslot = max(1, min(dv.c_max, dv.G * dv.tc));
-    if ((e = launch_pdl(k_dec_slot<GT>, dim3(SL_ANCHOR + SL_SPLIT * nslot, dv.units), dim3(AT_THREADS), sm, s,
-                        a)) != cudaSuccess)
-        return e;
-    if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
-    if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
+    if (events)
+        for (int i = 1; i < 4; ++i)
+            if ((e = cudaEventRecord(events[i], s)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
@@ -674,6 +794,10 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
         e = cudaMemcpyAsync(sel_out, dv.sel, sizeof(int32_t) * (size_t)dv.units * G * a.SW,
                             cudaMemcpyDeviceToDevice, s);
     return e;
+}
+
+size_t slot_smem_bytes(int G, int c_max, int tc) {
+    return (size_t)md_layout(G, tc, c_max, MOG_MAX_L, 1, 2).total;
 }
 
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
