@@ -181,7 +181,7 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     m.spos = take(4 * SUPER, 16);
     m.smk = take(4 * SUPER, 16);
     const int tiles = stages * AT_STAGE_BYTES;
-    const int resb = (m.SPC * l_max + RCH) * MOG_D * 4;
+    const int resb = (2 * l_max + RCH) * MOG_D * 4;  // two slots' subcluster means + a cluster chunk
     m.area = take(tiles > resb ? tiles : resb, 128);
     m.total = (o + 15) & ~15;
     return m;
@@ -374,18 +374,21 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
     // ----------------------------------------- P3: this CTA's union slots, residual
     const int nmy = Uc > k ? (Uc - k + CS - 1) / CS : 0;  // slots k, k+CS, ...
     const bool resid = dv.residual != 0;
-    float *vst = reinterpret_cast<float *>(area);           // [SPC*l_max][d] subcluster means
-    float *vcl = vst + (size_t)m.SPC * dv.l_max * MOG_D;    // [RCH][d] slice cluster means
+    float *vst = reinterpret_cast<float *>(area);           // [2][l_max][d] subcluster means
+    float *vcl = vst + (size_t)2 * dv.l_max * MOG_D;        // [RCH][d] slice cluster means
+    auto stage_subs = [&](int s) {  // value means of slot s's subclusters -> buffer s % 2
+        const size_t g0 = usg + (size_t)ucl[k + s * CS] * L;
+        for (int e = tid; e < L * 32; e += MD_THREADS)
+            cp_async16(smem_u32(vst + ((size_t)(s & 1) * dv.l_max + e / 32) * MOG_D + 4 * (e % 32)),
+                       dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
+    };
     for (int s = 0; s < nmy; ++s) {
         const int c = ucl[k + s * CS];
         const size_t g0 = usg + (size_t)c * L;
         const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
         if (tid <= L) sso[s * (MOG_MAX_L + 1) + tid] = so[tid];
         if (tid < L) snn[s * MOG_MAX_L + tid] = dv.sub_n[g0 + tid];
-        if (resid)
-            for (int e = tid; e < L * 32; e += MD_THREADS)
-                cp_async16(smem_u32(vst + ((size_t)s * dv.l_max + e / 32) * MOG_D + 4 * (e % 32)),
-                           dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
+        if (resid && s < 2) stage_subs(s);
         const int l = tid >> 2;
         const bool valid = l < L;
         float res[GT], sl[GT];
@@ -493,6 +496,14 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
             cp_async_wait<0>();
             __syncthreads();
             for (int s = 0; s < nmy; ++s) {
+                if (s >= 2) {  // slots beyond the first two: their means now
+                    __syncwarp();
+                    __syncthreads();
+                    stage_subs(s);
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    __syncthreads();
+                }
                 const int c = ucl[k + s * CS];
                 uint32_t hm = 0u;
                 for (int q = 0; q < G * tc; ++q)
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
                 for (int l = 0; l < L; ++l) {
                     if (snn[s * MOG_MAX_L + l] <= 0) continue;
                     const uint32_t need = hm & ~smask[s * MOG_MAX_L + l];
-                    const float *vrow = vst + ((size_t)s * dv.l_max + l) * MOG_D + 4 * lane;
+                    const float *vrow = vst + ((size_t)(s & 1) * dv.l_max + l) * MOG_D + 4 * lane;
 #pragma unroll
                     for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) {
                         const int g = warp + AT_WARPS * kk;
@@ -796,8 +807,8 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
     return e;
 }
 
-size_t slot_smem_bytes(int G, int c_max, int tc) {
-    return (size_t)md_layout(G, tc, c_max, MOG_MAX_L, 1, 2).total;
+size_t slot_smem_bytes(int G, int c_max, int tc) {  // the smallest layout (16-CTA clusters)
+    return (size_t)md_layout(G, tc, c_max, MOG_MAX_L, 16, 2).total;
 }
 
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
