@@ -132,7 +132,7 @@ constexpr int RCH = 32;                   // slice clusters staged per residual 
 
 // Shared-memory layout of the decode kernel (byte offsets, 16-byte aligned).
 struct MdLay {
-    int CS, SL, NSLOT, SPC, stages;
+    int CS, SL, KC, NSLOT, SPC, stages;  // KC: candidates per slice and head
     int cand_s, cand_i, pub_cnt, pub_coff, pub_state;                // read by other CTAs
     int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl, ucoff, pre;  // local
     int sres, ssl, snn, sso, spref, smask, wst, rst, spos, smk, area;
@@ -151,11 +151,12 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     const int tcc = tc > 0 ? tc : 1;
     m.CS = CS;
     m.SL = (c_max + CS - 1) / CS;
+    m.KC = m.SL < tcc ? m.SL : tcc;
     m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
     m.SPC = (m.NSLOT + CS - 1) / CS;
     m.stages = stages;
-    m.cand_s = take(4 * G * tcc, 16);
-    m.cand_i = take(4 * G * tcc, 16);
+    m.cand_s = take(4 * G * m.KC, 16);
+    m.cand_i = take(4 * G * m.KC, 16);
     m.pub_cnt = take(4 * m.SPC, 16);
     m.pub_coff = take(4 * m.SPC, 16);
     m.pub_state = take(4 * G * PART_W, 16);
@@ -163,8 +164,8 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     m.csl = take(4 * G * m.SL, 16);
     m.crs = take(4 * G * m.SL, 16);
     m.cnn = take(4 * m.SL, 16);
-    m.allc_s = take(4 * CS * G * tcc, 16);
-    m.allc_i = take(4 * CS * G * tcc, 16);
+    m.allc_s = take(4 * CS * G * m.KC, 16);
+    m.allc_i = take(4 * CS * G * m.KC, 16);
     m.selc = take(4 * G * tcc, 16);
     m.bm = take(4 * ((c_max + 31) / 32), 16);
     m.ucl = take(4 * m.NSLOT, 16);
@@ -266,21 +267,22 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
         }
     }
     __syncthreads();
-    if (tc > 0) {  // this slice's top-tc per head, sorted, as (score, cluster) with -1 padding
-        const int span = max(ns, tc);
+    const int KC = m.KC;
+    if (tc > 0) {  // this slice's top-KC per head (KC = min(slice, tc)), sorted, -1 padded
+        const int span = max(ns, KC);
         for (int e = tid; e < G * span; e += MD_THREADS) {
             const int g = e / span, i = e % span;
             if (i < ns) {
                 const float v = csl[g * m.SL + i];
                 int rank = 0;
                 for (int kk = 0; kk < ns; ++kk) rank += ranks_before(csl[g * m.SL + kk], kk, v, i);
-                if (rank < tc) {
-                    cand_s[g * tc + rank] = v;
-                    cand_i[g * tc + rank] = v == -INFINITY ? -1 : c0 + i;
+                if (rank < KC) {
+                    cand_s[g * KC + rank] = v;
+                    cand_i[g * KC + rank] = v == -INFINITY ? -1 : c0 + i;
                 }
             } else {
-                cand_s[g * tc + i] = -INFINITY;
-                cand_i[g * tc + i] = -1;
+                cand_s[g * KC + i] = -INFINITY;
+                cand_i[g * KC + i] = -1;
             }
         }
     }
@@ -297,31 +299,31 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
                 selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
             }
         } else {
-            for (int e = tid; e < CS * G * tc; e += MD_THREADS) {  // gather [g][src][r]
-                const int src = e / (G * tc), rem = e % (G * tc), g = rem / tc, r = rem % tc;
+            for (int e = tid; e < CS * G * KC; e += MD_THREADS) {  // gather [g][src][r]
+                const int src = e / (G * KC), rem = e % (G * KC), g = rem / KC, r = rem % KC;
                 const float *rs = cluster.map_shared_rank(cand_s, src);
                 const int *ri = cluster.map_shared_rank(cand_i, src);
-                allc_s[(g * CS + src) * tc + r] = rs[rem];
-                allc_i[(g * CS + src) * tc + r] = ri[rem];
+                allc_s[(g * CS + src) * KC + r] = rs[rem];
+                allc_i[(g * CS + src) * KC + r] = ri[rem];
             }
             __syncthreads();
             // element (g, list p, position r): rank over all lists of head g = r plus, for
             // every other list, the length of its prefix that ranks before the element
-            for (int e = tid; e < G * CS * tc; e += MD_THREADS) {
-                const int g = e / (CS * tc), pr = e % (CS * tc), pl = pr / tc, r = pr % tc;
-                const float *cs = allc_s + (size_t)g * CS * tc;
-                const int *ci = allc_i + (size_t)g * CS * tc;
+            for (int e = tid; e < G * CS * KC; e += MD_THREADS) {
+                const int g = e / (CS * KC), pr = e % (CS * KC), pl = pr / KC, r = pr % KC;
+                const float *cs = allc_s + (size_t)g * CS * KC;
+                const int *ci = allc_i + (size_t)g * CS * KC;
                 const int x = ci[pr];
                 if (x < 0) continue;
                 const float v = cs[pr];
                 int rank = r;
                 for (int q = 0; q < CS && rank < tc; ++q) {
                     if (q == pl) continue;
-                    int lo = 0, hi = tc;
+                    int lo = 0, hi = KC;
                     while (lo < hi) {
                         const int mid = (lo + hi) >> 1;
-                        const int xm = ci[q * tc + mid];
-                        if (xm >= 0 && ranks_before(cs[q * tc + mid], xm, v, x)) lo = mid + 1;
+                        const int xm = ci[q * KC + mid];
+                        if (xm >= 0 && ranks_before(cs[q * KC + mid], xm, v, x)) lo = mid + 1;
                         else hi = mid;
                     }
                     rank += lo;
