@@ -209,6 +209,25 @@ int dense_decode(const mog_kv *kv, const int32_t *lengths_dev, int32_t n_max, in
                  void *scratch_dev, size_t scratch_bytes, void *stream);
 
 /*
+ * dense_decode without a scratch argument.  No counterpart in the papers: this entry point
+ * exists for callers that cannot allocate device memory -- for example a serving engine
+ * that has handed its whole device budget to a preallocated KV pool and forbids further
+ * cudaMalloc, or code that runs where allocation is not allowed or would stall other work.
+ * The split partials live in a library-owned static device array of 4 MiB (every GPU that
+ * loads the library holds it until the process exits); shapes that need more return
+ * MOG_ERR_CAPACITY (mog_last_error states the sizes).  Nothing is allocated, by the
+ * library or any routine it calls.
+ *  - The first call on a device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, and each call rewrites all of it that
+ *    it reads; calls that overlap on the GPU (other streams, other threads) race.
+ * Arguments as dense_decode.
+ */
+int dense_decode_noalloc(const mog_kv *kv, const int32_t *lengths_dev, int32_t n_max,
+                         int32_t batch, int32_t h_kv, int32_t h_q, int32_t d, const void *q_dev,
+                         float *out_dev, void *stream);
+
+/*
  * Test export of one first-level k-means assignment step ([IA]'s partition, computed by
  * a Lloyd step): for each of the n rows x_i (bf16, row stride ld elements),
  * assign_out_dev[i] = argmin_c sum_j (x_ij - cent_cj)^2 with the lowest index on ties,

@@ -70,6 +70,8 @@ _SIGS = {
     "dense_decode_scratch_bytes": (C.c_int, [C.c_int32] * 5 + [_P]),
     "dense_decode": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                _P, _P, _P, C.c_size_t, _P]),
+    "dense_decode_noalloc": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                       C.c_int32, _P, _P, _P]),
     "mog_kmeans_assign_scratch_bytes": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, _P]),
     "mog_kmeans_assign": (C.c_int, [_P, C.c_int64, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P,
                                     C.c_size_t, _P, _P]),
@@ -274,6 +276,17 @@ def dense_decode(K, V, lengths_dev, n_max, q, out=None, scratch=None, stream=Non
     _check(lib().dense_decode(C.byref(kv), _ptr(lengths_dev), n_max, B, H_kv, H_q, 128, _ptr(q),
                               _ptr(out), _ptr(scratch), scratch.numel(), _stream(stream)),
            "dense_decode")
+    return out
+
+
+def dense_decode_noalloc(K, V, lengths_dev, n_max, q, out, stream=None):
+    """dense_decode whose scratch is the library's static device array: no device memory
+    is allocated by this call (the caller supplies `out`)."""
+    B, H_kv = K.shape[0], K.shape[1]
+    kv = _kv(K, V)
+    _check(lib().dense_decode_noalloc(C.byref(kv), _ptr(lengths_dev), n_max, B, H_kv, q.shape[1],
+                                      128, _ptr(q), _ptr(out), _stream(stream)),
+           "dense_decode_noalloc")
     return out
 
 

@@ -538,6 +538,34 @@ extern "C" int dense_decode(const mog_kv *kv, const int32_t *lengths_dev, int32_
     return MOG_OK;
 }
 
+extern "C" int dense_decode_noalloc(const mog_kv *kv, const int32_t *lengths_dev, int32_t n_max,
+                                    int32_t batch, int32_t h_kv, int32_t h_q, int32_t d,
+                                    const void *q_dev, float *out_dev, void *stream) {
+    size_t need = 0;
+    int st = dense_decode_scratch_bytes(batch, h_kv, h_q, d, n_max, &need);
+    if (st != MOG_OK) return st;
+    if ((st = check_kv(kv, batch, h_kv, n_max)) != MOG_OK) return st;
+    if (!lengths_dev || !q_dev || !out_dev) return MOG_ERR_INVALID_ARG;
+    if (!aligned16(q_dev) || !aligned16(out_dev)) return MOG_ERR_INVALID_ARG;
+    float *scratch = nullptr;
+    size_t cap = 0;
+    CK(dense_static_scratch(&scratch, &cap));  // set-up on the first call on a device
+    if (need > cap) {
+        snprintf(g_err, sizeof g_err,
+                 "dense_decode_noalloc: this shape needs %zu bytes of scratch, the static "
+                 "array holds %zu",
+                 need, cap);
+        return MOG_ERR_CAPACITY;
+    }
+    const int units = batch * h_kv;
+    cudaError_t e = launch_dense(static_cast<const uint16_t *>(kv->k), static_cast<const uint16_t *>(kv->v),
+                                 kv->stride_b, kv->stride_h, kv->stride_n, lengths_dev, n_max, batch,
+                                 h_kv, h_q / h_kv, q_dev, out_dev, scratch, dense_splits(units, n_max),
+                                 static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dense_decode_noalloc launch");
+    return MOG_OK;
+}
+
 // ----------------------------------------------------------------- parity exports
 
 extern "C" int mog_kmeans_assign_scratch_bytes(int32_t n, int32_t k, int32_t d, size_t *bytes) {

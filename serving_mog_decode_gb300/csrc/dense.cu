@@ -4,6 +4,10 @@
 // Abstract: decoding over a long context normally scans the whole KV cache; this is that
 // scan.  Split-KV: each (KV head, split) CTA streams a contiguous key range through the
 // attention engine and writes a partial (max, sum, acc); a second kernel merges them.
+#include <stdio.h>
+
+#include <mutex>
+
 #include "attend.cuh"
 #include "internal.h"
 
@@ -97,6 +101,38 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
     k_dense_split<<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
     k_dense_merge<<<U, MERGE_THREADS, MERGE_SMEM, s>>>(a);
     return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------
+// dense_decode_noalloc: dense_decode with its partial results in a fixed device array that
+// the library owns, for callers that cannot allocate device memory.
+// ------------------------------------------------------------------------------------
+
+// Scratch for the split partials of dense_decode_noalloc.  Every GPU that loads the library
+// keeps this array until the process exits.
+constexpr size_t DENSE_STATIC_BYTES = 4u << 20;
+static __device__ __align__(256) float g_dense_static[DENSE_STATIC_BYTES / sizeof(float)];
+
+// Device address of g_dense_static for the current device.  In host code the symbol is
+// only a stand-in, never an address a kernel may use, so the address is asked for once per
+// device (with that device current) and cached.
+cudaError_t dense_static_scratch(float **ptr, size_t *bytes) {
+    static std::mutex mu;
+    static float *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dense_static);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<float *>(p);
+    }
+    *ptr = addr[dev];
+    *bytes = DENSE_STATIC_BYTES;
+    return cudaSuccess;
 }
 
 }  // namespace mog

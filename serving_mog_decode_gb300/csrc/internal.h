@@ -83,6 +83,7 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
                          int G, const void *q, float *out, float *scratch, int splits,
                          cudaStream_t s);
 int dense_splits(int units, int n_max);
+cudaError_t dense_static_scratch(float **ptr, size_t *bytes);
 size_t slot_smem_bytes(int G, int c_max, int tc);
 cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
                              int32_t *assign, int *changed, int *fb_list, int *fb_cnt,
