@@ -85,13 +85,13 @@ __device__ __forceinline__ void issue_tile(uint8_t *stage, int nrows, const uint
     }
 }
 
-// Consume one tile (already in shared memory) into this warp's accumulator.
-__device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[8][4],
-                                             const uint8_t *stage, float scale2) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t sk = smem_u32(stage), sv = sk + AT_TILE_BYTES;
-    const uint32_t *smask = reinterpret_cast<const uint32_t *>(stage + 2 * AT_TILE_BYTES);
-    const int rbase = w * 16;
+// Consume 16 rows (keys) rbase..rbase+15 of a shared-memory K/V block into this warp's
+// accumulator.  sk, sv: shared addresses of the swizzled K and V rows; smask: per-row head
+// masks (bit g set: head g attends to the row).
+__device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa)[8][4],
+                                               uint32_t sk, uint32_t sv, const uint32_t *smask,
+                                               int rbase, float scale2) {
+    const int lane = threadIdx.x & 31;
     float s[2][4];
 #pragma unroll
     for (int t = 0; t < 2; ++t)
@@ -143,12 +143,14 @@ __device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[
         }
     acc.l[0] = acc.l[0] * al0 + ps0;
     acc.l[1] = acc.l[1] * al1 + ps1;
+    if (al0 != 1.f || al1 != 1.f) {  // the running max moved: rescale the output
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-        acc.o[t][0] *= al0;
-        acc.o[t][1] *= al0;
-        acc.o[t][2] *= al1;
-        acc.o[t][3] *= al1;
+        for (int t = 0; t < 16; ++t) {
+            acc.o[t][0] *= al0;
+            acc.o[t][1] *= al0;
+            acc.o[t][2] *= al1;
+            acc.o[t][3] *= al1;
+        }
     }
     uint32_t ahi[4], alo[4];
     {
@@ -175,6 +177,40 @@ __device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[
             mma_bf16(acc.o[dt + 1], alo, b2, b3);
         }
     }
+}
+
+// Consume one 64-row tile (already in shared memory): warp w takes rows 16w..16w+15.
+__device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[8][4],
+                                             const uint8_t *stage, float scale2) {
+    const uint32_t sk = smem_u32(stage);
+    compute_rows16(acc, qa, sk, sk + AT_TILE_BYTES,
+                   reinterpret_cast<const uint32_t *>(stage + 2 * AT_TILE_BYTES),
+                   (threadIdx.x >> 5) * 16, scale2);
+}
+
+// ---- per-warp pipeline: a warp streams its own 16-row blocks, no block-wide barrier ----
+constexpr int WB_ROWS = 16;
+constexpr int WB_KV = WB_ROWS * AT_ROW_BYTES;            // 4 KB of K (or V)
+constexpr int WB_BYTES = 2 * WB_KV + WB_ROWS * 4;         // K, V, masks: 8256 bytes
+
+// Copy a warp's block of nb <= 16 rows into buf: lane r < 16 holds row r's position `pos`
+// and head mask `mk`; rows >= nb are zero-filled with mask 0.
+__device__ __forceinline__ void warp_issue_block(uint8_t *buf, int nb, int pos, uint32_t mk,
+                                                 const uint16_t *kbase, const uint16_t *vbase,
+                                                 int64_t sn) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t sk = smem_u32(buf), sv = sk + WB_KV;
+    const int ch = lane & 15;
+#pragma unroll
+    for (int i = 0; i < WB_ROWS / 2; ++i) {
+        const int r = (lane >> 4) + 2 * i;
+        const int pr = __shfl_sync(0xffffffffu, pos, r);
+        const bool ok = r < nb;
+        const int64_t off = ok ? (int64_t)pr * sn + ch * 8 : 0;
+        cp_async16(sk + swz(r, ch), kbase + off, ok ? 16 : 0);
+        cp_async16(sv + swz(r, ch), vbase + off, ok ? 16 : 0);
+    }
+    if (lane < WB_ROWS) reinterpret_cast<uint32_t *>(buf + 2 * WB_KV)[lane] = lane < nb ? mk : 0u;
 }
 
 // Partial result layout: per head, [0] = m (log2 domain), [1] = l, [2], [3] unused,

@@ -126,20 +126,22 @@ struct OnlineAcc {
     }
 };
 
-constexpr int MD_THREADS = AT_THREADS;  // 4 warps (the attention engine's geometry)
-constexpr int SUPER = 256;                // row positions resolved per pass
-constexpr int RCH = 32;                   // slice clusters staged per residual pass
+constexpr int RCH = 64;  // slice clusters staged per residual pass
 
-// Shared-memory layout of the decode kernel (byte offsets, 16-byte aligned).
+__host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
+
+// Shared-memory layout of the decode kernel (byte offsets).
 struct MdLay {
-    int CS, SL, KC, NSLOT, SPC, stages;  // KC: candidates per slice and head
+    int CS, SL, KC, NSLOT, SPC, warps;  // KC: candidates per slice and head
     int cand_s, cand_i, pub_cnt, pub_coff, pub_state;                // read by other CTAs
     int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl, ucoff, pre;  // local
-    int sres, ssl, snn, sso, spref, smask, wst, rst, spos, smk, area;
+    int sres, ssl, snn, sso, spref, smask, rst, area;
     int total;
 };
 
-__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int stages) {
+// area: the per-warp row buffers in P4; before that the staged value means and the
+// residual warp states of P3; after P4 the warp states of the merge.
+__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps) {
     MdLay m;
     int o = 0;
     auto take = [&](int bytes, int align) {
@@ -150,11 +152,11 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     };
     const int tcc = tc > 0 ? tc : 1;
     m.CS = CS;
+    m.warps = warps;
     m.SL = (c_max + CS - 1) / CS;
     m.KC = m.SL < tcc ? m.SL : tcc;
     m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
     m.SPC = (m.NSLOT + CS - 1) / CS;
-    m.stages = stages;
     m.cand_s = take(4 * G * m.KC, 16);
     m.cand_i = take(4 * G * m.KC, 16);
     m.pub_cnt = take(4 * m.SPC, 16);
@@ -177,20 +179,21 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     m.sso = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
-    m.wst = take(4 * AT_WARPS * G * PART_W, 16);
-    m.rst = take(4 * G * PART_W, 16);  // right after wst: 5 contiguous states
-    m.spos = take(4 * SUPER, 16);
-    m.smk = take(4 * SUPER, 16);
-    const int tiles = stages * AT_STAGE_BYTES;
-    const int resb = (2 * l_max + RCH) * MOG_D * 4;  // two slots' subcluster means + a cluster chunk
-    m.area = take(tiles > resb ? tiles : resb, 128);
+    m.rst = take(4 * G * PART_W, 16);
+    const int rows = warps * 2 * WB_BYTES;
+    const int p3 = (m.SPC * l_max + RCH) * MOG_D * 4 + warps * G * PART_W * 4;
+    const int mrg = (warps + 1) * G * PART_W * 4;
+    int a = rows > p3 ? rows : p3;
+    a = a > mrg ? a : mrg;
+    m.area = take(a, 128);
     m.total = (o + 15) & ~15;
     return m;
 }
 
 template <int GT>
-__global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
+__global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, MdLay m) {
     namespace cg = cooperative_groups;
+    constexpr int W = md_warps(GT), NT = W * 32;
     extern __shared__ __align__(128) uint8_t sm[];
     cg::cluster_group cluster = cg::this_cluster();
     const Dev &dv = a.dv;
@@ -220,12 +223,9 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
     int *sso = reinterpret_cast<int *>(sm + m.sso);
     int *spref = reinterpret_cast<int *>(sm + m.spref);
     uint32_t *smask = reinterpret_cast<uint32_t *>(sm + m.smask);
-    float *wst = reinterpret_cast<float *>(sm + m.wst);
     float *rst = reinterpret_cast<float *>(sm + m.rst);
-    int *spos = reinterpret_cast<int *>(sm + m.spos);
-    uint32_t *smk = reinterpret_cast<uint32_t *>(sm + m.smk);
     uint8_t *area = sm + m.area;
-    __shared__ int s_wsum[AT_WARPS], s_uc;
+    __shared__ int s_wsum[W], s_uc;
 
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int b = ui[UI_B], h = u % dv.h_kv, C = ui[UI_C], L = ui[UI_L];
@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
     const size_t usg = (size_t)u * dv.c_max * dv.l_max;   // subcluster index base
     const uint16_t *qg = a.q + (size_t)u * G * MOG_D;
     int *selu = dv.sel + (size_t)u * G * a.SW;
+    const bool resid = dv.residual != 0;
 
     // ------------------------------------------------------------ P0: query, weights
     uint32_t qa[8][4];
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
     // ------------------------------------------------- P1: score this CTA's clusters
     const int c0 = k * m.SL;
     const int ns = max(0, min(C - c0, m.SL));
-    for (int base = 0; base < ns; base += MD_THREADS / 4) {
+    for (int base = 0; base < ns; base += NT / 4) {
         const int cl = base + (tid >> 2);
         const bool valid = cl < ns;
         const int c = c0 + (valid ? cl : 0);
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
     const int KC = m.KC;
     if (tc > 0) {  // this slice's top-KC per head (KC = min(slice, tc)), sorted, -1 padded
         const int span = max(ns, KC);
-        for (int e = tid; e < G * span; e += MD_THREADS) {
+        for (int e = tid; e < G * span; e += NT) {
             const int g = e / span, i = e % span;
             if (i < ns) {
                 const float v = csl[g * m.SL + i];
@@ -286,30 +287,28 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
             }
         }
     }
-    for (int e = tid; e < G * tcc; e += MD_THREADS) selc[e] = -1;
-    for (int e = tid; e < (dv.c_max + 31) / 32; e += MD_THREADS) bm[e] = 0u;
+    for (int e = tid; e < G * tcc; e += NT) selc[e] = -1;
+    for (int e = tid; e < (dv.c_max + 31) / 32; e += NT) bm[e] = 0u;
     cluster.sync();  // S1: candidates of every slice are published
 
     // ------------------------------------------------------- P2: selection and union
     if (tc > 0) {
         if (a.sel_in) {
-            for (int e = tid; e < G * tc; e += MD_THREADS) {
+            for (int e = tid; e < G * tc; e += NT) {
                 const int g = e / tc, r = e % tc;
                 const int cc = a.sel_in[((size_t)u * G + g) * a.SW + r];
                 selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
             }
         } else {
-            for (int e = tid; e < CS * G * KC; e += MD_THREADS) {  // gather [g][src][r]
+            for (int e = tid; e < CS * G * KC; e += NT) {  // gather [g][src][r]
                 const int src = e / (G * KC), rem = e % (G * KC), g = rem / KC, r = rem % KC;
-                const float *rs = cluster.map_shared_rank(cand_s, src);
-                const int *ri = cluster.map_shared_rank(cand_i, src);
-                allc_s[(g * CS + src) * KC + r] = rs[rem];
-                allc_i[(g * CS + src) * KC + r] = ri[rem];
+                allc_s[(g * CS + src) * KC + r] = cluster.map_shared_rank(cand_s, src)[rem];
+                allc_i[(g * CS + src) * KC + r] = cluster.map_shared_rank(cand_i, src)[rem];
             }
             __syncthreads();
             // element (g, list p, position r): rank over all lists of head g = r plus, for
             // every other list, the length of its prefix that ranks before the element
-            for (int e = tid; e < G * CS * KC; e += MD_THREADS) {
+            for (int e = tid; e < G * CS * KC; e += NT) {
                 const int g = e / (CS * KC), pr = e % (CS * KC), pl = pr / KC, r = pr % KC;
                 const float *cs = allc_s + (size_t)g * CS * KC;
                 const int *ci = allc_i + (size_t)g * CS * KC;
@@ -333,12 +332,12 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
         }
     }
     __syncthreads();
-    for (int e = tid; e < G * tc; e += MD_THREADS)
+    for (int e = tid; e < G * tc; e += NT)
         if (selc[e] >= 0) atomicOr(&bm[selc[e] >> 5], 1u << (selc[e] & 31));
     __syncthreads();
     {  // union = set bits of bm, ascending: ucl[0 .. Uc)
         const int nw = (dv.c_max + 31) / 32;
-        const int per = (nw + MD_THREADS - 1) / MD_THREADS;
+        const int per = (nw + NT - 1) / NT;
         const int w0 = tid * per, w1 = min(nw, w0 + per);
         int cnt = 0;
         for (int i = w0; i < w1; ++i) cnt += __popc(bm[i]);
@@ -352,7 +351,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
         __syncthreads();
         int base = incl - cnt;
         for (int kk = 0; kk < warp; ++kk) base += s_wsum[kk];
-        if (tid == MD_THREADS - 1) s_uc = base + cnt;
+        if (tid == NT - 1) s_uc = base + cnt;
         for (int i = w0; i < w1; ++i) {
             uint32_t bits = bm[i];
             while (bits) {
@@ -365,7 +364,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
     __syncthreads();
     const int Uc = s_uc;
     if (k == 0) {  // the cluster part of the exported selection
-        for (int e = tid; e < G * tc; e += MD_THREADS) {
+        for (int e = tid; e < G * tc; e += NT) {
             const int g = e / tc, r = e % tc;
             selu[(size_t)g * a.SW + r] = selc[e];
             if (selc[e] < 0)
@@ -375,27 +374,38 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
 
     // ----------------------------------------- P3: this CTA's union slots, residual
     const int nmy = Uc > k ? (Uc - k + CS - 1) / CS : 0;  // slots k, k+CS, ...
-    const bool resid = dv.residual != 0;
-    float *vst = reinterpret_cast<float *>(area);           // [2][l_max][d] subcluster means
-    float *vcl = vst + (size_t)2 * dv.l_max * MOG_D;        // [RCH][d] slice cluster means
-    auto stage_subs = [&](int s) {  // value means of slot s's subclusters -> buffer s % 2
-        const size_t g0 = usg + (size_t)ucl[k + s * CS] * L;
-        for (int e = tid; e < L * 32; e += MD_THREADS)
-            cp_async16(smem_u32(vst + ((size_t)(s & 1) * dv.l_max + e / 32) * MOG_D + 4 * (e % 32)),
-                       dv.sub_vbar + (g0 + e / 32) * MOG_D + 4 * (e % 32), 16);
-    };
-    for (int s = 0; s < nmy; ++s) {
+    const int npair = nmy * L;                              // (slot, subcluster) pairs
+    float *vst = reinterpret_cast<float *>(area);           // [SPC*l_max][d] subcluster means
+    float *vcl = vst + (size_t)m.SPC * dv.l_max * MOG_D;    // [RCH][d] slice cluster means
+    float *rws = vcl + (size_t)RCH * MOG_D;                 // [W][G][PART_W] residual states
+    for (int e = tid; e < nmy * (L + 1); e += NT) {
+        const int s = e / (L + 1), i = e % (L + 1);
         const int c = ucl[k + s * CS];
-        const size_t g0 = usg + (size_t)c * L;
-        const int *so = dv.sub_off + (size_t)u * dv.sub_off_stride + (size_t)c * L;
-        if (tid <= L) sso[s * (MOG_MAX_L + 1) + tid] = so[tid];
-        if (tid < L) snn[s * MOG_MAX_L + tid] = dv.sub_n[g0 + tid];
-        if (resid && s < 2) stage_subs(s);
-        const int l = tid >> 2;
-        const bool valid = l < L;
+        sso[s * (MOG_MAX_L + 1) + i] = dv.sub_off[(size_t)u * dv.sub_off_stride + (size_t)c * L + i];
+        if (i < L) snn[s * MOG_MAX_L + i] = dv.sub_n[usg + (size_t)c * L + i];
+    }
+    if (resid)
+        for (int e = tid; e < npair * 32; e += NT) {
+            const int pr = e / 32, s = pr / L, l = pr % L;
+            cp_async16(smem_u32(vst + ((size_t)s * dv.l_max + l) * MOG_D + 4 * (e % 32)),
+                       dv.sub_vbar + (usg + (size_t)ucl[k + s * CS] * L + l) * MOG_D + 4 * (e % 32), 16);
+        }
+    auto stage_slice = [&](int k0) {
+        const int cnt = min(RCH, ns - k0);
+        for (int e = tid; e < cnt * 32; e += NT)
+            cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
+                       dv.cl_vbar + (ug + c0 + k0 + e / 32) * MOG_D + 4 * (e % 32), 16);
+    };
+    if (resid && ns > 0) stage_slice(0);
+    cp_async_commit();
+    for (int base = 0; base < npair; base += NT / 4) {  // subcluster scores, 4 lanes a pair
+        const int pr = base + (tid >> 2);
+        const bool valid = pr < npair;
+        const int s = valid ? pr / L : 0, l = valid ? pr % L : 0;
+        const size_t gi = usg + (valid ? (size_t)ucl[k + s * CS] * L + l : 0);
         float res[GT], sl[GT];
-        quad_scores<GT>(dv.sub_ms + (g0 + (valid ? l : 0)) * 2 * MOG_D, valid ? dv.sub_n[g0 + l] : 0,
-                        valid, w, G, dv.score_mode, res, sl);
+        quad_scores<GT>(dv.sub_ms + gi * 2 * MOG_D, valid ? dv.sub_n[gi] : 0, valid, w, G,
+                        dv.score_mode, res, sl);
         if (valid && (tid & 3) == 0) {
 #pragma unroll
             for (int g = 0; g < GT; ++g)
@@ -404,28 +414,11 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
                     ssl[(s * G + g) * MOG_MAX_L + l] = sl[g];
                 }
         }
-        if (tid < MOG_MAX_L) smask[s * MOG_MAX_L + tid] = 0u;
     }
-    // slice clusters that some head did not select: value means, first chunk
-    auto need_cluster = [&](int cl) -> uint32_t {
-        const int c = c0 + cl;
-        if (cnn[cl] <= 0) return 0u;
-        uint32_t chose = 0u;
-        for (int q = 0; q < G * tc; ++q)
-            if (selc[q] == c) chose |= 1u << (q / tc);
-        return allm & ~chose;
-    };
-    auto stage_slice = [&](int k0) {
-        const int cnt = min(RCH, ns - k0);
-        for (int e = tid; e < cnt * 32; e += MD_THREADS)
-            cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
-                       dv.cl_vbar + (ug + c0 + k0 + e / 32) * MOG_D + 4 * (e % 32), 16);
-    };
-    if (resid && ns > 0) stage_slice(0);
-    cp_async_commit();
+    for (int e = tid; e < nmy * MOG_MAX_L; e += NT) smask[e] = 0u;
     __syncthreads();
     // top-ts subclusters of every head that chose a slot's cluster
-    for (int e = warp; e < nmy * G; e += AT_WARPS) {
+    for (int e = warp; e < nmy * G; e += W) {
         const int s = e / G, g = e % G;
         const int c = ucl[k + s * CS];
         int rk = -1;
@@ -456,7 +449,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
         }
     }
     __syncthreads();
-    for (int s = warp; s < nmy; s += AT_WARPS) {  // prefix of the chosen subclusters' sizes
+    for (int s = warp; s < nmy; s += W) {  // prefix of the chosen subclusters' sizes
         const int *so = sso + s * (MOG_MAX_L + 1);
         const int cnt = lane < L && smask[s * MOG_MAX_L + lane] ? so[lane + 1] - so[lane] : 0;
         int incl = cnt;
@@ -481,7 +474,7 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
             const int *sp = spref + s * (MOG_MAX_L + 1);
             const int *so = sso + s * (MOG_MAX_L + 1);
             const int tot = sp[L];
-            for (int i = tid; i < tot; i += MD_THREADS) {
+            for (int i = tid; i < tot; i += NT) {
                 int kk = 0;
                 while (sp[kk + 1] <= i) ++kk;
                 rowpos[so[0] + i] = perm[so[kk] + (i - sp[kk])];
@@ -489,38 +482,27 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
             }
         }
     }
-    // Gaussian residual: thread (warp, lane) owns dims 4*lane..+3 of heads warp, warp+4, ..
+    // Gaussian residual: warps take items (pairs, then slice clusters) round-robin; lane
+    // owns dims 4*lane..+3; per-warp states are merged into rst
     {
-        OnlineAcc st[MOG_MAX_G / AT_WARPS];
+        OnlineAcc st[GT];
 #pragma unroll
-        for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) st[kk].init();
+        for (int g = 0; g < GT; ++g) st[g].init();
         if (resid) {
             cp_async_wait<0>();
             __syncthreads();
-            for (int s = 0; s < nmy; ++s) {
-                if (s >= 2) {  // slots beyond the first two: their means now
-                    __syncwarp();
-                    __syncthreads();
-                    stage_subs(s);
-                    cp_async_commit();
-                    cp_async_wait<0>();
-                    __syncthreads();
-                }
+            for (int e = warp; e < npair; e += W) {
+                const int s = e / L, l = e % L;
+                if (snn[s * MOG_MAX_L + l] <= 0) continue;
                 const int c = ucl[k + s * CS];
-                uint32_t hm = 0u;
+                uint32_t hm = 0u;  // heads that chose c
                 for (int q = 0; q < G * tc; ++q)
                     if (selc[q] == c) hm |= 1u << (q / tc);
-                for (int l = 0; l < L; ++l) {
-                    if (snn[s * MOG_MAX_L + l] <= 0) continue;
-                    const uint32_t need = hm & ~smask[s * MOG_MAX_L + l];
-                    const float *vrow = vst + ((size_t)(s & 1) * dv.l_max + l) * MOG_D + 4 * lane;
+                const uint32_t need = hm & ~smask[s * MOG_MAX_L + l];
+                const float *vrow = vst + ((size_t)s * dv.l_max + l) * MOG_D + 4 * lane;
 #pragma unroll
-                    for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) {
-                        const int g = warp + AT_WARPS * kk;
-                        if (g < G && ((need >> g) & 1u))
-                            st[kk].absorb(sres[(s * G + g) * MOG_MAX_L + l] * LOG2E, vrow);
-                    }
-                }
+                for (int g = 0; g < GT; ++g)
+                    if (g < G && ((need >> g) & 1u)) st[g].absorb(sres[(s * G + g) * MOG_MAX_L + l] * LOG2E, vrow);
             }
             for (int k0 = 0; k0 < ns; k0 += RCH) {
                 if (k0 > 0) {
@@ -531,28 +513,32 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
                     __syncthreads();
                 }
                 const int cnt = min(RCH, ns - k0);
-                for (int e = 0; e < cnt; ++e) {
-                    const uint32_t need = need_cluster(k0 + e);
+                for (int e = warp; e < cnt; e += W) {
+                    const int cl = k0 + e;
+                    if (cnn[cl] <= 0) continue;
+                    uint32_t chose = 0u;
+                    for (int q = 0; q < G * tc; ++q)
+                        if (selc[q] == c0 + cl) chose |= 1u << (q / tc);
+                    const uint32_t need = allm & ~chose;
                     const float *vrow = vcl + (size_t)e * MOG_D + 4 * lane;
 #pragma unroll
-                    for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) {
-                        const int g = warp + AT_WARPS * kk;
-                        if (g < G && ((need >> g) & 1u)) st[kk].absorb(crs[g * m.SL + k0 + e] * LOG2E, vrow);
-                    }
+                    for (int g = 0; g < GT; ++g)
+                        if (g < G && ((need >> g) & 1u)) st[g].absorb(crs[g * m.SL + cl] * LOG2E, vrow);
                 }
             }
         }
 #pragma unroll
-        for (int kk = 0; kk < MOG_MAX_G / AT_WARPS; ++kk) {
-            const int g = warp + AT_WARPS * kk;
-            if (g >= G) continue;
-            float *o = rst + (size_t)g * PART_W;
+        for (int g = 0; g < GT; ++g) {
+            if (g >= G) break;
+            float *o = rws + ((size_t)warp * G + g) * PART_W;
             if (lane == 0) {
-                o[0] = st[kk].m;
-                o[1] = st[kk].l;
+                o[0] = st[g].m;
+                o[1] = st[g].l;
             }
-            *reinterpret_cast<float4 *>(o + PART_ACC + 4 * lane) = st[kk].a;
+            *reinterpret_cast<float4 *>(o + PART_ACC + 4 * lane) = st[g].a;
         }
+        __syncthreads();
+        merge_states(rws, W, G, rst);
     }
     cp_async_wait<0>();
     cluster.sync();  // S2: row lists (global) and their counts (shared) are published
@@ -589,13 +575,15 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
     WarpAcc acc;
     acc.init();
     const float scale2 = dv.tau * LOG2E;
-    const int NSTG = m.stages;
-    for (int sb = r0; sb < r1; sb += SUPER) {
-        const int nrow = min(SUPER, r1 - sb);
-        for (int t = tid; t < nrow; t += MD_THREADS) {
-            const int i = sb + t;
-            int pos;
-            uint32_t mk;
+    {
+        // per-warp pipeline over 16-row blocks: warp w takes blocks w, w+W, ...
+        uint8_t *buf0 = area + (size_t)warp * 2 * WB_BYTES, *buf1 = buf0 + WB_BYTES;
+        const int nblk = (int)ceil_div64(r1 - r0, WB_ROWS);
+        auto resolve = [&](int bi, int &pos, uint32_t &mk) {  // lane's row of block bi
+            pos = 0;
+            mk = 0u;
+            const int i = r0 + bi * WB_ROWS + lane;
+            if (bi >= nblk || lane >= WB_ROWS || i >= r1) return;
             if (i < n_anchor) {
                 pos = i < s_cnt ? i : rlo + (i - s_cnt);
                 mk = allm;
@@ -615,43 +603,46 @@ __global__ void __launch_bounds__(MD_THREADS) k_mog_decode(DecArgs a, MdLay m) {
                 pos = 0;
                 mk = 0u;
             }
-            spos[t] = pos;
-            smk[t] = mk;
-        }
-        __syncthreads();
-        const int nt = (int)ceil_div64(nrow, AT_ROWS);
-        auto issue = [&](int t) {
-            const int rb = t * AT_ROWS;
-            issue_tile(area + (t % NSTG) * AT_STAGE_BYTES, min(AT_ROWS, nrow - rb), kb, vb, dv.sn,
-                       [&](int r, int64_t &pos, uint32_t &mk) {
-                           pos = spos[rb + r];
-                           mk = smk[rb + r];
-                       });
         };
-        for (int s = 0; s < NSTG - 1; ++s) {
-            if (s < nt) issue(s);
+        auto nrows_of = [&](int bi) { return min(WB_ROWS, r1 - (r0 + bi * WB_ROWS)); };
+        int bi = warp;
+        int pos;
+        uint32_t mk;
+        resolve(bi, pos, mk);
+        if (bi < nblk) warp_issue_block(buf0, nrows_of(bi), pos, mk, kb, vb, dv.sn);
+        cp_async_commit();
+        int npos;
+        uint32_t nmk;
+        resolve(bi + W, npos, nmk);
+        for (int t = 0; bi < nblk; ++t) {
+            const int nb = bi + W;
+            uint8_t *cur = (t & 1) ? buf1 : buf0, *nxt = (t & 1) ? buf0 : buf1;
+            if (nb < nblk) warp_issue_block(nxt, nrows_of(nb), npos, nmk, kb, vb, dv.sn);
             cp_async_commit();
-        }
-        for (int t = 0; t < nt; ++t) {
-            cp_async_wait_dyn(NSTG - 2);
-            __syncthreads();
-            if (t + NSTG - 1 < nt) issue(t + NSTG - 1);
-            cp_async_commit();
-            compute_tile(acc, qa, area + (t % NSTG) * AT_STAGE_BYTES, scale2);
+            resolve(nb + W, npos, nmk);  // positions one block ahead of the copies
+            cp_async_wait<1>();
+            __syncwarp();
+            const uint32_t sk = smem_u32(cur);
+            compute_rows16(acc, qa, sk, sk + WB_KV, reinterpret_cast<const uint32_t *>(cur + 2 * WB_KV), 0,
+                           scale2);
+            __syncwarp();
+            bi = nb;
         }
         cp_async_wait<0>();
-        __syncthreads();
     }
-    warp_state_out(acc, wst, G);
     __syncthreads();
-    merge_states(wst, AT_WARPS + 1, G, pub_state);  // wst and rst are contiguous
+    float *wst = reinterpret_cast<float *>(area);  // [W][G][PART_W] + residual state after it
+    warp_state_out(acc, wst, G);
+    for (int e = tid; e < G * PART_W; e += NT) wst[(size_t)W * G * PART_W + e] = rst[e];
+    __syncthreads();
+    merge_states(wst, W + 1, G, pub_state);
     cluster.sync();  // S3: every CTA's partial is published
 
     // ------------------------------------- P5: this CTA's slice of the output
     {
         const int tot = G * MOG_D;
         const int e0 = (int)((int64_t)tot * k / CS), e1 = (int)((int64_t)tot * (k + 1) / CS);
-        for (int e = e0 + tid; e < e1; e += MD_THREADS) {
+        for (int e = e0 + tid; e < e1; e += NT) {
             const int g = e / MOG_D, j = e % MOG_D;
             float M = -INFINITY;
             for (int src = 0; src < CS; ++src)
@@ -710,8 +701,7 @@ static cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaS
 }
 
 // Cluster size (CTAs per unit) and pipeline depth for a decode launch: the largest cluster
-// (<= 16) such that every unit's cluster is resident at once, four tile stages when the
-// launch fits one CTA per SM.
+// (<= 16) such that every unit's cluster is resident at once.
 template <int GT>
 static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     const void *fn = (const void *)k_mog_decode<GT>;
@@ -719,14 +709,13 @@ static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     if (e != cudaSuccess) return e;
     const int sms = num_sms();
     for (int cs = 16; cs >= 1; cs >>= 1) {
-        if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;
-        const int stages = (int64_t)cs * dv.units <= sms ? 4 : 2;
-        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, stages);
+        if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;  // keep clusters resident
+        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT));
         if (m.total > 227 * 1024) continue;
         if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs, dv.units);
-        cfg.blockDim = dim3(MD_THREADS);
+        cfg.blockDim = dim3(md_warps(GT) * 32);
         cfg.dynamicSmemBytes = m.total;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
@@ -775,7 +764,7 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
     }
     if ((e = ensure_smem((const void *)k_mog_decode<GT>, (size_t)m.total)) != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[0], s)) != cudaSuccess) return e;
-    if ((e = launch_ex(k_mog_decode<GT>, dim3(cs, dv.units), dim3(MD_THREADS), m.total, s, cs, a, m)) !=
+    if ((e = launch_ex(k_mog_decode<GT>, dim3(cs, dv.units), dim3(md_warps(GT) * 32), m.total, s, cs, a, m)) !=
         cudaSuccess)
         return e;
     if (events)
@@ -810,7 +799,7 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
 }
 
 size_t slot_smem_bytes(int G, int c_max, int tc) {  // the smallest layout (16-CTA clusters)
-    return (size_t)md_layout(G, tc, c_max, MOG_MAX_L, 16, 2).total;
+    return (size_t)md_layout(G, tc, c_max, MOG_MAX_L, 16, md_warps(G <= 4 ? 4 : 16)).total;
 }
 
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
