@@ -127,12 +127,14 @@ struct OnlineAcc {
 };
 
 constexpr int RCH = 64;  // slice clusters staged per residual pass
+constexpr int PCH = 64;  // (slot, subcluster) pairs staged per residual pass
 
 __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
 // Shared-memory layout of the decode kernel (byte offsets).
 struct MdLay {
-    int CS, SL, KC, NSLOT, SPC, warps;  // KC: candidates per slice and head
+    int CS, SL, KC, NSLOT, SPC, warps, rwarps;  // KC: candidates per slice and head;
+                                                // rwarps: warps with row buffers
     int cand_s, cand_i, pub_cnt, pub_coff, pub_state;                // read by other CTAs
     int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl, ucoff, pre;  // local
     int sres, ssl, snn, sso, spref, smask, rst, area;
@@ -141,7 +143,8 @@ struct MdLay {
 
 // area: the per-warp row buffers in P4; before that the staged value means and the
 // residual warp states of P3; after P4 the warp states of the merge.
-__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps) {
+__host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_max, int CS, int warps,
+                                             int rwarps) {
     MdLay m;
     int o = 0;
     auto take = [&](int bytes, int align) {
@@ -153,6 +156,7 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     const int tcc = tc > 0 ? tc : 1;
     m.CS = CS;
     m.warps = warps;
+    m.rwarps = rwarps;
     m.SL = (c_max + CS - 1) / CS;
     m.KC = m.SL < tcc ? m.SL : tcc;
     m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
@@ -180,13 +184,21 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
     m.rst = take(4 * G * PART_W, 16);
-    const int rows = warps * 2 * WB_BYTES;
-    const int p3 = (m.SPC * l_max + RCH) * MOG_D * 4 + warps * G * PART_W * 4;
+    const int rows = rwarps * 2 * WB_BYTES;
+    const int p3 = (PCH + RCH) * MOG_D * 4 + warps * G * PART_W * 4;
     const int mrg = (warps + 1) * G * PART_W * 4;
     int a = rows > p3 ? rows : p3;
     a = a > mrg ? a : mrg;
     m.area = take(a, 128);
     m.total = (o + 15) & ~15;
+    return m;
+}
+
+// The largest number of row-pipeline warps (<= warps) whose layout fits a CTA.
+__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps) {
+    MdLay m = md_layout_rw(G, tc, c_max, l_max, CS, warps, warps);
+    for (int rw = warps - 1; rw >= 1 && m.total > 227 * 1024; --rw)
+        m = md_layout_rw(G, tc, c_max, l_max, CS, warps, rw);
     return m;
 }
 
@@ -375,8 +387,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     // ----------------------------------------- P3: this CTA's union slots, residual
     const int nmy = Uc > k ? (Uc - k + CS - 1) / CS : 0;  // slots k, k+CS, ...
     const int npair = nmy * L;                              // (slot, subcluster) pairs
-    float *vst = reinterpret_cast<float *>(area);           // [SPC*l_max][d] subcluster means
-    float *vcl = vst + (size_t)m.SPC * dv.l_max * MOG_D;    // [RCH][d] slice cluster means
+    float *vst = reinterpret_cast<float *>(area);           // [PCH][d] subcluster means
+    float *vcl = vst + (size_t)PCH * MOG_D;                 // [RCH][d] slice cluster means
     float *rws = vcl + (size_t)RCH * MOG_D;                 // [W][G][PART_W] residual states
     for (int e = tid; e < nmy * (L + 1); e += NT) {
         const int s = e / (L + 1), i = e % (L + 1);
@@ -384,12 +396,15 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         sso[s * (MOG_MAX_L + 1) + i] = dv.sub_off[(size_t)u * dv.sub_off_stride + (size_t)c * L + i];
         if (i < L) snn[s * MOG_MAX_L + i] = dv.sub_n[usg + (size_t)c * L + i];
     }
-    if (resid)
-        for (int e = tid; e < npair * 32; e += NT) {
-            const int pr = e / 32, s = pr / L, l = pr % L;
-            cp_async16(smem_u32(vst + ((size_t)s * dv.l_max + l) * MOG_D + 4 * (e % 32)),
+    auto stage_pairs = [&](int p0) {  // value means of pairs p0 .. p0 + PCH
+        const int cnt = min(PCH, npair - p0);
+        for (int e = tid; e < cnt * 32; e += NT) {
+            const int pr = p0 + e / 32, s = pr / L, l = pr % L;
+            cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
                        dv.sub_vbar + (usg + (size_t)ucl[k + s * CS] * L + l) * MOG_D + 4 * (e % 32), 16);
         }
+    };
+    if (resid && npair > 0) stage_pairs(0);
     auto stage_slice = [&](int k0) {
         const int cnt = min(RCH, ns - k0);
         for (int e = tid; e < cnt * 32; e += NT)
@@ -491,18 +506,29 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         if (resid) {
             cp_async_wait<0>();
             __syncthreads();
-            for (int e = warp; e < npair; e += W) {
-                const int s = e / L, l = e % L;
-                if (snn[s * MOG_MAX_L + l] <= 0) continue;
-                const int c = ucl[k + s * CS];
-                uint32_t hm = 0u;  // heads that chose c
-                for (int q = 0; q < G * tc; ++q)
-                    if (selc[q] == c) hm |= 1u << (q / tc);
-                const uint32_t need = hm & ~smask[s * MOG_MAX_L + l];
-                const float *vrow = vst + ((size_t)s * dv.l_max + l) * MOG_D + 4 * lane;
+            for (int p0 = 0; p0 < npair; p0 += PCH) {
+                if (p0 > 0) {  // further pairs (many slots per CTA)
+                    __syncthreads();
+                    stage_pairs(p0);
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    __syncthreads();
+                }
+                const int cnt = min(PCH, npair - p0);
+                for (int e = warp; e < cnt; e += W) {
+                    const int s = (p0 + e) / L, l = (p0 + e) % L;
+                    if (snn[s * MOG_MAX_L + l] <= 0) continue;
+                    const int c = ucl[k + s * CS];
+                    uint32_t hm = 0u;  // heads that chose c
+                    for (int q = 0; q < G * tc; ++q)
+                        if (selc[q] == c) hm |= 1u << (q / tc);
+                    const uint32_t need = hm & ~smask[s * MOG_MAX_L + l];
+                    const float *vrow = vst + (size_t)e * MOG_D + 4 * lane;
 #pragma unroll
-                for (int g = 0; g < GT; ++g)
-                    if (g < G && ((need >> g) & 1u)) st[g].absorb(sres[(s * G + g) * MOG_MAX_L + l] * LOG2E, vrow);
+                    for (int g = 0; g < GT; ++g)
+                        if (g < G && ((need >> g) & 1u))
+                            st[g].absorb(sres[(s * G + g) * MOG_MAX_L + l] * LOG2E, vrow);
+                }
             }
             for (int k0 = 0; k0 < ns; k0 += RCH) {
                 if (k0 > 0) {
@@ -576,7 +602,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     acc.init();
     const float scale2 = dv.tau * LOG2E;
     {
-        // per-warp pipeline over 16-row blocks: warp w takes blocks w, w+W, ...
+        // per-warp pipeline over 16-row blocks: row warp w takes blocks w, w+RW, ...
+        const int RW = m.rwarps;
         uint8_t *buf0 = area + (size_t)warp * 2 * WB_BYTES, *buf1 = buf0 + WB_BYTES;
         const int nblk = (int)ceil_div64(r1 - r0, WB_ROWS);
         auto resolve = [&](int bi, int &pos, uint32_t &mk) {  // lane's row of block bi
@@ -605,7 +632,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             }
         };
         auto nrows_of = [&](int bi) { return min(WB_ROWS, r1 - (r0 + bi * WB_ROWS)); };
-        int bi = warp;
+        int bi = warp < RW ? warp : nblk;  // warps without row buffers take no blocks
         int pos;
         uint32_t mk;
         resolve(bi, pos, mk);
@@ -613,13 +640,13 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         cp_async_commit();
         int npos;
         uint32_t nmk;
-        resolve(bi + W, npos, nmk);
+        resolve(bi + RW, npos, nmk);
         for (int t = 0; bi < nblk; ++t) {
-            const int nb = bi + W;
+            const int nb = bi + RW;
             uint8_t *cur = (t & 1) ? buf1 : buf0, *nxt = (t & 1) ? buf0 : buf1;
             if (nb < nblk) warp_issue_block(nxt, nrows_of(nb), npos, nmk, kb, vb, dv.sn);
             cp_async_commit();
-            resolve(nb + W, npos, nmk);  // positions one block ahead of the copies
+            resolve(nb + RW, npos, nmk);  // positions one block ahead of the copies
             cp_async_wait<1>();
             __syncwarp();
             const uint32_t sk = smem_u32(cur);
