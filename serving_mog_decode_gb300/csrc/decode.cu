@@ -133,8 +133,8 @@ __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
 // Shared-memory layout of the decode kernel (byte offsets).
 struct MdLay {
-    int CS, SL, KC, NSLOT, SPC, warps, rwarps;  // KC: candidates per slice and head;
-                                                // rwarps: warps with row buffers
+    int CS, SL, KC, NSLOT, SPC, warps, rwarps, nbuf;  // KC: candidates per slice and head;
+                                                      // rwarps x nbuf row buffers
     int cand_s, cand_i, pub_cnt, pub_coff, pub_state;                // read by other CTAs
     int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl, ucoff, pre;  // local
     int sres, ssl, snn, sso, spref, smask, rst, area;
@@ -144,7 +144,7 @@ struct MdLay {
 // area: the per-warp row buffers in P4; before that the staged value means and the
 // residual warp states of P3; after P4 the warp states of the merge.
 __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_max, int CS, int warps,
-                                             int rwarps) {
+                                             int rwarps, int nbuf) {
     MdLay m;
     int o = 0;
     auto take = [&](int bytes, int align) {
@@ -157,6 +157,7 @@ __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_ma
     m.CS = CS;
     m.warps = warps;
     m.rwarps = rwarps;
+    m.nbuf = nbuf;
     m.SL = (c_max + CS - 1) / CS;
     m.KC = m.SL < tcc ? m.SL : tcc;
     m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
@@ -184,7 +185,7 @@ __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_ma
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
     m.rst = take(4 * G * PART_W, 16);
-    const int rows = rwarps * 2 * WB_BYTES;
+    const int rows = rwarps * nbuf * WB_BYTES;
     const int p3 = (PCH + RCH) * MOG_D * 4 + warps * G * PART_W * 4;
     const int mrg = (warps + 1) * G * PART_W * 4;
     int a = rows > p3 ? rows : p3;
@@ -194,12 +195,23 @@ __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_ma
     return m;
 }
 
-// The largest number of row-pipeline warps (<= warps) whose layout fits a CTA.
+// Row pipeline shape: the most 16-row blocks in flight while a block is computed,
+// rwarps * (nbuf - 1), over nbuf in {2, 3} and rwarps <= warps, within a CTA's shared memory.
 __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps) {
-    MdLay m = md_layout_rw(G, tc, c_max, l_max, CS, warps, warps);
-    for (int rw = warps - 1; rw >= 1 && m.total > 227 * 1024; --rw)
-        m = md_layout_rw(G, tc, c_max, l_max, CS, warps, rw);
-    return m;
+    MdLay best = md_layout_rw(G, tc, c_max, l_max, CS, warps, 1, 2);
+    int score = -1;
+    for (int nbuf = 2; nbuf <= 3; ++nbuf)
+        for (int rw = warps; rw >= 1; --rw) {
+            MdLay m = md_layout_rw(G, tc, c_max, l_max, CS, warps, rw, nbuf);
+            if (m.total > 227 * 1024) continue;
+            const int sc = rw * (nbuf - 1) * 64 + rw;  // blocks in flight, then warps
+            if (sc > score) {
+                score = sc;
+                best = m;
+            }
+            break;
+        }
+    return best;
 }
 
 template <int GT>
@@ -602,9 +614,10 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     acc.init();
     const float scale2 = dv.tau * LOG2E;
     {
-        // per-warp pipeline over 16-row blocks: row warp w takes blocks w, w+RW, ...
-        const int RW = m.rwarps;
-        uint8_t *buf0 = area + (size_t)warp * 2 * WB_BYTES, *buf1 = buf0 + WB_BYTES;
+        // per-warp pipeline over 16-row blocks: row warp w takes blocks w, w+RW, ..., with
+        // NB buffers (NB-1 blocks in flight while one is computed)
+        const int RW = m.rwarps, NB = m.nbuf;
+        uint8_t *wbuf = area + (size_t)warp * NB * WB_BYTES;
         const int nblk = (int)ceil_div64(r1 - r0, WB_ROWS);
         auto resolve = [&](int bi, int &pos, uint32_t &mk) {  // lane's row of block bi
             pos = 0;
@@ -632,28 +645,32 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             }
         };
         auto nrows_of = [&](int bi) { return min(WB_ROWS, r1 - (r0 + bi * WB_ROWS)); };
-        int bi = warp < RW ? warp : nblk;  // warps without row buffers take no blocks
+        const int b0 = warp < RW ? warp : nblk;  // warps without row buffers take no blocks
         int pos;
         uint32_t mk;
-        resolve(bi, pos, mk);
-        if (bi < nblk) warp_issue_block(buf0, nrows_of(bi), pos, mk, kb, vb, dv.sn);
-        cp_async_commit();
+        for (int j = 0; j < NB - 1; ++j) {  // prologue: the first NB-1 blocks
+            const int bi = b0 + j * RW;
+            resolve(bi, pos, mk);
+            if (bi < nblk) warp_issue_block(wbuf + (size_t)j * WB_BYTES, nrows_of(bi), pos, mk, kb, vb, dv.sn);
+            cp_async_commit();
+        }
         int npos;
         uint32_t nmk;
-        resolve(bi + RW, npos, nmk);
-        for (int t = 0; bi < nblk; ++t) {
-            const int nb = bi + RW;
-            uint8_t *cur = (t & 1) ? buf1 : buf0, *nxt = (t & 1) ? buf0 : buf1;
-            if (nb < nblk) warp_issue_block(nxt, nrows_of(nb), npos, nmk, kb, vb, dv.sn);
+        resolve(b0 + (NB - 1) * RW, npos, nmk);
+        for (int t = 0; b0 + t * RW < nblk; ++t) {
+            const int bn = b0 + (t + NB - 1) * RW;  // block entering the pipeline
+            if (bn < nblk)
+                warp_issue_block(wbuf + (size_t)((t + NB - 1) % NB) * WB_BYTES, nrows_of(bn), npos, nmk, kb,
+                                 vb, dv.sn);
             cp_async_commit();
-            resolve(nb + RW, npos, nmk);  // positions one block ahead of the copies
-            cp_async_wait<1>();
+            resolve(bn + RW, npos, nmk);  // positions one block ahead of the copies
+            cp_async_wait_dyn(NB - 1);
             __syncwarp();
+            const uint8_t *cur = wbuf + (size_t)(t % NB) * WB_BYTES;
             const uint32_t sk = smem_u32(cur);
             compute_rows16(acc, qa, sk, sk + WB_KV, reinterpret_cast<const uint32_t *>(cur + 2 * WB_KV), 0,
                            scale2);
             __syncwarp();
-            bi = nb;
         }
         cp_async_wait<0>();
     }
