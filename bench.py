@@ -127,9 +127,23 @@ def oracle_decode_sample(w, budget_s, steps=None, warmup=0):
     Returns (us per step per layer, cores, description, per-step list)."""
     import oracle
     n = int(wl.lengths(w)[0])
-    K, V, q = wl.make_unit(w, 0, 0, n)
+    u = wl.UnitDraw(w, 0, 0, n)
+    K, V = u.keys_values()
+    q = u.q
     Cn, L = wl.clusters_for(w, n)
-    summ = oracle.build_unit(K, V, n, w.n_sink, w.n_recent, Cn, L)
+    if n <= 65536:
+        summ = oracle.build_unit(K, V, n, w.n_sink, w.n_recent, Cn, L)
+        part = "the oracle's own two-level k-means"
+    else:  # the fp64 k-means of a long context takes hours: a position-rule partition
+        S, R = w.n_sink, w.n_recent
+        pos = np.arange(S, n - R)
+        lab = (u.z[pos] % Cn) * L + (pos % L)
+        order = np.argsort(lab, kind="stable")
+        perm = pos[order].astype(np.int32)
+        sub_off = np.searchsorted(lab[order], np.arange(Cn * L + 1)).astype(np.int32)
+        summ = oracle.stats(K, V, perm, sub_off, Cn, L)
+        summ.update(perm=perm, sub_off=sub_off, C=Cn, L=L, n_build=n, S=S, R=R)
+        part = "a planted-centre/position partition (fp64 k-means of this length is out of budget)"
     units = w.batch * w.h_kv
 
     def one():
@@ -148,7 +162,7 @@ def oracle_decode_sample(w, budget_s, steps=None, warmup=0):
         if steps is None and len(times) >= 1000:
             break
     desc = (f"KV head (b=0,h=0) of {units} with its {w.group} query heads, oracle decode step "
-            f"timed {len(times)}x, scaled x{units} to the layer; build untimed")
+            f"timed {len(times)}x, scaled x{units} to the layer; summaries from {part}, untimed")
     return statistics.mean(times), 1, desc, times
 
 
