@@ -745,14 +745,15 @@ static cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaS
 }
 
 // Cluster size (CTAs per unit) and pipeline depth for a decode launch: the largest cluster
-// (<= 16) such that every unit's cluster is resident at once.
+// (<= 16) such that every unit's cluster is resident at once (the occupancy query decides;
+// on a 152-SM GB300 eight 12-CTA clusters of ~200 KB fit, eight 16-CTA clusters do not).
 template <int GT>
 static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     const void *fn = (const void *)k_mog_decode<GT>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     const int sms = num_sms();
-    for (int cs = 16; cs >= 1; cs >>= 1) {
+    for (int cs = 16; cs >= 1; --cs) {  // any size: e.g. 12-CTA clusters fit where 16 do not
         if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;  // keep clusters resident
         MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT));
         if (m.total > 227 * 1024) continue;
