@@ -128,6 +128,7 @@ struct OnlineAcc {
 
 constexpr int RCH = 64;  // slice clusters staged per residual pass
 constexpr int PCH = 64;  // (slot, subcluster) pairs staged per residual pass
+constexpr int POSCH = 1024;  // row positions staged per pass of the row phase
 
 __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
@@ -137,7 +138,7 @@ struct MdLay {
                                                       // rwarps x nbuf row buffers
     int cand_s, cand_i, pub_cnt, pub_coff, pub_state;                // read by other CTAs
     int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl, ucoff, pre;  // local
-    int sres, ssl, snn, sso, spref, smask, rst, area;
+    int sres, ssl, snn, sso, spref, smask, rst, posb, area;
     int total;
 };
 
@@ -185,6 +186,7 @@ __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_ma
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
     m.rst = take(4 * G * PART_W, 16);
+    m.posb = take(2 * 2 * POSCH * 4, 16);  // [2 buffers][pos | mask][POSCH]
     const int rows = rwarps * nbuf * WB_BYTES;
     const int p3 = (PCH + RCH) * MOG_D * 4 + warps * G * PART_W * 4;
     const int mrg = (warps + 1) * G * PART_W * 4;
@@ -614,65 +616,89 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     acc.init();
     const float scale2 = dv.tau * LOG2E;
     {
-        // per-warp pipeline over 16-row blocks: row warp w takes blocks w, w+RW, ..., with
-        // NB buffers (NB-1 blocks in flight while one is computed)
+        // Rows are taken POSCH at a time; the positions and head masks of the next POSCH rows
+        // are copied into shared memory (cp.async) while the current ones are attended, so
+        // no copy of a K/V row waits on a global load of its position.  Inside a pass each
+        // row warp runs its own pipeline over 16-row blocks w, w+RW, ... with NB buffers.
         const int RW = m.rwarps, NB = m.nbuf;
         uint8_t *wbuf = area + (size_t)warp * NB * WB_BYTES;
-        const int nblk = (int)ceil_div64(r1 - r0, WB_ROWS);
-        auto resolve = [&](int bi, int &pos, uint32_t &mk) {  // lane's row of block bi
-            pos = 0;
-            mk = 0u;
-            const int i = r0 + bi * WB_ROWS + lane;
-            if (bi >= nblk || lane >= WB_ROWS || i >= r1) return;
-            if (i < n_anchor) {
-                pos = i < s_cnt ? i : rlo + (i - s_cnt);
-                mk = allm;
-            } else {
-                int lo = 0, hi = Uc - 1;  // last slot with pre[slot] <= i
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (pre[mid] <= i) lo = mid;
-                    else hi = mid - 1;
+        int *posb = reinterpret_cast<int *>(sm + m.posb);  // [2][2][POSCH]
+        auto stage_pos = [&](int c0p, int buf) {  // rows c0p .. c0p + POSCH of [r0, r1)
+            int *pp = posb + buf * 2 * POSCH;
+            uint32_t *mm = reinterpret_cast<uint32_t *>(pp + POSCH);
+            const int n = min(POSCH, r1 - c0p);
+            for (int t = tid; t < n; t += NT) {
+                const int i = c0p + t;
+                if (i < n_anchor) {
+                    pp[t] = i < s_cnt ? i : rlo + (i - s_cnt);
+                    mm[t] = allm;
+                } else {
+                    int lo = 0, hi = Uc - 1;  // last slot with pre[slot] <= i
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (pre[mid] <= i) lo = mid;
+                        else hi = mid - 1;
+                    }
+                    const int kk = ucoff[lo] + (i - pre[lo]);
+                    cp_async4(smem_u32(pp + t), rowpos + kk);
+                    cp_async4(smem_u32(mm + t), rowmask + kk);
                 }
-                const int kk = ucoff[lo] + (i - pre[lo]);
-                pos = __ldcg(rowpos + kk);
-                mk = __ldcg(rowmask + kk);
             }
-            if ((unsigned)pos >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
-                flag_error(dv.status, ST_BAD_INDEX);
+            cp_async_commit();
+        };
+        if (r0 < r1) stage_pos(r0, 0);
+        int pb = 0;
+        for (int c0p = r0; c0p < r1; c0p += POSCH, pb ^= 1) {
+            const int nrow = min(POSCH, r1 - c0p);
+            cp_async_wait<0>();  // this pass's positions
+            __syncthreads();
+            if (c0p + POSCH < r1) stage_pos(c0p + POSCH, pb ^ 1);  // next pass's, in flight
+            const int *pp = posb + pb * 2 * POSCH;
+            const uint32_t *mm = reinterpret_cast<const uint32_t *>(pp + POSCH);
+            const int nblk = (int)ceil_div64(nrow, WB_ROWS);
+            auto rowinfo = [&](int bi, int &pos, uint32_t &mk) {  // lane's row of block bi
                 pos = 0;
                 mk = 0u;
+                const int t = bi * WB_ROWS + lane;
+                if (bi >= nblk || lane >= WB_ROWS || t >= nrow) return;
+                pos = pp[t];
+                mk = mm[t];
+                if ((unsigned)pos >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
+                    flag_error(dv.status, ST_BAD_INDEX);
+                    pos = 0;
+                    mk = 0u;
+                }
+            };
+            auto nrows_of = [&](int bi) { return min(WB_ROWS, nrow - bi * WB_ROWS); };
+            const int b0 = warp < RW ? warp : nblk;  // warps without row buffers take no blocks
+            int pos;
+            uint32_t mk;
+            for (int j = 0; j < NB - 1; ++j) {  // prologue: the first NB-1 blocks
+                const int bi = b0 + j * RW;
+                rowinfo(bi, pos, mk);
+                if (bi < nblk) warp_issue_block(wbuf + (size_t)j * WB_BYTES, nrows_of(bi), pos, mk, kb, vb, dv.sn);
+                cp_async_commit();
             }
-        };
-        auto nrows_of = [&](int bi) { return min(WB_ROWS, r1 - (r0 + bi * WB_ROWS)); };
-        const int b0 = warp < RW ? warp : nblk;  // warps without row buffers take no blocks
-        int pos;
-        uint32_t mk;
-        for (int j = 0; j < NB - 1; ++j) {  // prologue: the first NB-1 blocks
-            const int bi = b0 + j * RW;
-            resolve(bi, pos, mk);
-            if (bi < nblk) warp_issue_block(wbuf + (size_t)j * WB_BYTES, nrows_of(bi), pos, mk, kb, vb, dv.sn);
-            cp_async_commit();
+            for (int t = 0; b0 + t * RW < nblk; ++t) {
+                const int bn = b0 + (t + NB - 1) * RW;  // block entering the pipeline
+                rowinfo(bn, pos, mk);
+                if (bn < nblk)
+                    warp_issue_block(wbuf + (size_t)((t + NB - 1) % NB) * WB_BYTES, nrows_of(bn), pos, mk,
+                                     kb, vb, dv.sn);
+                cp_async_commit();
+                // the next pass's position copies (if any) were committed before this loop:
+                // they are older than every block group, so waiting for block t covers them
+                cp_async_wait_dyn(NB - 1);
+                __syncwarp();
+                const uint8_t *cur = wbuf + (size_t)(t % NB) * WB_BYTES;
+                const uint32_t sk = smem_u32(cur);
+                compute_rows16(acc, qa, sk, sk + WB_KV, reinterpret_cast<const uint32_t *>(cur + 2 * WB_KV), 0,
+                               scale2);
+                __syncwarp();
+            }
+            cp_async_wait<0>();
+            __syncthreads();  // the pass's buffers and positions are free
         }
-        int npos;
-        uint32_t nmk;
-        resolve(b0 + (NB - 1) * RW, npos, nmk);
-        for (int t = 0; b0 + t * RW < nblk; ++t) {
-            const int bn = b0 + (t + NB - 1) * RW;  // block entering the pipeline
-            if (bn < nblk)
-                warp_issue_block(wbuf + (size_t)((t + NB - 1) % NB) * WB_BYTES, nrows_of(bn), npos, nmk, kb,
-                                 vb, dv.sn);
-            cp_async_commit();
-            resolve(bn + RW, npos, nmk);  // positions one block ahead of the copies
-            cp_async_wait_dyn(NB - 1);
-            __syncwarp();
-            const uint8_t *cur = wbuf + (size_t)(t % NB) * WB_BYTES;
-            const uint32_t sk = smem_u32(cur);
-            compute_rows16(acc, qa, sk, sk + WB_KV, reinterpret_cast<const uint32_t *>(cur + 2 * WB_KV), 0,
-                           scale2);
-            __syncwarp();
-        }
-        cp_async_wait<0>();
     }
     __syncthreads();
     float *wst = reinterpret_cast<float *>(area);  // [W][G][PART_W] + residual state after it
