@@ -122,7 +122,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION || P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
     const int tcc = std::max(P.tc, 1);
     P.P1 = (int)ceil_div64(P.c_max, 32);  // 32-cluster scoring slices
-    if (slot_smem_bytes(P.G, P.c_max, P.tc) > 227 * 1024) return MOG_ERR_SHAPE;  // decode shared memory
+    if (slot_smem_bytes(P.G, P.c_max, P.tc) > 226 * 1024) return MOG_ERR_SHAPE;  // decode shared memory
     const int sms = num_sms();
     P.P = std::max(1, std::min(MAX_SPLITS, (int)ceil_div64(2 * sms, P.units)));
     P.nchunks = std::max(1, (int)ceil_div64(P.n_mid_max, SORT_CHUNK));

@@ -129,6 +129,8 @@ struct OnlineAcc {
 constexpr int RCH = 64;  // slice clusters staged per residual pass
 constexpr int PCH = 64;  // (slot, subcluster) pairs staged per residual pass
 constexpr int POSCH = 1024;  // row positions staged per pass of the row phase
+// dynamic shared memory of the decode kernel: the 227 KB block limit less its static arrays
+constexpr int MD_SMEM_MAX = 226 * 1024;
 
 __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
@@ -205,7 +207,7 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     for (int nbuf = 2; nbuf <= 3; ++nbuf)
         for (int rw = warps; rw >= 1; --rw) {
             MdLay m = md_layout_rw(G, tc, c_max, l_max, CS, warps, rw, nbuf);
-            if (m.total > 227 * 1024) continue;
+            if (m.total > MD_SMEM_MAX) continue;
             const int sc = rw * (nbuf - 1) * 64 + rw;  // blocks in flight, then warps
             if (sc > score) {
                 score = sc;
@@ -782,7 +784,7 @@ static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     for (int cs = 16; cs >= 1; --cs) {  // any size: e.g. 12-CTA clusters fit where 16 do not
         if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;  // keep clusters resident
         MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT));
-        if (m.total > 227 * 1024) continue;
+        if (m.total > MD_SMEM_MAX) continue;
         if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs, dv.units);
