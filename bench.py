@@ -179,7 +179,7 @@ def bytes_from_selection(h, w, sel, lens, n_now):
     off = h.array("sub_off", torch.int32, (U, lay.sub_off_stride)).cpu().numpy()
     tc, ts = w.top_c, w.top_s
     sel = sel.reshape(U, G, -1)
-    tot = dict(k1=0, k2=0, k3=0, rows=0)
+    tot = dict(select=0, attend=0, merge=0, rows=0)
     for u in range(U):
         Cn, L, nb, S, rlo, b = info[u, 0], info[u, 1], info[u, 2], info[u, 4], info[u, 5], info[u, 6]
         ucl, usub = set(), set()
@@ -195,11 +195,15 @@ def bytes_from_selection(h, w, sel, lens, n_now):
                         usub.add((int(c), int(l)))
         Uk = sum(int(off[u, c * L + l + 1] - off[u, c * L + l]) for c, l in usub)
         anchors = min(S, n_now[b]) + max(0, n_now[b] - rlo)
-        tot["k1"] += Cn * (8 * D + 4) + G * D * 2
-        tot["k2"] += len(ucl) * L * (8 * D + 4) + Uk * 12
-        tot["k3"] += Uk * (4 * D + 8) + anchors * 4 * D + (Cn + len(ucl) * L) * 4 * D + G * D * 4
+        # selection kernel: query, cluster summaries (mean, variance, count), the union's
+        # subcluster summaries, the value means of the residual, perm in / row list out
+        tot["select"] += G * D * 2 + Cn * (8 * D + 4) + len(ucl) * L * (8 * D + 4)
+        tot["select"] += (Cn + len(ucl) * L) * 4 * D + Uk * (4 + 8)
+        # rows kernel: query, row list, the K and V rows (bf16); merge: the output (fp32)
+        tot["attend"] += G * D * 2 + Uk * 8 + (Uk + anchors) * 4 * D
+        tot["merge"] += G * D * 4
         tot["rows"] += Uk + anchors
-    tot["step"] = tot["k1"] + tot["k2"] + tot["k3"]
+    tot["step"] = tot["select"] + tot["attend"] + tot["merge"]
     return tot
 
 
@@ -302,7 +306,7 @@ def run_gpu(a, w, rank, world):
     if world > 1:
         torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    # ---- per-kernel times (events between the three kernels) ----
+    # ---- per-kernel times (events around the selection, rows and merge kernels) ----
     phase = [[], [], []]
     for i in range(max(20, min(a.steps, 200))):
         cold_l2()
@@ -336,9 +340,9 @@ def run_gpu(a, w, rank, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         mean_ms = float(t.item())
     pm = [statistics.mean(p) for p in phase]
-    names = ["k_mog_decode"]
-    dom = 0
-    kbytes = [by["step"]]
+    names = ["k_mog_decode", "k_mog_rows", "k_mog_merge"]
+    kbytes = [by["select"], by["attend"], by["merge"]]
+    dom = max(range(3), key=lambda i: pm[i])
     peak, peak_kind = peaks()
     achieved = kbytes[dom] / (pm[dom] * 1e-3) / 1e9
     res = {
@@ -365,7 +369,8 @@ def run_gpu(a, w, rank, world):
                      "traffic": stored_traffic(w.name, names[dom]),
                      "algorithmic_bytes_per_launch": int(kbytes[dom]),
                      "launch_us": round(pm[dom] * 1e3, 3)},
-        "kernels_us": {names[0]: round(pm[0] * 1e3, 3)},
+        "kernels_us": {names[i]: round(pm[i] * 1e3, 3) for i in range(3)},
+        "kernels_GBps": {names[i]: round(kbytes[i] / (pm[i] * 1e-3) / 1e9, 1) for i in range(3)},
         "step_bytes": int(by["step"]),
         "step_GBps": round(by["step"] / (mean_ms * 1e-3) / 1e9, 1),
         "step_frac_of_peak": round(by["step"] / (mean_ms * 1e-3) / 1e9 / peak, 4),
@@ -379,7 +384,7 @@ def run_gpu(a, w, rank, world):
                   "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3)},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",
                 "h2d_bytes_per_step": int(q_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 4)},
-        "gpu_launches": a.steps,
+        "gpu_launches": 3 * a.steps,  # selection, rows and merge kernels per step
         "clocks": clk,
     }
     if rank == 0:

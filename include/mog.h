@@ -172,9 +172,10 @@ int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev, const int32_
 int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void *stream);
 
 /*
- * mog_decode_ex that also records four caller-created cudaEvent_t (passed as void*):
- * events[0] before the cluster-scoring kernel, events[1] after it, events[2] after the
- * subcluster kernel, events[3] after the exact-attention kernel, all on `stream`, so
+ * mog_decode_ex that also records four caller-created cudaEvent_t (passed as void*), all
+ * on `stream`: events[0] before the selection kernel (cluster and subcluster scores, top-k,
+ * the Gaussian residual, the row list), events[1] after it, events[2] after the
+ * exact-attention rows kernel, events[3] after the merge kernel (which normalises), so
  * that each phase of one decode step can be timed.  Same arguments otherwise.
  */
 int mog_decode_phased(mog_handle *h, const void *q_dev, float *out_dev,

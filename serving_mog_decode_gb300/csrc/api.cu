@@ -124,7 +124,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.P1 = (int)ceil_div64(P.c_max, 32);  // 32-cluster scoring slices
     if (slot_smem_bytes(P.G, P.c_max, P.tc) > 226 * 1024) return MOG_ERR_SHAPE;  // decode shared memory
     const int sms = num_sms();
-    P.P = std::max(1, std::min(MAX_SPLITS, (int)ceil_div64(2 * sms, P.units)));
+    P.P = std::max(1, std::min(MAX_SPLITS, (int)ceil_div64(2 * sms, P.units)));  // rows kernel
     P.nchunks = std::max(1, (int)ceil_div64(P.n_mid_max, SORT_CHUNK));
     P.sub_off_stride = (P.c_max * P.l_max + 1 + 3) & ~3;
     const int64_t U = P.units, G = P.G, cm = P.c_max, lm = P.l_max, nc = P.n_cap;
@@ -168,7 +168,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_ucl = take(4 * U * MOG_MAX_UNION);
     P.o_ucount = take(4 * U);
     P.o_sel = take(4 * U * G * std::max<int64_t>(SW, 1));
-    P.o_slotcnt = take(4 * U * MOG_MAX_UNION);
+    P.o_slotcnt = take(4 * U * PLAN_W);  // row plan per unit
     P.o_slotcoff = take(4 * U * MOG_MAX_UNION);
     P.o_rowpos = take(4 * U * nc);
     P.o_counters = take(4 * U * 4);

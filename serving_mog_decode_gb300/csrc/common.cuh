@@ -84,12 +84,16 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// wait until at most n (runtime, 0..3) cp.async groups are pending
+// wait until at most n (runtime, 0..5) cp.async groups are pending
 __device__ __forceinline__ void cp_async_wait_dyn(int n) {
-    if (n <= 0) cp_async_wait<0>();
-    else if (n == 1) cp_async_wait<1>();
-    else if (n == 2) cp_async_wait<2>();
-    else cp_async_wait<3>();
+    switch (n <= 0 ? 0 : n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        default: cp_async_wait<5>(); break;
+    }
 }
 
 // read-only 16-byte global load, not kept in L1

@@ -128,7 +128,6 @@ struct OnlineAcc {
 
 constexpr int RCH = 64;  // slice clusters staged per residual pass
 constexpr int PCH = 64;  // (slot, subcluster) pairs staged per residual pass
-constexpr int POSCH = 1024;  // row positions staged per pass of the row phase
 // dynamic shared memory of the decode kernel: the 227 KB block limit less its static arrays
 constexpr int MD_SMEM_MAX = 226 * 1024;
 
@@ -136,18 +135,15 @@ __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
 // Shared-memory layout of the decode kernel (byte offsets).
 struct MdLay {
-    int CS, SL, KC, NSLOT, SPC, warps, rwarps, nbuf;  // KC: candidates per slice and head;
-                                                      // rwarps x nbuf row buffers
-    int cand_s, cand_i, pub_cnt, pub_coff, pub_state;                // read by other CTAs
-    int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl, ucoff, pre;  // local
-    int sres, ssl, snn, sso, spref, smask, rst, posb, area;
+    int CS, SL, KC, NSLOT, SPC, warps;  // KC: candidates per slice and head
+    int cand_s, cand_i, pub_cnt, pub_coff;                 // read by other CTAs
+    int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl;  // local
+    int sres, ssl, snn, sso, spref, smask, shm, slm, slp, rst, area;
     int total;
 };
 
-// area: the per-warp row buffers in P4; before that the staged value means and the
-// residual warp states of P3; after P4 the warp states of the merge.
-__host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_max, int CS, int warps,
-                                             int rwarps, int nbuf) {
+// area: the staged value means and the residual warp states of P3.
+__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int CS, int warps) {
     MdLay m;
     int o = 0;
     auto take = [&](int bytes, int align) {
@@ -159,8 +155,6 @@ __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_ma
     const int tcc = tc > 0 ? tc : 1;
     m.CS = CS;
     m.warps = warps;
-    m.rwarps = rwarps;
-    m.nbuf = nbuf;
     m.SL = (c_max + CS - 1) / CS;
     m.KC = m.SL < tcc ? m.SL : tcc;
     m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
@@ -169,7 +163,6 @@ __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_ma
     m.cand_i = take(4 * G * m.KC, 16);
     m.pub_cnt = take(4 * m.SPC, 16);
     m.pub_coff = take(4 * m.SPC, 16);
-    m.pub_state = take(4 * G * PART_W, 16);
     m.w = take(16 * 64 * G, 16);
     m.csl = take(4 * G * m.SL, 16);
     m.crs = take(4 * G * m.SL, 16);
@@ -179,43 +172,30 @@ __host__ __device__ inline MdLay md_layout_rw(int G, int tc, int c_max, int l_ma
     m.selc = take(4 * G * tcc, 16);
     m.bm = take(4 * ((c_max + 31) / 32), 16);
     m.ucl = take(4 * m.NSLOT, 16);
-    m.ucoff = take(4 * m.NSLOT, 16);
-    m.pre = take(4 * (m.NSLOT + 1), 16);
     m.sres = take(4 * m.SPC * G * MOG_MAX_L, 16);
     m.ssl = take(4 * m.SPC * G * MOG_MAX_L, 16);
     m.snn = take(4 * m.SPC * MOG_MAX_L, 16);
     m.sso = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
+    m.shm = take(4 * m.SPC, 16);
+    m.slm = take(4 * m.SL, 16);
+    m.slp = take(4 * (m.SPC + 1), 16);
     m.rst = take(4 * G * PART_W, 16);
-    m.posb = take(2 * 2 * POSCH * 4, 16);  // [2 buffers][pos | mask][POSCH]
-    const int rows = rwarps * nbuf * WB_BYTES;
-    const int p3 = (PCH + RCH) * MOG_D * 4 + warps * G * PART_W * 4;
-    const int mrg = (warps + 1) * G * PART_W * 4;
-    int a = rows > p3 ? rows : p3;
-    a = a > mrg ? a : mrg;
-    m.area = take(a, 128);
+    m.area = take((PCH + RCH) * MOG_D * 4 + warps * G * PART_W * 4, 128);
     m.total = (o + 15) & ~15;
     return m;
 }
 
-// Row pipeline shape: the most 16-row blocks in flight while a block is computed,
-// rwarps * (nbuf - 1), over nbuf in {2, 3} and rwarps <= warps, within a CTA's shared memory.
-__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps) {
-    MdLay best = md_layout_rw(G, tc, c_max, l_max, CS, warps, 1, 2);
-    int score = -1;
-    for (int nbuf = 2; nbuf <= 3; ++nbuf)
-        for (int rw = warps; rw >= 1; --rw) {
-            MdLay m = md_layout_rw(G, tc, c_max, l_max, CS, warps, rw, nbuf);
-            if (m.total > MD_SMEM_MAX) continue;
-            const int sc = rw * (nbuf - 1) * 64 + rw;  // blocks in flight, then warps
-            if (sc > score) {
-                score = sc;
-                best = m;
-            }
-            break;
-        }
-    return best;
+// The last j in [0, n) with a[j] <= x, for a non-decreasing a with a[0] <= x.
+__device__ __forceinline__ int last_le(const int *a, int n, int x) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
 }
 
 template <int GT>
@@ -233,7 +213,6 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     int *cand_i = reinterpret_cast<int *>(sm + m.cand_i);
     int *pub_cnt = reinterpret_cast<int *>(sm + m.pub_cnt);
     int *pub_coff = reinterpret_cast<int *>(sm + m.pub_coff);
-    float *pub_state = reinterpret_cast<float *>(sm + m.pub_state);
     float4 *w = reinterpret_cast<float4 *>(sm + m.w);
     float *csl = reinterpret_cast<float *>(sm + m.csl);
     float *crs = reinterpret_cast<float *>(sm + m.crs);
@@ -243,14 +222,15 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     int *selc = reinterpret_cast<int *>(sm + m.selc);
     uint32_t *bm = reinterpret_cast<uint32_t *>(sm + m.bm);
     int *ucl = reinterpret_cast<int *>(sm + m.ucl);
-    int *ucoff = reinterpret_cast<int *>(sm + m.ucoff);
-    int *pre = reinterpret_cast<int *>(sm + m.pre);
     float *sres = reinterpret_cast<float *>(sm + m.sres);
     float *ssl = reinterpret_cast<float *>(sm + m.ssl);
     int *snn = reinterpret_cast<int *>(sm + m.snn);
     int *sso = reinterpret_cast<int *>(sm + m.sso);
     int *spref = reinterpret_cast<int *>(sm + m.spref);
     uint32_t *smask = reinterpret_cast<uint32_t *>(sm + m.smask);
+    uint32_t *shm = reinterpret_cast<uint32_t *>(sm + m.shm);  // heads that chose slot s
+    uint32_t *slm = reinterpret_cast<uint32_t *>(sm + m.slm);  // heads that chose slice cluster
+    int *slp = reinterpret_cast<int *>(sm + m.slp);            // row prefix over this CTA's slots
     float *rst = reinterpret_cast<float *>(sm + m.rst);
     uint8_t *area = sm + m.area;
     __shared__ int s_wsum[W], s_uc;
@@ -317,6 +297,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     }
     for (int e = tid; e < G * tcc; e += NT) selc[e] = -1;
     for (int e = tid; e < (dv.c_max + 31) / 32; e += NT) bm[e] = 0u;
+    for (int e = tid; e < m.SL; e += NT) slm[e] = 0u;
     cluster.sync();  // S1: candidates of every slice are published
 
     // ------------------------------------------------------- P2: selection and union
@@ -360,8 +341,12 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         }
     }
     __syncthreads();
-    for (int e = tid; e < G * tc; e += NT)
-        if (selc[e] >= 0) atomicOr(&bm[selc[e] >> 5], 1u << (selc[e] & 31));
+    for (int e = tid; e < G * tc; e += NT) {
+        const int c = selc[e];
+        if (c < 0) continue;
+        atomicOr(&bm[c >> 5], 1u << (c & 31));
+        if (c >= c0 && c < c0 + ns) atomicOr(&slm[c - c0], 1u << (e / tc));
+    }
     __syncthreads();
     {  // union = set bits of bm, ascending: ucl[0 .. Uc)
         const int nw = (dv.c_max + 31) / 32;
@@ -447,6 +432,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         }
     }
     for (int e = tid; e < nmy * MOG_MAX_L; e += NT) smask[e] = 0u;
+    for (int e = tid; e < nmy; e += NT) shm[e] = 0u;
     __syncthreads();
     // top-ts subclusters of every head that chose a slot's cluster
     for (int e = warp; e < nmy * G; e += W) {
@@ -456,6 +442,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         for (int r = 0; r < tc; ++r)
             if (selc[g * tc + r] == c) { rk = r; break; }
         if (rk < 0) continue;
+        if (lane == 0) atomicOr(&shm[s], 1u << g);
         int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
         const int *nn = snn + s * MOG_MAX_L;
         if (a.sel_in) {
@@ -497,20 +484,56 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         if (lane == L - 1) pub_cnt[s] = incl;
     }
     __syncthreads();
-    {  // member rows of the chosen subclusters -> the unit's row list (perm order)
+    if (warp == 0) {  // row prefix over this CTA's slots
+        int run = 0;
+        for (int s0 = 0; s0 < nmy; s0 += 32) {
+            const int s = s0 + lane;
+            const int cnt = s < nmy ? spref[s * (MOG_MAX_L + 1) + L] : 0;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (s < nmy) slp[s] = run + incl - cnt;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) slp[nmy] = run;
+    }
+    __syncthreads();
+    {  // member rows of the chosen subclusters -> the unit's row list (perm order); four
+       // independent perm loads in flight per thread
         const int *perm = dv.perm + (size_t)u * dv.n_cap;
         int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
         uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
-        for (int s = 0; s < nmy; ++s) {
-            const int *sp = spref + s * (MOG_MAX_L + 1);
-            const int *so = sso + s * (MOG_MAX_L + 1);
-            const int tot = sp[L];
-            for (int i = tid; i < tot; i += NT) {
-                int kk = 0;
-                while (sp[kk + 1] <= i) ++kk;
-                rowpos[so[0] + i] = perm[so[kk] + (i - sp[kk])];
-                rowmask[so[0] + i] = smask[s * MOG_MAX_L + kk];
+        const int tot = slp[nmy];
+        for (int i0 = tid; i0 < tot; i0 += 4 * NT) {
+            int src[4], dst[4];
+            uint32_t mk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * NT;
+                src[j] = -1;
+                if (i < tot) {
+                    const int s = last_le(slp, nmy, i);
+                    const int ii = i - slp[s];
+                    const int *sp = spref + s * (MOG_MAX_L + 1);
+                    const int kk = last_le(sp, L, ii);
+                    const int *so = sso + s * (MOG_MAX_L + 1);
+                    src[j] = so[kk] + (ii - sp[kk]);
+                    dst[j] = so[0] + ii;
+                    mk[j] = smask[s * MOG_MAX_L + kk];
+                }
             }
+            int pv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pv[j] = src[j] >= 0 ? __ldg(perm + src[j]) : 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (src[j] >= 0) {
+                    rowpos[dst[j]] = pv[j];
+                    rowmask[dst[j]] = mk[j];
+                }
         }
     }
     // Gaussian residual: warps take items (pairs, then slice clusters) round-robin; lane
@@ -534,11 +557,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                 for (int e = warp; e < cnt; e += W) {
                     const int s = (p0 + e) / L, l = (p0 + e) % L;
                     if (snn[s * MOG_MAX_L + l] <= 0) continue;
-                    const int c = ucl[k + s * CS];
-                    uint32_t hm = 0u;  // heads that chose c
-                    for (int q = 0; q < G * tc; ++q)
-                        if (selc[q] == c) hm |= 1u << (q / tc);
-                    const uint32_t need = hm & ~smask[s * MOG_MAX_L + l];
+                    const uint32_t need = shm[s] & ~smask[s * MOG_MAX_L + l];
                     const float *vrow = vst + (size_t)e * MOG_D + 4 * lane;
 #pragma unroll
                     for (int g = 0; g < GT; ++g)
@@ -558,10 +577,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                 for (int e = warp; e < cnt; e += W) {
                     const int cl = k0 + e;
                     if (cnn[cl] <= 0) continue;
-                    uint32_t chose = 0u;
-                    for (int q = 0; q < G * tc; ++q)
-                        if (selc[q] == c0 + cl) chose |= 1u << (q / tc);
-                    const uint32_t need = allm & ~chose;
+                    const uint32_t need = allm & ~slm[cl];
                     const float *vrow = vcl + (size_t)e * MOG_D + 4 * lane;
 #pragma unroll
                     for (int g = 0; g < GT; ++g)
@@ -584,17 +600,38 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     }
     cp_async_wait<0>();
     cluster.sync();  // S2: row lists (global) and their counts (shared) are published
-
-    // -------------------------------------------- P4: exact rows, split evenly
-    if (warp == 0) {  // slot prefix from the owners' counts
+    // ------------------------- P4: the unit's row plan for the rows kernel (CTA 0)
+    for (int g = k; g < G; g += CS) {  // the unit's residual: CS states merged per head
+        if (tid >= MOG_D) break;
+        float mx = -INFINITY;
+        for (int i = 0; i < CS; ++i) mx = fmaxf(mx, cluster.map_shared_rank(rst, i)[g * PART_W]);
+        float l = 0.f, acc = 0.f;
+        if (mx != -INFINITY)
+            for (int i = 0; i < CS; ++i) {
+                const float *r = cluster.map_shared_rank(rst, i) + g * PART_W;
+                const float mi = r[0];
+                if (mi == -INFINITY) continue;
+                const float sc = exp2f(mi - mx);
+                l += sc * r[1];
+                acc += sc * r[PART_ACC + tid];
+            }
+        float *o = dv.partials + (((size_t)u * PART_SLOTS + MAX_SPLITS) * G + g) * PART_W;
+        if (tid == 0) {
+            o[0] = mx;
+            o[1] = l;
+        }
+        o[PART_ACC + tid] = acc;
+    }
+    if (k == 0 && warp == W - 1) {
+        int *plan = dv.slotcnt + (size_t)u * PLAN_W;  // [8 | pre[0..Uc] | coff[0..Uc)]
         int run = n_anchor;
         for (int j0 = 0; j0 < Uc; j0 += 32) {
             const int j = j0 + lane;
-            int cnt = 0;
+            int cnt = 0, coff = 0;
             if (j < Uc) {
                 const int own = j % CS, s = j / CS;
                 cnt = cluster.map_shared_rank(pub_cnt, own)[s];
-                ucoff[j] = cluster.map_shared_rank(pub_coff, own)[s];
+                coff = cluster.map_shared_rank(pub_coff, own)[s];
             }
             int incl = cnt;
 #pragma unroll
@@ -602,137 +639,186 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                 const int y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            if (j < Uc) pre[j] = run + incl - cnt;
+            if (j < Uc) {
+                plan[PLAN_PRE + j] = run + incl - cnt;
+                plan[PLAN_COFF + j] = coff;
+            }
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) pre[Uc] = run;
+        if (lane == 0) {
+            plan[0] = Uc;
+            plan[1] = run;  // T: anchors + selected rows
+            plan[2] = n_anchor;
+            plan[3] = s_cnt;
+            plan[4] = rlo;
+            plan[PLAN_PRE + Uc] = run;
+        }
     }
-    __syncthreads();
-    const int T = pre[Uc];
-    const int r0 = (int)((int64_t)T * k / CS), r1 = (int)((int64_t)T * (k + 1) / CS);
+    cluster.sync();  // S3: the owners' counts and residual states have been read
+}
+
+
+constexpr int RW_SUPER = 256;                  // row positions per batch in the rows kernel
+constexpr int RW_TPB = RW_SUPER / AT_ROWS;     // tiles per batch
+constexpr int RW_PER = RW_SUPER / AT_THREADS;  // positions a thread fetches per batch
+static_assert(RW_TPB >= AT_STAGES - 1, "the first batch must cover the pipeline's prologue");
+
+// Kernel B: grid (P, units), 4 warps, two CTAs per SM.  Rows [p*T/P, (p+1)*T/P) of the
+// unit's exact list (anchors, then the union slots' rows in slot order) through the
+// 64-row tile engine.  Positions are fetched into registers one batch ahead and moved to
+// shared memory when the pipeline reaches the batch, so no tile copy waits on a position
+// load.  One unnormalised partial per CTA.
+template <int GT>
+__global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
+    extern __shared__ __align__(128) uint8_t tile[];
+    const Dev &dv = a.dv;
+    const int G = dv.G;
+    __shared__ __align__(16) int s_plan[PLAN_W];
+    __shared__ int s_pos[2][RW_SUPER];
+    __shared__ uint32_t s_mk[2][RW_SUPER];
+    const int u = blockIdx.y, p = blockIdx.x, P = gridDim.x;
+    const int tid = threadIdx.x;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int b = ui[UI_B], h = u % dv.h_kv;
+    const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
+    uint32_t qa[8][4];
+    load_q_frags(qa, a.q + (size_t)u * G * MOG_D, G);
+    pdl_wait();  // the selection kernel's row lists and plan
+    pdl_trigger();
+    {
+        const int *plan = dv.slotcnt + (size_t)u * PLAN_W;
+        for (int q = tid; q < PLAN_W / 4; q += AT_THREADS) cp_async16(smem_u32(s_plan + 4 * q), plan + 4 * q, 16);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+    }
+    const int Uc = s_plan[0], T = s_plan[1], n_anchor = s_plan[2], s_cnt = s_plan[3], rlo = s_plan[4];
+    const int *s_pre = s_plan + PLAN_PRE, *s_coff = s_plan + PLAN_COFF;
+    const int r0 = (int)((int64_t)T * p / P), r1 = (int)((int64_t)T * (p + 1) / P);
+    const int nrow = r1 - r0, nt = (nrow + AT_ROWS - 1) / AT_ROWS;
     const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
     const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
     const int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
     const uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
+    int pf_pos[RW_PER];
+    uint32_t pf_mk[RW_PER];
+    auto fetch = [&](int bt) {  // positions of batch bt into registers
+#pragma unroll
+        for (int jj = 0; jj < RW_PER; ++jj) {
+            const int i = r0 + bt * RW_SUPER + tid + jj * AT_THREADS;
+            int pp = 0;
+            uint32_t mm = 0u;
+            if (i < r1) {
+                if (i < n_anchor) {
+                    pp = i < s_cnt ? i : rlo + (i - s_cnt);
+                    mm = allm;
+                } else {
+                    const int sl = last_le(s_pre, Uc, i);  // the slot holding row i
+                    const int kk = s_coff[sl] + (i - s_pre[sl]);
+                    pp = __ldcg(rowpos + kk);
+                    mm = __ldcg(rowmask + kk);
+                }
+            }
+            pf_pos[jj] = pp;
+            pf_mk[jj] = mm;
+        }
+    };
+    auto place = [&](int bt) {  // registers -> shared buffer of batch bt
+#pragma unroll
+        for (int jj = 0; jj < RW_PER; ++jj) {
+            s_pos[bt & 1][tid + jj * AT_THREADS] = pf_pos[jj];
+            s_mk[bt & 1][tid + jj * AT_THREADS] = pf_mk[jj];
+        }
+    };
+    auto issue = [&](int t) {
+        const int buf = (t / RW_TPB) & 1, rb = (t % RW_TPB) * AT_ROWS;
+        issue_tile(tile + (t % AT_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, nrow - t * AT_ROWS), kb, vb,
+                   dv.sn, [&](int r, int64_t &pos, uint32_t &mk) {
+                       int pp = s_pos[buf][rb + r];
+                       uint32_t mm = s_mk[buf][rb + r];
+                       if ((unsigned)pp >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
+                           flag_error(dv.status, ST_BAD_INDEX);
+                           pp = 0;
+                           mm = 0u;
+                       }
+                       pos = pp;
+                       mk = mm;
+                   });
+    };
     WarpAcc acc;
     acc.init();
     const float scale2 = dv.tau * LOG2E;
-    {
-        // Rows are taken POSCH at a time; the positions and head masks of the next POSCH rows
-        // are copied into shared memory (cp.async) while the current ones are attended, so
-        // no copy of a K/V row waits on a global load of its position.  Inside a pass each
-        // row warp runs its own pipeline over 16-row blocks w, w+RW, ... with NB buffers.
-        const int RW = m.rwarps, NB = m.nbuf;
-        uint8_t *wbuf = area + (size_t)warp * NB * WB_BYTES;
-        int *posb = reinterpret_cast<int *>(sm + m.posb);  // [2][2][POSCH]
-        auto stage_pos = [&](int c0p, int buf) {  // rows c0p .. c0p + POSCH of [r0, r1)
-            int *pp = posb + buf * 2 * POSCH;
-            uint32_t *mm = reinterpret_cast<uint32_t *>(pp + POSCH);
-            const int n = min(POSCH, r1 - c0p);
-            for (int t = tid; t < n; t += NT) {
-                const int i = c0p + t;
-                if (i < n_anchor) {
-                    pp[t] = i < s_cnt ? i : rlo + (i - s_cnt);
-                    mm[t] = allm;
-                } else {
-                    int lo = 0, hi = Uc - 1;  // last slot with pre[slot] <= i
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (pre[mid] <= i) lo = mid;
-                        else hi = mid - 1;
-                    }
-                    const int kk = ucoff[lo] + (i - pre[lo]);
-                    cp_async4(smem_u32(pp + t), rowpos + kk);
-                    cp_async4(smem_u32(mm + t), rowmask + kk);
-                }
-            }
-            cp_async_commit();
-        };
-        if (r0 < r1) stage_pos(r0, 0);
-        int pb = 0;
-        for (int c0p = r0; c0p < r1; c0p += POSCH, pb ^= 1) {
-            const int nrow = min(POSCH, r1 - c0p);
-            cp_async_wait<0>();  // this pass's positions
-            __syncthreads();
-            if (c0p + POSCH < r1) stage_pos(c0p + POSCH, pb ^ 1);  // next pass's, in flight
-            const int *pp = posb + pb * 2 * POSCH;
-            const uint32_t *mm = reinterpret_cast<const uint32_t *>(pp + POSCH);
-            const int nblk = (int)ceil_div64(nrow, WB_ROWS);
-            auto rowinfo = [&](int bi, int &pos, uint32_t &mk) {  // lane's row of block bi
-                pos = 0;
-                mk = 0u;
-                const int t = bi * WB_ROWS + lane;
-                if (bi >= nblk || lane >= WB_ROWS || t >= nrow) return;
-                pos = pp[t];
-                mk = mm[t];
-                if ((unsigned)pos >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
-                    flag_error(dv.status, ST_BAD_INDEX);
-                    pos = 0;
-                    mk = 0u;
-                }
-            };
-            auto nrows_of = [&](int bi) { return min(WB_ROWS, nrow - bi * WB_ROWS); };
-            const int b0 = warp < RW ? warp : nblk;  // warps without row buffers take no blocks
-            int pos;
-            uint32_t mk;
-            for (int j = 0; j < NB - 1; ++j) {  // prologue: the first NB-1 blocks
-                const int bi = b0 + j * RW;
-                rowinfo(bi, pos, mk);
-                if (bi < nblk) warp_issue_block(wbuf + (size_t)j * WB_BYTES, nrows_of(bi), pos, mk, kb, vb, dv.sn);
-                cp_async_commit();
-            }
-            for (int t = 0; b0 + t * RW < nblk; ++t) {
-                const int bn = b0 + (t + NB - 1) * RW;  // block entering the pipeline
-                rowinfo(bn, pos, mk);
-                if (bn < nblk)
-                    warp_issue_block(wbuf + (size_t)((t + NB - 1) % NB) * WB_BYTES, nrows_of(bn), pos, mk,
-                                     kb, vb, dv.sn);
-                cp_async_commit();
-                // the next pass's position copies (if any) were committed before this loop:
-                // they are older than every block group, so waiting for block t covers them
-                cp_async_wait_dyn(NB - 1);
-                __syncwarp();
-                const uint8_t *cur = wbuf + (size_t)(t % NB) * WB_BYTES;
-                const uint32_t sk = smem_u32(cur);
-                compute_rows16(acc, qa, sk, sk + WB_KV, reinterpret_cast<const uint32_t *>(cur + 2 * WB_KV), 0,
-                               scale2);
-                __syncwarp();
-            }
-            cp_async_wait<0>();
-            __syncthreads();  // the pass's buffers and positions are free
-        }
+    if (nt > 0) {
+        fetch(0);
+        place(0);
+        if (nrow > RW_SUPER) fetch(1);
     }
     __syncthreads();
-    float *wst = reinterpret_cast<float *>(area);  // [W][G][PART_W] + residual state after it
-    warp_state_out(acc, wst, G);
-    for (int e = tid; e < G * PART_W; e += NT) wst[(size_t)W * G * PART_W + e] = rst[e];
+#pragma unroll
+    for (int s2 = 0; s2 < AT_STAGES - 1; ++s2) {
+        if (s2 < nt) issue(s2);
+        cp_async_commit();
+    }
+    for (int t = 0; t < nt; ++t) {
+        cp_async_wait<AT_STAGES - 2>();
+        __syncthreads();
+        const int ti = t + AT_STAGES - 1;
+        if (ti < nt) {
+            if (ti % RW_TPB == 0) {  // first tile of a batch: its positions go to shared memory
+                const int bt = ti / RW_TPB;
+                place(bt);
+                __syncthreads();
+                if ((bt + 1) * RW_SUPER < nrow) fetch(bt + 1);
+            }
+            issue(ti);
+        }
+        cp_async_commit();
+        compute_tile(acc, qa, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
+    }
+    cp_async_wait<0>();
     __syncthreads();
-    merge_states(wst, W + 1, G, pub_state);
-    cluster.sync();  // S3: every CTA's partial is published
+    float *st = reinterpret_cast<float *>(tile);
+    warp_state_out(acc, st, G);
+    __syncthreads();
+    merge_states(st, AT_WARPS, G, dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W);
+}
 
-    // ------------------------------------- P5: this CTA's slice of the output
-    {
-        const int tot = G * MOG_D;
-        const int e0 = (int)((int64_t)tot * k / CS), e1 = (int)((int64_t)tot * (k + 1) / CS);
-        for (int e = e0 + tid; e < e1; e += NT) {
-            const int g = e / MOG_D, j = e % MOG_D;
-            float M = -INFINITY;
-            for (int src = 0; src < CS; ++src)
-                M = fmaxf(M, cluster.map_shared_rank(pub_state, src)[g * PART_W]);
-            float lsum = 0.f, asum = 0.f;
-            if (M != -INFINITY)
-                for (int src = 0; src < CS; ++src) {
-                    const float *ps = cluster.map_shared_rank(pub_state, src) + g * PART_W;
-                    const float mi = ps[0];
-                    if (mi == -INFINITY) continue;
-                    const float sc = exp2f(mi - M);
-                    lsum += sc * ps[1];
-                    asum += sc * ps[PART_ACC + j];
-                }
-            a.out[(size_t)u * G * MOG_D + e] = lsum > 0.f ? asum / lsum : 0.f;
-        }
+// Kernel C: grid (G, units), 512 threads.  Merges the P row partials and the residual
+// partial of one query head (running max, rescaled sums) and normalises once.  Thread
+// (part, j) sums partials part, part + 4, ... for dimension j; all loads are independent.
+constexpr int MG_THREADS = 4 * MOG_D;
+__global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int G,
+                                                          float *out) {
+    const int g = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
+    const int j = tid % MOG_D, part = tid / MOG_D;
+    __shared__ float s_m[MAX_SPLITS + 1], s_l[MAX_SPLITS + 1], s_w[MAX_SPLITS + 1];
+    __shared__ float s_acc[MG_THREADS / MOG_D][MOG_D];
+    pdl_wait();
+    pdl_trigger();
+    const int n = P + 1;  // row partials, then the residual
+    auto src = [&](int i) {
+        return partials + (((size_t)u * PART_SLOTS + (i < P ? i : MAX_SPLITS)) * G + g) * PART_W;
+    };
+    if (tid < n) {
+        s_m[tid] = __ldcg(src(tid));
+        s_l[tid] = __ldcg(src(tid) + 1);
     }
-    cluster.sync();  // S4: keep this CTA's shared memory alive for the other readers
+    __syncthreads();
+    float mx = -INFINITY;
+    for (int i = 0; i < n; ++i) mx = fmaxf(mx, s_m[i]);
+    if (tid < n) s_w[tid] = (s_m[tid] == -INFINITY) ? 0.f : exp2f(s_m[tid] - mx);
+    __syncthreads();
+    float l = 0.f;
+    for (int i = 0; i < n; ++i) l += s_w[i] * s_l[i];
+    float v = 0.f;
+#pragma unroll 4
+    for (int i = part; i < n; i += MG_THREADS / MOG_D) v += s_w[i] * __ldcg(src(i) + PART_ACC + j);
+    s_acc[part][j] = v;
+    __syncthreads();
+    if (part == 0) {
+        for (int q = 1; q < MG_THREADS / MOG_D; ++q) v += s_acc[q][j];
+        out[((size_t)u * G + g) * MOG_D + j] = l > 0.f ? v / l : 0.f;
+    }
 }
 
 // Append one token per sequence at position n_now[b], then advance n_now[b].
@@ -772,6 +858,22 @@ static cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaS
     return cudaLaunchKernelEx(&cfg, kernel, a, m);
 }
 
+template <typename K, typename... Args>
+static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Cluster size (CTAs per unit) and pipeline depth for a decode launch: the largest cluster
 // (<= 16) such that every unit's cluster is resident at once (the occupancy query decides;
 // on a 152-SM GB300 eight 12-CTA clusters of ~200 KB fit, eight 16-CTA clusters do not).
@@ -783,7 +885,7 @@ static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     const int sms = num_sms();
     for (int cs = 16; cs >= 1; --cs) {  // any size: e.g. 12-CTA clusters fit where 16 do not
         if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;  // keep clusters resident
-        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT));
+        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, cs, md_warps(GT));
         if (m.total > MD_SMEM_MAX) continue;
         if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -840,9 +942,16 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
     if ((e = launch_ex(k_mog_decode<GT>, dim3(cs, dv.units), dim3(md_warps(GT) * 32), m.total, s, cs, a, m)) !=
         cudaSuccess)
         return e;
-    if (events)
-        for (int i = 1; i < 4; ++i)
-            if ((e = cudaEventRecord(events[i], s)) != cudaSuccess) return e;
+    if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void *)k_mog_rows<GT>, AT_SMEM)) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_mog_rows<GT>, dim3(dv.P, dv.units), dim3(AT_THREADS), AT_SMEM, s, a)) !=
+        cudaSuccess)
+        return e;
+    if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_mog_merge, dim3(dv.G, dv.units), dim3(MG_THREADS), 0, s,
+                        (const float *)dv.partials, dv.P, dv.G, a.out)) != cudaSuccess)
+        return e;
+    if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
@@ -872,7 +981,7 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
 }
 
 size_t slot_smem_bytes(int G, int c_max, int tc) {  // the smallest layout (16-CTA clusters)
-    return (size_t)md_layout(G, tc, c_max, MOG_MAX_L, 16, md_warps(G <= 4 ? 4 : 16)).total;
+    return (size_t)md_layout(G, tc, c_max, 16, md_warps(G <= 4 ? 4 : 16)).total;
 }
 
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,

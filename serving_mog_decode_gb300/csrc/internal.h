@@ -13,7 +13,13 @@ enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
 
 constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
 constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
-constexpr int PART_SLOTS = 4 + 2 * 256;  // partials per unit: anchor CTAs + 2 per union slot
+constexpr int PART_SLOTS = MAX_SPLITS + 1;  // partials per unit: rows CTAs, then the residual
+// Row plan per unit, written by the selection kernel for the rows kernel:
+// [0] union size Uc, [1] rows T, [2] anchors, [3] sink rows, [4] first recent position,
+// [PLAN_PRE + j] first row of slot j (j <= Uc), [PLAN_COFF + j] slot j's row-list offset.
+constexpr int PLAN_PRE = 8;
+constexpr int PLAN_COFF = PLAN_PRE + MOG_MAX_UNION + 1;
+constexpr int PLAN_W = (PLAN_COFF + MOG_MAX_UNION + 3) / 4 * 4;  // ints, whole 16-byte chunks
 constexpr int MAX_C = 4096;        // clusters per unit supported
 
 // Typed view of an arena, passed by value to every kernel.
