@@ -120,11 +120,9 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     }
     if (P.l_max > MOG_MAX_L || P.c_max > MAX_C || P.ts > MOG_MAX_L) return MOG_ERR_SHAPE;
     if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION || P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
-    const int tcc = std::max(P.tc, 1);
-    P.P1 = (int)ceil_div64(P.c_max, 32);  // 32-cluster scoring slices
-    if (slot_smem_bytes(P.G, P.c_max, P.tc) > 226 * 1024) return MOG_ERR_SHAPE;  // decode shared memory
+    if (slot_smem_bytes(P.G, P.c_max, P.l_max, P.tc) > 226 * 1024) return MOG_ERR_SHAPE;  // decode shared memory
     const int sms = num_sms();
-    P.P = std::max(1, std::min(MAX_SPLITS, (int)ceil_div64(2 * sms, P.units)));  // rows kernel
+    P.P = std::max(1, std::min(MAX_SPLITS, 2 * sms / P.units));  // rows kernel: one wave of 2 CTAs/SM
     P.nchunks = std::max(1, (int)ceil_div64(P.n_mid_max, SORT_CHUNK));
     P.sub_off_stride = (P.c_max * P.l_max + 1 + 3) & ~3;
     const int64_t U = P.units, G = P.G, cm = P.c_max, lm = P.l_max, nc = P.n_cap;
@@ -158,22 +156,13 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_ctot = take(4 * U * cm);
     P.o_coff = take(4 * U * (cm + 1));
     P.o_sub_assign = take(4 * U * nc);
-    P.o_cscore = take(4 * U * 2 * G * cm);
-    P.o_subscore = take(4 * U * MOG_MAX_UNION * G * MOG_MAX_L);
+    P.nseg_max = (int)std::max<int64_t>(1, std::min<int64_t>(cm, G * P.tc) * lm);  // union x subclusters
     P.o_partials = take(4 * U * PART_SLOTS * G * (MOG_D + 4));
-    P.o_cselmask = take(4 * U * cm);
-    P.o_uhm = take(4 * U * MOG_MAX_UNION);
-    P.o_subres = take(4 * U * MOG_MAX_UNION * MOG_MAX_L);
-    P.o_rowmask = take(4 * U * nc);
-    P.o_ucl = take(4 * U * MOG_MAX_UNION);
-    P.o_ucount = take(4 * U);
     P.o_sel = take(4 * U * G * std::max<int64_t>(SW, 1));
-    P.o_slotcnt = take(4 * U * PLAN_W);  // row plan per unit
-    P.o_slotcoff = take(4 * U * MOG_MAX_UNION);
-    P.o_rowpos = take(4 * U * nc);
-    P.o_counters = take(4 * U * 4);
-    P.o_cand_s = take(4 * U * P.P1 * G * tcc);
-    P.o_cand_i = take(4 * U * P.P1 * G * tcc);
+    P.o_plan = take(4 * U * PLAN_W);
+    P.o_segrow = take(4 * U * P.nseg_max);
+    P.o_segoff = take(4 * U * P.nseg_max);
+    P.o_segmask = take(4 * U * P.nseg_max);
     P.total = o;
     return MOG_OK;
 }
@@ -203,7 +192,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.score_mode = P.score_mode;
     d.residual = P.residual;
     d.P = P.P;
-    d.P1 = P.P1;
+    d.nseg_max = P.nseg_max;
     d.nchunks = P.nchunks;
     d.sub_off_stride = P.sub_off_stride;
     d.tau = (float)(1.0 / sqrt((double)P.d));
@@ -231,22 +220,12 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     PTR(ctot, int);
     PTR(coff, int);
     PTR(sub_assign, int);
-    PTR(cscore, float);
-    PTR(subscore, float);
     PTR(partials, float);
-    PTR(cselmask, uint32_t);
-    PTR(uhm, uint32_t);
-    PTR(subres, uint32_t);
-    PTR(rowmask, uint32_t);
-    PTR(ucl, int);
-    PTR(ucount, int);
     PTR(sel, int);
-    PTR(slotcnt, int);
-    PTR(slotcoff, int);
-    PTR(rowpos, int);
-    PTR(counters, unsigned);
-    PTR(cand_s, float);
-    PTR(cand_i, int);
+    PTR(plan, int);
+    PTR(segrow, int);
+    PTR(segoff, int);
+    PTR(segmask, uint32_t);
 #undef PTR
     return d;
 }
@@ -353,11 +332,9 @@ static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
     CKH(cudaMemsetAsync(a + pl.o_status, 0, 64, s));
     CKH(cudaMemsetAsync(a + pl.o_changed, 0, 4 * (size_t)pl.units * pl.T1, s));
     CKH(cudaMemsetAsync(a + pl.o_fb_cnt, 0, 4 * (size_t)pl.units * pl.T1, s));
-    CKH(cudaMemsetAsync(a + pl.o_counters, 0, 16 * (size_t)pl.units, s));
     CKH(cudaMemsetAsync(a + pl.o_coff, 0, 4 * (size_t)pl.units * (pl.c_max + 1), s));
     CKH(cudaMemsetAsync(a + pl.o_l1_assign, 0xff, 4 * (size_t)pl.units * pl.n_cap, s));
     CKH(cudaMemsetAsync(a + pl.o_l1_steps, 0, 4 * (size_t)pl.units, s));
-    CKH(cudaMemsetAsync(a + pl.o_ucount, 0, 4 * (size_t)pl.units, s));
     // groups beyond a unit's C / L keep count 0 (the decode scores every c < c_max)
     CKH(cudaMemsetAsync(a + pl.o_cl_n, 0, 4 * (size_t)pl.units * pl.c_max, s));
     CKH(cudaMemsetAsync(a + pl.o_sub_n, 0, 4 * (size_t)pl.units * pl.c_max * pl.l_max, s));

@@ -38,8 +38,6 @@ struct DecArgs {
     float *out;             // [units*G][d]
     const int32_t *sel_in;  // [units*G][SW] or null
     int SW;
-    float *cand_s;  // [units][P1][G][tc]
-    int *cand_i;
 };
 
 // per-head score weights, float4-chunked: w[g][k] (k < 32) holds tau*q over dims 4k..4k+3,
@@ -133,17 +131,18 @@ constexpr int MD_SMEM_MAX = 226 * 1024;
 
 __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
-// Shared-memory layout of the decode kernel (byte offsets).
+// Shared-memory layout of the selection kernel (byte offsets).
 struct MdLay {
-    int CS, SL, KC, NSLOT, SPC, warps;  // KC: candidates per slice and head
-    int cand_s, cand_i, pub_cnt, pub_coff;                 // read by other CTAs
-    int w, csl, crs, cnn, allc_s, allc_i, selc, bm, ucl;  // local
-    int sres, ssl, snn, sso, spref, smask, shm, slm, slp, rst, area;
+    int CS, SL, SLp, KC, NPOOL, NSLOT, SPC, warps, PCHd, RCHd;  // KC: candidates per slice and
+                                                                  // head; NPOOL: CS*KC padded
+    int cand_k, pub_cnt, pub_nseg, rst;                           // read by other CTAs
+    int w, ckey, crs, cnn, slm, allc_k, selc, bm, ucl, gpre, gseg;  // local
+    int sres, skey, snn, sso, spref, smask, shm, area;
     int total;
 };
 
-// area: the staged value means and the residual warp states of P3.
-__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int CS, int warps) {
+// area: the staged value means of P3, then (aliased) the residual warp states.
+__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps) {
     MdLay m;
     int o = 0;
     auto take = [&](int bytes, int align) {
@@ -156,33 +155,46 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int CS, int
     m.CS = CS;
     m.warps = warps;
     m.SL = (c_max + CS - 1) / CS;
+    m.SLp = (m.SL + 7) & ~7;
     m.KC = m.SL < tcc ? m.SL : tcc;
+    m.NPOOL = (CS * m.KC + 7) & ~7;
     m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
     m.SPC = (m.NSLOT + CS - 1) / CS;
-    m.cand_s = take(4 * G * m.KC, 16);
-    m.cand_i = take(4 * G * m.KC, 16);
+    m.cand_k = take(8 * G * m.KC, 16);
     m.pub_cnt = take(4 * m.SPC, 16);
-    m.pub_coff = take(4 * m.SPC, 16);
+    m.pub_nseg = take(4 * m.SPC, 16);
+    m.rst = take(4 * G * PART_W, 16);
     m.w = take(16 * 64 * G, 16);
-    m.csl = take(4 * G * m.SL, 16);
+    m.ckey = take(8 * G * m.SLp, 16);
     m.crs = take(4 * G * m.SL, 16);
     m.cnn = take(4 * m.SL, 16);
-    m.allc_s = take(4 * CS * G * m.KC, 16);
-    m.allc_i = take(4 * CS * G * m.KC, 16);
+    m.slm = take(4 * m.SL, 16);
+    m.allc_k = take(8 * G * m.NPOOL, 16);
     m.selc = take(4 * G * tcc, 16);
     m.bm = take(4 * ((c_max + 31) / 32), 16);
     m.ucl = take(4 * m.NSLOT, 16);
+    m.gpre = take(4 * (m.NSLOT + 1), 16);
+    m.gseg = take(4 * (m.NSLOT + 1), 16);
     m.sres = take(4 * m.SPC * G * MOG_MAX_L, 16);
-    m.ssl = take(4 * m.SPC * G * MOG_MAX_L, 16);
+    m.skey = take(8 * m.SPC * G * MOG_MAX_L, 16);
     m.snn = take(4 * m.SPC * MOG_MAX_L, 16);
     m.sso = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
     m.shm = take(4 * m.SPC, 16);
-    m.slm = take(4 * m.SL, 16);
-    m.slp = take(4 * (m.SPC + 1), 16);
-    m.rst = take(4 * G * PART_W, 16);
-    m.area = take((PCH + RCH) * MOG_D * 4 + warps * G * PART_W * 4, 128);
+    // value means: all of this CTA's (slot, subcluster) pairs and slice clusters in one pass
+    // when they fit, else passes of at most 64 each
+    const int base = (o + 127) & ~127;
+    const int states = warps * G * PART_W * 4;
+    int pch = m.SPC * l_max, rch = m.SL;
+    if (base + ((pch + rch) * MOG_D * 4 > states ? (pch + rch) * MOG_D * 4 : states) > MD_SMEM_MAX) {
+        pch = pch < PCH ? pch : PCH;
+        rch = rch < RCH ? rch : RCH;
+    }
+    m.PCHd = pch > 0 ? pch : 1;
+    m.RCHd = rch > 0 ? rch : 1;
+    const int vm = (m.PCHd + m.RCHd) * MOG_D * 4;
+    m.area = take(vm > states ? vm : states, 128);
     m.total = (o + 15) & ~15;
     return m;
 }
@@ -198,6 +210,40 @@ __device__ __forceinline__ int last_le(const int *a, int n, int x) {
     return lo;
 }
 
+// Selection order as one integer: a larger key ranks first (score descending, then index
+// ascending); 0 for a candidate that is never chosen (score -inf or NaN, index < 0).
+__device__ __forceinline__ unsigned long long rank_key(float sc, int idx) {
+    if (!(sc > -INFINITY) || idx < 0) return 0ull;
+    uint32_t bits = __float_as_uint(sc == 0.f ? 0.f : sc);  // -0 ranks as +0
+    bits = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+    return ((unsigned long long)bits << 32) | (uint32_t)(0x7fffffff - idx);
+}
+__device__ __forceinline__ int key_index(unsigned long long key) {
+    return 0x7fffffff - (int)(uint32_t)key;
+}
+// Rank of key x among keys[0 .. n) (n a multiple of 8, zero padded): how many are larger,
+// counted up to `cap` (the result is >= cap once the key is out of the selection).
+__device__ __forceinline__ int key_rank(const unsigned long long *keys, int n, unsigned long long x,
+                                        int cap) {
+    int rank = 0;
+    for (int j0 = 0; j0 < n && rank < cap; j0 += 8) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) rank += keys[j0 + jj] > x;
+    }
+    return rank;
+}
+
+// Kernel A: one thread-block cluster of CS CTAs per unit.  Selection, the Gaussian
+// residual and the rows kernel's plan:
+//  P1  CTA k scores its slice of clusters for the G query heads and keeps the slice's
+//      top-KC per head;
+//  P2  every CTA gathers the slices' candidates over distributed shared memory, takes each
+//      head's top-tc clusters and their union over the heads (ascending index);
+//  P3  CTA k takes union slots k, k+CS, ...: subcluster scores, the top-ts subclusters of
+//      every head that chose the slot's cluster, and the residual of the unchosen
+//      subclusters of those heads and of its slice clusters no head chose;
+//  P4  the unit's row segments (one per chosen subcluster, in slot order), the first
+//      segment of every rows-kernel CTA, and the residual merged over the CTAs.
 template <int GT>
 __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, MdLay m) {
     namespace cg = cooperative_groups;
@@ -209,34 +255,33 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     const int CS = m.CS, k = (int)cluster.block_rank();
     const int u = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float *cand_s = reinterpret_cast<float *>(sm + m.cand_s);
-    int *cand_i = reinterpret_cast<int *>(sm + m.cand_i);
-    int *pub_cnt = reinterpret_cast<int *>(sm + m.pub_cnt);
-    int *pub_coff = reinterpret_cast<int *>(sm + m.pub_coff);
+    unsigned long long *cand_k = reinterpret_cast<unsigned long long *>(sm + m.cand_k);
+    int *pub_cnt = reinterpret_cast<int *>(sm + m.pub_cnt);    // rows of my slot s
+    int *pub_nseg = reinterpret_cast<int *>(sm + m.pub_nseg);  // chosen subclusters of slot s
+    float *rst = reinterpret_cast<float *>(sm + m.rst);        // this CTA's residual state
     float4 *w = reinterpret_cast<float4 *>(sm + m.w);
-    float *csl = reinterpret_cast<float *>(sm + m.csl);
+    unsigned long long *ckey = reinterpret_cast<unsigned long long *>(sm + m.ckey);  // slice keys
     float *crs = reinterpret_cast<float *>(sm + m.crs);
     int *cnn = reinterpret_cast<int *>(sm + m.cnn);
-    float *allc_s = reinterpret_cast<float *>(sm + m.allc_s);
-    int *allc_i = reinterpret_cast<int *>(sm + m.allc_i);
+    uint32_t *slm = reinterpret_cast<uint32_t *>(sm + m.slm);  // heads that chose slice cluster
+    unsigned long long *allc_k = reinterpret_cast<unsigned long long *>(sm + m.allc_k);  // [g][r][src]
     int *selc = reinterpret_cast<int *>(sm + m.selc);
     uint32_t *bm = reinterpret_cast<uint32_t *>(sm + m.bm);
     int *ucl = reinterpret_cast<int *>(sm + m.ucl);
+    int *gpre = reinterpret_cast<int *>(sm + m.gpre);  // first row of union slot j
+    int *gseg = reinterpret_cast<int *>(sm + m.gseg);  // first segment of union slot j
     float *sres = reinterpret_cast<float *>(sm + m.sres);
-    float *ssl = reinterpret_cast<float *>(sm + m.ssl);
+    unsigned long long *skey = reinterpret_cast<unsigned long long *>(sm + m.skey);
     int *snn = reinterpret_cast<int *>(sm + m.snn);
     int *sso = reinterpret_cast<int *>(sm + m.sso);
     int *spref = reinterpret_cast<int *>(sm + m.spref);
     uint32_t *smask = reinterpret_cast<uint32_t *>(sm + m.smask);
     uint32_t *shm = reinterpret_cast<uint32_t *>(sm + m.shm);  // heads that chose slot s
-    uint32_t *slm = reinterpret_cast<uint32_t *>(sm + m.slm);  // heads that chose slice cluster
-    int *slp = reinterpret_cast<int *>(sm + m.slp);            // row prefix over this CTA's slots
-    float *rst = reinterpret_cast<float *>(sm + m.rst);
     uint8_t *area = sm + m.area;
     __shared__ int s_wsum[W], s_uc;
 
     const int *ui = dv.unit_info + u * UI_STRIDE;
-    const int b = ui[UI_B], h = u % dv.h_kv, C = ui[UI_C], L = ui[UI_L];
+    const int b = ui[UI_B], C = ui[UI_C], L = ui[UI_L];
     const int S = ui[UI_S], rlo = ui[UI_RLO];
     const int nnow = dv.n_now[b];
     const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
@@ -248,8 +293,6 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     const bool resid = dv.residual != 0;
 
     // ------------------------------------------------------------ P0: query, weights
-    uint32_t qa[8][4];
-    load_q_frags(qa, qg, G);
     load_weights(w, qg, G, dv.tau);
     pdl_wait();
     pdl_trigger();
@@ -269,35 +312,28 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
 #pragma unroll
             for (int g = 0; g < GT; ++g)
                 if (g < G) {
-                    csl[g * m.SL + cl] = sl[g];
+                    ckey[g * m.SLp + cl] = rank_key(sl[g], c);
                     crs[g * m.SL + cl] = res[g];
                 }
             cnn[cl] = n;
         }
     }
-    __syncthreads();
-    const int KC = m.KC;
-    if (tc > 0) {  // this slice's top-KC per head (KC = min(slice, tc)), sorted, -1 padded
-        const int span = max(ns, KC);
-        for (int e = tid; e < G * span; e += NT) {
-            const int g = e / span, i = e % span;
-            if (i < ns) {
-                const float v = csl[g * m.SL + i];
-                int rank = 0;
-                for (int kk = 0; kk < ns; ++kk) rank += ranks_before(csl[g * m.SL + kk], kk, v, i);
-                if (rank < KC) {
-                    cand_s[g * KC + rank] = v;
-                    cand_i[g * KC + rank] = v == -INFINITY ? -1 : c0 + i;
-                }
-            } else {
-                cand_s[g * KC + i] = -INFINITY;
-                cand_i[g * KC + i] = -1;
-            }
-        }
-    }
+    for (int e = tid; e < G * (m.SLp - ns); e += NT)  // padding keys
+        ckey[(e / (m.SLp - ns)) * m.SLp + ns + e % (m.SLp - ns)] = 0ull;
+    for (int e = tid; e < m.SL; e += NT) slm[e] = 0u;
     for (int e = tid; e < G * tcc; e += NT) selc[e] = -1;
     for (int e = tid; e < (dv.c_max + 31) / 32; e += NT) bm[e] = 0u;
-    for (int e = tid; e < m.SL; e += NT) slm[e] = 0u;
+    const int KC = m.KC;
+    for (int e = tid; e < G * KC; e += NT) cand_k[e] = 0ull;
+    __syncthreads();
+    if (tc > 0)  // this slice's top-KC per head (KC = min(slice, tc)) by rank, 0 padded
+        for (int e = tid; e < G * ns; e += NT) {
+            const int g = e / ns, i = e % ns;
+            const unsigned long long x = ckey[g * m.SLp + i];
+            if (x == 0ull) continue;
+            const int rank = key_rank(ckey + g * m.SLp, m.SLp, x, KC);
+            if (rank < KC) cand_k[g * KC + rank] = x;
+        }
     cluster.sync();  // S1: candidates of every slice are published
 
     // ------------------------------------------------------- P2: selection and union
@@ -309,34 +345,18 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                 selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
             }
         } else {
-            for (int e = tid; e < CS * G * KC; e += NT) {  // gather [g][src][r]
-                const int src = e / (G * KC), rem = e % (G * KC), g = rem / KC, r = rem % KC;
-                allc_s[(g * CS + src) * KC + r] = cluster.map_shared_rank(cand_s, src)[rem];
-                allc_i[(g * CS + src) * KC + r] = cluster.map_shared_rank(cand_i, src)[rem];
+            const int npool = CS * KC;
+            for (int e = tid; e < G * m.NPOOL; e += NT) {  // gather, rank-major: [g][r][src]
+                const int g = e / m.NPOOL, q = e % m.NPOOL, r = q / CS, src = q % CS;
+                allc_k[e] = q < npool ? cluster.map_shared_rank(cand_k, src)[g * KC + r] : 0ull;
             }
             __syncthreads();
-            // element (g, list p, position r): rank over all lists of head g = r plus, for
-            // every other list, the length of its prefix that ranks before the element
-            for (int e = tid; e < G * CS * KC; e += NT) {
-                const int g = e / (CS * KC), pr = e % (CS * KC), pl = pr / KC, r = pr % KC;
-                const float *cs = allc_s + (size_t)g * CS * KC;
-                const int *ci = allc_i + (size_t)g * CS * KC;
-                const int x = ci[pr];
-                if (x < 0) continue;
-                const float v = cs[pr];
-                int rank = r;
-                for (int q = 0; q < CS && rank < tc; ++q) {
-                    if (q == pl) continue;
-                    int lo = 0, hi = KC;
-                    while (lo < hi) {
-                        const int mid = (lo + hi) >> 1;
-                        const int xm = ci[q * KC + mid];
-                        if (xm >= 0 && ranks_before(cs[q * KC + mid], xm, v, x)) lo = mid + 1;
-                        else hi = mid;
-                    }
-                    rank += lo;
-                }
-                if (rank < tc) selc[g * tc + rank] = x;
+            for (int e = tid; e < G * npool; e += NT) {
+                const int g = e / npool;
+                const unsigned long long x = allc_k[g * m.NPOOL + e % npool];
+                if (x == 0ull) continue;
+                const int rank = key_rank(allc_k + g * m.NPOOL, m.NPOOL, x, tc);
+                if (rank < tc) selc[g * tc + rank] = key_index(x);
             }
         }
     }
@@ -388,30 +408,31 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     // ----------------------------------------- P3: this CTA's union slots, residual
     const int nmy = Uc > k ? (Uc - k + CS - 1) / CS : 0;  // slots k, k+CS, ...
     const int npair = nmy * L;                              // (slot, subcluster) pairs
-    float *vst = reinterpret_cast<float *>(area);           // [PCH][d] subcluster means
-    float *vcl = vst + (size_t)PCH * MOG_D;                 // [RCH][d] slice cluster means
-    float *rws = vcl + (size_t)RCH * MOG_D;                 // [W][G][PART_W] residual states
+    float *vst = reinterpret_cast<float *>(area);           // [PCHd][d] subcluster means
+    float *vcl = vst + (size_t)m.PCHd * MOG_D;              // [RCHd][d] slice cluster means
+    // offsets and sizes of the slots' subclusters, and the first value means, in flight
+    // while the subcluster scores are computed
     for (int e = tid; e < nmy * (L + 1); e += NT) {
         const int s = e / (L + 1), i = e % (L + 1);
-        const int c = ucl[k + s * CS];
-        sso[s * (MOG_MAX_L + 1) + i] = dv.sub_off[(size_t)u * dv.sub_off_stride + (size_t)c * L + i];
-        if (i < L) snn[s * MOG_MAX_L + i] = dv.sub_n[usg + (size_t)c * L + i];
+        const size_t c = (size_t)ucl[k + s * CS];
+        cp_async4(smem_u32(sso + s * (MOG_MAX_L + 1) + i), dv.sub_off + (size_t)u * dv.sub_off_stride + c * L + i);
+        if (i < L) cp_async4(smem_u32(snn + s * MOG_MAX_L + i), dv.sub_n + usg + c * L + i);
     }
-    auto stage_pairs = [&](int p0) {  // value means of pairs p0 .. p0 + PCH
-        const int cnt = min(PCH, npair - p0);
+    auto stage_pairs = [&](int p0) {  // value means of pairs p0 .. p0 + PCHd
+        const int cnt = min(m.PCHd, npair - p0);
         for (int e = tid; e < cnt * 32; e += NT) {
             const int pr = p0 + e / 32, s = pr / L, l = pr % L;
             cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
                        dv.sub_vbar + (usg + (size_t)ucl[k + s * CS] * L + l) * MOG_D + 4 * (e % 32), 16);
         }
     };
-    if (resid && npair > 0) stage_pairs(0);
     auto stage_slice = [&](int k0) {
-        const int cnt = min(RCH, ns - k0);
+        const int cnt = min(m.RCHd, ns - k0);
         for (int e = tid; e < cnt * 32; e += NT)
             cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
                        dv.cl_vbar + (ug + c0 + k0 + e / 32) * MOG_D + 4 * (e % 32), 16);
     };
+    if (resid && npair > 0) stage_pairs(0);
     if (resid && ns > 0) stage_slice(0);
     cp_async_commit();
     for (int base = 0; base < npair; base += NT / 4) {  // subcluster scores, 4 lanes a pair
@@ -427,20 +448,23 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             for (int g = 0; g < GT; ++g)
                 if (g < G) {
                     sres[(s * G + g) * MOG_MAX_L + l] = res[g];
-                    ssl[(s * G + g) * MOG_MAX_L + l] = sl[g];
+                    skey[(s * G + g) * MOG_MAX_L + l] = rank_key(sl[g], l);
                 }
         }
     }
     for (int e = tid; e < nmy * MOG_MAX_L; e += NT) smask[e] = 0u;
     for (int e = tid; e < nmy; e += NT) shm[e] = 0u;
+    cp_async_wait<0>();
     __syncthreads();
     // top-ts subclusters of every head that chose a slot's cluster
     for (int e = warp; e < nmy * G; e += W) {
         const int s = e / G, g = e % G;
         const int c = ucl[k + s * CS];
-        int rk = -1;
-        for (int r = 0; r < tc; ++r)
-            if (selc[g * tc + r] == c) { rk = r; break; }
+        int rk = -1;  // the rank at which head g chose c
+        for (int r0 = 0; r0 < tc && rk < 0; r0 += 32) {
+            const uint32_t hit = __ballot_sync(0xffffffffu, r0 + lane < tc && selc[g * tc + r0 + lane] == c);
+            if (hit) rk = r0 + __ffs(hit) - 1;
+        }
         if (rk < 0) continue;
         if (lane == 0) atomicOr(&shm[s], 1u << g);
         int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
@@ -454,87 +478,36 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                 if (ok) atomicOr(&smask[s * MOG_MAX_L + l2], 1u << g);
             }
         } else {
-            for (int r = lane; r < ts; r += 32) subs[r] = -1;
-            __syncwarp();
-            const float *sc = ssl + (s * G + g) * MOG_MAX_L;
-            const float v = lane < L ? sc[lane] : -INFINITY;
+            const unsigned long long *kk = skey + (s * G + g) * MOG_MAX_L;
+            const unsigned long long x = lane < L ? kk[lane] : 0ull;
             int rank = 0;
-            for (int kk = 0; kk < L; ++kk) rank += ranks_before(sc[kk], kk, v, lane);
-            if (lane < L && v != -INFINITY && rank < ts) {
+            for (int j = 0; j < L; ++j) rank += kk[j] > x;
+            if (x != 0ull && rank < ts) {
                 subs[rank] = lane;
                 atomicOr(&smask[s * MOG_MAX_L + lane], 1u << g);
             }
+            const int nvalid = __popc(__ballot_sync(0xffffffffu, x != 0ull));
+            for (int r = nvalid + lane; r < ts; r += 32) subs[r] = -1;
         }
     }
     __syncthreads();
     for (int s = warp; s < nmy; s += W) {  // prefix of the chosen subclusters' sizes
         const int *so = sso + s * (MOG_MAX_L + 1);
-        const int cnt = lane < L && smask[s * MOG_MAX_L + lane] ? so[lane + 1] - so[lane] : 0;
+        const bool ch = lane < L && smask[s * MOG_MAX_L + lane] != 0u;
+        const int cnt = ch ? so[lane + 1] - so[lane] : 0;
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
+        const uint32_t chosen = __ballot_sync(0xffffffffu, ch);
         if (lane < L) spref[s * (MOG_MAX_L + 1) + lane + 1] = incl;
         if (lane == 0) {
             spref[s * (MOG_MAX_L + 1)] = 0;
-            pub_coff[s] = so[0];
+            pub_nseg[s] = __popc(chosen);
         }
         if (lane == L - 1) pub_cnt[s] = incl;
-    }
-    __syncthreads();
-    if (warp == 0) {  // row prefix over this CTA's slots
-        int run = 0;
-        for (int s0 = 0; s0 < nmy; s0 += 32) {
-            const int s = s0 + lane;
-            const int cnt = s < nmy ? spref[s * (MOG_MAX_L + 1) + L] : 0;
-            int incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (s < nmy) slp[s] = run + incl - cnt;
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) slp[nmy] = run;
-    }
-    __syncthreads();
-    {  // member rows of the chosen subclusters -> the unit's row list (perm order); four
-       // independent perm loads in flight per thread
-        const int *perm = dv.perm + (size_t)u * dv.n_cap;
-        int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
-        uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
-        const int tot = slp[nmy];
-        for (int i0 = tid; i0 < tot; i0 += 4 * NT) {
-            int src[4], dst[4];
-            uint32_t mk[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = i0 + j * NT;
-                src[j] = -1;
-                if (i < tot) {
-                    const int s = last_le(slp, nmy, i);
-                    const int ii = i - slp[s];
-                    const int *sp = spref + s * (MOG_MAX_L + 1);
-                    const int kk = last_le(sp, L, ii);
-                    const int *so = sso + s * (MOG_MAX_L + 1);
-                    src[j] = so[kk] + (ii - sp[kk]);
-                    dst[j] = so[0] + ii;
-                    mk[j] = smask[s * MOG_MAX_L + kk];
-                }
-            }
-            int pv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) pv[j] = src[j] >= 0 ? __ldg(perm + src[j]) : 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (src[j] >= 0) {
-                    rowpos[dst[j]] = pv[j];
-                    rowmask[dst[j]] = mk[j];
-                }
-        }
     }
     // Gaussian residual: warps take items (pairs, then slice clusters) round-robin; lane
     // owns dims 4*lane..+3; per-warp states are merged into rst
@@ -543,9 +516,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
 #pragma unroll
         for (int g = 0; g < GT; ++g) st[g].init();
         if (resid) {
-            cp_async_wait<0>();
             __syncthreads();
-            for (int p0 = 0; p0 < npair; p0 += PCH) {
+            for (int p0 = 0; p0 < npair; p0 += m.PCHd) {
                 if (p0 > 0) {  // further pairs (many slots per CTA)
                     __syncthreads();
                     stage_pairs(p0);
@@ -553,7 +525,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                     cp_async_wait<0>();
                     __syncthreads();
                 }
-                const int cnt = min(PCH, npair - p0);
+                const int cnt = min(m.PCHd, npair - p0);
                 for (int e = warp; e < cnt; e += W) {
                     const int s = (p0 + e) / L, l = (p0 + e) % L;
                     if (snn[s * MOG_MAX_L + l] <= 0) continue;
@@ -565,7 +537,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                             st[g].absorb(sres[(s * G + g) * MOG_MAX_L + l] * LOG2E, vrow);
                 }
             }
-            for (int k0 = 0; k0 < ns; k0 += RCH) {
+            for (int k0 = 0; k0 < ns; k0 += m.RCHd) {
                 if (k0 > 0) {
                     __syncthreads();
                     stage_slice(k0);
@@ -573,7 +545,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                     cp_async_wait<0>();
                     __syncthreads();
                 }
-                const int cnt = min(RCH, ns - k0);
+                const int cnt = min(m.RCHd, ns - k0);
                 for (int e = warp; e < cnt; e += W) {
                     const int cl = k0 + e;
                     if (cnn[cl] <= 0) continue;
@@ -585,6 +557,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                 }
             }
         }
+        __syncthreads();  // the value means are read: the warp states take their place
+        float *rws = reinterpret_cast<float *>(area);  // [W][G][PART_W]
 #pragma unroll
         for (int g = 0; g < GT; ++g) {
             if (g >= G) break;
@@ -598,9 +572,13 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         __syncthreads();
         merge_states(rws, W, G, rst);
     }
-    cp_async_wait<0>();
-    cluster.sync();  // S2: row lists (global) and their counts (shared) are published
-    // ------------------------- P4: the unit's row plan for the rows kernel (CTA 0)
+    cluster.sync();  // S2: slot counts and residual states are published
+
+    // ------------------------------- P4: row segments, rows-kernel plan, residual merge
+    for (int j = tid; j < Uc; j += NT) {  // every slot's rows and segments, from its owner
+        gpre[j] = cluster.map_shared_rank(pub_cnt, j % CS)[j / CS];
+        gseg[j] = cluster.map_shared_rank(pub_nseg, j % CS)[j / CS];
+    }
     for (int g = k; g < G; g += CS) {  // the unit's residual: CS states merged per head
         if (tid >= MOG_D) break;
         float mx = -INFINITY;
@@ -622,52 +600,85 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         }
         o[PART_ACC + tid] = acc;
     }
-    if (k == 0 && warp == W - 1) {
-        int *plan = dv.slotcnt + (size_t)u * PLAN_W;  // [8 | pre[0..Uc] | coff[0..Uc)]
-        int run = n_anchor;
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefixes: rows after the anchors, segments from 0
+        int rrun = n_anchor, srun = 0;
         for (int j0 = 0; j0 < Uc; j0 += 32) {
             const int j = j0 + lane;
-            int cnt = 0, coff = 0;
-            if (j < Uc) {
-                const int own = j % CS, s = j / CS;
-                cnt = cluster.map_shared_rank(pub_cnt, own)[s];
-                coff = cluster.map_shared_rank(pub_coff, own)[s];
-            }
-            int incl = cnt;
+            const int rc = j < Uc ? gpre[j] : 0, sc = j < Uc ? gseg[j] : 0;
+            int ri = rc, si = sc;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+                const int y = __shfl_up_sync(0xffffffffu, ri, o);
+                const int z = __shfl_up_sync(0xffffffffu, si, o);
+                if (lane >= o) {
+                    ri += y;
+                    si += z;
+                }
             }
             if (j < Uc) {
-                plan[PLAN_PRE + j] = run + incl - cnt;
-                plan[PLAN_COFF + j] = coff;
+                gpre[j] = rrun + ri - rc;
+                gseg[j] = srun + si - sc;
             }
-            run += __shfl_sync(0xffffffffu, incl, 31);
+            rrun += __shfl_sync(0xffffffffu, ri, 31);
+            srun += __shfl_sync(0xffffffffu, si, 31);
         }
         if (lane == 0) {
-            plan[0] = Uc;
-            plan[1] = run;  // T: anchors + selected rows
+            gpre[Uc] = rrun;
+            gseg[Uc] = srun;
+        }
+    }
+    __syncthreads();
+    const int T = gpre[Uc], P = dv.P;
+    int *plan = dv.plan + (size_t)u * PLAN_W;
+    const size_t useg = (size_t)u * dv.nseg_max;
+    for (int s = warp; s < nmy; s += W) {  // this CTA's slots: segments and rows-CTA starts
+        const int j = k + s * CS;
+        const uint32_t chosen = __ballot_sync(0xffffffffu, lane < L && smask[s * MOG_MAX_L + lane] != 0u);
+        if (lane < L && ((chosen >> lane) & 1u)) {
+            const size_t sg = useg + gseg[j] + __popc(chosen & lanemask_lt());
+            dv.segrow[sg] = gpre[j] + spref[s * (MOG_MAX_L + 1) + lane];
+            dv.segoff[sg] = sso[s * (MOG_MAX_L + 1) + lane];
+            dv.segmask[sg] = smask[s * MOG_MAX_L + lane];
+        }
+        const int ra = gpre[j], rb = gpre[j + 1];
+        if (ra < rb) {  // rows-kernel CTAs p whose first row floor(T p / P) lies in [ra, rb)
+            const int pa = (int)(((int64_t)ra * P + T - 1) / T);
+            const int pb = (int)(((int64_t)rb * P + T - 1) / T);
+            for (int p = pa + lane; p < pb; p += 32) {
+                const int rr = (int)((int64_t)T * p / P) - ra;
+                const int l = last_le(spref + s * (MOG_MAX_L + 1), L, rr);  // a chosen subcluster
+                plan[PLAN_START + p] = gseg[j] + __popc(chosen & ((1u << l) - 1u));
+            }
+        }
+    }
+    if (k == 0) {
+        if (tid == 0) {
+            plan[0] = gseg[Uc];  // segments
+            plan[1] = T;
             plan[2] = n_anchor;
             plan[3] = s_cnt;
             plan[4] = rlo;
-            plan[PLAN_PRE + Uc] = run;
         }
+        // CTAs that start among the anchors (or in an empty list) start at segment 0
+        const int pe = T > 0 ? (int)(((int64_t)n_anchor * P + T - 1) / T) : P;
+        for (int p = tid; p < min(pe, P); p += NT) plan[PLAN_START + p] = 0;
     }
-    cluster.sync();  // S3: the owners' counts and residual states have been read
+    cluster.sync();  // S3: the owners' counts, residual states and candidates have been read
 }
-
 
 constexpr int RW_SUPER = 256;                  // row positions per batch in the rows kernel
 constexpr int RW_TPB = RW_SUPER / AT_ROWS;     // tiles per batch
 constexpr int RW_PER = RW_SUPER / AT_THREADS;  // positions a thread fetches per batch
+constexpr int RW_SEGW = 512;                   // row segments held in shared memory
 static_assert(RW_TPB >= AT_STAGES - 1, "the first batch must cover the pipeline's prologue");
 
 // Kernel B: grid (P, units), 4 warps, two CTAs per SM.  Rows [p*T/P, (p+1)*T/P) of the
-// unit's exact list (anchors, then the union slots' rows in slot order) through the
-// 64-row tile engine.  Positions are fetched into registers one batch ahead and moved to
-// shared memory when the pipeline reaches the batch, so no tile copy waits on a position
-// load.  One unnormalised partial per CTA.
+// unit's exact list (anchors, then the chosen subclusters' rows, segment by segment)
+// through the 64-row tile engine.  A window of segments sits in shared memory; a row's
+// position is read from the partition (perm) at its segment's offset.  Positions are
+// fetched into registers two batches ahead and moved to shared memory when the pipeline
+// reaches the batch, so no tile copy waits on a position load.  One partial per CTA.
 template <int GT>
 __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     extern __shared__ __align__(128) uint8_t tile[];
@@ -676,6 +687,8 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     __shared__ __align__(16) int s_plan[PLAN_W];
     __shared__ int s_pos[2][RW_SUPER];
     __shared__ uint32_t s_mk[2][RW_SUPER];
+    __shared__ int s_segrow[RW_SEGW + 1], s_segoff[RW_SEGW];
+    __shared__ uint32_t s_segmask[RW_SEGW];
     const int u = blockIdx.y, p = blockIdx.x, P = gridDim.x;
     const int tid = threadIdx.x;
     const int *ui = dv.unit_info + u * UI_STRIDE;
@@ -683,51 +696,76 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
     uint32_t qa[8][4];
     load_q_frags(qa, a.q + (size_t)u * G * MOG_D, G);
-    pdl_wait();  // the selection kernel's row lists and plan
+    pdl_wait();  // the selection kernel's segments and plan
     pdl_trigger();
     {
-        const int *plan = dv.slotcnt + (size_t)u * PLAN_W;
+        const int *plan = dv.plan + (size_t)u * PLAN_W;
         for (int q = tid; q < PLAN_W / 4; q += AT_THREADS) cp_async16(smem_u32(s_plan + 4 * q), plan + 4 * q, 16);
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
     }
-    const int Uc = s_plan[0], T = s_plan[1], n_anchor = s_plan[2], s_cnt = s_plan[3], rlo = s_plan[4];
-    const int *s_pre = s_plan + PLAN_PRE, *s_coff = s_plan + PLAN_COFF;
+    const int NS = s_plan[0], T = s_plan[1], n_anchor = s_plan[2], s_cnt = s_plan[3], rlo = s_plan[4];
     const int r0 = (int)((int64_t)T * p / P), r1 = (int)((int64_t)T * (p + 1) / P);
     const int nrow = r1 - r0, nt = (nrow + AT_ROWS - 1) / AT_ROWS;
     const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
     const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
-    const int *rowpos = dv.rowpos + (size_t)u * dv.n_cap;
-    const uint32_t *rowmask = dv.rowmask + (size_t)u * dv.n_cap;
-    int pf_pos[RW_PER];
-    uint32_t pf_mk[RW_PER];
-    auto fetch = [&](int bt) {  // positions of batch bt into registers
+    const int *perm = dv.perm + (size_t)u * dv.n_cap;
+    const size_t useg = (size_t)u * dv.nseg_max;
+    int wfirst = 0, wn = 0;  // the window: segments wfirst .. wfirst + wn
+    auto load_window = [&](int w0) {  // all threads; the caller synchronises
+        wfirst = w0;
+        wn = max(0, min(RW_SEGW, NS - w0));
+        for (int t = tid; t <= wn; t += AT_THREADS) {
+            const int sg = w0 + t;
+            s_segrow[t] = sg < NS ? __ldcg(dv.segrow + useg + sg) : T;
+            if (t < wn) {
+                s_segoff[t] = __ldcg(dv.segoff + useg + sg);
+                s_segmask[t] = __ldcg(dv.segmask + useg + sg);
+            }
+        }
+    };
+    // positions of batch bt into registers; two batches in flight (even / odd sets)
+    int pf_pos[2][RW_PER];
+    uint32_t pf_mk[2][RW_PER];
+    auto fetch_into = [&](int bt, int (&pp)[RW_PER], uint32_t (&mm)[RW_PER]) {
+        const int first = r0 + bt * RW_SUPER, last = min(r1, first + RW_SUPER) - 1;
+        if (last >= n_anchor && last >= s_segrow[wn]) {  // past the window: move it
+            const int f = max(first, n_anchor);
+            const int w0 = f < s_segrow[wn] ? wfirst + last_le(s_segrow, wn, f) : wfirst + wn;
+            __syncthreads();
+            load_window(w0);
+            __syncthreads();
+        }
 #pragma unroll
         for (int jj = 0; jj < RW_PER; ++jj) {
-            const int i = r0 + bt * RW_SUPER + tid + jj * AT_THREADS;
-            int pp = 0;
-            uint32_t mm = 0u;
-            if (i < r1) {
+            const int i = first + tid + jj * AT_THREADS;
+            int q = 0;
+            uint32_t mk = 0u;
+            if (i <= last) {
                 if (i < n_anchor) {
-                    pp = i < s_cnt ? i : rlo + (i - s_cnt);
-                    mm = allm;
+                    q = i < s_cnt ? i : rlo + (i - s_cnt);
+                    mk = allm;
                 } else {
-                    const int sl = last_le(s_pre, Uc, i);  // the slot holding row i
-                    const int kk = s_coff[sl] + (i - s_pre[sl]);
-                    pp = __ldcg(rowpos + kk);
-                    mm = __ldcg(rowmask + kk);
+                    const int sg = last_le(s_segrow, wn, i);  // the segment holding row i
+                    const int pi = s_segoff[sg] + (i - s_segrow[sg]);
+                    q = (unsigned)pi < (unsigned)dv.n_cap ? __ldg(perm + pi) : -1;
+                    mk = s_segmask[sg];
                 }
             }
-            pf_pos[jj] = pp;
-            pf_mk[jj] = mm;
+            pp[jj] = q;
+            mm[jj] = mk;
         }
+    };
+    auto fetch = [&](int bt) {
+        if (bt & 1) fetch_into(bt, pf_pos[1], pf_mk[1]);
+        else fetch_into(bt, pf_pos[0], pf_mk[0]);
     };
     auto place = [&](int bt) {  // registers -> shared buffer of batch bt
 #pragma unroll
         for (int jj = 0; jj < RW_PER; ++jj) {
-            s_pos[bt & 1][tid + jj * AT_THREADS] = pf_pos[jj];
-            s_mk[bt & 1][tid + jj * AT_THREADS] = pf_mk[jj];
+            s_pos[bt & 1][tid + jj * AT_THREADS] = (bt & 1) ? pf_pos[1][jj] : pf_pos[0][jj];
+            s_mk[bt & 1][tid + jj * AT_THREADS] = (bt & 1) ? pf_mk[1][jj] : pf_mk[0][jj];
         }
     };
     auto issue = [&](int t) {
@@ -749,9 +787,12 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     acc.init();
     const float scale2 = dv.tau * LOG2E;
     if (nt > 0) {
+        load_window(s_plan[PLAN_START + p]);
+        __syncthreads();
         fetch(0);
         place(0);
         if (nrow > RW_SUPER) fetch(1);
+        if (nrow > 2 * RW_SUPER) fetch(2);
     }
     __syncthreads();
 #pragma unroll
@@ -763,17 +804,19 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
         cp_async_wait<AT_STAGES - 2>();
         __syncthreads();
         const int ti = t + AT_STAGES - 1;
+        int next = -1;  // batch whose positions are fetched after this tile's compute
         if (ti < nt) {
             if (ti % RW_TPB == 0) {  // first tile of a batch: its positions go to shared memory
                 const int bt = ti / RW_TPB;
                 place(bt);
                 __syncthreads();
-                if ((bt + 1) * RW_SUPER < nrow) fetch(bt + 1);
+                if ((bt + 2) * RW_SUPER < nrow) next = bt + 2;  // into the set place() freed
             }
             issue(ti);
         }
         cp_async_commit();
         compute_tile(acc, qa, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
+        if (next >= 0) fetch(next);
     }
     cp_async_wait<0>();
     __syncthreads();
@@ -885,7 +928,7 @@ static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     const int sms = num_sms();
     for (int cs = 16; cs >= 1; --cs) {  // any size: e.g. 12-CTA clusters fit where 16 do not
         if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;  // keep clusters resident
-        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, cs, md_warps(GT));
+        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT));
         if (m.total > MD_SMEM_MAX) continue;
         if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -964,8 +1007,6 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
     a.out = out;
     a.sel_in = sel_in;
     a.SW = dv.tc + dv.tc * dv.ts;
-    a.cand_s = dv.cand_s;
-    a.cand_i = dv.cand_i;
     const int G = dv.G;
     cudaError_t e;
     if (G <= 1) e = launch_steps<1>(a, s, events);
@@ -980,8 +1021,8 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
     return e;
 }
 
-size_t slot_smem_bytes(int G, int c_max, int tc) {  // the smallest layout (16-CTA clusters)
-    return (size_t)md_layout(G, tc, c_max, 16, md_warps(G <= 4 ? 4 : 16)).total;
+size_t slot_smem_bytes(int G, int c_max, int l_max, int tc) {  // the smallest layout (16-CTA clusters)
+    return (size_t)md_layout(G, tc, c_max, l_max, 16, md_warps(G <= 4 ? 4 : 16)).total;
 }
 
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,

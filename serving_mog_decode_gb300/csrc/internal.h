@@ -14,12 +14,11 @@ enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
 constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
 constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
 constexpr int PART_SLOTS = MAX_SPLITS + 1;  // partials per unit: rows CTAs, then the residual
-// Row plan per unit, written by the selection kernel for the rows kernel:
-// [0] union size Uc, [1] rows T, [2] anchors, [3] sink rows, [4] first recent position,
-// [PLAN_PRE + j] first row of slot j (j <= Uc), [PLAN_COFF + j] slot j's row-list offset.
-constexpr int PLAN_PRE = 8;
-constexpr int PLAN_COFF = PLAN_PRE + MOG_MAX_UNION + 1;
-constexpr int PLAN_W = (PLAN_COFF + MOG_MAX_UNION + 3) / 4 * 4;  // ints, whole 16-byte chunks
+// Rows-kernel plan per unit, written by the selection kernel: [0] segments NS, [1] rows T,
+// [2] anchors, [3] sink rows, [4] first recent position, [PLAN_START + p] the segment
+// holding the first row of rows-kernel CTA p (0 while that row is an anchor).
+constexpr int PLAN_START = 8;
+constexpr int PLAN_W = PLAN_START + MAX_SPLITS;  // ints, whole 16-byte chunks
 constexpr int MAX_C = 4096;        // clusters per unit supported
 
 // Typed view of an arena, passed by value to every kernel.
@@ -30,7 +29,7 @@ struct Dev {
     int64_t sb, sh, sn;
     // shape
     int batch, h_kv, G, units, n_cap, c_max, l_max, tc, ts, T1, T2, score_mode, residual;
-    int P, P1, nchunks;
+    int P, nchunks, nseg_max;
     int64_t sub_off_stride;
     float tau;
     // persistent
@@ -40,12 +39,11 @@ struct Dev {
     float *cent;
     int *permA, *changed, *fb_list, *fb_cnt, *hist, *offs, *ctot, *coff, *sub_assign;
     // decode workspace
-    float *cscore, *subscore, *partials;
-    uint32_t *cselmask, *uhm, *subres, *rowmask;
-    int *ucl, *ucount, *sel, *slotcnt, *slotcoff, *rowpos;
-    unsigned *counters;
-    float *cand_s;  // [units][P1][G][tc] per-slice top clusters
-    int *cand_i;
+    float *partials;  // [units][PART_SLOTS][G][PART_W]
+    int *sel;         // [units][G][tc + tc*ts] selection of the last step
+    int *plan;        // [units][PLAN_W]
+    int *segrow, *segoff;  // [units][nseg_max] first row of a segment, its offset in perm
+    uint32_t *segmask;     // [units][nseg_max] heads that attend the segment
 
     __host__ __device__ const uint16_t *krow(int b, int h, int64_t pos) const {
         return K + b * sb + h * sh + pos * sn;
@@ -58,14 +56,13 @@ struct Dev {
 // Host-side plan: sizes and byte offsets of every array in the arena.
 struct Plan {
     int batch, h_kv, h_q, G, d, n_cap, units, c_max, l_max, tc, ts, T1, T2;
-    int score_mode, residual, P, P1, nchunks, n_mid_max;
+    int score_mode, residual, P, nchunks, n_mid_max, nseg_max;
     int64_t sub_off_stride;
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
         o_sub_vbar, o_l1_assign, o_status, o_l1_steps;
     int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
         o_sub_assign;
-    int64_t o_cscore, o_subscore, o_partials, o_cselmask, o_uhm, o_subres, o_rowmask, o_ucl,
-        o_ucount, o_sel, o_slotcnt, o_slotcoff, o_rowpos, o_counters, o_cand_s, o_cand_i;
+    int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask;
     int64_t total;
 };
 
@@ -90,7 +87,7 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
                          cudaStream_t s);
 int dense_splits(int units, int n_max);
 cudaError_t dense_static_scratch(float **ptr, size_t *bytes);
-size_t slot_smem_bytes(int G, int c_max, int tc);
+size_t slot_smem_bytes(int G, int c_max, int l_max, int tc);
 cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
                              int32_t *assign, int *changed, int *fb_list, int *fb_cnt,
                              cudaStream_t s);
