@@ -128,6 +128,8 @@ constexpr int RCH = 64;  // slice clusters staged per residual pass
 constexpr int PCH = 64;  // (slot, subcluster) pairs staged per residual pass
 // dynamic shared memory of the decode kernel: the 227 KB block limit less its static arrays
 constexpr int MD_SMEM_MAX = 226 * 1024;
+// ... and the budget that lets two CTAs share an SM (228 KB less reserved and static memory)
+constexpr int MD_SMEM_HALF = 110 * 1024;
 
 __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
@@ -135,14 +137,17 @@ __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 struct MdLay {
     int CS, SL, SLp, KC, NPOOL, NSLOT, SPC, warps, PCHd, RCHd;  // KC: candidates per slice and
                                                                   // head; NPOOL: CS*KC padded
-    int cand_k, pub_cnt, pub_nseg, rst;                           // read by other CTAs
-    int w, ckey, crs, cnn, slm, allc_k, selc, bm, ucl, gpre, gseg;  // local
-    int sres, skey, snn, sso, spref, smask, shm, area;
+    int cand_k, allc_k, selc, gpre, gseg;  // allc_k, selc, gpre, gseg receive other CTAs' pushes
+    int w, ckey, crs, cnn, slm, bm, ucl;
+    int sres, ssl, snn, sso, spref, smask, shm, area;
     int total;
 };
 
-// area: the staged value means of P3, then (aliased) the residual warp states.
-__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps) {
+// area: the staged value means of P3, then (aliased) the residual's group sums.  The value
+// means of all of a CTA's (slot, subcluster) pairs and slice clusters are staged at once
+// when that fits within `cap` bytes, else in passes sized to fit.
+__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps,
+                                           int cap) {
     MdLay m;
     int o = 0;
     auto take = [&](int bytes, int align) {
@@ -161,40 +166,41 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     m.NSLOT = tc > 0 ? (c_max < G * tc ? c_max : G * tc) : 1;
     m.SPC = (m.NSLOT + CS - 1) / CS;
     m.cand_k = take(8 * G * m.KC, 16);
-    m.pub_cnt = take(4 * m.SPC, 16);
-    m.pub_nseg = take(4 * m.SPC, 16);
-    m.rst = take(4 * G * PART_W, 16);
+    m.allc_k = take(8 * G * m.NPOOL, 16);
+    m.selc = take(4 * G * tcc, 16);
+    m.gpre = take(4 * (m.NSLOT + 1), 16);
+    m.gseg = take(4 * (m.NSLOT + 1), 16);
     m.w = take(16 * 64 * G, 16);
     m.ckey = take(8 * G * m.SLp, 16);
     m.crs = take(4 * G * m.SL, 16);
     m.cnn = take(4 * m.SL, 16);
     m.slm = take(4 * m.SL, 16);
-    m.allc_k = take(8 * G * m.NPOOL, 16);
-    m.selc = take(4 * G * tcc, 16);
     m.bm = take(4 * ((c_max + 31) / 32), 16);
     m.ucl = take(4 * m.NSLOT, 16);
-    m.gpre = take(4 * (m.NSLOT + 1), 16);
-    m.gseg = take(4 * (m.NSLOT + 1), 16);
     m.sres = take(4 * m.SPC * G * MOG_MAX_L, 16);
-    m.skey = take(8 * m.SPC * G * MOG_MAX_L, 16);
+    m.ssl = take(4 * m.SPC * G * MOG_MAX_L, 16);
     m.snn = take(4 * m.SPC * MOG_MAX_L, 16);
     m.sso = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
     m.shm = take(4 * m.SPC, 16);
-    // value means: all of this CTA's (slot, subcluster) pairs and slice clusters in one pass
-    // when they fit, else passes of at most 64 each
     const int base = (o + 127) & ~127;
-    const int states = warps * G * PART_W * 4;
+    const int red = warps * 32 * 16;  // group sums
     int pch = m.SPC * l_max, rch = m.SL;
-    if (base + ((pch + rch) * MOG_D * 4 > states ? (pch + rch) * MOG_D * 4 : states) > MD_SMEM_MAX) {
-        pch = pch < PCH ? pch : PCH;
-        rch = rch < RCH ? rch : RCH;
+    const int fit = (cap - base) / (MOG_D * 4);  // value means that fit
+    if (pch + rch > fit) {  // passes: shares in proportion, at least 8 each
+        const int r8 = rch < 8 ? rch : 8, p8 = pch < 8 ? pch : 8;
+        int rc = fit > 0 ? (int)((long long)fit * rch / (pch + rch)) : 0;
+        rc = rc < r8 ? r8 : rc;
+        int pc = fit - rc;
+        pc = pc < p8 ? p8 : pc;
+        rch = rch < rc ? rch : rc;
+        pch = pch < pc ? pch : pc;
     }
     m.PCHd = pch > 0 ? pch : 1;
     m.RCHd = rch > 0 ? rch : 1;
     const int vm = (m.PCHd + m.RCHd) * MOG_D * 4;
-    m.area = take(vm > states ? vm : states, 128);
+    m.area = take(vm > red ? vm : red, 128);
     m.total = (o + 15) & ~15;
     return m;
 }
@@ -234,16 +240,18 @@ __device__ __forceinline__ int key_rank(const unsigned long long *keys, int n, u
 }
 
 // Kernel A: one thread-block cluster of CS CTAs per unit.  Selection, the Gaussian
-// residual and the rows kernel's plan:
-//  P1  CTA k scores its slice of clusters for the G query heads and keeps the slice's
-//      top-KC per head;
-//  P2  every CTA gathers the slices' candidates over distributed shared memory, takes each
-//      head's top-tc clusters and their union over the heads (ascending index);
+// residual and the rows kernel's plan.  Hand-offs between the CTAs are pushed (stores
+// into the other CTAs' shared memory) and made visible by a cluster barrier:
+//  P1  CTA k scores its slice of clusters for the G query heads and pushes the slice's
+//      top-KC keys per head into every CTA's candidate pool;
+//  P2  CTA k ranks its share of each head's pool and pushes the winners into every CTA's
+//      top-tc list; each CTA then forms the union over the heads (ascending index);
 //  P3  CTA k takes union slots k, k+CS, ...: subcluster scores, the top-ts subclusters of
-//      every head that chose the slot's cluster, and the residual of the unchosen
-//      subclusters of those heads and of its slice clusters no head chose;
-//  P4  the unit's row segments (one per chosen subcluster, in slot order), the first
-//      segment of every rows-kernel CTA, and the residual merged over the CTAs.
+//      every head that chose the slot's cluster, the slot's row and segment counts
+//      (pushed), and the residual of the unchosen subclusters of those heads and of its
+//      slice clusters no head chose, written as one unnormalised partial;
+//  P4  the unit's row segments (one per chosen subcluster, in slot order) and the first
+//      segment of every rows-kernel CTA.
 template <int GT>
 __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, MdLay m) {
     namespace cg = cooperative_groups;
@@ -256,22 +264,19 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     const int u = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned long long *cand_k = reinterpret_cast<unsigned long long *>(sm + m.cand_k);
-    int *pub_cnt = reinterpret_cast<int *>(sm + m.pub_cnt);    // rows of my slot s
-    int *pub_nseg = reinterpret_cast<int *>(sm + m.pub_nseg);  // chosen subclusters of slot s
-    float *rst = reinterpret_cast<float *>(sm + m.rst);        // this CTA's residual state
+    unsigned long long *allc_k = reinterpret_cast<unsigned long long *>(sm + m.allc_k);  // [g][r][src]
+    int *selc = reinterpret_cast<int *>(sm + m.selc);
+    int *gpre = reinterpret_cast<int *>(sm + m.gpre);  // rows of union slot j, then its first row
+    int *gseg = reinterpret_cast<int *>(sm + m.gseg);  // segments of slot j, then its first one
     float4 *w = reinterpret_cast<float4 *>(sm + m.w);
     unsigned long long *ckey = reinterpret_cast<unsigned long long *>(sm + m.ckey);  // slice keys
     float *crs = reinterpret_cast<float *>(sm + m.crs);
     int *cnn = reinterpret_cast<int *>(sm + m.cnn);
     uint32_t *slm = reinterpret_cast<uint32_t *>(sm + m.slm);  // heads that chose slice cluster
-    unsigned long long *allc_k = reinterpret_cast<unsigned long long *>(sm + m.allc_k);  // [g][r][src]
-    int *selc = reinterpret_cast<int *>(sm + m.selc);
     uint32_t *bm = reinterpret_cast<uint32_t *>(sm + m.bm);
     int *ucl = reinterpret_cast<int *>(sm + m.ucl);
-    int *gpre = reinterpret_cast<int *>(sm + m.gpre);  // first row of union slot j
-    int *gseg = reinterpret_cast<int *>(sm + m.gseg);  // first segment of union slot j
     float *sres = reinterpret_cast<float *>(sm + m.sres);
-    unsigned long long *skey = reinterpret_cast<unsigned long long *>(sm + m.skey);
+    float *ssl = reinterpret_cast<float *>(sm + m.ssl);  // subcluster selection scores
     int *snn = reinterpret_cast<int *>(sm + m.snn);
     int *sso = reinterpret_cast<int *>(sm + m.sso);
     int *spref = reinterpret_cast<int *>(sm + m.spref);
@@ -279,18 +284,19 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     uint32_t *shm = reinterpret_cast<uint32_t *>(sm + m.shm);  // heads that chose slot s
     uint8_t *area = sm + m.area;
     __shared__ int s_wsum[W], s_uc;
+    __shared__ float s_rm[MOG_MAX_G], s_rl[MOG_MAX_G];
 
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int b = ui[UI_B], C = ui[UI_C], L = ui[UI_L];
     const int S = ui[UI_S], rlo = ui[UI_RLO];
     const int nnow = dv.n_now[b];
     const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
-    const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
     const size_t ug = (size_t)u * dv.c_max;               // cluster index base
     const size_t usg = (size_t)u * dv.c_max * dv.l_max;   // subcluster index base
     const uint16_t *qg = a.q + (size_t)u * G * MOG_D;
     int *selu = dv.sel + (size_t)u * G * a.SW;
     const bool resid = dv.residual != 0;
+    const bool pooled = tc > 0 && !a.sel_in;  // selection from the scores (not given)
 
     // ------------------------------------------------------------ P0: query, weights
     load_weights(w, qg, G, dv.tau);
@@ -323,10 +329,13 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     for (int e = tid; e < m.SL; e += NT) slm[e] = 0u;
     for (int e = tid; e < G * tcc; e += NT) selc[e] = -1;
     for (int e = tid; e < (dv.c_max + 31) / 32; e += NT) bm[e] = 0u;
-    const int KC = m.KC;
+    const int KC = m.KC, npool = CS * KC;
     for (int e = tid; e < G * KC; e += NT) cand_k[e] = 0ull;
+    for (int e = tid; e < G * (m.NPOOL - npool); e += NT)  // this CTA's own pool padding
+        allc_k[(e / (m.NPOOL - npool)) * m.NPOOL + npool + e % (m.NPOOL - npool)] = 0ull;
     __syncthreads();
-    if (tc > 0)  // this slice's top-KC per head (KC = min(slice, tc)) by rank, 0 padded
+    if (pooled) {
+        // this slice's top-KC per head (KC = min(slice, tc)) by rank, 0 padded ...
         for (int e = tid; e < G * ns; e += NT) {
             const int g = e / ns, i = e % ns;
             const unsigned long long x = ckey[g * m.SLp + i];
@@ -334,33 +343,34 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             const int rank = key_rank(ckey + g * m.SLp, m.SLp, x, KC);
             if (rank < KC) cand_k[g * KC + rank] = x;
         }
-    cluster.sync();  // S1: candidates of every slice are published
-
-    // ------------------------------------------------------- P2: selection and union
-    if (tc > 0) {
-        if (a.sel_in) {
-            for (int e = tid; e < G * tc; e += NT) {
-                const int g = e / tc, r = e % tc;
-                const int cc = a.sel_in[((size_t)u * G + g) * a.SW + r];
-                selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
-            }
-        } else {
-            const int npool = CS * KC;
-            for (int e = tid; e < G * m.NPOOL; e += NT) {  // gather, rank-major: [g][r][src]
-                const int g = e / m.NPOOL, q = e % m.NPOOL, r = q / CS, src = q % CS;
-                allc_k[e] = q < npool ? cluster.map_shared_rank(cand_k, src)[g * KC + r] : 0ull;
-            }
-            __syncthreads();
-            for (int e = tid; e < G * npool; e += NT) {
-                const int g = e / npool;
-                const unsigned long long x = allc_k[g * m.NPOOL + e % npool];
-                if (x == 0ull) continue;
-                const int rank = key_rank(allc_k + g * m.NPOOL, m.NPOOL, x, tc);
-                if (rank < tc) selc[g * tc + rank] = key_index(x);
-            }
+        __syncthreads();
+        // ... pushed into every CTA's pool, rank-major: pool[g][r][k]
+        for (int e = tid; e < CS * G * KC; e += NT) {
+            const int dst = e / (G * KC), q = e % (G * KC), g = q / KC, r = q % KC;
+            cluster.map_shared_rank(allc_k, dst)[g * m.NPOOL + r * CS + k] = cand_k[q];
         }
     }
-    __syncthreads();
+    cluster.sync();  // S1: every CTA's pool is complete
+
+    // ------------------------------------------------------- P2: selection and union
+    if (pooled) {  // CTA k ranks pool entries e = k, k + CS, ... and pushes the winners
+        for (int e = k + CS * tid; e < G * npool; e += CS * NT) {
+            const int g = e / npool;
+            const unsigned long long x = allc_k[g * m.NPOOL + e % npool];
+            if (x == 0ull) continue;
+            const int rank = key_rank(allc_k + g * m.NPOOL, m.NPOOL, x, tc);
+            if (rank < tc)
+                for (int dst = 0; dst < CS; ++dst)
+                    cluster.map_shared_rank(selc, dst)[g * tc + rank] = key_index(x);
+        }
+    } else if (tc > 0) {
+        for (int e = tid; e < G * tc; e += NT) {
+            const int g = e / tc, r = e % tc;
+            const int cc = a.sel_in[((size_t)u * G + g) * a.SW + r];
+            selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
+        }
+    }
+    cluster.sync();  // S1b: every CTA holds the full top-tc lists
     for (int e = tid; e < G * tc; e += NT) {
         const int c = selc[e];
         if (c < 0) continue;
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             for (int g = 0; g < GT; ++g)
                 if (g < G) {
                     sres[(s * G + g) * MOG_MAX_L + l] = res[g];
-                    skey[(s * G + g) * MOG_MAX_L + l] = rank_key(sl[g], l);
+                    ssl[(s * G + g) * MOG_MAX_L + l] = sl[g];
                 }
         }
     }
@@ -478,10 +488,10 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                 if (ok) atomicOr(&smask[s * MOG_MAX_L + l2], 1u << g);
             }
         } else {
-            const unsigned long long *kk = skey + (s * G + g) * MOG_MAX_L;
-            const unsigned long long x = lane < L ? kk[lane] : 0ull;
+            const float *sc = ssl + (s * G + g) * MOG_MAX_L;
+            const unsigned long long x = lane < L ? rank_key(sc[lane], lane) : 0ull;
             int rank = 0;
-            for (int j = 0; j < L; ++j) rank += kk[j] > x;
+            for (int j = 0; j < L; ++j) rank += rank_key(sc[j], j) > x;
             if (x != 0ull && rank < ts) {
                 subs[rank] = lane;
                 atomicOr(&smask[s * MOG_MAX_L + lane], 1u << g);
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         }
     }
     __syncthreads();
-    for (int s = warp; s < nmy; s += W) {  // prefix of the chosen subclusters' sizes
+    for (int s = warp; s < nmy; s += W) {  // chosen subclusters: prefix of sizes, counts
         const int *so = sso + s * (MOG_MAX_L + 1);
         const bool ch = lane < L && smask[s * MOG_MAX_L + lane] != 0u;
         const int cnt = ch ? so[lane + 1] - so[lane] : 0;
@@ -501,22 +511,90 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        const uint32_t chosen = __ballot_sync(0xffffffffu, ch);
+        const int nseg = __popc(__ballot_sync(0xffffffffu, ch));
+        const int rows = __shfl_sync(0xffffffffu, incl, 31);
         if (lane < L) spref[s * (MOG_MAX_L + 1) + lane + 1] = incl;
-        if (lane == 0) {
-            spref[s * (MOG_MAX_L + 1)] = 0;
-            pub_nseg[s] = __popc(chosen);
+        if (lane == 0) spref[s * (MOG_MAX_L + 1)] = 0;
+        const int j = k + s * CS;  // the slot's counts, pushed to every CTA
+        for (int dst = lane; dst < CS; dst += 32) {
+            cluster.map_shared_rank(gpre, dst)[j] = rows;
+            cluster.map_shared_rank(gseg, dst)[j] = nseg;
         }
-        if (lane == L - 1) pub_cnt[s] = incl;
     }
-    // Gaussian residual: warps take items (pairs, then slice clusters) round-robin; lane
-    // owns dims 4*lane..+3; per-warp states are merged into rst
+    // Gaussian residual: for the heads that chose slot s but not its subcluster l, and for
+    // the heads that did not choose slice cluster c, exp(score) * value mean.  Pair weights
+    // go to wpr[p][g] (p = s*L + l, over the subcluster selection scores, no longer needed),
+    // slice weights replace the exponents in crs; per head the maximum M and the weight sum
+    // l; the weighted sum of the value means per (head, 4 dimensions), items split over
+    // ngrp thread groups; one partial (M, l, acc) per CTA.
     {
-        OnlineAcc st[GT];
+        float *wpr = ssl;
+        __syncthreads();
+        for (int e = tid; e < npair * G; e += NT) {  // exponents (log2), -inf when not needed
+            const int p = e / G, g = e - p * G, s = p / L, l = p - s * L;
+            const bool need = resid && snn[s * MOG_MAX_L + l] > 0 &&
+                              (((shm[s] & ~smask[s * MOG_MAX_L + l]) >> g) & 1u);
+            wpr[e] = need ? sres[(s * G + g) * MOG_MAX_L + l] * LOG2E : -INFINITY;
+        }
+        for (int e = tid; e < ns * G; e += NT) {
+            const int cl = e / G, g = e - cl * G;
+            float &x = crs[g * m.SL + cl];
+            const bool need = resid && cnn[cl] > 0 && !((slm[cl] >> g) & 1u);
+            x = need ? x * LOG2E : -INFINITY;
+        }
+        __syncthreads();
+        for (int g = warp; g < G; g += W) {  // per-head maximum
+            float mx = -INFINITY;
+            for (int p = lane; p < npair; p += 32) mx = fmaxf(mx, wpr[p * G + g]);
+            for (int cl = lane; cl < ns; cl += 32) mx = fmaxf(mx, crs[g * m.SL + cl]);
+            mx = warp_max(mx);
+            if (lane == 0) s_rm[g] = mx;
+        }
+        __syncthreads();
+        for (int e = tid; e < npair * G; e += NT) {  // weights
+            const float x = wpr[e];
+            wpr[e] = x == -INFINITY ? 0.f : exp2f(x - s_rm[e % G]);
+        }
+        for (int e = tid; e < ns * G; e += NT) {
+            const int g = e / ns;
+            float &x = crs[g * m.SL + e - g * ns];
+            x = x == -INFINITY ? 0.f : exp2f(x - s_rm[g]);
+        }
+        __syncthreads();
+        for (int g = warp; g < G; g += W) {  // per-head weight sums
+            float sw = 0.f;
+            for (int p = lane; p < npair; p += 32) sw += wpr[p * G + g];
+            for (int cl = lane; cl < ns; cl += 32) sw += crs[g * m.SL + cl];
+            sw = warp_sum(sw);
+            if (lane == 0) s_rl[g] = sw;
+        }
+        constexpr int MAXU = (GT * 32 + NT - 1) / NT;  // (head, 4 dims) units per thread
+        const int U4 = G * 32;
+        const int ngrp = max(1, NT / U4);
+        const int grp = ngrp > 1 ? tid / U4 : 0;
+        float4 acc4[MAXU];
 #pragma unroll
-        for (int g = 0; g < GT; ++g) st[g].init();
+        for (int uu = 0; uu < MAXU; ++uu) acc4[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto accumulate = [&](const float *vb, int cnt, auto weight) {
+#pragma unroll
+            for (int uu = 0; uu < MAXU; ++uu) {
+                const int unit = ngrp > 1 ? tid % U4 : tid + uu * NT;
+                if ((ngrp > 1 && (uu > 0 || grp >= ngrp)) || unit >= U4) continue;
+                const int g = unit >> 5, d4 = unit & 31;
+                float4 s4 = acc4[uu];
+                for (int i = grp; i < cnt; i += ngrp) {
+                    const float wt = weight(i, g);
+                    if (wt == 0.f) continue;
+                    const float4 v = *reinterpret_cast<const float4 *>(vb + (size_t)i * MOG_D + 4 * d4);
+                    s4.x += wt * v.x;
+                    s4.y += wt * v.y;
+                    s4.z += wt * v.z;
+                    s4.w += wt * v.w;
+                }
+                acc4[uu] = s4;
+            }
+        };
         if (resid) {
-            __syncthreads();
             for (int p0 = 0; p0 < npair; p0 += m.PCHd) {
                 if (p0 > 0) {  // further pairs (many slots per CTA)
                     __syncthreads();
@@ -525,17 +603,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                     cp_async_wait<0>();
                     __syncthreads();
                 }
-                const int cnt = min(m.PCHd, npair - p0);
-                for (int e = warp; e < cnt; e += W) {
-                    const int s = (p0 + e) / L, l = (p0 + e) % L;
-                    if (snn[s * MOG_MAX_L + l] <= 0) continue;
-                    const uint32_t need = shm[s] & ~smask[s * MOG_MAX_L + l];
-                    const float *vrow = vst + (size_t)e * MOG_D + 4 * lane;
-#pragma unroll
-                    for (int g = 0; g < GT; ++g)
-                        if (g < G && ((need >> g) & 1u))
-                            st[g].absorb(sres[(s * G + g) * MOG_MAX_L + l] * LOG2E, vrow);
-                }
+                accumulate(vst, min(m.PCHd, npair - p0), [&](int i, int g) { return wpr[(p0 + i) * G + g]; });
             }
             for (int k0 = 0; k0 < ns; k0 += m.RCHd) {
                 if (k0 > 0) {
@@ -545,62 +613,42 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
                     cp_async_wait<0>();
                     __syncthreads();
                 }
-                const int cnt = min(m.RCHd, ns - k0);
-                for (int e = warp; e < cnt; e += W) {
-                    const int cl = k0 + e;
-                    if (cnn[cl] <= 0) continue;
-                    const uint32_t need = allm & ~slm[cl];
-                    const float *vrow = vcl + (size_t)e * MOG_D + 4 * lane;
+                accumulate(vcl, min(m.RCHd, ns - k0), [&](int i, int g) { return crs[g * m.SL + k0 + i]; });
+            }
+        }
+        __syncthreads();  // the value means are read: the group sums take their place
+        float4 *red = reinterpret_cast<float4 *>(area);  // [ngrp][U4]
+        if (ngrp > 1) {
+            if (grp < ngrp) red[grp * U4 + tid % U4] = acc4[0];
+            __syncthreads();
+        }
+        float *o = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS + k) * G * PART_W;
 #pragma unroll
-                    for (int g = 0; g < GT; ++g)
-                        if (g < G && ((need >> g) & 1u)) st[g].absorb(crs[g * m.SL + cl] * LOG2E, vrow);
+        for (int uu = 0; uu < MAXU; ++uu) {
+            const int unit = tid + uu * NT;
+            if (unit >= U4) continue;
+            float4 s4 = acc4[uu];
+            if (ngrp > 1) {
+                s4 = red[unit];
+                for (int q = 1; q < ngrp; ++q) {
+                    const float4 t4 = red[q * U4 + unit];
+                    s4.x += t4.x;
+                    s4.y += t4.y;
+                    s4.z += t4.z;
+                    s4.w += t4.w;
                 }
             }
-        }
-        __syncthreads();  // the value means are read: the warp states take their place
-        float *rws = reinterpret_cast<float *>(area);  // [W][G][PART_W]
-#pragma unroll
-        for (int g = 0; g < GT; ++g) {
-            if (g >= G) break;
-            float *o = rws + ((size_t)warp * G + g) * PART_W;
-            if (lane == 0) {
-                o[0] = st[g].m;
-                o[1] = st[g].l;
+            const int g = unit >> 5, d4 = unit & 31;
+            *reinterpret_cast<float4 *>(o + (size_t)g * PART_W + PART_ACC + 4 * d4) = s4;
+            if (d4 == 0) {
+                o[(size_t)g * PART_W] = s_rm[g];
+                o[(size_t)g * PART_W + 1] = s_rl[g];
             }
-            *reinterpret_cast<float4 *>(o + PART_ACC + 4 * lane) = st[g].a;
         }
-        __syncthreads();
-        merge_states(rws, W, G, rst);
     }
-    cluster.sync();  // S2: slot counts and residual states are published
+    cluster.sync();  // S2: every slot's counts have been pushed
 
-    // ------------------------------- P4: row segments, rows-kernel plan, residual merge
-    for (int j = tid; j < Uc; j += NT) {  // every slot's rows and segments, from its owner
-        gpre[j] = cluster.map_shared_rank(pub_cnt, j % CS)[j / CS];
-        gseg[j] = cluster.map_shared_rank(pub_nseg, j % CS)[j / CS];
-    }
-    for (int g = k; g < G; g += CS) {  // the unit's residual: CS states merged per head
-        if (tid >= MOG_D) break;
-        float mx = -INFINITY;
-        for (int i = 0; i < CS; ++i) mx = fmaxf(mx, cluster.map_shared_rank(rst, i)[g * PART_W]);
-        float l = 0.f, acc = 0.f;
-        if (mx != -INFINITY)
-            for (int i = 0; i < CS; ++i) {
-                const float *r = cluster.map_shared_rank(rst, i) + g * PART_W;
-                const float mi = r[0];
-                if (mi == -INFINITY) continue;
-                const float sc = exp2f(mi - mx);
-                l += sc * r[1];
-                acc += sc * r[PART_ACC + tid];
-            }
-        float *o = dv.partials + (((size_t)u * PART_SLOTS + MAX_SPLITS) * G + g) * PART_W;
-        if (tid == 0) {
-            o[0] = mx;
-            o[1] = l;
-        }
-        o[PART_ACC + tid] = acc;
-    }
-    __syncthreads();
+    // ------------------------------------- P4: row segments and the rows-kernel plan
     if (warp == 0) {  // exclusive prefixes: rows after the anchors, segments from 0
         int rrun = n_anchor, srun = 0;
         for (int j0 = 0; j0 < Uc; j0 += 32) {
@@ -664,7 +712,6 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
         const int pe = T > 0 ? (int)(((int64_t)n_anchor * P + T - 1) / T) : P;
         for (int p = tid; p < min(pe, P); p += NT) plan[PLAN_START + p] = 0;
     }
-    cluster.sync();  // S3: the owners' counts, residual states and candidates have been read
 }
 
 constexpr int RW_SUPER = 256;                  // row positions per batch in the rows kernel
@@ -826,21 +873,22 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     merge_states(st, AT_WARPS, G, dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W);
 }
 
-// Kernel C: grid (G, units), 512 threads.  Merges the P row partials and the residual
-// partial of one query head (running max, rescaled sums) and normalises once.  Thread
+// Kernel C: grid (G, units), 512 threads.  Merges the P row partials and the CS residual
+// partials of one query head (running max, rescaled sums) and normalises once.  Thread
 // (part, j) sums partials part, part + 4, ... for dimension j; all loads are independent.
 constexpr int MG_THREADS = 4 * MOG_D;
-__global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int G,
-                                                          float *out) {
+__global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int CS,
+                                                          int G, float *out) {
     const int g = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
     const int j = tid % MOG_D, part = tid / MOG_D;
-    __shared__ float s_m[MAX_SPLITS + 1], s_l[MAX_SPLITS + 1], s_w[MAX_SPLITS + 1];
+    constexpr int NMAX = MAX_SPLITS + MAX_CS;
+    __shared__ float s_m[NMAX], s_l[NMAX], s_w[NMAX];
     __shared__ float s_acc[MG_THREADS / MOG_D][MOG_D];
     pdl_wait();
     pdl_trigger();
-    const int n = P + 1;  // row partials, then the residual
+    const int n = P + CS;  // row partials, then the residual partials
     auto src = [&](int i) {
-        return partials + (((size_t)u * PART_SLOTS + (i < P ? i : MAX_SPLITS)) * G + g) * PART_W;
+        return partials + (((size_t)u * PART_SLOTS + (i < P ? i : MAX_SPLITS + i - P)) * G + g) * PART_W;
     };
     if (tid < n) {
         s_m[tid] = __ldcg(src(tid));
@@ -855,7 +903,8 @@ __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials,
     for (int i = 0; i < n; ++i) l += s_w[i] * s_l[i];
     float v = 0.f;
 #pragma unroll 4
-    for (int i = part; i < n; i += MG_THREADS / MOG_D) v += s_w[i] * __ldcg(src(i) + PART_ACC + j);
+    for (int i = part; i < n; i += MG_THREADS / MOG_D)
+        if (s_w[i] != 0.f) v += s_w[i] * __ldcg(src(i) + PART_ACC + j);
     s_acc[part][j] = v;
     __syncthreads();
     if (part == 0) {
@@ -928,30 +977,32 @@ static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     const int sms = num_sms();
     for (int cs = 16; cs >= 1; --cs) {  // any size: e.g. 12-CTA clusters fit where 16 do not
         if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;  // keep clusters resident
-        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT));
-        if (m.total > MD_SMEM_MAX) continue;
-        if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(cs, dv.units);
-        cfg.blockDim = dim3(md_warps(GT) * 32);
-        cfg.dynamicSmemBytes = m.total;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = cs;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        int ncl = 0;
-        e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            continue;
-        }
-        if (ncl >= dv.units || cs == 1) {
-            *cs_out = cs;
-            *m_out = m;
-            return cudaSuccess;
+        for (int cap : {MD_SMEM_MAX, MD_SMEM_HALF}) {  // one CTA per SM, or two
+            MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT), cap);
+            if (m.total > cap) continue;
+            if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(cs, dv.units);
+            cfg.blockDim = dim3(md_warps(GT) * 32);
+            cfg.dynamicSmemBytes = m.total;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = cs;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int ncl = 0;
+            e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                continue;
+            }
+            if (ncl >= dv.units || cs == 1) {
+                *cs_out = cs;
+                *m_out = m;
+                return cudaSuccess;
+            }
         }
     }
     return cudaErrorInvalidConfiguration;
@@ -992,7 +1043,7 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
         return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_mog_merge, dim3(dv.G, dv.units), dim3(MG_THREADS), 0, s,
-                        (const float *)dv.partials, dv.P, dv.G, a.out)) != cudaSuccess)
+                        (const float *)dv.partials, dv.P, cs, dv.G, a.out)) != cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -1022,7 +1073,7 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
 }
 
 size_t slot_smem_bytes(int G, int c_max, int l_max, int tc) {  // the smallest layout (16-CTA clusters)
-    return (size_t)md_layout(G, tc, c_max, l_max, 16, md_warps(G <= 4 ? 4 : 16)).total;
+    return (size_t)md_layout(G, tc, c_max, l_max, 16, md_warps(G <= 4 ? 4 : 16), MD_SMEM_MAX).total;
 }
 
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,

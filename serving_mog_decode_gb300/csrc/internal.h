@@ -13,7 +13,8 @@ enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
 
 constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
 constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
-constexpr int PART_SLOTS = MAX_SPLITS + 1;  // partials per unit: rows CTAs, then the residual
+constexpr int MAX_CS = 16;          // CTAs per thread-block cluster of the selection kernel
+constexpr int PART_SLOTS = MAX_SPLITS + MAX_CS;  // partials per unit: rows CTAs, then selection CTAs
 // Rows-kernel plan per unit, written by the selection kernel: [0] segments NS, [1] rows T,
 // [2] anchors, [3] sink rows, [4] first recent position, [PLAN_START + p] the segment
 // holding the first row of rows-kernel CTA p (0 while that row is an anchor).
