@@ -163,6 +163,9 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_segrow = take(4 * U * P.nseg_max);
     P.o_segoff = take(4 * U * P.nseg_max);
     P.o_segmask = take(4 * U * P.nseg_max);
+    // residual items per unit: union pairs, then clusters; G exponents each
+    P.resx_stride = ((std::min<int64_t>(cm, G * std::max(P.tc, 1)) * lm + cm) * G + 3) & ~3LL;
+    P.o_resx = take(4 * U * P.resx_stride);
     P.total = o;
     return MOG_OK;
 }
@@ -193,6 +196,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.residual = P.residual;
     d.P = P.P;
     d.nseg_max = P.nseg_max;
+    d.resx_stride = P.resx_stride;
     d.nchunks = P.nchunks;
     d.sub_off_stride = P.sub_off_stride;
     d.tau = (float)(1.0 / sqrt((double)P.d));
@@ -226,6 +230,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     PTR(segrow, int);
     PTR(segoff, int);
     PTR(segmask, uint32_t);
+    PTR(resx, float);
 #undef PTR
     return d;
 }

@@ -95,59 +95,22 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
 }
 
-// Running (max, sum, acc) of a softmax-weighted sum over 4 output dimensions, log2 domain.
-struct OnlineAcc {
-    float m, l;
-    float4 a;
-    __device__ __forceinline__ void init() {
-        m = -INFINITY;
-        l = 0.f;
-        a = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __device__ __forceinline__ void absorb(float ex, const float *v4) {
-        if (ex > m) {
-            const float sc = exp2f(m - ex);
-            l *= sc;
-            a.x *= sc;
-            a.y *= sc;
-            a.z *= sc;
-            a.w *= sc;
-            m = ex;
-        }
-        const float wgt = exp2f(ex - m);
-        const float4 v = *reinterpret_cast<const float4 *>(v4);
-        l += wgt;
-        a.x += wgt * v.x;
-        a.y += wgt * v.y;
-        a.z += wgt * v.z;
-        a.w += wgt * v.w;
-    }
-};
-
-constexpr int RCH = 64;  // slice clusters staged per residual pass
-constexpr int PCH = 64;  // (slot, subcluster) pairs staged per residual pass
 // dynamic shared memory of the decode kernel: the 227 KB block limit less its static arrays
 constexpr int MD_SMEM_MAX = 226 * 1024;
-// ... and the budget that lets two CTAs share an SM (228 KB less reserved and static memory)
-constexpr int MD_SMEM_HALF = 110 * 1024;
 
 __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
 
 // Shared-memory layout of the selection kernel (byte offsets).
 struct MdLay {
-    int CS, SL, SLp, KC, NPOOL, NSLOT, SPC, warps, PCHd, RCHd;  // KC: candidates per slice and
-                                                                  // head; NPOOL: CS*KC padded
+    int CS, SL, SLp, KC, NPOOL, NSLOT, SPC, warps;  // KC: candidates per slice and head;
+                                                    // NPOOL: CS*KC padded
     int cand_k, allc_k, selc, gpre, gseg;  // allc_k, selc, gpre, gseg receive other CTAs' pushes
     int w, ckey, crs, cnn, slm, bm, ucl;
-    int sres, ssl, snn, sso, spref, smask, shm, area;
+    int sres, ssl, snn, sso, spref, smask, shm;
     int total;
 };
 
-// area: the staged value means of P3, then (aliased) the residual's group sums.  The value
-// means of all of a CTA's (slot, subcluster) pairs and slice clusters are staged at once
-// when that fits within `cap` bytes, else in passes sized to fit.
-__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, int CS, int warps,
-                                           int cap) {
+__host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int CS, int warps) {
     MdLay m;
     int o = 0;
     auto take = [&](int bytes, int align) {
@@ -184,23 +147,6 @@ __host__ __device__ inline MdLay md_layout(int G, int tc, int c_max, int l_max, 
     m.spref = take(4 * m.SPC * (MOG_MAX_L + 1), 16);
     m.smask = take(4 * m.SPC * MOG_MAX_L, 16);
     m.shm = take(4 * m.SPC, 16);
-    const int base = (o + 127) & ~127;
-    const int red = warps * 32 * 16;  // group sums
-    int pch = m.SPC * l_max, rch = m.SL;
-    const int fit = (cap - base) / (MOG_D * 4);  // value means that fit
-    if (pch + rch > fit) {  // passes: shares in proportion, at least 8 each
-        const int r8 = rch < 8 ? rch : 8, p8 = pch < 8 ? pch : 8;
-        int rc = fit > 0 ? (int)((long long)fit * rch / (pch + rch)) : 0;
-        rc = rc < r8 ? r8 : rc;
-        int pc = fit - rc;
-        pc = pc < p8 ? p8 : pc;
-        rch = rch < rc ? rch : rc;
-        pch = pch < pc ? pch : pc;
-    }
-    m.PCHd = pch > 0 ? pch : 1;
-    m.RCHd = rch > 0 ? rch : 1;
-    const int vm = (m.PCHd + m.RCHd) * MOG_D * 4;
-    m.area = take(vm > red ? vm : red, 128);
     m.total = (o + 15) & ~15;
     return m;
 }
@@ -248,8 +194,8 @@ __device__ __forceinline__ int key_rank(const unsigned long long *keys, int n, u
 //      top-tc list; each CTA then forms the union over the heads (ascending index);
 //  P3  CTA k takes union slots k, k+CS, ...: subcluster scores, the top-ts subclusters of
 //      every head that chose the slot's cluster, the slot's row and segment counts
-//      (pushed), and the residual of the unchosen subclusters of those heads and of its
-//      slice clusters no head chose, written as one unnormalised partial;
+//      (pushed), and the exponents of the residual terms: the unchosen subclusters of those
+//      heads and its slice clusters no head chose;
 //  P4  the unit's row segments (one per chosen subcluster, in slot order) and the first
 //      segment of every rows-kernel CTA.
 template <int GT>
@@ -282,9 +228,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     int *spref = reinterpret_cast<int *>(sm + m.spref);
     uint32_t *smask = reinterpret_cast<uint32_t *>(sm + m.smask);
     uint32_t *shm = reinterpret_cast<uint32_t *>(sm + m.shm);  // heads that chose slot s
-    uint8_t *area = sm + m.area;
     __shared__ int s_wsum[W], s_uc;
-    __shared__ float s_rm[MOG_MAX_G], s_rl[MOG_MAX_G];
 
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int b = ui[UI_B], C = ui[UI_C], L = ui[UI_L];
@@ -418,32 +362,13 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     // ----------------------------------------- P3: this CTA's union slots, residual
     const int nmy = Uc > k ? (Uc - k + CS - 1) / CS : 0;  // slots k, k+CS, ...
     const int npair = nmy * L;                              // (slot, subcluster) pairs
-    float *vst = reinterpret_cast<float *>(area);           // [PCHd][d] subcluster means
-    float *vcl = vst + (size_t)m.PCHd * MOG_D;              // [RCHd][d] slice cluster means
-    // offsets and sizes of the slots' subclusters, and the first value means, in flight
-    // while the subcluster scores are computed
+    // offsets and sizes of the slots' subclusters, in flight while their scores are computed
     for (int e = tid; e < nmy * (L + 1); e += NT) {
         const int s = e / (L + 1), i = e % (L + 1);
         const size_t c = (size_t)ucl[k + s * CS];
         cp_async4(smem_u32(sso + s * (MOG_MAX_L + 1) + i), dv.sub_off + (size_t)u * dv.sub_off_stride + c * L + i);
         if (i < L) cp_async4(smem_u32(snn + s * MOG_MAX_L + i), dv.sub_n + usg + c * L + i);
     }
-    auto stage_pairs = [&](int p0) {  // value means of pairs p0 .. p0 + PCHd
-        const int cnt = min(m.PCHd, npair - p0);
-        for (int e = tid; e < cnt * 32; e += NT) {
-            const int pr = p0 + e / 32, s = pr / L, l = pr % L;
-            cp_async16(smem_u32(vst + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
-                       dv.sub_vbar + (usg + (size_t)ucl[k + s * CS] * L + l) * MOG_D + 4 * (e % 32), 16);
-        }
-    };
-    auto stage_slice = [&](int k0) {
-        const int cnt = min(m.RCHd, ns - k0);
-        for (int e = tid; e < cnt * 32; e += NT)
-            cp_async16(smem_u32(vcl + (size_t)(e / 32) * MOG_D + 4 * (e % 32)),
-                       dv.cl_vbar + (ug + c0 + k0 + e / 32) * MOG_D + 4 * (e % 32), 16);
-    };
-    if (resid && npair > 0) stage_pairs(0);
-    if (resid && ns > 0) stage_slice(0);
     cp_async_commit();
     for (int base = 0; base < npair; base += NT / 4) {  // subcluster scores, 4 lanes a pair
         const int pr = base + (tid >> 2);
@@ -521,129 +446,23 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             cluster.map_shared_rank(gseg, dst)[j] = nseg;
         }
     }
-    // Gaussian residual: for the heads that chose slot s but not its subcluster l, and for
-    // the heads that did not choose slice cluster c, exp(score) * value mean.  Pair weights
-    // go to wpr[p][g] (p = s*L + l, over the subcluster selection scores, no longer needed),
-    // slice weights replace the exponents in crs; per head the maximum M and the weight sum
-    // l; the weighted sum of the value means per (head, 4 dimensions), items split over
-    // ngrp thread groups; one partial (M, l, acc) per CTA.
+    // Gaussian residual terms, attended by the rows kernel: for the heads that chose slot s
+    // but not its subcluster l, and for the heads that did not choose slice cluster c, the
+    // exponent (log2) of the term; -inf where the head does not take it.  Items: the union
+    // pairs (slot j, subcluster l) at j*L + l, then the clusters at Uc*L + c.
+    __syncthreads();
     {
-        float *wpr = ssl;
-        __syncthreads();
-        for (int e = tid; e < npair * G; e += NT) {  // exponents (log2), -inf when not needed
+        float *rx = dv.resx + (size_t)u * dv.resx_stride;
+        for (int e = tid; e < npair * G; e += NT) {
             const int p = e / G, g = e - p * G, s = p / L, l = p - s * L;
             const bool need = resid && snn[s * MOG_MAX_L + l] > 0 &&
                               (((shm[s] & ~smask[s * MOG_MAX_L + l]) >> g) & 1u);
-            wpr[e] = need ? sres[(s * G + g) * MOG_MAX_L + l] * LOG2E : -INFINITY;
+            rx[((size_t)(k + s * CS) * L + l) * G + g] = need ? sres[(s * G + g) * MOG_MAX_L + l] * LOG2E : -INFINITY;
         }
         for (int e = tid; e < ns * G; e += NT) {
             const int cl = e / G, g = e - cl * G;
-            float &x = crs[g * m.SL + cl];
             const bool need = resid && cnn[cl] > 0 && !((slm[cl] >> g) & 1u);
-            x = need ? x * LOG2E : -INFINITY;
-        }
-        __syncthreads();
-        for (int g = warp; g < G; g += W) {  // per-head maximum
-            float mx = -INFINITY;
-            for (int p = lane; p < npair; p += 32) mx = fmaxf(mx, wpr[p * G + g]);
-            for (int cl = lane; cl < ns; cl += 32) mx = fmaxf(mx, crs[g * m.SL + cl]);
-            mx = warp_max(mx);
-            if (lane == 0) s_rm[g] = mx;
-        }
-        __syncthreads();
-        for (int e = tid; e < npair * G; e += NT) {  // weights
-            const float x = wpr[e];
-            wpr[e] = x == -INFINITY ? 0.f : exp2f(x - s_rm[e % G]);
-        }
-        for (int e = tid; e < ns * G; e += NT) {
-            const int g = e / ns;
-            float &x = crs[g * m.SL + e - g * ns];
-            x = x == -INFINITY ? 0.f : exp2f(x - s_rm[g]);
-        }
-        __syncthreads();
-        for (int g = warp; g < G; g += W) {  // per-head weight sums
-            float sw = 0.f;
-            for (int p = lane; p < npair; p += 32) sw += wpr[p * G + g];
-            for (int cl = lane; cl < ns; cl += 32) sw += crs[g * m.SL + cl];
-            sw = warp_sum(sw);
-            if (lane == 0) s_rl[g] = sw;
-        }
-        constexpr int MAXU = (GT * 32 + NT - 1) / NT;  // (head, 4 dims) units per thread
-        const int U4 = G * 32;
-        const int ngrp = max(1, NT / U4);
-        const int grp = ngrp > 1 ? tid / U4 : 0;
-        float4 acc4[MAXU];
-#pragma unroll
-        for (int uu = 0; uu < MAXU; ++uu) acc4[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
-        auto accumulate = [&](const float *vb, int cnt, auto weight) {
-#pragma unroll
-            for (int uu = 0; uu < MAXU; ++uu) {
-                const int unit = ngrp > 1 ? tid % U4 : tid + uu * NT;
-                if ((ngrp > 1 && (uu > 0 || grp >= ngrp)) || unit >= U4) continue;
-                const int g = unit >> 5, d4 = unit & 31;
-                float4 s4 = acc4[uu];
-                for (int i = grp; i < cnt; i += ngrp) {
-                    const float wt = weight(i, g);
-                    if (wt == 0.f) continue;
-                    const float4 v = *reinterpret_cast<const float4 *>(vb + (size_t)i * MOG_D + 4 * d4);
-                    s4.x += wt * v.x;
-                    s4.y += wt * v.y;
-                    s4.z += wt * v.z;
-                    s4.w += wt * v.w;
-                }
-                acc4[uu] = s4;
-            }
-        };
-        if (resid) {
-            for (int p0 = 0; p0 < npair; p0 += m.PCHd) {
-                if (p0 > 0) {  // further pairs (many slots per CTA)
-                    __syncthreads();
-                    stage_pairs(p0);
-                    cp_async_commit();
-                    cp_async_wait<0>();
-                    __syncthreads();
-                }
-                accumulate(vst, min(m.PCHd, npair - p0), [&](int i, int g) { return wpr[(p0 + i) * G + g]; });
-            }
-            for (int k0 = 0; k0 < ns; k0 += m.RCHd) {
-                if (k0 > 0) {
-                    __syncthreads();
-                    stage_slice(k0);
-                    cp_async_commit();
-                    cp_async_wait<0>();
-                    __syncthreads();
-                }
-                accumulate(vcl, min(m.RCHd, ns - k0), [&](int i, int g) { return crs[g * m.SL + k0 + i]; });
-            }
-        }
-        __syncthreads();  // the value means are read: the group sums take their place
-        float4 *red = reinterpret_cast<float4 *>(area);  // [ngrp][U4]
-        if (ngrp > 1) {
-            if (grp < ngrp) red[grp * U4 + tid % U4] = acc4[0];
-            __syncthreads();
-        }
-        float *o = dv.partials + ((size_t)u * PART_SLOTS + MAX_SPLITS + k) * G * PART_W;
-#pragma unroll
-        for (int uu = 0; uu < MAXU; ++uu) {
-            const int unit = tid + uu * NT;
-            if (unit >= U4) continue;
-            float4 s4 = acc4[uu];
-            if (ngrp > 1) {
-                s4 = red[unit];
-                for (int q = 1; q < ngrp; ++q) {
-                    const float4 t4 = red[q * U4 + unit];
-                    s4.x += t4.x;
-                    s4.y += t4.y;
-                    s4.z += t4.z;
-                    s4.w += t4.w;
-                }
-            }
-            const int g = unit >> 5, d4 = unit & 31;
-            *reinterpret_cast<float4 *>(o + (size_t)g * PART_W + PART_ACC + 4 * d4) = s4;
-            if (d4 == 0) {
-                o[(size_t)g * PART_W] = s_rm[g];
-                o[(size_t)g * PART_W + 1] = s_rl[g];
-            }
+            rx[((size_t)Uc * L + c0 + cl) * G + g] = need ? crs[g * m.SL + cl] * LOG2E : -INFINITY;
         }
     }
     cluster.sync();  // S2: every slot's counts have been pushed
@@ -707,7 +526,11 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
             plan[2] = n_anchor;
             plan[3] = s_cnt;
             plan[4] = rlo;
+            plan[5] = Uc;
+            plan[6] = L;
+            plan[7] = C;
         }
+        for (int j = tid; j < Uc; j += NT) plan[PLAN_UCL + j] = ucl[j];
         // CTAs that start among the anchors (or in an empty list) start at segment 0
         const int pe = T > 0 ? (int)(((int64_t)n_anchor * P + T - 1) / T) : P;
         for (int p = tid; p < min(pe, P); p += NT) plan[PLAN_START + p] = 0;
@@ -725,7 +548,8 @@ static_assert(RW_TPB >= AT_STAGES - 1, "the first batch must cover the pipeline'
 // through the 64-row tile engine.  A window of segments sits in shared memory; a row's
 // position is read from the partition (perm) at its segment's offset.  Positions are
 // fetched into registers two batches ahead and moved to shared memory when the pipeline
-// reaches the batch, so no tile copy waits on a position load.  One partial per CTA.
+// reaches the batch, so no tile copy waits on a position load.  After the rows, the CTA
+// adds its share of the Gaussian residual terms.  One unnormalised partial per CTA.
 template <int GT>
 __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     extern __shared__ __align__(128) uint8_t tile[];
@@ -867,43 +691,118 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     }
     cp_async_wait<0>();
     __syncthreads();
-    float *st = reinterpret_cast<float *>(tile);
+    // The Gaussian residual: items [ia, ib) of the unit's list (union pairs, then clusters),
+    // exponents from the selection kernel, value means staged in passes into the tile
+    // memory after the states.  Thread (grp, g, d4) keeps a running (max, sum, acc) of
+    // items grp, grp + ngrp, ... for head g, dims 4*d4 .. 4*d4+3.
+    constexpr int MAXU = (GT * 32 + AT_THREADS - 1) / AT_THREADS;
+    const int U4 = G * 32, ngrp = max(1, AT_THREADS / U4), grp = ngrp > 1 ? tid / U4 : 0;
+    float *st = reinterpret_cast<float *>(tile);  // [AT_WARPS + ngrp][G][PART_W]
+    const int st_floats = (AT_WARPS + ngrp) * G * PART_W;
+    float rM[MAXU], rL[MAXU];
+    float4 rA[MAXU];
+#pragma unroll
+    for (int uu = 0; uu < MAXU; ++uu) {
+        rM[uu] = -INFINITY;
+        rL[uu] = 0.f;
+        rA[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int Uc = s_plan[5], L = s_plan[6], C = s_plan[7];
+    const int npi = Uc * L, I = npi + C;
+    const int ia = (int)((int64_t)I * p / P), ib = (int)((int64_t)I * (p + 1) / P);
+    if (dv.residual && ia < ib) {
+        const int rch = min(256, (AT_SMEM / 4 - st_floats) / (MOG_D + G));
+        float *rv = st + st_floats;          // [rch][d] value means
+        float *re = rv + (size_t)rch * MOG_D;  // [rch][G] exponents
+        const float *rx = dv.resx + (size_t)u * dv.resx_stride;
+        const size_t ug = (size_t)u * dv.c_max, usg = ug * dv.l_max;
+        for (int c0 = ia; c0 < ib; c0 += rch) {
+            const int cnt = min(rch, ib - c0);
+            for (int e = tid; e < cnt * 32; e += AT_THREADS) {
+                const int it = c0 + e / 32, q = e % 32;
+                const float *src = it < npi ? dv.sub_vbar + (usg + (size_t)s_plan[PLAN_UCL + it / L] * L + it % L) * MOG_D
+                                            : dv.cl_vbar + (ug + (it - npi)) * MOG_D;
+                cp_async16(smem_u32(rv + (size_t)(e / 32) * MOG_D + 4 * q), src + 4 * q, 16);
+            }
+            for (int e = tid; e < cnt * G; e += AT_THREADS) cp_async4(smem_u32(re + e), rx + (size_t)c0 * G + e);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncthreads();
+#pragma unroll
+            for (int uu = 0; uu < MAXU; ++uu) {
+                const int unit = ngrp > 1 ? tid % U4 : tid + uu * AT_THREADS;
+                if ((ngrp > 1 && (uu > 0 || grp >= ngrp)) || unit >= U4) continue;
+                const int g = unit >> 5, d4 = unit & 31;
+                float mp = rM[uu];
+                for (int i = grp; i < cnt; i += ngrp) mp = fmaxf(mp, re[i * G + g]);
+                if (mp > rM[uu]) {  // rescale to the new maximum
+                    const float sc = rM[uu] == -INFINITY ? 0.f : exp2f(rM[uu] - mp);
+                    rL[uu] *= sc;
+                    rA[uu].x *= sc;
+                    rA[uu].y *= sc;
+                    rA[uu].z *= sc;
+                    rA[uu].w *= sc;
+                    rM[uu] = mp;
+                }
+                for (int i = grp; i < cnt; i += ngrp) {
+                    const float x = re[i * G + g];
+                    if (x == -INFINITY) continue;
+                    const float wt = exp2f(x - rM[uu]);
+                    const float4 v = *reinterpret_cast<const float4 *>(rv + (size_t)i * MOG_D + 4 * d4);
+                    rL[uu] += wt;
+                    rA[uu].x += wt * v.x;
+                    rA[uu].y += wt * v.y;
+                    rA[uu].z += wt * v.z;
+                    rA[uu].w += wt * v.w;
+                }
+            }
+            __syncthreads();
+        }
+    }
     warp_state_out(acc, st, G);
+#pragma unroll
+    for (int uu = 0; uu < MAXU; ++uu) {  // the residual groups' states after the warps'
+        const int unit = ngrp > 1 ? tid % U4 : tid + uu * AT_THREADS;
+        if ((ngrp > 1 && (uu > 0 || grp >= ngrp)) || unit >= U4) continue;
+        const int g = unit >> 5, d4 = unit & 31;
+        float *o = st + ((size_t)(AT_WARPS + grp) * G + g) * PART_W;
+        if (d4 == 0) {
+            o[0] = rM[uu];
+            o[1] = rL[uu];
+        }
+        *reinterpret_cast<float4 *>(o + PART_ACC + 4 * d4) = rA[uu];
+    }
     __syncthreads();
-    merge_states(st, AT_WARPS, G, dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W);
+    merge_states(st, AT_WARPS + ngrp, G, dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W);
 }
 
-// Kernel C: grid (G, units), 512 threads.  Merges the P row partials and the CS residual
-// partials of one query head (running max, rescaled sums) and normalises once.  Thread
-// (part, j) sums partials part, part + 4, ... for dimension j; all loads are independent.
+// Kernel C: grid (G, units), 512 threads.  Merges the P partials of one query head
+// (running max, rescaled sums) and normalises once.  Thread (part, j) sums partials part,
+// part + 4, ... for dimension j; all loads are independent.
 constexpr int MG_THREADS = 4 * MOG_D;
-__global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int CS,
-                                                          int G, float *out) {
+__global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int G,
+                                                          float *out) {
     const int g = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
     const int j = tid % MOG_D, part = tid / MOG_D;
-    constexpr int NMAX = MAX_SPLITS + MAX_CS;
-    __shared__ float s_m[NMAX], s_l[NMAX], s_w[NMAX];
+    __shared__ float s_m[MAX_SPLITS], s_l[MAX_SPLITS], s_w[MAX_SPLITS];
     __shared__ float s_acc[MG_THREADS / MOG_D][MOG_D];
     pdl_wait();
     pdl_trigger();
-    const int n = P + CS;  // row partials, then the residual partials
-    auto src = [&](int i) {
-        return partials + (((size_t)u * PART_SLOTS + (i < P ? i : MAX_SPLITS + i - P)) * G + g) * PART_W;
-    };
-    if (tid < n) {
+    auto src = [&](int i) { return partials + (((size_t)u * PART_SLOTS + i) * G + g) * PART_W; };
+    if (tid < P) {
         s_m[tid] = __ldcg(src(tid));
         s_l[tid] = __ldcg(src(tid) + 1);
     }
     __syncthreads();
     float mx = -INFINITY;
-    for (int i = 0; i < n; ++i) mx = fmaxf(mx, s_m[i]);
-    if (tid < n) s_w[tid] = (s_m[tid] == -INFINITY) ? 0.f : exp2f(s_m[tid] - mx);
+    for (int i = 0; i < P; ++i) mx = fmaxf(mx, s_m[i]);
+    if (tid < P) s_w[tid] = (s_m[tid] == -INFINITY) ? 0.f : exp2f(s_m[tid] - mx);
     __syncthreads();
     float l = 0.f;
-    for (int i = 0; i < n; ++i) l += s_w[i] * s_l[i];
+    for (int i = 0; i < P; ++i) l += s_w[i] * s_l[i];
     float v = 0.f;
 #pragma unroll 4
-    for (int i = part; i < n; i += MG_THREADS / MOG_D)
+    for (int i = part; i < P; i += MG_THREADS / MOG_D)
         if (s_w[i] != 0.f) v += s_w[i] * __ldcg(src(i) + PART_ACC + j);
     s_acc[part][j] = v;
     __syncthreads();
@@ -977,32 +876,30 @@ static cudaError_t pick_shape(const Dev &dv, int *cs_out, MdLay *m_out) {
     const int sms = num_sms();
     for (int cs = 16; cs >= 1; --cs) {  // any size: e.g. 12-CTA clusters fit where 16 do not
         if (cs > 1 && (int64_t)cs * dv.units > 2LL * sms) continue;  // keep clusters resident
-        for (int cap : {MD_SMEM_MAX, MD_SMEM_HALF}) {  // one CTA per SM, or two
-            MdLay m = md_layout(dv.G, dv.tc, dv.c_max, dv.l_max, cs, md_warps(GT), cap);
-            if (m.total > cap) continue;
-            if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(cs, dv.units);
-            cfg.blockDim = dim3(md_warps(GT) * 32);
-            cfg.dynamicSmemBytes = m.total;
-            cudaLaunchAttribute at[1];
-            at[0].id = cudaLaunchAttributeClusterDimension;
-            at[0].val.clusterDim.x = cs;
-            at[0].val.clusterDim.y = 1;
-            at[0].val.clusterDim.z = 1;
-            cfg.attrs = at;
-            cfg.numAttrs = 1;
-            int ncl = 0;
-            e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
-            if (e != cudaSuccess) {
-                cudaGetLastError();
-                continue;
-            }
-            if (ncl >= dv.units || cs == 1) {
-                *cs_out = cs;
-                *m_out = m;
-                return cudaSuccess;
-            }
+        MdLay m = md_layout(dv.G, dv.tc, dv.c_max, cs, md_warps(GT));
+        if (m.total > MD_SMEM_MAX) continue;
+        if ((e = ensure_smem(fn, (size_t)m.total)) != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs, dv.units);
+        cfg.blockDim = dim3(md_warps(GT) * 32);
+        cfg.dynamicSmemBytes = m.total;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = cs;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int ncl = 0;
+        e = cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (ncl >= dv.units || cs == 1) {
+            *cs_out = cs;
+            *m_out = m;
+            return cudaSuccess;
         }
     }
     return cudaErrorInvalidConfiguration;
@@ -1043,7 +940,7 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
         return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_mog_merge, dim3(dv.G, dv.units), dim3(MG_THREADS), 0, s,
-                        (const float *)dv.partials, dv.P, cs, dv.G, a.out)) != cudaSuccess)
+                        (const float *)dv.partials, dv.P, dv.G, a.out)) != cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -1073,7 +970,7 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
 }
 
 size_t slot_smem_bytes(int G, int c_max, int l_max, int tc) {  // the smallest layout (16-CTA clusters)
-    return (size_t)md_layout(G, tc, c_max, l_max, 16, md_warps(G <= 4 ? 4 : 16), MD_SMEM_MAX).total;
+    return (size_t)md_layout(G, tc, c_max, 16, md_warps(G <= 4 ? 4 : 16)).total;
 }
 
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,

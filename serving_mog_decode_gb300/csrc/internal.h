@@ -13,13 +13,15 @@ enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
 
 constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
 constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
-constexpr int MAX_CS = 16;          // CTAs per thread-block cluster of the selection kernel
-constexpr int PART_SLOTS = MAX_SPLITS + MAX_CS;  // partials per unit: rows CTAs, then selection CTAs
+constexpr int PART_SLOTS = MAX_SPLITS;  // partials per unit: one per rows-kernel CTA
 // Rows-kernel plan per unit, written by the selection kernel: [0] segments NS, [1] rows T,
-// [2] anchors, [3] sink rows, [4] first recent position, [PLAN_START + p] the segment
-// holding the first row of rows-kernel CTA p (0 while that row is an anchor).
+// [2] anchors, [3] sink rows, [4] first recent position, [5] union size Uc, [6] subclusters
+// per cluster L, [7] clusters C, [PLAN_START + p] the segment holding the first row of
+// rows-kernel CTA p (0 while that row is an anchor), [PLAN_UCL + j] the cluster of union
+// slot j.
 constexpr int PLAN_START = 8;
-constexpr int PLAN_W = PLAN_START + MAX_SPLITS;  // ints, whole 16-byte chunks
+constexpr int PLAN_UCL = PLAN_START + MAX_SPLITS;
+constexpr int PLAN_W = PLAN_UCL + MOG_MAX_UNION;  // ints, whole 16-byte chunks
 constexpr int MAX_C = 4096;        // clusters per unit supported
 
 // Typed view of an arena, passed by value to every kernel.
@@ -45,6 +47,8 @@ struct Dev {
     int *plan;        // [units][PLAN_W]
     int *segrow, *segoff;  // [units][nseg_max] first row of a segment, its offset in perm
     uint32_t *segmask;     // [units][nseg_max] heads that attend the segment
+    float *resx;           // [units][resx_stride]: residual exponents [item][G]
+    int64_t resx_stride;
 
     __host__ __device__ const uint16_t *krow(int b, int h, int64_t pos) const {
         return K + b * sb + h * sh + pos * sn;
@@ -63,7 +67,7 @@ struct Plan {
         o_sub_vbar, o_l1_assign, o_status, o_l1_steps;
     int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
         o_sub_assign;
-    int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask;
+    int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask, o_resx, resx_stride;
     int64_t total;
 };
 
