@@ -144,6 +144,8 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_sub_n = take(4 * U * cm * lm);
     P.o_sub_ms = take(4 * U * cm * lm * 2 * MOG_D);
     P.o_sub_vbar = take(4 * U * cm * lm * MOG_D);
+    P.o_cl_vhl = take(2 * U * cm * 2 * MOG_D);
+    P.o_sub_vhl = take(2 * U * cm * lm * 2 * MOG_D);
     P.o_l1_assign = take(4 * U * nc);
     P.o_l1_steps = take(4 * U);
     P.o_cent = take(4 * U * cm * MOG_D);
@@ -163,8 +165,8 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_segrow = take(4 * U * P.nseg_max);
     P.o_segoff = take(4 * U * P.nseg_max);
     P.o_segmask = take(4 * U * P.nseg_max);
-    // residual items per unit: union pairs, then clusters; G exponents each
-    P.resx_stride = ((std::min<int64_t>(cm, G * std::max(P.tc, 1)) * lm + cm) * G + 3) & ~3LL;
+    // residual items per unit: union pairs, then clusters; G exponents each (16-byte rows)
+    P.resx_stride = (std::min<int64_t>(cm, G * std::max(P.tc, 1)) * lm + cm) * ((G + 3) & ~3LL);
     P.o_resx = take(4 * U * P.resx_stride);
     P.total = o;
     return MOG_OK;
@@ -214,6 +216,8 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     PTR(cl_vbar, float);
     PTR(sub_ms, float);
     PTR(sub_vbar, float);
+    PTR(cl_vhl, uint16_t);
+    PTR(sub_vhl, uint16_t);
     PTR(cent, float);
     PTR(permA, int);
     PTR(changed, int);

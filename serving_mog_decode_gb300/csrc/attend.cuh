@@ -88,16 +88,21 @@ __device__ __forceinline__ void issue_tile(uint8_t *stage, int nrows, const uint
 // Consume 16 rows (keys) rbase..rbase+15 of a shared-memory K/V block into this warp's
 // accumulator.  sk, sv: shared addresses of the swizzled K and V rows; smask: per-row head
 // masks (bit g set: head g attends to the row).
+// GIVEN: the block holds precomputed terms instead of keys: row pairs (2i, 2i+1) are the
+// bf16 high and low parts of a value vector, and `given` holds their log2-domain logits
+// E[i][16] (16 heads per item), used as they are.
+template <bool GIVEN = false>
 __device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa)[8][4],
                                                uint32_t sk, uint32_t sv, const uint32_t *smask,
-                                               int rbase, float scale2) {
+                                               int rbase, float scale2,
+                                               const float *given = nullptr) {
     const int lane = threadIdx.x & 31;
     float s[2][4];
 #pragma unroll
     for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[t][e] = 0.f;
-    {
+    if (!GIVEN) {
         const int mat = lane >> 3, r8 = lane & 7;
         const int key = rbase + (mat >> 1) * 8 + r8;
 #pragma unroll
@@ -116,8 +121,13 @@ __device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa
         for (int e = 0; e < 2; ++e) {
             const int key = rbase + t * 8 + (lane & 3) * 2 + e;
             const uint32_t mk = smask[key];
-            s[t][e] = ((mk >> h0) & 1u) ? s[t][e] * scale2 : -INFINITY;
-            s[t][e + 2] = ((mk >> h1) & 1u) ? s[t][e + 2] * scale2 : -INFINITY;
+            if (GIVEN) {
+                s[t][e] = ((mk >> h0) & 1u) ? given[(key >> 1) * MOG_MAX_G + h0] : -INFINITY;
+                s[t][e + 2] = ((mk >> h1) & 1u) ? given[(key >> 1) * MOG_MAX_G + h1] : -INFINITY;
+            } else {
+                s[t][e] = ((mk >> h0) & 1u) ? s[t][e] * scale2 : -INFINITY;
+                s[t][e + 2] = ((mk >> h1) & 1u) ? s[t][e + 2] * scale2 : -INFINITY;
+            }
             mx0 = fmaxf(mx0, s[t][e]);
             mx1 = fmaxf(mx1, s[t][e + 2]);
         }
@@ -138,8 +148,10 @@ __device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa
         for (int e = 0; e < 2; ++e) {
             p[t][e] = mn0 == -INFINITY ? 0.f : exp2f(s[t][e] - mn0);
             p[t][e + 2] = mn1 == -INFINITY ? 0.f : exp2f(s[t][e + 2] - mn1);
-            ps0 += p[t][e];
-            ps1 += p[t][e + 2];
+            if (!GIVEN || e == 0) {  // a given term's low-part row adds no weight of its own
+                ps0 += p[t][e];
+                ps1 += p[t][e + 2];
+            }
         }
     acc.l[0] = acc.l[0] * al0 + ps0;
     acc.l[1] = acc.l[1] * al1 + ps1;
@@ -180,37 +192,14 @@ __device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa
 }
 
 // Consume one 64-row tile (already in shared memory): warp w takes rows 16w..16w+15.
+// GIVEN: the tile holds precomputed terms whose logits sit at the start of the stage.
+template <bool GIVEN = false>
 __device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[8][4],
                                              const uint8_t *stage, float scale2) {
     const uint32_t sk = smem_u32(stage);
-    compute_rows16(acc, qa, sk, sk + AT_TILE_BYTES,
-                   reinterpret_cast<const uint32_t *>(stage + 2 * AT_TILE_BYTES),
-                   (threadIdx.x >> 5) * 16, scale2);
-}
-
-// ---- per-warp pipeline: a warp streams its own 16-row blocks, no block-wide barrier ----
-constexpr int WB_ROWS = 16;
-constexpr int WB_KV = WB_ROWS * AT_ROW_BYTES;            // 4 KB of K (or V)
-constexpr int WB_BYTES = 2 * WB_KV + WB_ROWS * 4;         // K, V, masks: 8256 bytes
-
-// Copy a warp's block of nb <= 16 rows into buf: lane r < 16 holds row r's position `pos`
-// and head mask `mk`; rows >= nb are zero-filled with mask 0.
-__device__ __forceinline__ void warp_issue_block(uint8_t *buf, int nb, int pos, uint32_t mk,
-                                                 const uint16_t *kbase, const uint16_t *vbase,
-                                                 int64_t sn) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t sk = smem_u32(buf), sv = sk + WB_KV;
-    const int ch = lane & 15;
-#pragma unroll
-    for (int i = 0; i < WB_ROWS / 2; ++i) {
-        const int r = (lane >> 4) + 2 * i;
-        const int pr = __shfl_sync(0xffffffffu, pos, r);
-        const bool ok = r < nb;
-        const int64_t off = ok ? (int64_t)pr * sn + ch * 8 : 0;
-        cp_async16(sk + swz(r, ch), kbase + off, ok ? 16 : 0);
-        cp_async16(sv + swz(r, ch), vbase + off, ok ? 16 : 0);
-    }
-    if (lane < WB_ROWS) reinterpret_cast<uint32_t *>(buf + 2 * WB_KV)[lane] = lane < nb ? mk : 0u;
+    compute_rows16<GIVEN>(acc, qa, sk, sk + AT_TILE_BYTES,
+                          reinterpret_cast<const uint32_t *>(stage + 2 * AT_TILE_BYTES),
+                          (threadIdx.x >> 5) * 16, scale2, reinterpret_cast<const float *>(stage));
 }
 
 // Partial result layout: per head, [0] = m (log2 domain), [1] = l, [2], [3] unused,

@@ -449,20 +449,22 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, 
     // Gaussian residual terms, attended by the rows kernel: for the heads that chose slot s
     // but not its subcluster l, and for the heads that did not choose slice cluster c, the
     // exponent (log2) of the term; -inf where the head does not take it.  Items: the union
-    // pairs (slot j, subcluster l) at j*L + l, then the clusters at Uc*L + c.
+    // pairs (slot j, subcluster l) at j*L + l, then the clusters at Uc*L + c; rows of G
+    // exponents padded to a multiple of 4.
     __syncthreads();
     {
         float *rx = dv.resx + (size_t)u * dv.resx_stride;
-        for (int e = tid; e < npair * G; e += NT) {
-            const int p = e / G, g = e - p * G, s = p / L, l = p - s * L;
-            const bool need = resid && snn[s * MOG_MAX_L + l] > 0 &&
+        const int GP = (G + 3) & ~3;  // 16-byte rows
+        for (int e = tid; e < npair * GP; e += NT) {
+            const int p = e / GP, g = e - p * GP, s = p / L, l = p - s * L;
+            const bool need = resid && g < G && snn[s * MOG_MAX_L + l] > 0 &&
                               (((shm[s] & ~smask[s * MOG_MAX_L + l]) >> g) & 1u);
-            rx[((size_t)(k + s * CS) * L + l) * G + g] = need ? sres[(s * G + g) * MOG_MAX_L + l] * LOG2E : -INFINITY;
+            rx[((size_t)(k + s * CS) * L + l) * GP + g] = need ? sres[(s * G + g) * MOG_MAX_L + l] * LOG2E : -INFINITY;
         }
-        for (int e = tid; e < ns * G; e += NT) {
-            const int cl = e / G, g = e - cl * G;
-            const bool need = resid && cnn[cl] > 0 && !((slm[cl] >> g) & 1u);
-            rx[((size_t)Uc * L + c0 + cl) * G + g] = need ? crs[g * m.SL + cl] * LOG2E : -INFINITY;
+        for (int e = tid; e < ns * GP; e += NT) {
+            const int cl = e / GP, g = e - cl * GP;
+            const bool need = resid && g < G && cnn[cl] > 0 && !((slm[cl] >> g) & 1u);
+            rx[((size_t)Uc * L + c0 + cl) * GP + g] = need ? crs[g * m.SL + cl] * LOG2E : -INFINITY;
         }
     }
     cluster.sync();  // S2: every slot's counts have been pushed
@@ -548,8 +550,9 @@ static_assert(RW_TPB >= AT_STAGES - 1, "the first batch must cover the pipeline'
 // through the 64-row tile engine.  A window of segments sits in shared memory; a row's
 // position is read from the partition (perm) at its segment's offset.  Positions are
 // fetched into registers two batches ahead and moved to shared memory when the pipeline
-// reaches the batch, so no tile copy waits on a position load.  After the rows, the CTA
-// adds its share of the Gaussian residual terms.  One unnormalised partial per CTA.
+// reaches the batch, so no tile copy waits on a position load.  After its rows, the CTA
+// streams its share of the Gaussian residual terms through the same pipeline.  One
+// unnormalised partial per CTA.
 template <int GT>
 __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     extern __shared__ __align__(128) uint8_t tile[];
@@ -654,6 +657,43 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
                        mk = mm;
                    });
     };
+    // The Gaussian residual terms follow the rows as 64-row tiles of given logits: items
+    // [ia, ib) of the unit's list (union pairs, then clusters), 32 per tile, each as two
+    // rows (bf16 high and low parts of its value mean) with its exponents from the
+    // selection kernel.
+    const int Uc = s_plan[5], L = s_plan[6], C = s_plan[7];
+    const int npi = Uc * L, I = dv.residual ? npi + C : 0;
+    const int ia = (int)((int64_t)I * p / P), ib = (int)((int64_t)I * (p + 1) / P);
+    const int nr = (ib - ia + AT_ROWS / 2 - 1) / (AT_ROWS / 2);
+    const float *rx = dv.resx + (size_t)u * dv.resx_stride;
+    const size_t ug = (size_t)u * dv.c_max, usg = ug * dv.l_max;
+    auto issue_terms = [&](int t, int tr) {  // tile t of the stream = terms tile tr
+        uint8_t *stg = tile + (t % AT_STAGES) * AT_STAGE_BYTES;
+        const int i0 = ia + tr * (AT_ROWS / 2), cnt = min(AT_ROWS / 2, ib - i0);
+        const uint32_t sv = smem_u32(stg) + AT_TILE_BYTES;
+        uint32_t *smk = reinterpret_cast<uint32_t *>(stg + 2 * AT_TILE_BYTES);
+        const int ch = tid & 15;
+#pragma unroll
+        for (int i = 0; i < AT_ROWS / 8; ++i) {
+            const int r = (tid >> 4) + 8 * i, it = r >> 1;
+            const bool ok = it < cnt;
+            const uint16_t *src = dv.cl_vhl;
+            if (ok) {
+                const int item = i0 + it;
+                src = item < npi ? dv.sub_vhl + (usg + (size_t)s_plan[PLAN_UCL + item / L] * L + item % L) * 2 * MOG_D
+                                 : dv.cl_vhl + (ug + (item - npi)) * 2 * MOG_D;
+                src += (r & 1) * MOG_D + ch * 8;
+            }
+            cp_async16(sv + swz(r, ch), src, ok ? 16 : 0);
+            if (ch == 0) smk[r] = ok ? allm : 0u;
+        }
+        float *E = reinterpret_cast<float *>(stg);  // [item][MOG_MAX_G] exponents
+        const int G4 = (G + 3) >> 2;
+        for (int e = tid; e < cnt * G4; e += AT_THREADS) {
+            const int it = e / G4, q = e - it * G4;
+            cp_async16(smem_u32(E + it * MOG_MAX_G + 4 * q), rx + (size_t)(i0 + it) * 4 * G4 + 4 * q, 16);
+        }
+    };
     WarpAcc acc;
     acc.init();
     const float scale2 = dv.tau * LOG2E;
@@ -691,104 +731,47 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     }
     cp_async_wait<0>();
     __syncthreads();
-    // The Gaussian residual: items [ia, ib) of the unit's list (union pairs, then clusters),
-    // exponents from the selection kernel, value means staged in passes into the tile
-    // memory after the states.  Thread (grp, g, d4) keeps a running (max, sum, acc) of
-    // items grp, grp + ngrp, ... for head g, dims 4*d4 .. 4*d4+3.
-    constexpr int MAXU = (GT * 32 + AT_THREADS - 1) / AT_THREADS;
-    const int U4 = G * 32, ngrp = max(1, AT_THREADS / U4), grp = ngrp > 1 ? tid / U4 : 0;
-    float *st = reinterpret_cast<float *>(tile);  // [AT_WARPS + ngrp][G][PART_W]
-    const int st_floats = (AT_WARPS + ngrp) * G * PART_W;
-    float rM[MAXU], rL[MAXU];
-    float4 rA[MAXU];
+    // the residual terms: the same pipeline over nr tiles of given logits
 #pragma unroll
-    for (int uu = 0; uu < MAXU; ++uu) {
-        rM[uu] = -INFINITY;
-        rL[uu] = 0.f;
-        rA[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s2 = 0; s2 < AT_STAGES - 1; ++s2) {
+        if (s2 < nr) issue_terms(s2, s2);
+        cp_async_commit();
     }
-    const int Uc = s_plan[5], L = s_plan[6], C = s_plan[7];
-    const int npi = Uc * L, I = npi + C;
-    const int ia = (int)((int64_t)I * p / P), ib = (int)((int64_t)I * (p + 1) / P);
-    if (dv.residual && ia < ib) {
-        const int rch = min(256, (AT_SMEM / 4 - st_floats) / (MOG_D + G));
-        float *rv = st + st_floats;          // [rch][d] value means
-        float *re = rv + (size_t)rch * MOG_D;  // [rch][G] exponents
-        const float *rx = dv.resx + (size_t)u * dv.resx_stride;
-        const size_t ug = (size_t)u * dv.c_max, usg = ug * dv.l_max;
-        for (int c0 = ia; c0 < ib; c0 += rch) {
-            const int cnt = min(rch, ib - c0);
-            for (int e = tid; e < cnt * 32; e += AT_THREADS) {
-                const int it = c0 + e / 32, q = e % 32;
-                const float *src = it < npi ? dv.sub_vbar + (usg + (size_t)s_plan[PLAN_UCL + it / L] * L + it % L) * MOG_D
-                                            : dv.cl_vbar + (ug + (it - npi)) * MOG_D;
-                cp_async16(smem_u32(rv + (size_t)(e / 32) * MOG_D + 4 * q), src + 4 * q, 16);
-            }
-            for (int e = tid; e < cnt * G; e += AT_THREADS) cp_async4(smem_u32(re + e), rx + (size_t)c0 * G + e);
-            cp_async_commit();
-            cp_async_wait<0>();
-            __syncthreads();
-#pragma unroll
-            for (int uu = 0; uu < MAXU; ++uu) {
-                const int unit = ngrp > 1 ? tid % U4 : tid + uu * AT_THREADS;
-                if ((ngrp > 1 && (uu > 0 || grp >= ngrp)) || unit >= U4) continue;
-                const int g = unit >> 5, d4 = unit & 31;
-                float mp = rM[uu];
-                for (int i = grp; i < cnt; i += ngrp) mp = fmaxf(mp, re[i * G + g]);
-                if (mp > rM[uu]) {  // rescale to the new maximum
-                    const float sc = rM[uu] == -INFINITY ? 0.f : exp2f(rM[uu] - mp);
-                    rL[uu] *= sc;
-                    rA[uu].x *= sc;
-                    rA[uu].y *= sc;
-                    rA[uu].z *= sc;
-                    rA[uu].w *= sc;
-                    rM[uu] = mp;
-                }
-                for (int i = grp; i < cnt; i += ngrp) {
-                    const float x = re[i * G + g];
-                    if (x == -INFINITY) continue;
-                    const float wt = exp2f(x - rM[uu]);
-                    const float4 v = *reinterpret_cast<const float4 *>(rv + (size_t)i * MOG_D + 4 * d4);
-                    rL[uu] += wt;
-                    rA[uu].x += wt * v.x;
-                    rA[uu].y += wt * v.y;
-                    rA[uu].z += wt * v.z;
-                    rA[uu].w += wt * v.w;
-                }
-            }
-            __syncthreads();
-        }
+    for (int t = 0; t < nr; ++t) {
+        cp_async_wait<AT_STAGES - 2>();
+        __syncthreads();
+        if (t + AT_STAGES - 1 < nr) issue_terms(t + AT_STAGES - 1, t + AT_STAGES - 1);
+        cp_async_commit();
+        compute_tile<true>(acc, qa, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
     }
-    warp_state_out(acc, st, G);
-#pragma unroll
-    for (int uu = 0; uu < MAXU; ++uu) {  // the residual groups' states after the warps'
-        const int unit = ngrp > 1 ? tid % U4 : tid + uu * AT_THREADS;
-        if ((ngrp > 1 && (uu > 0 || grp >= ngrp)) || unit >= U4) continue;
-        const int g = unit >> 5, d4 = unit & 31;
-        float *o = st + ((size_t)(AT_WARPS + grp) * G + g) * PART_W;
-        if (d4 == 0) {
-            o[0] = rM[uu];
-            o[1] = rL[uu];
-        }
-        *reinterpret_cast<float4 *>(o + PART_ACC + 4 * d4) = rA[uu];
-    }
+    cp_async_wait<0>();
     __syncthreads();
-    merge_states(st, AT_WARPS + ngrp, G, dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W);
+    float *st = reinterpret_cast<float *>(tile);
+    warp_state_out(acc, st, G);
+    __syncthreads();
+    merge_states(st, AT_WARPS, G, dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W);
 }
 
 // Kernel C: grid (G, units), 512 threads.  Merges the P partials of one query head
-// (running max, rescaled sums) and normalises once.  Thread (part, j) sums partials part,
-// part + 4, ... for dimension j; all loads are independent.
+// (running max, rescaled sums) and normalises once.  Thread (part, j) owns partials part,
+// part + 4, ... for dimension j; every load is issued before the maximum is known.
 constexpr int MG_THREADS = 4 * MOG_D;
+constexpr int MG_PARTS = MG_THREADS / MOG_D;
 __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int G,
                                                           float *out) {
     const int g = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
     const int j = tid % MOG_D, part = tid / MOG_D;
-    __shared__ float s_m[MAX_SPLITS], s_l[MAX_SPLITS], s_w[MAX_SPLITS];
-    __shared__ float s_acc[MG_THREADS / MOG_D][MOG_D];
+    __shared__ float s_m[MAX_SPLITS], s_l[MAX_SPLITS];
+    __shared__ float s_acc[MG_PARTS][MOG_D];
     pdl_wait();
     pdl_trigger();
     auto src = [&](int i) { return partials + (((size_t)u * PART_SLOTS + i) * G + g) * PART_W; };
+    float av[MAX_SPLITS / MG_PARTS];
+#pragma unroll
+    for (int q = 0; q < MAX_SPLITS / MG_PARTS; ++q) {
+        const int i = part + q * MG_PARTS;
+        av[q] = i < P ? __ldcg(src(i) + PART_ACC + j) : 0.f;
+    }
     if (tid < P) {
         s_m[tid] = __ldcg(src(tid));
         s_l[tid] = __ldcg(src(tid) + 1);
@@ -796,18 +779,20 @@ __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials,
     __syncthreads();
     float mx = -INFINITY;
     for (int i = 0; i < P; ++i) mx = fmaxf(mx, s_m[i]);
-    if (tid < P) s_w[tid] = (s_m[tid] == -INFINITY) ? 0.f : exp2f(s_m[tid] - mx);
-    __syncthreads();
-    float l = 0.f;
-    for (int i = 0; i < P; ++i) l += s_w[i] * s_l[i];
-    float v = 0.f;
-#pragma unroll 4
-    for (int i = part; i < P; i += MG_THREADS / MOG_D)
-        if (s_w[i] != 0.f) v += s_w[i] * __ldcg(src(i) + PART_ACC + j);
+    float l = 0.f, v = 0.f;
+    if (mx != -INFINITY) {
+        for (int i = 0; i < P; ++i)
+            if (s_m[i] != -INFINITY) l += exp2f(s_m[i] - mx) * s_l[i];
+#pragma unroll
+        for (int q = 0; q < MAX_SPLITS / MG_PARTS; ++q) {
+            const int i = part + q * MG_PARTS;
+            if (i < P && s_m[i] != -INFINITY) v += exp2f(s_m[i] - mx) * av[q];
+        }
+    }
     s_acc[part][j] = v;
     __syncthreads();
     if (part == 0) {
-        for (int q = 1; q < MG_THREADS / MOG_D; ++q) v += s_acc[q][j];
+        for (int q = 1; q < MG_PARTS; ++q) v += s_acc[q][j];
         out[((size_t)u * G + g) * MOG_D + j] = l > 0.f ? v / l : 0.f;
     }
 }

@@ -38,6 +38,7 @@ struct Dev {
     // persistent
     int *unit_info, *n_now, *perm, *sub_off, *cl_n, *sub_n, *l1_assign, *status, *l1_steps;
     float *cl_ms, *cl_vbar, *sub_ms, *sub_vbar;
+    uint16_t *cl_vhl, *sub_vhl;  // value means as bf16 high and low parts [item][2][d]
     // build workspace
     float *cent;
     int *permA, *changed, *fb_list, *fb_cnt, *hist, *offs, *ctot, *coff, *sub_assign;
@@ -47,7 +48,7 @@ struct Dev {
     int *plan;        // [units][PLAN_W]
     int *segrow, *segoff;  // [units][nseg_max] first row of a segment, its offset in perm
     uint32_t *segmask;     // [units][nseg_max] heads that attend the segment
-    float *resx;           // [units][resx_stride]: residual exponents [item][G]
+    float *resx;           // [units][resx_stride]: residual exponents [item][G, padded to 4]
     int64_t resx_stride;
 
     __host__ __device__ const uint16_t *krow(int b, int h, int64_t pos) const {
@@ -64,7 +65,7 @@ struct Plan {
     int score_mode, residual, P, nchunks, n_mid_max, nseg_max;
     int64_t sub_off_stride;
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
-        o_sub_vbar, o_l1_assign, o_status, o_l1_steps;
+        o_sub_vbar, o_cl_vhl, o_sub_vhl, o_l1_assign, o_status, o_l1_steps;
     int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
         o_sub_assign;
     int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask, o_resx, resx_stride;

@@ -651,6 +651,9 @@ __global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) 
         const float mean = ng > 0 ? s.s / (float)ng : 0.f;
         if (isV) {
             dv.sub_vbar[sg * MOG_D + j] = mean;
+            const uint32_t hi = f2bf(mean);  // bf16 high and low parts, for the decode
+            dv.sub_vhl[sg * 2 * MOG_D + j] = (uint16_t)hi;
+            dv.sub_vhl[sg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(mean - bf1((uint16_t)hi));
         } else {
             dv.sub_ms[sg * 2 * MOG_D + j] = mean;
             Kahan q;
@@ -666,6 +669,9 @@ __global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) 
     const float cmean = n > 0 ? tot.s / (float)n : 0.f;
     if (isV) {
         dv.cl_vbar[cg * MOG_D + j] = cmean;
+        const uint32_t hi = f2bf(cmean);
+        dv.cl_vhl[cg * 2 * MOG_D + j] = (uint16_t)hi;
+        dv.cl_vhl[cg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(cmean - bf1((uint16_t)hi));
         // cluster variance (keys), computed by the V threads in parallel with the K threads
         Kahan s;
         s.init();
