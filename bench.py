@@ -169,9 +169,10 @@ def oracle_decode_sample(w, budget_s, steps=None, warmup=0):
 # ------------------------------------------------------------------------ GPU path
 
 def bytes_from_selection(h, w, sel, lens, n_now):
-    """Algorithmic bytes of one decode step: all cluster summaries, the subcluster summaries
-    of each unit's union of selected clusters, the K/V rows (+ index) of the union of
-    selected subclusters, the anchors, and the output."""
+    """Algorithmic bytes of one decode step, per kernel: all cluster summaries and the
+    subcluster summaries of each unit's union of selected clusters (selection); the K/V
+    rows (+ index) of the union of selected subclusters, the anchors and the residual terms
+    (rows); the partials and the output (merge)."""
     import torch
     lay = h.layout()
     U, cm, lm, G = lay.units, lay.c_max, lay.l_max, lay.group
@@ -195,13 +196,19 @@ def bytes_from_selection(h, w, sel, lens, n_now):
                         usub.add((int(c), int(l)))
         Uk = sum(int(off[u, c * L + l + 1] - off[u, c * L + l]) for c, l in usub)
         anchors = min(S, n_now[b]) + max(0, n_now[b] - rlo)
+        items = len(ucl) * L + Cn  # residual terms: the union's subclusters, then clusters
+        gp = (G + 3) // 4 * 4
+        P = h.splits()
         # selection kernel: query, cluster summaries (mean, variance, count), the union's
-        # subcluster summaries, the value means of the residual, perm in / row list out
-        tot["select"] += G * D * 2 + Cn * (8 * D + 4) + len(ucl) * L * (8 * D + 4)
-        tot["select"] += (Cn + len(ucl) * L) * 4 * D + Uk * (4 + 8)
-        # rows kernel: query, row list, the K and V rows (bf16); merge: the output (fp32)
-        tot["attend"] += G * D * 2 + Uk * 8 + (Uk + anchors) * 4 * D
-        tot["merge"] += G * D * 4
+        # subcluster summaries and offsets; writes the segments and the residual exponents
+        tot["select"] += G * D * 2 + Cn * (8 * D + 4) + len(ucl) * (L * (8 * D + 8) + 4)
+        tot["select"] += len(usub) * 12 + items * gp * 4
+        # rows kernel: query, segments, perm index and K, V rows (bf16) of the chosen rows and
+        # the anchors, the residual terms (bf16 high/low value means and exponents), partials
+        tot["attend"] += G * D * 2 + len(usub) * 12 + Uk * 4 + (Uk + anchors) * 4 * D
+        tot["attend"] += items * (4 * D + gp * 4) + P * G * (D + 4) * 4
+        # merge kernel: partials in, the output (fp32) out
+        tot["merge"] += P * G * (D + 4) * 4 + G * D * 4
         tot["rows"] += Uk + anchors
     tot["step"] = tot["select"] + tot["attend"] + tot["merge"]
     return tot
@@ -334,11 +341,7 @@ def run_gpu(a, w, rank, world):
     clk = clocks.stop()
     assert h.sync_status() == 0
 
-    mean_ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([mean_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(statistics.mean(step_ms), dev)
     pm = [statistics.mean(p) for p in phase]
     names = ["k_mog_decode", "k_mog_rows", "k_mog_merge"]
     kbytes = [by["select"], by["attend"], by["merge"]]
@@ -392,6 +395,17 @@ def run_gpu(a, w, rank, world):
         res["cpu_baseline"] = {"value": round(mu, 1), "unit": "us/step/layer", "cores": cores,
                                "kind": "oracle", "sample": desc}
         print(json.dumps(res), flush=True)
+
+
+def max_over_ranks(value, device):
+    """The maximum of `value` over all ranks of the default process group (the value itself
+    when no group is initialised): the job's time is its slowest replica's."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_reference(a, w, rank):

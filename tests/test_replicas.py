@@ -1,0 +1,62 @@
+"""Host logic of the replicas-only multi-GPU mode, on CPU with two gloo ranks: the job time
+is the maximum over ranks, and the reference arm runs on rank 0 only."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import os, sys
+sys.path.insert(0, sys.argv[1])
+import torch, torch.distributed as dist
+import bench
+rank, world = int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"])
+dist.init_process_group("gloo")
+v = bench.max_over_ranks(10.0 + 5.0 * rank, "cpu")
+dist.barrier()
+print(f"rank{rank} max={v}", flush=True)
+dist.destroy_process_group()
+"""
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_max_over_ranks_gloo_world2():
+    port = _free_port()
+    procs = []
+    for r in range(2):
+        env = dict(os.environ, RANK=str(r), WORLD_SIZE="2", MASTER_ADDR="127.0.0.1",
+                   MASTER_PORT=str(port), LOCAL_RANK=str(r))
+        procs.append(subprocess.Popen([sys.executable, "-c", CHILD, ROOT], env=env,
+                                      stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True))
+    outs = []
+    for p in procs:
+        out, _ = p.communicate(timeout=180)
+        outs.append(out)
+        assert p.returncode == 0, out
+    for r, out in enumerate(outs):
+        assert f"rank{r} max=15.0" in out, out
+
+
+def test_max_over_ranks_single_process():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.25, "cpu") == 3.25
+
+
+def test_reference_arm_rank_nonzero_does_no_work(capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        cpu_seconds, steps, warmup, gpus = 1.0, 1, 1, 2
+    bench.run_reference(A(), None, rank=1)
+    assert capsys.readouterr().out == ""
