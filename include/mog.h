@@ -233,14 +233,20 @@ int dense_decode_noalloc(const mog_kv *kv, const int32_t *lengths_dev, int32_t n
  * a Lloyd step): for each of the n rows x_i (bf16, row stride ld elements),
  * assign_out_dev[i] = argmin_c sum_j (x_ij - cent_cj)^2 with the lowest index on ties,
  * decided exactly as the fp64 sum of rounded squares in index order.  The same kernels
- * as mog_build's first level.  cent_dev: f32 [k][d].  scratch_dev: at least
- * mog_kmeans_assign_scratch_bytes() bytes.  fallback_rows_host (may be NULL) receives the
- * number of rows the exact fallback decided (this synchronises the stream).
+ * as mog_build's first level: the distances are scored on the tensor cores (bf16 keys,
+ * centroids as bf16 high + low parts, fp32 accumulate); a row whose best centroid is not
+ * separated from the others by the scores' error bound is decided by the direct fp32
+ * pass, and a row that pass cannot certify by the fp64 rule.  cent_dev: f32 [k][d],
+ * k <= 4096.  scratch_dev: 16-byte aligned, at least mog_kmeans_assign_scratch_bytes()
+ * bytes.  counts_host (may be NULL; int32[2]) receives the rows decided by the fp64 rule
+ * and the rows the tensor-core pass left to the direct pass; with it the call
+ * synchronises the stream and reports a device-side failure (MOG_ERR_TIMEOUT,
+ * MOG_ERR_DEVICE_CHECK).
  */
 int mog_kmeans_assign_scratch_bytes(int32_t n, int32_t k, int32_t d, size_t *bytes);
 int mog_kmeans_assign(const void *x_dev, int64_t ld, int32_t n, const float *cent_dev,
                       int32_t k, int32_t d, int32_t *assign_out_dev, void *scratch_dev,
-                      size_t scratch_bytes, void *stream, int32_t *fallback_rows_host);
+                      size_t scratch_bytes, void *stream, int32_t *counts_host);
 
 /*
  * Test export of one second-level assignment step: n_seg segments, segment s holding

@@ -290,20 +290,23 @@ def dense_decode_noalloc(K, V, lengths_dev, n_max, q, out, stream=None):
     return out
 
 
-def kmeans_assign(x, cent, stream=None):
+def kmeans_assign(x, cent, stream=None, with_recheck=False):
     """One first-level assignment step: x bf16 [n, d] (row stride x.stride(0)), cent f32
-    [k, d].  Returns (assign int32 [n], rows decided by the exact fallback)."""
+    [k, d].  Returns (assign int32 [n], rows decided by the exact fallback), plus the rows
+    the tensor-core pass left to the direct pass when with_recheck."""
     torch = _torch()
     n, k = x.shape[0], cent.shape[0]
     out = torch.empty(n, dtype=torch.int32, device=x.device)
     need = C.c_size_t(0)
     _check(lib().mog_kmeans_assign_scratch_bytes(n, k, 128, C.byref(need)), "scratch")
     scratch = torch.empty(need.value, dtype=torch.uint8, device=x.device)
-    fb = C.c_int32(0)
+    counts = (C.c_int32 * 2)()
     _check(lib().mog_kmeans_assign(_ptr(x), x.stride(0), n, _ptr(cent), k, 128, _ptr(out),
-                                   _ptr(scratch), need.value, _stream(stream), C.byref(fb)),
+                                   _ptr(scratch), need.value, _stream(stream), counts),
            "mog_kmeans_assign")
-    return out, fb.value
+    if with_recheck:
+        return out, counts[0], counts[1]
+    return out, counts[0]
 
 
 def kmeans_assign_segments(x, rows, seg_off, cent, stream=None):

@@ -153,6 +153,12 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_changed = take(4 * U * P.T1);
     P.o_fb_list = take(4 * U * nc);
     P.o_fb_cnt = take(4 * U * P.T1);
+    P.o_rc_list = take(4 * U * nc);
+    P.o_rc_cnt = take(4 * U * P.T1);
+    P.cimg_ustride = (int64_t)ceil_div64(cm, KM_CHUNK) * KM_IMG_CHUNK;
+    P.cn_ustride = (int64_t)ceil_div64(cm, KM_CHUNK) * KM_CHUNK;
+    P.o_cimg = take(2 * U * P.cimg_ustride);
+    P.o_cnorm = take(4 * U * P.cn_ustride);
     P.o_hist = take(4 * U * P.nchunks * cm);
     P.o_offs = take(4 * U * P.nchunks * cm);
     P.o_ctot = take(4 * U * cm);
@@ -198,6 +204,8 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.residual = P.residual;
     d.P = P.P;
     d.nseg_max = P.nseg_max;
+    d.cimg_ustride = P.cimg_ustride;
+    d.cn_ustride = P.cn_ustride;
     d.resx_stride = P.resx_stride;
     d.nchunks = P.nchunks;
     d.sub_off_stride = P.sub_off_stride;
@@ -223,6 +231,10 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     PTR(changed, int);
     PTR(fb_list, int);
     PTR(fb_cnt, int);
+    PTR(rc_list, int);
+    PTR(rc_cnt, int);
+    PTR(cimg, uint16_t);
+    PTR(cnorm, float);
     PTR(hist, int);
     PTR(offs, int);
     PTR(ctot, int);
@@ -341,6 +353,7 @@ static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
     CKH(cudaMemsetAsync(a + pl.o_status, 0, 64, s));
     CKH(cudaMemsetAsync(a + pl.o_changed, 0, 4 * (size_t)pl.units * pl.T1, s));
     CKH(cudaMemsetAsync(a + pl.o_fb_cnt, 0, 4 * (size_t)pl.units * pl.T1, s));
+    CKH(cudaMemsetAsync(a + pl.o_rc_cnt, 0, 4 * (size_t)pl.units * pl.T1, s));
     CKH(cudaMemsetAsync(a + pl.o_coff, 0, 4 * (size_t)pl.units * (pl.c_max + 1), s));
     CKH(cudaMemsetAsync(a + pl.o_l1_assign, 0xff, 4 * (size_t)pl.units * pl.n_cap, s));
     CKH(cudaMemsetAsync(a + pl.o_l1_steps, 0, 4 * (size_t)pl.units, s));
@@ -483,6 +496,7 @@ extern "C" int mog_sync_status(mog_handle *h, void *stream) {
     CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
     int st = 0;
     CK(cudaMemcpy(&st, h->arena + h->plan.o_status, 4, cudaMemcpyDeviceToHost));
+    if (st & (1 << ST_TIMEOUT)) return MOG_ERR_TIMEOUT;
     return st ? MOG_ERR_DEVICE_CHECK : MOG_OK;
 }
 
@@ -554,30 +568,52 @@ extern "C" int dense_decode_noalloc(const mog_kv *kv, const int32_t *lengths_dev
 
 // ----------------------------------------------------------------- parity exports
 
+// scratch of mog_kmeans_assign: counters (256 B), the fallback and recheck row lists,
+// the centroid images and norms of the tensor-core pass
+static size_t km_off_lists() { return 256; }
+static size_t km_list_bytes(int n) { return ((4 * (size_t)std::max(n, 1)) + 255) & ~(size_t)255; }
+static size_t km_img_bytes(int k) { return 2 * (size_t)ceil_div64(k, KM_CHUNK) * KM_IMG_CHUNK; }
+
 extern "C" int mog_kmeans_assign_scratch_bytes(int32_t n, int32_t k, int32_t d, size_t *bytes) {
     if (!bytes || n < 0 || k <= 0) return MOG_ERR_INVALID_ARG;
     if (d != MOG_D) return MOG_ERR_SHAPE;
-    *bytes = 256 + 4 * (size_t)std::max(n, 1);
+    if (k > MAX_C) return MOG_ERR_SHAPE;
+    *bytes = km_off_lists() + 2 * km_list_bytes(n) + km_img_bytes(k) + 4 * (size_t)ceil_div64(k, KM_CHUNK) * KM_CHUNK;
     return MOG_OK;
 }
 
 extern "C" int mog_kmeans_assign(const void *x_dev, int64_t ld, int32_t n, const float *cent_dev,
                                  int32_t k, int32_t d, int32_t *assign_out_dev, void *scratch_dev,
-                                 size_t scratch_bytes, void *stream, int32_t *fallback_rows_host) {
+                                 size_t scratch_bytes, void *stream, int32_t *counts_host) {
     size_t need = 0;
     int st = mog_kmeans_assign_scratch_bytes(n, k, d, &need);
     if (st != MOG_OK) return st;
     if (!x_dev || !cent_dev || !assign_out_dev || !scratch_dev) return MOG_ERR_INVALID_ARG;
     if (!aligned16(x_dev) || !aligned16(cent_dev) || ld < MOG_D || (ld & 7)) return MOG_ERR_SHAPE;
-    if (scratch_bytes < need) return MOG_ERR_ARENA_TOO_SMALL;
+    if (scratch_bytes < need || !aligned16(scratch_dev)) return MOG_ERR_ARENA_TOO_SMALL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int *sc = static_cast<int *>(scratch_dev);
+    char *base = static_cast<char *>(scratch_dev);
+    int *sc = reinterpret_cast<int *>(base);
+    KmScratch ks;
+    ks.changed = sc;
+    ks.fb_cnt = sc + 32;
+    ks.rc_cnt = sc + 40;
+    ks.status = sc + 48;
+    ks.fb_list = reinterpret_cast<int *>(base + km_off_lists());
+    ks.rc_list = reinterpret_cast<int *>(base + km_off_lists() + km_list_bytes(n));
+    ks.cimg = reinterpret_cast<uint16_t *>(base + km_off_lists() + 2 * km_list_bytes(n));
+    ks.cnorm = reinterpret_cast<float *>(base + km_off_lists() + 2 * km_list_bytes(n) + km_img_bytes(k));
     CK(cudaMemsetAsync(sc, 0, 256, s));
-    CK(launch_assign_l1(static_cast<const uint16_t *>(x_dev), ld, n, cent_dev, k, assign_out_dev,
-                        sc, sc + 64, sc + 32, s));
-    if (fallback_rows_host) {
-        CK(cudaMemcpyAsync(fallback_rows_host, sc + 32, 4, cudaMemcpyDeviceToHost, s));
+    CK(launch_assign_l1(static_cast<const uint16_t *>(x_dev), ld, n, cent_dev, k, assign_out_dev, ks, s));
+    if (counts_host) {
+        int32_t c[3];
+        CK(cudaMemcpyAsync(&c[0], ks.fb_cnt, 4, cudaMemcpyDeviceToHost, s));
+        CK(cudaMemcpyAsync(&c[1], ks.rc_cnt, 4, cudaMemcpyDeviceToHost, s));
+        CK(cudaMemcpyAsync(&c[2], ks.status, 4, cudaMemcpyDeviceToHost, s));
         CK(cudaStreamSynchronize(s));
+        counts_host[0] = c[0];
+        counts_host[1] = c[1];
+        if (c[2]) return (c[2] & (1 << ST_TIMEOUT)) ? MOG_ERR_TIMEOUT : MOG_ERR_DEVICE_CHECK;
     }
     return MOG_OK;
 }

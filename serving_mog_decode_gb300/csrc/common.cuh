@@ -143,7 +143,7 @@ __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) {
 }
 
 // Device status word bits (arena status[0])
-enum : int { ST_OK = 0, ST_BAD_INDEX = 1, ST_BAD_SIZE = 2 };
+enum : int { ST_OK = 0, ST_BAD_INDEX = 1, ST_BAD_SIZE = 2, ST_TIMEOUT = 3 };
 
 __device__ __forceinline__ void flag_error(int *status, int code) {
     if (status) atomicOr(status, 1 << code);

@@ -12,6 +12,10 @@ namespace mog {
 enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
 
 constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
+// First-level assignment on the tensor cores: centroids in chunks of KM_CHUNK, each chunk
+// an image of KM_IMG_CHUNK bf16 ({high, low} x two 64-column halves x KM_CHUNK rows).
+constexpr int KM_CHUNK = 256;
+constexpr int64_t KM_IMG_CHUNK = 4LL * KM_CHUNK * 64;
 constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
 constexpr int PART_SLOTS = MAX_SPLITS;  // partials per unit: one per rows-kernel CTA
 // Rows-kernel plan per unit, written by the selection kernel: [0] segments NS, [1] rows T,
@@ -42,6 +46,10 @@ struct Dev {
     // build workspace
     float *cent;
     int *permA, *changed, *fb_list, *fb_cnt, *hist, *offs, *ctot, *coff, *sub_assign;
+    int *rc_list, *rc_cnt;  // rows the tensor-core pass leaves to the direct pass
+    uint16_t *cimg;         // centroid images for the tensor cores [unit][cimg_ustride]
+    float *cnorm;           // |c|^2 [unit][cn_ustride]
+    int64_t cimg_ustride, cn_ustride;
     // decode workspace
     float *partials;  // [units][PART_SLOTS][G][PART_W]
     int *sel;         // [units][G][tc + tc*ts] selection of the last step
@@ -67,7 +75,7 @@ struct Plan {
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
         o_sub_vbar, o_cl_vhl, o_sub_vhl, o_l1_assign, o_status, o_l1_steps;
     int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
-        o_sub_assign;
+        o_sub_assign, o_rc_list, o_rc_cnt, o_cimg, o_cnorm, cimg_ustride, cn_ustride;
     int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask, o_resx, resx_stride;
     int64_t total;
 };
@@ -94,9 +102,14 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
 int dense_splits(int units, int n_max);
 cudaError_t dense_static_scratch(float **ptr, size_t *bytes);
 size_t slot_smem_bytes(int G, int c_max, int l_max, int tc);
+// Work buffers of a single-matrix first-level assignment step.
+struct KmScratch {
+    int *changed, *fb_cnt, *rc_cnt, *status, *fb_list, *rc_list;
+    uint16_t *cimg;
+    float *cnorm;
+};
 cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
-                             int32_t *assign, int *changed, int *fb_list, int *fb_cnt,
-                             cudaStream_t s);
+                             int32_t *assign, const KmScratch &ks, cudaStream_t s);
 cudaError_t launch_assign_segments(const uint16_t *x, int64_t ld, const int32_t *rows,
                                    const int32_t *seg_off, int n_seg, const float *cent, int k,
                                    int32_t *assign, cudaStream_t s);

@@ -18,8 +18,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace mog {
 
@@ -68,6 +71,18 @@ struct AssignJob {
     int64_t fb_ustride;
     int *fb_cnt;  // [unit][T]
     int t, T;
+    // row-list mode of the direct pass: rows[u][0 .. rows_cnt[u*T + t]) instead of all rows
+    const int *rows;
+    int64_t rows_ustride;
+    const int *rows_cnt;
+    // tensor-core pass: centroid images, squared norms, rows it leaves to the direct pass
+    uint16_t *cimg;  // [unit][cimg_ustride]: per 256-centroid chunk [2 parts][2 halves][256][64]
+    int64_t cimg_ustride;
+    float *cnorm;  // [unit][cn_ustride]
+    int64_t cn_ustride;
+    int *rc_list;  // [unit][fb_ustride]
+    int *rc_cnt;   // [unit][T]
+    int *status;
 };
 
 constexpr int AS_ROWS = 64, AS_CENT = 64, AS_THREADS = 256, AS_PAD = 68;
@@ -100,17 +115,23 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
     const uint16_t *x;
     int n, k;
     job_unit(jb, u, x, n, k);
-    const int r0 = blockIdx.x * AS_ROWS;
-    if (r0 >= n || k <= 0) return;
+    const int *rl = jb.rows ? jb.rows + u * jb.rows_ustride : nullptr;
+    const int nrows = rl ? jb.rows_cnt[u * jb.T + jb.t] : n;  // rows of this pass
+    if (k <= 0) return;
     const float *cent = jb.cent + u * jb.cent_ustride;
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    __shared__ int s_row[AS_ROWS];
+    for (int r0 = blockIdx.x * AS_ROWS; r0 < nrows; r0 += gridDim.x * AS_ROWS) {
+    __syncthreads();
     if (tid == 0) s_changed = 0;
+    if (tid < AS_ROWS) s_row[tid] = r0 + tid < nrows ? (rl ? rl[r0 + tid] : r0 + tid) : -1;
+    __syncthreads();
 
     // rows -> Xs[j][r] (fp32), 16-byte loads of 8 bf16
     for (int e = tid; e < AS_ROWS * 16; e += AS_THREADS) {
         int r = e >> 4, ch = e & 15;
         uint4 w = make_uint4(0, 0, 0, 0);
-        if (r0 + r < n) w = *reinterpret_cast<const uint4 *>(x + (int64_t)(r0 + r) * jb.sn + ch * 8);
+        if (s_row[r] >= 0) w = *reinterpret_cast<const uint4 *>(x + (int64_t)s_row[r] * jb.sn + ch * 8);
         uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -194,9 +215,9 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
     if (tx == 0) {
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            int r = r0 + ty * 4 + a;
+            int r = s_row[ty * 4 + a];
             s_unc[ty * 4 + a] = 0;
-            if (r >= n) continue;
+            if (r < 0) continue;
             int *dst = jb.assign + u * jb.assign_ustride + r;
             if (k == 1 || certified(b1[a], b2[a])) {
                 int old = *dst;
@@ -220,10 +241,11 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
         int base = s_base;
         uint32_t m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
         int *fl = jb.fb_list + u * jb.fb_ustride;
-        if (f0) fl[base + __popc(m0 & lanemask_lt())] = r0 + tid;
-        if (f1) fl[base + __popc(m0) + __popc(m1 & lanemask_lt())] = r0 + 32 + tid;
+        if (f0) fl[base + __popc(m0 & lanemask_lt())] = s_row[tid];
+        if (f1) fl[base + __popc(m0) + __popc(m1 & lanemask_lt())] = s_row[32 + tid];
         if (tid == 0 && s_changed) atomicAdd(jb.changed + u * jb.T + jb.t, s_changed);
     }
+    }  // rows of this CTA
 }
 
 // Rows the fp32 pass could not certify: one warp per row, lanes over centroids, the exact
@@ -691,6 +713,254 @@ __global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) 
 }
 
 // ------------------------------------------------------------------------------------
+// First-level assignment on the tensor cores (tcgen05, TMA-fed tiles).
+//
+// The approximate distance of key k to centroid c (up to |k|^2, equal for every c) is
+//     a_c = |c|^2 - 2 k.c,   k.c = k.c_hi + k.c_lo   (c split into bf16 high + low parts),
+// computed for 128 keys x 256 centroids per MMA group, fp32 accumulate in tensor memory.
+// Its error against the exact D(k, c) - |k|^2 is below 2^-14.5 (|k|^2 + |c|^2): the split
+// leaves 2^-18 |c_j| per element, the fp32 sums add at most 2^-23 per term over 256
+// terms, |c|^2 is an fp32 sum of 128 squares.  With f = 2^-13 a key keeps its best
+// approximate centroid b only when every other centroid j has
+//     a_j - f(|k|^2 + |c_j|^2) > a_b + f(|k|^2 + |c_b|^2),
+// which makes b the unique exact argmin; every other key goes to the direct fp32 pass
+// (and from there, if needed, to the exact fp64 rule).
+// ------------------------------------------------------------------------------------
+constexpr int TC_M = 128;                       // keys per tile (TMEM lanes)
+constexpr int TC_NC = 256;                      // centroids per MMA group (TMEM columns)
+constexpr uint32_t TC_A_BYTES = TC_M * 256;     // 128 keys x 128 bf16
+constexpr uint32_t TC_B_HALF = TC_NC * 128;     // 256 rows x 64 bf16 (one 128-byte swizzle column)
+constexpr uint32_t TC_B_BYTES = 4 * TC_B_HALF;  // {high, low} x {k 0-63, k 64-127}
+constexpr size_t TC_SMEM = 1024 + TC_A_BYTES + TC_B_BYTES + TC_NC * 4;
+constexpr float TC_F = 1.0f / 8192.0f;          // 2^-13
+
+__host__ __device__ inline int tc_chunks(int k) { return (k + TC_NC - 1) / TC_NC; }
+
+// Centroid images for the tensor-core pass: bf16 high and low parts in the 128-byte
+// swizzle layout (16-byte chunk q of row r at position q ^ (r & 7)), and |c|^2 (fp32,
+// +inf for padding).  Block: 8 centroids x 16 chunks of 8 dimensions.
+__global__ void __launch_bounds__(128) k_cent_prep(AssignJob jb) {
+    const int u = blockIdx.y;
+    const int *chg = jb.changed + (int64_t)u * jb.T;
+    if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
+    const uint16_t *x;
+    int n, k;
+    job_unit(jb, u, x, n, k);
+    const int c = blockIdx.x * 8 + (threadIdx.x >> 4), q = threadIdx.x & 15;
+    if (c >= tc_chunks(k) * TC_NC) return;
+    float v[8];
+    const bool real = c < k;
+    const float *cp = jb.cent + u * jb.cent_ustride + (int64_t)c * MOG_D + q * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = real ? cp[i] : 0.f;
+    uint32_t hi[4], lo[4];
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t h0 = f2bf(v[2 * i]), h1 = f2bf(v[2 * i + 1]);
+        hi[i] = h0 | (h1 << 16);
+        lo[i] = f2bf(v[2 * i] - bf1((uint16_t)h0)) | (f2bf(v[2 * i + 1] - bf1((uint16_t)h1)) << 16);
+        sq = __fmaf_rn(v[2 * i], v[2 * i], sq);
+        sq = __fmaf_rn(v[2 * i + 1], v[2 * i + 1], sq);
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    const int ch = c / TC_NC, r = c % TC_NC, half = q >> 3, pos = (q & 7) ^ (r & 7);
+    uint16_t *img = jb.cimg + u * jb.cimg_ustride + (int64_t)ch * (TC_B_BYTES / 2);
+    *reinterpret_cast<uint4 *>(img + (0 * 2 + half) * (TC_B_HALF / 2) + r * 64 + pos * 8) =
+        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4 *>(img + (1 * 2 + half) * (TC_B_HALF / 2) + r * 64 + pos * 8) =
+        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    if (q == 0) jb.cnorm[u * jb.cn_ustride + c] = real ? sq : INFINITY;
+}
+
+// One CTA: 128 keys of one unit against all centroids, 256 at a time.  Thread 0 issues the
+// copies and the MMAs; every thread then reads its key's row of scores from tensor memory.
+__global__ void __launch_bounds__(128, 1) k_assign_tc(AssignJob jb, const __grid_constant__ CUtensorMap kmap) {
+    extern __shared__ uint8_t tc_raw[];
+    __shared__ __align__(8) uint64_t s_bar[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_changed, s_base;
+    __shared__ int s_unc[TC_M];
+    const int u = blockIdx.y;
+    const int *chg = jb.changed + (int64_t)u * jb.T;
+    if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
+    const uint16_t *x;
+    int n, k;
+    job_unit(jb, u, x, n, k);
+    const int r0 = blockIdx.x * TC_M;
+    if (r0 >= n || k <= 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t raw = smem_u32(tc_raw);
+    const uint32_t sA = (raw + 1023u) & ~1023u, sB = sA + TC_A_BYTES, sC = sB + TC_B_BYTES;
+    const float *scn = reinterpret_cast<const float *>(tc_raw + (sC - raw));
+    const uint32_t bar_ld = smem_u32(&s_bar[0]), bar_mma = smem_u32(&s_bar[1]);
+    // TMA coordinates of the tile's first key
+    int cb = 0, ch_ = 0, crow = r0;
+    if (jb.unit_info) {
+        const int *ui = jb.unit_info + u * UI_STRIDE;
+        cb = ui[UI_B];
+        ch_ = u % jb.h_kv;
+        crow = ui[UI_S] + r0;
+    }
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        fence_barrier_init();
+        s_changed = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&s_tmem), TC_NC);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint16_t *img = jb.cimg + u * jb.cimg_ustride;
+    const float *cng = jb.cnorm + u * jb.cn_ustride;
+    const int row = r0 + tid;  // this thread's key (TMEM lane tid)
+    float kn = 0.f;
+    float b1 = INFINITY, u1 = INFINITY, l1 = INFINITY, l2 = INFINITY;
+    int i1 = 0x7fffffff, li1 = -1;
+    uint32_t ph_ld = 0, ph_mma = 0;
+    int fail = 0;  // 1: a copy timed out, 2: the MMAs timed out
+    const int nch = tc_chunks(k);
+    for (int ch = 0; ch < nch; ++ch) {
+        const int nreal = min(TC_NC, k - ch * TC_NC);
+        const int ncp = (nreal + 15) & ~15;  // MMA N: a multiple of 16
+        if (tid == 0) {
+            fence_proxy_async();  // earlier generic reads of the buffers precede the copies
+            const uint32_t bbytes = (uint32_t)ncp * 128;
+            mbar_expect_tx(bar_ld, 4 * bbytes + (uint32_t)ncp * 4 + (ch == 0 ? TC_A_BYTES : 0u));
+            if (ch == 0) {
+                tma_load_4d(sA, &kmap, 0, crow, ch_, cb, bar_ld);
+                tma_load_4d(sA + TC_A_BYTES / 2, &kmap, 64, crow, ch_, cb, bar_ld);
+            }
+            const uint16_t *cimg = img + (int64_t)ch * (TC_B_BYTES / 2);
+            for (int part = 0; part < 4; ++part)
+                bulk_load(sB + part * TC_B_HALF, cimg + part * (TC_B_HALF / 2), bbytes, bar_ld);
+            bulk_load(sC, cng + ch * TC_NC, (uint32_t)ncp * 4, bar_ld);
+        }
+        if (__syncthreads_or(!mbar_wait(bar_ld, ph_ld))) {
+            fail = 1;
+            break;
+        }
+        ph_ld ^= 1u;
+        if (ch == 0) {  // this key's |k|^2 from the swizzled tile
+            const uint8_t *ta = tc_raw + (sA - raw);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(
+                    ta + (q >> 3) * (TC_A_BYTES / 2) + tid * 128 + (((q & 7) ^ (tid & 7)) << 4));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    kn = __fmaf_rn(bf_lo(ws[i]), bf_lo(ws[i]), kn);
+                    kn = __fmaf_rn(bf_hi(ws[i]), bf_hi(ws[i]), kn);
+                }
+            }
+        }
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16_f32(TC_M, ncp);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t aoff = (ks >> 2) * (TC_A_BYTES / 2) + (ks & 3) * 32;
+                    const uint32_t boff = (part * 2 + (ks >> 2)) * TC_B_HALF + (ks & 3) * 32;
+                    tc_mma(tmem, smem_desc_sw128(sA + aoff), smem_desc_sw128(sB + boff), idesc,
+                           (part | ks) != 0);
+                }
+            tc_commit(bar_mma);
+        }
+        if (__syncthreads_or(!mbar_wait(bar_mma, ph_mma))) {
+            fail = 2;
+            break;
+        }
+        ph_mma ^= 1u;
+        tc_fence_after();
+        for (int c0 = 0; c0 < ncp; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (c0 + j >= nreal) break;
+                const int c = ch * TC_NC + c0 + j;
+                const float cn = scn[c0 + j];
+                const float ap = cn - 2.f * v[j];
+                const float e = TC_F * (kn + cn);
+                if (ap < b1) {  // ascending c: the first minimum keeps the lowest index
+                    b1 = ap;
+                    i1 = c;
+                    u1 = ap + e;
+                }
+                const float lw = ap - e;
+                if (lw < l1) {
+                    l2 = l1;
+                    l1 = lw;
+                    li1 = c;
+                } else if (lw < l2) {
+                    l2 = lw;
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // scores read, operands consumed: the next group may overwrite them
+    }
+    if (fail) {
+        if (tid == 0) flag_error(jb.status, ST_TIMEOUT);
+        // the copy or the MMAs still in flight get a bounded chance to finish
+        if (fail == 1) mbar_wait(bar_ld, ph_ld);
+        else mbar_wait(bar_mma, ph_mma);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TC_NC);
+    if (fail) return;
+    // decide this key: certain, or left to the direct pass
+    const float comp = (li1 == i1) ? l2 : l1;
+    const bool certain = (k == 1) || (comp > u1);
+    s_unc[tid] = 0;
+    int my_changed = 0;
+    if (row < n) {
+        if (certain) {
+            int *dst = jb.assign + u * jb.assign_ustride + row;
+            if (*dst != i1) {
+                *dst = i1;
+                my_changed = 1;
+            }
+        } else {
+            s_unc[tid] = 1;
+        }
+    }
+    const int wc = __reduce_add_sync(0xffffffffu, my_changed);
+    if ((tid & 31) == 0 && wc) atomicAdd(&s_changed, wc);
+    __syncthreads();
+    if (tid < 32) {
+        int f[4], cnt = 0;
+        uint32_t m[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            f[q] = s_unc[q * 32 + tid];
+            m[q] = __ballot_sync(0xffffffffu, f[q]);
+            cnt += __popc(m[q]);
+        }
+        if (tid == 0) s_base = cnt ? atomicAdd(jb.rc_cnt + u * jb.T + jb.t, cnt) : 0;
+        __syncwarp();
+        int base = s_base;
+        int *rl = jb.rc_list + u * jb.fb_ustride;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (f[q]) rl[base + __popc(m[q] & lanemask_lt())] = r0 + q * 32 + tid;
+            base += __popc(m[q]);
+        }
+        if (tid == 0 && s_changed) atomicAdd(jb.changed + u * jb.T + jb.t, s_changed);
+    }
+}
+
+// ------------------------------------------------------------------------------------
 // launchers
 // ------------------------------------------------------------------------------------
 static AssignJob build_job(const Dev &dv, int t) {
@@ -713,10 +983,85 @@ static AssignJob build_job(const Dev &dv, int t) {
     jb.fb_cnt = dv.fb_cnt;
     jb.t = t;
     jb.T = dv.T1;
+    jb.rows = nullptr;
+    jb.rows_ustride = 0;
+    jb.rows_cnt = nullptr;
+    jb.cimg = dv.cimg;
+    jb.cimg_ustride = dv.cimg_ustride;
+    jb.cnorm = dv.cnorm;
+    jb.cn_ustride = dv.cn_ustride;
+    jb.rc_list = dv.rc_list;
+    jb.rc_cnt = dv.rc_cnt;
+    jb.status = dv.status;
     return jb;
 }
 
 static cudaError_t set_smem(const void *fn, size_t bytes) { return ensure_smem(fn, bytes); }
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Tensor map of bf16 keys [b][h][row][128] (element strides sn, sh, sb), boxes of 64
+// dimensions x TC_M rows in the 128-byte swizzle.  False if TMA cannot describe it.
+static bool key_map(CUtensorMap *map, const uint16_t *base, int64_t rows, int64_t h, int64_t b,
+                    int64_t sn, int64_t sh, int64_t sb) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)MOG_D, (cuuint64_t)rows, (cuuint64_t)h, (cuuint64_t)b};
+    const cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+    for (int i = 0; i < 3; ++i)
+        if (strides[i] == 0 || (strides[i] & 15) || strides[i] >= (1ull << 40)) return false;
+    const cuuint32_t box[4] = {64, (cuuint32_t)TC_M, 1, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One assignment step: the tensor-core pass over every row (when the keys have a tensor
+// map), the direct fp32 pass over the rows it could not decide (else over every row),
+// then the exact fp64 rule for whatever the direct pass could not certify.
+static cudaError_t assign_step(const AssignJob &jb, const CUtensorMap *kmap, int units, int n_max,
+                               int k_max, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = set_smem((const void *)k_assign_l1, AS_SMEM)) != cudaSuccess) return e;
+    if (kmap) {
+        if ((e = set_smem((const void *)k_assign_tc, TC_SMEM)) != cudaSuccess) return e;
+        k_cent_prep<<<dim3(tc_chunks(k_max) * (TC_NC / 8), units), 128, 0, s>>>(jb);
+        k_assign_tc<<<dim3((int)ceil_div64(n_max, TC_M), units), 128, TC_SMEM, s>>>(jb, *kmap);
+        AssignJob jl = jb;
+        jl.rows = jb.rc_list;
+        jl.rows_ustride = jb.fb_ustride;
+        jl.rows_cnt = jb.rc_cnt;
+        const int gx = std::max(1, std::min((int)ceil_div64(n_max, AS_ROWS), 2 * num_sms() / std::max(units, 1)));
+        k_assign_l1<<<dim3(gx, units), AS_THREADS, AS_SMEM, s>>>(jl);
+    } else {
+        AssignJob jf = jb;
+        jf.rows = nullptr;
+        k_assign_l1<<<dim3((int)ceil_div64(n_max, AS_ROWS), units), AS_THREADS, AS_SMEM, s>>>(jf);
+    }
+    k_assign_fallback<<<dim3(16, units), 256, 0, s>>>(jb);
+    return cudaGetLastError();
+}
 
 static size_t l2_smem() { return 3 * MOG_MAX_L * MOG_D * sizeof(float); }
 
@@ -729,11 +1074,12 @@ cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s) {
     const int U = pl.units;
     if (pl.n_mid_max > 0) {
         k_l1_init<<<dim3(pl.c_max, U), 128, 0, s>>>(dv);
-        const int rblocks = (int)ceil_div64(pl.n_mid_max, AS_ROWS);
+        CUtensorMap kmap;
+        const bool tma = key_map(&kmap, dv.K, pl.n_cap, dv.h_kv, pl.batch, dv.sn, dv.sh, dv.sb);
         for (int t = 0; t < pl.T1; ++t) {
             AssignJob jb = build_job(dv, t);
-            k_assign_l1<<<dim3(rblocks, U), AS_THREADS, AS_SMEM, s>>>(jb);
-            k_assign_fallback<<<dim3(16, U), 256, 0, s>>>(jb);
+            if ((e = assign_step(jb, tma ? &kmap : nullptr, U, pl.n_mid_max, pl.c_max, s)) != cudaSuccess)
+                return e;
             k_sort_hist<<<dim3(pl.nchunks, U), 256, pl.c_max * sizeof(int), s>>>(dv, t);
             k_sort_colscan<<<dim3((int)ceil_div64(pl.c_max, 128), U), 128, 0, s>>>(dv, t);
             k_sort_base<<<U, 1024, 0, s>>>(dv, t);
@@ -754,10 +1100,7 @@ cudaError_t launch_stats_only(const Dev &dv, const Plan &pl, cudaStream_t s) {
 }
 
 cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
-                             int32_t *assign, int *changed, int *fb_list, int *fb_cnt,
-                             cudaStream_t s) {
-    cudaError_t e;
-    if ((e = set_smem((const void *)k_assign_l1, AS_SMEM)) != cudaSuccess) return e;
+                             int32_t *assign, const KmScratch &ks, cudaStream_t s) {
     AssignJob jb;
     jb.K = x;
     jb.sb = jb.sh = 0;
@@ -770,17 +1113,26 @@ cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *
     jb.cent_ustride = 0;
     jb.assign = assign;
     jb.assign_ustride = 0;
-    jb.changed = changed;
-    jb.fb_list = fb_list;
+    jb.changed = ks.changed;
+    jb.fb_list = ks.fb_list;
     jb.fb_ustride = 0;
-    jb.fb_cnt = fb_cnt;
+    jb.fb_cnt = ks.fb_cnt;
     jb.t = 0;
     jb.T = 1;
-    if (n > 0) {
-        k_assign_l1<<<dim3((int)ceil_div64(n, AS_ROWS), 1), AS_THREADS, AS_SMEM, s>>>(jb);
-        k_assign_fallback<<<dim3(16, 1), 256, 0, s>>>(jb);
-    }
-    return cudaGetLastError();
+    jb.rows = nullptr;
+    jb.rows_ustride = 0;
+    jb.rows_cnt = nullptr;
+    jb.cimg = ks.cimg;
+    jb.cimg_ustride = 0;
+    jb.cnorm = ks.cnorm;
+    jb.cn_ustride = 0;
+    jb.rc_list = ks.rc_list;
+    jb.rc_cnt = ks.rc_cnt;
+    jb.status = ks.status;
+    if (n <= 0) return cudaSuccess;
+    CUtensorMap kmap;
+    const bool tma = key_map(&kmap, x, n, 1, 1, ld, ld * n, ld * n);
+    return assign_step(jb, tma ? &kmap : nullptr, 1, n, k, s);
 }
 
 cudaError_t launch_assign_segments(const uint16_t *x, int64_t ld, const int32_t *rows,

@@ -118,6 +118,46 @@ def test_l1_assign_bit_exact_qwen3_4b_unit():
     _assign_steps(mid, w.n_clusters, 2)
 
 
+def test_l1_assign_tensor_core_pass_decides_most_rows():
+    """The tensor-core scores decide almost every row of a full 32K-key head; the rest go
+    through the direct fp32 pass (and, if needed, the fp64 rule) and still match."""
+    w = wl.WORKLOADS["qwen3-4b-32k"]
+    K, _, _ = wl.make_unit(w, 0, 5)
+    mid = K[w.n_sink:w.n - w.n_recent]
+    _, _, steps, hist = ora.lloyd(mid, w.n_clusters, 2, history=True)
+    c32 = hist[steps - 1].astype(np.float32)
+    gpu, fb, rc = mog.kmeans_assign(bf(mid), torch.from_numpy(c32).to(DEV), with_recheck=True)
+    assert np.array_equal(gpu.cpu().numpy(), ora.assign(mid, c32.astype(np.float64)))
+    print(f"32K head: {rc} of {mid.shape[0]} rows rechecked, {fb} by the fp64 rule")
+    assert rc < 0.05 * mid.shape[0]
+
+
+def test_l1_assign_bit_exact_many_chunks_ragged_outliers():
+    """More than 256 centroids (several tensor-core groups, the last one ragged), a row
+    count that is not a multiple of the 128-row tile, and keys scaled x4 (large norms)."""
+    g = np.random.default_rng(11)
+    centres = g.standard_normal((700, D))
+    z = g.integers(0, 700, size=3001)
+    X = centres[z] + 0.5 * g.standard_normal((3001, D))
+    X[g.choice(3001, size=30, replace=False)] *= 4.0
+    Xb = wl.to_bf16(X)
+    cent = (centres[:301] + 0.05 * g.standard_normal((301, D))).astype(np.float32)
+    gpu, fb, rc = mog.kmeans_assign(bf(Xb), torch.from_numpy(cent).to(DEV), with_recheck=True)
+    assert np.array_equal(gpu.cpu().numpy(), ora.assign(Xb, cent.astype(np.float64)))
+    assert rc < 3001
+
+
+def test_l1_assign_single_centroid_and_single_row():
+    g = np.random.default_rng(12)
+    X = wl.to_bf16(g.standard_normal((1, D)))
+    cent = g.standard_normal((1, D)).astype(np.float32)
+    gpu, fb = mog.kmeans_assign(bf(X), torch.from_numpy(cent).to(DEV))
+    assert gpu.cpu().numpy().tolist() == [0]
+    cent5 = g.standard_normal((5, D)).astype(np.float32)
+    gpu, fb = mog.kmeans_assign(bf(X), torch.from_numpy(cent5).to(DEV))
+    assert np.array_equal(gpu.cpu().numpy(), ora.assign(X, cent5.astype(np.float64)))
+
+
 def test_l2_segmented_assign_bit_exact():
     w = wl.WORKLOADS["tiny-4k"]
     K, V, _ = wl.make_unit(w)
