@@ -61,10 +61,14 @@ def peaks():
     return 6800.0, "fallback"
 
 
+DECODE_SOURCES = ("attend.cuh", "common.cuh", "decode.cu", "internal.h")
+
+
 def kernel_hash():
+    """Hash of the sources the decode kernels are compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_mog_decode_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DECODE_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
