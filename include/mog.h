@@ -82,7 +82,8 @@ typedef struct mog_params {
 /* A bf16 KV cache in device memory.  Element (b, h, n, j) of K is
  * k[b*stride_b + h*stride_h + n*stride_n + j]; V uses the same strides.  stride_n >= d,
  * all strides multiples of 8 elements (16-byte aligned rows), base pointers 16-byte
- * aligned.  mog_append writes into this cache. */
+ * aligned, and n_cap * stride_n * 2 bytes below 4 GiB (one head's rows are addressed with
+ * 32-bit offsets; MOG_ERR_SHAPE otherwise).  mog_append writes into this cache. */
 typedef struct mog_kv {
     void *k;
     void *v;

@@ -293,7 +293,8 @@ static int check_kv(const mog_kv *kv, int batch, int h_kv, int n_cap) {
     if ((kv->stride_n | kv->stride_b | kv->stride_h) & 7) return MOG_ERR_SHAPE;
     (void)batch;
     (void)h_kv;
-    (void)n_cap;
+    // the attention kernels address a row inside its head's slab with a 32-bit byte offset
+    if ((int64_t)n_cap * kv->stride_n * 2 >= (1LL << 32)) return MOG_ERR_SHAPE;
     return MOG_OK;
 }
 

@@ -77,8 +77,10 @@ __device__ __forceinline__ void issue_tile(uint8_t *stage, int nrows, const uint
         uint32_t mk = 0;
         const bool ok = r < nrows;
         if (ok) posf(r, pos, mk);
-        const uint16_t *ks = kbase + (ok ? pos * sn : 0) + ch * 8;
-        const uint16_t *vs = vbase + (ok ? pos * sn : 0) + ch * 8;
+        // byte offset of the row within its head's slab (< 4 GB: n_cap * row bytes)
+        const uint32_t off = ok ? (uint32_t)pos * (uint32_t)(sn * 2) + ch * 16 : 0u;
+        const uint16_t *ks = reinterpret_cast<const uint16_t *>(reinterpret_cast<const char *>(kbase) + off);
+        const uint16_t *vs = reinterpret_cast<const uint16_t *>(reinterpret_cast<const char *>(vbase) + off);
         cp_async16(sk + swz(r, ch), ks, ok ? 16 : 0);
         cp_async16(sv + swz(r, ch), vs, ok ? 16 : 0);
         if (ch == 0) smask[r] = ok ? mk : 0u;
@@ -136,8 +138,8 @@ __device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
-    const float al0 = mn0 == -INFINITY ? 1.f : exp2f(acc.m[0] - mn0);
-    const float al1 = mn1 == -INFINITY ? 1.f : exp2f(acc.m[1] - mn1);
+    const float al0 = mn0 == -INFINITY ? 1.f : ex2(acc.m[0] - mn0);
+    const float al1 = mn1 == -INFINITY ? 1.f : ex2(acc.m[1] - mn1);
     acc.m[0] = mn0;
     acc.m[1] = mn1;
     float p[2][4];
@@ -146,8 +148,8 @@ __device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa
     for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            p[t][e] = mn0 == -INFINITY ? 0.f : exp2f(s[t][e] - mn0);
-            p[t][e + 2] = mn1 == -INFINITY ? 0.f : exp2f(s[t][e + 2] - mn1);
+            p[t][e] = mn0 == -INFINITY ? 0.f : ex2(s[t][e] - mn0);
+            p[t][e + 2] = mn1 == -INFINITY ? 0.f : ex2(s[t][e + 2] - mn1);
             if (!GIVEN || e == 0) {  // a given term's low-part row adds no weight of its own
                 ps0 += p[t][e];
                 ps1 += p[t][e + 2];
@@ -170,10 +172,10 @@ __device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa
                                {p[1][2], p[1][3]}};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t hb = pack_bf2(v[i][0], v[i][1]);
+            const uint32_t hb = cvt_bf2(v[i][0], v[i][1]);
             ahi[i] = hb;
             const float r0 = v[i][0] - bf_lo(hb), r1 = v[i][1] - bf_hi(hb);
-            alo[i] = pack_bf2(r0, r1);
+            alo[i] = cvt_bf2(r0, r1);
         }
     }
     {

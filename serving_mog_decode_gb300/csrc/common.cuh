@@ -26,6 +26,18 @@ __device__ __forceinline__ uint32_t f2bf(float f) {
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     return f2bf(lo) | (f2bf(hi) << 16);
 }
+// the same with one conversion instruction (round to nearest even, both halves)
+__device__ __forceinline__ uint32_t cvt_bf2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// 2^x by the hardware approximation (flush-to-zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 
 // ------------------------------------------------------------------------------ warp ops
 
