@@ -4,11 +4,12 @@
 // One CTA = 4 warps.  Rows (keys) are copied into shared memory with 16-byte cp.async,
 // three stages deep, in a layout whose 16-byte chunks are XOR-swizzled by (row & 7) so
 // that ldmatrix reads are bank-conflict free.  Warp w owns rows 16w..16w+15 of every
-// tile and keeps its own running (max, sum, output) for the G query heads of the KV head,
-// which sit in the M dimension of an m16n8k16 bf16 mma (rows >= G stay masked).
-//  - logits S = Q K^T: A = Q (bf16, exact), B = K tile, fp32 accumulate;
+// tile and keeps its own running (max, sum, output) for the G query heads of the KV head.
+// The keys sit in the M dimension of an m16n8k16 bf16 mma and the heads in N (8 per
+// block), so no MMA row is padding:
+//  - logits S^T = K Q^T: A = K tile, B = Q^T (bf16, exact), fp32 accumulate;
 //  - weights P = 2^(S*tau*log2e - m), split into bf16 hi + lo parts (16-bit precision)
-//    so the P V product (fp32 accumulate) keeps ~2^-17 relative weight error;
+//    so the product O^T += V^T P^T (fp32 accumulate) keeps ~2^-17 relative weight error;
 //  - a per-row head mask removes heads for which a row is not selected (logit -inf).
 #pragma once
 
@@ -26,33 +27,48 @@ constexpr int AT_STAGE_BYTES = 2 * AT_TILE_BYTES + AT_ROWS * 4;
 constexpr int AT_SMEM = AT_STAGES * AT_STAGE_BYTES;
 constexpr float LOG2E = 1.4426950408889634f;
 
+// Per-warp running state for the G query heads of a KV head, in the transposed layout of
+// the P.V product: O^T (dimensions x heads) = V^T (dimensions x keys) . P^T (keys x heads).
+// NB blocks of 8 heads (N = 8 per mma).  Lane l holds, for head block nb and dimension
+// tile mt (16 dimensions), dimensions mt*16 + l/4 (+8) of heads nb*8 + (l%4)*2 (+1).
+template <int NB>
 struct WarpAcc {
-    float o[16][4];  // output fragment: 16 dim tiles of 8, rows lane/4 and lane/4 + 8
-    float m[2];      // running max (log2 domain) of rows lane/4, lane/4 + 8
-    float l[2];      // this lane's share of the running sum
+    float o[NB][8][4];
+    float m[NB][2];  // running max (log2 domain) of heads nb*8 + (l%4)*2, +1
+    float l[NB][2];  // this lane's share of their running sums
     __device__ __forceinline__ void init() {
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
+        for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[t][e] = 0.f;
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
+            for (int t = 0; t < 8; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[nb][t][e] = 0.f;
+            m[nb][0] = m[nb][1] = -INFINITY;
+            l[nb][0] = l[nb][1] = 0.f;
+        }
     }
 };
 
-// Q as mma A fragments for the 8 k-steps of d = 128; heads >= G are zero.
-__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[8][4], const uint16_t *q, int G) {
+// Q^T as mma B fragments (k = dimensions, n = heads) for the 8 k-steps of d = 128:
+// b[nb][ks] = {Q[h][k0], Q[h][k0+1]}, {Q[h][k0+8], Q[h][k0+9]} with h = nb*8 + l/4,
+// k0 = 16ks + (l%4)*2; heads >= G are zero.
+template <int NB>
+struct QFrags {
+    uint32_t b[NB][8][2];
+};
+template <int NB>
+__device__ __forceinline__ void load_q_frags(QFrags<NB> &qf, const uint16_t *q, int G) {
     const int lane = threadIdx.x & 31;
-    const int h0 = lane >> 2, h1 = h0 + 8, c = (lane & 3) * 2;
-    const uint32_t *q0 = reinterpret_cast<const uint32_t *>(q + h0 * MOG_D);
-    const uint32_t *q1 = reinterpret_cast<const uint32_t *>(q + h1 * MOG_D);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const int k0 = ks * 16 + c;
-        qa[ks][0] = h0 < G ? q0[k0 / 2] : 0u;
-        qa[ks][1] = h1 < G ? q1[k0 / 2] : 0u;
-        qa[ks][2] = h0 < G ? q0[(k0 + 8) / 2] : 0u;
-        qa[ks][3] = h1 < G ? q1[(k0 + 8) / 2] : 0u;
+    for (int nb = 0; nb < NB; ++nb) {
+        const int h = nb * 8 + (lane >> 2);
+        const uint32_t *qr = reinterpret_cast<const uint32_t *>(q + (size_t)h * MOG_D);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int k0 = ks * 16 + (lane & 3) * 2;
+            qf.b[nb][ks][0] = h < G ? qr[k0 / 2] : 0u;
+            qf.b[nb][ks][1] = h < G ? qr[(k0 + 8) / 2] : 0u;
+        }
     }
 }
 
@@ -90,118 +106,111 @@ __device__ __forceinline__ void issue_tile(uint8_t *stage, int nrows, const uint
 // Consume 16 rows (keys) rbase..rbase+15 of a shared-memory K/V block into this warp's
 // accumulator.  sk, sv: shared addresses of the swizzled K and V rows; smask: per-row head
 // masks (bit g set: head g attends to the row).
+//  - logits S^T = K Q^T: keys in M (16), heads in N (8 per block), fp32 accumulate;
+//  - weights P = 2^(S*tau*log2e - m), split into bf16 high + low parts; each 8 x 8 block
+//    is transposed in registers (movmatrix) into the B operand of O^T += V^T P^T.
 // GIVEN: the block holds precomputed terms instead of keys: row pairs (2i, 2i+1) are the
 // bf16 high and low parts of a value vector, and `given` holds their log2-domain logits
 // E[i][16] (16 heads per item), used as they are.
-template <bool GIVEN = false>
-__device__ __forceinline__ void compute_rows16(WarpAcc &acc, const uint32_t (&qa)[8][4],
-                                               uint32_t sk, uint32_t sv, const uint32_t *smask,
-                                               int rbase, float scale2,
-                                               const float *given = nullptr) {
+template <int NB, bool GIVEN = false>
+__device__ __forceinline__ void compute_rows16(WarpAcc<NB> &acc, const QFrags<NB> &qf, uint32_t sk,
+                                               uint32_t sv, const uint32_t *smask, int rbase,
+                                               float scale2, const float *given = nullptr) {
     const int lane = threadIdx.x & 31;
-    float s[2][4];
+    const int mat = lane >> 3, r8 = lane & 7;
+    float s[NB][4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
+    for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s[t][e] = 0.f;
+        for (int e = 0; e < 4; ++e) s[nb][e] = 0.f;
     if (!GIVEN) {
-        const int mat = lane >> 3, r8 = lane & 7;
-        const int key = rbase + (mat >> 1) * 8 + r8;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(sk + swz(key, 2 * ks + (mat & 1)), b0, b1, b2, b3);
-            mma_bf16(s[0], qa[ks], b0, b1);
-            mma_bf16(s[1], qa[ks], b2, b3);
-        }
-    }
-    const int h0 = lane >> 2, h1 = h0 + 8;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int key = rbase + t * 8 + (lane & 3) * 2 + e;
-            const uint32_t mk = smask[key];
-            if (GIVEN) {
-                s[t][e] = ((mk >> h0) & 1u) ? given[(key >> 1) * MOG_MAX_G + h0] : -INFINITY;
-                s[t][e + 2] = ((mk >> h1) & 1u) ? given[(key >> 1) * MOG_MAX_G + h1] : -INFINITY;
-            } else {
-                s[t][e] = ((mk >> h0) & 1u) ? s[t][e] * scale2 : -INFINITY;
-                s[t][e + 2] = ((mk >> h1) & 1u) ? s[t][e + 2] * scale2 : -INFINITY;
-            }
-            mx0 = fmaxf(mx0, s[t][e]);
-            mx1 = fmaxf(mx1, s[t][e + 2]);
-        }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(acc.m[0], mx0), mn1 = fmaxf(acc.m[1], mx1);
-    const float al0 = mn0 == -INFINITY ? 1.f : ex2(acc.m[0] - mn0);
-    const float al1 = mn1 == -INFINITY ? 1.f : ex2(acc.m[1] - mn1);
-    acc.m[0] = mn0;
-    acc.m[1] = mn1;
-    float p[2][4];
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            p[t][e] = mn0 == -INFINITY ? 0.f : ex2(s[t][e] - mn0);
-            p[t][e + 2] = mn1 == -INFINITY ? 0.f : ex2(s[t][e + 2] - mn1);
-            if (!GIVEN || e == 0) {  // a given term's low-part row adds no weight of its own
-                ps0 += p[t][e];
-                ps1 += p[t][e + 2];
-            }
-        }
-    acc.l[0] = acc.l[0] * al0 + ps0;
-    acc.l[1] = acc.l[1] * al1 + ps1;
-    if (al0 != 1.f || al1 != 1.f) {  // the running max moved: rescale the output
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            acc.o[t][0] *= al0;
-            acc.o[t][1] *= al0;
-            acc.o[t][2] *= al1;
-            acc.o[t][3] *= al1;
-        }
-    }
-    uint32_t ahi[4], alo[4];
-    {
-        const float v[4][2] = {{p[0][0], p[0][1]}, {p[0][2], p[0][3]}, {p[1][0], p[1][1]},
-                               {p[1][2], p[1][3]}};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t hb = cvt_bf2(v[i][0], v[i][1]);
-            ahi[i] = hb;
-            const float r0 = v[i][0] - bf_lo(hb), r1 = v[i][1] - bf_hi(hb);
-            alo[i] = cvt_bf2(r0, r1);
-        }
-    }
-    {
-        const int mat = lane >> 3, r8 = lane & 7;
         const int key = rbase + (mat & 1) * 8 + r8;
 #pragma unroll
-        for (int dt = 0; dt < 16; dt += 2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sv + swz(key, dt + (mat >> 1)), b0, b1, b2, b3);
-            mma_bf16(acc.o[dt], ahi, b0, b1);
-            mma_bf16(acc.o[dt], alo, b0, b1);
-            mma_bf16(acc.o[dt + 1], ahi, b2, b3);
-            mma_bf16(acc.o[dt + 1], alo, b2, b3);
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(sk + swz(key, 2 * ks + (mat >> 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_bf16(s[nb], a, qf.b[nb][ks][0], qf.b[nb][ks][1]);
+        }
+    }
+    const int kA = rbase + (lane >> 2), kB = kA + 8;  // this lane's keys
+    const uint32_t mkA = smask[kA], mkB = smask[kB];
+    uint32_t bhi[NB][2], blo[NB][2];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const int hh = nb * 8 + (lane & 3) * 2;  // this lane's heads hh, hh + 1
+        if (GIVEN) {
+            s[nb][0] = ((mkA >> hh) & 1u) ? given[(kA >> 1) * MOG_MAX_G + hh] : -INFINITY;
+            s[nb][1] = ((mkA >> (hh + 1)) & 1u) ? given[(kA >> 1) * MOG_MAX_G + hh + 1] : -INFINITY;
+            s[nb][2] = ((mkB >> hh) & 1u) ? given[(kB >> 1) * MOG_MAX_G + hh] : -INFINITY;
+            s[nb][3] = ((mkB >> (hh + 1)) & 1u) ? given[(kB >> 1) * MOG_MAX_G + hh + 1] : -INFINITY;
+        } else {
+            s[nb][0] = ((mkA >> hh) & 1u) ? s[nb][0] * scale2 : -INFINITY;
+            s[nb][1] = ((mkA >> (hh + 1)) & 1u) ? s[nb][1] * scale2 : -INFINITY;
+            s[nb][2] = ((mkB >> hh) & 1u) ? s[nb][2] * scale2 : -INFINITY;
+            s[nb][3] = ((mkB >> (hh + 1)) & 1u) ? s[nb][3] * scale2 : -INFINITY;
+        }
+        // per-head maximum over the 16 keys: the 8 lanes that share l%4
+        float mx0 = fmaxf(s[nb][0], s[nb][2]), mx1 = fmaxf(s[nb][1], s[nb][3]);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(acc.m[nb][0], mx0), mn1 = fmaxf(acc.m[nb][1], mx1);
+        const float al0 = mn0 == -INFINITY ? 1.f : ex2(acc.m[nb][0] - mn0);
+        const float al1 = mn1 == -INFINITY ? 1.f : ex2(acc.m[nb][1] - mn1);
+        acc.m[nb][0] = mn0;
+        acc.m[nb][1] = mn1;
+        const float p0 = mn0 == -INFINITY ? 0.f : ex2(s[nb][0] - mn0);
+        const float p1 = mn1 == -INFINITY ? 0.f : ex2(s[nb][1] - mn1);
+        const float p2 = mn0 == -INFINITY ? 0.f : ex2(s[nb][2] - mn0);
+        const float p3 = mn1 == -INFINITY ? 0.f : ex2(s[nb][3] - mn1);
+        // a given term's low-part row (odd key) adds no weight of its own
+        const bool wA = !GIVEN || !(kA & 1);
+        acc.l[nb][0] = acc.l[nb][0] * al0 + (wA ? p0 + p2 : 0.f);
+        acc.l[nb][1] = acc.l[nb][1] * al1 + (wA ? p1 + p3 : 0.f);
+        if (al0 != 1.f || al1 != 1.f) {  // the running max moved: rescale the output
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                acc.o[nb][t][0] *= al0;
+                acc.o[nb][t][1] *= al1;
+                acc.o[nb][t][2] *= al0;
+                acc.o[nb][t][3] *= al1;
+            }
+        }
+        const uint32_t hA = cvt_bf2(p0, p1), hB = cvt_bf2(p2, p3);
+        const uint32_t lA = cvt_bf2(p0 - bf_lo(hA), p1 - bf_hi(hA));
+        const uint32_t lB = cvt_bf2(p2 - bf_lo(hB), p3 - bf_hi(hB));
+        bhi[nb][0] = movmatrix_t(hA);
+        bhi[nb][1] = movmatrix_t(hB);
+        blo[nb][0] = movmatrix_t(lA);
+        blo[nb][1] = movmatrix_t(lB);
+    }
+    {
+        const int key = rbase + (mat >> 1) * 8 + r8;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_t(sv + swz(key, 2 * mt + (mat & 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                mma_bf16(acc.o[nb][mt], a, bhi[nb][0], bhi[nb][1]);
+                mma_bf16(acc.o[nb][mt], a, blo[nb][0], blo[nb][1]);
+            }
         }
     }
 }
 
 // Consume one 64-row tile (already in shared memory): warp w takes rows 16w..16w+15.
 // GIVEN: the tile holds precomputed terms whose logits sit at the start of the stage.
-template <bool GIVEN = false>
-__device__ __forceinline__ void compute_tile(WarpAcc &acc, const uint32_t (&qa)[8][4],
+template <int NB, bool GIVEN = false>
+__device__ __forceinline__ void compute_tile(WarpAcc<NB> &acc, const QFrags<NB> &qf,
                                              const uint8_t *stage, float scale2) {
     const uint32_t sk = smem_u32(stage);
-    compute_rows16<GIVEN>(acc, qa, sk, sk + AT_TILE_BYTES,
-                          reinterpret_cast<const uint32_t *>(stage + 2 * AT_TILE_BYTES),
-                          (threadIdx.x >> 5) * 16, scale2, reinterpret_cast<const float *>(stage));
+    compute_rows16<NB, GIVEN>(acc, qf, sk, sk + AT_TILE_BYTES,
+                              reinterpret_cast<const uint32_t *>(stage + 2 * AT_TILE_BYTES),
+                              (threadIdx.x >> 5) * 16, scale2, reinterpret_cast<const float *>(stage));
 }
 
 // Partial result layout: per head, [0] = m (log2 domain), [1] = l, [2], [3] unused,
@@ -210,37 +219,33 @@ constexpr int PART_W = MOG_D + 4;
 constexpr int PART_ACC = 4;
 
 // Write this warp's state for heads < G into st[w][g][PART_W] (shared memory).
-__device__ __forceinline__ void warp_state_out(const WarpAcc &acc, float *st, int G) {
+template <int NB>
+__device__ __forceinline__ void warp_state_out(const WarpAcc<NB> &acc, float *st, int G) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    float l0 = acc.l[0], l1 = acc.l[1];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const int h0 = lane >> 2, h1 = h0 + 8, c = (lane & 3) * 2;
     float *b = st + (size_t)w * G * PART_W;
-    if (h0 < G) {
-        float *r = b + h0 * PART_W;
-        if ((lane & 3) == 0) {
-            r[0] = acc.m[0];
-            r[1] = l0;
-        }
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            r[PART_ACC + t * 8 + c] = acc.o[t][0];
-            r[PART_ACC + t * 8 + c + 1] = acc.o[t][1];
-        }
-    }
-    if (h1 < G) {
-        float *r = b + h1 * PART_W;
-        if ((lane & 3) == 0) {
-            r[0] = acc.m[1];
-            r[1] = l1;
-        }
+    for (int nb = 0; nb < NB; ++nb) {
+        float l0 = acc.l[nb][0], l1 = acc.l[nb][1];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            r[PART_ACC + t * 8 + c] = acc.o[t][2];
-            r[PART_ACC + t * 8 + c + 1] = acc.o[t][3];
+        for (int o = 4; o < 32; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        }
+        const int hh = nb * 8 + (lane & 3) * 2, d0 = lane >> 2;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = hh + e;
+            if (h >= G) continue;
+            float *r = b + h * PART_W;
+            if (d0 == 0) {
+                r[0] = acc.m[nb][e];
+                r[1] = e ? l1 : l0;
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                r[PART_ACC + t * 16 + d0] = acc.o[nb][t][e];
+                r[PART_ACC + t * 16 + d0 + 8] = acc.o[nb][t][e + 2];
+            }
         }
     }
 }

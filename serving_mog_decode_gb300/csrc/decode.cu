@@ -568,8 +568,9 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int b = ui[UI_B], h = u % dv.h_kv;
     const uint32_t allm = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
-    uint32_t qa[8][4];
-    load_q_frags(qa, a.q + (size_t)u * G * MOG_D, G);
+    constexpr int NB = GT <= 8 ? 1 : 2;  // blocks of 8 query heads
+    QFrags<NB> qf;
+    load_q_frags(qf, a.q + (size_t)u * G * MOG_D, G);
     pdl_wait();  // the selection kernel's segments and plan
     pdl_trigger();
     {
@@ -694,7 +695,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
             cp_async16(smem_u32(E + it * MOG_MAX_G + 4 * q), rx + (size_t)(i0 + it) * 4 * G4 + 4 * q, 16);
         }
     };
-    WarpAcc acc;
+    WarpAcc<NB> acc;
     acc.init();
     const float scale2 = dv.tau * LOG2E;
     if (nt > 0) {
@@ -726,7 +727,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
             issue(ti);
         }
         cp_async_commit();
-        compute_tile(acc, qa, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
+        compute_tile(acc, qf, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
         if (next >= 0) fetch(next);
     }
     cp_async_wait<0>();
@@ -742,7 +743,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
         __syncthreads();
         if (t + AT_STAGES - 1 < nr) issue_terms(t + AT_STAGES - 1, t + AT_STAGES - 1);
         cp_async_commit();
-        compute_tile<true>(acc, qa, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
+        compute_tile<NB, true>(acc, qf, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
     }
     cp_async_wait<0>();
     __syncthreads();

@@ -23,6 +23,8 @@ struct DenseArgs {
     float scale2;
 };
 
+// NB: blocks of 8 query heads per KV head (1 for G <= 8, else 2)
+template <int NB>
 __global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
     const int u = blockIdx.y, p = blockIdx.x;
@@ -36,9 +38,9 @@ __global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
     const uint16_t *kb = a.K + b * a.sb + h * a.sh;
     const uint16_t *vb = a.V + b * a.sb + h * a.sh;
     const uint32_t allm = a.G >= 32 ? 0xffffffffu : ((1u << a.G) - 1u);
-    uint32_t qa[8][4];
-    load_q_frags(qa, a.q + ((int64_t)b * a.h_kv * a.G + (int64_t)h * a.G) * MOG_D, a.G);
-    WarpAcc acc;
+    QFrags<NB> qf;
+    load_q_frags(qf, a.q + ((int64_t)b * a.h_kv * a.G + (int64_t)h * a.G) * MOG_D, a.G);
+    WarpAcc<NB> acc;
     acc.init();
     auto issue = [&](int t) {
         const int64_t r0 = lo + (int64_t)t * AT_ROWS;
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
         __syncthreads();
         if (t + AT_STAGES - 1 < nt) issue(t + AT_STAGES - 1);
         cp_async_commit();
-        compute_tile(acc, qa, dsm + (t % AT_STAGES) * AT_STAGE_BYTES, a.scale2);
+        compute_tile(acc, qf, dsm + (t % AT_STAGES) * AT_STAGE_BYTES, a.scale2);
     }
     cp_async_wait<0>();
     __syncthreads();
@@ -91,14 +93,16 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
                          int64_t sn, const int32_t *lengths, int n_max, int batch, int h_kv,
                          int G, const void *q, float *out, float *scratch, int splits,
                          cudaStream_t s) {
-    cudaError_t e = ensure_smem((const void *)k_dense_split, AT_SMEM);
+    const void *split_fn = G <= 8 ? (const void *)k_dense_split<1> : (const void *)k_dense_split<2>;
+    cudaError_t e = ensure_smem(split_fn, AT_SMEM);
     if (e == cudaSuccess) e = ensure_smem((const void *)k_dense_merge, MERGE_SMEM);
     if (e != cudaSuccess) return e;
     DenseArgs a{K, V, sb, sh, sn, lengths, h_kv, G, splits,
                 static_cast<const uint16_t *>(q), out, scratch,
                 (float)(LOG2E / sqrt((double)MOG_D))};
     const int U = batch * h_kv;
-    k_dense_split<<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
+    if (G <= 8) k_dense_split<1><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
+    else k_dense_split<2><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
     k_dense_merge<<<U, MERGE_THREADS, MERGE_SMEM, s>>>(a);
     return cudaGetLastError();
 }
