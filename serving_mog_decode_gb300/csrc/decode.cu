@@ -99,6 +99,9 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
 constexpr int MD_SMEM_MAX = 226 * 1024;
 
 __host__ __device__ constexpr int md_warps(int GT) { return GT <= 4 ? 12 : 8; }
+// CTAs per SM the selection kernel is compiled for (register budget): two for G > 4, so
+// that a batch of many KV heads gets 8-CTA clusters
+__host__ __device__ constexpr int md_min_blocks(int GT) { return GT <= 4 ? 1 : 2; }
 
 // Shared-memory layout of the selection kernel (byte offsets).
 struct MdLay {
@@ -199,7 +202,7 @@ __device__ __forceinline__ int key_rank(const unsigned long long *keys, int n, u
 //  P4  the unit's row segments (one per chosen subcluster, in slot order) and the first
 //      segment of every rows-kernel CTA.
 template <int GT>
-__global__ void __launch_bounds__(md_warps(GT) * 32, 1) k_mog_decode(DecArgs a, MdLay m) {
+__global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_decode(DecArgs a, MdLay m) {
     namespace cg = cooperative_groups;
     constexpr int W = md_warps(GT), NT = W * 32;
     extern __shared__ __align__(128) uint8_t sm[];
