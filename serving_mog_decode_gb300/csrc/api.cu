@@ -122,7 +122,10 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION || P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
     if (slot_smem_bytes(P.G, P.c_max, P.l_max, P.tc) > 226 * 1024) return MOG_ERR_SHAPE;  // decode shared memory
     const int sms = num_sms();
-    P.P = std::max(1, std::min(MAX_SPLITS, 2 * sms / P.units));  // rows kernel: one wave of 2 CTAs/SM
+    // rows kernel: one wave of two CTAs per SM; with so many units that a wave gives each
+    // fewer than four CTAs, four per unit over several waves, which the CTA scheduler
+    // balances across units of different lengths
+    P.P = std::min(MAX_SPLITS, std::max(4, 2 * sms / P.units));
     P.nchunks = std::max(1, (int)ceil_div64(P.n_mid_max, SORT_CHUNK));
     P.sub_off_stride = (P.c_max * P.l_max + 1 + 3) & ~3;
     const int64_t U = P.units, G = P.G, cm = P.c_max, lm = P.l_max, nc = P.n_cap;
