@@ -453,3 +453,70 @@ def test_sixteen_query_heads_per_kv_head():
     inj = Injected(w)
     _check_stats(inj)
     _check_decode(inj)
+
+
+# ------------------------------------------------- full-size heads of the large workloads
+
+class FromBuild:
+    """One KV head of a workload, clustered by the library's own build; the oracle's
+    summaries are recomputed from the partition the GPU chose."""
+
+    def __init__(self, name, steps=0):
+        import dataclasses
+        base = wl.WORKLOADS[name]
+        self.unit = wl.UnitDraw(base, 0, 0, base.n)
+        self.w = dataclasses.replace(base, batch=1, h_kv=1, h_q=base.group)
+        n = base.n
+        self.lens = np.array([n], np.int32)
+        self.n_cap = n + steps
+        K = np.zeros((1, 1, self.n_cap, D), np.uint16)
+        V = np.zeros_like(K)
+        self.unit.keys_values(K[0, 0], V[0, 0])
+        self.K, self.V = K, V
+        self.q = self.unit.q[None].copy()
+        prm = mog.make_params(1, 1, base.group, self.n_cap, n_clusters=base.n_clusters,
+                              n_sub=base.n_sub, top_c=base.top_c, top_s=base.top_s,
+                              n_sink=base.n_sink, n_recent=base.n_recent)
+        self.Kd, self.Vd = bf(K), bf(V)
+        self.h = mog.build(self.Kd, self.Vd, self.lens, prm)
+        Cn, L, nm, S, perm, off = _partition(self.h, 0, n, self.w)
+        s = ora.stats(K[0, 0], V[0, 0], perm, off, Cn, L)
+        s.update(perm=perm, sub_off=off, C=Cn, L=L, n_build=n, S=S, R=base.n_recent)
+        self.summ = {(0, 0): s}
+        self.qd = bf(self.q)
+
+    gpu_summaries = Injected.gpu_summaries
+
+
+def test_full_size_1m_head_build_and_decode():
+    """A 1M-key KV head of the 1M workload (1024 x 20 groups, top 16 x 8, 4 query heads):
+    the GPU's own two-level clustering, its statistics against the oracle's on that
+    partition, the selection and the decode step."""
+    fb = FromBuild("ctx-1m")
+    Cn, L, nm, S, perm, off = _partition(fb.h, 0, fb.lens[0], fb.w)
+    assert np.array_equal(np.sort(perm), np.arange(S, S + nm))
+    worst_s = _check_stats(fb)
+    ties, worst = _check_decode(fb)
+    print(f"1M head: stats worst {worst_s:.2e}, {ties} near-tie heads, decode worst {worst:.2e}")
+
+
+def test_append_64_steps_qwen3_14b_head():
+    """The Qwen3-14B-shaped head (131072 keys, 362 x 17 groups, top 12 x 8, 5 query heads)
+    over 64 decode steps that each append one key and value: appended keys join the
+    recent anchors and every 16th step is checked against the oracle."""
+    steps = 64
+    fb = FromBuild("qwen3-14b-128k", steps=steps)
+    n = int(fb.lens[0])
+    worst = 0.0
+    for t in range(1, steps + 1):
+        kn, vn, qt = fb.unit.step(t)
+        fb.h.append(bf(kn[None, None]), bf(vn[None, None]))
+        fb.K[0, 0, n + t - 1] = kn
+        fb.V[0, 0, n + t - 1] = vn
+        fb.q = qt[None]
+        fb.qd = bf(fb.q)
+        if t % 16 == 0:
+            _, w_t = _check_decode(fb, n_now=[n + t])
+            worst = max(worst, w_t)
+    assert np.array_equal(fb.Kd.view(torch.int16).cpu().numpy().view(np.uint16), fb.K)
+    print(f"64 appending steps: decode worst {worst:.2e}")
