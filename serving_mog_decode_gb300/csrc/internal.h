@@ -14,7 +14,7 @@ enum { UI_C = 0, UI_L, UI_NBUILD, UI_NMID, UI_S, UI_RLO, UI_B, UI_STRIDE = 8 };
 constexpr int SORT_CHUNK = 1024;   // rows per stable-sort chunk (one warp)
 // First-level assignment on the tensor cores: centroids in chunks of KM_CHUNK, each chunk
 // an image of KM_IMG_CHUNK bf16 ({high, low} x two 64-column halves x KM_CHUNK rows).
-constexpr int KM_CHUNK = 256;
+constexpr int KM_CHUNK = 128;
 constexpr int64_t KM_IMG_CHUNK = 4LL * KM_CHUNK * 64;
 constexpr int MAX_SPLITS = 64;     // partials per unit in the exact-attention kernel
 constexpr int PART_SLOTS = MAX_SPLITS;  // partials per unit: one per rows-kernel CTA

@@ -724,14 +724,19 @@ __global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) 
 // approximate centroid b only when every other centroid j has
 //     a_j - f(|k|^2 + |c_j|^2) > a_b + f(|k|^2 + |c_b|^2),
 // which makes b the unique exact argmin; every other key goes to the direct fp32 pass
-// (and from there, if needed, to the exact fp64 rule).
+// (and from there, if needed, to the exact fp64 rule).  The kernel checks the sufficient
+// form  a_2 - f(|k|^2 + max_j |c_j|^2) > a_b + f(|k|^2 + |c_b|^2)  with a_2 the runner-up,
+// so that a key only needs its two best scores.
 // ------------------------------------------------------------------------------------
 constexpr int TC_M = 128;                       // keys per tile (TMEM lanes)
-constexpr int TC_NC = 256;                      // centroids per MMA group (TMEM columns)
+constexpr int TC_NC = KM_CHUNK;                 // centroids per MMA group (TMEM columns)
 constexpr uint32_t TC_A_BYTES = TC_M * 256;     // 128 keys x 128 bf16
-constexpr uint32_t TC_B_HALF = TC_NC * 128;     // 256 rows x 64 bf16 (one 128-byte swizzle column)
+constexpr uint32_t TC_B_HALF = TC_NC * 128;     // TC_NC rows x 64 bf16 (one 128-byte swizzle column)
 constexpr uint32_t TC_B_BYTES = 4 * TC_B_HALF;  // {high, low} x {k 0-63, k 64-127}
-constexpr size_t TC_SMEM = 1024 + TC_A_BYTES + TC_B_BYTES + TC_NC * 4;
+constexpr uint32_t TC_CN_BYTES = MAX_C * 4;     // |c|^2 of every centroid
+constexpr size_t TC_SMEM = 1024 + 2 * TC_A_BYTES + 2 * TC_B_BYTES + TC_CN_BYTES;
+constexpr int TC_EPI = 8;                       // epilogue warps: 4 lane quarters x 2 column halves
+constexpr int TC_THREADS = (TC_EPI + 1) * 32;   // + 1 producer warp
 constexpr float TC_F = 1.0f / 8192.0f;          // 2^-13
 
 __host__ __device__ inline int tc_chunks(int k) { return (k + TC_NC - 1) / TC_NC; }
@@ -774,190 +779,267 @@ __global__ void __launch_bounds__(128) k_cent_prep(AssignJob jb) {
     if (q == 0) jb.cnorm[u * jb.cn_ustride + c] = real ? sq : INFINITY;
 }
 
-// One CTA: 128 keys of one unit against all centroids, 256 at a time.  Thread 0 issues the
-// copies and the MMAs; every thread then reads its key's row of scores from tensor memory.
-__global__ void __launch_bounds__(128, 1) k_assign_tc(AssignJob jb, const __grid_constant__ CUtensorMap kmap) {
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// One CTA: tiles [tile0, tile0 + ntl) of one unit (128 keys each) against all centroids,
+// TC_NC at a time, in a pipeline over (tile, group) steps.  Warp 4 (one lane) is the
+// producer: TMA copies of the keys, bulk copies of the centroid images, the MMAs into one
+// of two tensor-memory accumulators.  Warps 0-3 are the epilogue: thread r reads its key's
+// row of scores, keeps the best centroid and the runner-up bounds, and decides the key.
+// Two key buffers, two centroid buffers and two accumulators let the copies, the MMAs
+// and the epilogue of neighbouring steps overlap.
+__global__ void __launch_bounds__(TC_THREADS, 1) k_assign_tc(AssignJob jb, const __grid_constant__ CUtensorMap kmap,
+                                                             int tiles_per_cta) {
     extern __shared__ uint8_t tc_raw[];
-    __shared__ __align__(8) uint64_t s_bar[2];
+    // barriers: a_full[2], a_free[2], a_kn[2], b_full[2], b_free[2], acc_full[2], acc_free[2], cn
+    __shared__ __align__(8) uint64_t s_bar[15];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_changed, s_base;
-    __shared__ int s_unc[TC_M];
+    __shared__ int s_fail;
     const int u = blockIdx.y;
     const int *chg = jb.changed + (int64_t)u * jb.T;
     if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
     const uint16_t *x;
     int n, k;
     job_unit(jb, u, x, n, k);
-    const int r0 = blockIdx.x * TC_M;
-    if (r0 >= n || k <= 0) return;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int ntile = (n + TC_M - 1) / TC_M;
+    const int tile0 = blockIdx.x * tiles_per_cta;
+    const int ntl = min(tiles_per_cta, ntile - tile0);
+    if (ntl <= 0 || k <= 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t raw = smem_u32(tc_raw);
-    const uint32_t sA = (raw + 1023u) & ~1023u, sB = sA + TC_A_BYTES, sC = sB + TC_B_BYTES;
+    const uint32_t sA = (raw + 1023u) & ~1023u, sB = sA + 2 * TC_A_BYTES, sC = sB + 2 * TC_B_BYTES;
     const float *scn = reinterpret_cast<const float *>(tc_raw + (sC - raw));
-    const uint32_t bar_ld = smem_u32(&s_bar[0]), bar_mma = smem_u32(&s_bar[1]);
-    // TMA coordinates of the tile's first key
-    int cb = 0, ch_ = 0, crow = r0;
+    auto bar = [&](int i) { return smem_u32(&s_bar[i]); };
+    enum { A_FULL = 0, A_FREE = 2, A_KN = 4, B_FULL = 6, B_FREE = 8, ACC_FULL = 10, ACC_FREE = 12, CN = 14 };
+    int cb = 0, ch_ = 0, crow = 0;
     if (jb.unit_info) {
         const int *ui = jb.unit_info + u * UI_STRIDE;
         cb = ui[UI_B];
         ch_ = u % jb.h_kv;
-        crow = ui[UI_S] + r0;
+        crow = ui[UI_S];
     }
+    const int nch = tc_chunks(k);
     if (tid == 0) {
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_mma, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(A_FULL + i), 1);
+            mbar_init(bar(A_FREE + i), 1);
+            mbar_init(bar(A_KN + i), 4);
+            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(B_FREE + i), 1);
+            mbar_init(bar(ACC_FULL + i), 1);
+            mbar_init(bar(ACC_FREE + i), TC_EPI);
+        }
+        mbar_init(bar(CN), 1);
         fence_barrier_init();
-        s_changed = 0;
+        s_fail = 0;
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(&s_tmem), TC_NC);
+        tmem_alloc(smem_u32(&s_tmem), 2 * TC_NC);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint16_t *img = jb.cimg + u * jb.cimg_ustride;
-    const float *cng = jb.cnorm + u * jb.cn_ustride;
-    const int row = r0 + tid;  // this thread's key (TMEM lane tid)
-    float kn = 0.f;
-    float b1 = INFINITY, u1 = INFINITY, l1 = INFINITY, l2 = INFINITY;
-    int i1 = 0x7fffffff, li1 = -1;
-    uint32_t ph_ld = 0, ph_mma = 0;
-    int fail = 0;  // 1: a copy timed out, 2: the MMAs timed out
-    const int nch = tc_chunks(k);
-    for (int ch = 0; ch < nch; ++ch) {
-        const int nreal = min(TC_NC, k - ch * TC_NC);
-        const int ncp = (nreal + 15) & ~15;  // MMA N: a multiple of 16
-        if (tid == 0) {
-            fence_proxy_async();  // earlier generic reads of the buffers precede the copies
-            const uint32_t bbytes = (uint32_t)ncp * 128;
-            mbar_expect_tx(bar_ld, 4 * bbytes + (uint32_t)ncp * 4 + (ch == 0 ? TC_A_BYTES : 0u));
-            if (ch == 0) {
-                tma_load_4d(sA, &kmap, 0, crow, ch_, cb, bar_ld);
-                tma_load_4d(sA + TC_A_BYTES / 2, &kmap, 64, crow, ch_, cb, bar_ld);
+    const int total = ntl * nch;
+
+    if (warp == TC_EPI) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint16_t *img = jb.cimg + u * jb.cimg_ustride;
+            bool ok = true;
+            mbar_expect_tx(bar(CN), (uint32_t)nch * TC_NC * 4);
+            bulk_load(sC, jb.cnorm + u * jb.cn_ustride, (uint32_t)nch * TC_NC * 4, bar(CN));
+            auto load_step = [&](int it) {
+                const int tl = it / nch, c = it - tl * nch;
+                if (c == 0) {
+                    const int a = tl & 1, na = tl >> 1;
+                    if (na >= 1)
+                        ok = ok && mbar_wait(bar(A_FREE + a), (na - 1) & 1) && mbar_wait(bar(A_KN + a), (na - 1) & 1);
+                    if (!ok) return;
+                    fence_proxy_async();
+                    mbar_expect_tx(bar(A_FULL + a), TC_A_BYTES);
+                    const int r0 = crow + (tile0 + tl) * TC_M;
+                    tma_load_4d(sA + a * TC_A_BYTES, &kmap, 0, r0, ch_, cb, bar(A_FULL + a));
+                    tma_load_4d(sA + a * TC_A_BYTES + TC_A_BYTES / 2, &kmap, 64, r0, ch_, cb, bar(A_FULL + a));
+                }
+                const int b = it & 1, nb = it >> 1;
+                if (nb >= 1) ok = ok && mbar_wait(bar(B_FREE + b), (nb - 1) & 1);
+                if (!ok) return;
+                const int nreal = min(TC_NC, k - c * TC_NC), ncp = (nreal + 15) & ~15;
+                const uint32_t bytes = (uint32_t)ncp * 128;
+                fence_proxy_async();
+                mbar_expect_tx(bar(B_FULL + b), 4 * bytes);
+                const uint16_t *cimg = img + (int64_t)c * (TC_B_BYTES / 2);
+                for (int part = 0; part < 4; ++part)
+                    bulk_load(sB + b * TC_B_BYTES + part * TC_B_HALF, cimg + part * (TC_B_HALF / 2), bytes,
+                              bar(B_FULL + b));
+            };
+            load_step(0);
+            for (int it = 0; it < total && ok; ++it) {
+                if (it + 1 < total) load_step(it + 1);
+                const int tl = it / nch, c = it - tl * nch;
+                const int a = tl & 1, na = tl >> 1, b = it & 1, nb = it >> 1, acc = it & 1, nacc = it >> 1;
+                ok = ok && mbar_wait(bar(B_FULL + b), nb & 1);
+                if (c == 0) ok = ok && mbar_wait(bar(A_FULL + a), na & 1);
+                if (nacc >= 1) ok = ok && mbar_wait(bar(ACC_FREE + acc), (nacc - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const int nreal = min(TC_NC, k - c * TC_NC), ncp = (nreal + 15) & ~15;
+                const uint32_t idesc = idesc_bf16_f32(TC_M, ncp);
+                const uint32_t d = tmem + (uint32_t)(acc * TC_NC);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t aoff = a * TC_A_BYTES + (ks >> 2) * (TC_A_BYTES / 2) + (ks & 3) * 32;
+                        const uint32_t boff = b * TC_B_BYTES + (part * 2 + (ks >> 2)) * TC_B_HALF + (ks & 3) * 32;
+                        tc_mma(d, smem_desc_sw128(sA + aoff), smem_desc_sw128(sB + boff), idesc, (part | ks) != 0);
+                    }
+                tc_commit(bar(B_FREE + b));
+                tc_commit(bar(ACC_FULL + acc));
+                if (c == nch - 1) tc_commit(bar(A_FREE + a));
             }
-            const uint16_t *cimg = img + (int64_t)ch * (TC_B_BYTES / 2);
-            for (int part = 0; part < 4; ++part)
-                bulk_load(sB + part * TC_B_HALF, cimg + part * (TC_B_HALF / 2), bbytes, bar_ld);
-            bulk_load(sC, cng + ch * TC_NC, (uint32_t)ncp * 4, bar_ld);
+            if (!ok) atomicExch(&s_fail, 1);
         }
-        if (__syncthreads_or(!mbar_wait(bar_ld, ph_ld))) {
-            fail = 1;
-            break;
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        // warp w: TMEM lanes (keys) 32*(w%4) .. +31, columns of its half w/4 of each group
+        __shared__ float s_xb[TC_M][2];
+        __shared__ int s_xi[TC_M];
+        __shared__ float s_cmax[TC_EPI];
+        const int qw = warp & 3, hw = warp >> 2, r = qw * 32 + lane;
+        bool ok = mbar_wait(bar(CN), 0);
+        float cmax = 0.f;  // max |c|^2 over the unit's centroids
+        if (ok) {
+            for (int c = tid; c < k; c += TC_EPI * 32) cmax = fmaxf(cmax, scn[c]);
+            cmax = warp_max(cmax);
+            if (lane == 0) s_cmax[warp] = cmax;
         }
-        ph_ld ^= 1u;
-        if (ch == 0) {  // this key's |k|^2 from the swizzled tile
-            const uint8_t *ta = tc_raw + (sA - raw);
+        named_sync(1, TC_EPI * 32);
+        cmax = 0.f;
+        for (int w = 0; w < TC_EPI; ++w) cmax = fmaxf(cmax, s_cmax[w]);
+        int chg_w = 0;
+        // every epilogue warp runs every tile's two named barriers, also after a failed wait
+        // (it then skips the work), so that no warp is left waiting at one
+        for (int tl = 0; tl < ntl; ++tl) {
+            const int a = tl & 1, na = tl >> 1;
+            const int row = (tile0 + tl) * TC_M + r;
+            float kn = 0.f;
+            float cb1[4], cb2[4];  // four independent chains (columns j mod 4) for ILP
+            int ci1[4];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(
-                    ta + (q >> 3) * (TC_A_BYTES / 2) + tid * 128 + (((q & 7) ^ (tid & 7)) << 4));
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int z = 0; z < 4; ++z) {
+                cb1[z] = INFINITY;
+                cb2[z] = INFINITY;
+                ci1[z] = 0x7fffffff;
+            }
+            for (int c = 0; c < nch; ++c) {
+                const int it = tl * nch + c, acc = it & 1, nacc = it >> 1;
+                ok = ok && mbar_wait(bar(ACC_FULL + acc), nacc & 1);
+                if (c == 0 && hw == 0) ok = ok && mbar_wait(bar(A_FULL + a), na & 1);
+                if (!ok) continue;
+                tc_fence_after();
+                if (c == 0 && hw == 0) {  // this key's |k|^2 from the swizzled tile, then release it
+                    const uint8_t *ta = tc_raw + (sA + a * TC_A_BYTES - raw);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    kn = __fmaf_rn(bf_lo(ws[i]), bf_lo(ws[i]), kn);
-                    kn = __fmaf_rn(bf_hi(ws[i]), bf_hi(ws[i]), kn);
+                    for (int q = 0; q < 16; ++q) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(
+                            ta + (q >> 3) * (TC_A_BYTES / 2) + r * 128 + (((q & 7) ^ (r & 7)) << 4));
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            kn = __fmaf_rn(bf_lo(ws[i]), bf_lo(ws[i]), kn);
+                            kn = __fmaf_rn(bf_hi(ws[i]), bf_hi(ws[i]), kn);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(A_KN + a));
+                }
+                const int nreal = min(TC_NC, k - c * TC_NC);
+                const int cend = min(nreal, (hw + 1) * (TC_NC / 2));
+                for (int c0 = hw * (TC_NC / 2); c0 < cend; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * TC_NC + c0), v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int cc = c * TC_NC + c0 + j, z = j & 3;
+                        const float ap = c0 + j < nreal ? __fmaf_rn(-2.f, v[j], scn[cc]) : INFINITY;
+                        const bool lt = ap < cb1[z];
+                        cb2[z] = lt ? cb1[z] : fminf(cb2[z], ap);
+                        cb1[z] = lt ? ap : cb1[z];
+                        ci1[z] = lt ? cc : ci1[z];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ACC_FREE + acc));
+            }
+            // the chains, then the two column halves of each key: the two smallest scores and
+            // the index of the smallest (an exact tie leaves the key uncertain, so which
+            // index is kept then does not matter)
+            float b1 = cb1[0], b2 = cb2[0];
+            int i1 = ci1[0];
+#pragma unroll
+            for (int z = 1; z < 4; ++z) {
+                b2 = fminf(fmaxf(b1, cb1[z]), fminf(b2, cb2[z]));
+                if (cb1[z] < b1) {
+                    b1 = cb1[z];
+                    i1 = ci1[z];
                 }
             }
-        }
-        tc_fence_after();
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16_f32(TC_M, ncp);
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t aoff = (ks >> 2) * (TC_A_BYTES / 2) + (ks & 3) * 32;
-                    const uint32_t boff = (part * 2 + (ks >> 2)) * TC_B_HALF + (ks & 3) * 32;
-                    tc_mma(tmem, smem_desc_sw128(sA + aoff), smem_desc_sw128(sB + boff), idesc,
-                           (part | ks) != 0);
+            if (hw == 1) {
+                s_xb[r][0] = b1;
+                s_xb[r][1] = b2;
+                s_xi[r] = i1;
+            }
+            named_sync(1, TC_EPI * 32);
+            if (hw == 0 && ok) {
+                const float ob1 = s_xb[r][0], ob2 = s_xb[r][1];
+                const int oi1 = s_xi[r];
+                const float nb2 = fminf(fmaxf(b1, ob1), fminf(b2, ob2));
+                if (ob1 < b1) {
+                    b1 = ob1;
+                    i1 = oi1;
                 }
-            tc_commit(bar_mma);
-        }
-        if (__syncthreads_or(!mbar_wait(bar_mma, ph_mma))) {
-            fail = 2;
-            break;
-        }
-        ph_mma ^= 1u;
-        tc_fence_after();
-        for (int c0 = 0; c0 < ncp; c0 += 32) {
-            float v[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (c0 + j >= nreal) break;
-                const int c = ch * TC_NC + c0 + j;
-                const float cn = scn[c0 + j];
-                const float ap = cn - 2.f * v[j];
-                const float e = TC_F * (kn + cn);
-                if (ap < b1) {  // ascending c: the first minimum keeps the lowest index
-                    b1 = ap;
-                    i1 = c;
-                    u1 = ap + e;
+                b2 = nb2;
+                const bool certain =
+                    (k == 1) || (b2 - TC_F * (kn + cmax) > b1 + TC_F * (kn + scn[i1]));
+                const bool valid = row < n;
+                int changed = 0;
+                if (valid && certain) {
+                    int *dst = jb.assign + u * jb.assign_ustride + row;
+                    if (*dst != i1) {
+                        *dst = i1;
+                        changed = 1;
+                    }
                 }
-                const float lw = ap - e;
-                if (lw < l1) {
-                    l2 = l1;
-                    l1 = lw;
-                    li1 = c;
-                } else if (lw < l2) {
-                    l2 = lw;
+                chg_w += changed;
+                const uint32_t unc = __ballot_sync(0xffffffffu, valid && !certain);
+                if (unc) {
+                    int base = 0;
+                    if (lane == 0) base = atomicAdd(jb.rc_cnt + u * jb.T + jb.t, __popc(unc));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    if (valid && !certain)
+                        jb.rc_list[u * jb.fb_ustride + base + __popc(unc & lanemask_lt())] = row;
                 }
             }
+            named_sync(1, TC_EPI * 32);
         }
-        tc_fence_before();
-        __syncthreads();  // scores read, operands consumed: the next group may overwrite them
-    }
-    if (fail) {
-        if (tid == 0) flag_error(jb.status, ST_TIMEOUT);
-        // the copy or the MMAs still in flight get a bounded chance to finish
-        if (fail == 1) mbar_wait(bar_ld, ph_ld);
-        else mbar_wait(bar_mma, ph_mma);
+        chg_w = __reduce_add_sync(0xffffffffu, chg_w);
+        if (lane == 0 && chg_w) atomicAdd(jb.changed + u * jb.T + jb.t, chg_w);
+        if (!ok) atomicExch(&s_fail, 1);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, TC_NC);
-    if (fail) return;
-    // decide this key: certain, or left to the direct pass
-    const float comp = (li1 == i1) ? l2 : l1;
-    const bool certain = (k == 1) || (comp > u1);
-    s_unc[tid] = 0;
-    int my_changed = 0;
-    if (row < n) {
-        if (certain) {
-            int *dst = jb.assign + u * jb.assign_ustride + row;
-            if (*dst != i1) {
-                *dst = i1;
-                my_changed = 1;
-            }
-        } else {
-            s_unc[tid] = 1;
-        }
-    }
-    const int wc = __reduce_add_sync(0xffffffffu, my_changed);
-    if ((tid & 31) == 0 && wc) atomicAdd(&s_changed, wc);
-    __syncthreads();
-    if (tid < 32) {
-        int f[4], cnt = 0;
-        uint32_t m[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            f[q] = s_unc[q * 32 + tid];
-            m[q] = __ballot_sync(0xffffffffu, f[q]);
-            cnt += __popc(m[q]);
-        }
-        if (tid == 0) s_base = cnt ? atomicAdd(jb.rc_cnt + u * jb.T + jb.t, cnt) : 0;
-        __syncwarp();
-        int base = s_base;
-        int *rl = jb.rc_list + u * jb.fb_ustride;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (f[q]) rl[base + __popc(m[q] & lanemask_lt())] = r0 + q * 32 + tid;
-            base += __popc(m[q]);
-        }
-        if (tid == 0 && s_changed) atomicAdd(jb.changed + u * jb.T + jb.t, s_changed);
-    }
+    if (s_fail && tid == 0) flag_error(jb.status, ST_TIMEOUT);
+    if (warp == 0) tmem_dealloc(tmem, 2 * TC_NC);
 }
 
 // ------------------------------------------------------------------------------------
@@ -1047,7 +1129,11 @@ static cudaError_t assign_step(const AssignJob &jb, const CUtensorMap *kmap, int
     if (kmap) {
         if ((e = set_smem((const void *)k_assign_tc, TC_SMEM)) != cudaSuccess) return e;
         k_cent_prep<<<dim3(tc_chunks(k_max) * (TC_NC / 8), units), 128, 0, s>>>(jb);
-        k_assign_tc<<<dim3((int)ceil_div64(n_max, TC_M), units), 128, TC_SMEM, s>>>(jb, *kmap);
+        // persistent CTAs: about one per SM, each over a run of its unit's tiles
+        const int ntile = (int)ceil_div64(n_max, TC_M);
+        const int per_unit = std::max(1, num_sms() / std::max(units, 1));
+        const int tpc = (int)ceil_div64(ntile, per_unit);
+        k_assign_tc<<<dim3((int)ceil_div64(ntile, tpc), units), TC_THREADS, TC_SMEM, s>>>(jb, *kmap, tpc);
         AssignJob jl = jb;
         jl.rows = jb.rc_list;
         jl.rows_ustride = jb.fb_ustride;
