@@ -248,8 +248,10 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
     }  // rows of this CTA
 }
 
-// Rows the fp32 pass could not certify: one warp per row, lanes over centroids, the exact
-// fp64 rule; lowest index on ties.
+// Rows the fp32 pass could not certify: one warp per row, lanes over centroids.  Only a
+// centroid whose fp32 distance is within the fp32 error bound of the smallest can be the
+// exact argmin, so the fp32 distances (the same evaluation as the direct pass) pick the
+// candidates and the exact fp64 rule decides among them; lowest index on ties.
 __global__ void k_assign_fallback(AssignJob jb) {
     const int u = blockIdx.y;
     const int *chg = jb.changed + (int64_t)u * jb.T;
@@ -265,9 +267,25 @@ __global__ void k_assign_fallback(AssignJob jb) {
     for (int e = warp; e < cnt; e += nwarps) {
         int r = jb.fb_list[u * jb.fb_ustride + e];
         const uint16_t *xr = x + (int64_t)r * jb.sn;
+        auto dist32 = [&](int c) {  // as in the direct pass: difference, fused square-add
+            const float *cc = cent + (int64_t)c * MOG_D;
+            float acc = 0.f;
+            for (int j = 0; j < MOG_D; ++j) {
+                const float df = __fsub_rn(bf1(xr[j]), cc[j]);
+                acc = __fmaf_rn(df, df, acc);
+            }
+            return acc;
+        };
+        float b32 = INFINITY;
+        for (int c = lane; c < k; c += 32) b32 = fminf(b32, dist32(c));
+        b32 = warp_min(b32);
+        // every centroid whose exact distance can be the smallest (kCertRel is above the
+        // relative fp32 error on each side)
+        const float thr = b32 * (1.f + 2.5f * kCertRel);
         double best = INFINITY;
         int bi = 0x7fffffff;
         for (int c = lane; c < k; c += 32) {
+            if (dist32(c) > thr) continue;
             double dd = exact_dist(xr, cent + (int64_t)c * MOG_D);
             if (dd < best) {
                 best = dd;
