@@ -555,20 +555,79 @@ __global__ void __launch_bounds__(L2_THREADS) k_assign_segments(SegJob jb) {
         jb.assign[m] = assign_small(jb.x + (int64_t)jb.rows[m] * jb.ld, cs, jb.k);
 }
 
-__global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) {
-    extern __shared__ __align__(16) float l2s[];
-    float *cs = l2s;                          // [L][d] centroids
-    float *ks = cs + MOG_MAX_L * MOG_D;       // [L][d] Kahan sums
-    float *kc = ks + MOG_MAX_L * MOG_D;       // [L][d] Kahan compensation
-    __shared__ int cnt[MOG_MAX_L], pref[MOG_MAX_L + 1], fill[MOG_MAX_L];
-    __shared__ int s_changed;
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Row streaming for the per-cluster passes: the rows pos[a..e) of one KV head pass through
+// a ring of L2_NS shared-memory stages of L2_CH rows (keys, and values when with_v), in
+// order, with L2_NS - 1 stages in flight.  `grp` threads (thread ids gt = 0..grp-1) share
+// the ring and synchronise on named barrier `bar`; body(m0, cnt, k, v) sees rows m0..m0+cnt
+// as k[r * d + j], v[r * d + j].
+constexpr int L2_CH = 32;
+constexpr int L2_NS = 3;
+constexpr int L2_ROWB = MOG_D * 2;
+constexpr int L2_RING = L2_NS * 2 * L2_CH * L2_ROWB;  // 48 KB: stages of keys + values
+constexpr int L2_WARPS = L2_THREADS / 32;
+
+template <class Body>
+__device__ __forceinline__ void stream_rows(const Dev &dv, int b, int h, const int *pos, int a,
+                                            int e, bool with_v, uint8_t *ring, int gt, int grp,
+                                            int bar, Body &&body) {
+    const int nch = (e - a + L2_CH - 1) / L2_CH;
+    const int mats = with_v ? 2 : 1;
+    const int stage_bytes = mats * L2_CH * L2_ROWB;
+    auto issue = [&](int ci) {
+        if (ci < nch) {
+            uint8_t *st = ring + (ci % L2_NS) * stage_bytes;
+            const int m0 = a + ci * L2_CH;
+            for (int p = gt; p < mats * L2_CH * 16; p += grp) {
+                const int mat = p / (L2_CH * 16), r = (p >> 4) & (L2_CH - 1), q = p & 15;
+                const int m = m0 + r;
+                const bool ok = m < e;
+                const int64_t ps = pos[ok ? m : a];
+                const uint16_t *src = (mat ? dv.vrow(b, h, ps) : dv.krow(b, h, ps)) + q * 8;
+                cp_async16(smem_u32(st + (mat * L2_CH + r) * L2_ROWB + q * 16), src, ok ? 16 : 0);
+            }
+        }
+        cp_async_commit();
+    };
+    for (int s = 0; s < L2_NS - 1; ++s) issue(s);
+    for (int ci = 0; ci < nch; ++ci) {
+        cp_async_wait<L2_NS - 2>();
+        named_sync(bar, grp);  // chunk ci landed for every thread; chunk ci-1 consumed
+        issue(ci + L2_NS - 1);
+        const uint8_t *st = ring + (ci % L2_NS) * stage_bytes;
+        const int m0 = a + ci * L2_CH;
+        body(m0, min(L2_CH, e - m0), reinterpret_cast<const uint16_t *>(st),
+             reinterpret_cast<const uint16_t *>(st + L2_CH * L2_ROWB));
+    }
+    cp_async_wait<0>();
+    named_sync(bar, grp);  // the ring is free again
+}
+
+// One CTA per (unit, cluster).  With do_kmeans: the second-level Lloyd loop over the
+// cluster's members (position order, strided seeding), then the final stable order by
+// (subcluster, position).  Then the summaries of the cluster and its subclusters.
+// Member rows are read through the shared-memory ring; every mean is an fp32 Kahan sum
+// in (subcluster, position) order, every variance a second pass about that mean.
+__global__ void __launch_bounds__(L2_THREADS, 2) k_l2_stats(Dev dv, int do_kmeans) {
+    extern __shared__ __align__(16) uint8_t l2raw[];
+    float *cs = reinterpret_cast<float *>(l2raw);  // [L][d] centroids, then subcluster key means
+    uint8_t *ring = l2raw + MOG_MAX_L * MOG_D * sizeof(float);
+    __shared__ int cnt[MOG_MAX_L], pref[MOG_MAX_L + 1];
+    __shared__ int whist[L2_WARPS][MOG_MAX_L];
+    __shared__ int s_changed, s_half;
+    __shared__ float s_cm[MOG_D];
     const int u = blockIdx.y, c = blockIdx.x;
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int C = ui[UI_C], L = ui[UI_L];
     if (c >= C) return;
     if (!do_kmeans && *(volatile const int *)dv.status != 0) return;  // rejected partition
     const int b = ui[UI_B], h = u % dv.h_kv;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int j = tid & (MOG_D - 1);
+    const bool upper = tid >= MOG_D;
     int *so = dv.sub_off + u * dv.sub_off_stride;
     int *permF = dv.perm + (int64_t)u * dv.n_cap;
     int lo, n;
@@ -590,10 +649,65 @@ __global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) 
     if (do_kmeans) {
         const int *pA = dv.permA + (int64_t)u * dv.n_cap + lo;
         int *sa = dv.sub_assign + (int64_t)u * dv.n_cap + lo;
+        // Stable order of the members by subcluster into permF[lo, lo + n): warp w scatters
+        // the contiguous member range [w n / W, (w + 1) n / W) after the members of every
+        // earlier subcluster and of its subcluster in earlier warps.  Leaves cnt, pref and
+        // s_half (the subcluster where the member offsets cross n / 2).
+        auto order_members = [&]() {
+            const int m_b = (int)((int64_t)warp * n / L2_WARPS);
+            const int m_e = (int)((int64_t)(warp + 1) * n / L2_WARPS);
+            int *wh = whist[warp];
+            wh[lane] = 0;
+            __syncwarp();
+            for (int m = m_b + lane; m - lane < m_e; m += 32) {
+                const int a = m < m_e ? sa[m] : -1;
+                const uint32_t g = __match_any_sync(0xffffffffu, a);
+                if (a >= 0 && (g & lanemask_lt()) == 0) wh[a] += __popc(g);
+                __syncwarp();
+            }
+            __syncthreads();
+            if (tid < L) {
+                int t = 0;
+                for (int w = 0; w < L2_WARPS; ++w) t += whist[w][tid];
+                cnt[tid] = t;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                pref[0] = 0;
+                int best = 0;
+                for (int l = 0; l < L; ++l) {
+                    pref[l + 1] = pref[l] + cnt[l];
+                    if (abs(2 * pref[l + 1] - n) < abs(2 * pref[best] - n)) best = l + 1;
+                }
+                s_half = best;
+            }
+            __syncthreads();
+            if (tid < L) {
+                int run = pref[tid];
+                for (int w = 0; w < L2_WARPS; ++w) {
+                    const int t = whist[w][tid];
+                    whist[w][tid] = run;
+                    run += t;
+                }
+            }
+            __syncthreads();
+            for (int m = m_b + lane; m - lane < m_e; m += 32) {
+                const int a = m < m_e ? sa[m] : -1;
+                const uint32_t g = __match_any_sync(0xffffffffu, a);
+                const int base = a >= 0 ? wh[a] : 0;
+                __syncwarp();
+                if (a >= 0) {
+                    permF[lo + base + __popc(g & lanemask_lt())] = pA[m];
+                    if ((g & lanemask_lt()) == 0) wh[a] = base + __popc(g);
+                }
+                __syncwarp();
+            }
+            __syncthreads();
+        };
         if (n > 0) {
             for (int e = tid; e < L * MOG_D; e += blockDim.x) {
-                int l = e / MOG_D, j = e % MOG_D;
-                cs[e] = bf1(dv.krow(b, h, pA[(int64_t)l * n / L])[j]);
+                int l = e / MOG_D, jj = e % MOG_D;
+                cs[e] = bf1(dv.krow(b, h, pA[(int64_t)l * n / L])[jj]);
             }
             for (int m = tid; m < n; m += blockDim.x) sa[m] = -1;
         }
@@ -612,121 +726,124 @@ __global__ void __launch_bounds__(L2_THREADS) k_l2_stats(Dev dv, int do_kmeans) 
             __syncthreads();
             if (t > 0 && s_changed == 0) break;
             if (t + 1 == dv.T2) break;
-            // update: thread j owns dimension j, members in position order
-            if (tid < MOG_D) {
-                for (int l = 0; l < L; ++l) {
-                    ks[l * MOG_D + tid] = 0.f;
-                    kc[l * MOG_D + tid] = 0.f;
-                }
-                for (int m = 0; m < n; ++m) {
-                    int a = sa[m];
-                    float v = bf1(dv.krow(b, h, pA[m])[tid]);
-                    float y = __fsub_rn(v, kc[a * MOG_D + tid]);
-                    float s0 = ks[a * MOG_D + tid];
-                    float tt = __fadd_rn(s0, y);
-                    kc[a * MOG_D + tid] = __fsub_rn(__fsub_rn(tt, s0), y);
-                    ks[a * MOG_D + tid] = tt;
-                }
-            }
-            if (tid < MOG_MAX_L) cnt[tid] = 0;
-            __syncthreads();
-            for (int m = tid; m < n; m += blockDim.x) atomicAdd(&cnt[sa[m]], 1);
-            __syncthreads();
-            if (tid < MOG_D)
-                for (int l = 0; l < L; ++l)
-                    if (cnt[l] > 0) cs[l * MOG_D + tid] = ks[l * MOG_D + tid] / (float)cnt[l];
+            // update: each half of the block takes a run of subclusters; thread j of a
+            // half owns dimension j and sums its subclusters' members in position order
+            order_members();
+            const int l_b = upper ? s_half : 0, l_e = upper ? L : s_half;
+            int l = l_b, next = l_b < l_e ? pref[l_b + 1] : n;
+            Kahan acc;
+            acc.init();
+            stream_rows(dv, b, h, permF + lo, pref[l_b], pref[l_e], false,
+                        ring + (upper ? L2_RING / 2 : 0), j, MOG_D, 1 + (int)upper,
+                        [&](int m0, int k, const uint16_t *sk, const uint16_t *) {
+                            for (int r = 0; r < k; ++r) {
+                                while (m0 + r >= next) {
+                                    if (cnt[l] > 0) cs[l * MOG_D + j] = acc.s / (float)cnt[l];
+                                    acc.init();
+                                    ++l;
+                                    next = pref[l + 1];
+                                }
+                                acc.add(bf1(sk[r * MOG_D + j]));
+                            }
+                        });
+            if (pref[l_b] < pref[l_e]) cs[l * MOG_D + j] = acc.s / (float)cnt[l];
             __syncthreads();
         }
         // final order: (subcluster, position), stable
-        if (tid < MOG_MAX_L) cnt[tid] = 0;
-        __syncthreads();
-        for (int m = tid; m < n; m += blockDim.x) atomicAdd(&cnt[sa[m]], 1);
-        __syncthreads();
-        if (tid == 0) {
-            pref[0] = 0;
-            for (int l = 0; l < L; ++l) pref[l + 1] = pref[l] + cnt[l];
-            for (int l = 0; l < L; ++l) {
-                so[c * L + l] = lo + pref[l];
-                fill[l] = 0;
-            }
-            if (c == C - 1) so[C * L] = lo + n;
-        }
-        __syncthreads();
-        if (tid < 32) {
-            for (int m0 = 0; m0 < n; m0 += 32) {
-                int m = m0 + tid;
-                bool valid = m < n;
-                int a = valid ? sa[m] : -1;
-                uint32_t grp = __match_any_sync(0xffffffffu, a);
-                int rank = __popc(grp & lanemask_lt());
-                if (valid) permF[lo + pref[a] + fill[a] + rank] = pA[m];
-                __syncwarp();
-                if (valid && rank == 0) fill[a] += __popc(grp);
-                __syncwarp();
-            }
-        }
+        order_members();
+        if (tid < L) so[c * L + tid] = lo + pref[tid];
+        if (tid == 0 && c == C - 1) so[C * L] = lo + n;
         __syncthreads();
     }
-    // ---------------- summaries: thread j < d on K, thread d + j on V -----------------
+    // ------ summaries.  Pass 1 (keys and values): thread j < d sums key dimension j,
+    // thread d + j value dimension j, per subcluster and over the cluster.  Pass 2 (keys):
+    // thread j the subcluster variances, thread d + j the cluster variance.
     const int *pf = permF + lo;
-    const int j = tid & (MOG_D - 1);
-    const bool isV = tid >= MOG_D;
     const int64_t cg = (int64_t)u * dv.c_max + c;
-    Kahan tot;
-    tot.init();
-    for (int l = 0; l < L; ++l) {
-        // the end of the last subcluster is this cluster's end (the next entry belongs
-        // to the next cluster's CTA)
-        const int g0 = so[c * L + l] - lo, g1 = (l + 1 < L ? so[c * L + l + 1] : lo + n) - lo;
-        const int64_t sg = (int64_t)u * dv.c_max * dv.l_max + (int64_t)c * L + l;
-        Kahan s;
+    const int64_t sg0 = (int64_t)u * dv.c_max * dv.l_max + (int64_t)c * L;
+    // subcluster l spans [g(l), g(l + 1)) of pf; the end of the last one is this
+    // cluster's end (the next entry of the offsets belongs to the next cluster's CTA)
+    auto g_of = [&](int l) { return l < L ? so[c * L + l] - lo : n; };
+    {
+        Kahan s, tot;
         s.init();
-        for (int m = g0; m < g1; ++m) {
-            const uint16_t *row = isV ? dv.vrow(b, h, pf[m]) : dv.krow(b, h, pf[m]);
-            float v = bf1(row[j]);
-            s.add(v);
-            tot.add(v);
-        }
-        const int ng = g1 - g0;
-        const float mean = ng > 0 ? s.s / (float)ng : 0.f;
-        if (isV) {
-            dv.sub_vbar[sg * MOG_D + j] = mean;
-            const uint32_t hi = f2bf(mean);  // bf16 high and low parts, for the decode
-            dv.sub_vhl[sg * 2 * MOG_D + j] = (uint16_t)hi;
-            dv.sub_vhl[sg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(mean - bf1((uint16_t)hi));
-        } else {
-            dv.sub_ms[sg * 2 * MOG_D + j] = mean;
-            Kahan q;
-            q.init();
-            for (int m = g0; m < g1; ++m) {
-                float df = __fsub_rn(bf1(dv.krow(b, h, pf[m])[j]), mean);
-                q.add(__fmul_rn(df, df));
+        tot.init();
+        int l = 0, g_lo = 0, g_hi = g_of(1);
+        auto flush = [&]() {
+            const int ng = g_hi - g_lo;
+            const float mean = ng > 0 ? s.s / (float)ng : 0.f;
+            const int64_t sg = sg0 + l;
+            if (upper) {
+                dv.sub_vbar[sg * MOG_D + j] = mean;
+                const uint32_t hi = f2bf(mean);  // bf16 high and low parts, for the decode
+                dv.sub_vhl[sg * 2 * MOG_D + j] = (uint16_t)hi;
+                dv.sub_vhl[sg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(mean - bf1((uint16_t)hi));
+            } else {
+                dv.sub_ms[sg * 2 * MOG_D + j] = mean;
+                cs[l * MOG_D + j] = mean;
+                if (j == 0) dv.sub_n[sg] = ng;
             }
-            dv.sub_ms[sg * 2 * MOG_D + MOG_D + j] = ng > 0 ? q.s / (float)ng : 0.f;
-            if (j == 0) dv.sub_n[sg] = ng;
+            s.init();
+            ++l;
+            g_lo = g_hi;
+            g_hi = g_of(l + 1);
+        };
+        stream_rows(dv, b, h, pf, 0, n, true, ring, tid, L2_THREADS, 0,
+                    [&](int m0, int k, const uint16_t *sk, const uint16_t *sv) {
+                        const uint16_t *src = upper ? sv : sk;
+                        for (int r = 0; r < k; ++r) {
+                            while (m0 + r >= g_hi) flush();
+                            const float v = bf1(src[r * MOG_D + j]);
+                            s.add(v);
+                            tot.add(v);
+                        }
+                    });
+        while (l < L) flush();
+        const float cmean = n > 0 ? tot.s / (float)n : 0.f;
+        if (upper) {
+            dv.cl_vbar[cg * MOG_D + j] = cmean;
+            const uint32_t hi = f2bf(cmean);
+            dv.cl_vhl[cg * 2 * MOG_D + j] = (uint16_t)hi;
+            dv.cl_vhl[cg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(cmean - bf1((uint16_t)hi));
+        } else {
+            dv.cl_ms[cg * 2 * MOG_D + j] = cmean;
+            s_cm[j] = cmean;
+            if (j == 0) dv.cl_n[cg] = n;
         }
     }
-    const float cmean = n > 0 ? tot.s / (float)n : 0.f;
-    if (isV) {
-        dv.cl_vbar[cg * MOG_D + j] = cmean;
-        const uint32_t hi = f2bf(cmean);
-        dv.cl_vhl[cg * 2 * MOG_D + j] = (uint16_t)hi;
-        dv.cl_vhl[cg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(cmean - bf1((uint16_t)hi));
-        // cluster variance (keys), computed by the V threads in parallel with the K threads
-        Kahan s;
-        s.init();
-        for (int m = 0; m < n; ++m) s.add(bf1(dv.krow(b, h, pf[m])[j]));
-        const float km = n > 0 ? s.s / (float)n : 0.f;
+    __syncthreads();
+    {
         Kahan q;
         q.init();
-        for (int m = 0; m < n; ++m) {
-            float df = __fsub_rn(bf1(dv.krow(b, h, pf[m])[j]), km);
-            q.add(__fmul_rn(df, df));
+        int l = 0, g_lo = 0, g_hi = g_of(1);
+        auto flush = [&]() {
+            const int ng = g_hi - g_lo;
+            if (!upper) dv.sub_ms[(sg0 + l) * 2 * MOG_D + MOG_D + j] = ng > 0 ? q.s / (float)ng : 0.f;
+            q.init();
+            ++l;
+            g_lo = g_hi;
+            g_hi = g_of(l + 1);
+        };
+        const float cm = s_cm[j];
+        stream_rows(dv, b, h, pf, 0, n, false, ring, tid, L2_THREADS, 0,
+                    [&](int m0, int k, const uint16_t *sk, const uint16_t *) {
+                        for (int r = 0; r < k; ++r) {
+                            const float x = bf1(sk[r * MOG_D + j]);
+                            if (upper) {
+                                const float df = __fsub_rn(x, cm);
+                                q.add(__fmul_rn(df, df));
+                            } else {
+                                while (m0 + r >= g_hi) flush();
+                                const float df = __fsub_rn(x, cs[l * MOG_D + j]);
+                                q.add(__fmul_rn(df, df));
+                            }
+                        }
+                    });
+        if (upper) {
+            dv.cl_ms[cg * 2 * MOG_D + MOG_D + j] = n > 0 ? q.s / (float)n : 0.f;
+        } else {
+            while (l < L) flush();
         }
-        dv.cl_ms[cg * 2 * MOG_D + MOG_D + j] = n > 0 ? q.s / (float)n : 0.f;
-    } else {
-        dv.cl_ms[cg * 2 * MOG_D + j] = cmean;
-        if (j == 0) dv.cl_n[cg] = n;
     }
 }
 
@@ -795,10 +912,6 @@ __global__ void __launch_bounds__(128) k_cent_prep(AssignJob jb) {
     *reinterpret_cast<uint4 *>(img + (1 * 2 + half) * (TC_B_HALF / 2) + r * 64 + pos * 8) =
         make_uint4(lo[0], lo[1], lo[2], lo[3]);
     if (q == 0) jb.cnorm[u * jb.cn_ustride + c] = real ? sq : INFINITY;
-}
-
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -1167,7 +1280,7 @@ static cudaError_t assign_step(const AssignJob &jb, const CUtensorMap *kmap, int
     return cudaGetLastError();
 }
 
-static size_t l2_smem() { return 3 * MOG_MAX_L * MOG_D * sizeof(float); }
+static size_t l2_smem() { return MOG_MAX_L * MOG_D * sizeof(float) + L2_RING; }
 
 cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s) {
     cudaError_t e;
