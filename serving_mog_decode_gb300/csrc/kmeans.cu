@@ -28,6 +28,9 @@ namespace mog {
 
 // relative error bound of the fp32 distance, with a safety factor of ~3 over (d+2)*2^-24
 constexpr float kCertRel = 2.5e-5f;
+// error factor of the tensor-core distances |c|^2 - 2 k.c (split-bf16 centroids, fp32
+// accumulate): a score within TC_F (|k|^2 + |c|^2) of the exact one, with a safety margin
+constexpr float TC_F = 1.0f / 8192.0f;  // 2^-13
 
 __device__ __forceinline__ bool certified(float b1, float b2) {
     // true minimum is b1's centroid for every rounding within the bound
@@ -250,9 +253,14 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
 
 // Rows the fp32 pass could not certify: one warp per row, lanes over centroids.  Only a
 // centroid whose fp32 distance is within the fp32 error bound of the smallest can be the
-// exact argmin, so the fp32 distances (the same evaluation as the direct pass) pick the
-// candidates and the exact fp64 rule decides among them; lowest index on ties.
-__global__ void k_assign_fallback(AssignJob jb) {
+// exact argmin, so fp32 distances pick the candidates and the exact fp64 rule decides
+// among them; lowest index on ties.  The row is staged as fp32 in shared memory and read
+// by broadcast; each lane streams its centroids with 16-byte loads when they are aligned.
+constexpr int FB_THREADS = 256;
+constexpr int FB_CTAS = 64;  // CTAs per unit
+
+__global__ void __launch_bounds__(FB_THREADS) k_assign_fallback(AssignJob jb) {
+    __shared__ __align__(16) float xs_all[FB_THREADS / 32][MOG_D];
     const int u = blockIdx.y;
     const int *chg = jb.changed + (int64_t)u * jb.T;
     if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
@@ -261,18 +269,42 @@ __global__ void k_assign_fallback(AssignJob jb) {
     job_unit(jb, u, x, n, k);
     const int cnt = jb.fb_cnt[u * jb.T + jb.t];
     const float *cent = jb.cent + u * jb.cent_ustride;
+    const bool vec = (reinterpret_cast<uintptr_t>(cent) & 15) == 0;
     const int lane = threadIdx.x & 31;
+    float *xs = xs_all[threadIdx.x >> 5];
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int e = warp; e < cnt; e += nwarps) {
         int r = jb.fb_list[u * jb.fb_ustride + e];
         const uint16_t *xr = x + (int64_t)r * jb.sn;
-        auto dist32 = [&](int c) {  // as in the direct pass: difference, fused square-add
+        __syncwarp();
+        for (int jj = lane; jj < MOG_D; jj += 32) xs[jj] = bf1(xr[jj]);
+        __syncwarp();
+        // fp32 distance in index order: difference, fused square-add
+        auto dist32 = [&](int c) {
             const float *cc = cent + (int64_t)c * MOG_D;
             float acc = 0.f;
-            for (int j = 0; j < MOG_D; ++j) {
-                const float df = __fsub_rn(bf1(xr[j]), cc[j]);
-                acc = __fmaf_rn(df, df, acc);
+            if (vec) {
+                const float4 *c4 = reinterpret_cast<const float4 *>(cc);
+                const float4 *x4 = reinterpret_cast<const float4 *>(xs);
+#pragma unroll 8
+                for (int v = 0; v < MOG_D / 4; ++v) {
+                    const float4 cv = __ldg(c4 + v), xv = x4[v];
+                    float df = __fsub_rn(xv.x, cv.x);
+                    acc = __fmaf_rn(df, df, acc);
+                    df = __fsub_rn(xv.y, cv.y);
+                    acc = __fmaf_rn(df, df, acc);
+                    df = __fsub_rn(xv.z, cv.z);
+                    acc = __fmaf_rn(df, df, acc);
+                    df = __fsub_rn(xv.w, cv.w);
+                    acc = __fmaf_rn(df, df, acc);
+                }
+            } else {
+#pragma unroll 8
+                for (int jj = 0; jj < MOG_D; ++jj) {
+                    const float df = __fsub_rn(xs[jj], __ldg(cc + jj));
+                    acc = __fmaf_rn(df, df, acc);
+                }
             }
             return acc;
         };
@@ -489,29 +521,34 @@ __global__ void k_l1_init(Dev dv) {
 // Second level + summaries, one CTA per (unit, cluster).
 // ------------------------------------------------------------------------------------
 
-// One assignment of row x (bf16, 128) among k centroids cs[k][d] in shared memory.
+// One assignment of row x (bf16, 128) among k centroids cs[k][d] in shared memory: the
+// direct fp32 distance in index order with its certificate; when it fails, the exact fp64
+// rule over the centroids whose fp32 distance is within the fp32 error bound of the
+// smallest (no other centroid can be the exact argmin; fp64 is slow on this GPU).
+// The row is re-read (L1-resident) for each centroid rather than held in registers.
 __device__ __forceinline__ int assign_small(const uint16_t *x, const float *cs, int k) {
-    uint32_t w[64];
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+    auto dist32 = [&](int l) {
+        const float *c = cs + l * MOG_D;
+        float acc = 0.f;
+#pragma unroll 4
+        for (int q = 0; q < 16; ++q) {
+            const uint4 v = xv[q];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        uint4 v = *reinterpret_cast<const uint4 *>(x + q * 8);
-        w[4 * q] = v.x;
-        w[4 * q + 1] = v.y;
-        w[4 * q + 2] = v.z;
-        w[4 * q + 3] = v.w;
-    }
+            for (int e = 0; e < 4; ++e) {
+                float d0 = __fsub_rn(bf_lo(w[e]), c[8 * q + 2 * e]);
+                acc = __fmaf_rn(d0, d0, acc);
+                float d1 = __fsub_rn(bf_hi(w[e]), c[8 * q + 2 * e + 1]);
+                acc = __fmaf_rn(d1, d1, acc);
+            }
+        }
+        return acc;
+    };
     float b1 = INFINITY, b2 = INFINITY;
     int i1 = 0;
     for (int l = 0; l < k; ++l) {
-        const float *c = cs + l * MOG_D;
-        float acc = 0.f;
-#pragma unroll
-        for (int q = 0; q < 64; ++q) {
-            float d0 = __fsub_rn(bf_lo(w[q]), c[2 * q]);
-            acc = __fmaf_rn(d0, d0, acc);
-            float d1 = __fsub_rn(bf_hi(w[q]), c[2 * q + 1]);
-            acc = __fmaf_rn(d1, d1, acc);
-        }
+        const float acc = dist32(l);
         if (acc < b1) {
             b2 = b1;
             b1 = acc;
@@ -521,9 +558,11 @@ __device__ __forceinline__ int assign_small(const uint16_t *x, const float *cs, 
         }
     }
     if (k == 1 || certified(b1, b2)) return i1;
+    const float thr = b1 * (1.f + 2.5f * kCertRel);
     double best = INFINITY;
     int bi = 0;
     for (int l = 0; l < k; ++l) {
+        if (dist32(l) > thr) continue;
         double dd = exact_dist(x, cs + l * MOG_D);
         if (dd < best) {
             best = dd;
@@ -531,6 +570,168 @@ __device__ __forceinline__ int assign_small(const uint16_t *x, const float *cs, 
         }
     }
     return bi;
+}
+
+constexpr int L2_THREADS = 256;
+constexpr int L2_WARPS = L2_THREADS / 32;
+constexpr int L2_CST = 160;  // bf16 row stride of the centroid images (320 B)
+
+// Second-level assignment of n rows (row(m), m < n) among the k <= 32 centroids cs[k][d]
+// (fp32, shared memory), by the whole block.  The approximate distance |c|^2 - 2 k.c is
+// computed with mma.sync (keys bf16; centroids split into bf16 high + low parts; fp32
+// accumulate) and a row keeps its best centroid when it passes the same certificate as
+// the first-level tensor-core pass; the other rows take assign_small.  `img` (20 KB of
+// shared memory) receives the centroid images, s_cn[32] the squared norms.  sa[m] holds
+// the previous assignment (-1 if none) and receives the new one; returns this thread's
+// count of changed rows.
+//
+// Fragment layout: k-step pair p (dimensions 32p..32p+31) is read as one 16-byte word
+// group per thread (words 16p + 4q .. +3, q = lane % 4) of both the key rows and the
+// centroid images; words 0-1 feed the even k-step and 2-3 the odd one, with the MMA's
+// logical pairs q and q + 4 on the first and second word.  Keys and centroids use the
+// same map, so the dot products are those of the rows.
+template <class RowFn>
+__device__ int l2_assign(RowFn row, int *sa, int n, int k, const float *cs, uint8_t *img,
+                         float *s_cn) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t *chi = reinterpret_cast<uint32_t *>(img);
+    uint32_t *clo = chi + MOG_MAX_L * L2_CST / 2;
+    for (int e = tid; e < MOG_MAX_L * MOG_D / 2; e += L2_THREADS) {
+        const int l = e >> 6, p = e & 63;
+        float c0 = 0.f, c1 = 0.f;
+        if (l < k) {
+            c0 = cs[l * MOG_D + 2 * p];
+            c1 = cs[l * MOG_D + 2 * p + 1];
+        }
+        const uint32_t hi = cvt_bf2(c0, c1);
+        chi[l * (L2_CST / 2) + p] = hi;
+        clo[l * (L2_CST / 2) + p] = cvt_bf2(__fsub_rn(c0, bf_lo(hi)), __fsub_rn(c1, bf_hi(hi)));
+    }
+    for (int l = warp; l < MOG_MAX_L; l += L2_WARPS) {
+        float s2 = 0.f;
+        if (l < k)
+            for (int jj = lane; jj < MOG_D; jj += 32) s2 = __fmaf_rn(cs[l * MOG_D + jj], cs[l * MOG_D + jj], s2);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        if (lane == 0) s_cn[l] = l < k ? s2 : INFINITY;
+    }
+    __syncthreads();
+    float cmax = 0.f;
+    for (int l = 0; l < k; ++l) cmax = fmaxf(cmax, s_cn[l]);
+    const int g = lane >> 2, q = lane & 3;
+    const int NT = (k + 7) >> 3;
+    int my = 0;
+    for (int tile = warp; tile * 16 < n; tile += L2_WARPS) {
+        const int m0 = tile * 16 + g, m1 = m0 + 8;
+        const uint4 *p0 = reinterpret_cast<const uint4 *>(row(min(m0, n - 1)));
+        const uint4 *p1 = reinterpret_cast<const uint4 *>(row(min(m1, n - 1)));
+        uint4 x0[4], x1[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            x0[p] = p0[4 * p + q];
+            x1[p] = p1[4 * p + q];
+        }
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t ae[4] = {x0[p].x, x1[p].x, x0[p].y, x1[p].y};
+            const uint32_t ao[4] = {x0[p].z, x1[p].z, x0[p].w, x1[p].w};
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                if (nt < NT) {
+                    const int off = (nt * 8 + g) * (L2_CST / 2) + 16 * p + 4 * q;
+                    const uint4 bh = *reinterpret_cast<const uint4 *>(chi + off);
+                    const uint4 bl = *reinterpret_cast<const uint4 *>(clo + off);
+                    mma_bf16(acc[nt], ae, bh.x, bh.y);
+                    mma_bf16(acc[nt], ae, bl.x, bl.y);
+                    mma_bf16(acc[nt], ao, bh.z, bh.w);
+                    mma_bf16(acc[nt], ao, bl.z, bl.w);
+                }
+            }
+        }
+        // |k|^2 of both rows (fp32)
+        float kn[2] = {0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t w0[4] = {x0[p].x, x0[p].y, x0[p].z, x0[p].w};
+            const uint32_t w1[4] = {x1[p].x, x1[p].y, x1[p].z, x1[p].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                kn[0] = __fmaf_rn(bf_lo(w0[e]), bf_lo(w0[e]), kn[0]);
+                kn[0] = __fmaf_rn(bf_hi(w0[e]), bf_hi(w0[e]), kn[0]);
+                kn[1] = __fmaf_rn(bf_lo(w1[e]), bf_lo(w1[e]), kn[1]);
+                kn[1] = __fmaf_rn(bf_hi(w1[e]), bf_hi(w1[e]), kn[1]);
+            }
+        }
+        float b1[2] = {INFINITY, INFINITY}, b2[2] = {INFINITY, INFINITY};
+        int i1[2] = {0, 0};
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            if (nt < NT) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = e >> 1, col = nt * 8 + 2 * q + (e & 1);
+                    const float a = __fmaf_rn(-2.f, acc[nt][e], s_cn[col]);
+                    if (a < b1[r]) {
+                        b2[r] = b1[r];
+                        b1[r] = a;
+                        i1[r] = col;
+                    } else if (a < b2[r]) {
+                        b2[r] = a;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                const float ob1 = __shfl_xor_sync(0xffffffffu, b1[r], o);
+                const float ob2 = __shfl_xor_sync(0xffffffffu, b2[r], o);
+                const int oi = __shfl_xor_sync(0xffffffffu, i1[r], o);
+                if (ob1 < b1[r] || (ob1 == b1[r] && oi < i1[r])) {
+                    b2[r] = fminf(b1[r], ob2);
+                    b1[r] = ob1;
+                    i1[r] = oi;
+                } else {
+                    b2[r] = fminf(b2[r], ob1);
+                }
+            }
+            kn[r] += __shfl_xor_sync(0xffffffffu, kn[r], 1);
+            kn[r] += __shfl_xor_sync(0xffffffffu, kn[r], 2);
+        }
+        if (q == 0) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int m = r ? m1 : m0;
+                if (m < n) {
+                    const bool cert = k == 1 || (b2[r] - TC_F * (kn[r] + cmax) >
+                                                 b1[r] + TC_F * (kn[r] + s_cn[i1[r]]));
+                    const int old = sa[m];
+                    if (!cert) {
+                        sa[m] = old - 64;  // undecided: the exact pass below
+                    } else if (i1[r] != old) {
+                        sa[m] = i1[r];
+                        ++my;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int m = tid; m < n; m += L2_THREADS) {
+        const int v = sa[m];
+        if (v < -32) {
+            const int a = assign_small(row(m), cs, k);
+            sa[m] = a;
+            my += a != v + 64;
+        }
+    }
+    return my;
 }
 
 struct SegJob {  // standalone segmented assignment (parity export)
@@ -542,17 +743,21 @@ struct SegJob {  // standalone segmented assignment (parity export)
     int32_t *assign;
 };
 
-constexpr int L2_THREADS = 256;
-
+// One CTA per segment: the segment's rows against its own k centroids, by l2_assign.
 __global__ void __launch_bounds__(L2_THREADS) k_assign_segments(SegJob jb) {
-    __shared__ __align__(16) float cs[MOG_MAX_L * MOG_D];
+    extern __shared__ __align__(16) uint8_t segraw[];
+    float *cs = reinterpret_cast<float *>(segraw);
+    uint8_t *img = segraw + MOG_MAX_L * MOG_D * sizeof(float);
+    __shared__ float s_cn[MOG_MAX_L];
     const int s = blockIdx.x;
-    const int lo = jb.seg_off[s], hi = jb.seg_off[s + 1];
+    const int lo = jb.seg_off[s], n = jb.seg_off[s + 1] - lo;
     for (int e = threadIdx.x; e < jb.k * MOG_D; e += blockDim.x)
         cs[e] = jb.cent[(int64_t)s * jb.k * MOG_D + e];
+    int32_t *sa = jb.assign + lo;
+    for (int m = threadIdx.x; m < n; m += blockDim.x) sa[m] = -1;
     __syncthreads();
-    for (int m = lo + threadIdx.x; m < hi; m += blockDim.x)
-        jb.assign[m] = assign_small(jb.x + (int64_t)jb.rows[m] * jb.ld, cs, jb.k);
+    const int32_t *rows = jb.rows + lo;
+    l2_assign([&](int m) { return jb.x + (int64_t)rows[m] * jb.ld; }, sa, n, jb.k, cs, img, s_cn);
 }
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
@@ -568,7 +773,6 @@ constexpr int L2_CH = 32;
 constexpr int L2_NS = 3;
 constexpr int L2_ROWB = MOG_D * 2;
 constexpr int L2_RING = L2_NS * 2 * L2_CH * L2_ROWB;  // 48 KB: stages of keys + values
-constexpr int L2_WARPS = L2_THREADS / 32;
 
 template <class Body>
 __device__ __forceinline__ void stream_rows(const Dev &dv, int b, int h, const int *pos, int a,
@@ -611,14 +815,14 @@ __device__ __forceinline__ void stream_rows(const Dev &dv, int b, int h, const i
 // (subcluster, position).  Then the summaries of the cluster and its subclusters.
 // Member rows are read through the shared-memory ring; every mean is an fp32 Kahan sum
 // in (subcluster, position) order, every variance a second pass about that mean.
-__global__ void __launch_bounds__(L2_THREADS, 2) k_l2_stats(Dev dv, int do_kmeans) {
+__global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmeans) {
     extern __shared__ __align__(16) uint8_t l2raw[];
     float *cs = reinterpret_cast<float *>(l2raw);  // [L][d] centroids, then subcluster key means
     uint8_t *ring = l2raw + MOG_MAX_L * MOG_D * sizeof(float);
     __shared__ int cnt[MOG_MAX_L], pref[MOG_MAX_L + 1];
     __shared__ int whist[L2_WARPS][MOG_MAX_L];
     __shared__ int s_changed, s_half;
-    __shared__ float s_cm[MOG_D];
+    __shared__ float s_cm[MOG_D], s_cn[MOG_MAX_L];
     const int u = blockIdx.y, c = blockIdx.x;
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int C = ui[UI_C], L = ui[UI_L];
@@ -714,14 +918,8 @@ __global__ void __launch_bounds__(L2_THREADS, 2) k_l2_stats(Dev dv, int do_kmean
         for (int t = 0; t < dv.T2 && n > 0; ++t) {
             if (tid == 0) s_changed = 0;
             __syncthreads();
-            int my = 0;
-            for (int m = tid; m < n; m += blockDim.x) {
-                int a = assign_small(dv.krow(b, h, pA[m]), cs, L);
-                if (a != sa[m]) {
-                    sa[m] = a;
-                    ++my;
-                }
-            }
+            const int my = l2_assign([&](int m) { return dv.krow(b, h, pA[m]); }, sa, n, L, cs,
+                                     ring, s_cn);
             if (my) atomicAdd(&s_changed, my);
             __syncthreads();
             if (t > 0 && s_changed == 0) break;
@@ -872,7 +1070,6 @@ constexpr uint32_t TC_CN_BYTES = MAX_C * 4;     // |c|^2 of every centroid
 constexpr size_t TC_SMEM = 1024 + 2 * TC_A_BYTES + 2 * TC_B_BYTES + TC_CN_BYTES;
 constexpr int TC_EPI = 8;                       // epilogue warps: 4 lane quarters x 2 column halves
 constexpr int TC_THREADS = (TC_EPI + 1) * 32;   // + 1 producer warp
-constexpr float TC_F = 1.0f / 8192.0f;          // 2^-13
 
 __host__ __device__ inline int tc_chunks(int k) { return (k + TC_NC - 1) / TC_NC; }
 
@@ -1276,7 +1473,7 @@ static cudaError_t assign_step(const AssignJob &jb, const CUtensorMap *kmap, int
         jf.rows = nullptr;
         k_assign_l1<<<dim3((int)ceil_div64(n_max, AS_ROWS), units), AS_THREADS, AS_SMEM, s>>>(jf);
     }
-    k_assign_fallback<<<dim3(16, units), 256, 0, s>>>(jb);
+    k_assign_fallback<<<dim3(FB_CTAS, units), FB_THREADS, 0, s>>>(jb);
     return cudaGetLastError();
 }
 
@@ -1356,7 +1553,11 @@ cudaError_t launch_assign_segments(const uint16_t *x, int64_t ld, const int32_t 
                                    const int32_t *seg_off, int n_seg, const float *cent, int k,
                                    int32_t *assign, cudaStream_t s) {
     SegJob jb{x, ld, rows, seg_off, cent, k, assign};
-    if (n_seg > 0) k_assign_segments<<<n_seg, L2_THREADS, 0, s>>>(jb);
+    cudaError_t e;
+    if (n_seg > 0) {
+        if ((e = set_smem((const void *)k_assign_segments, l2_smem())) != cudaSuccess) return e;
+        k_assign_segments<<<n_seg, L2_THREADS, l2_smem(), s>>>(jb);
+    }
     return cudaGetLastError();
 }
 
