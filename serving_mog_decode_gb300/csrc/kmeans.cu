@@ -1050,10 +1050,12 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
 //
 // The approximate distance of key k to centroid c (up to |k|^2, equal for every c) is
 //     a_c = |c|^2 - 2 k.c,   k.c = k.c_hi + k.c_lo   (c split into bf16 high + low parts),
-// computed for 128 keys x 256 centroids per MMA group, fp32 accumulate in tensor memory.
+// computed for 128 keys x 128 centroids per MMA group, fp32 accumulate in tensor memory.
 // Its error against the exact D(k, c) - |k|^2 is below 2^-14.5 (|k|^2 + |c|^2): the split
 // leaves 2^-18 |c_j| per element, the fp32 sums add at most 2^-23 per term over 256
-// terms, |c|^2 is an fp32 sum of 128 squares.  With f = 2^-13 a key keeps its best
+// terms, |c|^2 is an fp32 sum of 128 squares.  The epilogue writes the column (0..63)
+// into the low six mantissa bits of each score, which moves it by at most 2^-17 |a_c|
+// <= 2^-16 (|k|^2 + |c|^2), below 2^-14 (|k|^2 + |c|^2) in all.  With f = 2^-13 a key keeps its best
 // approximate centroid b only when every other centroid j has
 //     a_j - f(|k|^2 + |c_j|^2) > a_b + f(|k|^2 + |c_b|^2),
 // which makes b the unique exact argmin; every other key goes to the direct fp32 pass
@@ -1070,6 +1072,7 @@ constexpr uint32_t TC_CN_BYTES = MAX_C * 4;     // |c|^2 of every centroid
 constexpr size_t TC_SMEM = 1024 + 2 * TC_A_BYTES + 2 * TC_B_BYTES + TC_CN_BYTES;
 constexpr int TC_EPI = 8;                       // epilogue warps: 4 lane quarters x 2 column halves
 constexpr int TC_THREADS = (TC_EPI + 1) * 32;   // + 1 producer warp
+constexpr float TC_BIG = 1e37f;                 // above every score; finite, so packable
 
 __host__ __device__ inline int tc_chunks(int k) { return (k + TC_NC - 1) / TC_NC; }
 
@@ -1260,14 +1263,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_assign_tc(AssignJob jb, const
             const int a = tl & 1, na = tl >> 1;
             const int row = (tile0 + tl) * TC_M + r;
             float kn = 0.f;
-            float cb1[4], cb2[4];  // four independent chains (columns j mod 4) for ILP
-            int ci1[4];
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                cb1[z] = INFINITY;
-                cb2[z] = INFINITY;
-                ci1[z] = 0x7fffffff;
-            }
+            float b1 = TC_BIG, b2 = TC_BIG;  // the two smallest scores of this key (half)
+            int i1 = 0;                      // a valid index even if no score is finite
             for (int c = 0; c < nch; ++c) {
                 const int it = tl * nch + c, acc = it & 1, nacc = it >> 1;
                 ok = ok && mbar_wait(bar(ACC_FULL + acc), nacc & 1);
@@ -1290,38 +1287,61 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_assign_tc(AssignJob jb, const
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(A_KN + a));
                 }
-                const int nreal = min(TC_NC, k - c * TC_NC);
-                const int cend = min(nreal, (hw + 1) * (TC_NC / 2));
-                for (int c0 = hw * (TC_NC / 2); c0 < cend; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * TC_NC + c0), v);
+                // this warp's columns h0 .. h0 + hcnt - 1 of the group; each score carries its
+                // column (0..63) in the low six mantissa bits, so that plain min / max
+                // keep the two smallest and the argmin; eight chains for ILP
+                const int h0 = hw * (TC_NC / 2);
+                const int hcnt = min(TC_NC / 2, min(TC_NC, k - c * TC_NC) - h0);
+                float pb1[8], pb2[8];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int cc = c * TC_NC + c0 + j, z = j & 3;
-                        const float ap = c0 + j < nreal ? __fmaf_rn(-2.f, v[j], scn[cc]) : INFINITY;
-                        const bool lt = ap < cb1[z];
-                        cb2[z] = lt ? cb1[z] : fminf(cb2[z], ap);
-                        cb1[z] = lt ? ap : cb1[z];
-                        ci1[z] = lt ? cc : ci1[z];
+                for (int z = 0; z < 8; ++z) pb1[z] = pb2[z] = TC_BIG;
+                // both 32-column blocks are loaded before one wait
+                uint32_t vr[2][32];
+                const uint32_t tl0 = tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(acc * TC_NC + h0);
+                if (hcnt > 0) tmem_ld32_nowait(tl0, vr[0]);
+                if (hcnt > 32) tmem_ld32_nowait(tl0 + 32, vr[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    if (blk * 32 < hcnt) {
+                        const uint32_t (&v)[32] = vr[blk];
+                        const float4 *cn4 = reinterpret_cast<const float4 *>(scn + c * TC_NC + h0 + blk * 32);
+                        const bool full = blk * 32 + 32 <= hcnt;
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 cn = cn4[j4];
+                            const float cq[4] = {cn.x, cn.y, cn.z, cn.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = 4 * j4 + e, z = j & 7;
+                                const float ap = __fmaf_rn(-2.f, __uint_as_float(v[j]), cq[e]);
+                                float pk = __uint_as_float((__float_as_uint(ap) & ~63u) | (uint32_t)(blk * 32 + j));
+                                if (!full && blk * 32 + j >= hcnt) pk = TC_BIG;
+                                pb2[z] = fminf(pb2[z], fmaxf(pb1[z], pk));
+                                pb1[z] = fminf(pb1[z], pk);
+                            }
+                        }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(ACC_FREE + acc));
-            }
-            // the chains, then the two column halves of each key: the two smallest scores and
-            // the index of the smallest (an exact tie leaves the key uncertain, so which
-            // index is kept then does not matter)
-            float b1 = cb1[0], b2 = cb2[0];
-            int i1 = ci1[0];
 #pragma unroll
-            for (int z = 1; z < 4; ++z) {
-                b2 = fminf(fmaxf(b1, cb1[z]), fminf(b2, cb2[z]));
-                if (cb1[z] < b1) {
-                    b1 = cb1[z];
-                    i1 = ci1[z];
+                for (int z = 1; z < 8; ++z) {
+                    pb2[0] = fminf(fmaxf(pb1[0], pb1[z]), fminf(pb2[0], pb2[z]));
+                    pb1[0] = fminf(pb1[0], pb1[z]);
+                }
+                if (pb1[0] < TC_BIG) {  // fold the group into the key's running pair
+                    const int ci = c * TC_NC + h0 + (int)(__float_as_uint(pb1[0]) & 63u);
+                    b2 = fminf(fmaxf(b1, pb1[0]), fminf(b2, pb2[0]));
+                    if (pb1[0] < b1) {
+                        b1 = pb1[0];
+                        i1 = ci;
+                    }
                 }
             }
+            // the two column halves of each key: the two smallest scores and the index of
+            // the smallest (scores of different columns differ in their low bits)
             if (hw == 1) {
                 s_xb[r][0] = b1;
                 s_xb[r][1] = b2;
