@@ -205,3 +205,37 @@ def mog_head(K, V, n_now, q, summ, top_c, top_s, score_mode=0, residual=True):
     sel_c, sel_s, _, _ = select(q, summ, top_c, top_s, score_mode)
     out, diag = decode(K, V, n_now, q, summ, sel_c, sel_s, residual)
     return out, sel_c, sel_s, diag
+
+
+def union_selection(sels, L: int):
+    """Union of the choices of the query heads that share one KV head (the GQA union-exact
+    variant of this library; the pages select per query head and do not define it).
+    sels: (sel_c[tc], sel_s[tc, ts]) per head, as select() returns them.
+    Returns (uc[U], us[U, L]): every cluster some head chose, ascending, and inside each
+    every subcluster some head chose for it, ascending, -1 padded."""
+    chosen = {}
+    for sel_c, sel_s in sels:
+        sel_s = np.asarray(sel_s).reshape(len(sel_c), -1)
+        for i, c in enumerate(np.asarray(sel_c).tolist()):
+            if c < 0:
+                continue
+            subs = chosen.setdefault(int(c), set())
+            subs.update(int(l) for l in sel_s[i].tolist() if l >= 0)
+    uc = np.array(sorted(chosen), np.int32)
+    us = np.full((len(uc), L), -1, np.int32)
+    for i, c in enumerate(uc.tolist()):
+        sub = sorted(chosen[c])
+        us[i, :len(sub)] = sub
+    return uc, us
+
+
+def mog_group_union(K, V, n_now, qs, summ, top_c, top_s, score_mode=0, residual=True):
+    """GQA union-exact decode of the query heads qs[G][d] of one KV head: each head makes
+    its own selection; every head then attends exactly the anchors and the members of
+    every subcluster in the union of the heads' choices, and takes the Gaussian residual
+    of every other non-empty group (the subclusters of union clusters outside the union,
+    the clusters outside the union).  Returns (out[G][d], uc, us, per-head selections)."""
+    sels = [select(q, summ, top_c, top_s, score_mode)[:2] for q in qs]
+    uc, us = union_selection(sels, summ["L"])
+    outs = [decode(K, V, n_now, q, summ, uc, us, residual)[0] for q in qs]
+    return np.stack(outs), uc, us, sels

@@ -363,3 +363,97 @@ def test_residual_reduces_error_on_planted_data(ora):
     mog, _, _, _ = ora.mog_head(K, V, w.n, q[0], b, w.top_c, w.top_s)
     top, _, _, _ = ora.mog_head(K, V, w.n, q[0], b, w.top_c, w.top_s, residual=False)
     assert rel_l2(mog, ref) < rel_l2(top, ref)
+
+
+# ------------------------------------------------------- GQA union-exact (library variant)
+
+def mixture_ref(K, V, n_now, q, exact, groups):
+    """Exact attention over the positions `exact` plus one Gaussian term per member list
+    in `groups` (count, mean, population variance and value mean taken with numpy), all
+    in one softmax: an independent restatement of the residual mixture."""
+    Kf, Vf, qf = f64(K), f64(V), f64(q)
+    logits = [TAU * (Kf[p] @ qf) for p in exact]
+    rows = [Vf[p] for p in exact]
+    for mem in groups:
+        X = Kf[mem]
+        mu, var = X.mean(0), X.var(0)
+        logits.append(math.log(len(mem)) + TAU * (qf @ mu) + 0.5 * TAU ** 2 * float(qf ** 2 @ var))
+        rows.append(Vf[mem].mean(0))
+    wgt = softmax(np.array(logits))
+    return wgt @ np.array(rows)
+
+
+def _union_case(ora, G=4, seed=0):
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    b = ora.build_unit(K, V, w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    g = np.random.default_rng(seed)
+    centres = f64(K[g.integers(w.n_sink, w.n - w.n_recent, G)])
+    qs = wl.to_bf16(0.5 * centres + 0.5 * g.standard_normal((G, D)))
+    return w, K, V, qs, b
+
+
+def test_union_selection_is_the_union_of_the_heads(ora):
+    w, K, V, qs, b = _union_case(ora)
+    out, uc, us, sels = ora.mog_group_union(K, V, w.n, qs, b, w.top_c, w.top_s)
+    want = set()
+    for sel_c, sel_s in sels:
+        for i, c in enumerate(sel_c):
+            want |= {(int(c), int(l)) for l in sel_s[i] if c >= 0 and l >= 0}
+    got = {(int(c), int(l)) for i, c in enumerate(uc) for l in us[i] if l >= 0}
+    assert got == want
+    assert list(uc) == sorted(set(uc.tolist())) and len(uc) > w.top_c   # heads differ
+
+
+def test_union_exact_matches_independent_mixture(ora):
+    """Every head attends the anchors and the union's rows exactly; the groups no head
+    chose are Gaussians, checked against numpy statistics of the partition."""
+    w, K, V, qs, b = _union_case(ora, seed=1)
+    out, uc, us, _ = ora.mog_group_union(K, V, w.n, qs, b, w.top_c, w.top_s)
+    perm, off, L = b["perm"], b["sub_off"], b["L"]
+    chosen = {(int(c), int(l)) for i, c in enumerate(uc) for l in us[i] if l >= 0}
+    exact = list(range(w.n_sink)) + list(range(w.n - w.n_recent, w.n))
+    groups = []
+    for c in range(b["C"]):
+        if c in set(uc.tolist()):
+            for l in range(L):
+                mem = perm[off[c * L + l]:off[c * L + l + 1]]
+                if (c, l) in chosen:
+                    exact += mem.tolist()
+                elif mem.size:
+                    groups.append(mem)
+        else:
+            mem = perm[off[c * L]:off[(c + 1) * L]]
+            if mem.size:
+                groups.append(mem)
+    for gq in range(len(qs)):
+        assert rel_l2(out[gq], mixture_ref(K, V, w.n, qs[gq], exact, groups)) < 1e-12
+
+
+def test_union_exact_with_one_head_is_the_standard_decode(ora):
+    w, K, V, qs, b = _union_case(ora, G=1, seed=2)
+    out, _, _, _ = ora.mog_group_union(K, V, w.n, qs, b, w.top_c, w.top_s)
+    ref, _, _, _ = ora.mog_head(K, V, w.n, qs[0], b, w.top_c, w.top_s)
+    assert rel_l2(out[0], ref) < 1e-14
+
+
+def test_union_exact_of_identical_heads_is_the_standard_decode(ora):
+    w, K, V, qs, b = _union_case(ora, G=1, seed=3)
+    same = np.repeat(qs, 3, axis=0)
+    out, _, _, _ = ora.mog_group_union(K, V, w.n, same, b, w.top_c, w.top_s)
+    ref, _, _, _ = ora.mog_head(K, V, w.n, qs[0], b, w.top_c, w.top_s)
+    for g in range(3):
+        assert rel_l2(out[g], ref) < 1e-14
+
+
+def test_union_exact_never_attends_fewer_rows(ora):
+    """Each head's exact set grows from its own selection to the union; the error against
+    dense attention is reported, and with everything chosen both are dense."""
+    w, K, V, qs, b = _union_case(ora, seed=4)
+    out, uc, us, sels = ora.mog_group_union(K, V, w.n, qs, b, w.top_c, w.top_s)
+    n_union = ora.decode(K, V, w.n, qs[0], b, uc, us)[1][2]
+    for g, (sel_c, sel_s) in enumerate(sels):
+        assert ora.decode(K, V, w.n, qs[g], b, sel_c, sel_s)[1][2] <= n_union
+    full, _, _, _ = ora.mog_group_union(K, V, w.n, qs, b, w.n_clusters, w.n_sub)
+    for g in range(len(qs)):
+        assert rel_l2(full[g], dense_ref(K, V, w.n, qs[g])) < 1e-12
