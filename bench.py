@@ -50,6 +50,9 @@ def args_():
     ap.add_argument("--workload", default="qwen3-4b-32k", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="budget of the oracle timing sample")
+    ap.add_argument("--union-exact", action="store_true",
+                    help="GQA union-exact mode: every query head attends the union of the "
+                         "chosen subclusters of its KV group")
     return ap.parse_args()
 
 
@@ -241,7 +244,8 @@ def run_gpu(a, w, rank, world):
     Kd, Vd, qd = bf(K), bf(V), bf(q)
     del K, V
     prm = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], n_clusters=w.n_clusters, n_sub=w.n_sub,
-                          top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent)
+                          top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
+                          union_exact=int(a.union_exact))
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -298,6 +302,13 @@ def run_gpu(a, w, rank, world):
         if i >= 3:
             dense_ms.append(s0.elapsed_time(s1))
     dense_bytes = float(sum(int(lens[u // w.h_kv]) for u in range(lay.units))) * 4 * D
+    # approximation error of the MoG output against the full scan, per query head
+    h.decode(qd, out)
+    torch.cuda.synchronize()
+    o, dn = out.reshape(-1, D).double(), dense_out.reshape(-1, D).double()
+    err = ((o - dn).norm(dim=1) / dn.norm(dim=1).clamp_min(1e-30)).cpu().numpy()
+    approx = {"median_rel_l2": float(np.median(err)), "p90_rel_l2": float(np.percentile(err, 90)),
+              "max_rel_l2": float(err.max()), "heads": int(err.size)}
     # ---- the timed decode steps ----
     for _ in range(a.warmup):
         cold_l2()
@@ -368,6 +379,7 @@ def run_gpu(a, w, rank, world):
         "config": {"workload": w.name, "batch": w.batch, "h_kv": w.h_kv, "h_q": w.h_q, "d": D,
                    "context": int(lens.max()), "clusters": w.n_clusters, "subclusters": w.n_sub,
                    "top_c": w.top_c, "top_s": w.top_s, "n_sink": w.n_sink, "n_recent": w.n_recent,
+                   "mode": "union-exact" if a.union_exact else "per-head selection",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
@@ -387,6 +399,7 @@ def run_gpu(a, w, rank, world):
                          "GBps": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9, 1),
                          "frac": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9 / peak, 4)},
         "speedup_vs_dense": round(statistics.mean(dense_ms) / mean_ms, 2),
+        "approx_vs_dense": {k: (round(v, 6) if isinstance(v, float) else v) for k, v in approx.items()},
         "build": {"ms": round(build_ms, 2), "l1_flop": l1_flop, "l2_flop": l2_flop,
                   "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3)},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",

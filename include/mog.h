@@ -65,8 +65,16 @@ typedef enum {
  *  score_mode        : 0 = log-mass score ln n + tau q.mu + tau^2/2 sum q^2 sigma2 (the
  *                      residual's own exponent); 1 = tau q.mu only.
  *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
- *  flags             : must be 0.
+ *  flags             : 0, or MOG_FLAG_UNION_EXACT.
+ *
+ * MOG_FLAG_UNION_EXACT (a variant of this library; the pages select per query head and do
+ * not define it): each query head still makes its own selection, but every query head of a
+ * KV head attends exactly the anchors and the rows of every subcluster that any of them
+ * chose (the rows are loaded once for the group anyway); the Gaussian residual then covers
+ * the groups no head chose: the other non-empty subclusters of the chosen clusters and the
+ * clusters no head chose.  The bytes read are those of the default mode.
  */
+#define MOG_FLAG_UNION_EXACT 1
 typedef struct mog_params {
     int32_t batch, h_kv, h_q, d;
     int32_t n_cap;

@@ -85,7 +85,7 @@ static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
 
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
-    if (p->flags != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
+    if ((p->flags & ~MOG_FLAG_UNION_EXACT) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
         p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
         p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
         (p->score_mode != 0 && p->score_mode != 1) || (p->residual != 0 && p->residual != 1))
@@ -107,6 +107,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.T2 = p->iters_l2 > 0 ? p->iters_l2 : 10;
     P.score_mode = p->score_mode;
     P.residual = p->residual;
+    P.union_exact = (p->flags & MOG_FLAG_UNION_EXACT) ? 1 : 0;
     P.c_max = P.l_max = 1;
     P.n_mid_max = 0;
     for (int b = 0; b < p->batch; ++b) {
@@ -205,6 +206,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.T2 = P.T2;
     d.score_mode = P.score_mode;
     d.residual = P.residual;
+    d.union_exact = P.union_exact;
     d.P = P.P;
     d.nseg_max = P.nseg_max;
     d.cimg_ustride = P.cimg_ustride;

@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     const uint16_t *qg = a.q + (size_t)u * G * MOG_D;
     int *selu = dv.sel + (size_t)u * G * a.SW;
     const bool resid = dv.residual != 0;
+    const bool uex = dv.union_exact != 0;  // every head attends the union's subclusters
+    const uint32_t allg = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
     const bool pooled = tc > 0 && !a.sel_in;  // selection from the scores (not given)
 
     // ------------------------------------------------------------ P0: query, weights
@@ -451,22 +453,25 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     }
     // Gaussian residual terms, attended by the rows kernel: for the heads that chose slot s
     // but not its subcluster l, and for the heads that did not choose slice cluster c, the
-    // exponent (log2) of the term; -inf where the head does not take it.  Items: the union
-    // pairs (slot j, subcluster l) at j*L + l, then the clusters at Uc*L + c; rows of G
-    // exponents padded to a multiple of 4.
+    // exponent (log2) of the term; -inf where the head does not take it.  In the
+    // union-exact mode every head takes the subclusters no head chose and the clusters
+    // outside the union instead.  Items: the union pairs (slot j, subcluster l) at
+    // j*L + l, then the clusters at Uc*L + c; rows of G exponents padded to a multiple of 4.
     __syncthreads();
     {
         float *rx = dv.resx + (size_t)u * dv.resx_stride;
         const int GP = (G + 3) & ~3;  // 16-byte rows
         for (int e = tid; e < npair * GP; e += NT) {
             const int p = e / GP, g = e - p * GP, s = p / L, l = p - s * L;
-            const bool need = resid && g < G && snn[s * MOG_MAX_L + l] > 0 &&
-                              (((shm[s] & ~smask[s * MOG_MAX_L + l]) >> g) & 1u);
+            const uint32_t takers = uex ? (smask[s * MOG_MAX_L + l] ? 0u : allg)
+                                        : (shm[s] & ~smask[s * MOG_MAX_L + l]);
+            const bool need = resid && g < G && snn[s * MOG_MAX_L + l] > 0 && ((takers >> g) & 1u);
             rx[((size_t)(k + s * CS) * L + l) * GP + g] = need ? sres[(s * G + g) * MOG_MAX_L + l] * LOG2E : -INFINITY;
         }
         for (int e = tid; e < ns * GP; e += NT) {
             const int cl = e / GP, g = e - cl * GP;
-            const bool need = resid && g < G && cnn[cl] > 0 && !((slm[cl] >> g) & 1u);
+            const uint32_t takers = uex ? (slm[cl] ? 0u : allg) : ~slm[cl];
+            const bool need = resid && g < G && cnn[cl] > 0 && ((takers >> g) & 1u);
             rx[((size_t)Uc * L + c0 + cl) * GP + g] = need ? crs[g * m.SL + cl] * LOG2E : -INFINITY;
         }
     }
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
             const size_t sg = useg + gseg[j] + __popc(chosen & lanemask_lt());
             dv.segrow[sg] = gpre[j] + spref[s * (MOG_MAX_L + 1) + lane];
             dv.segoff[sg] = sso[s * (MOG_MAX_L + 1) + lane];
-            dv.segmask[sg] = smask[s * MOG_MAX_L + lane];
+            dv.segmask[sg] = uex ? allg : smask[s * MOG_MAX_L + lane];
         }
         const int ra = gpre[j], rb = gpre[j + 1];
         if (ra < rb) {  // rows-kernel CTAs p whose first row floor(T p / P) lies in [ra, rb)

@@ -36,6 +36,7 @@ struct Dev {
     int64_t sb, sh, sn;
     // shape
     int batch, h_kv, G, units, n_cap, c_max, l_max, tc, ts, T1, T2, score_mode, residual;
+    int union_exact;  // every head attends the union of the heads' chosen subclusters
     int P, nchunks, nseg_max;
     int64_t sub_off_stride;
     float tau;
@@ -70,7 +71,7 @@ struct Dev {
 // Host-side plan: sizes and byte offsets of every array in the arena.
 struct Plan {
     int batch, h_kv, h_q, G, d, n_cap, units, c_max, l_max, tc, ts, T1, T2;
-    int score_mode, residual, P, nchunks, n_mid_max, nseg_max;
+    int score_mode, residual, union_exact, P, nchunks, n_mid_max, nseg_max;
     int64_t sub_off_stride;
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
         o_sub_vbar, o_cl_vhl, o_sub_vhl, o_l1_assign, o_status, o_l1_steps;

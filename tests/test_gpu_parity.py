@@ -189,7 +189,7 @@ class Injected:
     """A batch whose (cluster, subcluster) partition is given: the oracle's own build of
     each unit (small cases) or a rule applied to positions (large cases)."""
 
-    def __init__(self, w, lens=None, mode="oracle", n_cap=None):
+    def __init__(self, w, lens=None, mode="oracle", n_cap=None, union_exact=0):
         self.w = w
         lens = wl.lengths(w) if lens is None else np.asarray(lens, np.int32)
         self.lens = lens
@@ -201,7 +201,7 @@ class Injected:
         self.summ = {}
         self.prm = mog.make_params(B, Hkv, Hkv * G, self.n_cap, n_clusters=w.n_clusters,
                                    n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink,
-                                   n_recent=w.n_recent)
+                                   n_recent=w.n_recent, union_exact=union_exact)
         stride = mog.sub_off_stride(self.prm, lens)
         perm_all = np.zeros((B * Hkv, self.n_cap), np.int32)
         off_all = np.zeros((B * Hkv, stride), np.int32)
@@ -266,7 +266,9 @@ def _check_stats(inj):
     return worst
 
 
-def _check_decode(inj, n_now=None, sample_heads=None):
+def _selection_vs_oracle(inj, heads=None):
+    """The GPU's own selection against the oracle's, head by head (differences only at
+    near-ties).  Returns (the oracle's selections [U*G][SW], near-tie count)."""
     w, G = inj.w, inj.w.group
     SW = w.top_c + w.top_c * w.top_s
     U = w.batch * w.h_kv
@@ -275,7 +277,7 @@ def _check_decode(inj, n_now=None, sample_heads=None):
     gsel = sel_out.cpu().numpy()
     ties = 0
     sel_ref = np.full((U * G, max(SW, 1)), -1, np.int32)
-    heads = range(U * G) if sample_heads is None else sample_heads
+    heads = range(U * G) if heads is None else heads
     for hq in heads:
         u, g = hq // G, hq % G
         b, h = u // w.h_kv, u % w.h_kv
@@ -297,6 +299,15 @@ def _check_decode(inj, n_now=None, sample_heads=None):
                 for l in set(gs[i].tolist()) ^ set(ss[i].tolist()):
                     assert l >= 0 and abs(sscore[i][l] - cut) < TIE, ("sub selection", hq, i, l)
                 ties += 1
+    return sel_ref, ties
+
+
+def _check_decode(inj, n_now=None, sample_heads=None):
+    w, G = inj.w, inj.w.group
+    SW = w.top_c + w.top_c * w.top_s
+    U = w.batch * w.h_kv
+    heads = range(U * G) if sample_heads is None else sample_heads
+    sel_ref, ties = _selection_vs_oracle(inj, heads)
     # outputs under the oracle's selection
     sin = torch.from_numpy(sel_ref).to(DEV)
     out = inj.h.decode(inj.qd, sel_in=sin).cpu().numpy().reshape(U * G, D)
@@ -446,6 +457,45 @@ def test_many_units_many_slots_per_split():
     inj = Injected(w)
     assert inj.h.splits() == 4
     _check_decode(inj, sample_heads=range(0, 256, 7))
+
+
+def _check_decode_union(inj):
+    """Union-exact mode: each head's own selection (checked against the oracle), then
+    every head of a KV group attends the union of the group's chosen subclusters."""
+    w, G = inj.w, inj.w.group
+    tc, ts, SW = w.top_c, w.top_s, w.top_c + w.top_c * w.top_s
+    U = w.batch * w.h_kv
+    sel_ref, ties = _selection_vs_oracle(inj)
+    out = inj.h.decode(inj.qd, sel_in=torch.from_numpy(sel_ref).to(DEV)).cpu().numpy().reshape(U * G, D)
+    worst, grew = 0.0, 0
+    for u in range(U):
+        b, h = u // w.h_kv, u % w.h_kv
+        s = inj.summ[(b, h)]
+        sels = [(sel_ref[u * G + g, :tc], sel_ref[u * G + g, tc:SW].reshape(tc, ts)) for g in range(G)]
+        uc, us = ora.union_selection(sels, s["L"])
+        for g in range(G):
+            ref, diag = ora.decode(inj.K[b, h], inj.V[b, h], int(inj.lens[b]), inj.q[b, h * G + g], s, uc, us)
+            own = ora.decode(inj.K[b, h], inj.V[b, h], int(inj.lens[b]), inj.q[b, h * G + g], s, *sels[g])[1]
+            grew += diag[2] > own[2]
+            e = rel(out[u * G + g], ref)
+            worst = max(worst, e)
+            assert e <= OUT_TOL, (u, g, e)
+    assert grew > 0   # the union adds rows for some heads: the mode is exercised
+    assert inj.h.sync_status() == 0
+    return ties, worst
+
+
+def test_union_exact_gqa_matches_oracle():
+    w = small_workload(2500, h_kv=2, h_q=8, top_c=5, top_s=3, seed=71)
+    inj = Injected(w, union_exact=1)
+    print("union-exact decode", _check_decode_union(inj))
+
+
+def test_union_exact_sixteen_heads_many_units():
+    w = small_workload(1500, batch=3, h_kv=2, h_q=32, centres=40, n_clusters=30, n_sub=6,
+                       top_c=6, top_s=2, n_recent=32, seed=72)
+    inj = Injected(w, union_exact=1)
+    print("union-exact decode", _check_decode_union(inj))
 
 
 def test_sixteen_query_heads_per_kv_head():
