@@ -239,3 +239,46 @@ def mog_group_union(K, V, n_now, qs, summ, top_c, top_s, score_mode=0, residual=
     uc, us = union_selection(sels, summ["L"])
     outs = [decode(K, V, n_now, q, summ, uc, us, residual)[0] for q in qs]
     return np.stack(outs), uc, us, sels
+
+
+def slide(K: np.ndarray, V: np.ndarray, summ: dict, force=None):
+    """One step of the sliding recent window (a reading of this library; the pages keep a
+    recent window but do not say what happens to a key that leaves it).  The oldest recent
+    key, position max(S, n_build - R), leaves the window: it joins the nearest non-empty
+    cluster under the assignment rule R5 against the cluster means, then the nearest
+    non-empty subcluster of that cluster against the subcluster means (or `force` =
+    (c, l)), and both groups take it with Welford's update of count, mean, population
+    variance and value mean.  The key goes to the end of its subcluster's run of `perm`
+    and n_build advances by one, so that the recent window [n_build - R, n) keeps R keys.
+    Returns (the updated copy of summ, (c, l)); (summ, None) when no cluster is non-empty."""
+    s = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in summ.items()}
+    S, R, Cn, L = s["S"], s["R"], s["C"], s["L"]
+    p = max(S, s["n_build"] - R)
+    full = np.nonzero(s["cl_n"][:Cn] > 0)[0]
+    if full.size == 0:
+        return s, None
+    x_bf = np.ascontiguousarray(_u16(K)[p:p + 1])
+    if force is None:
+        c = int(full[assign(x_bf, s["cl_mu"][full])[0]])
+        subs = np.nonzero(s["sub_n"][c * L:(c + 1) * L] > 0)[0]
+        l = int(subs[assign(x_bf, s["sub_mu"][c * L + subs])[0]])
+    else:
+        c, l = int(force[0]), int(force[1])
+    x = _u16(K)[p].astype(np.uint32) << 16
+    v = _u16(V)[p].astype(np.uint32) << 16
+    x = x.view(np.float32).astype(np.float64)
+    v = v.view(np.float32).astype(np.float64)
+    for cnt, mu, var, vb, i in ((s["cl_n"], s["cl_mu"], s["cl_var"], s["cl_vbar"], c),
+                                (s["sub_n"], s["sub_mu"], s["sub_var"], s["sub_vbar"], c * L + l)):
+        n = float(cnt[i])
+        delta = x - mu[i]
+        mu_new = mu[i] + delta / (n + 1.0)
+        var[i] = (n * var[i] + delta * (x - mu_new)) / (n + 1.0)
+        mu[i] = mu_new
+        vb[i] = vb[i] + (v - vb[i]) / (n + 1.0)
+        cnt[i] += 1
+    g = c * L + l
+    s["perm"] = np.insert(s["perm"], int(s["sub_off"][g + 1]), p).astype(np.int32)
+    s["sub_off"][g + 1:] += 1
+    s["n_build"] += 1
+    return s, (c, l)

@@ -457,3 +457,65 @@ def test_union_exact_never_attends_fewer_rows(ora):
     full, _, _, _ = ora.mog_group_union(K, V, w.n, qs, b, w.n_clusters, w.n_sub)
     for g in range(len(qs)):
         assert rel_l2(full[g], dense_ref(K, V, w.n, qs[g])) < 1e-12
+
+
+# ------------------------------------------------------ sliding recent window (variant)
+
+def _slid(ora, steps, seed=5):
+    """tiny-4k built on its first 4096 - steps keys, then `steps` appends, each pushing the
+    oldest recent key into the clusters."""
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    nb = w.n - steps
+    b = ora.build_unit(K, V, nb, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    s, moves = b, []
+    for t in range(steps):
+        s, cl = ora.slide(K, V, s)
+        moves.append(cl)
+    return w, K, V, q, b, s, moves
+
+
+def test_slide_welford_equals_two_pass_statistics(ora):
+    w, K, V, q, b, s, moves = _slid(ora, 40)
+    ref = ora.stats(K, V, s["perm"], s["sub_off"], s["C"], s["L"])
+    for key in ("cl_n", "sub_n"):
+        assert np.array_equal(s[key], ref[key])
+    for key in ("cl_mu", "cl_var", "cl_vbar", "sub_mu", "sub_var", "sub_vbar"):
+        err = np.abs(s[key] - ref[key]).max() / max(np.abs(ref[key]).max(), 1e-300)
+        assert err < 1e-12, (key, err)
+    assert s["n_build"] == b["n_build"] + 40 and s["perm"].size == b["perm"].size + 40
+
+
+def test_slide_joins_the_nearest_nonempty_groups(ora):
+    w, K, V, q, b, _, _ = _slid(ora, 0)
+    s = b
+    for t in range(12):
+        p = max(s["S"], s["n_build"] - s["R"])
+        x = f64(K[p:p + 1])
+        full = np.nonzero(s["cl_n"] > 0)[0]
+        dc = cdist(x, s["cl_mu"][full], "sqeuclidean")[0]
+        c_ref = int(full[np.argmin(dc)])
+        L = s["L"]
+        subs = np.nonzero(s["sub_n"][c_ref * L:(c_ref + 1) * L] > 0)[0]
+        ds = cdist(x, s["sub_mu"][c_ref * L + subs], "sqeuclidean")[0]
+        s, (c, l) = ora.slide(K, V, s)
+        assert (c, l) == (c_ref, int(subs[np.argmin(ds)]))
+        g = c * L + l
+        assert p in s["perm"][s["sub_off"][g]:s["sub_off"][g + 1]]
+        assert p == s["perm"][s["sub_off"][g + 1] - 1]   # at the end of its subcluster's run
+
+
+def test_slide_keeps_r_anchors_and_all_selected_is_dense(ora):
+    w, K, V, q, b, s, _ = _slid(ora, 30)
+    out, _, _, diag = ora.mog_head(K, V, w.n, q[0], s, 0, 0)       # nothing selected
+    assert diag[2] == w.n_sink + w.n_recent
+    full, _, _, diag = ora.mog_head(K, V, w.n, q[0], s, w.n_clusters, w.n_sub)
+    assert diag[2] == w.n
+    assert rel_l2(full, dense_ref(K, V, w.n, q[0])) < 1e-12
+
+
+def test_slide_with_no_nonempty_cluster_is_a_no_op(ora):
+    K, V, q = planted(200, seed=14)
+    b = ora.build_unit(K, V, 200, 4, 196, 3, 2)       # everything is an anchor
+    s, cl = ora.slide(K, V, b)
+    assert cl is None and s["n_build"] == b["n_build"] and s["perm"].size == 0
