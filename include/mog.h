@@ -65,7 +65,7 @@ typedef enum {
  *  score_mode        : 0 = log-mass score ln n + tau q.mu + tau^2/2 sum q^2 sigma2 (the
  *                      residual's own exponent); 1 = tau q.mu only.
  *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
- *  flags             : 0, or MOG_FLAG_UNION_EXACT.
+ *  flags             : 0, or any of MOG_FLAG_UNION_EXACT, MOG_FLAG_SLIDING.
  *
  * MOG_FLAG_UNION_EXACT (a variant of this library; the pages select per query head and do
  * not define it): each query head still makes its own selection, but every query head of a
@@ -75,6 +75,17 @@ typedef enum {
  * clusters no head chose.  The bytes read are those of the default mode.
  */
 #define MOG_FLAG_UNION_EXACT 1
+/*
+ * MOG_FLAG_SLIDING (a variant of this library; the pages keep a recent window but do not
+ * say what happens to a key leaving it): the recent anchors stay the last n_recent keys.
+ * When mog_append makes a KV head's window longer, its oldest recent key joins the nearest
+ * non-empty cluster and, inside it, the nearest non-empty subcluster (the build's
+ * nearest-centroid rule against the groups' means), and both groups' count, mean,
+ * population variance and value mean take it by Welford's update.  The key's row joins
+ * its subcluster in the partition (`perm`, `sub_off`), so it is attended exactly whenever
+ * that subcluster is chosen.  A head with no non-empty cluster keeps a growing window.
+ */
+#define MOG_FLAG_SLIDING 2
 typedef struct mog_params {
     int32_t batch, h_kv, h_q, d;
     int32_t n_cap;

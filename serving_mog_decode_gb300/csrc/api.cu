@@ -85,7 +85,7 @@ static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
 
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
-    if ((p->flags & ~MOG_FLAG_UNION_EXACT) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
+    if ((p->flags & ~(MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING)) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
         p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
         p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
         (p->score_mode != 0 && p->score_mode != 1) || (p->residual != 0 && p->residual != 1))
@@ -108,6 +108,8 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.score_mode = p->score_mode;
     P.residual = p->residual;
     P.union_exact = (p->flags & MOG_FLAG_UNION_EXACT) ? 1 : 0;
+    P.sliding = (p->flags & MOG_FLAG_SLIDING) ? 1 : 0;
+    P.R = p->n_recent;
     P.c_max = P.l_max = 1;
     P.n_mid_max = 0;
     for (int b = 0; b < p->batch; ++b) {
@@ -463,6 +465,10 @@ extern "C" int mog_append(mog_handle *h, const void *k_new_dev, const void *v_ne
     if ((int64_t)nmax + h->appended + 1 > h->plan.n_cap) return MOG_ERR_CAPACITY;
     cudaError_t e = launch_append(h->dev, h->plan, k_new_dev, v_new_dev, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mog_append launch");
+    if (h->plan.sliding) {
+        e = launch_slide(h->dev, h->plan, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "mog_append slide launch");
+    }
     h->appended += 1;
     return MOG_OK;
 }

@@ -71,7 +71,7 @@ struct Dev {
 // Host-side plan: sizes and byte offsets of every array in the arena.
 struct Plan {
     int batch, h_kv, h_q, G, d, n_cap, units, c_max, l_max, tc, ts, T1, T2;
-    int score_mode, residual, union_exact, P, nchunks, n_mid_max, nseg_max;
+    int score_mode, residual, union_exact, sliding, R, P, nchunks, n_mid_max, nseg_max;
     int64_t sub_off_stride;
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
         o_sub_vbar, o_cl_vhl, o_sub_vhl, o_l1_assign, o_status, o_l1_steps;
@@ -96,6 +96,7 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
                           cudaEvent_t const *events = nullptr);
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
                           cudaStream_t s);
+cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s);
 cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64_t sh,
                          int64_t sn, const int32_t *lengths, int n_max, int batch, int h_kv,
                          int G, const void *q, float *out, float *scratch, int splits,

@@ -21,31 +21,15 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "exact.cuh"
 #include "internal.h"
 #include "tc.cuh"
 
 namespace mog {
 
-// relative error bound of the fp32 distance, with a safety factor of ~3 over (d+2)*2^-24
-constexpr float kCertRel = 2.5e-5f;
 // error factor of the tensor-core distances |c|^2 - 2 k.c (split-bf16 centroids, fp32
 // accumulate): a score within TC_F (|k|^2 + |c|^2) of the exact one, with a safety margin
 constexpr float TC_F = 1.0f / 8192.0f;  // 2^-13
-
-__device__ __forceinline__ bool certified(float b1, float b2) {
-    // true minimum is b1's centroid for every rounding within the bound
-    return b2 - b1 > kCertRel * (b1 + b2);
-}
-
-// exact rule: fp64, index order, no contraction
-__device__ __forceinline__ double exact_dist(const uint16_t *x, const float *c) {
-    double acc = 0.0;
-    for (int j = 0; j < MOG_D; ++j) {
-        double diff = __dsub_rn((double)bf1(x[j]), (double)c[j]);
-        acc = __dadd_rn(acc, __dmul_rn(diff, diff));
-    }
-    return acc;
-}
 
 // converged before or at step t: some step 1..t changed nothing
 __device__ __forceinline__ bool converged_by(const int *changed, int t) {

@@ -189,7 +189,7 @@ class Injected:
     """A batch whose (cluster, subcluster) partition is given: the oracle's own build of
     each unit (small cases) or a rule applied to positions (large cases)."""
 
-    def __init__(self, w, lens=None, mode="oracle", n_cap=None, union_exact=0):
+    def __init__(self, w, lens=None, mode="oracle", n_cap=None, union_exact=0, sliding=0):
         self.w = w
         lens = wl.lengths(w) if lens is None else np.asarray(lens, np.int32)
         self.lens = lens
@@ -201,7 +201,7 @@ class Injected:
         self.summ = {}
         self.prm = mog.make_params(B, Hkv, Hkv * G, self.n_cap, n_clusters=w.n_clusters,
                                    n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink,
-                                   n_recent=w.n_recent, union_exact=union_exact)
+                                   n_recent=w.n_recent, union_exact=union_exact, sliding=sliding)
         stride = mog.sub_off_stride(self.prm, lens)
         perm_all = np.zeros((B * Hkv, self.n_cap), np.int32)
         off_all = np.zeros((B * Hkv, stride), np.int32)
@@ -496,6 +496,55 @@ def test_union_exact_sixteen_heads_many_units():
                        top_c=6, top_s=2, n_recent=32, seed=72)
     inj = Injected(w, union_exact=1)
     print("union-exact decode", _check_decode_union(inj))
+
+
+def test_sliding_window_matches_oracle():
+    """Sliding recent window: after each append the oldest recent key of every KV head
+    joins a cluster.  The GPU's choice is the exact argmin under its own means at that
+    moment; the oracle replays the same moves (Welford in fp64); statistics, partition,
+    window and decode then agree."""
+    steps, n0 = 40, 3000
+    w = small_workload(n0, batch=2, h_kv=2, h_q=8, n_recent=32, seed=81)
+    inj = Injected(w, n_cap=n0 + steps, sliding=1)
+    rng = np.random.default_rng(8)
+    L, U = w.n_sub, w.batch * w.h_kv
+    lay = inj.h.layout()
+    for t in range(steps):
+        before = inj.gpu_summaries()
+        kn = wl.to_bf16(rng.standard_normal((w.batch, w.h_kv, D)))
+        vn = wl.to_bf16(rng.standard_normal((w.batch, w.h_kv, D)))
+        inj.h.append(bf(kn), bf(vn))
+        inj.K[:, :, n0 + t], inj.V[:, :, n0 + t] = kn, vn
+        after = inj.gpu_summaries()
+        for u in range(U):
+            b, h = u // w.h_kv, u % w.h_kv
+            s = inj.summ[(b, h)]
+            Cn = s["C"]
+            moved = np.nonzero(after["sub_n"][u, :Cn * L] != before["sub_n"][u, :Cn * L])[0]
+            assert moved.size == 1, (t, u, moved)
+            c, l = divmod(int(moved[0]), L)
+            p = max(s["S"], s["n_build"] - s["R"])
+            x = inj.K[b, h, p:p + 1]
+            full = np.nonzero(before["cl_n"][u, :Cn] > 0)[0]
+            means = before["cl_ms"][u, full, 0].astype(np.float64)
+            assert full[ora.assign(x, means)[0]] == c, (t, u)
+            subs = np.nonzero(before["sub_n"][u, c * L:(c + 1) * L] > 0)[0]
+            smeans = before["sub_ms"][u, c * L + subs, 0].astype(np.float64)
+            assert subs[ora.assign(x, smeans)[0]] == l, (t, u)
+            inj.summ[(b, h)], _ = ora.slide(inj.K[b, h], inj.V[b, h], s, force=(c, l))
+    info = inj.h.array("unit_info", torch.int32, (U, 8)).cpu().numpy()
+    perm = inj.h.array("perm", torch.int32, (U, lay.n_cap)).cpu().numpy()
+    off = inj.h.array("sub_off", torch.int32, (U, lay.sub_off_stride)).cpu().numpy()
+    for u in range(U):
+        s = inj.summ[(u // w.h_kv, u % w.h_kv)]
+        Cn = s["C"]
+        assert info[u, 5] == s["n_build"] - s["R"] and info[u, 3] == s["perm"].size
+        assert np.array_equal(off[u, :Cn * L + 1], s["sub_off"])
+        for g in range(Cn * L):
+            a, e = s["sub_off"][g], s["sub_off"][g + 1]
+            assert np.array_equal(np.sort(perm[u, a:e]), np.sort(s["perm"][a:e])), (u, g)
+    print("sliding: stats worst", _check_stats(inj))
+    print("sliding: decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
 
 
 def test_sixteen_query_heads_per_kv_head():
