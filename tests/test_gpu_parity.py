@@ -547,6 +547,44 @@ def test_sliding_window_matches_oracle():
     print("sliding: decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
 
 
+def test_sliding_window_union_exact_ragged_batch():
+    """Both variants at once on a ragged batch: a 2600-key sequence slides its window into
+    the clusters, a 40-key one has no cluster and keeps a growing window; the decode is
+    then checked under the union-exact rule."""
+    steps = 24
+    w = small_workload(2600, batch=2, h_kv=2, h_q=8, n_recent=48, seed=82)
+    lens = np.array([2600, 40], np.int32)
+    inj = Injected(w, lens=lens, n_cap=2600 + steps, sliding=1, union_exact=1)
+    rng = np.random.default_rng(9)
+    L, U = w.n_sub, w.batch * w.h_kv
+    for t in range(steps):
+        before = inj.gpu_summaries()
+        kn = wl.to_bf16(rng.standard_normal((w.batch, w.h_kv, D)))
+        vn = wl.to_bf16(rng.standard_normal((w.batch, w.h_kv, D)))
+        inj.h.append(bf(kn), bf(vn))
+        for b in range(w.batch):
+            inj.K[b, :, lens[b] + t], inj.V[b, :, lens[b] + t] = kn[b], vn[b]
+        after = inj.gpu_summaries()
+        for u in range(U):
+            b, h = u // w.h_kv, u % w.h_kv
+            s = inj.summ[(b, h)]
+            Cn = s["C"]
+            moved = np.nonzero(after["sub_n"][u, :Cn * L] != before["sub_n"][u, :Cn * L])[0]
+            if not (s["cl_n"] > 0).any():
+                assert moved.size == 0
+                assert ora.slide(inj.K[b, h], inj.V[b, h], s)[1] is None
+                continue
+            assert moved.size == 1, (t, u, moved)
+            c, l = divmod(int(moved[0]), L)
+            inj.summ[(b, h)], _ = ora.slide(inj.K[b, h], inj.V[b, h], s, force=(c, l))
+    info = inj.h.array("unit_info", torch.int32, (U, 8)).cpu().numpy()
+    for u in range(U):
+        s = inj.summ[(u // w.h_kv, u % w.h_kv)]
+        assert info[u, 5] == max(s["S"], s["n_build"] - s["R"])
+    inj.lens = lens + steps
+    print("sliding + union-exact: stats", _check_stats(inj), "decode", _check_decode_union(inj))
+
+
 def test_sixteen_query_heads_per_kv_head():
     w = small_workload(2500, h_kv=1, h_q=16, top_c=5, top_s=3, seed=61)
     inj = Injected(w)
