@@ -43,7 +43,9 @@ __device__ __forceinline__ void merge2(float &b1, int &i1, float &b2, float ob1,
     }
 }
 
-struct SlideRed {
+struct __align__(16) SlideRed {
+    float d32[MAX_C];               // fp32 distance of every group (+inf if empty)
+    float mean[SL_WARPS][MOG_D];    // a candidate mean per warp for the exact rule
     float b1[SL_WARPS], b2[SL_WARPS];
     int i1[SL_WARPS];
     double d[SL_WARPS];
@@ -54,24 +56,13 @@ struct SlideRed {
     int out_di;
 };
 
-// fp32 squared distance of the staged key xs to the mean c, in index order
-__device__ __forceinline__ float dist32(const float *xs, const float *c) {
-    float acc = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < MOG_D; ++j) {
-        const float df = __fsub_rn(xs[j], c[j]);
-        acc = __fmaf_rn(df, df, acc);
-    }
-    return acc;
-}
-
 // The nearest of the k groups with count > 0 whose means sit at ms + i * ld, for the key
-// x (bf16 row; xs its fp32 copy in shared memory), under the exact rule; -1 when no group
+// whose (exact) fp32 copy xs sits in shared memory, under the exact rule; -1 when no group
 // is non-empty.  Called by the whole block.  Warp w scores groups w, w + W, ... with its
 // lanes over the dimensions (four each, 16-byte loads of eight groups in flight); the fp32
 // sum order does not matter to the certificate, only the fp64 rule fixes an order.
-__device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, const uint16_t *x,
-                             const float *xs, SlideRed &red) {
+__device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, const float *xs,
+                             SlideRed &red) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float b1 = INFINITY, b2 = INFINITY;
     int i1 = 0x7fffffff;
@@ -80,10 +71,10 @@ __device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, con
         float4 m[8];
         bool ok[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 8; ++q) {  // counts and means are read together
             const int i = i0 + q * SL_WARPS;
             ok[q] = i < k && cnt[i] > 0;
-            m[q] = ok[q] ? reinterpret_cast<const float4 *>(ms + (size_t)i * ld)[lane]
+            m[q] = i < k ? reinterpret_cast<const float4 *>(ms + (size_t)i * ld)[lane]
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
@@ -94,6 +85,7 @@ __device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, con
 #pragma unroll
             for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             if (ok[q]) keep2(b1, i1, b2, acc, i0 + q * SL_WARPS);
+            if (lane == 0 && i0 + q * SL_WARPS < k) red.d32[i0 + q * SL_WARPS] = ok[q] ? acc : INFINITY;
         }
     }
     if (lane == 0) {
@@ -124,17 +116,30 @@ __device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, con
     i1 = red.out_i1;
     if (i1 == 0x7fffffff) return -1;
     if (b2 == INFINITY || certified(b1, b2)) return i1;
-    // the exact rule among the groups whose fp32 distance is within the error bound
+    // The exact rule among the groups whose fp32 distance is within the error bound: warp
+    // w takes candidates w, w + W, ...; the warp stages the candidate's mean in shared
+    // memory and lane 0 sums the fp64 squares in index order (the key's fp32 copy holds
+    // its bf16 values exactly).
     const float thr = b1 * (1.f + 2.5f * kCertRel);
     double best = INFINITY;
     int bi = 0x7fffffff;
-    for (int i = tid; i < k; i += SL_THREADS) {
-        if (cnt[i] <= 0 || dist32(xs, ms + (size_t)i * ld) > thr) continue;
-        const double dd = exact_dist(x, ms + (size_t)i * ld);
-        if (dd < best || (dd == best && i < bi)) {
-            best = dd;
-            bi = i;
+    float *mw = red.mean[warp];
+    for (int i = warp; i < k; i += SL_WARPS) {
+        if (!(red.d32[i] <= thr)) continue;
+        reinterpret_cast<float4 *>(mw)[lane] = reinterpret_cast<const float4 *>(ms + (size_t)i * ld)[lane];
+        __syncwarp();
+        if (lane == 0) {
+            double dd = 0.0;
+            for (int j = 0; j < MOG_D; ++j) {
+                const double df = __dsub_rn((double)xs[j], (double)mw[j]);
+                dd = __dadd_rn(dd, __dmul_rn(df, df));
+            }
+            if (dd < best || (dd == best && i < bi)) {
+                best = dd;
+                bi = i;
+            }
         }
+        __syncwarp();
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -208,10 +213,10 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
     }
     __syncthreads();
     const size_t cg0 = (size_t)u * dv.c_max, sg0 = (size_t)u * dv.c_max * dv.l_max;
-    const int c = nearest_group(dv.cl_ms + cg0 * 2 * MOG_D, 2 * MOG_D, dv.cl_n + cg0, C, kr, xs, red);
+    const int c = nearest_group(dv.cl_ms + cg0 * 2 * MOG_D, 2 * MOG_D, dv.cl_n + cg0, C, xs, red);
     if (c < 0) return;  // no cluster to join: the window grows instead
     const int l = nearest_group(dv.sub_ms + (sg0 + (size_t)c * L) * 2 * MOG_D, 2 * MOG_D,
-                                dv.sub_n + sg0 + (size_t)c * L, L, kr, xs, red);
+                                dv.sub_n + sg0 + (size_t)c * L, L, xs, red);
     if (l < 0) {  // a non-empty cluster has a non-empty subcluster; reaching here is corrupt
         if (tid == 0) flag_error(dv.status, ST_BAD_INDEX);
         return;
