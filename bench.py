@@ -37,6 +37,7 @@ from serving_mog_decode_gb300 import workloads as wl  # noqa: E402
 METRIC = "MoG decode us/step/layer at 32K-1M ctx; achieved HBM GB/s vs roofline"
 D = 128
 FLUSH_BYTES = 256 << 20
+APPEND_STEPS = 36         # appends timed with --sliding (the first four are warm-up)
 CUSHION_CYCLES = 200_000   # GPU-side spin before each timed step (~0.1 ms): the host
                            # finishes enqueueing the step before the start event is reached
 
@@ -50,6 +51,9 @@ def args_():
     ap.add_argument("--workload", default="qwen3-4b-32k", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="budget of the oracle timing sample")
+    ap.add_argument("--sliding", action="store_true",
+                    help="sliding recent window; the cache gets room for the append timing "
+                         "that follows the decode timing")
     ap.add_argument("--union-exact", action="store_true",
                     help="GQA union-exact mode: every query head attends the union of the "
                          "chosen subclusters of its KV group")
@@ -241,11 +245,14 @@ def run_gpu(a, w, rank, world):
     def bf(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
 
+    if a.sliding:  # room for the appends timed after the decode steps
+        pad = ((0, 0), (0, 0), (0, APPEND_STEPS), (0, 0))
+        K, V = np.pad(K, pad), np.pad(V, pad)
     Kd, Vd, qd = bf(K), bf(V), bf(q)
     del K, V
     prm = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], n_clusters=w.n_clusters, n_sub=w.n_sub,
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
-                          union_exact=int(a.union_exact))
+                          union_exact=int(a.union_exact), sliding=int(a.sliding))
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -355,6 +362,22 @@ def run_gpu(a, w, rank, world):
             e2e_ms.append(s0.elapsed_time(s1))
     clk = clocks.stop()
     assert h.sync_status() == 0
+    append = None
+    if a.sliding:  # mog_append: the new rows, then each KV head's oldest recent key moves in
+        kn = torch.randn(w.batch, w.h_kv, D, device=dev).to(torch.bfloat16)
+        vn = torch.randn(w.batch, w.h_kv, D, device=dev).to(torch.bfloat16)
+        app_ms = []
+        for i in range(APPEND_STEPS):
+            s0, s1 = ev(), ev()
+            s0.record()
+            h.append(kn, vn)
+            s1.record()
+            torch.cuda.synchronize()
+            if i >= 4:
+                app_ms.append(s0.elapsed_time(s1))
+        assert h.sync_status() == 0
+        append = {"us_median": round(statistics.median(app_ms) * 1e3, 2), "appends": len(app_ms),
+                  "what": "mog_append with the sliding window, events around the call (launch overhead included)"}
 
     mean_ms = max_over_ranks(statistics.mean(step_ms), dev)
     pm = [statistics.mean(p) for p in phase]
@@ -380,6 +403,7 @@ def run_gpu(a, w, rank, world):
                    "context": int(lens.max()), "clusters": w.n_clusters, "subclusters": w.n_sub,
                    "top_c": w.top_c, "top_s": w.top_s, "n_sink": w.n_sink, "n_recent": w.n_recent,
                    "mode": "union-exact" if a.union_exact else "per-head selection",
+                   "recent_window": "sliding" if a.sliding else "growing",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
@@ -404,6 +428,7 @@ def run_gpu(a, w, rank, world):
                   "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3)},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",
                 "h2d_bytes_per_step": int(q_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 4)},
+        "append": append,
         "gpu_launches": 3 * a.steps,  # selection, rows and merge kernels per step
         "clocks": clk,
     }
