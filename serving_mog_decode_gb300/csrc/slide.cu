@@ -11,8 +11,16 @@
 // Welford's recurrence.  Its row goes to the end of its subcluster's run of the partition;
 // every later non-empty subcluster moves its first row to its end to make room, which keeps
 // each run contiguous (rows within a run are a set for the attention).
+//
+// One thread-block cluster of up to 8 CTAs per KV head shares the work: each CTA scores a
+// slice of the cluster means and moves a slice of the subclusters' rows; the slices' best
+// scores are merged through distributed shared memory, and cluster barriers order the
+// reads of the partition before its writes.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "exact.cuh"
@@ -22,6 +30,7 @@ namespace mog {
 
 constexpr int SL_THREADS = 1024;
 constexpr int SL_WARPS = SL_THREADS / 32;
+constexpr int SL_MAX_CS = 8;  // CTAs per KV head (portable cluster size)
 
 // keep the two smallest values and the index of the smallest (lowest index on ties)
 __device__ __forceinline__ void keep2(float &b1, int &i1, float &b2, float v, int i) {
@@ -42,50 +51,57 @@ __device__ __forceinline__ void merge2(float &b1, int &i1, float &b2, float ob1,
         b2 = fminf(b2, ob1);
     }
 }
+__device__ __forceinline__ void keep_min(double &best, int &bi, double d, int i) {
+    if (d < best || (d == best && i < bi)) {
+        best = d;
+        bi = i;
+    }
+}
 
 struct __align__(16) SlideRed {
-    float d32[MAX_C];               // fp32 distance of every group (+inf if empty)
-    float mean[SL_WARPS][MOG_D];    // a candidate mean per warp for the exact rule
+    float d32[MAX_C];             // fp32 distance of every group of this CTA's slice (+inf if empty)
+    float mean[SL_WARPS][MOG_D];  // a candidate mean per warp for the exact rule
     float b1[SL_WARPS], b2[SL_WARPS];
     int i1[SL_WARPS];
     double d[SL_WARPS];
     int di[SL_WARPS];
-    float out_b1, out_b2;
+    float out_b1, out_b2;  // this CTA's result, read by the cluster
     int out_i1;
     double out_d;
     int out_di;
 };
 
-// The nearest of the k groups with count > 0 whose means sit at ms + i * ld, for the key
-// whose (exact) fp32 copy xs sits in shared memory, under the exact rule; -1 when no group
-// is non-empty.  Called by the whole block.  Warp w scores groups w, w + W, ... with its
-// lanes over the dimensions (four each, 16-byte loads of eight groups in flight); the fp32
-// sum order does not matter to the certificate, only the fp64 rule fixes an order.
-__device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, const float *xs,
-                             SlideRed &red) {
+// Block-wide: the two smallest fp32 distances of the key (fp32 copy xs in shared memory)
+// to the non-empty groups lo .. hi-1 (means at ms + i * ld) and the index of the smallest,
+// into red.out_*; red.d32[i - lo] keeps every distance.  Warp w scores groups lo + w,
+// lo + w + W, ..., its lanes over the dimensions (four each; 16-byte loads of eight groups
+// in flight).  The fp32 sum order does not matter to the certificate.
+__device__ void score_range(const float *ms, int ld, const int *cnt, int lo, int hi, const float *xs,
+                            SlideRed &red) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float b1 = INFINITY, b2 = INFINITY;
     int i1 = 0x7fffffff;
     const float4 xv = reinterpret_cast<const float4 *>(xs)[lane];
-    for (int i0 = warp; i0 < k; i0 += 8 * SL_WARPS) {
+    for (int i0 = lo + warp; i0 < hi; i0 += 8 * SL_WARPS) {
         float4 m[8];
         bool ok[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {  // counts and means are read together
             const int i = i0 + q * SL_WARPS;
-            ok[q] = i < k && cnt[i] > 0;
-            m[q] = i < k ? reinterpret_cast<const float4 *>(ms + (size_t)i * ld)[lane]
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            ok[q] = i < hi && cnt[i] > 0;
+            m[q] = i < hi ? reinterpret_cast<const float4 *>(ms + (size_t)i * ld)[lane]
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * SL_WARPS;
             float d0 = __fsub_rn(xv.x, m[q].x), d1 = __fsub_rn(xv.y, m[q].y);
             float d2 = __fsub_rn(xv.z, m[q].z), d3 = __fsub_rn(xv.w, m[q].w);
             float acc = __fmaf_rn(d3, d3, __fmaf_rn(d2, d2, __fmaf_rn(d1, d1, d0 * d0)));
 #pragma unroll
             for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (ok[q]) keep2(b1, i1, b2, acc, i0 + q * SL_WARPS);
-            if (lane == 0 && i0 + q * SL_WARPS < k) red.d32[i0 + q * SL_WARPS] = ok[q] ? acc : INFINITY;
+            if (ok[q]) keep2(b1, i1, b2, acc, i);
+            if (lane == 0 && i < hi) red.d32[i - lo] = ok[q] ? acc : INFINITY;
         }
     }
     if (lane == 0) {
@@ -111,21 +127,21 @@ __device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, con
         }
     }
     __syncthreads();
-    b1 = red.out_b1;
-    b2 = red.out_b2;
-    i1 = red.out_i1;
-    if (i1 == 0x7fffffff) return -1;
-    if (b2 == INFINITY || certified(b1, b2)) return i1;
-    // The exact rule among the groups whose fp32 distance is within the error bound: warp
-    // w takes candidates w, w + W, ...; the warp stages the candidate's mean in shared
-    // memory and lane 0 sums the fp64 squares in index order (the key's fp32 copy holds
-    // its bf16 values exactly).
-    const float thr = b1 * (1.f + 2.5f * kCertRel);
+}
+
+// Block-wide: the exact rule (R5: fp64, index order, lowest index on ties) among the
+// groups lo .. hi-1 whose fp32 distance (red.d32, from score_range) is at most thr, into
+// red.out_d / red.out_di.  Warp w takes candidates lo + w, lo + w + W, ...; the warp
+// stages the candidate's mean in shared memory and lane 0 sums the fp64 squares (the
+// key's fp32 copy holds its bf16 values exactly).
+__device__ void exact_range(const float *ms, int ld, int lo, int hi, float thr, const float *xs,
+                            SlideRed &red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     double best = INFINITY;
     int bi = 0x7fffffff;
     float *mw = red.mean[warp];
-    for (int i = warp; i < k; i += SL_WARPS) {
-        if (!(red.d32[i] <= thr)) continue;
+    for (int i = lo + warp; i < hi; i += SL_WARPS) {
+        if (!(red.d32[i - lo] <= thr)) continue;
         reinterpret_cast<float4 *>(mw)[lane] = reinterpret_cast<const float4 *>(ms + (size_t)i * ld)[lane];
         __syncwarp();
         if (lane == 0) {
@@ -134,21 +150,9 @@ __device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, con
                 const double df = __dsub_rn((double)xs[j], (double)mw[j]);
                 dd = __dadd_rn(dd, __dmul_rn(df, df));
             }
-            if (dd < best || (dd == best && i < bi)) {
-                best = dd;
-                bi = i;
-            }
+            keep_min(best, bi, dd, i);
         }
         __syncwarp();
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ob < best || (ob == best && oi < bi)) {
-            best = ob;
-            bi = oi;
-        }
     }
     if (lane == 0) {
         red.d[warp] = best;
@@ -162,15 +166,30 @@ __device__ int nearest_group(const float *ms, int ld, const int *cnt, int k, con
         for (int o = 16; o; o >>= 1) {
             const double ob = __shfl_xor_sync(0xffffffffu, best, o);
             const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ob < best || (ob == best && oi < bi)) {
-                best = ob;
-                bi = oi;
-            }
+            keep_min(best, bi, ob, oi);
         }
-        if (lane == 0) red.out_di = bi;
+        if (lane == 0) {
+            red.out_d = best;
+            red.out_di = bi;
+        }
     }
     __syncthreads();
-    return red.out_di;
+}
+
+// Block-wide, one CTA: the nearest of the k groups with count > 0 under the exact rule;
+// -1 when none is non-empty.
+__device__ int nearest_local(const float *ms, int ld, const int *cnt, int k, const float *xs,
+                             SlideRed &red) {
+    score_range(ms, ld, cnt, 0, k, xs, red);
+    const float b1 = red.out_b1, b2 = red.out_b2;
+    const int i1 = red.out_i1;
+    __syncthreads();
+    if (i1 == 0x7fffffff) return -1;
+    if (b2 == INFINITY || certified(b1, b2)) return i1;
+    exact_range(ms, ld, 0, k, b1 * (1.f + 2.5f * kCertRel), xs, red);
+    const int r = red.out_di;
+    __syncthreads();
+    return r;
 }
 
 // Welford's update of one group (count n, mean and variance rows ms[0..d), ms[d..2d),
@@ -197,15 +216,21 @@ __device__ __forceinline__ void welford(int n, float *ms, float *vb, uint16_t *v
     }
 }
 
-// One CTA per unit, after the append kernel has advanced the lengths.
+// One cluster of CS CTAs per unit (grid (CS, units)), after the append kernel has advanced
+// the lengths.  Every decision is computed identically by all CTAs of the cluster, so that
+// they take the same path through every cluster barrier.
 __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
     __shared__ __align__(16) float xs[MOG_D], vs[MOG_D];
     __shared__ SlideRed red;
-    const int u = blockIdx.x, tid = threadIdx.x;
+    __shared__ int s_top;
+    const int CS = (int)cluster.num_blocks(), rk = (int)cluster.block_rank();
+    const int u = blockIdx.y, tid = threadIdx.x;
     int *ui = dv.unit_info + u * UI_STRIDE;
     const int C = ui[UI_C], L = ui[UI_L], b = ui[UI_B], h = u % dv.h_kv;
     const int p = ui[UI_RLO];
-    if (dv.n_now[b] - p <= R) return;  // the window still holds at most R keys
+    if (dv.n_now[b] - p <= R) return;  // the window still holds at most R keys (whole cluster)
     const uint16_t *kr = dv.krow(b, h, p), *vr = dv.vrow(b, h, p);
     if (tid < MOG_D) {
         xs[tid] = bf1(kr[tid]);
@@ -213,66 +238,113 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
     }
     __syncthreads();
     const size_t cg0 = (size_t)u * dv.c_max, sg0 = (size_t)u * dv.c_max * dv.l_max;
-    const int c = nearest_group(dv.cl_ms + cg0 * 2 * MOG_D, 2 * MOG_D, dv.cl_n + cg0, C, xs, red);
-    if (c < 0) return;  // no cluster to join: the window grows instead
-    const int l = nearest_group(dv.sub_ms + (sg0 + (size_t)c * L) * 2 * MOG_D, 2 * MOG_D,
+    const float *cms = dv.cl_ms + cg0 * 2 * MOG_D;
+    // 1. the nearest non-empty cluster: slices scored per CTA, merged over the cluster
+    const int lo = (int)((int64_t)C * rk / CS), hi = (int)((int64_t)C * (rk + 1) / CS);
+    score_range(cms, 2 * MOG_D, dv.cl_n + cg0, lo, hi, xs, red);
+    cluster.sync();
+    float b1 = INFINITY, b2 = INFINITY;
+    int i1 = 0x7fffffff;
+    for (int r = 0; r < CS; ++r) {
+        const SlideRed *o = cluster.map_shared_rank(&red, r);
+        merge2(b1, i1, b2, o->out_b1, o->out_i1, o->out_b2);
+    }
+    int c = i1;
+    if (i1 != 0x7fffffff && !(b2 == INFINITY || certified(b1, b2))) {
+        exact_range(cms, 2 * MOG_D, lo, hi, b1 * (1.f + 2.5f * kCertRel), xs, red);
+        cluster.sync();
+        double best = INFINITY;
+        int bi = 0x7fffffff;
+        for (int r = 0; r < CS; ++r) {
+            const SlideRed *o = cluster.map_shared_rank(&red, r);
+            keep_min(best, bi, o->out_d, o->out_di);
+        }
+        c = bi;
+    }
+    cluster.sync();  // every CTA is done reading the others' results
+    if (c == 0x7fffffff) return;  // no cluster to join: the window grows instead
+    // 2. the nearest non-empty subcluster of c (each CTA on its own, identically)
+    const int l = nearest_local(dv.sub_ms + (sg0 + (size_t)c * L) * 2 * MOG_D, 2 * MOG_D,
                                 dv.sub_n + sg0 + (size_t)c * L, L, xs, red);
     if (l < 0) {  // a non-empty cluster has a non-empty subcluster; reaching here is corrupt
-        if (tid == 0) flag_error(dv.status, ST_BAD_INDEX);
+        if (tid == 0 && rk == 0) flag_error(dv.status, ST_BAD_INDEX);
         return;
     }
-    const size_t cg = cg0 + c, sg = sg0 + (size_t)c * L + l;
-    const int ncl = dv.cl_n[cg], nsub = dv.sub_n[sg];
-    welford(ncl, dv.cl_ms + cg * 2 * MOG_D, dv.cl_vbar + cg * MOG_D, dv.cl_vhl + cg * 2 * MOG_D, xs, vs);
-    welford(nsub, dv.sub_ms + sg * 2 * MOG_D, dv.sub_vbar + sg * MOG_D, dv.sub_vhl + sg * 2 * MOG_D, xs, vs);
-    // The partition: every later non-empty subcluster moves its first row to its end and
-    // every later offset grows by one.  Batches of eight subclusters per thread run from
-    // the top down, reads before writes, so that no batch reads a slot that a batch above
-    // it has written; s_top keeps the old offset at the top of the batch below.
+    const size_t cgi = cg0 + c, sgi = sg0 + (size_t)c * L + l;
+    const int ncl = dv.cl_n[cgi], nsub = dv.sub_n[sgi];
+    // 3-4. The partition: every later non-empty subcluster moves its first row to its end and
+    // every later offset grows by one.  Batches run from the top down over all threads of
+    // the cluster, reads before writes (a cluster barrier between), so that no batch reads
+    // a slot a batch above it has written; s_top (in every CTA) keeps the old offset at the
+    // top of the batch below.
     const int CL = C * L, g = c * L + l;
     int *so = dv.sub_off + (size_t)u * dv.sub_off_stride;
     int *pm = dv.perm + (size_t)u * dv.n_cap;
-    constexpr int B8 = 8, BATCH = B8 * SL_THREADS;
-    __shared__ int s_top;
+    constexpr int B4 = 4;
+    const int nthr = CS * SL_THREADS, gt = rk * SL_THREADS + tid, batch = B4 * nthr;
     const int first = g + 1, old_end = so[CL];
     if (tid == 0) s_top = old_end;
-    __syncthreads();
-    for (int bi = (CL - first + BATCH - 1) / BATCH - 1; bi >= 0; --bi) {
-        const int base = first + bi * BATCH, top = min(CL, base + BATCH);
-        int a[B8], e[B8], v[B8];
+    cluster.sync();  // every CTA has chosen (c, l) from the means before they change
+    if (rk == 0) {   // 3. Welford
+        welford(ncl, dv.cl_ms + cgi * 2 * MOG_D, dv.cl_vbar + cgi * MOG_D, dv.cl_vhl + cgi * 2 * MOG_D, xs, vs);
+        welford(nsub, dv.sub_ms + sgi * 2 * MOG_D, dv.sub_vbar + sgi * MOG_D, dv.sub_vhl + sgi * 2 * MOG_D, xs,
+                vs);
+    }
+    for (int bi = (CL - first + batch - 1) / batch - 1; bi >= 0; --bi) {
+        const int base = first + bi * batch, top = min(CL, base + batch);
+        const int below_top = s_top;
+        int a[B4], e[B4], v[B4];
 #pragma unroll
-        for (int q = 0; q < B8; ++q) {
-            const int gg = base + q * SL_THREADS + tid;
+        for (int q = 0; q < B4; ++q) {
+            const int gg = base + q * nthr + gt;
             a[q] = gg < top ? so[gg] : 0;
-            e[q] = gg < top ? (gg + 1 == top ? s_top : so[gg + 1]) : 0;
+            e[q] = gg < top ? (gg + 1 == top ? below_top : so[gg + 1]) : 0;
         }
 #pragma unroll
-        for (int q = 0; q < B8; ++q) v[q] = a[q] < e[q] ? pm[a[q]] : 0;
-        __syncthreads();
+        for (int q = 0; q < B4; ++q) v[q] = a[q] < e[q] ? pm[a[q]] : 0;
+        cluster.sync();
 #pragma unroll
-        for (int q = 0; q < B8; ++q) {
-            const int gg = base + q * SL_THREADS + tid;
+        for (int q = 0; q < B4; ++q) {
+            const int gg = base + q * nthr + gt;
             if (gg < top) {
                 if (a[q] < e[q]) pm[e[q]] = v[q];
                 so[gg] = a[q] + 1;
             }
         }
-        if (tid == 0) s_top = a[0];  // the old offset of subcluster `base`
-        __syncthreads();
+        if (gt == 0)  // the old offset of subcluster `base`, to every CTA
+            for (int r = 0; r < CS; ++r) *cluster.map_shared_rank(&s_top, r) = a[0];
+        cluster.sync();
     }
-    if (tid == 0) {
+    if (rk == 0 && tid == 0) {
         pm[s_top] = p;  // the old end of subcluster g
         so[CL] = old_end + 1;
-        dv.cl_n[cg] = ncl + 1;
-        dv.sub_n[sg] = nsub + 1;
+        dv.cl_n[cgi] = ncl + 1;
+        dv.sub_n[sgi] = nsub + 1;
         ui[UI_NMID] += 1;
         ui[UI_RLO] = p + 1;
     }
 }
 
 cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s) {
-    k_slide<<<pl.units, SL_THREADS, 0, s>>>(dv, pl.R);
-    return cudaGetLastError();
+    // CTAs per unit: one for up to 4096 subclusters (there the cluster barriers cost more
+    // than they save), else one per 2048, at most 8, and few enough that every unit's
+    // cluster is resident
+    const int64_t groups = (int64_t)pl.c_max * pl.l_max;
+    const int want = groups <= 4096 ? 1 : (int)std::min<int64_t>(SL_MAX_CS, (groups + 2047) / 2048);
+    const int cs = std::max(1, std::min(want, num_sms() / std::max(1, pl.units)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, pl.units);
+    cfg.blockDim = dim3(SL_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = cs;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_slide, dv, pl.R);
 }
 
 }  // namespace mog

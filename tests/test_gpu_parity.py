@@ -498,17 +498,13 @@ def test_union_exact_sixteen_heads_many_units():
     print("union-exact decode", _check_decode_union(inj))
 
 
-def test_sliding_window_matches_oracle():
-    """Sliding recent window: after each append the oldest recent key of every KV head
-    joins a cluster.  The GPU's choice is the exact argmin under its own means at that
-    moment; the oracle replays the same moves (Welford in fp64); statistics, partition,
-    window and decode then agree."""
-    steps, n0 = 40, 3000
-    w = small_workload(n0, batch=2, h_kv=2, h_q=8, n_recent=32, seed=81)
-    inj = Injected(w, n_cap=n0 + steps, sliding=1)
-    rng = np.random.default_rng(8)
+def _slide_steps(inj, n0, steps, seed):
+    """Append `steps` random tokens to a sliding-window handle; after each, check that the
+    key that moved into every KV head's clusters went to the exact argmin under the GPU's
+    own means, and replay the move in the oracle."""
+    w = inj.w
+    rng = np.random.default_rng(seed)
     L, U = w.n_sub, w.batch * w.h_kv
-    lay = inj.h.layout()
     for t in range(steps):
         before = inj.gpu_summaries()
         kn = wl.to_bf16(rng.standard_normal((w.batch, w.h_kv, D)))
@@ -532,19 +528,49 @@ def test_sliding_window_matches_oracle():
             smeans = before["sub_ms"][u, c * L + subs, 0].astype(np.float64)
             assert subs[ora.assign(x, smeans)[0]] == l, (t, u)
             inj.summ[(b, h)], _ = ora.slide(inj.K[b, h], inj.V[b, h], s, force=(c, l))
+
+
+def _check_partition(inj):
+    w, lay = inj.w, inj.h.layout()
+    L, U = w.n_sub, w.batch * w.h_kv
     info = inj.h.array("unit_info", torch.int32, (U, 8)).cpu().numpy()
     perm = inj.h.array("perm", torch.int32, (U, lay.n_cap)).cpu().numpy()
     off = inj.h.array("sub_off", torch.int32, (U, lay.sub_off_stride)).cpu().numpy()
     for u in range(U):
         s = inj.summ[(u // w.h_kv, u % w.h_kv)]
         Cn = s["C"]
-        assert info[u, 5] == s["n_build"] - s["R"] and info[u, 3] == s["perm"].size
+        assert info[u, 5] == max(s["S"], s["n_build"] - s["R"]) and info[u, 3] == s["perm"].size
         assert np.array_equal(off[u, :Cn * L + 1], s["sub_off"])
         for g in range(Cn * L):
             a, e = s["sub_off"][g], s["sub_off"][g + 1]
             assert np.array_equal(np.sort(perm[u, a:e]), np.sort(s["perm"][a:e])), (u, g)
+
+
+def test_sliding_window_matches_oracle():
+    """Sliding recent window: after each append the oldest recent key of every KV head
+    joins a cluster.  The GPU's choice is the exact argmin under its own means at that
+    moment; the oracle replays the same moves (Welford in fp64); statistics, partition,
+    window and decode then agree."""
+    steps, n0 = 40, 3000
+    w = small_workload(n0, batch=2, h_kv=2, h_q=8, n_recent=32, seed=81)
+    inj = Injected(w, n_cap=n0 + steps, sliding=1)
+    _slide_steps(inj, n0, steps, seed=8)
+    _check_partition(inj)
     print("sliding: stats worst", _check_stats(inj))
     print("sliding: decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
+
+
+def test_sliding_window_large_partition_cluster_of_ctas():
+    """A 256 x 20 partition (5120 subclusters): the slide runs as a cluster of several CTAs
+    per KV head (slices of the cluster search, batches of the partition update)."""
+    steps, n0 = 16, 12000
+    w = small_workload(n0, batch=1, h_kv=2, h_q=4, centres=300, n_clusters=256, n_sub=20,
+                       top_c=6, top_s=4, n_recent=24, seed=83)
+    inj = Injected(w, mode="planted", n_cap=n0 + steps, sliding=1)
+    _slide_steps(inj, n0, steps, seed=10)
+    _check_partition(inj)
+    print("sliding, large partition: stats worst", _check_stats(inj))
+    print("sliding, large partition: decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
 
 
 def test_sliding_window_union_exact_ragged_batch():
