@@ -186,8 +186,13 @@ int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev, const int32_
 /*
  * Append one decode token per sequence: k_new_dev, v_new_dev bf16 [batch][h_kv][d] are
  * written at position n_now[b] of the cache, then n_now[b] += 1.  Appended keys join the
- * recent anchors; summaries are unchanged.  MOG_ERR_CAPACITY if a sequence would exceed
- * n_cap (checked on the host from the build lengths and the number of appends).
+ * recent anchors; without MOG_FLAG_SLIDING the summaries are unchanged and the window
+ * grows.  With it, a second kernel then moves each KV head's oldest recent key into its
+ * nearest cluster and subcluster once the window holds more than n_recent keys (see
+ * MOG_FLAG_SLIDING), updating that head's counts, means, variances, value means,
+ * partition and window start in the arena.  MOG_ERR_CAPACITY if a sequence would exceed
+ * n_cap (checked on the host from the build lengths and the number of appends).  Not to
+ * be run concurrently with a decode on the same handle.
  */
 int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void *stream);
 
