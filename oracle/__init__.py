@@ -282,3 +282,43 @@ def slide(K: np.ndarray, V: np.ndarray, summ: dict, force=None):
     s["sub_off"][g + 1:] += 1
     s["n_build"] += 1
     return s, (c, l)
+
+
+def group_selection(qs, summ: dict, top_c: int, top_s: int, score_mode: int = 0):
+    """Group-shared selection (a variant of this library; the pages select per query head):
+    the query heads qs[G][d] of one KV head select once.  A group's score is the log of the
+    sum over the heads of exp(its per-head selection score) -- the log of the group's total
+    estimated attention mass -- and the top_c clusters, then the top_s subclusters inside
+    each, are taken by that score (descending, index ascending, empty groups never).
+    Returns (sel_c[top_c], sel_s[top_c, top_s], group cluster scores[C], group subcluster
+    scores[C, L]), -1 padded."""
+    Cn, L = summ["C"], summ["L"]
+    cl = np.full((len(qs), Cn), -np.inf)
+    sub = np.full((len(qs), Cn, L), -np.inf)
+    for g, q in enumerate(qs):  # every head's scores of every group
+        sc_all, _, cs, ss = select(q, summ, Cn, L, score_mode)
+        cl[g] = cs
+        for i, c in enumerate(sc_all):
+            if c >= 0:
+                sub[g, c] = ss[i]
+    with np.errstate(invalid="ignore"):
+        gc = np.logaddexp.reduce(cl, axis=0)
+        gs = np.logaddexp.reduce(sub, axis=0)
+    sel_c = np.full(max(top_c, 1), -1, np.int32)
+    sel_s = np.full((max(top_c, 1), max(top_s, 1)), -1, np.int32)
+    order = [int(i) for i in np.lexsort((np.arange(Cn), -gc)) if np.isfinite(gc[i]) and summ["cl_n"][i] > 0]
+    for r, c in enumerate(order[:top_c]):
+        sel_c[r] = c
+        so = [int(l) for l in np.lexsort((np.arange(L), -gs[c])) if np.isfinite(gs[c, l])
+              and summ["sub_n"][c * L + l] > 0]
+        sel_s[r, :len(so[:top_s])] = so[:top_s]
+    return sel_c[:top_c], sel_s[:top_c, :top_s], gc, gs
+
+
+def mog_group_shared(K, V, n_now, qs, summ, top_c, top_s, score_mode=0, residual=True):
+    """Group-shared decode: every head attends exactly the anchors and the rows of the
+    group's selection, and takes its own Gaussian residual of every other non-empty group.
+    Returns (out[G][d], sel_c, sel_s)."""
+    sel_c, sel_s, _, _ = group_selection(qs, summ, top_c, top_s, score_mode)
+    outs = [decode(K, V, n_now, q, summ, sel_c, sel_s, residual)[0] for q in qs]
+    return np.stack(outs), sel_c, sel_s

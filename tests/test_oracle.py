@@ -519,3 +519,50 @@ def test_slide_with_no_nonempty_cluster_is_a_no_op(ora):
     b = ora.build_unit(K, V, 200, 4, 196, 3, 2)       # everything is an anchor
     s, cl = ora.slide(K, V, b)
     assert cl is None and s["n_build"] == b["n_build"] and s["perm"].size == 0
+
+
+# -------------------------------------------------- group-shared selection (variant)
+
+def _log_mass_np(q, n, mu, var):
+    """ln n + tau q.mu + tau^2/2 sum_j q_j^2 var_j, restated with numpy (-inf if empty)."""
+    qf = f64(q)
+    with np.errstate(divide="ignore"):
+        return np.where(n > 0, np.log(np.maximum(n, 1)) + TAU * (mu @ qf) + 0.5 * TAU ** 2 * (var @ qf ** 2),
+                        -np.inf)
+
+
+def test_group_selection_matches_numpy_log_sum_exp(ora):
+    w, K, V, qs, b = _union_case(ora, G=4, seed=6)
+    sel_c, sel_s, gc, gs = ora.group_selection(qs, b, w.top_c, w.top_s)
+    Cn, L = b["C"], b["L"]
+    cl = np.stack([_log_mass_np(q, b["cl_n"], b["cl_mu"], b["cl_var"]) for q in qs])
+    sub = np.stack([_log_mass_np(q, b["sub_n"], b["sub_mu"], b["sub_var"]) for q in qs])
+    gc_ref = np.log(np.exp(cl - cl.max(0)).sum(0)) + cl.max(0)
+    order = [c for c in np.lexsort((np.arange(Cn), -gc_ref)) if b["cl_n"][c] > 0][:w.top_c]
+    assert list(sel_c) == order
+    np.testing.assert_allclose(gc[b["cl_n"] > 0], gc_ref[b["cl_n"] > 0], rtol=1e-12, atol=1e-9)
+    for r, c in enumerate(order):
+        s = sub[:, c * L:(c + 1) * L]
+        gsc = np.log(np.exp(s - s.max(0)).sum(0)) + s.max(0)
+        so = [l for l in np.lexsort((np.arange(L), -gsc)) if b["sub_n"][c * L + l] > 0][:w.top_s]
+        assert list(sel_s[r][:len(so)]) == so and np.all(sel_s[r][len(so):] == -1)
+
+
+def test_group_shared_with_one_head_or_identical_heads_is_the_standard_decode(ora):
+    w, K, V, qs, b = _union_case(ora, G=1, seed=7)
+    ref, _, _, _ = ora.mog_head(K, V, w.n, qs[0], b, w.top_c, w.top_s)
+    out, _, _ = ora.mog_group_shared(K, V, w.n, qs, b, w.top_c, w.top_s)
+    assert rel_l2(out[0], ref) < 1e-14
+    out3, _, _ = ora.mog_group_shared(K, V, w.n, np.repeat(qs, 3, axis=0), b, w.top_c, w.top_s)
+    for g in range(3):
+        assert rel_l2(out3[g], ref) < 1e-14
+
+
+def test_group_shared_all_selected_is_dense_and_rows_are_shared(ora):
+    w, K, V, qs, b = _union_case(ora, G=4, seed=8)
+    out, sel_c, sel_s = ora.mog_group_shared(K, V, w.n, qs, b, w.n_clusters, w.n_sub)
+    for g in range(len(qs)):
+        assert rel_l2(out[g], dense_ref(K, V, w.n, qs[g])) < 1e-12
+    _, sel_c, sel_s = ora.mog_group_shared(K, V, w.n, qs, b, w.top_c, w.top_s)
+    n_rows = [ora.decode(K, V, w.n, q, b, sel_c, sel_s)[1][2] for q in qs]
+    assert len(set(n_rows)) == 1      # every head attends the same rows
