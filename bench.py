@@ -54,6 +54,9 @@ def args_():
     ap.add_argument("--sliding", action="store_true",
                     help="sliding recent window; the cache gets room for the append timing "
                          "that follows the decode timing")
+    ap.add_argument("--group-select", action="store_true",
+                    help="group-shared selection: the query heads of a KV head select once, "
+                         "by the log-sum-exp of their scores")
     ap.add_argument("--union-exact", action="store_true",
                     help="GQA union-exact mode: every query head attends the union of the "
                          "chosen subclusters of its KV group")
@@ -252,7 +255,8 @@ def run_gpu(a, w, rank, world):
     del K, V
     prm = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], n_clusters=w.n_clusters, n_sub=w.n_sub,
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
-                          union_exact=int(a.union_exact), sliding=int(a.sliding))
+                          union_exact=int(a.union_exact), sliding=int(a.sliding),
+                          group_select=int(a.group_select))
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -402,7 +406,8 @@ def run_gpu(a, w, rank, world):
         "config": {"workload": w.name, "batch": w.batch, "h_kv": w.h_kv, "h_q": w.h_q, "d": D,
                    "context": int(lens.max()), "clusters": w.n_clusters, "subclusters": w.n_sub,
                    "top_c": w.top_c, "top_s": w.top_s, "n_sink": w.n_sink, "n_recent": w.n_recent,
-                   "mode": "union-exact" if a.union_exact else "per-head selection",
+                   "mode": ("group-shared selection" if a.group_select else "per-head selection")
+                           + (", union-exact" if a.union_exact else ""),
                    "recent_window": "sliding" if a.sliding else "growing",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},

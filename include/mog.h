@@ -65,7 +65,8 @@ typedef enum {
  *  score_mode        : 0 = log-mass score ln n + tau q.mu + tau^2/2 sum q^2 sigma2 (the
  *                      residual's own exponent); 1 = tau q.mu only.
  *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
- *  flags             : 0, or any of MOG_FLAG_UNION_EXACT, MOG_FLAG_SLIDING.
+ *  flags             : 0, or any of MOG_FLAG_UNION_EXACT, MOG_FLAG_SLIDING,
+ *                      MOG_FLAG_GROUP_SELECT.
  *
  * MOG_FLAG_UNION_EXACT (a variant of this library; the pages select per query head and do
  * not define it): each query head still makes its own selection, but every query head of a
@@ -86,6 +87,17 @@ typedef enum {
  * that subcluster is chosen.  A head with no non-empty cluster keeps a growing window.
  */
 #define MOG_FLAG_SLIDING 2
+/*
+ * MOG_FLAG_GROUP_SELECT (a variant of this library; the pages select per query head): the
+ * G query heads of a KV head select once.  A group's score is the log of the sum over the
+ * heads of exp(its per-head selection score), the log of the group's total estimated
+ * attention mass; the top_c clusters and the top_s subclusters inside each are taken by
+ * that score.  Every head attends the group's selection exactly and takes its own Gaussian
+ * residual of every other non-empty group.  Fewer rows are read than with per-head
+ * selections.  The exported selection repeats the group's lists for every head; a given
+ * selection (mog_decode_ex) is taken from the group's first head.
+ */
+#define MOG_FLAG_GROUP_SELECT 4
 typedef struct mog_params {
     int32_t batch, h_kv, h_q, d;
     int32_t n_cap;

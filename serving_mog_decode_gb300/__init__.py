@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libmog.so")
 MOG_OK = 0
 FLAG_UNION_EXACT = 1  # MOG_FLAG_UNION_EXACT in mog.h
 FLAG_SLIDING = 2      # MOG_FLAG_SLIDING in mog.h
+FLAG_GROUP_SELECT = 4  # MOG_FLAG_GROUP_SELECT in mog.h
 STATUS = ["MOG_OK", "MOG_ERR_INVALID_ARG", "MOG_ERR_SHAPE", "MOG_ERR_ARENA_TOO_SMALL",
           "MOG_ERR_CUDA", "MOG_ERR_DEVICE_CHECK", "MOG_ERR_TIMEOUT", "MOG_ERR_NOT_IMPLEMENTED",
           "MOG_ERR_CAPACITY"]
@@ -136,10 +137,11 @@ def _kv(K, V):
 
 def make_params(batch, h_kv, h_q, n_cap, *, d=128, n_clusters=0, n_sub=0, top_c=8, top_s=8,
                 n_sink=4, n_recent=256, iters_l1=10, iters_l2=10, score_mode=0, residual=1,
-                union_exact=0, sliding=0):
+                union_exact=0, sliding=0, group_select=0):
     return Params(batch, h_kv, h_q, d, n_cap, n_clusters, n_sub, top_c, top_s, n_sink,
                   n_recent, iters_l1, iters_l2, score_mode, residual,
-                  (FLAG_UNION_EXACT if union_exact else 0) | (FLAG_SLIDING if sliding else 0))
+                  (FLAG_UNION_EXACT if union_exact else 0) | (FLAG_SLIDING if sliding else 0)
+                  | (FLAG_GROUP_SELECT if group_select else 0))
 
 
 def arena_bytes(params: Params, lengths_host) -> int:

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 #include <set>
 #include <tuple>
@@ -50,17 +51,19 @@ int num_sms() {
     return n;
 }
 
+// The attribute is an upper bound, so it only ever grows: a launch that needs less than
+// the largest value set so far for (kernel, device) needs no call.
 cudaError_t ensure_smem(const void *fn, size_t bytes) {
     static std::mutex mu;
-    static std::set<std::tuple<const void *, int, size_t>> done;
+    static std::map<std::pair<const void *, int>, size_t> top;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(mu);
-    auto key = std::make_tuple(fn, dev, bytes);
-    if (done.count(key)) return cudaSuccess;
+    size_t &cur = top[std::make_pair(fn, dev)];
+    if (bytes <= cur) return cudaSuccess;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) done.insert(key);
+    if (e == cudaSuccess) cur = bytes;
     return e;
 }
 
@@ -85,7 +88,7 @@ static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
 
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
-    if ((p->flags & ~(MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING)) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
+    if ((p->flags & ~(MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT)) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
         p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
         p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
         (p->score_mode != 0 && p->score_mode != 1) || (p->residual != 0 && p->residual != 1))
@@ -109,6 +112,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.residual = p->residual;
     P.union_exact = (p->flags & MOG_FLAG_UNION_EXACT) ? 1 : 0;
     P.sliding = (p->flags & MOG_FLAG_SLIDING) ? 1 : 0;
+    P.group_select = (p->flags & MOG_FLAG_GROUP_SELECT) ? 1 : 0;
     P.R = p->n_recent;
     P.c_max = P.l_max = 1;
     P.n_mid_max = 0;
@@ -209,6 +213,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.score_mode = P.score_mode;
     d.residual = P.residual;
     d.union_exact = P.union_exact;
+    d.group_select = P.group_select;
     d.P = P.P;
     d.nseg_max = P.nseg_max;
     d.cimg_ustride = P.cimg_ustride;

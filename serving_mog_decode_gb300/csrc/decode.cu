@@ -91,6 +91,22 @@ __device__ __forceinline__ void quad_scores(const float *ms, int n, bool valid, 
     }
 }
 
+// Group score of a summary for the group-shared selection: the log of the sum over the G
+// heads of exp(selection score) (-inf when every score is -inf).
+template <int GT>
+__device__ __forceinline__ float group_score(const float (&sl)[GT], int G) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < GT; ++g)
+        if (g < G) mx = fmaxf(mx, sl[g]);
+    if (mx == -INFINITY) return -INFINITY;
+    float sum = 0.f;
+#pragma unroll
+    for (int g = 0; g < GT; ++g)
+        if (g < G) sum += expf(sl[g] - mx);
+    return mx + logf(sum);
+}
+
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
 }
@@ -244,6 +260,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     int *selu = dv.sel + (size_t)u * G * a.SW;
     const bool resid = dv.residual != 0;
     const bool uex = dv.union_exact != 0;  // every head attends the union's subclusters
+    const bool grp = dv.group_select != 0;  // one selection per KV head, by log-sum-exp
+    const int GS = grp ? 1 : G;             // selection lists
     const uint32_t allg = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
     const bool pooled = tc > 0 && !a.sel_in;  // selection from the scores (not given)
 
@@ -270,6 +288,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
                     ckey[g * m.SLp + cl] = rank_key(sl[g], c);
                     crs[g * m.SL + cl] = res[g];
                 }
+            if (grp) ckey[cl] = rank_key(group_score<GT>(sl, G), c);
             cnn[cl] = n;
         }
     }
@@ -285,7 +304,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     __syncthreads();
     if (pooled) {
         // this slice's top-KC per head (KC = min(slice, tc)) by rank, 0 padded ...
-        for (int e = tid; e < G * ns; e += NT) {
+        for (int e = tid; e < GS * ns; e += NT) {
             const int g = e / ns, i = e % ns;
             const unsigned long long x = ckey[g * m.SLp + i];
             if (x == 0ull) continue;
@@ -294,8 +313,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
         }
         __syncthreads();
         // ... pushed into every CTA's pool, rank-major: pool[g][r][k]
-        for (int e = tid; e < CS * G * KC; e += NT) {
-            const int dst = e / (G * KC), q = e % (G * KC), g = q / KC, r = q % KC;
+        for (int e = tid; e < CS * GS * KC; e += NT) {
+            const int dst = e / (GS * KC), q = e % (GS * KC), g = q / KC, r = q % KC;
             cluster.map_shared_rank(allc_k, dst)[g * m.NPOOL + r * CS + k] = cand_k[q];
         }
     }
@@ -303,7 +322,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
 
     // ------------------------------------------------------- P2: selection and union
     if (pooled) {  // CTA k ranks pool entries e = k, k + CS, ... and pushes the winners
-        for (int e = k + CS * tid; e < G * npool; e += CS * NT) {
+        for (int e = k + CS * tid; e < GS * npool; e += CS * NT) {
             const int g = e / npool;
             const unsigned long long x = allc_k[g * m.NPOOL + e % npool];
             if (x == 0ull) continue;
@@ -313,18 +332,18 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
                     cluster.map_shared_rank(selc, dst)[g * tc + rank] = key_index(x);
         }
     } else if (tc > 0) {
-        for (int e = tid; e < G * tc; e += NT) {
+        for (int e = tid; e < GS * tc; e += NT) {  // (group mode: head 0's row)
             const int g = e / tc, r = e % tc;
             const int cc = a.sel_in[((size_t)u * G + g) * a.SW + r];
             selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
         }
     }
     cluster.sync();  // S1b: every CTA holds the full top-tc lists
-    for (int e = tid; e < G * tc; e += NT) {
+    for (int e = tid; e < GS * tc; e += NT) {
         const int c = selc[e];
         if (c < 0) continue;
         atomicOr(&bm[c >> 5], 1u << (c & 31));
-        if (c >= c0 && c < c0 + ns) atomicOr(&slm[c - c0], 1u << (e / tc));
+        if (c >= c0 && c < c0 + ns) atomicOr(&slm[c - c0], grp ? allg : 1u << (e / tc));
     }
     __syncthreads();
     {  // union = set bits of bm, ascending: ucl[0 .. Uc)
@@ -358,8 +377,9 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     if (k == 0) {  // the cluster part of the exported selection
         for (int e = tid; e < G * tc; e += NT) {
             const int g = e / tc, r = e % tc;
-            selu[(size_t)g * a.SW + r] = selc[e];
-            if (selc[e] < 0)
+            const int cs = selc[(grp ? 0 : g) * tc + r];
+            selu[(size_t)g * a.SW + r] = cs;
+            if (cs < 0)
                 for (int kk = 0; kk < ts; ++kk) selu[(size_t)g * a.SW + tc + r * ts + kk] = -1;
         }
     }
@@ -390,6 +410,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
                     sres[(s * G + g) * MOG_MAX_L + l] = res[g];
                     ssl[(s * G + g) * MOG_MAX_L + l] = sl[g];
                 }
+            if (grp) ssl[(s * G) * MOG_MAX_L + l] = group_score<GT>(sl, G);
         }
     }
     for (int e = tid; e < nmy * MOG_MAX_L; e += NT) smask[e] = 0u;
@@ -398,11 +419,11 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     __syncthreads();
     // top-ts subclusters of every head that chose a slot's cluster
     for (int e = warp; e < nmy * G; e += W) {
-        const int s = e / G, g = e % G;
+        const int s = e / G, g = e % G, gs = grp ? 0 : g;  // gs: the selection head g follows
         const int c = ucl[k + s * CS];
         int rk = -1;  // the rank at which head g chose c
         for (int r0 = 0; r0 < tc && rk < 0; r0 += 32) {
-            const uint32_t hit = __ballot_sync(0xffffffffu, r0 + lane < tc && selc[g * tc + r0 + lane] == c);
+            const uint32_t hit = __ballot_sync(0xffffffffu, r0 + lane < tc && selc[gs * tc + r0 + lane] == c);
             if (hit) rk = r0 + __ffs(hit) - 1;
         }
         if (rk < 0) continue;
@@ -410,7 +431,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
         int *subs = selu + (size_t)g * a.SW + tc + (size_t)rk * ts;
         const int *nn = snn + s * MOG_MAX_L;
         if (a.sel_in) {
-            const int32_t *si = a.sel_in + ((size_t)u * G + g) * a.SW + tc + (size_t)rk * ts;
+            const int32_t *si = a.sel_in + ((size_t)u * G + gs) * a.SW + tc + (size_t)rk * ts;
             for (int r = lane; r < ts; r += 32) {
                 const int l2 = si[r];
                 const bool ok = l2 >= 0 && l2 < L && nn[l2] > 0;
@@ -418,7 +439,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
                 if (ok) atomicOr(&smask[s * MOG_MAX_L + l2], 1u << g);
             }
         } else {
-            const float *sc = ssl + (s * G + g) * MOG_MAX_L;
+            const float *sc = ssl + (s * G + gs) * MOG_MAX_L;
             const unsigned long long x = lane < L ? rank_key(sc[lane], lane) : 0ull;
             int rank = 0;
             for (int j = 0; j < L; ++j) rank += rank_key(sc[j], j) > x;

@@ -37,6 +37,7 @@ struct Dev {
     // shape
     int batch, h_kv, G, units, n_cap, c_max, l_max, tc, ts, T1, T2, score_mode, residual;
     int union_exact;  // every head attends the union of the heads' chosen subclusters
+    int group_select;  // one selection per KV head (log-sum-exp of the heads' scores)
     int P, nchunks, nseg_max;
     int64_t sub_off_stride;
     float tau;
@@ -71,7 +72,7 @@ struct Dev {
 // Host-side plan: sizes and byte offsets of every array in the arena.
 struct Plan {
     int batch, h_kv, h_q, G, d, n_cap, units, c_max, l_max, tc, ts, T1, T2;
-    int score_mode, residual, union_exact, sliding, R, P, nchunks, n_mid_max, nseg_max;
+    int score_mode, residual, union_exact, group_select, sliding, R, P, nchunks, n_mid_max, nseg_max;
     int64_t sub_off_stride;
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
         o_sub_vbar, o_cl_vhl, o_sub_vhl, o_l1_assign, o_status, o_l1_steps;

@@ -189,7 +189,8 @@ class Injected:
     """A batch whose (cluster, subcluster) partition is given: the oracle's own build of
     each unit (small cases) or a rule applied to positions (large cases)."""
 
-    def __init__(self, w, lens=None, mode="oracle", n_cap=None, union_exact=0, sliding=0):
+    def __init__(self, w, lens=None, mode="oracle", n_cap=None, union_exact=0, sliding=0,
+                 group_select=0):
         self.w = w
         lens = wl.lengths(w) if lens is None else np.asarray(lens, np.int32)
         self.lens = lens
@@ -201,7 +202,8 @@ class Injected:
         self.summ = {}
         self.prm = mog.make_params(B, Hkv, Hkv * G, self.n_cap, n_clusters=w.n_clusters,
                                    n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink,
-                                   n_recent=w.n_recent, union_exact=union_exact, sliding=sliding)
+                                   n_recent=w.n_recent, union_exact=union_exact, sliding=sliding,
+                                   group_select=group_select)
         stride = mog.sub_off_stride(self.prm, lens)
         perm_all = np.zeros((B * Hkv, self.n_cap), np.int32)
         off_all = np.zeros((B * Hkv, stride), np.int32)
@@ -609,6 +611,68 @@ def test_sliding_window_union_exact_ragged_batch():
         assert info[u, 5] == max(s["S"], s["n_build"] - s["R"])
     inj.lens = lens + steps
     print("sliding + union-exact: stats", _check_stats(inj), "decode", _check_decode_union(inj))
+
+
+def _check_decode_group(inj):
+    """Group-shared selection: the GPU's selection against the oracle's group selection
+    (differences only at near-ties), repeated for every head; then every head's output
+    under the oracle's group selection."""
+    w, G = inj.w, inj.w.group
+    tc, ts, SW = w.top_c, w.top_s, w.top_c + w.top_c * w.top_s
+    U = w.batch * w.h_kv
+    sel_out = torch.full((U * G, SW), -7, dtype=torch.int32, device=DEV)
+    inj.h.decode(inj.qd, sel_out=sel_out)
+    gsel = sel_out.cpu().numpy()
+    sel_ref = np.full((U * G, SW), -1, np.int32)
+    ties = 0
+    for u in range(U):
+        b, h = u // w.h_kv, u % w.h_kv
+        s = inj.summ[(b, h)]
+        sc, ss, gc, gsc = ora.group_selection(inj.q[b, h * G:(h + 1) * G], s, tc, ts)
+        for g in range(G):
+            sel_ref[u * G + g, :tc] = sc
+            sel_ref[u * G + g, tc:] = ss.reshape(-1)
+            assert np.array_equal(gsel[u * G + g], gsel[u * G])   # the group's lists, repeated
+        if not np.array_equal(gsel[u * G, :tc], sc):
+            cut = gc[sc[sc >= 0]].min()
+            for c in set(gsel[u * G, :tc].tolist()) ^ set(sc.tolist()):
+                assert c >= 0 and abs(gc[c] - cut) < TIE, ("group cluster selection", u, c)
+            ties += 1
+            continue
+        gs = gsel[u * G, tc:].reshape(tc, ts)
+        for i in range(tc):
+            if sc[i] >= 0 and not np.array_equal(gs[i], ss[i]):
+                row = gsc[sc[i]]
+                cut = row[ss[i][ss[i] >= 0]].min()
+                for l in set(gs[i].tolist()) ^ set(ss[i].tolist()):
+                    assert l >= 0 and abs(row[l] - cut) < TIE, ("group sub selection", u, i, l)
+                ties += 1
+    out = inj.h.decode(inj.qd, sel_in=torch.from_numpy(sel_ref).to(DEV)).cpu().numpy().reshape(U * G, D)
+    worst = 0.0
+    for u in range(U):
+        b, h = u // w.h_kv, u % w.h_kv
+        s = inj.summ[(b, h)]
+        for g in range(G):
+            ref, _ = ora.decode(inj.K[b, h], inj.V[b, h], int(inj.lens[b]), inj.q[b, h * G + g], s,
+                                sel_ref[u * G + g, :tc], sel_ref[u * G + g, tc:].reshape(tc, ts))
+            e = rel(out[u * G + g], ref)
+            worst = max(worst, e)
+            assert e <= OUT_TOL, (u, g, e)
+    assert inj.h.sync_status() == 0
+    return ties, worst
+
+
+def test_group_shared_selection_matches_oracle():
+    w = small_workload(2500, h_kv=2, h_q=8, top_c=5, top_s=3, seed=91)
+    inj = Injected(w, group_select=1)
+    print("group-shared decode", _check_decode_group(inj))
+
+
+def test_group_shared_selection_sixteen_heads_ragged():
+    w = small_workload(1800, batch=2, h_kv=2, h_q=32, centres=40, n_clusters=30, n_sub=6,
+                       top_c=6, top_s=2, n_recent=32, seed=92)
+    inj = Injected(w, lens=np.array([1800, 900], np.int32), group_select=1, union_exact=1)
+    print("group-shared decode, 16 heads", _check_decode_group(inj))
 
 
 def test_sixteen_query_heads_per_kv_head():
