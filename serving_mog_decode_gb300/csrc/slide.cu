@@ -218,14 +218,20 @@ __device__ __forceinline__ void welford(int n, float *ms, float *vb, uint16_t *v
 
 // One cluster of CS CTAs per unit (grid (CS, units)), after the append kernel has advanced
 // the lengths.  Every decision is computed identically by all CTAs of the cluster, so that
-// they take the same path through every cluster barrier.
+// they take the same path through every cluster barrier.  CLU = false: one CTA per unit,
+// launched without a cluster, with block barriers.
+template <bool CLU>
 __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
+    auto csync = [&]() {
+        if constexpr (CLU) cluster.sync();
+        else __syncthreads();
+    };
     __shared__ __align__(16) float xs[MOG_D], vs[MOG_D];
     __shared__ SlideRed red;
     __shared__ int s_top;
-    const int CS = (int)cluster.num_blocks(), rk = (int)cluster.block_rank();
+    const int CS = CLU ? (int)cluster.num_blocks() : 1, rk = CLU ? (int)cluster.block_rank() : 0;
     const int u = blockIdx.y, tid = threadIdx.x;
     int *ui = dv.unit_info + u * UI_STRIDE;
     const int C = ui[UI_C], L = ui[UI_L], b = ui[UI_B], h = u % dv.h_kv;
@@ -242,26 +248,26 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
     // 1. the nearest non-empty cluster: slices scored per CTA, merged over the cluster
     const int lo = (int)((int64_t)C * rk / CS), hi = (int)((int64_t)C * (rk + 1) / CS);
     score_range(cms, 2 * MOG_D, dv.cl_n + cg0, lo, hi, xs, red);
-    cluster.sync();
+    csync();
     float b1 = INFINITY, b2 = INFINITY;
     int i1 = 0x7fffffff;
     for (int r = 0; r < CS; ++r) {
-        const SlideRed *o = cluster.map_shared_rank(&red, r);
+        const SlideRed *o = CLU ? cluster.map_shared_rank(&red, r) : &red;
         merge2(b1, i1, b2, o->out_b1, o->out_i1, o->out_b2);
     }
     int c = i1;
     if (i1 != 0x7fffffff && !(b2 == INFINITY || certified(b1, b2))) {
         exact_range(cms, 2 * MOG_D, lo, hi, b1 * (1.f + 2.5f * kCertRel), xs, red);
-        cluster.sync();
+        csync();
         double best = INFINITY;
         int bi = 0x7fffffff;
         for (int r = 0; r < CS; ++r) {
-            const SlideRed *o = cluster.map_shared_rank(&red, r);
+            const SlideRed *o = CLU ? cluster.map_shared_rank(&red, r) : &red;
             keep_min(best, bi, o->out_d, o->out_di);
         }
         c = bi;
     }
-    cluster.sync();  // every CTA is done reading the others' results
+    csync();  // every CTA is done reading the others' results
     if (c == 0x7fffffff) return;  // no cluster to join: the window grows instead
     // 2. the nearest non-empty subcluster of c (each CTA on its own, identically)
     const int l = nearest_local(dv.sub_ms + (sg0 + (size_t)c * L) * 2 * MOG_D, 2 * MOG_D,
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
     const int nthr = CS * SL_THREADS, gt = rk * SL_THREADS + tid, batch = B4 * nthr;
     const int first = g + 1, old_end = so[CL];
     if (tid == 0) s_top = old_end;
-    cluster.sync();  // every CTA has chosen (c, l) from the means before they change
+    csync();  // every CTA has chosen (c, l) from the means before they change
     if (rk == 0) {   // 3. Welford
         welford(ncl, dv.cl_ms + cgi * 2 * MOG_D, dv.cl_vbar + cgi * MOG_D, dv.cl_vhl + cgi * 2 * MOG_D, xs, vs);
         welford(nsub, dv.sub_ms + sgi * 2 * MOG_D, dv.sub_vbar + sgi * MOG_D, dv.sub_vhl + sgi * 2 * MOG_D, xs,
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
         }
 #pragma unroll
         for (int q = 0; q < B4; ++q) v[q] = a[q] < e[q] ? pm[a[q]] : 0;
-        cluster.sync();
+        csync();
 #pragma unroll
         for (int q = 0; q < B4; ++q) {
             const int gg = base + q * nthr + gt;
@@ -311,9 +317,14 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
                 so[gg] = a[q] + 1;
             }
         }
-        if (gt == 0)  // the old offset of subcluster `base`, to every CTA
-            for (int r = 0; r < CS; ++r) *cluster.map_shared_rank(&s_top, r) = a[0];
-        cluster.sync();
+        if (gt == 0) {  // the old offset of subcluster `base`, to every CTA
+            if constexpr (CLU) {
+                for (int r = 0; r < CS; ++r) *cluster.map_shared_rank(&s_top, r) = a[0];
+            } else {
+                s_top = a[0];
+            }
+        }
+        csync();
     }
     if (rk == 0 && tid == 0) {
         pm[s_top] = p;  // the old end of subcluster g
@@ -332,6 +343,10 @@ cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s) {
     const int64_t groups = (int64_t)pl.c_max * pl.l_max;
     const int want = groups <= 4096 ? 1 : (int)std::min<int64_t>(SL_MAX_CS, (groups + 2047) / 2048);
     const int cs = std::max(1, std::min(want, num_sms() / std::max(1, pl.units)));
+    if (cs == 1) {
+        k_slide<false><<<dim3(1, pl.units), SL_THREADS, 0, s>>>(dv, pl.R);
+        return cudaGetLastError();
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, pl.units);
     cfg.blockDim = dim3(SL_THREADS);
@@ -344,7 +359,7 @@ cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_slide, dv, pl.R);
+    return cudaLaunchKernelEx(&cfg, k_slide<true>, dv, pl.R);
 }
 
 }  // namespace mog
