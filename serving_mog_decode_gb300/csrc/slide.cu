@@ -359,7 +359,13 @@ cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_slide<true>, dv, pl.R);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_slide<true>, dv, pl.R);
+    if (e == cudaErrorClusterOutOfResources || e == cudaErrorInvalidConfiguration) {
+        cudaGetLastError();  // no room for the clusters here: one CTA per unit instead
+        k_slide<false><<<dim3(1, pl.units), SL_THREADS, 0, s>>>(dv, pl.R);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace mog
