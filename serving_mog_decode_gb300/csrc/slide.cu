@@ -360,7 +360,7 @@ cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_slide<true>, dv, pl.R);
-    if (e == cudaErrorClusterOutOfResources || e == cudaErrorInvalidConfiguration) {
+    if (e == cudaErrorInvalidClusterSize || e == cudaErrorInvalidConfiguration) {
         cudaGetLastError();  // no room for the clusters here: one CTA per unit instead
         k_slide<false><<<dim3(1, pl.units), SL_THREADS, 0, s>>>(dv, pl.R);
         e = cudaGetLastError();
