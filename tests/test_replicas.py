@@ -60,3 +60,20 @@ def test_reference_arm_rank_nonzero_does_no_work(capsys):
         cpu_seconds, steps, warmup, gpus = 1.0, 1, 1, 2
     bench.run_reference(A(), None, rank=1)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_json_line():
+    """bench.py --impl reference on the host cores: one JSON line with the contract's keys,
+    the oracle as the CPU baseline, no host-device traffic."""
+    import json
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny-4k", "--steps", "2", "--warmup", "1", "--cpu-seconds", "0.5"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["config"]["workload"] == "tiny-4k"
+    assert d["value"] > 0 and d["higher_is_better"] is False and d["steps"] == 2
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
