@@ -1,5 +1,6 @@
-"""Host logic of the replicas-only multi-GPU mode, on CPU with two gloo ranks: the job time
-is the maximum over ranks, and the reference arm runs on rank 0 only."""
+"""Host logic of the benchmark, on CPU: the replicas-only multi-GPU mode with two gloo ranks
+(the job time is the maximum over ranks, the reference arm runs on rank 0 only), the
+reference arm's JSON line, and the algorithmic byte count behind the roofline."""
 import os
 import socket
 import subprocess
@@ -77,3 +78,43 @@ def test_reference_arm_prints_one_json_line():
     assert d["value"] > 0 and d["higher_is_better"] is False and d["steps"] == 2
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_bench_counts_algorithmic_bytes_from_the_selection():
+    """The bench's byte count on a hand-made unit: the union of the heads' choices, the
+    anchors of a grown window, and the residual items, checked against numbers worked out
+    by hand (C = 3 clusters x L = 2 subclusters, G = 2 heads, top 2 x 1, P = 4 splits)."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class Lay:
+        units, c_max, l_max, group, sub_off_stride = 1, 3, 2, 2, 7
+
+    class H:
+        arrays = {"unit_info": np.array([[3, 2, 100, 21, 4, 90, 0, 0]], np.int32),
+                  "sub_off": np.array([[0, 5, 8, 10, 14, 20, 21]], np.int32)}
+
+        def layout(self):
+            return Lay()
+
+        def array(self, name, dtype, shape):
+            return torch.from_numpy(self.arrays[name].reshape(shape))
+
+        def splits(self):
+            return 4
+
+    class W:
+        top_c, top_s = 2, 1
+
+    # head 0 chose clusters 0 (subcluster 1) and 2 (subcluster 0); head 1 chose cluster 2
+    # (subcluster 1) and nothing else
+    sel = np.array([[0, 2, 1, 0], [2, -1, 1, -1]], np.int32)
+    by = bench.bytes_from_selection(H(), W(), sel, np.array([100]), [100])
+    # union rows 3 + 6 + 1 = 10, anchors 4 sinks + (100 - 90) recent = 14
+    assert by["rows"] == 24
+    assert by["select"] == 512 + 3 * 1028 + 2 * (2 * 1032 + 4) + 3 * 12 + 7 * 16
+    assert by["attend"] == 512 + 3 * 12 + 10 * 4 + 24 * 512 + 7 * (512 + 16) + 4 * 2 * 132 * 4
+    assert by["merge"] == 4 * 2 * 132 * 4 + 2 * 128 * 4
+    assert by["step"] == by["select"] + by["attend"] + by["merge"]
