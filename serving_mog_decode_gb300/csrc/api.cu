@@ -88,7 +88,8 @@ static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
 
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
-    if ((p->flags & ~(MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT)) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
+    const int known_flags = MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT;
+    if ((p->flags & ~known_flags) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
         p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
         p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
         (p->score_mode != 0 && p->score_mode != 1) || (p->residual != 0 && p->residual != 1))
