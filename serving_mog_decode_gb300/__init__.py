@@ -138,6 +138,13 @@ def _kv(K, V):
 def make_params(batch, h_kv, h_q, n_cap, *, d=128, n_clusters=0, n_sub=0, top_c=8, top_s=8,
                 n_sink=4, n_recent=256, iters_l1=10, iters_l2=10, score_mode=0, residual=1,
                 union_exact=0, sliding=0, group_select=0):
+    """mog_params for a batch of `batch` sequences with h_kv KV heads and h_q query heads
+    (d = 128), a KV cache of n_cap positions.  n_clusters / n_sub = 0 pick round(sqrt N)
+    and ceil(log2 N) per sequence; top_c clusters and top_s subclusters per chosen cluster
+    are attended exactly, with n_sink sink and n_recent recent anchors.  The flags select
+    the variants: union_exact (every head of a KV group attends the union of the group's
+    chosen rows), sliding (a fixed recent window whose leaving keys join the clusters),
+    group_select (one selection per KV group by the log-sum-exp of its heads' scores)."""
     return Params(batch, h_kv, h_q, d, n_cap, n_clusters, n_sub, top_c, top_s, n_sink,
                   n_recent, iters_l1, iters_l2, score_mode, residual,
                   (FLAG_UNION_EXACT if union_exact else 0) | (FLAG_SLIDING if sliding else 0)
