@@ -255,8 +255,10 @@ int dense_decode(const mog_kv *kv, const int32_t *lengths_dev, int32_t n_max, in
  * loads the library holds it until the process exits); shapes that need more return
  * MOG_ERR_CAPACITY (mog_last_error states the sizes).  Nothing is allocated, by the
  * library or any routine it calls.
- *  - The first call on a device looks up the array's device address (once per device,
- *    with that device current); make that first call before any stream capture.
+ *  - The first call on a device looks up the array's device address (with that device
+ *    current) and caches it under the current CUDA context; a call in a new context (after
+ *    cudaDeviceReset, or under another context the caller made current) looks it up again.
+ *    Make the first call in each context before any stream capture.
  *  - Every call on a device shares the one array, and each call rewrites all of it that
  *    it reads; calls that overlap on the GPU (other streams, other threads) race.
  * Arguments as dense_decode.

@@ -275,6 +275,19 @@ def dense_scratch_bytes(batch, h_kv, h_q, n_max, d=128) -> int:
     return v.value
 
 
+def _check_q_out(K, q, out):
+    """q must be a contiguous CUDA bf16 [B, H_q, 128] on K's device and out a contiguous
+    float32 tensor of q's shape on the same device: the kernels write B*H_q*128 floats."""
+    torch = _torch()
+    B = K.shape[0]
+    if (q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[0] != B or q.shape[2] != 128
+            or not q.is_contiguous() or q.device != K.device):
+        raise ValueError("q must be a contiguous bf16 tensor [B, H_q, 128] on the cache's device")
+    if (out.dtype != torch.float32 or tuple(out.shape) != tuple(q.shape) or not out.is_contiguous()
+            or out.device != q.device):
+        raise ValueError("out must be a contiguous float32 tensor of q's shape on q's device")
+
+
 def dense_decode(K, V, lengths_dev, n_max, q, out=None, scratch=None, stream=None):
     """Full-scan exact attention.  q: bf16 [B, H_q, d] -> out f32 [B, H_q, d]."""
     torch = _torch()
@@ -282,6 +295,7 @@ def dense_decode(K, V, lengths_dev, n_max, q, out=None, scratch=None, stream=Non
     H_q = q.shape[1]
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check_q_out(K, q, out)
     need = dense_scratch_bytes(B, H_kv, H_q, n_max)
     if scratch is None:
         scratch = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -296,6 +310,7 @@ def dense_decode_noalloc(K, V, lengths_dev, n_max, q, out, stream=None):
     """dense_decode whose scratch is the library's static device array: no device memory
     is allocated by this call (the caller supplies `out`)."""
     B, H_kv = K.shape[0], K.shape[1]
+    _check_q_out(K, q, out)
     kv = _kv(K, V)
     _check(lib().dense_decode_noalloc(C.byref(kv), _ptr(lengths_dev), n_max, B, H_kv, q.shape[1],
                                       128, _ptr(q), _ptr(out), _stream(stream)),

@@ -8,18 +8,23 @@
 // (sink/tail anchors attended exactly; exact and estimated numerator and denominator
 // added in the unnormalised domain, one normalisation).
 //
-// One kernel per decode step: a thread-block cluster of CS CTAs per KV head ("unit"),
-// all hand-offs in distributed shared memory behind cluster barriers:
-//  P1  CTA k scores its slice of clusters for the G query heads of the unit,
-//      s = ln n + tau q.mu + tau^2/2 sum_j q_j^2 var_j, and keeps its slice's top-tc per head;
-//  P2  every CTA reads all slices' candidates, derives each head's top-tc clusters (score
-//      descending, index ascending) and their union over the heads (ascending index);
-//  P3  CTA k takes union slots k, k+CS, ...: subcluster scores, top-ts per head that chose
-//      the cluster, the member rows of the chosen subclusters (written to a row list), and
-//      the Gaussian residual of the unselected subclusters and of its own slice clusters;
-//  P4  the unit's exact rows (anchors, then the slots' rows) are split evenly over the CS
-//      CTAs and attended (mma.sync engine), giving one partial (max, sum, acc) per CTA;
-//  P5  CTA k merges a slice of the output over all partials and normalises once.
+// Three kernels per decode step, launched back to back on one stream with programmatic
+// dependent launch (each starts while its predecessor drains and waits with
+// griddepcontrol.wait before its first dependent read):
+//  k_mog_decode  selection: one thread-block cluster of CS CTAs per KV head ("unit").
+//                Cluster scores for the G query heads, each head's top-tc clusters, their
+//                union, the subcluster scores and each head's top-ts inside every chosen
+//                cluster, the exponents of the Gaussian residual terms, and the row
+//                segments and split plan of the next kernel.  Hand-offs between the CTAs
+//                go through distributed shared memory behind cluster barriers.
+//  k_mog_rows    exact attention: grid (P, units).  Each CTA streams its share of the
+//                unit's exact rows (anchors, then the chosen subclusters' rows gathered
+//                through the partition) and then its share of the residual terms through
+//                the same mma.sync tile pipeline, and writes one unnormalised partial
+//                (max, sum, acc).
+//  k_mog_merge   grid (G, units): folds the P partials of one query head with one running
+//                maximum and normalises once.
+// k_append writes the new key and value of each sequence and advances its length.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -249,11 +254,11 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     uint32_t *shm = reinterpret_cast<uint32_t *>(sm + m.shm);  // heads that chose slot s
     __shared__ int s_wsum[W], s_uc;
 
+    // Build-time constants of the unit (never rewritten after the build) may be read
+    // before the wait; the sink count, the window start and the current length are
+    // advanced by the append and slide kernels and are read after it.
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int b = ui[UI_B], C = ui[UI_C], L = ui[UI_L];
-    const int S = ui[UI_S], rlo = ui[UI_RLO];
-    const int nnow = dv.n_now[b];
-    const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
     const size_t ug = (size_t)u * dv.c_max;               // cluster index base
     const size_t usg = (size_t)u * dv.c_max * dv.l_max;   // subcluster index base
     const uint16_t *qg = a.q + (size_t)u * G * MOG_D;
@@ -266,9 +271,14 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     const bool pooled = tc > 0 && !a.sel_in;  // selection from the scores (not given)
 
     // ------------------------------------------------------------ P0: query, weights
-    load_weights(w, qg, G, dv.tau);
+    // The query may be written by the kernel just before this one, so it is read only
+    // after the dependency wait too.
     pdl_wait();
     pdl_trigger();
+    const int S = ui[UI_S], rlo = ui[UI_RLO];
+    const int nnow = dv.n_now[b];
+    const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
+    load_weights(w, qg, G, dv.tau);
     __syncthreads();
 
     // ------------------------------------------------- P1: score this CTA's clusters

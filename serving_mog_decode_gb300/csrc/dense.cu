@@ -4,8 +4,10 @@
 // Abstract: decoding over a long context normally scans the whole KV cache; this is that
 // scan.  Split-KV: each (KV head, split) CTA streams a contiguous key range through the
 // attention engine and writes a partial (max, sum, acc); a second kernel merges them.
+#include <cuda.h>
 #include <stdio.h>
 
+#include <map>
 #include <mutex>
 
 #include "attend.cuh"
@@ -117,25 +119,55 @@ cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64
 constexpr size_t DENSE_STATIC_BYTES = 4u << 20;
 static __device__ __align__(256) float g_dense_static[DENSE_STATIC_BYTES / sizeof(float)];
 
-// Device address of g_dense_static for the current device.  In host code the symbol is
-// only a stand-in, never an address a kernel may use, so the address is asked for once per
-// device (with that device current) and cached.
+// The CUDA context current on the calling thread, as a process-unique id, through the
+// runtime's driver entry points (false if there is none or the driver cannot say).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+static bool current_context_id(unsigned long long *id) {
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+    });
+    CUcontext c = nullptr;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c) return false;
+    return get_id(c, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_dense_static in the current context.  In host code the symbol is
+// only a stand-in, never an address a kernel may use.  The address belongs to the module
+// loaded in one context: it is asked for once per context (the first call on a device,
+// with that device current, and again after a device reset makes a new context) and
+// cached under the context's id.  If the context cannot be identified the address is
+// asked for on every call.
 cudaError_t dense_static_scratch(float **ptr, size_t *bytes) {
     static std::mutex mu;
-    static float *addr[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_dense_static);
-        if (e != cudaSuccess) return e;
-        addr[dev] = static_cast<float *>(p);
-    }
-    *ptr = addr[dev];
+    static std::map<unsigned long long, float *> addr;
     *bytes = DENSE_STATIC_BYTES;
+    unsigned long long id = 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (current_context_id(&id)) {
+        auto it = addr.find(id);
+        if (it != addr.end()) {
+            *ptr = it->second;
+            return cudaSuccess;
+        }
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_dense_static);  // makes the context if needed
+    if (e != cudaSuccess) return e;
+    *ptr = static_cast<float *>(p);
+    if (current_context_id(&id)) addr[id] = *ptr;
     return cudaSuccess;
 }
 
