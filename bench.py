@@ -1,18 +1,20 @@
 #!/usr/bin/env python
 """MoG decode benchmark: microseconds per decode step per layer, and achieved HBM GB/s of
-the exact-attention kernel against the measured HBM roofline.
+the dominant decode kernel against the measured HBM roofline.
 
-Workload (default): the Qwen3-4B-shaped decode layer -- 32 query heads over 8 KV heads,
-d = 128, N = 32768 bf16 keys per KV head from the planted-centre generator, 181 clusters
-x 15 subclusters, top-8 clusters x top-8 subclusters, 4 sink + 256 recent anchors.  The
-build runs once before timing (prefill time); a step is one mog_decode of the whole
-layer.  Before every timed step L2 is made cold: a 256 MB write, then a 256 MB read.
+Workload (default): the 1M-token layer -- 32 query heads over 8 KV heads, d = 128,
+N = 1048576 bf16 keys per KV head from the planted-centre generator (4096 centres,
+sigma 0.5), 1024 clusters x 20 subclusters, top-16 clusters x top-8 subclusters, 4 sink +
+512 recent anchors.  The build runs once before timing (prefill time); a step is one
+mog_decode of the whole layer.  Before every timed step L2 is made cold: a 256 MB write,
+then a 256 MB read.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mog|reference] [--workload W]
 
 --impl reference times the CPU oracle (the plain fp64 statement of the method) on the
-host cores on a bounded sample of the same workload.  Under torchrun every rank runs an
-independent replica (the method has no cross-GPU exchange); rank 0 prints one JSON line.
+host cores, on every KV head and query head of the same layer, for K steps after W.
+Under torchrun every rank runs an independent replica (the method has no cross-GPU
+exchange); rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -48,9 +50,11 @@ def args_():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mog", choices=["mog", "reference"])
-    ap.add_argument("--workload", default="qwen3-4b-32k", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default="ctx-1m", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="budget of the oracle timing sample")
+                    help="budget of the oracle timing sample (decode steps of the whole layer)")
+    ap.add_argument("--no-ablation", action="store_true",
+                    help="skip the top-only and score-mode-1 arms")
     ap.add_argument("--sliding", action="store_true",
                     help="sliding recent window; the cache gets room for the append timing "
                          "that follows the decode timing")
@@ -135,49 +139,88 @@ class Clocks:
 
 # ------------------------------------------------------------------------ the oracle
 
-def oracle_decode_sample(w, budget_s, steps=None, warmup=0):
-    """Time the oracle's decode step (selection + exact + residual, every query head of
-    one KV head) on unit (0, 0); the oracle's own build of that unit is untimed.
-    Returns (us per step per layer, cores, description, per-step list)."""
+def oracle_layer(w, arrays=None):
+    """Per-unit inputs and oracle summaries of the whole layer (untimed set-up).  Small
+    layers use the oracle's own two-level k-means; for larger ones (whose fp64 k-means
+    takes hours) every unit gets a planted-centre/position partition: clusters by planted
+    centre, subclusters by position.  `arrays` = (K, V, q) of the batch, if already drawn.
+    Returns (units, how the partition was made) with units = [(K, V, n, q[G], summ)]."""
     import oracle
-    n = int(wl.lengths(w)[0])
-    u = wl.UnitDraw(w, 0, 0, n)
-    K, V = u.keys_values()
-    q = u.q
-    Cn, L = wl.clusters_for(w, n)
-    if n <= 65536:
-        summ = oracle.build_unit(K, V, n, w.n_sink, w.n_recent, Cn, L)
-        part = "the oracle's own two-level k-means"
-    else:  # the fp64 k-means of a long context takes hours: a position-rule partition
-        S, R = w.n_sink, w.n_recent
-        pos = np.arange(S, n - R)
-        lab = (u.z[pos] % Cn) * L + (pos % L)
-        order = np.argsort(lab, kind="stable")
-        perm = pos[order].astype(np.int32)
-        sub_off = np.searchsorted(lab[order], np.arange(Cn * L + 1)).astype(np.int32)
-        summ = oracle.stats(K, V, perm, sub_off, Cn, L)
-        summ.update(perm=perm, sub_off=sub_off, C=Cn, L=L, n_build=n, S=S, R=R)
-        part = "a planted-centre/position partition (fp64 k-means of this length is out of budget)"
-    units = w.batch * w.h_kv
+    lens = wl.lengths(w)
+    own = w.batch * w.h_kv * int(lens.max()) <= (1 << 18)
+    G, units = w.group, []
+    for b in range(w.batch):
+        n = int(lens[b])
+        Cn, L = wl.clusters_for(w, n)
+        for h in range(w.h_kv):
+            u = wl.UnitDraw(w, b, h, n)
+            if arrays is None:
+                K, V = u.keys_values()
+                q = u.q
+            else:
+                K, V = arrays[0][b, h, :n], arrays[1][b, h, :n]
+                q = arrays[2][b, h * G:(h + 1) * G]
+            S, R = w.n_sink, w.n_recent
+            if own:
+                summ = oracle.build_unit(K, V, n, S, R, Cn, L)
+            else:
+                pos = np.arange(S, max(S, n - R))
+                lab = (u.z[pos] % Cn) * L + (pos % L)
+                order = np.argsort(lab, kind="stable")
+                perm = pos[order].astype(np.int32)
+                sub_off = np.searchsorted(lab[order], np.arange(Cn * L + 1)).astype(np.int32)
+                summ = oracle.stats(K, V, perm, sub_off, Cn, L)
+                summ.update(perm=perm, sub_off=sub_off, C=Cn, L=L, n_build=n, S=S, R=R)
+            units.append((K, V, n, q, summ))
+    how = ("the oracle's own two-level k-means" if own else
+           "a planted-centre/position partition (the fp64 k-means of this layer is out of budget)")
+    return units, how
 
-    def one():
-        for g in range(w.group):
-            oracle.mog_head(K, V, n, q[g], summ, w.top_c, w.top_s)
 
-    for _ in range(warmup):
-        one()
-    times = []
-    t_end = time.perf_counter() + budget_s
-    while (steps is None and (time.perf_counter() < t_end or len(times) < 3)) or \
-            (steps is not None and len(times) < steps):
-        t0 = time.perf_counter()
-        one()
-        times.append((time.perf_counter() - t0) * 1e6 * units)
-        if steps is None and len(times) >= 1000:
-            break
-    desc = (f"KV head (b=0,h=0) of {units} with its {w.group} query heads, oracle decode step "
-            f"timed {len(times)}x, scaled x{units} to the layer; summaries from {part}, untimed")
-    return statistics.mean(times), 1, desc, times
+def oracle_decode_sample(w, budget_s, steps=None, warmup=0, arrays=None, dense_steps=0):
+    """Time the oracle's decode step (selection + exact + residual) of the whole layer:
+    every query head of every KV head, spread over a thread pool of all host cores (each
+    oracle call is single-threaded and releases the interpreter lock).  Runs `steps`
+    steps after `warmup` (or, with steps None, as many as fit in budget_s).  With
+    dense_steps > 0 the oracle's dense attention of the layer is timed too.
+    Returns (us per step per layer, cores, description, per-step list, dense us or None)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    oracle.build()
+    units, how = oracle_layer(w, arrays)
+    cores = os.cpu_count() or 1
+    tasks = [(i, g) for i in range(len(units)) for g in range(w.group)]
+
+    def head(t):
+        K, V, n, q, summ = units[t[0]]
+        oracle.mog_head(K, V, n, q[t[1]], summ, w.top_c, w.top_s)
+
+    def dense_head(t):
+        K, V, n, q, _ = units[t[0]]
+        oracle.dense(K, V, n, q[t[1]])
+
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        def one(fn):
+            t0 = time.perf_counter()
+            list(ex.map(fn, tasks))
+            return (time.perf_counter() - t0) * 1e6
+
+        for _ in range(warmup):
+            one(head)
+        times = []
+        t_end = time.perf_counter() + budget_s
+        while (steps is None and (time.perf_counter() < t_end or len(times) < 3)) or \
+                (steps is not None and len(times) < steps):
+            times.append(one(head))
+            if steps is None and len(times) >= 1000:
+                break
+        dense_us = statistics.mean(one(dense_head) for _ in range(dense_steps)) if dense_steps else None
+    desc = (f"the whole layer ({len(units)} KV heads x {w.group} query heads), oracle decode step "
+            f"timed {len(times)}x on a pool of {cores} threads; summaries from {how}, untimed")
+    if dense_us is not None:
+        desc += f"; the oracle's dense attention of the layer timed {dense_steps}x"
+    return statistics.mean(times), cores, desc, times, dense_us
 
 
 # ------------------------------------------------------------------------ GPU path
@@ -252,7 +295,7 @@ def run_gpu(a, w, rank, world):
         pad = ((0, 0), (0, 0), (0, APPEND_STEPS), (0, 0))
         K, V = np.pad(K, pad), np.pad(V, pad)
     Kd, Vd, qd = bf(K), bf(V), bf(q)
-    del K, V
+    host_arrays = (K, V, q)  # kept for the oracle's timing sample (rank 0)
     prm = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], n_clusters=w.n_clusters, n_sub=w.n_sub,
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
                           union_exact=int(a.union_exact), sliding=int(a.sliding),
@@ -320,6 +363,45 @@ def run_gpu(a, w, rank, world):
     err = ((o - dn).norm(dim=1) / dn.norm(dim=1).clamp_min(1e-30)).cpu().numpy()
     approx = {"median_rel_l2": float(np.median(err)), "p90_rel_l2": float(np.percentile(err, 90)),
               "max_rel_l2": float(err.max()), "heads": int(err.size)}
+    # ---- ablations on the same partition: top-only (no residual) and score mode 1 ----
+    ablation = None
+    if not a.no_ablation:
+        perm_t = h.array("perm", torch.int32, (lay.units, lay.n_cap)).clone()
+        off_t = h.array("sub_off", torch.int32, (lay.units, lay.sub_off_stride)).clone()
+        ablation = {}
+        for name, over in (("top_only", dict(residual=0)), ("score_mode_1", dict(score_mode=1))):
+            kw = dict(n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s,
+                      n_sink=w.n_sink, n_recent=w.n_recent, union_exact=int(a.union_exact),
+                      sliding=int(a.sliding), group_select=int(a.group_select))
+            kw.update(over)
+            pv = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], **kw)
+            hv = mog.build(Kd, Vd, lens, pv, partition=(perm_t, off_t))
+            sv = torch.empty_like(sel)
+            ov = hv.decode(qd, sel_out=sv)
+            torch.cuda.synchronize()
+            assert hv.sync_status() == 0
+            ev_ = ((ov.reshape(-1, D).double() - dn).norm(dim=1) / dn.norm(dim=1).clamp_min(1e-30)).cpu().numpy()
+            byv = bytes_from_selection(hv, w, sv.cpu().numpy(), lens, n_now)
+            tv = []
+            for i in range(3 + 20):
+                cold_l2()
+                torch.cuda._sleep(CUSHION_CYCLES)
+                s0, s1 = ev(), ev()
+                s0.record()
+                hv.decode(qd, ov)
+                s1.record()
+                torch.cuda.synchronize()
+                if i >= 3:
+                    tv.append(s0.elapsed_time(s1))
+            ablation[name] = {
+                "us": round(statistics.mean(tv) * 1e3, 2),
+                "kv_rows_read": int(byv["rows"]),
+                "kv_read_fraction": round(byv["rows"] / float(sum(n_now[u // w.h_kv] for u in range(lay.units))), 4),
+                "approx_vs_dense": {"median_rel_l2": round(float(np.median(ev_)), 6),
+                                    "p90_rel_l2": round(float(np.percentile(ev_, 90)), 6),
+                                    "max_rel_l2": round(float(ev_.max()), 6)}}
+            del hv, ov, sv
+        del perm_t, off_t
     # ---- the timed decode steps ----
     for _ in range(a.warmup):
         cold_l2()
@@ -398,6 +480,8 @@ def run_gpu(a, w, rank, world):
         "steps": a.steps,
         "warmup": a.warmup,
         "ms_per_step": round(mean_ms, 5),
+        "step_us_median": round(statistics.median(step_ms) * 1e3, 3),
+        "step_us_min": round(min(step_ms) * 1e3, 3),
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
@@ -429,6 +513,8 @@ def run_gpu(a, w, rank, world):
                          "frac": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9 / peak, 4)},
         "speedup_vs_dense": round(statistics.mean(dense_ms) / mean_ms, 2),
         "approx_vs_dense": {k: (round(v, 6) if isinstance(v, float) else v) for k, v in approx.items()},
+        "approx_vs_dense_top_only": ablation["top_only"]["approx_vs_dense"] if ablation else None,
+        "ablation": ablation,
         "build": {"ms": round(build_ms, 2), "l1_flop": l1_flop, "l2_flop": l2_flop,
                   "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3)},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",
@@ -437,10 +523,14 @@ def run_gpu(a, w, rank, world):
         "gpu_launches": 3 * a.steps,  # selection, rows and merge kernels per step
         "clocks": clk,
     }
-    if rank == 0:
-        mu, cores, desc, _ = oracle_decode_sample(w, a.cpu_seconds)
+    if rank == 0 and a.cpu_seconds <= 0:   # timing experiments only: no CPU baseline
+        print(json.dumps(res), flush=True)
+    elif rank == 0:
+        mu, cores, desc, _, dense_cpu = oracle_decode_sample(w, a.cpu_seconds, arrays=host_arrays,
+                                                             dense_steps=2)
         res["cpu_baseline"] = {"value": round(mu, 1), "unit": "us/step/layer", "cores": cores,
-                               "kind": "oracle", "sample": desc}
+                               "kind": "oracle", "sample": desc,
+                               "dense_us": round(dense_cpu, 1) if dense_cpu else None}
         print(json.dumps(res), flush=True)
 
 
@@ -460,7 +550,7 @@ def run_reference(a, w, rank):
         return
     import oracle
     oracle.build()
-    mu, cores, desc, times = oracle_decode_sample(w, a.cpu_seconds, steps=a.steps, warmup=a.warmup)
+    mu, cores, desc, times, _ = oracle_decode_sample(w, a.cpu_seconds, steps=a.steps, warmup=a.warmup)
     res = {"metric": METRIC, "impl": "reference", "value": round(mu, 1), "unit": "us/step/layer",
            "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
            "ms_per_step": round(mu / 1e3, 4), "higher_is_better": False, "scaling": "weak",

@@ -298,6 +298,45 @@ int mog_kmeans_assign_segments(const void *x_dev, int64_t ld, const int32_t *row
                                int32_t k, int32_t d, int32_t *assign_out_dev, void *stream);
 
 /*
+ * Build trace: the intermediate states of mog_build's two Lloyd loops ([IA]'s hierarchical
+ * partition), for step-by-step comparison with a reference implementation.  Byte offsets
+ * into the caller's trace buffer; u = b*h_kv + h indexes units, n_mid is the row stride of
+ * the assignment arrays (the longest sequence's mid-region length); mid key i of a unit is
+ * position S + i.
+ *  l1_cent   f32   [units][iters_l1][c_max][d]: the centroids first-level step t assigned to
+ *                  (step 0: the seeds)
+ *  l1_assign int32 [units][iters_l1][n_mid]: the cluster of mid key i after step t
+ *  l2_cent   f32   [units][c_max][iters_l2][l_max][d]: cluster c's second-level centroids
+ *                  used by its step t
+ *  l2_assign int32 [units][iters_l2][n_mid]: after second-level step t, the subcluster of
+ *                  the cluster member at index j of the unit's members listed by (final
+ *                  first-level cluster, position): entry cluster_start(c) + j
+ *  l2_steps  int32 [units][c_max]: second-level steps taken by each cluster
+ * A level stops early when a step changes no assignment; entries of later steps repeat
+ * the last one (first level) or stay zero (second level).  The first level's step count
+ * is mog_layout.l1_steps.
+ */
+typedef struct mog_trace_layout {
+    int32_t units, iters_l1, iters_l2, c_max, l_max, d;
+    int64_t n_mid;
+    int64_t l1_cent, l1_assign, l2_cent, l2_assign, l2_steps;
+    int64_t bytes;  /* size of the trace buffer */
+} mog_trace_layout;
+
+/* Layout and size of the build trace for these parameters and build lengths. */
+int mog_trace_layout_of(const mog_params *p, const int32_t *lengths_host, mog_trace_layout *out);
+
+/*
+ * mog_build that also records its build trace (see mog_trace_layout) into trace_dev, a
+ * caller-owned device buffer of at least mog_trace_layout_of().bytes bytes, 16-byte
+ * aligned.  The clustering and the handle are exactly those of mog_build; the trace
+ * costs a copy of the centroids and assignments after every step.  For parity tests.
+ */
+int mog_build_traced(const mog_kv *kv, const int32_t *lengths_dev, const int32_t *lengths_host,
+                     const mog_params *p, void *arena_dev, size_t arena_bytes, void *trace_dev,
+                     size_t trace_bytes, void *stream, mog_handle **out);
+
+/*
  * mog_build with the partition given instead of clustered: perm_dev int32 [units][n_cap]
  * lists each unit's mid positions ordered by (cluster, subcluster, position) and
  * sub_off_dev int32 [units][sub_off_stride] the offsets (C_u*L_u+1 used, relative to the
@@ -309,6 +348,18 @@ int mog_build_from_partition(const mog_kv *kv, const int32_t *lengths_dev,
                              const int32_t *perm_dev, const int32_t *sub_off_dev,
                              void *arena_dev, size_t arena_bytes, void *stream,
                              mog_handle **out);
+
+/*
+ * Self-check of the bounded device waits (no counterpart in the papers).  Every wait of the
+ * library's kernels on an mbarrier (the tensor-core assignment's pipeline) gives up after
+ * a fixed number of polls, records MOG_ERR_TIMEOUT in the status word and lets the kernel
+ * return, so that a lost arrival cannot hang the GPU.  This call runs that same wait on a
+ * one-arrival mbarrier with `limit` polls: with arrive != 0 the arrival is made first and
+ * the call returns MOG_OK; with arrive == 0 nothing completes the barrier and the call
+ * returns MOG_ERR_TIMEOUT, leaving the CUDA context usable.  scratch_dev: one int32 of
+ * device memory.  Synchronises `stream`.
+ */
+int mog_check_bounded_wait(int32_t limit, int32_t arrive, int32_t *scratch_dev, void *stream);
 
 #ifdef __cplusplus
 }

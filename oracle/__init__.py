@@ -47,8 +47,8 @@ def lib():
     if _lib is None:
         build()
         l = C.CDLL(_LIB)
-        for name in ("ora_assign", "ora_lloyd", "ora_stats", "ora_build", "ora_select",
-                     "ora_decode", "ora_dense"):
+        for name in ("ora_assign", "ora_update", "ora_lloyd", "ora_stats", "ora_build",
+                     "ora_select", "ora_decode", "ora_dense"):
             getattr(l, name).restype = C.c_int
         _lib = l
     return _lib
@@ -83,6 +83,21 @@ def assign(x: np.ndarray, cent: np.ndarray, rows=None) -> np.ndarray:
     out = np.empty(rows.shape[0], np.int32)
     _check(lib().ora_assign(_ptr(x), _i64(d), _ptr(rows), _i64(rows.shape[0]), _ptr(cent),
                             _i64(cent.shape[0]), _i64(d), _ptr(out)), "assign")
+    return out
+
+
+def update(x: np.ndarray, a: np.ndarray, cent: np.ndarray, rows=None) -> np.ndarray:
+    """One centroid update (R6): the fp64 mean of the rows x[rows] assigned to each
+    centroid by `a`; a centroid with no rows keeps its value from `cent`."""
+    x = _u16(x)
+    d = x.shape[1]
+    rows = np.arange(x.shape[0], dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    a = np.ascontiguousarray(a, np.int32)
+    if a.shape[0] != rows.shape[0]:
+        raise ValueError("one assignment per row")
+    out = np.array(cent, np.float64, copy=True, order="C")
+    _check(lib().ora_update(_ptr(x), _i64(d), _ptr(rows), _i64(rows.shape[0]), _ptr(a),
+                            _i64(out.shape[0]), _i64(d), _ptr(out)), "update")
     return out
 
 

@@ -128,6 +128,30 @@ static void update_means(const uint16_t *x, int64_t ld, const int64_t *rows, int
 }
 
 /*
+ * The update step on its own (R6), for lockstep comparison with another implementation's
+ * steps: cent[c] becomes the fp64 mean of the rows r with a[r] == c, summed in row order;
+ * a centroid with no rows keeps its value.  cent [k*d] is read and written.
+ */
+int ora_update(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, const int32_t *a,
+               int64_t k, int64_t d, double *cent)
+{
+    if (n < 0 || k <= 0 || d <= 0)
+        return ORA_EINVAL;
+    for (int64_t r = 0; r < n; ++r)
+        if (a[r] < 0 || a[r] >= k)
+            return ORA_EINVAL;
+    double *sum = malloc((size_t)(k * d) * sizeof(double));
+    int64_t *cnt = malloc((size_t)k * sizeof(int64_t));
+    if (!sum || !cnt) {
+        free(sum); free(cnt);
+        return ORA_ENOMEM;
+    }
+    update_means(x, ld, rows, n, a, k, d, cent, sum, cnt);
+    free(sum); free(cnt);
+    return ORA_OK;
+}
+
+/*
  * Lloyd's algorithm over the rows listed in `rows` (ascending positions), k centroids,
  * at most `iters` assignment steps (R3, R4).
  *   cent_out  [k*d]   centroids used by the last assignment step

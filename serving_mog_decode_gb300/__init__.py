@@ -53,6 +53,12 @@ class Layout(C.Structure):
                                            "l1_steps", "fallback")])
 
 
+class TraceLayout(C.Structure):
+    _fields_ = ([(n, C.c_int32) for n in ("units", "iters_l1", "iters_l2", "c_max", "l_max", "d")] +
+                [(n, C.c_int64) for n in ("n_mid", "l1_cent", "l1_assign", "l2_cent", "l2_assign",
+                                           "l2_steps", "bytes")])
+
+
 _lib = None
 _P = C.c_void_p
 _SIGS = {
@@ -62,6 +68,8 @@ _SIGS = {
     "mog_build": (C.c_int, [_P, _P, _P, _P, _P, C.c_size_t, _P, _P]),
     "mog_build_from_partition": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P, _P]),
     "mog_sub_off_stride": (C.c_int, [_P, _P, _P]),
+    "mog_trace_layout_of": (C.c_int, [_P, _P, _P]),
+    "mog_build_traced": (C.c_int, [_P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, _P]),
     "mog_decode": (C.c_int, [_P, _P, _P, _P]),
     "mog_decode_ex": (C.c_int, [_P, _P, _P, _P, _P, _P]),
     "mog_decode_phased": (C.c_int, [_P, _P, _P, _P, _P, _P, _P]),
@@ -80,6 +88,7 @@ _SIGS = {
                                     C.c_size_t, _P, _P]),
     "mog_kmeans_assign_segments": (C.c_int, [_P, C.c_int64, _P, _P, C.c_int32, _P, C.c_int32,
                                              C.c_int32, _P, _P]),
+    "mog_check_bounded_wait": (C.c_int, [C.c_int32, C.c_int32, _P, _P]),
 }
 
 
@@ -233,9 +242,43 @@ class Handle:
         return self.arena[off:off + n * itemsize].view(dtype).view(*shape)
 
 
-def build(K, V, lengths, params: Params, stream=None, partition=None) -> Handle:
-    """mog_build (or mog_build_from_partition when partition=(perm, sub_off) is given).
-    `lengths` is a host sequence of int; a device copy is made."""
+class Trace:
+    """The build trace of mog_build_traced (see mog_trace_layout in mog.h) as torch views:
+    l1_cent [U, T1, c_max, d], l1_assign [U, T1, n_mid], l2_cent [U, c_max, T2, l_max, d],
+    l2_assign [U, T2, n_mid], l2_steps [U, c_max]."""
+
+    def __init__(self, buf, lay: TraceLayout):
+        torch = _torch()
+        self.buf, self.layout = buf, lay
+        U, T1, T2, cm, lm, d, nm = (lay.units, lay.iters_l1, lay.iters_l2, lay.c_max, lay.l_max,
+                                    lay.d, lay.n_mid)
+
+        def view(off, dtype, shape):
+            n = 1
+            for x in shape:
+                n *= x
+            return buf[off:off + 4 * n].view(dtype).view(*shape)
+
+        self.l1_cent = view(lay.l1_cent, torch.float32, (U, T1, cm, d))
+        self.l1_assign = view(lay.l1_assign, torch.int32, (U, T1, nm))
+        self.l2_cent = view(lay.l2_cent, torch.float32, (U, cm, T2, lm, d))
+        self.l2_assign = view(lay.l2_assign, torch.int32, (U, T2, nm))
+        self.l2_steps = view(lay.l2_steps, torch.int32, (U, cm))
+
+
+def trace_layout(params: Params, lengths_host) -> TraceLayout:
+    import numpy as np
+    lh = np.ascontiguousarray(lengths_host, np.int32)
+    lay = TraceLayout()
+    _check(lib().mog_trace_layout_of(C.byref(params), lh.ctypes.data_as(_P), C.byref(lay)),
+           "mog_trace_layout_of")
+    return lay
+
+
+def build(K, V, lengths, params: Params, stream=None, partition=None, trace=False):
+    """mog_build (or mog_build_from_partition when partition=(perm, sub_off) is given, or
+    mog_build_traced when trace=True, which returns (handle, Trace)).  `lengths` is a host
+    sequence of int; a device copy is made."""
     import numpy as np
     torch = _torch()
     lh = np.ascontiguousarray(lengths, np.int32)
@@ -246,6 +289,14 @@ def build(K, V, lengths, params: Params, stream=None, partition=None) -> Handle:
     arena = arena[off:off + nbytes]
     kv = _kv(K, V)
     h = _P()
+    if trace:
+        lay = trace_layout(params, lh)
+        tbuf = torch.empty(lay.bytes, dtype=torch.uint8, device=K.device)
+        rc = lib().mog_build_traced(C.byref(kv), _ptr(ld), lh.ctypes.data_as(_P), C.byref(params),
+                                    _ptr(arena), nbytes, _ptr(tbuf), lay.bytes, _stream(stream),
+                                    C.byref(h))
+        _check(rc, "mog_build_traced")
+        return Handle(h, arena, params, K, V, ld, lh), Trace(tbuf, lay)
     if partition is None:
         rc = lib().mog_build(C.byref(kv), _ptr(ld), lh.ctypes.data_as(_P), C.byref(params),
                              _ptr(arena), nbytes, _stream(stream), C.byref(h))
@@ -347,3 +398,9 @@ def kmeans_assign_segments(x, rows, seg_off, cent, stream=None):
                                             _ptr(cent), k, 128, _ptr(out), _stream(stream)),
            "mog_kmeans_assign_segments")
     return out
+
+
+def check_bounded_wait(limit, arrive, scratch, stream=None) -> int:
+    """Run the library's bounded mbarrier wait on a barrier that is (arrive=True) or is not
+    completed; returns the status code (MOG_OK or MOG_ERR_TIMEOUT = 6)."""
+    return lib().mog_check_bounded_wait(limit, 1 if arrive else 0, _ptr(scratch), _stream(stream))

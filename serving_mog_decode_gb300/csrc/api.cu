@@ -189,6 +189,30 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     return MOG_OK;
 }
 
+void trace_layout(const Plan &P, mog_trace_layout *t) {
+    memset(t, 0, sizeof *t);
+    t->units = P.units;
+    t->iters_l1 = P.T1;
+    t->iters_l2 = P.T2;
+    t->c_max = P.c_max;
+    t->l_max = P.l_max;
+    t->d = MOG_D;
+    t->n_mid = std::max(P.n_mid_max, 1);
+    const int64_t U = P.units;
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t r = o;
+        o += al(std::max<int64_t>(bytes, 4));
+        return r;
+    };
+    t->l1_cent = take(4 * U * P.T1 * P.c_max * MOG_D);
+    t->l1_assign = take(4 * U * P.T1 * t->n_mid);
+    t->l2_cent = take(4 * U * P.c_max * P.T2 * P.l_max * MOG_D);
+    t->l2_assign = take(4 * U * P.T2 * t->n_mid);
+    t->l2_steps = take(4 * U * P.c_max);
+    t->bytes = o;
+}
+
 Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     Dev d;
     memset(&d, 0, sizeof d);
@@ -390,6 +414,48 @@ extern "C" int mog_build(const mog_kv *kv, const int32_t *lengths_dev, const int
     if (e != cudaSuccess) {
         delete h;
         return cuda_fail(e, "mog_build launch");
+    }
+    *out = h;
+    return MOG_OK;
+}
+
+extern "C" int mog_trace_layout_of(const mog_params *p, const int32_t *lengths_host,
+                                   mog_trace_layout *out) {
+    if (!out) return MOG_ERR_INVALID_ARG;
+    Plan pl;
+    int st = make_plan(p, lengths_host, &pl);
+    if (st != MOG_OK) return st;
+    trace_layout(pl, out);
+    return MOG_OK;
+}
+
+extern "C" int mog_build_traced(const mog_kv *kv, const int32_t *lengths_dev,
+                                const int32_t *lengths_host, const mog_params *p, void *arena_dev,
+                                size_t arena_bytes, void *trace_dev, size_t trace_bytes,
+                                void *stream, mog_handle **out) {
+    if (!trace_dev || !aligned16(trace_dev)) return MOG_ERR_INVALID_ARG;
+    if (out) *out = nullptr;
+    mog_trace_layout tl;
+    int st = mog_trace_layout_of(p, lengths_host, &tl);
+    if (st != MOG_OK) return st;
+    if (trace_bytes < (size_t)tl.bytes) return MOG_ERR_ARENA_TOO_SMALL;
+    mog_handle *h = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = common_build(kv, lengths_dev, lengths_host, p, arena_dev, arena_bytes, s, out, &h);
+    if (st != MOG_OK) return st;
+    char *tr = static_cast<char *>(trace_dev);
+    Dev dv = h->dev;  // the handle keeps the untraced view
+    dv.tr_l1c = reinterpret_cast<float *>(tr + tl.l1_cent);
+    dv.tr_l1a = reinterpret_cast<int *>(tr + tl.l1_assign);
+    dv.tr_l2c = reinterpret_cast<float *>(tr + tl.l2_cent);
+    dv.tr_l2a = reinterpret_cast<int *>(tr + tl.l2_assign);
+    dv.tr_l2s = reinterpret_cast<int *>(tr + tl.l2_steps);
+    dv.tr_nm = tl.n_mid;
+    cudaError_t e = cudaMemsetAsync(trace_dev, 0, (size_t)tl.bytes, s);
+    if (e == cudaSuccess) e = launch_build(dv, h->plan, s);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "mog_build_traced launch");
     }
     *out = h;
     return MOG_OK;
@@ -647,4 +713,17 @@ extern "C" int mog_kmeans_assign_segments(const void *x_dev, int64_t ld, const i
     CK(launch_assign_segments(static_cast<const uint16_t *>(x_dev), ld, rows_dev, seg_off_dev, n_seg,
                               cent_dev, k, assign_out_dev, static_cast<cudaStream_t>(stream)));
     return MOG_OK;
+}
+
+extern "C" int mog_check_bounded_wait(int32_t limit, int32_t arrive, int32_t *scratch_dev,
+                                      void *stream) {
+    if (!scratch_dev || limit <= 0) return MOG_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = 0;
+    CK(cudaMemsetAsync(scratch_dev, 0, sizeof(int32_t), s));
+    CK(launch_wait_check(limit, arrive, scratch_dev, s));
+    CK(cudaMemcpyAsync(&st, scratch_dev, sizeof st, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if (st & (1 << ST_TIMEOUT)) return MOG_ERR_TIMEOUT;
+    return st ? MOG_ERR_DEVICE_CHECK : MOG_OK;
 }

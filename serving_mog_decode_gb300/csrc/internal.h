@@ -60,6 +60,10 @@ struct Dev {
     uint32_t *segmask;     // [units][nseg_max] heads that attend the segment
     float *resx;           // [units][resx_stride]: residual exponents [item][G, padded to 4]
     int64_t resx_stride;
+    // build trace (all null unless the build is traced; see mog_trace_layout)
+    float *tr_l1c, *tr_l2c;
+    int *tr_l1a, *tr_l2a, *tr_l2s;
+    int64_t tr_nm;  // row stride of the traced assignments
 
     __host__ __device__ const uint16_t *krow(int b, int h, int64_t pos) const {
         return K + b * sb + h * sh + pos * sn;
@@ -86,6 +90,7 @@ int num_sms();
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (function, device, size)
 cudaError_t ensure_smem(const void *fn, size_t bytes);
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl);
+void trace_layout(const Plan &pl, mog_trace_layout *t);
 Dev make_dev(const Plan &pl, void *arena, const mog_kv *kv);
 void unit_clusters(const mog_params *p, int n, int *C, int *L);
 
@@ -113,6 +118,7 @@ struct KmScratch {
 };
 cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *cent, int k,
                              int32_t *assign, const KmScratch &ks, cudaStream_t s);
+cudaError_t launch_wait_check(int limit, int arrive, int *status, cudaStream_t s);
 cudaError_t launch_assign_segments(const uint16_t *x, int64_t ld, const int32_t *rows,
                                    const int32_t *seg_off, int n_seg, const float *cent, int k,
                                    int32_t *assign, cudaStream_t s);

@@ -899,13 +899,23 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
             }
             for (int m = tid; m < n; m += blockDim.x) sa[m] = -1;
         }
+        int steps2 = 0;
         for (int t = 0; t < dv.T2 && n > 0; ++t) {
             if (tid == 0) s_changed = 0;
             __syncthreads();
+            if (dv.tr_l2c) {  // traced build: the centroids of this step
+                float *tc = dv.tr_l2c + (((int64_t)u * dv.c_max + c) * dv.T2 + t) * dv.l_max * MOG_D;
+                for (int e = tid; e < L * MOG_D; e += blockDim.x) tc[e] = cs[e];
+            }
             const int my = l2_assign([&](int m) { return dv.krow(b, h, pA[m]); }, sa, n, L, cs,
                                      ring, s_cn);
             if (my) atomicAdd(&s_changed, my);
             __syncthreads();
+            steps2 = t + 1;
+            if (dv.tr_l2a) {  // ... and the assignment it made
+                int *ta = dv.tr_l2a + ((int64_t)u * dv.T2 + t) * dv.tr_nm + lo;
+                for (int m = tid; m < n; m += blockDim.x) ta[m] = sa[m];
+            }
             if (t > 0 && s_changed == 0) break;
             if (t + 1 == dv.T2) break;
             // update: each half of the block takes a run of subclusters; thread j of a
@@ -931,6 +941,7 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
             if (pref[l_b] < pref[l_e]) cs[l * MOG_D + j] = acc.s / (float)cnt[l];
             __syncthreads();
         }
+        if (dv.tr_l2s && tid == 0) dv.tr_l2s[(int64_t)u * dv.c_max + c] = steps2;
         // final order: (subcluster, position), stable
         order_members();
         if (tid < L) so[c * L + tid] = lo + pref[tid];
@@ -1496,7 +1507,18 @@ cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s) {
         const bool tma = key_map(&kmap, dv.K, pl.n_cap, dv.h_kv, pl.batch, dv.sn, dv.sh, dv.sb);
         for (int t = 0; t < pl.T1; ++t) {
             AssignJob jb = build_job(dv, t);
+            if (dv.tr_l1c &&  // traced build: the centroids this step assigns to
+                (e = cudaMemcpy2DAsync(dv.tr_l1c + (int64_t)t * pl.c_max * MOG_D,
+                                       4 * (size_t)pl.T1 * pl.c_max * MOG_D, dv.cent,
+                                       4 * (size_t)pl.c_max * MOG_D, 4 * (size_t)pl.c_max * MOG_D, U,
+                                       cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+                return e;
             if ((e = assign_step(jb, tma ? &kmap : nullptr, U, pl.n_mid_max, pl.c_max, s)) != cudaSuccess)
+                return e;
+            if (dv.tr_l1a &&  // ... and the assignment it made
+                (e = cudaMemcpy2DAsync(dv.tr_l1a + (int64_t)t * dv.tr_nm, 4 * (size_t)pl.T1 * dv.tr_nm,
+                                       dv.l1_assign, 4 * (size_t)pl.n_cap, 4 * (size_t)pl.n_mid_max, U,
+                                       cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
                 return e;
             k_sort_hist<<<dim3(pl.nchunks, U), 256, pl.c_max * sizeof(int), s>>>(dv, t);
             k_sort_colscan<<<dim3((int)ceil_div64(pl.c_max, 128), U), 128, 0, s>>>(dv, t);
@@ -1551,6 +1573,29 @@ cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *
     CUtensorMap kmap;
     const bool tma = key_map(&kmap, x, n, 1, 1, ld, ld * n, ld * n);
     return assign_step(jb, tma ? &kmap : nullptr, 1, n, k, s);
+}
+
+// Self-check of the bounded wait the tensor-core pass uses: thread 0 initialises an
+// mbarrier that expects one arrival and waits on it with `limit` polls.  With arrive != 0
+// thread 1 arrives first and the wait completes; without, nothing completes the phase and
+// the wait gives up, records ST_TIMEOUT in status[0] and the kernel returns.
+__global__ void k_wait_check(int limit, int arrive, int *status) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (arrive && threadIdx.x == 1)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(b, 0, limit)) flag_error(status, ST_TIMEOUT);
+}
+
+cudaError_t launch_wait_check(int limit, int arrive, int *status, cudaStream_t s) {
+    k_wait_check<<<1, 32, 0, s>>>(limit, arrive, status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_assign_segments(const uint16_t *x, int64_t ld, const int32_t *rows,

@@ -118,6 +118,27 @@ def test_lloyd_objective_never_increases(ora):
     assert all(b <= a * (1 + 1e-12) for a, b in zip(obj, obj[1:]))
 
 
+def test_update_is_the_member_mean_and_empty_keeps(ora):
+    """The oracle's update step on its own: numpy's mean of each centroid's rows; a
+    centroid with no rows keeps its value (R6); rows may be a subset, in any order."""
+    K, _, _ = planted(700, M=9, seed=8)
+    g = np.random.default_rng(8)
+    cent = g.standard_normal((6, D))
+    a = g.integers(0, 5, size=400).astype(np.int32)      # centroid 5 gets no rows
+    rows = g.choice(700, size=400, replace=False)
+    new = ora.update(K, a, cent, rows=rows)
+    X = f64(K)
+    for c in range(5):
+        np.testing.assert_allclose(new[c], X[rows[a == c]].mean(0), rtol=1e-13, atol=1e-14)
+    assert np.array_equal(new[5], cent[5])
+    # with the full row set it is one step of the oracle's own Lloyd loop
+    _, _, steps, hist = ora.lloyd(K, 6, 4, history=True)
+    for t in range(steps - 1):
+        assert np.array_equal(ora.update(K, ora.assign(K, hist[t]), hist[t]), hist[t + 1])
+    with pytest.raises(RuntimeError):
+        ora.update(K, np.full(700, 6, np.int32), cent)   # label out of range
+
+
 def test_lloyd_more_centroids_than_points(ora):
     K, _, _ = planted(5, M=5, seed=7)
     cent, asg, steps, _ = ora.lloyd(K, 8, 3)
@@ -185,8 +206,10 @@ def test_build_partition_is_consistent(ora):
     s1 = b["steps"][0]
     _, lab = kmeans2(X, init, iter=s1, minit="matrix", missing="warn")
     assert np.array_equal(a1, lab)
-    # the second level of every cluster is scipy's k-means on its members
-    for c in range(0, Cn, 7):
+    # the second level of every cluster is scipy's k-means on its members, run for
+    # exactly the number of steps the oracle's loop took on that cluster
+    checked = 0
+    for c in range(Cn):
         seg = np.sort(perm[off[c * L]:off[(c + 1) * L]])
         if seg.size == 0:
             continue
@@ -195,10 +218,12 @@ def test_build_partition_is_consistent(ora):
         sub_of = np.empty(seg.size, np.int64)
         for l in range(L):
             sub_of[np.isin(seg, perm[off[c * L + l]:off[c * L + l + 1]])] = l
-        # run scipy until it reproduces (it has no early stop; 10 steps at most)
-        ok = any(np.array_equal(kmeans2(Xc, init2.copy(), iter=t, minit="matrix", missing="warn")[1], sub_of)
-                 for t in range(1, 11))
-        assert ok
+        _, own, st2, _ = ora.lloyd(K, L, 10, rows=seg)
+        assert np.array_equal(own, sub_of), c
+        lab2 = kmeans2(Xc, init2.copy(), iter=st2, minit="matrix", missing="warn")[1]
+        assert np.array_equal(lab2, sub_of), (c, st2)
+        checked += 1
+    assert checked == int((b["cl_n"] > 0).sum())
 
 
 # ----------------------------------------------------------------------------- estimator
@@ -308,20 +333,53 @@ def test_appended_keys_join_recent_anchors(ora):
     assert rel_l2(out, dense_ref(K, V, 600, q)) < 1e-12
 
 
-def test_tiny_sweep_is_a_convex_combination(ora):
+def test_tiny_sweep_brute_force(ora):
+    """Tiny N (64 keys, 8 clusters x 4 subclusters): every (top_c, top_s) case against a
+    direct restatement in numpy -- scores of every group from numpy statistics of the
+    partition, the ranking by brute force, the exact set and the residual groups listed
+    by hand, and the whole mixture as one softmax."""
     K, V, q = planted(64, M=5, seed=16)
-    b = ora.build_unit(K, V, 64, 2, 6, 8, 4)
-    Y = f64(V)
-    allv = np.concatenate([Y, b["cl_vbar"], b["sub_vbar"]])
-    lo, hi = allv.min(0) - 1e-12, allv.max(0) + 1e-12
-    ref = dense_ref(K, V, 64, q)
-    for tc in range(0, 9):
-        for ts in range(0, 5):
-            out, sel_c, sel_s, diag = ora.mog_head(K, V, 64, q, b, tc, ts)
-            assert diag[1] > 0 and np.all(out >= lo) and np.all(out <= hi)
-            assert (sel_c >= 0).sum() == min(tc, int((b["cl_n"] > 0).sum()))
-            if tc == 8 and ts == 4:
-                assert rel_l2(out, ref) < 1e-12
+    S, R, Cn, L = 2, 6, 8, 4
+    b = ora.build_unit(K, V, 64, S, R, Cn, L)
+    perm, off = b["perm"], b["sub_off"]
+    Kf, qf = f64(K), f64(q)
+
+    def score(mem):
+        X = Kf[mem]
+        return math.log(len(mem)) + TAU * (qf @ X.mean(0)) + 0.5 * TAU ** 2 * float(qf ** 2 @ X.var(0))
+
+    def ranked(scores):   # (score desc, index asc) over the non-empty groups
+        return [i for _, i in sorted((-sc, i) for i, sc in scores.items())]
+
+    cl_mem = {c: perm[off[c * L]:off[(c + 1) * L]] for c in range(Cn)}
+    sub_mem = {(c, l): perm[off[c * L + l]:off[c * L + l + 1]] for c in range(Cn) for l in range(L)}
+    cl_rank = ranked({c: score(m) for c, m in cl_mem.items() if m.size})
+    anchors = list(range(S)) + list(range(64 - R, 64))
+    cases = 0
+    for tc in range(0, Cn + 1):
+        for ts in range(0, L + 1):
+            out, sel_c, sel_s, _ = ora.mog_head(K, V, 64, q, b, tc, ts)
+            chosen = cl_rank[:tc]
+            assert [int(c) for c in sel_c if c >= 0] == chosen
+            exact, groups = list(anchors), []
+            for c in range(Cn):
+                if c not in chosen:
+                    if cl_mem[c].size:
+                        groups.append(cl_mem[c])
+                    continue
+                i = chosen.index(c)
+                sub_rank = ranked({l: score(sub_mem[(c, l)]) for l in range(L) if sub_mem[(c, l)].size})
+                assert [int(l) for l in sel_s[i] if l >= 0] == sub_rank[:ts]
+                for l in range(L):
+                    if l in sub_rank[:ts]:
+                        exact += sub_mem[(c, l)].tolist()
+                    elif sub_mem[(c, l)].size:
+                        groups.append(sub_mem[(c, l)])
+            assert rel_l2(out, mixture_ref(K, V, 64, q, exact, groups)) < 1e-12, (tc, ts)
+            if tc == Cn and ts == L:
+                assert rel_l2(out, dense_ref(K, V, 64, q)) < 1e-12
+            cases += 1
+    assert cases == (Cn + 1) * (L + 1)
 
 
 def test_selection_order_and_variance_term(ora):
