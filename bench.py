@@ -422,9 +422,27 @@ def run_gpu(a, w, rank, world):
         torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     # ---- per-kernel times (events around the selection, rows and merge kernels) ----
+    # Events between the kernels stop each from starting early, so the rows and merge
+    # kernels would fetch their code from DRAM after the L2 flush with nothing to overlap
+    # it (in the step they load it while their predecessor runs).  The data stays cold;
+    # a decode on a small side handle after the flush brings the kernels' code back.
+    side = None
+    try:
+        sw = wl.Workload("side", batch=1, h_kv=w.h_kv, h_q=w.h_q, n=4096, centres=32, seed=7)
+        sK, sV, sq, sl = wl.make_batch(sw)
+        sL = min(w.n_sub if w.n_sub > 0 else 8, 8)
+        sp = mog.make_params(1, w.h_kv, w.h_q, 4096, n_clusters=32, n_sub=sL, top_c=min(w.top_c, 16),
+                             top_s=min(w.top_s, sL), n_sink=4, n_recent=64,
+                             union_exact=int(a.union_exact), group_select=int(a.group_select))
+        sKd, sVd, sqd = bf(sK), bf(sV), bf(sq)
+        side = (mog.build(sKd, sVd, sl, sp), sqd, torch.empty(sqd.shape, dtype=torch.float32, device=dev))
+    except Exception:
+        side = None
     phase = [[], [], []]
     for i in range(max(20, min(a.steps, 200))):
         cold_l2()
+        if side is not None:
+            side[0].decode(side[1], side[2])
         torch.cuda._sleep(CUSHION_CYCLES)
         evs = [ev() for _ in range(4)]
         h.decode_phased(qd, out, evs)
@@ -502,6 +520,9 @@ def run_gpu(a, w, rank, world):
                      "algorithmic_bytes_per_launch": int(kbytes[dom]),
                      "launch_us": round(pm[dom] * 1e3, 3)},
         "kernels_us": {names[i]: round(pm[i] * 1e3, 3) for i in range(3)},
+        "kernels_timing": ("events around each kernel; data cold (L2 flushed); the kernels' code "
+                           "re-warmed by a decode on a small side handle" if side is not None else
+                           "events around each kernel; data and code cold (L2 flushed)"),
         "kernels_GBps": {names[i]: round(kbytes[i] / (pm[i] * 1e-3) / 1e9, 1) for i in range(3)},
         "step_bytes": int(by["step"]),
         "step_GBps": round(by["step"] / (mean_ms * 1e-3) / 1e9, 1),

@@ -444,15 +444,15 @@ extern "C" int mog_build_traced(const mog_kv *kv, const int32_t *lengths_dev,
     st = common_build(kv, lengths_dev, lengths_host, p, arena_dev, arena_bytes, s, out, &h);
     if (st != MOG_OK) return st;
     char *tr = static_cast<char *>(trace_dev);
-    Dev dv = h->dev;  // the handle keeps the untraced view
-    dv.tr_l1c = reinterpret_cast<float *>(tr + tl.l1_cent);
-    dv.tr_l1a = reinterpret_cast<int *>(tr + tl.l1_assign);
-    dv.tr_l2c = reinterpret_cast<float *>(tr + tl.l2_cent);
-    dv.tr_l2a = reinterpret_cast<int *>(tr + tl.l2_assign);
-    dv.tr_l2s = reinterpret_cast<int *>(tr + tl.l2_steps);
-    dv.tr_nm = tl.n_mid;
+    TraceDev td;
+    td.l1c = reinterpret_cast<float *>(tr + tl.l1_cent);
+    td.l1a = reinterpret_cast<int *>(tr + tl.l1_assign);
+    td.l2c = reinterpret_cast<float *>(tr + tl.l2_cent);
+    td.l2a = reinterpret_cast<int *>(tr + tl.l2_assign);
+    td.l2s = reinterpret_cast<int *>(tr + tl.l2_steps);
+    td.nm = tl.n_mid;
     cudaError_t e = cudaMemsetAsync(trace_dev, 0, (size_t)tl.bytes, s);
-    if (e == cudaSuccess) e = launch_build(dv, h->plan, s);
+    if (e == cudaSuccess) e = launch_build(h->dev, h->plan, s, td);
     if (e != cudaSuccess) {
         delete h;
         return cuda_fail(e, "mog_build_traced launch");

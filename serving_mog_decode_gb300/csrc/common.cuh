@@ -39,6 +39,14 @@ __device__ __forceinline__ float ex2(float x) {
     return r;
 }
 
+// min(a, b, c) in one three-input instruction (the minimum of three floats; NaN inputs
+// are ignored as by fminf)
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // ------------------------------------------------------------------------------ warp ops
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -255,10 +255,10 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     __shared__ int s_wsum[W], s_uc;
 
     // Build-time constants of the unit (never rewritten after the build) may be read
-    // before the wait; the sink count, the window start and the current length are
-    // advanced by the append and slide kernels and are read after it.
+    // before the wait; the window start and the current length are advanced by the append
+    // and slide kernels and are read after it, where they are used.
     const int *ui = dv.unit_info + u * UI_STRIDE;
-    const int b = ui[UI_B], C = ui[UI_C], L = ui[UI_L];
+    const int b = ui[UI_B], C = ui[UI_C], L = ui[UI_L], S = ui[UI_S];
     const size_t ug = (size_t)u * dv.c_max;               // cluster index base
     const size_t usg = (size_t)u * dv.c_max * dv.l_max;   // subcluster index base
     const uint16_t *qg = a.q + (size_t)u * G * MOG_D;
@@ -275,9 +275,6 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     // after the dependency wait too.
     pdl_wait();
     pdl_trigger();
-    const int S = ui[UI_S], rlo = ui[UI_RLO];
-    const int nnow = dv.n_now[b];
-    const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
     load_weights(w, qg, G, dv.tau);
     __syncthreads();
 
@@ -509,6 +506,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     cluster.sync();  // S2: every slot's counts have been pushed
 
     // ------------------------------------- P4: row segments and the rows-kernel plan
+    const int rlo = __ldcg(ui + UI_RLO), nnow = __ldcg(dv.n_now + b);
+    const int s_cnt = min(S, nnow), n_anchor = s_cnt + max(0, nnow - rlo);
     if (warp == 0) {  // exclusive prefixes: rows after the anchors, segments from 0
         int rrun = n_anchor, srun = 0;
         for (int j0 = 0; j0 < Uc; j0 += 32) {
@@ -610,9 +609,22 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     constexpr int NB = GT <= 8 ? 1 : 2;  // blocks of 8 query heads
     QFrags<NB> qf;
     load_q_frags(qf, a.q + (size_t)u * G * MOG_D, G);
-    pdl_wait();  // the selection kernel's segments and plan
-    pdl_trigger();
-    {
+    // Two passes through the same code.  Pass 0 runs before the dependency wait, mostly
+    // while the selection kernel is still working (this kernel is launched early): one
+    // zero-filled tile of 64 masked rows and one empty tile of residual terms, into an
+    // accumulator that is then discarded.  It brings the tile loop's instructions into the
+    // caches, so that the real pass does not stall on instruction fetch between its memory
+    // waits.  Pass 1 waits for the selection kernel and does the work.
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+    const bool dry = pass == 0;
+    if (dry) {  // a plan of 64 anchor rows (T, anchors, sinks), no segments, no terms, L = 1
+        for (int q = tid; q < PLAN_W; q += AT_THREADS)
+            s_plan[q] = (q >= 1 && q <= 3) ? AT_ROWS : (q == 6 ? 1 : 0);
+        __syncthreads();
+    } else {
+        pdl_wait();  // the selection kernel's segments and plan
+        pdl_trigger();
         const int *plan = dv.plan + (size_t)u * PLAN_W;
         for (int q = tid; q < PLAN_W / 4; q += AT_THREADS) cp_async16(smem_u32(s_plan + 4 * q), plan + 4 * q, 16);
         cp_async_commit();
@@ -620,7 +632,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
         __syncthreads();
     }
     const int NS = s_plan[0], T = s_plan[1], n_anchor = s_plan[2], s_cnt = s_plan[3], rlo = s_plan[4];
-    const int r0 = (int)((int64_t)T * p / P), r1 = (int)((int64_t)T * (p + 1) / P);
+    const int r0 = dry ? 0 : (int)((int64_t)T * p / P), r1 = dry ? T : (int)((int64_t)T * (p + 1) / P);
     const int nrow = r1 - r0, nt = (nrow + AT_ROWS - 1) / AT_ROWS;
     const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
     const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
@@ -658,8 +670,8 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
             uint32_t mk = 0u;
             if (i <= last) {
                 if (i < n_anchor) {
-                    q = i < s_cnt ? i : rlo + (i - s_cnt);
-                    mk = allm;
+                    q = dry ? 0 : (i < s_cnt ? i : rlo + (i - s_cnt));
+                    mk = dry ? 0u : allm;
                 } else {
                     const int sg = last_le(s_segrow, wn, i);  // the segment holding row i
                     const int pi = s_segoff[sg] + (i - s_segrow[sg]);
@@ -682,9 +694,9 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
             s_mk[bt & 1][tid + jj * AT_THREADS] = (bt & 1) ? pf_mk[1][jj] : pf_mk[0][jj];
         }
     };
-    auto issue = [&](int t) {
+    auto issue = [&](int t) {  // (the warm-up tile is zero-filled: no rows are read)
         const int buf = (t / RW_TPB) & 1, rb = (t % RW_TPB) * AT_ROWS;
-        issue_tile(tile + (t % AT_STAGES) * AT_STAGE_BYTES, min(AT_ROWS, nrow - t * AT_ROWS), kb, vb,
+        issue_tile(tile + (t % AT_STAGES) * AT_STAGE_BYTES, dry ? 0 : min(AT_ROWS, nrow - t * AT_ROWS), kb, vb,
                    dv.sn, [&](int r, int64_t &pos, uint32_t &mk) {
                        int pp = s_pos[buf][rb + r];
                        uint32_t mm = s_mk[buf][rb + r];
@@ -704,7 +716,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     const int Uc = s_plan[5], L = s_plan[6], C = s_plan[7];
     const int npi = Uc * L, I = dv.residual ? npi + C : 0;
     const int ia = (int)((int64_t)I * p / P), ib = (int)((int64_t)I * (p + 1) / P);
-    const int nr = (ib - ia + AT_ROWS / 2 - 1) / (AT_ROWS / 2);
+    const int nr = dry ? 1 : (ib - ia + AT_ROWS / 2 - 1) / (AT_ROWS / 2);
     const float *rx = dv.resx + (size_t)u * dv.resx_stride;
     const size_t ug = (size_t)u * dv.c_max, usg = ug * dv.l_max;
     auto issue_terms = [&](int t, int tr) {  // tile t of the stream = terms tile tr
@@ -786,10 +798,15 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     }
     cp_async_wait<0>();
     __syncthreads();
+    if (dry) {  // keep the discarded pass from being optimised away
+        if (acc.l[0][0] == 1.5f && acc.m[0][0] == -1.5f) flag_error(dv.status, ST_BAD_SIZE);
+        continue;
+    }
     float *st = reinterpret_cast<float *>(tile);
     warp_state_out(acc, st, G);
     __syncthreads();
     merge_states(st, AT_WARPS, G, dv.partials + ((size_t)u * PART_SLOTS + p) * G * PART_W);
+    }
 }
 
 // Kernel C: grid (G, units), 512 threads.  Merges the P partials of one query head
@@ -803,9 +820,16 @@ __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials,
     const int j = tid % MOG_D, part = tid / MOG_D;
     __shared__ float s_m[MAX_SPLITS], s_l[MAX_SPLITS];
     __shared__ float s_acc[MG_PARTS][MOG_D];
-    pdl_wait();
-    pdl_trigger();
     auto src = [&](int i) { return partials + (((size_t)u * PART_SLOTS + i) * G + g) * PART_W; };
+    // Pass 0 runs the same code on whatever the partials hold before the rows kernel has
+    // finished (this kernel is launched early) and writes nothing: it brings the code into
+    // the caches.  Pass 1 waits for the rows kernel and merges.
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+        pdl_wait();
+        pdl_trigger();
+    }
     float av[MAX_SPLITS / MG_PARTS];
 #pragma unroll
     for (int q = 0; q < MAX_SPLITS / MG_PARTS; ++q) {
@@ -833,7 +857,8 @@ __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials,
     __syncthreads();
     if (part == 0) {
         for (int q = 1; q < MG_PARTS; ++q) v += s_acc[q][j];
-        out[((size_t)u * G + g) * MOG_D + j] = l > 0.f ? v / l : 0.f;
+        if (pass == 1) out[((size_t)u * G + g) * MOG_D + j] = l > 0.f ? v / l : 0.f;
+    }
     }
 }
 

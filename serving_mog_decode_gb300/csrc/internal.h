@@ -60,10 +60,6 @@ struct Dev {
     uint32_t *segmask;     // [units][nseg_max] heads that attend the segment
     float *resx;           // [units][resx_stride]: residual exponents [item][G, padded to 4]
     int64_t resx_stride;
-    // build trace (all null unless the build is traced; see mog_trace_layout)
-    float *tr_l1c, *tr_l2c;
-    int *tr_l1a, *tr_l2a, *tr_l2s;
-    int64_t tr_nm;  // row stride of the traced assignments
 
     __host__ __device__ const uint16_t *krow(int b, int h, int64_t pos) const {
         return K + b * sb + h * sh + pos * sn;
@@ -71,6 +67,14 @@ struct Dev {
     __host__ __device__ const uint16_t *vrow(int b, int h, int64_t pos) const {
         return V + b * sb + h * sh + pos * sn;
     }
+};
+
+// Device pointers of a build trace (see mog_trace_layout); all null for an untraced build.
+// Only the build's kernels take it, so that the decode kernels' parameters stay as they are.
+struct TraceDev {
+    float *l1c, *l2c;
+    int *l1a, *l2a, *l2s;
+    int64_t nm;  // row stride of the traced assignments
 };
 
 // Host-side plan: sizes and byte offsets of every array in the arena.
@@ -95,7 +99,7 @@ Dev make_dev(const Plan &pl, void *arena, const mog_kv *kv);
 void unit_clusters(const mog_params *p, int n, int *C, int *L);
 
 // launchers (return cudaError_t of the launch)
-cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s);
+cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s, const TraceDev &tr = TraceDev{});
 cudaError_t launch_stats_only(const Dev &dv, const Plan &pl, cudaStream_t s);
 cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *out,
                           const int32_t *sel_in, int32_t *sel_out, cudaStream_t s,

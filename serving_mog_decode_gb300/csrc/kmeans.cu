@@ -799,7 +799,7 @@ __device__ __forceinline__ void stream_rows(const Dev &dv, int b, int h, const i
 // (subcluster, position).  Then the summaries of the cluster and its subclusters.
 // Member rows are read through the shared-memory ring; every mean is an fp32 Kahan sum
 // in (subcluster, position) order, every variance a second pass about that mean.
-__global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmeans) {
+__global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmeans, TraceDev tr) {
     extern __shared__ __align__(16) uint8_t l2raw[];
     float *cs = reinterpret_cast<float *>(l2raw);  // [L][d] centroids, then subcluster key means
     uint8_t *ring = l2raw + MOG_MAX_L * MOG_D * sizeof(float);
@@ -903,8 +903,8 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
         for (int t = 0; t < dv.T2 && n > 0; ++t) {
             if (tid == 0) s_changed = 0;
             __syncthreads();
-            if (dv.tr_l2c) {  // traced build: the centroids of this step
-                float *tc = dv.tr_l2c + (((int64_t)u * dv.c_max + c) * dv.T2 + t) * dv.l_max * MOG_D;
+            if (tr.l2c) {  // traced build: the centroids of this step
+                float *tc = tr.l2c + (((int64_t)u * dv.c_max + c) * dv.T2 + t) * dv.l_max * MOG_D;
                 for (int e = tid; e < L * MOG_D; e += blockDim.x) tc[e] = cs[e];
             }
             const int my = l2_assign([&](int m) { return dv.krow(b, h, pA[m]); }, sa, n, L, cs,
@@ -912,8 +912,8 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
             if (my) atomicAdd(&s_changed, my);
             __syncthreads();
             steps2 = t + 1;
-            if (dv.tr_l2a) {  // ... and the assignment it made
-                int *ta = dv.tr_l2a + ((int64_t)u * dv.T2 + t) * dv.tr_nm + lo;
+            if (tr.l2a) {  // ... and the assignment it made
+                int *ta = tr.l2a + ((int64_t)u * dv.T2 + t) * tr.nm + lo;
                 for (int m = tid; m < n; m += blockDim.x) ta[m] = sa[m];
             }
             if (t > 0 && s_changed == 0) break;
@@ -941,7 +941,7 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
             if (pref[l_b] < pref[l_e]) cs[l * MOG_D + j] = acc.s / (float)cnt[l];
             __syncthreads();
         }
-        if (dv.tr_l2s && tid == 0) dv.tr_l2s[(int64_t)u * dv.c_max + c] = steps2;
+        if (tr.l2s && tid == 0) tr.l2s[(int64_t)u * dv.c_max + c] = steps2;
         // final order: (subcluster, position), stable
         order_members();
         if (tid < L) so[c * L + tid] = lo + pref[tid];
@@ -1296,27 +1296,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_assign_tc(AssignJob jb, const
                 if (hcnt > 0) tmem_ld32_nowait(tl0, vr[0]);
                 if (hcnt > 32) tmem_ld32_nowait(tl0 + 32, vr[1]);
                 tmem_wait_ld();
+                // Scores are folded two at a time: with lo <= hi the pair's own order, the
+                // two smallest of {b1 <= b2, lo, hi} are min(b1, lo) and
+                // min(b2, hi, max(b1, lo)), the latter one three-input min.
+                auto fold_block = [&](const uint32_t (&v)[32], int blk, bool full) {
+                    const float4 *cn4 = reinterpret_cast<const float4 *>(scn + c * TC_NC + h0 + blk * 32);
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    if (blk * 32 < hcnt) {
-                        const uint32_t (&v)[32] = vr[blk];
-                        const float4 *cn4 = reinterpret_cast<const float4 *>(scn + c * TC_NC + h0 + blk * 32);
-                        const bool full = blk * 32 + 32 <= hcnt;
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 cn = cn4[j4];
+                        const float cq[4] = {cn.x, cn.y, cn.z, cn.w};
 #pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 cn = cn4[j4];
-                            const float cq[4] = {cn.x, cn.y, cn.z, cn.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int j = 4 * j4 + e, z = j & 7;
-                                const float ap = __fmaf_rn(-2.f, __uint_as_float(v[j]), cq[e]);
-                                float pk = __uint_as_float((__float_as_uint(ap) & ~63u) | (uint32_t)(blk * 32 + j));
-                                if (!full && blk * 32 + j >= hcnt) pk = TC_BIG;
-                                pb2[z] = fminf(pb2[z], fmaxf(pb1[z], pk));
-                                pb1[z] = fminf(pb1[z], pk);
+                        for (int e = 0; e < 4; e += 2) {
+                            const int j = 4 * j4 + e, z = (j >> 1) & 7;
+                            const float a0 = __fmaf_rn(-2.f, __uint_as_float(v[j]), cq[e]);
+                            const float a1 = __fmaf_rn(-2.f, __uint_as_float(v[j + 1]), cq[e + 1]);
+                            float p0 = __uint_as_float((__float_as_uint(a0) & ~63u) | (uint32_t)(blk * 32 + j));
+                            float p1 = __uint_as_float((__float_as_uint(a1) & ~63u) | (uint32_t)(blk * 32 + j + 1));
+                            if (!full) {
+                                if (blk * 32 + j >= hcnt) p0 = TC_BIG;
+                                if (blk * 32 + j + 1 >= hcnt) p1 = TC_BIG;
                             }
+                            const float lo = fminf(p0, p1), hi = fmaxf(p0, p1);
+                            pb2[z] = fmin3(pb2[z], hi, fmaxf(pb1[z], lo));
+                            pb1[z] = fminf(pb1[z], lo);
                         }
                     }
+                };
+                if (hcnt >= 64) {
+                    fold_block(vr[0], 0, true);
+                    fold_block(vr[1], 1, true);
+                } else {
+                    if (hcnt > 0) fold_block(vr[0], 0, hcnt >= 32);
+                    if (hcnt > 32) fold_block(vr[1], 1, false);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1494,7 +1505,7 @@ static cudaError_t assign_step(const AssignJob &jb, const CUtensorMap *kmap, int
 
 static size_t l2_smem() { return MOG_MAX_L * MOG_D * sizeof(float) + L2_RING; }
 
-cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s) {
+cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s, const TraceDev &tr) {
     cudaError_t e;
     if ((e = set_smem((const void *)k_assign_l1, AS_SMEM)) != cudaSuccess) return e;
     if ((e = set_smem((const void *)k_l2_stats, l2_smem())) != cudaSuccess) return e;
@@ -1507,16 +1518,16 @@ cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s) {
         const bool tma = key_map(&kmap, dv.K, pl.n_cap, dv.h_kv, pl.batch, dv.sn, dv.sh, dv.sb);
         for (int t = 0; t < pl.T1; ++t) {
             AssignJob jb = build_job(dv, t);
-            if (dv.tr_l1c &&  // traced build: the centroids this step assigns to
-                (e = cudaMemcpy2DAsync(dv.tr_l1c + (int64_t)t * pl.c_max * MOG_D,
+            if (tr.l1c &&  // traced build: the centroids this step assigns to
+                (e = cudaMemcpy2DAsync(tr.l1c + (int64_t)t * pl.c_max * MOG_D,
                                        4 * (size_t)pl.T1 * pl.c_max * MOG_D, dv.cent,
                                        4 * (size_t)pl.c_max * MOG_D, 4 * (size_t)pl.c_max * MOG_D, U,
                                        cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
                 return e;
             if ((e = assign_step(jb, tma ? &kmap : nullptr, U, pl.n_mid_max, pl.c_max, s)) != cudaSuccess)
                 return e;
-            if (dv.tr_l1a &&  // ... and the assignment it made
-                (e = cudaMemcpy2DAsync(dv.tr_l1a + (int64_t)t * dv.tr_nm, 4 * (size_t)pl.T1 * dv.tr_nm,
+            if (tr.l1a &&  // ... and the assignment it made
+                (e = cudaMemcpy2DAsync(tr.l1a + (int64_t)t * tr.nm, 4 * (size_t)pl.T1 * tr.nm,
                                        dv.l1_assign, 4 * (size_t)pl.n_cap, 4 * (size_t)pl.n_mid_max, U,
                                        cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
                 return e;
@@ -1528,14 +1539,14 @@ cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s) {
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
-    k_l2_stats<<<dim3(pl.c_max, U), L2_THREADS, l2_smem(), s>>>(dv, 1);
+    k_l2_stats<<<dim3(pl.c_max, U), L2_THREADS, l2_smem(), s>>>(dv, 1, tr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_stats_only(const Dev &dv, const Plan &pl, cudaStream_t s) {
     cudaError_t e;
     if ((e = set_smem((const void *)k_l2_stats, l2_smem())) != cudaSuccess) return e;
-    k_l2_stats<<<dim3(pl.c_max, pl.units), L2_THREADS, l2_smem(), s>>>(dv, 0);
+    k_l2_stats<<<dim3(pl.c_max, pl.units), L2_THREADS, l2_smem(), s>>>(dv, 0, TraceDev{});
     return cudaGetLastError();
 }
 
