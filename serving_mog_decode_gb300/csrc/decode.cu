@@ -59,11 +59,12 @@ __device__ __forceinline__ void load_weights(float4 *w, const uint16_t *q, int G
 }
 
 // Scores of one group by 4 cooperating lanes (lanes 4i..4i+3 of a warp): lane part q reads
-// the float4 chunks k = q + 4i of the mean and of the variance.  Returns, on all 4 lanes,
-// the log-mass exponent res[g] (the residual's) and the selection score sel[g].
-template <int GT>
+// the float4 chunks k = q + 4i of the mean and of the variance.  For every head g < G
+// (G <= GT), emit(g, res, sel) is called on all 4 lanes with the log-mass exponent res
+// (the residual's) and the selection score sel.
+template <int GT, class Emit>
 __device__ __forceinline__ void quad_scores(const float *ms, int n, bool valid, const float4 *w,
-                                            int G, int mode, float (&res)[GT], float (&sel)[GT]) {
+                                            int G, int mode, Emit &&emit) {
     const int q = threadIdx.x & 3;
     float4 mu[8], va[8];
 #pragma unroll
@@ -76,6 +77,7 @@ __device__ __forceinline__ void quad_scores(const float *ms, int n, bool valid, 
         }
     }
     const float ln = n > 0 ? logf((float)n) : 0.f;
+    const bool ok = valid && n > 0;
 #pragma unroll
     for (int g = 0; g < GT; ++g) {
         if (g >= G) break;
@@ -90,27 +92,27 @@ __device__ __forceinline__ void quad_scores(const float *ms, int n, bool valid, 
         dm += __shfl_xor_sync(0xffffffffu, dm, 2);
         dq += __shfl_xor_sync(0xffffffffu, dq, 1);
         dq += __shfl_xor_sync(0xffffffffu, dq, 2);
-        const bool ok = valid && n > 0;
-        res[g] = ok ? ln + dm + dq : -INFINITY;
-        sel[g] = !ok ? -INFINITY : (mode == 0 ? res[g] : dm);
+        const float res = ok ? ln + dm + dq : -INFINITY;
+        emit(g, res, !ok ? -INFINITY : (mode == 0 ? res : dm));
     }
 }
 
-// Group score of a summary for the group-shared selection: the log of the sum over the G
-// heads of exp(selection score) (-inf when every score is -inf).
-template <int GT>
-__device__ __forceinline__ float group_score(const float (&sl)[GT], int G) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int g = 0; g < GT; ++g)
-        if (g < G) mx = fmaxf(mx, sl[g]);
-    if (mx == -INFINITY) return -INFINITY;
-    float sum = 0.f;
-#pragma unroll
-    for (int g = 0; g < GT; ++g)
-        if (g < G) sum += expf(sl[g] - mx);
-    return mx + logf(sum);
-}
+// Running log-sum-exp over the heads' selection scores, the group score of the
+// group-shared selection: the log of the sum over the G heads of exp(selection score)
+// (-inf when every score is -inf).
+struct LogSumExp {
+    float mx = -INFINITY, sum = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        if (x == -INFINITY) return;
+        if (x > mx) {
+            sum = sum * expf(mx - x) + 1.f;
+            mx = x;
+        } else {
+            sum += expf(x - mx);
+        }
+    }
+    __device__ __forceinline__ float value() const { return mx == -INFINITY ? -INFINITY : mx + logf(sum); }
+};
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
@@ -270,45 +272,61 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     const uint32_t allg = (G >= 32) ? 0xffffffffu : ((1u << G) - 1u);
     const bool pooled = tc > 0 && !a.sel_in;  // selection from the scores (not given)
 
-    // ------------------------------------------------------------ P0: query, weights
-    // The query may be written by the kernel just before this one, so it is read only
-    // after the dependency wait too.
-    pdl_wait();
-    pdl_trigger();
-    load_weights(w, qg, G, dv.tau);
-    __syncthreads();
-
-    // ------------------------------------------------- P1: score this CTA's clusters
+    // Every CTA of the cluster must have started before any pushes into its shared memory:
+    // arrive now, wait before the first push.
+    cluster_arrive_relaxed();
     const int c0 = k * m.SL;
     const int ns = max(0, min(C - c0, m.SL));
-    for (int base = 0; base < ns; base += NT / 4) {
-        const int cl = base + (tid >> 2);
-        const bool valid = cl < ns;
-        const int c = c0 + (valid ? cl : 0);
-        const int n = valid ? dv.cl_n[ug + c] : 0;
-        float res[GT], sl[GT];
-        quad_scores<GT>(dv.cl_ms + (ug + c) * 2 * MOG_D, n, valid, w, G, dv.score_mode, res, sl);
-        if (valid && (tid & 3) == 0) {
-#pragma unroll
-            for (int g = 0; g < GT; ++g)
-                if (g < G) {
-                    ckey[g * m.SLp + cl] = rank_key(sl[g], c);
-                    crs[g * m.SL + cl] = res[g];
-                }
-            if (grp) ckey[cl] = rank_key(group_score<GT>(sl, G), c);
-            cnn[cl] = n;
-        }
-    }
+    const int KC = m.KC, npool = CS * KC;
+    // this CTA's own shared arrays (nothing global is read before the wait)
     for (int e = tid; e < G * (m.SLp - ns); e += NT)  // padding keys
         ckey[(e / (m.SLp - ns)) * m.SLp + ns + e % (m.SLp - ns)] = 0ull;
     for (int e = tid; e < m.SL; e += NT) slm[e] = 0u;
     for (int e = tid; e < G * tcc; e += NT) selc[e] = -1;
     for (int e = tid; e < (dv.c_max + 31) / 32; e += NT) bm[e] = 0u;
-    const int KC = m.KC, npool = CS * KC;
     for (int e = tid; e < G * KC; e += NT) cand_k[e] = 0ull;
     for (int e = tid; e < G * (m.NPOOL - npool); e += NT)  // this CTA's own pool padding
         allc_k[(e / (m.NPOOL - npool)) * m.NPOOL + npool + e % (m.NPOOL - npool)] = 0ull;
+
+    // ------------------------------------------------------------ P0: query, weights
+    // The query may be written by the kernel just before this one, so it is read only
+    // after the dependency wait too.  The slice's summaries and counts are requested into
+    // L2 first, so that their latency overlaps the query's.
+    pdl_wait();
+    pdl_trigger();
+    {
+        const char *ms0 = reinterpret_cast<const char *>(dv.cl_ms + (ug + c0) * 2 * MOG_D);
+        for (int e = tid; e < ns * 8; e += NT) prefetch_l2(ms0 + 128 * (size_t)e);
+        const char *n0 = reinterpret_cast<const char *>(dv.cl_n + ug + c0);
+        if (tid * 128 < ns * 4) prefetch_l2(n0 + 128 * tid);
+        if (tid == 0 && ns > 0) prefetch_l2(n0 + 4 * (ns - 1));
+    }
+    load_weights(w, qg, G, dv.tau);
     __syncthreads();
+
+    // ------------------------------------------------- P1: score this CTA's clusters
+    for (int base = 0; base < ns; base += NT / 4) {
+        const int cl = base + (tid >> 2);
+        const bool valid = cl < ns;
+        const int c = c0 + (valid ? cl : 0);
+        const int n = valid ? dv.cl_n[ug + c] : 0;
+        const bool wr = valid && (tid & 3) == 0;
+        LogSumExp gsc;
+        quad_scores<GT>(dv.cl_ms + (ug + c) * 2 * MOG_D, n, valid, w, G, dv.score_mode,
+                    [&](int g, float res, float sl) {
+                        if (wr) {
+                            ckey[g * m.SLp + cl] = rank_key(sl, c);
+                            crs[g * m.SL + cl] = res;
+                        }
+                        gsc.add(sl);
+                    });
+        if (wr) {
+            if (grp) ckey[cl] = rank_key(gsc.value(), c);
+            cnn[cl] = n;
+        }
+    }
+    __syncthreads();
+    cluster_wait();
     if (pooled) {
         // this slice's top-KC per head (KC = min(slice, tc)) by rank, 0 padded ...
         for (int e = tid; e < GS * ns; e += NT) {
@@ -328,15 +346,13 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     cluster.sync();  // S1: every CTA's pool is complete
 
     // ------------------------------------------------------- P2: selection and union
-    if (pooled) {  // CTA k ranks pool entries e = k, k + CS, ... and pushes the winners
-        for (int e = k + CS * tid; e < GS * npool; e += CS * NT) {
+    if (pooled) {  // every CTA ranks the whole pool: each head's top-tc, in rank order
+        for (int e = tid; e < GS * npool; e += NT) {
             const int g = e / npool;
             const unsigned long long x = allc_k[g * m.NPOOL + e % npool];
             if (x == 0ull) continue;
             const int rank = key_rank(allc_k + g * m.NPOOL, m.NPOOL, x, tc);
-            if (rank < tc)
-                for (int dst = 0; dst < CS; ++dst)
-                    cluster.map_shared_rank(selc, dst)[g * tc + rank] = key_index(x);
+            if (rank < tc) selc[g * tc + rank] = key_index(x);
         }
     } else if (tc > 0) {
         for (int e = tid; e < GS * tc; e += NT) {  // (group mode: head 0's row)
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
             selc[e] = (cc >= 0 && cc < C && dv.cl_n[ug + cc] > 0) ? cc : -1;
         }
     }
-    cluster.sync();  // S1b: every CTA holds the full top-tc lists
+    __syncthreads();  // this CTA holds the full top-tc lists
     for (int e = tid; e < GS * tc; e += NT) {
         const int c = selc[e];
         if (c < 0) continue;
@@ -407,18 +423,17 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
         const bool valid = pr < npair;
         const int s = valid ? pr / L : 0, l = valid ? pr % L : 0;
         const size_t gi = usg + (valid ? (size_t)ucl[k + s * CS] * L + l : 0);
-        float res[GT], sl[GT];
+        const bool wr = valid && (tid & 3) == 0;
+        LogSumExp gsc;
         quad_scores<GT>(dv.sub_ms + gi * 2 * MOG_D, valid ? dv.sub_n[gi] : 0, valid, w, G,
-                        dv.score_mode, res, sl);
-        if (valid && (tid & 3) == 0) {
-#pragma unroll
-            for (int g = 0; g < GT; ++g)
-                if (g < G) {
-                    sres[(s * G + g) * MOG_MAX_L + l] = res[g];
-                    ssl[(s * G + g) * MOG_MAX_L + l] = sl[g];
-                }
-            if (grp) ssl[(s * G) * MOG_MAX_L + l] = group_score<GT>(sl, G);
-        }
+                    dv.score_mode, [&](int g, float res, float sl) {
+                        if (wr) {
+                            sres[(s * G + g) * MOG_MAX_L + l] = res;
+                            ssl[(s * G + g) * MOG_MAX_L + l] = sl;
+                        }
+                        gsc.add(sl);
+                    });
+        if (wr && grp) ssl[(s * G) * MOG_MAX_L + l] = gsc.value();
     }
     for (int e = tid; e < nmy * MOG_MAX_L; e += NT) smask[e] = 0u;
     for (int e = tid; e < nmy; e += NT) shm[e] = 0u;
@@ -449,6 +464,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
             const float *sc = ssl + (s * G + gs) * MOG_MAX_L;
             const unsigned long long x = lane < L ? rank_key(sc[lane], lane) : 0ull;
             int rank = 0;
+#pragma unroll 2
             for (int j = 0; j < L; ++j) rank += rank_key(sc[j], j) > x;
             if (x != 0ull && rank < ts) {
                 subs[rank] = lane;
