@@ -55,6 +55,12 @@ def args_():
                     help="budget of the oracle timing sample (decode steps of the whole layer)")
     ap.add_argument("--no-ablation", action="store_true",
                     help="skip the top-only and score-mode-1 arms")
+    ap.add_argument("--settle-seconds", type=float, default=0.5,
+                    help="decode loop before the timings, to settle the clocks")
+    ap.add_argument("--phase-steps", type=int, default=0,
+                    help="steps of the per-kernel timing (0: max(20, min(steps, 200)))")
+    ap.add_argument("--no-dense", action="store_true",
+                    help="skip the dense_decode comparison (profiling runs)")
     ap.add_argument("--sliding", action="store_true",
                     help="sliding recent window; the cache gets room for the append timing "
                          "that follows the decode timing")
@@ -336,7 +342,7 @@ def run_gpu(a, w, rank, world):
 
     clocks = Clocks(local)
     # ---- settle clocks, then dense_decode (the full scan) for comparison ----
-    t_end = time.time() + 0.5
+    t_end = time.time() + a.settle_seconds
     while time.time() < t_end:
         for _ in range(50):
             h.decode(qd, out)
@@ -345,7 +351,7 @@ def run_gpu(a, w, rank, world):
     dscratch = torch.empty(mog.dense_scratch_bytes(w.batch, w.h_kv, w.h_q, int(lens.max())),
                            dtype=torch.uint8, device=dev)
     dense_ms = []
-    for i in range(3 + 10):
+    for i in range(1 if a.no_dense else 3 + 10):  # (one untimed call for the error below)
         cold_l2()
         torch.cuda._sleep(CUSHION_CYCLES)
         s0, s1 = ev(), ev()
@@ -353,7 +359,7 @@ def run_gpu(a, w, rank, world):
         mog.dense_decode(Kd, Vd, h.lengths_dev, int(lens.max()), qd, dense_out, dscratch)
         s1.record()
         torch.cuda.synchronize()
-        if i >= 3:
+        if i >= 3 and not a.no_dense:
             dense_ms.append(s0.elapsed_time(s1))
     dense_bytes = float(sum(int(lens[u // w.h_kv]) for u in range(lay.units))) * 4 * D
     # approximation error of the MoG output against the full scan, per query head
@@ -439,7 +445,7 @@ def run_gpu(a, w, rank, world):
     except Exception:
         side = None
     phase = [[], [], []]
-    for i in range(max(20, min(a.steps, 200))):
+    for i in range(a.phase_steps if a.phase_steps > 0 else max(20, min(a.steps, 200))):
         cold_l2()
         if side is not None:
             side[0].decode(side[1], side[2])
@@ -529,10 +535,11 @@ def run_gpu(a, w, rank, world):
         "step_frac_of_peak": round(by["step"] / (mean_ms * 1e-3) / 1e9 / peak, 4),
         "kv_rows_read": int(by["rows"]),
         "kv_read_fraction": round(by["rows"] / float(sum(n_now[u // w.h_kv] for u in range(lay.units))), 4),
-        "dense_decode": {"us": round(statistics.mean(dense_ms) * 1e3, 2),
-                         "GBps": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9, 1),
-                         "frac": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9 / peak, 4)},
-        "speedup_vs_dense": round(statistics.mean(dense_ms) / mean_ms, 2),
+        "dense_decode": ({"us": round(statistics.mean(dense_ms) * 1e3, 2),
+                          "GBps": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9, 1),
+                          "frac": round(dense_bytes / (statistics.mean(dense_ms) * 1e-3) / 1e9 / peak, 4)}
+                         if dense_ms else None),
+        "speedup_vs_dense": round(statistics.mean(dense_ms) / mean_ms, 2) if dense_ms else None,
         "approx_vs_dense": {k: (round(v, 6) if isinstance(v, float) else v) for k, v in approx.items()},
         "approx_vs_dense_top_only": ablation["top_only"]["approx_vs_dense"] if ablation else None,
         "ablation": ablation,
