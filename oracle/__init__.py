@@ -299,6 +299,27 @@ def slide(K: np.ndarray, V: np.ndarray, summ: dict, force=None):
     return s, (c, l)
 
 
+def bf16_round(x) -> np.ndarray:
+    """x (float64) rounded to float32, then to bfloat16, each to nearest with ties to even;
+    returned as float64.  (The summaries' storage path: fp32 values rounded to bf16.)"""
+    f = np.ascontiguousarray(np.asarray(x, np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def summaries_bf16(summ: dict) -> dict:
+    """The bf16-summary variant of this library (MOG_FLAG_BF16_SUMMARIES; the pages do not
+    fix the summaries' precision): every group's key mean, per-dimension variance and value
+    mean rounded as bf16_round does; counts, partition and everything else unchanged.
+    Selection and decode on the returned dict are the method on the rounded summaries."""
+    s = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in summ.items()}
+    for k in ("cl_mu", "cl_var", "cl_vbar", "sub_mu", "sub_var", "sub_vbar"):
+        s[k] = bf16_round(s[k])
+    return s
+
+
 def group_selection(qs, summ: dict, top_c: int, top_s: int, score_mode: int = 0):
     """Group-shared selection (a variant of this library; the pages select per query head):
     the query heads qs[G][d] of one KV head select once.  A group's score is the log of the

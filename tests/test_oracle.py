@@ -624,3 +624,88 @@ def test_group_shared_all_selected_is_dense_and_rows_are_shared(ora):
     _, sel_c, sel_s = ora.mog_group_shared(K, V, w.n, qs, b, w.top_c, w.top_s)
     n_rows = [ora.decode(K, V, w.n, q, b, sel_c, sel_s)[1][2] for q in qs]
     assert len(set(n_rows)) == 1      # every head attends the same rows
+
+
+# ------------------------------------------------------------- bf16 summaries (variant)
+
+def test_bf16_round_matches_torch_and_ties_go_to_even(ora):
+    """The summaries' rounding: to float32, then to bfloat16, nearest with ties to even --
+    torch's float32 -> bfloat16 conversion on the float32 value."""
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(40)
+    x = np.concatenate([g.standard_normal(5000) * 10.0 ** g.integers(-6, 6, 5000), [0.0, -0.0, 1.0, -2.5]])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ora.bf16_round(x), ref)
+    # exact halfway cases: 1 + 2^-8 lies between 1 and 1 + 2^-7 -> even (1); 1 + 3*2^-8 -> 1 + 2^-6
+    assert ora.bf16_round(1.0 + 2.0 ** -8) == 1.0
+    assert ora.bf16_round(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+
+
+def test_bf16_summaries_exact_when_statistics_are_representable(ora):
+    """Groups of identical bf16 keys and values: every mean is a bf16 value and every
+    variance is zero, so rounding changes nothing and the decode is unchanged."""
+    g = np.random.default_rng(41)
+    base_k = wl.to_bf16(g.standard_normal((6, D)))
+    base_v = wl.to_bf16(g.standard_normal((6, D)))
+    K = np.repeat(base_k, 40, axis=0)
+    V = np.repeat(base_v, 40, axis=0)
+    q = wl.to_bf16(g.standard_normal(D))
+    b = ora.build_unit(K, V, 240, 0, 0, 6, 2)
+    r = ora.summaries_bf16(b)
+    for k in ("cl_mu", "cl_var", "cl_vbar", "sub_mu", "sub_var", "sub_vbar"):
+        assert np.array_equal(r[k], b[k]), k
+    o1, _, _, _ = ora.mog_head(K, V, 240, q, b, 2, 1)
+    o2, _, _, _ = ora.mog_head(K, V, 240, q, r, 2, 1)
+    assert np.array_equal(o1, o2)
+
+
+def test_bf16_summaries_decode_matches_independent_mixture(ora):
+    """Decode on the rounded summaries, against a numpy restatement of the mixture whose
+    group statistics are rounded by torch (float32 -> bfloat16), with selection by brute
+    force on the rounded scores."""
+    torch = pytest.importorskip("torch")
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    b = ora.build_unit(K, V, w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    r = ora.summaries_bf16(b)
+    out, sel_c, sel_s, _ = ora.mog_head(K, V, w.n, q[0], r, w.top_c, w.top_s)
+    tq = lambda a: torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    Kf, Vf, qf = f64(K), f64(V), f64(q[0])
+    perm, off, L = b["perm"], b["sub_off"], w.n_sub
+
+    def gstats(mem):
+        X = Kf[mem]
+        return tq(X.mean(0)), tq(X.var(0)), tq(Vf[mem].mean(0))
+
+    def score(mu, var, n):
+        return math.log(n) + TAU * (qf @ mu) + 0.5 * TAU ** 2 * float(qf ** 2 @ var)
+
+    cl = {c: perm[off[c * L]:off[(c + 1) * L]] for c in range(w.n_clusters)}
+    cs = {c: score(*gstats(m)[:2], m.size) for c, m in cl.items() if m.size}
+    chosen = [c for _, c in sorted((-v, c) for c, v in cs.items())][:w.top_c]
+    assert [int(c) for c in sel_c if c >= 0] == chosen
+    logits = [TAU * (Kf[p] @ qf) for p in list(range(w.n_sink)) + list(range(w.n - w.n_recent, w.n))]
+    rows = [Vf[p] for p in list(range(w.n_sink)) + list(range(w.n - w.n_recent, w.n))]
+    for c in range(w.n_clusters):
+        if c not in chosen:
+            if cl[c].size:
+                mu, var, vb = gstats(cl[c])
+                logits.append(score(mu, var, cl[c].size))
+                rows.append(vb)
+            continue
+        subs = {l: perm[off[c * L + l]:off[c * L + l + 1]] for l in range(L)}
+        ss = {l: score(*gstats(m)[:2], m.size) for l, m in subs.items() if m.size}
+        top = [l for _, l in sorted((-v, l) for l, v in ss.items())][:w.top_s]
+        assert [int(l) for l in sel_s[chosen.index(c)] if l >= 0] == top
+        for l, m in subs.items():
+            if l in top:
+                logits += [TAU * (Kf[p] @ qf) for p in m]
+                rows += [Vf[p] for p in m]
+            elif m.size:
+                mu, var, vb = gstats(m)
+                logits.append(score(mu, var, m.size))
+                rows.append(vb)
+    ref = softmax(np.array(logits)) @ np.array(rows)
+    assert rel_l2(out, ref) < 1e-12
+    full, _, _, _ = ora.mog_head(K, V, w.n, q[0], b, w.top_c, w.top_s)
+    print("bf16 summaries vs fp64 summaries, rel-L2", rel_l2(out, full))
