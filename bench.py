@@ -67,6 +67,8 @@ def args_():
     ap.add_argument("--group-select", action="store_true",
                     help="group-shared selection: the query heads of a KV head select once, "
                          "by the log-sum-exp of their scores")
+    ap.add_argument("--bf16-summaries", action="store_true",
+                    help="selection scores and residual terms from the summaries rounded to bf16")
     ap.add_argument("--union-exact", action="store_true",
                     help="GQA union-exact mode: every query head attends the union of the "
                          "chosen subclusters of its KV group")
@@ -231,7 +233,7 @@ def oracle_decode_sample(w, budget_s, steps=None, warmup=0, arrays=None, dense_s
 
 # ------------------------------------------------------------------------ GPU path
 
-def bytes_from_selection(h, w, sel, lens, n_now):
+def bytes_from_selection(h, w, sel, lens, n_now, bf16s=False):
     """Algorithmic bytes of one decode step, per kernel: all cluster summaries and the
     subcluster summaries of each unit's union of selected clusters (selection); the K/V
     rows (+ index) of the union of selected subclusters, the anchors and the residual terms
@@ -262,14 +264,15 @@ def bytes_from_selection(h, w, sel, lens, n_now):
         items = len(ucl) * L + Cn  # residual terms: the union's subclusters, then clusters
         gp = (G + 3) // 4 * 4
         P = h.splits()
+        sb = 2 if bf16s else 4  # bytes per summary element (mean, variance; value mean's high part)
         # selection kernel: query, cluster summaries (mean, variance, count), the union's
         # subcluster summaries and offsets; writes the segments and the residual exponents
-        tot["select"] += G * D * 2 + Cn * (8 * D + 4) + len(ucl) * (L * (8 * D + 8) + 4)
+        tot["select"] += G * D * 2 + Cn * (2 * sb * D + 4) + len(ucl) * (L * (2 * sb * D + 8) + 4)
         tot["select"] += len(usub) * 12 + items * gp * 4
         # rows kernel: query, segments, perm index and K, V rows (bf16) of the chosen rows and
         # the anchors, the residual terms (bf16 high/low value means and exponents), partials
         tot["attend"] += G * D * 2 + len(usub) * 12 + Uk * 4 + (Uk + anchors) * 4 * D
-        tot["attend"] += items * (4 * D + gp * 4) + P * G * (D + 4) * 4
+        tot["attend"] += items * (sb * D + gp * 4) + P * G * (D + 4) * 4
         # merge kernel: partials in, the output (fp32) out
         tot["merge"] += P * G * (D + 4) * 4 + G * D * 4
         tot["rows"] += Uk + anchors
@@ -305,7 +308,7 @@ def run_gpu(a, w, rank, world):
     prm = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], n_clusters=w.n_clusters, n_sub=w.n_sub,
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
                           union_exact=int(a.union_exact), sliding=int(a.sliding),
-                          group_select=int(a.group_select))
+                          group_select=int(a.group_select), bf16_summaries=int(a.bf16_summaries))
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -338,7 +341,7 @@ def run_gpu(a, w, rank, world):
     h.decode(qd, out, sel_out=sel)
     torch.cuda.synchronize()
     n_now = [int(x) for x in lens]
-    by = bytes_from_selection(h, w, sel.cpu().numpy(), lens, n_now)
+    by = bytes_from_selection(h, w, sel.cpu().numpy(), lens, n_now, a.bf16_summaries)
 
     clocks = Clocks(local)
     # ---- settle clocks, then dense_decode (the full scan) for comparison ----
@@ -378,7 +381,8 @@ def run_gpu(a, w, rank, world):
         for name, over in (("top_only", dict(residual=0)), ("score_mode_1", dict(score_mode=1))):
             kw = dict(n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s,
                       n_sink=w.n_sink, n_recent=w.n_recent, union_exact=int(a.union_exact),
-                      sliding=int(a.sliding), group_select=int(a.group_select))
+                      sliding=int(a.sliding), group_select=int(a.group_select),
+                      bf16_summaries=int(a.bf16_summaries))
             kw.update(over)
             pv = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], **kw)
             hv = mog.build(Kd, Vd, lens, pv, partition=(perm_t, off_t))
@@ -387,7 +391,7 @@ def run_gpu(a, w, rank, world):
             torch.cuda.synchronize()
             assert hv.sync_status() == 0
             ev_ = ((ov.reshape(-1, D).double() - dn).norm(dim=1) / dn.norm(dim=1).clamp_min(1e-30)).cpu().numpy()
-            byv = bytes_from_selection(hv, w, sv.cpu().numpy(), lens, n_now)
+            byv = bytes_from_selection(hv, w, sv.cpu().numpy(), lens, n_now, a.bf16_summaries)
             tv = []
             for i in range(3 + 20):
                 cold_l2()
@@ -439,7 +443,8 @@ def run_gpu(a, w, rank, world):
         sL = min(w.n_sub if w.n_sub > 0 else 8, 8)
         sp = mog.make_params(1, w.h_kv, w.h_q, 4096, n_clusters=32, n_sub=sL, top_c=min(w.top_c, 16),
                              top_s=min(w.top_s, sL), n_sink=4, n_recent=64,
-                             union_exact=int(a.union_exact), group_select=int(a.group_select))
+                             union_exact=int(a.union_exact), group_select=int(a.group_select),
+                             bf16_summaries=int(a.bf16_summaries))
         sKd, sVd, sqd = bf(sK), bf(sV), bf(sq)
         side = (mog.build(sKd, sVd, sl, sp), sqd, torch.empty(sqd.shape, dtype=torch.float32, device=dev))
     except Exception:
@@ -515,7 +520,8 @@ def run_gpu(a, w, rank, world):
                    "context": int(lens.max()), "clusters": w.n_clusters, "subclusters": w.n_sub,
                    "top_c": w.top_c, "top_s": w.top_s, "n_sink": w.n_sink, "n_recent": w.n_recent,
                    "mode": ("group-shared selection" if a.group_select else "per-head selection")
-                           + (", union-exact" if a.union_exact else ""),
+                           + (", union-exact" if a.union_exact else "")
+                           + (", bf16 summaries" if a.bf16_summaries else ""),
                    "recent_window": "sliding" if a.sliding else "growing",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -526,9 +532,10 @@ def run_gpu(a, w, rank, world):
                      "algorithmic_bytes_per_launch": int(kbytes[dom]),
                      "launch_us": round(pm[dom] * 1e3, 3)},
         "kernels_us": {names[i]: round(pm[i] * 1e3, 3) for i in range(3)},
-        "kernels_timing": ("events around each kernel; data cold (L2 flushed); the kernels' code "
+        "kernels_timing": ("mog_decode_phased: events around each kernel (no overlap between the "
+                           "kernels, no warm-up passes); data cold (L2 flushed); the kernels' code "
                            "re-warmed by a decode on a small side handle" if side is not None else
-                           "events around each kernel; data and code cold (L2 flushed)"),
+                           "mog_decode_phased: events around each kernel; data and code cold (L2 flushed)"),
         "kernels_GBps": {names[i]: round(kbytes[i] / (pm[i] * 1e-3) / 1e9, 1) for i in range(3)},
         "step_bytes": int(by["step"]),
         "step_GBps": round(by["step"] / (mean_ms * 1e-3) / 1e9, 1),

@@ -66,7 +66,7 @@ typedef enum {
  *                      residual's own exponent); 1 = tau q.mu only.
  *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
  *  flags             : 0, or any of MOG_FLAG_UNION_EXACT, MOG_FLAG_SLIDING,
- *                      MOG_FLAG_GROUP_SELECT.
+ *                      MOG_FLAG_GROUP_SELECT, MOG_FLAG_BF16_SUMMARIES.
  *
  * MOG_FLAG_UNION_EXACT (a variant of this library; the pages select per query head and do
  * not define it): each query head still makes its own selection, but every query head of a
@@ -98,6 +98,15 @@ typedef enum {
  * selection (mog_decode_ex) is taken from the group's first head.
  */
 #define MOG_FLAG_GROUP_SELECT 4
+/*
+ * MOG_FLAG_BF16_SUMMARIES (a variant of this library; the pages do not fix the summaries'
+ * precision): the selection scores and the Gaussian residual terms use every group's key
+ * mean, per-dimension variance and value mean rounded from their fp32 values to bf16
+ * (nearest, ties to even); counts stay exact.  The build keeps the fp32 summaries and
+ * writes the bf16 copies beside them (mog_layout.cl_ms16, sub_ms16); the sliding window
+ * updates both.  The decode reads half the summary bytes.
+ */
+#define MOG_FLAG_BF16_SUMMARIES 8
 typedef struct mog_params {
     int32_t batch, h_kv, h_q, d;
     int32_t n_cap;
@@ -142,6 +151,8 @@ typedef struct mog_layout {
     int64_t status;     /* int32 [8]: device status word, check counters */
     int64_t l1_steps;   /* int32 [units]: assignment steps taken by the first level */
     int64_t fallback;   /* int32 [units][iters_l1]: rows decided by the exact fp64 fallback */
+    int64_t cl_ms16;    /* bf16  [units][c_max][2][d]: mean, variance (MOG_FLAG_BF16_SUMMARIES; else 0) */
+    int64_t sub_ms16;   /* bf16  [units][c_max*l_max][2][d] (MOG_FLAG_BF16_SUMMARIES; else 0) */
 } mog_layout;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -213,7 +224,10 @@ int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void
  * on `stream`: events[0] before the selection kernel (cluster and subcluster scores, top-k,
  * the Gaussian residual, the row list), events[1] after it, events[2] after the
  * exact-attention rows kernel, events[3] after the merge kernel (which normalises), so
- * that each phase of one decode step can be timed.  Same arguments otherwise.
+ * that each phase of one decode step can be timed.  The events keep each kernel from
+ * starting before its predecessor has finished, so the rows and merge kernels skip the
+ * warm-up pass over their own code that mog_decode lets them run while they wait.  Same
+ * arguments and results otherwise.
  */
 int mog_decode_phased(mog_handle *h, const void *q_dev, float *out_dev,
                       const int32_t *sel_in_dev, int32_t *sel_out_dev, void *const *events,

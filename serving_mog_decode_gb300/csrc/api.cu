@@ -88,7 +88,8 @@ static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
 
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
-    const int known_flags = MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT;
+    const int known_flags =
+        MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT | MOG_FLAG_BF16_SUMMARIES;
     if ((p->flags & ~known_flags) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
         p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
         p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
@@ -114,6 +115,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.union_exact = (p->flags & MOG_FLAG_UNION_EXACT) ? 1 : 0;
     P.sliding = (p->flags & MOG_FLAG_SLIDING) ? 1 : 0;
     P.group_select = (p->flags & MOG_FLAG_GROUP_SELECT) ? 1 : 0;
+    P.bf16s = (p->flags & MOG_FLAG_BF16_SUMMARIES) ? 1 : 0;
     P.R = p->n_recent;
     P.c_max = P.l_max = 1;
     P.n_mid_max = 0;
@@ -157,6 +159,8 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_sub_vbar = take(4 * U * cm * lm * MOG_D);
     P.o_cl_vhl = take(2 * U * cm * 2 * MOG_D);
     P.o_sub_vhl = take(2 * U * cm * lm * 2 * MOG_D);
+    P.o_cl_ms16 = P.bf16s ? take(2 * U * cm * 2 * MOG_D) : 0;
+    P.o_sub_ms16 = P.bf16s ? take(2 * U * cm * lm * 2 * MOG_D) : 0;
     P.o_l1_assign = take(4 * U * nc);
     P.o_l1_steps = take(4 * U);
     P.o_cent = take(4 * U * cm * MOG_D);
@@ -239,6 +243,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.residual = P.residual;
     d.union_exact = P.union_exact;
     d.group_select = P.group_select;
+    d.bf16s = P.bf16s;
     d.P = P.P;
     d.nseg_max = P.nseg_max;
     d.cimg_ustride = P.cimg_ustride;
@@ -263,6 +268,10 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     PTR(sub_vbar, float);
     PTR(cl_vhl, uint16_t);
     PTR(sub_vhl, uint16_t);
+    if (P.bf16s) {
+        PTR(cl_ms16, uint16_t);
+        PTR(sub_ms16, uint16_t);
+    }
     PTR(cent, float);
     PTR(permA, int);
     PTR(changed, int);
@@ -572,6 +581,8 @@ extern "C" int mog_get_layout(const mog_handle *h, mog_layout *o) {
     o->status = P.o_status;
     o->l1_steps = P.o_l1_steps;
     o->fallback = P.o_fb_cnt;
+    o->cl_ms16 = P.o_cl_ms16;
+    o->sub_ms16 = P.o_sub_ms16;
     return MOG_OK;
 }
 

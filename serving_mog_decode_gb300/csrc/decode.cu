@@ -43,6 +43,7 @@ struct DecArgs {
     float *out;             // [units*G][d]
     const int32_t *sel_in;  // [units*G][SW] or null
     int SW;
+    int warm;  // 1: the rows and merge kernels run their warm-up pass before the wait
 };
 
 // per-head score weights, float4-chunked: w[g][k] (k < 32) holds tau*q over dims 4k..4k+3,
@@ -59,17 +60,23 @@ __device__ __forceinline__ void load_weights(float4 *w, const uint16_t *q, int G
 }
 
 // Scores of one group by 4 cooperating lanes (lanes 4i..4i+3 of a warp): lane part q reads
-// the float4 chunks k = q + 4i of the mean and of the variance.  For every head g < G
+// the chunks k = q + 4i (dimensions 4k..4k+3) of the mean and of the variance, from the
+// fp32 summary ms or, when ms16 is given, from its bf16 copy.  For every head g < G
 // (G <= GT), emit(g, res, sel) is called on all 4 lanes with the log-mass exponent res
 // (the residual's) and the selection score sel.
 template <int GT, class Emit>
-__device__ __forceinline__ void quad_scores(const float *ms, int n, bool valid, const float4 *w,
-                                            int G, int mode, Emit &&emit) {
+__device__ __forceinline__ void quad_scores(const float *ms, const uint16_t *ms16, int n, bool valid,
+                                            const float4 *w, int G, int mode, Emit &&emit) {
     const int q = threadIdx.x & 3;
     float4 mu[8], va[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        if (valid) {
+        if (valid && ms16) {
+            const uint2 a = *reinterpret_cast<const uint2 *>(ms16 + 4 * (q + 4 * i));
+            const uint2 b = *reinterpret_cast<const uint2 *>(ms16 + MOG_D + 4 * (q + 4 * i));
+            mu[i] = make_float4(bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y));
+            va[i] = make_float4(bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y));
+        } else if (valid) {
             mu[i] = *reinterpret_cast<const float4 *>(ms + 4 * (q + 4 * i));
             va[i] = *reinterpret_cast<const float4 *>(ms + MOG_D + 4 * (q + 4 * i));
         } else {
@@ -295,8 +302,10 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     pdl_wait();
     pdl_trigger();
     {
-        const char *ms0 = reinterpret_cast<const char *>(dv.cl_ms + (ug + c0) * 2 * MOG_D);
-        for (int e = tid; e < ns * 8; e += NT) prefetch_l2(ms0 + 128 * (size_t)e);
+        const char *ms0 = dv.cl_ms16 ? reinterpret_cast<const char *>(dv.cl_ms16 + (ug + c0) * 2 * MOG_D)
+                                     : reinterpret_cast<const char *>(dv.cl_ms + (ug + c0) * 2 * MOG_D);
+        const int lines = ns * (dv.cl_ms16 ? 4 : 8);  // 128-byte lines of the slice's summaries
+        for (int e = tid; e < lines; e += NT) prefetch_l2(ms0 + 128 * (size_t)e);
         const char *n0 = reinterpret_cast<const char *>(dv.cl_n + ug + c0);
         if (tid * 128 < ns * 4) prefetch_l2(n0 + 128 * tid);
         if (tid == 0 && ns > 0) prefetch_l2(n0 + 4 * (ns - 1));
@@ -312,7 +321,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
         const int n = valid ? dv.cl_n[ug + c] : 0;
         const bool wr = valid && (tid & 3) == 0;
         LogSumExp gsc;
-        quad_scores<GT>(dv.cl_ms + (ug + c) * 2 * MOG_D, n, valid, w, G, dv.score_mode,
+        quad_scores<GT>(dv.cl_ms + (ug + c) * 2 * MOG_D,
+                        dv.cl_ms16 ? dv.cl_ms16 + (ug + c) * 2 * MOG_D : nullptr, n, valid, w, G, dv.score_mode,
                     [&](int g, float res, float sl) {
                         if (wr) {
                             ckey[g * m.SLp + cl] = rank_key(sl, c);
@@ -425,7 +435,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
         const size_t gi = usg + (valid ? (size_t)ucl[k + s * CS] * L + l : 0);
         const bool wr = valid && (tid & 3) == 0;
         LogSumExp gsc;
-        quad_scores<GT>(dv.sub_ms + gi * 2 * MOG_D, valid ? dv.sub_n[gi] : 0, valid, w, G,
+        quad_scores<GT>(dv.sub_ms + gi * 2 * MOG_D, dv.sub_ms16 ? dv.sub_ms16 + gi * 2 * MOG_D : nullptr,
+                        valid ? dv.sub_n[gi] : 0, valid, w, G,
                     dv.score_mode, [&](int g, float res, float sl) {
                         if (wr) {
                             sres[(s * G + g) * MOG_MAX_L + l] = res;
@@ -632,7 +643,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     // caches, so that the real pass does not stall on instruction fetch between its memory
     // waits.  Pass 1 waits for the selection kernel and does the work.
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = a.warm ? 0 : 1; pass < 2; ++pass) {
     const bool dry = pass == 0;
     if (dry) {  // a plan of 64 anchor rows (T, anchors, sinks), no segments, no terms, L = 1
         for (int q = tid; q < PLAN_W; q += AT_THREADS)
@@ -752,7 +763,8 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
                                  : dv.cl_vhl + (ug + (item - npi)) * 2 * MOG_D;
                 src += (r & 1) * MOG_D + ch * 8;
             }
-            cp_async16(sv + swz(r, ch), src, ok ? 16 : 0);
+            // with bf16 summaries a term's value mean is its high part alone: the low row is zero
+            cp_async16(sv + swz(r, ch), src, ok && !(dv.bf16s && (r & 1)) ? 16 : 0);
             if (ch == 0) smk[r] = ok ? allm : 0u;
         }
         float *E = reinterpret_cast<float *>(stg);  // [item][MOG_MAX_G] exponents
@@ -831,7 +843,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
 constexpr int MG_THREADS = 4 * MOG_D;
 constexpr int MG_PARTS = MG_THREADS / MOG_D;
 __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int G,
-                                                          float *out) {
+                                                          float *out, int warm) {
     const int g = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
     const int j = tid % MOG_D, part = tid / MOG_D;
     __shared__ float s_m[MAX_SPLITS], s_l[MAX_SPLITS];
@@ -841,7 +853,7 @@ __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials,
     // finished (this kernel is launched early) and writes nothing: it brings the code into
     // the caches.  Pass 1 waits for the rows kernel and merges.
 #pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = warm ? 0 : 1; pass < 2; ++pass) {
     if (pass == 1) {
         pdl_wait();
         pdl_trigger();
@@ -1006,7 +1018,7 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
         return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_mog_merge, dim3(dv.G, dv.units), dim3(MG_THREADS), 0, s,
-                        (const float *)dv.partials, dv.P, dv.G, a.out)) != cudaSuccess)
+                        (const float *)dv.partials, dv.P, dv.G, a.out, a.warm)) != cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -1017,6 +1029,9 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
                           cudaEvent_t const *events) {
     DecArgs a;
     a.dv = dv;
+    // with events between the kernels none starts before its predecessor ends, so the
+    // warm-up passes would only add time
+    a.warm = events ? 0 : 1;
     a.q = static_cast<const uint16_t *>(q);
     a.out = out;
     a.sel_in = sel_in;

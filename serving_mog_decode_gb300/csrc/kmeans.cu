@@ -973,6 +973,7 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
                 dv.sub_vhl[sg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(mean - bf1((uint16_t)hi));
             } else {
                 dv.sub_ms[sg * 2 * MOG_D + j] = mean;
+                if (dv.sub_ms16) dv.sub_ms16[sg * 2 * MOG_D + j] = (uint16_t)f2bf(mean);
                 cs[l * MOG_D + j] = mean;
                 if (j == 0) dv.sub_n[sg] = ng;
             }
@@ -1000,6 +1001,7 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
             dv.cl_vhl[cg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(cmean - bf1((uint16_t)hi));
         } else {
             dv.cl_ms[cg * 2 * MOG_D + j] = cmean;
+            if (dv.cl_ms16) dv.cl_ms16[cg * 2 * MOG_D + j] = (uint16_t)f2bf(cmean);
             s_cm[j] = cmean;
             if (j == 0) dv.cl_n[cg] = n;
         }
@@ -1011,7 +1013,11 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
         int l = 0, g_lo = 0, g_hi = g_of(1);
         auto flush = [&]() {
             const int ng = g_hi - g_lo;
-            if (!upper) dv.sub_ms[(sg0 + l) * 2 * MOG_D + MOG_D + j] = ng > 0 ? q.s / (float)ng : 0.f;
+            if (!upper) {
+                const float var = ng > 0 ? q.s / (float)ng : 0.f;
+                dv.sub_ms[(sg0 + l) * 2 * MOG_D + MOG_D + j] = var;
+                if (dv.sub_ms16) dv.sub_ms16[(sg0 + l) * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(var);
+            }
             q.init();
             ++l;
             g_lo = g_hi;
@@ -1033,7 +1039,9 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
                         }
                     });
         if (upper) {
-            dv.cl_ms[cg * 2 * MOG_D + MOG_D + j] = n > 0 ? q.s / (float)n : 0.f;
+            const float var = n > 0 ? q.s / (float)n : 0.f;
+            dv.cl_ms[cg * 2 * MOG_D + MOG_D + j] = var;
+            if (dv.cl_ms16) dv.cl_ms16[cg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(var);
         } else {
             while (l < L) flush();
         }

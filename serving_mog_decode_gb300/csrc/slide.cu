@@ -193,10 +193,11 @@ __device__ int nearest_local(const float *ms, int ld, const int *cnt, int k, con
 }
 
 // Welford's update of one group (count n, mean and variance rows ms[0..d), ms[d..2d),
-// value mean vb, its bf16 high/low copy vhl) by the key x and value v (shared memory).
-// Threads j < d update key dimension j, threads d + j value dimension j.
-__device__ __forceinline__ void welford(int n, float *ms, float *vb, uint16_t *vhl, const float *xs,
-                                        const float *vs) {
+// their bf16 copy ms16 (or null), value mean vb, its bf16 high/low copy vhl) by the key x
+// and value v (shared memory).  Threads j < d update key dimension j, threads d + j value
+// dimension j.
+__device__ __forceinline__ void welford(int n, float *ms, uint16_t *ms16, float *vb, uint16_t *vhl,
+                                        const float *xs, const float *vs) {
     const int tid = threadIdx.x;
     const float n1 = (float)(n + 1);
     if (tid < MOG_D) {
@@ -204,8 +205,13 @@ __device__ __forceinline__ void welford(int n, float *ms, float *vb, uint16_t *v
         const float mu = ms[j], var = ms[MOG_D + j];
         const float delta = xs[j] - mu;
         const float mu_new = mu + delta / n1;
+        const float var_new = ((float)n * var + delta * (xs[j] - mu_new)) / n1;
         ms[j] = mu_new;
-        ms[MOG_D + j] = ((float)n * var + delta * (xs[j] - mu_new)) / n1;
+        ms[MOG_D + j] = var_new;
+        if (ms16) {
+            ms16[j] = (uint16_t)f2bf(mu_new);
+            ms16[MOG_D + j] = (uint16_t)f2bf(var_new);
+        }
     } else if (tid < 2 * MOG_D) {
         const int j = tid - MOG_D;
         const float m = vb[j] + (vs[j] - vb[j]) / n1;
@@ -292,8 +298,10 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
     if (tid == 0) s_top = old_end;
     csync();  // every CTA has chosen (c, l) from the means before they change
     if (rk == 0) {   // 3. Welford
-        welford(ncl, dv.cl_ms + cgi * 2 * MOG_D, dv.cl_vbar + cgi * MOG_D, dv.cl_vhl + cgi * 2 * MOG_D, xs, vs);
-        welford(nsub, dv.sub_ms + sgi * 2 * MOG_D, dv.sub_vbar + sgi * MOG_D, dv.sub_vhl + sgi * 2 * MOG_D, xs,
+        welford(ncl, dv.cl_ms + cgi * 2 * MOG_D, dv.cl_ms16 ? dv.cl_ms16 + cgi * 2 * MOG_D : nullptr,
+                dv.cl_vbar + cgi * MOG_D, dv.cl_vhl + cgi * 2 * MOG_D, xs, vs);
+        welford(nsub, dv.sub_ms + sgi * 2 * MOG_D, dv.sub_ms16 ? dv.sub_ms16 + sgi * 2 * MOG_D : nullptr,
+                dv.sub_vbar + sgi * MOG_D, dv.sub_vhl + sgi * 2 * MOG_D, xs,
                 vs);
     }
     for (int bi = (CL - first + batch - 1) / batch - 1; bi >= 0; --bi) {

@@ -190,7 +190,7 @@ class Injected:
     each unit (small cases) or a rule applied to positions (large cases)."""
 
     def __init__(self, w, lens=None, mode="oracle", n_cap=None, union_exact=0, sliding=0,
-                 group_select=0, score_mode=0, residual=1):
+                 group_select=0, score_mode=0, residual=1, bf16_summaries=0):
         self.w = w
         self.score_mode, self.residual = score_mode, residual
         lens = wl.lengths(w) if lens is None else np.asarray(lens, np.int32)
@@ -205,7 +205,7 @@ class Injected:
                                    n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink,
                                    n_recent=w.n_recent, union_exact=union_exact, sliding=sliding,
                                    group_select=group_select, score_mode=score_mode,
-                                   residual=residual)
+                                   residual=residual, bf16_summaries=bf16_summaries)
         stride = mog.sub_off_stride(self.prm, lens)
         perm_all = np.zeros((B * Hkv, self.n_cap), np.int32)
         off_all = np.zeros((B * Hkv, stride), np.int32)
@@ -873,3 +873,82 @@ def test_corrupt_partition_is_reported():
         o[16 * 6] = nm - 1
     for mutate in (bad_position, backwards, short_total):
         assert _corrupt_build(mutate) == 5, mutate.__name__      # MOG_ERR_DEVICE_CHECK
+
+
+# ------------------------------------------------------------ bf16 summaries (variant)
+
+def _bf16_bits_to_f64(a):
+    return (np.asarray(a).astype(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _check_bf16_copies(inj):
+    """The GPU's bf16 copies of the key means and variances (and the value means' high
+    parts) against the oracle's rounding of its own statistics: equal, except one bf16 ulp
+    where the fp32 value sits on a rounding tie (the GPU's and the oracle's fp32 values may
+    differ in their last bits)."""
+    lay = inj.h.layout()
+    U, cm, lm = lay.units, lay.c_max, lay.l_max
+    cl16 = _bf16_bits_to_f64(inj.h.array("cl_ms16", torch.int16, (U, cm, 2, D)).cpu().numpy())
+    sb16 = _bf16_bits_to_f64(inj.h.array("sub_ms16", torch.int16, (U, cm * lm, 2, D)).cpu().numpy())
+    total, off_by_one = 0, 0
+    for (b, h), s in inj.summ.items():
+        u = b * inj.w.h_kv + h
+        Cn, L = s["C"], s["L"]
+        for gpu, ref, n in ((cl16[u, :Cn, 0], s["cl_mu"], s["cl_n"]), (cl16[u, :Cn, 1], s["cl_var"], s["cl_n"]),
+                            (sb16[u, :Cn * L, 0], s["sub_mu"], s["sub_n"]),
+                            (sb16[u, :Cn * L, 1], s["sub_var"], s["sub_n"])):
+            keep = n > 0
+            g, r = gpu[keep], ora.bf16_round(ref[keep])
+            total += g.size
+            bad = g != r
+            if bad.any():
+                ulp = np.abs(r[bad]) * 2.0 ** -7
+                assert np.all(np.abs(g[bad] - r[bad]) <= ulp * 1.0001), "more than one bf16 ulp"
+                f32 = ref[keep][bad].astype(np.float32).astype(np.float64)
+                mid = (g[bad] + r[bad]) / 2
+                assert np.all(np.abs(f32 - mid) <= np.abs(mid) * 2.0 ** -20), "not at a rounding tie"
+                off_by_one += int(bad.sum())
+    assert off_by_one <= max(2, total // 10000), (off_by_one, total)
+    return total, off_by_one
+
+
+def test_bf16_summaries_match_oracle():
+    """MOG_FLAG_BF16_SUMMARIES on the oracle's partition: the fp32 summaries as usual, their
+    bf16 copies against the oracle's rounding, then the selection and the decode against the
+    oracle on the rounded summaries."""
+    w = small_workload(3000, batch=2, h_kv=2, h_q=8, top_c=5, top_s=3, seed=35)
+    inj = Injected(w, bf16_summaries=1)
+    _check_stats(inj)
+    total, ob1 = _check_bf16_copies(inj)
+    inj.summ = {k: ora.summaries_bf16(s) for k, s in inj.summ.items()}
+    ties, worst = _check_decode(inj)
+    print(f"bf16 summaries: {total} values, {ob1} one ulp off at ties; {ties} near-tie heads, "
+          f"decode worst {worst:.2e}")
+
+
+def test_bf16_summaries_full_size_qwen3_4b():
+    """The 32K workload at full size with bf16 summaries (position-rule partition)."""
+    w = wl.WORKLOADS["qwen3-4b-32k"]
+    inj = Injected(w, mode="rule", bf16_summaries=1)
+    _check_bf16_copies(inj)
+    inj.summ = {k: ora.summaries_bf16(s) for k, s in inj.summ.items()}
+    print("bf16 summaries 32K", _check_decode(inj))
+
+
+def test_bf16_summaries_follow_the_sliding_window():
+    """With the sliding window the Welford updates keep the bf16 copies equal to the
+    rounding of the updated fp32 summaries."""
+    steps, n0 = 12, 3000
+    w = small_workload(n0, batch=1, h_kv=2, h_q=4, n_recent=32, seed=84)
+    inj = Injected(w, n_cap=n0 + steps, sliding=1, bf16_summaries=1)
+    _slide_steps(inj, n0, steps, seed=12)
+    lay = inj.h.layout()
+    U, cm, lm = lay.units, lay.c_max, lay.l_max
+    g = inj.gpu_summaries()
+    cl16 = _bf16_bits_to_f64(inj.h.array("cl_ms16", torch.int16, (U, cm, 2, D)).cpu().numpy())
+    sb16 = _bf16_bits_to_f64(inj.h.array("sub_ms16", torch.int16, (U, cm * lm, 2, D)).cpu().numpy())
+    as_bf = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(cl16, as_bf(g["cl_ms"]))
+    assert np.array_equal(sb16, as_bf(g["sub_ms"]))
+    inj.summ = {k: ora.summaries_bf16(s) for k, s in inj.summ.items()}
+    print("bf16 + sliding decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
