@@ -119,15 +119,29 @@ typedef struct mog_params {
     int32_t flags;
 } mog_params;
 
-/* A bf16 KV cache in device memory.  Element (b, h, n, j) of K is
- * k[b*stride_b + h*stride_h + n*stride_n + j]; V uses the same strides.  stride_n >= d,
- * all strides multiples of 8 elements (16-byte aligned rows), base pointers 16-byte
- * aligned, and n_cap * stride_n * 2 bytes below 4 GiB (one head's rows are addressed with
- * 32-bit offsets; MOG_ERR_SHAPE otherwise).  mog_append writes into this cache. */
+/* A bf16 KV cache in device memory, contiguous or paged.  mog_append writes into it.
+ *  Contiguous (block_table == NULL): element (b, h, n, j) of K is
+ *    k[b*stride_b + h*stride_h + n*stride_n + j], and n_cap * stride_n * 2 bytes must stay
+ *    below 4 GiB (one head's rows are addressed with 32-bit offsets; MOG_ERR_SHAPE
+ *    otherwise).
+ *  Paged (a serving engine's block table): position n of sequence b lives in page
+ *    block_table[b*pages_per_seq + n / page_rows] (a device int32 array of
+ *    batch*pages_per_seq entries, caller-owned), row n % page_rows of it, and element
+ *    (b, h, n, j) of K is k[page*stride_b + h*stride_h + (n % page_rows)*stride_n + j]:
+ *    stride_b is the stride of one page.  page_rows is a power of two >= 16,
+ *    pages_per_seq * page_rows >= n_cap, and every page index p used must have
+ *    p * page_rows < 2^31.  The block table must not change while a handle uses it.  The
+ *    build's first-level assignment then skips its tensor-core pass (whose TMA tiles need
+ *    contiguous rows) and scores every key with the direct fp32 pass; results are the same.
+ *  V uses the same strides and table.  stride_n >= d, all strides multiples of 8 elements
+ *  (16-byte aligned rows), base pointers 16-byte aligned. */
 typedef struct mog_kv {
     void *k;
     void *v;
     int64_t stride_b, stride_h, stride_n;
+    const int32_t *block_table; /* NULL: contiguous */
+    int32_t page_rows;
+    int32_t pages_per_seq;
 } mog_kv;
 
 typedef struct mog_handle mog_handle;
@@ -218,6 +232,19 @@ int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev, const int32_
  * be run concurrently with a decode on the same handle.
  */
 int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void *stream);
+
+/*
+ * Periodic re-clustering during long generation ([IA]'s post-prefill partition, redone
+ * on the grown sequence): rebuilds the partition and every summary of the handle, in
+ * place, over each sequence's current mid region [S, N_now - n_recent), with the numbers
+ * of clusters and subclusters of the original build (the arena is sized for them).  The
+ * recent window restarts as the last n_recent keys, and keys that the sliding window had
+ * moved into the clusters are clustered afresh with the rest.  Equivalent to mog_build on
+ * the first N_now keys with those explicit C and L.  A serving loop calls it every so many
+ * appended tokens.  Enqueued on `stream`; not to overlap a decode or an append on the
+ * handle.
+ */
+int mog_recluster(mog_handle *h, void *stream);
 
 /*
  * mog_decode_ex that also records four caller-created cudaEvent_t (passed as void*), all

@@ -42,7 +42,35 @@ class Params(C.Structure):
 
 class KV(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("stride_b", C.c_int64),
-                ("stride_h", C.c_int64), ("stride_n", C.c_int64)]
+                ("stride_h", C.c_int64), ("stride_n", C.c_int64), ("block_table", C.c_void_p),
+                ("page_rows", C.c_int32), ("pages_per_seq", C.c_int32)]
+
+
+class PagedKV:
+    """A paged bf16 KV cache: page pools K, V of shape [pages, H_kv, page_rows, d]
+    (heads_first) or [pages, page_rows, H_kv, d], and an int32 block table [B, pages_per_seq]
+    on the device (page of position n of sequence b: block_table[b, n // page_rows]).
+    Pass it as K (with V=None) wherever a cache is taken."""
+
+    def __init__(self, K, V, block_table, page_rows, heads_first=True):
+        torch = _torch()
+        for t in (K, V):
+            if t.dtype != torch.bfloat16 or t.dim() != 4 or t.stride(3) != 1 or not t.is_cuda:
+                raise ValueError("page pools must be CUDA bf16 tensors with 4 dims, last contiguous")
+        if K.shape != V.shape or K.stride() != V.stride():
+            raise ValueError("K and V pools must share shape and strides")
+        if block_table.dtype != torch.int32 or block_table.dim() != 2 or not block_table.is_contiguous():
+            raise ValueError("block_table must be a contiguous int32 tensor [B, pages_per_seq]")
+        self.K, self.V, self.block_table, self.page_rows = K, V, block_table, page_rows
+        self.heads_first = heads_first
+        self.h_kv = K.shape[1] if heads_first else K.shape[2]
+        self.device = K.device
+
+    def struct(self) -> KV:
+        K = self.K
+        sh, sn = (K.stride(1), K.stride(2)) if self.heads_first else (K.stride(2), K.stride(1))
+        return KV(K.data_ptr(), self.V.data_ptr(), K.stride(0), sh, sn, self.block_table.data_ptr(),
+                  self.page_rows, self.block_table.shape[1])
 
 
 class Layout(C.Structure):
@@ -75,6 +103,7 @@ _SIGS = {
     "mog_decode_ex": (C.c_int, [_P, _P, _P, _P, _P, _P]),
     "mog_decode_phased": (C.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "mog_append": (C.c_int, [_P, _P, _P, _P]),
+    "mog_recluster": (C.c_int, [_P, _P]),
     "mog_get_layout": (C.c_int, [_P, _P]),
     "mog_sync_status": (C.c_int, [_P, _P]),
     "mog_decode_splits": (C.c_int, [_P, _P]),
@@ -135,7 +164,10 @@ def _ptr(t):
 
 
 def _kv(K, V):
-    """KV descriptor of bf16 tensors [B, H_kv, n_cap, d] (last dim contiguous)."""
+    """KV descriptor of bf16 tensors [B, H_kv, n_cap, d] (last dim contiguous), or of a
+    PagedKV passed as K."""
+    if isinstance(K, PagedKV):
+        return K.struct()
     torch = _torch()
     for t in (K, V):
         if t.dtype != torch.bfloat16 or t.dim() != 4 or t.stride(3) != 1 or not t.is_cuda:
@@ -176,7 +208,7 @@ class Handle:
     """A built MoG index over a KV cache.  Owns (references) the arena tensor; the KV
     tensors must stay alive and unmoved while the handle is used."""
 
-    def __init__(self, ptr, arena, params, K, V, lengths_dev, lengths_host):
+    def __init__(self, ptr, arena, params, K, V, lengths_dev, lengths_host):  # K may be a PagedKV
         self._h = ptr
         self.arena = arena
         self.params = params
@@ -220,6 +252,10 @@ class Handle:
 
     def append(self, k_new, v_new, stream=None):
         _check(lib().mog_append(self._h, _ptr(k_new), _ptr(v_new), _stream(stream)), "mog_append")
+
+    def recluster(self, stream=None):
+        """Rebuild the partition and summaries over the grown sequences (mog_recluster)."""
+        _check(lib().mog_recluster(self._h, _stream(stream)), "mog_recluster")
 
     def splits(self) -> int:
         v = C.c_int32(0)
@@ -285,7 +321,7 @@ def build(K, V, lengths, params: Params, stream=None, partition=None, trace=Fals
     import numpy as np
     torch = _torch()
     lh = np.ascontiguousarray(lengths, np.int32)
-    ld = torch.from_numpy(lh.copy()).to(K.device)
+    ld = torch.from_numpy(lh.copy()).to(K.device)  # (a PagedKV has a device too)
     nbytes = arena_bytes(params, lh)
     arena = torch.empty(nbytes + 256, dtype=torch.uint8, device=K.device)
     off = (-arena.data_ptr()) % 256
@@ -333,7 +369,7 @@ def _check_q_out(K, q, out):
     """q must be a contiguous CUDA bf16 [B, H_q, 128] on K's device and out a contiguous
     float32 tensor of q's shape on the same device: the kernels write B*H_q*128 floats."""
     torch = _torch()
-    B = K.shape[0]
+    B = q.shape[0] if isinstance(K, PagedKV) else K.shape[0]
     if (q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[0] != B or q.shape[2] != 128
             or not q.is_contiguous() or q.device != K.device):
         raise ValueError("q must be a contiguous bf16 tensor [B, H_q, 128] on the cache's device")
@@ -345,7 +381,7 @@ def _check_q_out(K, q, out):
 def dense_decode(K, V, lengths_dev, n_max, q, out=None, scratch=None, stream=None):
     """Full-scan exact attention.  q: bf16 [B, H_q, d] -> out f32 [B, H_q, d]."""
     torch = _torch()
-    B, H_kv = K.shape[0], K.shape[1]
+    B, H_kv = (q.shape[0], K.h_kv) if isinstance(K, PagedKV) else (K.shape[0], K.shape[1])
     H_q = q.shape[1]
     if out is None:
         out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
@@ -363,7 +399,7 @@ def dense_decode(K, V, lengths_dev, n_max, q, out=None, scratch=None, stream=Non
 def dense_decode_noalloc(K, V, lengths_dev, n_max, q, out, stream=None):
     """dense_decode whose scratch is the library's static device array: no device memory
     is allocated by this call (the caller supplies `out`)."""
-    B, H_kv = K.shape[0], K.shape[1]
+    B, H_kv = (q.shape[0], K.h_kv) if isinstance(K, PagedKV) else (K.shape[0], K.shape[1])
     _check_q_out(K, q, out)
     kv = _kv(K, V)
     _check(lib().dense_decode_noalloc(C.byref(kv), _ptr(lengths_dev), n_max, B, H_kv, q.shape[1],

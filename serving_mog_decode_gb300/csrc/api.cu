@@ -136,7 +136,9 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     // fewer than four CTAs, four per unit over several waves, which the CTA scheduler
     // balances across units of different lengths
     P.P = std::min(MAX_SPLITS, std::max(4, 2 * sms / P.units));
-    P.nchunks = std::max(1, (int)ceil_div64(P.n_mid_max, SORT_CHUNK));
+    // the sort workspace covers the longest mid region a later re-clustering can see
+    P.nchunks = std::max(1, (int)ceil_div64(std::max(P.n_mid_max, p->n_cap - p->n_recent - p->n_sink),
+                                            SORT_CHUNK));
     P.sub_off_stride = (P.c_max * P.l_max + 1 + 3) & ~3;
     const int64_t U = P.units, G = P.G, cm = P.c_max, lm = P.l_max, nc = P.n_cap;
     const int64_t SW = P.tc + P.tc * P.ts;
@@ -228,6 +230,9 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.sb = kv->stride_b;
     d.sh = kv->stride_h;
     d.sn = kv->stride_n;
+    d.bt = kv->block_table;
+    d.pshift = kv->block_table ? log2_exact(kv->page_rows) : 0;
+    d.pps = kv->block_table ? kv->pages_per_seq : 0;
     d.batch = P.batch;
     d.h_kv = P.h_kv;
     d.G = P.G;
@@ -332,6 +337,15 @@ extern "C" const char *mog_last_error(void) { return g_err; }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+namespace mog {
+int log2_exact(int x) {
+    if (x <= 0 || (x & (x - 1))) return -1;
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return l;
+}
+}  // namespace mog
+
 static int check_kv(const mog_kv *kv, int batch, int h_kv, int n_cap) {
     if (!kv || !kv->k || !kv->v) return MOG_ERR_INVALID_ARG;
     if (!aligned16(kv->k) || !aligned16(kv->v)) return MOG_ERR_INVALID_ARG;
@@ -339,6 +353,12 @@ static int check_kv(const mog_kv *kv, int batch, int h_kv, int n_cap) {
     if ((kv->stride_n | kv->stride_b | kv->stride_h) & 7) return MOG_ERR_SHAPE;
     (void)batch;
     (void)h_kv;
+    if (kv->block_table) {  // paged: whole pages of a power-of-two number of rows
+        const int sh = log2_exact(kv->page_rows);
+        if (sh < 4 || sh > 20 || kv->pages_per_seq <= 0) return MOG_ERR_SHAPE;
+        if ((int64_t)kv->pages_per_seq * kv->page_rows < n_cap) return MOG_ERR_SHAPE;
+        return MOG_OK;
+    }
     // the attention kernels address a row inside its head's slab with a 32-bit byte offset
     if ((int64_t)n_cap * kv->stride_n * 2 >= (1LL << 32)) return MOG_ERR_SHAPE;
     return MOG_OK;
@@ -351,6 +371,36 @@ extern "C" int mog_arena_bytes(const mog_params *p, const int32_t *lengths_host,
     if (st != MOG_OK) return st;
     *bytes = (size_t)pl.total;
     return MOG_OK;
+}
+
+// One unit's row of unit_info for a build over the first n keys of its sequence.
+static void set_unit_info(int32_t *r, int C, int L, int n, int S, int R, int b) {
+    r[UI_C] = C;
+    r[UI_L] = L;
+    r[UI_NBUILD] = n;
+    r[UI_NMID] = std::max(0, n - R - S);
+    r[UI_S] = S;
+    r[UI_RLO] = std::max(S, n - R);
+    r[UI_B] = b;
+}
+
+// Upload the handle's unit_info and clear what a build accumulates into.
+static cudaError_t reset_build_state(mog_handle *h, cudaStream_t s) {
+    const Plan &pl = h->plan;
+    char *a = h->arena;
+    cudaError_t e = cudaMemcpyAsync(a + pl.o_unit_info, h->info.data(), h->info.size() * 4,
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_changed, 0, 4 * (size_t)pl.units * pl.T1, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_fb_cnt, 0, 4 * (size_t)pl.units * pl.T1, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_rc_cnt, 0, 4 * (size_t)pl.units * pl.T1, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_coff, 0, 4 * (size_t)pl.units * (pl.c_max + 1), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_l1_assign, 0xff, 4 * (size_t)pl.units * pl.n_cap, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_l1_steps, 0, 4 * (size_t)pl.units, s);
+    // groups beyond a unit's C / L keep count 0 (the decode scores every c < c_max)
+    if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_cl_n, 0, 4 * (size_t)pl.units * pl.c_max, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(a + pl.o_sub_n, 0, 4 * (size_t)pl.units * pl.c_max * pl.l_max, s);
+    return e;
 }
 
 static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
@@ -373,41 +423,19 @@ static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
     h->appended = 0;
     h->info.assign((size_t)pl.units * UI_STRIDE, 0);
     for (int u = 0; u < pl.units; ++u) {
-        const int b = u / p->h_kv, n = lengths_host[b];
+        const int b = u / p->h_kv;
         int C, L;
-        unit_clusters(p, n, &C, &L);
-        int32_t *r = &h->info[(size_t)u * UI_STRIDE];
-        r[UI_C] = C;
-        r[UI_L] = L;
-        r[UI_NBUILD] = n;
-        r[UI_NMID] = std::max(0, n - p->n_recent - p->n_sink);
-        r[UI_S] = p->n_sink;
-        r[UI_RLO] = std::max(p->n_sink, n - p->n_recent);
-        r[UI_B] = b;
+        unit_clusters(p, lengths_host[b], &C, &L);
+        set_unit_info(&h->info[(size_t)u * UI_STRIDE], C, L, lengths_host[b], p->n_sink, p->n_recent, b);
     }
-    char *a = h->arena;
-    cudaError_t e;
-#define CKH(call)                                  \
-    do {                                           \
-        if ((e = (call)) != cudaSuccess) {         \
-            delete h;                              \
-            return cuda_fail(e, #call);            \
-        }                                          \
-    } while (0)
-    CKH(cudaMemcpyAsync(a + pl.o_unit_info, h->info.data(), h->info.size() * 4,
-                        cudaMemcpyHostToDevice, s));
-    CKH(cudaMemcpyAsync(a + pl.o_n_now, lengths_dev, 4 * (size_t)pl.batch, cudaMemcpyDeviceToDevice, s));
-    CKH(cudaMemsetAsync(a + pl.o_status, 0, 64, s));
-    CKH(cudaMemsetAsync(a + pl.o_changed, 0, 4 * (size_t)pl.units * pl.T1, s));
-    CKH(cudaMemsetAsync(a + pl.o_fb_cnt, 0, 4 * (size_t)pl.units * pl.T1, s));
-    CKH(cudaMemsetAsync(a + pl.o_rc_cnt, 0, 4 * (size_t)pl.units * pl.T1, s));
-    CKH(cudaMemsetAsync(a + pl.o_coff, 0, 4 * (size_t)pl.units * (pl.c_max + 1), s));
-    CKH(cudaMemsetAsync(a + pl.o_l1_assign, 0xff, 4 * (size_t)pl.units * pl.n_cap, s));
-    CKH(cudaMemsetAsync(a + pl.o_l1_steps, 0, 4 * (size_t)pl.units, s));
-    // groups beyond a unit's C / L keep count 0 (the decode scores every c < c_max)
-    CKH(cudaMemsetAsync(a + pl.o_cl_n, 0, 4 * (size_t)pl.units * pl.c_max, s));
-    CKH(cudaMemsetAsync(a + pl.o_sub_n, 0, 4 * (size_t)pl.units * pl.c_max * pl.l_max, s));
-#undef CKH
+    cudaError_t e = cudaMemcpyAsync(h->arena + pl.o_n_now, lengths_dev, 4 * (size_t)pl.batch,
+                                    cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->arena + pl.o_status, 0, 64, s);
+    if (e == cudaSuccess) e = reset_build_state(h, s);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "mog_build set-up");
+    }
     *hh = h;
     return MOG_OK;
 }
@@ -554,6 +582,26 @@ extern "C" int mog_append(mog_handle *h, const void *k_new_dev, const void *v_ne
     return MOG_OK;
 }
 
+extern "C" int mog_recluster(mog_handle *h, void *stream) {
+    if (!h) return MOG_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Plan &pl = h->plan;
+    // every sequence has taken the same number of appends since the last build
+    int nmid = 0;
+    for (int b = 0; b < pl.batch; ++b) h->lengths[b] += h->appended;
+    h->appended = 0;
+    for (int u = 0; u < pl.units; ++u) {
+        int32_t *r = &h->info[(size_t)u * UI_STRIDE];
+        set_unit_info(r, r[UI_C], r[UI_L], h->lengths[r[UI_B]], r[UI_S], pl.R, r[UI_B]);
+        nmid = std::max(nmid, r[UI_NMID]);
+    }
+    h->plan.n_mid_max = nmid;
+    cudaError_t e = reset_build_state(h, s);
+    if (e == cudaSuccess) e = launch_build(h->dev, h->plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mog_recluster");
+    return MOG_OK;
+}
+
 extern "C" int mog_get_layout(const mog_handle *h, mog_layout *o) {
     if (!h || !o) return MOG_ERR_INVALID_ARG;
     const Plan &P = h->plan;
@@ -625,10 +673,9 @@ extern "C" int dense_decode(const mog_kv *kv, const int32_t *lengths_dev, int32_
     if (!aligned16(q_dev) || !aligned16(out_dev) || !aligned16(scratch_dev)) return MOG_ERR_INVALID_ARG;
     if (scratch_bytes < need) return MOG_ERR_ARENA_TOO_SMALL;
     const int units = batch * h_kv;
-    cudaError_t e = launch_dense(static_cast<const uint16_t *>(kv->k), static_cast<const uint16_t *>(kv->v),
-                                 kv->stride_b, kv->stride_h, kv->stride_n, lengths_dev, n_max, batch,
-                                 h_kv, h_q / h_kv, q_dev, out_dev, static_cast<float *>(scratch_dev),
-                                 dense_splits(units, n_max), static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_dense(kv, lengths_dev, n_max, batch, h_kv, h_q / h_kv, q_dev, out_dev,
+                                 static_cast<float *>(scratch_dev), dense_splits(units, n_max),
+                                 static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dense_decode launch");
     return MOG_OK;
 }
@@ -653,10 +700,8 @@ extern "C" int dense_decode_noalloc(const mog_kv *kv, const int32_t *lengths_dev
         return MOG_ERR_CAPACITY;
     }
     const int units = batch * h_kv;
-    cudaError_t e = launch_dense(static_cast<const uint16_t *>(kv->k), static_cast<const uint16_t *>(kv->v),
-                                 kv->stride_b, kv->stride_h, kv->stride_n, lengths_dev, n_max, batch,
-                                 h_kv, h_q / h_kv, q_dev, out_dev, scratch, dense_splits(units, n_max),
-                                 static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_dense(kv, lengths_dev, n_max, batch, h_kv, h_q / h_kv, q_dev, out_dev,
+                                 scratch, dense_splits(units, n_max), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dense_decode_noalloc launch");
     return MOG_OK;
 }

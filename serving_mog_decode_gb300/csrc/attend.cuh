@@ -76,11 +76,27 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)(row * AT_ROW_BYTES + ((chunk ^ (row & 7)) << 4));
 }
 
+// Row addressing of the tile engine.  Contiguous (PAGED = false): row `pos` of a head's
+// slab is at byte pos * row_bytes from the slab base (a 32-bit offset: the slab is below
+// 4 GB).  Paged: `pos` is a physical row, (page << pshift) | row-in-page, at
+// page * page_bytes + row * row_bytes from the base (64-bit).
+template <bool PAGED>
+struct RowAddr {
+    uint32_t row_bytes;
+    int pshift;
+    int64_t page_bytes;
+    __device__ __forceinline__ uint64_t off(int64_t pos) const {
+        if (!PAGED) return (uint32_t)pos * row_bytes;
+        return (uint64_t)(pos >> pshift) * (uint64_t)page_bytes +
+               (uint32_t)(pos & ((1 << pshift) - 1)) * row_bytes;
+    }
+};
+
 // Issue the copies of one tile: rows r < nrows come from krow/vrow(pos(r)); others are
 // zero-filled with mask 0.  `posf(r, &pos, &mask)` supplies row positions.
-template <typename RowFn>
+template <bool PAGED, typename RowFn>
 __device__ __forceinline__ void issue_tile(uint8_t *stage, int nrows, const uint16_t *kbase,
-                                           const uint16_t *vbase, int64_t sn, RowFn posf) {
+                                           const uint16_t *vbase, const RowAddr<PAGED> &ra, RowFn posf) {
     uint32_t *smask = reinterpret_cast<uint32_t *>(stage + 2 * AT_TILE_BYTES);
     const uint32_t sk = smem_u32(stage), sv = sk + AT_TILE_BYTES;
     const int tid = threadIdx.x;
@@ -93,8 +109,7 @@ __device__ __forceinline__ void issue_tile(uint8_t *stage, int nrows, const uint
         uint32_t mk = 0;
         const bool ok = r < nrows;
         if (ok) posf(r, pos, mk);
-        // byte offset of the row within its head's slab (< 4 GB: n_cap * row bytes)
-        const uint32_t off = ok ? (uint32_t)pos * (uint32_t)(sn * 2) + ch * 16 : 0u;
+        const uint64_t off = ok ? ra.off(pos) + ch * 16 : 0u;
         const uint16_t *ks = reinterpret_cast<const uint16_t *>(reinterpret_cast<const char *>(kbase) + off);
         const uint16_t *vs = reinterpret_cast<const uint16_t *>(reinterpret_cast<const char *>(vbase) + off);
         cp_async16(sk + swz(r, ch), ks, ok ? 16 : 0);

@@ -618,7 +618,7 @@ static_assert(RW_TPB >= AT_STAGES - 1, "the first batch must cover the pipeline'
 // reaches the batch, so no tile copy waits on a position load.  After its rows, the CTA
 // streams its share of the Gaussian residual terms through the same pipeline.  One
 // unnormalised partial per CTA.
-template <int GT>
+template <int GT, bool PAGED>
 __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     extern __shared__ __align__(128) uint8_t tile[];
     const Dev &dv = a.dv;
@@ -661,8 +661,11 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     const int NS = s_plan[0], T = s_plan[1], n_anchor = s_plan[2], s_cnt = s_plan[3], rlo = s_plan[4];
     const int r0 = dry ? 0 : (int)((int64_t)T * p / P), r1 = dry ? T : (int)((int64_t)T * (p + 1) / P);
     const int nrow = r1 - r0, nt = (nrow + AT_ROWS - 1) / AT_ROWS;
-    const uint16_t *kb = dv.K + b * dv.sb + h * dv.sh;
-    const uint16_t *vb = dv.V + b * dv.sb + h * dv.sh;
+    // a paged cache: positions become physical rows (page << pshift | row) when fetched
+    const uint16_t *kb = dv.K + (PAGED ? 0 : b * dv.sb) + h * dv.sh;
+    const uint16_t *vb = dv.V + (PAGED ? 0 : b * dv.sb) + h * dv.sh;
+    const RowAddr<PAGED> ra{(uint32_t)(dv.sn * 2), dv.pshift, dv.sb * 2};
+    const int *btb = PAGED ? dv.bt + (int64_t)b * dv.pps : nullptr;
     const int *perm = dv.perm + (size_t)u * dv.n_cap;
     const size_t useg = (size_t)u * dv.nseg_max;
     int wfirst = 0, wn = 0;  // the window: segments wfirst .. wfirst + wn
@@ -714,20 +717,28 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
         if (bt & 1) fetch_into(bt, pf_pos[1], pf_mk[1]);
         else fetch_into(bt, pf_pos[0], pf_mk[0]);
     };
-    auto place = [&](int bt) {  // registers -> shared buffer of batch bt
+    // registers -> shared buffer of batch bt (the loads have landed by now: the values are
+    // first used here, so that fetching them never stalls); a paged cache's positions become
+    // physical rows, an invalid one -1
+    auto place = [&](int bt) {
 #pragma unroll
         for (int jj = 0; jj < RW_PER; ++jj) {
-            s_pos[bt & 1][tid + jj * AT_THREADS] = (bt & 1) ? pf_pos[1][jj] : pf_pos[0][jj];
+            int v = (bt & 1) ? pf_pos[1][jj] : pf_pos[0][jj];
+            if (PAGED)
+                v = (unsigned)v < (unsigned)dv.n_cap
+                        ? (__ldg(btb + (v >> dv.pshift)) << dv.pshift) | (v & ((1 << dv.pshift) - 1))
+                        : -1;
+            s_pos[bt & 1][tid + jj * AT_THREADS] = v;
             s_mk[bt & 1][tid + jj * AT_THREADS] = (bt & 1) ? pf_mk[1][jj] : pf_mk[0][jj];
         }
     };
     auto issue = [&](int t) {  // (the warm-up tile is zero-filled: no rows are read)
         const int buf = (t / RW_TPB) & 1, rb = (t % RW_TPB) * AT_ROWS;
         issue_tile(tile + (t % AT_STAGES) * AT_STAGE_BYTES, dry ? 0 : min(AT_ROWS, nrow - t * AT_ROWS), kb, vb,
-                   dv.sn, [&](int r, int64_t &pos, uint32_t &mk) {
+                   ra, [&](int r, int64_t &pos, uint32_t &mk) {
                        int pp = s_pos[buf][rb + r];
                        uint32_t mm = s_mk[buf][rb + r];
-                       if ((unsigned)pp >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
+                       if (PAGED ? pp < 0 : (unsigned)pp >= (unsigned)dv.n_cap) {  // corrupt partition: flag, skip
                            flag_error(dv.status, ST_BAD_INDEX);
                            pp = 0;
                            mm = 0u;
@@ -897,8 +908,9 @@ __global__ void k_append(Dev dv, const uint16_t *kn, const uint16_t *vn) {
     for (int e = threadIdx.x; e < dv.h_kv * 16; e += blockDim.x) {
         const int h = e / 16, ch = e % 16;
         const size_t src = ((size_t)b * dv.h_kv + h) * MOG_D + ch * 8;
-        uint16_t *kd = dv.Kw + b * dv.sb + h * dv.sh + (int64_t)pos * dv.sn + ch * 8;
-        uint16_t *vd = dv.Vw + b * dv.sb + h * dv.sh + (int64_t)pos * dv.sn + ch * 8;
+        const int64_t ro = dv.row_off(b, h, pos);
+        uint16_t *kd = dv.Kw + ro + ch * 8;
+        uint16_t *vd = dv.Vw + ro + ch * 8;
         *reinterpret_cast<uint4 *>(kd) = *reinterpret_cast<const uint4 *>(kn + src);
         *reinterpret_cast<uint4 *>(vd) = *reinterpret_cast<const uint4 *>(vn + src);
     }
@@ -1012,10 +1024,13 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
         cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
-    if ((e = ensure_smem((const void *)k_mog_rows<GT>, AT_SMEM)) != cudaSuccess) return e;
-    if ((e = launch_pdl(k_mog_rows<GT>, dim3(dv.P, dv.units), dim3(AT_THREADS), AT_SMEM, s, a)) !=
-        cudaSuccess)
-        return e;
+    const void *rows_fn = dv.bt ? (const void *)k_mog_rows<GT, true> : (const void *)k_mog_rows<GT, false>;
+    if ((e = ensure_smem(rows_fn, AT_SMEM)) != cudaSuccess) return e;
+    if (dv.bt)
+        e = launch_pdl(k_mog_rows<GT, true>, dim3(dv.P, dv.units), dim3(AT_THREADS), AT_SMEM, s, a);
+    else
+        e = launch_pdl(k_mog_rows<GT, false>, dim3(dv.P, dv.units), dim3(AT_THREADS), AT_SMEM, s, a);
+    if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_mog_merge, dim3(dv.G, dv.units), dim3(MG_THREADS), 0, s,
                         (const float *)dv.partials, dv.P, dv.G, a.out, a.warm)) != cudaSuccess)

@@ -18,6 +18,8 @@ namespace mog {
 struct DenseArgs {
     const uint16_t *K, *V;
     int64_t sb, sh, sn;
+    const int *bt;  // block table of a paged cache, or null
+    int pshift, pps;
     const int32_t *lengths;
     int h_kv, G, splits;
     const uint16_t *q;
@@ -25,8 +27,8 @@ struct DenseArgs {
     float scale2;
 };
 
-// NB: blocks of 8 query heads per KV head (1 for G <= 8, else 2)
-template <int NB>
+// NB: blocks of 8 query heads per KV head (1 for G <= 8, else 2); PAGED: a block-table cache
+template <int NB, bool PAGED>
 __global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
     extern __shared__ __align__(128) uint8_t dsm[];
     const int u = blockIdx.y, p = blockIdx.x;
@@ -37,8 +39,10 @@ __global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
     const int64_t t0 = ntile * p / a.splits, t1 = ntile * (p + 1) / a.splits;
     const int64_t lo = t0 * AT_ROWS, hi = min((int64_t)n, t1 * AT_ROWS);
     const int nt = (int)(t1 - t0);
-    const uint16_t *kb = a.K + b * a.sb + h * a.sh;
-    const uint16_t *vb = a.V + b * a.sb + h * a.sh;
+    const uint16_t *kb = a.K + (PAGED ? 0 : b * a.sb) + h * a.sh;
+    const uint16_t *vb = a.V + (PAGED ? 0 : b * a.sb) + h * a.sh;
+    const RowAddr<PAGED> ra{(uint32_t)(a.sn * 2), a.pshift, a.sb * 2};
+    const int *btb = PAGED ? a.bt + (int64_t)b * a.pps : nullptr;
     const uint32_t allm = a.G >= 32 ? 0xffffffffu : ((1u << a.G) - 1u);
     QFrags<NB> qf;
     load_q_frags(qf, a.q + ((int64_t)b * a.h_kv * a.G + (int64_t)h * a.G) * MOG_D, a.G);
@@ -47,9 +51,12 @@ __global__ void __launch_bounds__(AT_THREADS) k_dense_split(DenseArgs a) {
     auto issue = [&](int t) {
         const int64_t r0 = lo + (int64_t)t * AT_ROWS;
         const int nr = (int)min((int64_t)AT_ROWS, hi - r0);
-        issue_tile(dsm + (t % AT_STAGES) * AT_STAGE_BYTES, nr, kb, vb, a.sn,
+        issue_tile(dsm + (t % AT_STAGES) * AT_STAGE_BYTES, nr, kb, vb, ra,
                    [&](int r, int64_t &pos, uint32_t &mk) {
                        pos = r0 + r;
+                       if (PAGED)  // physical row: (page << pshift) | row in page
+                           pos = ((int64_t)__ldg(btb + (pos >> a.pshift)) << a.pshift) |
+                                 (pos & ((1 << a.pshift) - 1));
                        mk = allm;
                    });
     };
@@ -91,20 +98,25 @@ int dense_splits(int units, int n_max) {
     return max(1, min(want, by_len));
 }
 
-cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64_t sh,
-                         int64_t sn, const int32_t *lengths, int n_max, int batch, int h_kv,
+cudaError_t launch_dense(const mog_kv *kv, const int32_t *lengths, int n_max, int batch, int h_kv,
                          int G, const void *q, float *out, float *scratch, int splits,
                          cudaStream_t s) {
-    const void *split_fn = G <= 8 ? (const void *)k_dense_split<1> : (const void *)k_dense_split<2>;
+    const bool pg = kv->block_table != nullptr;
+    const void *split_fn = G <= 8 ? (pg ? (const void *)k_dense_split<1, true> : (const void *)k_dense_split<1, false>)
+                                  : (pg ? (const void *)k_dense_split<2, true> : (const void *)k_dense_split<2, false>);
     cudaError_t e = ensure_smem(split_fn, AT_SMEM);
     if (e == cudaSuccess) e = ensure_smem((const void *)k_dense_merge, MERGE_SMEM);
     if (e != cudaSuccess) return e;
-    DenseArgs a{K, V, sb, sh, sn, lengths, h_kv, G, splits,
-                static_cast<const uint16_t *>(q), out, scratch,
+    DenseArgs a{static_cast<const uint16_t *>(kv->k), static_cast<const uint16_t *>(kv->v),
+                kv->stride_b, kv->stride_h, kv->stride_n, kv->block_table,
+                kv->block_table ? log2_exact(kv->page_rows) : 0, kv->block_table ? kv->pages_per_seq : 0,
+                lengths, h_kv, G, splits, static_cast<const uint16_t *>(q), out, scratch,
                 (float)(LOG2E / sqrt((double)MOG_D))};
     const int U = batch * h_kv;
-    if (G <= 8) k_dense_split<1><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
-    else k_dense_split<2><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
+    if (G <= 8 && !pg) k_dense_split<1, false><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
+    else if (G <= 8) k_dense_split<1, true><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
+    else if (!pg) k_dense_split<2, false><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
+    else k_dense_split<2, true><<<dim3(splits, U), AT_THREADS, AT_SMEM, s>>>(a);
     k_dense_merge<<<U, MERGE_THREADS, MERGE_SMEM, s>>>(a);
     return cudaGetLastError();
 }

@@ -34,6 +34,8 @@ struct Dev {
     const uint16_t *K, *V;
     uint16_t *Kw, *Vw;  // writable views (append)
     int64_t sb, sh, sn;
+    const int *bt;      // block table of a paged cache (null: contiguous), [batch][pps]
+    int pshift, pps;    // log2(rows per page), pages per sequence
     // shape
     int batch, h_kv, G, units, n_cap, c_max, l_max, tc, ts, T1, T2, score_mode, residual;
     int union_exact;  // every head attends the union of the heads' chosen subclusters
@@ -63,11 +65,17 @@ struct Dev {
     float *resx;           // [units][resx_stride]: residual exponents [item][G, padded to 4]
     int64_t resx_stride;
 
-    __host__ __device__ const uint16_t *krow(int b, int h, int64_t pos) const {
-        return K + b * sb + h * sh + pos * sn;
+    // element offset of row pos of (b, h): through the block table when the cache is paged
+    __device__ __forceinline__ int64_t row_off(int b, int h, int64_t pos) const {
+        if (!bt) return b * sb + h * sh + pos * sn;
+        const int64_t page = bt[(int64_t)b * pps + (pos >> pshift)];
+        return page * sb + h * sh + (pos & ((1 << pshift) - 1)) * sn;
     }
-    __host__ __device__ const uint16_t *vrow(int b, int h, int64_t pos) const {
-        return V + b * sb + h * sh + pos * sn;
+    __device__ __forceinline__ const uint16_t *krow(int b, int h, int64_t pos) const {
+        return K + row_off(b, h, pos);
+    }
+    __device__ __forceinline__ const uint16_t *vrow(int b, int h, int64_t pos) const {
+        return V + row_off(b, h, pos);
     }
 };
 
@@ -109,10 +117,10 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
                           cudaStream_t s);
 cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s);
-cudaError_t launch_dense(const uint16_t *K, const uint16_t *V, int64_t sb, int64_t sh,
-                         int64_t sn, const int32_t *lengths, int n_max, int batch, int h_kv,
+cudaError_t launch_dense(const mog_kv *kv, const int32_t *lengths, int n_max, int batch, int h_kv,
                          int G, const void *q, float *out, float *scratch, int splits,
                          cudaStream_t s);
+int log2_exact(int x);  // log2 of a power of two, -1 otherwise
 int dense_splits(int units, int n_max);
 cudaError_t dense_static_scratch(float **ptr, size_t *bytes);
 size_t slot_smem_bytes(int G, int c_max, int l_max, int tc);

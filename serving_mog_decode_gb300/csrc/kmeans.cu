@@ -46,6 +46,8 @@ __device__ __forceinline__ bool converged_by(const int *changed, int t) {
 struct AssignJob {
     const uint16_t *K;
     int64_t sb, sh, sn;
+    const int *bt;  // block table of a paged cache, or null
+    int pshift, pps;
     int h_kv;
     const int *unit_info;  // null: a single unit of n_single rows at K, row stride sn
     int n_single, k_single;
@@ -75,19 +77,35 @@ struct AssignJob {
 constexpr int AS_ROWS = 64, AS_CENT = 64, AS_THREADS = 256, AS_PAD = 68;
 constexpr size_t AS_SMEM = 2 * MOG_D * AS_PAD * sizeof(float);
 
-__device__ __forceinline__ void job_unit(const AssignJob &jb, int u, const uint16_t *&x,
-                                         int &n, int &k) {
+// Where unit u's rows are: n mid rows, k centroids.  Row r of the unit is the key at
+// position S + r of (b, h); mid_row() returns its address.
+struct JobUnit {
+    const uint16_t *x;  // row 0 of a contiguous unit
+    int n, k, b, h, s0;
+};
+__device__ __forceinline__ JobUnit job_unit(const AssignJob &jb, int u) {
+    JobUnit j;
     if (jb.unit_info) {
         const int *ui = jb.unit_info + u * UI_STRIDE;
-        int b = ui[UI_B], h = u % jb.h_kv;
-        n = ui[UI_NMID];
-        k = ui[UI_C];
-        x = jb.K + b * jb.sb + h * jb.sh + (int64_t)ui[UI_S] * jb.sn;
+        j.b = ui[UI_B];
+        j.h = u % jb.h_kv;
+        j.n = ui[UI_NMID];
+        j.k = ui[UI_C];
+        j.s0 = ui[UI_S];
+        j.x = jb.K + j.b * jb.sb + j.h * jb.sh + (int64_t)j.s0 * jb.sn;
     } else {
-        n = jb.n_single;
-        k = jb.k_single;
-        x = jb.K;
+        j.n = jb.n_single;
+        j.k = jb.k_single;
+        j.b = j.h = j.s0 = 0;
+        j.x = jb.K;
     }
+    return j;
+}
+__device__ __forceinline__ const uint16_t *mid_row(const AssignJob &jb, const JobUnit &j, int r) {
+    if (!jb.bt) return j.x + (int64_t)r * jb.sn;
+    const int64_t pos = (int64_t)j.s0 + r;
+    const int64_t page = jb.bt[(int64_t)j.b * jb.pps + (pos >> jb.pshift)];
+    return jb.K + page * jb.sb + j.h * jb.sh + (pos & ((1 << jb.pshift) - 1)) * jb.sn;
 }
 
 __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
@@ -99,9 +117,8 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
     const int u = blockIdx.y;
     const int *chg = jb.changed + (int64_t)u * jb.T;
     if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
-    const uint16_t *x;
-    int n, k;
-    job_unit(jb, u, x, n, k);
+    const JobUnit ju = job_unit(jb, u);
+    const int n = ju.n, k = ju.k;
     const int *rl = jb.rows ? jb.rows + u * jb.rows_ustride : nullptr;
     const int nrows = rl ? jb.rows_cnt[u * jb.T + jb.t] : n;  // rows of this pass
     if (k <= 0) return;
@@ -118,7 +135,7 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
     for (int e = tid; e < AS_ROWS * 16; e += AS_THREADS) {
         int r = e >> 4, ch = e & 15;
         uint4 w = make_uint4(0, 0, 0, 0);
-        if (s_row[r] >= 0) w = *reinterpret_cast<const uint4 *>(x + (int64_t)s_row[r] * jb.sn + ch * 8);
+        if (s_row[r] >= 0) w = *reinterpret_cast<const uint4 *>(mid_row(jb, ju, s_row[r]) + ch * 8);
         uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -248,9 +265,8 @@ __global__ void __launch_bounds__(FB_THREADS) k_assign_fallback(AssignJob jb) {
     const int u = blockIdx.y;
     const int *chg = jb.changed + (int64_t)u * jb.T;
     if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
-    const uint16_t *x;
-    int n, k;
-    job_unit(jb, u, x, n, k);
+    const JobUnit ju = job_unit(jb, u);
+    const int k = ju.k;
     const int cnt = jb.fb_cnt[u * jb.T + jb.t];
     const float *cent = jb.cent + u * jb.cent_ustride;
     const bool vec = (reinterpret_cast<uintptr_t>(cent) & 15) == 0;
@@ -260,7 +276,7 @@ __global__ void __launch_bounds__(FB_THREADS) k_assign_fallback(AssignJob jb) {
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int e = warp; e < cnt; e += nwarps) {
         int r = jb.fb_list[u * jb.fb_ustride + e];
-        const uint16_t *xr = x + (int64_t)r * jb.sn;
+        const uint16_t *xr = mid_row(jb, ju, r);
         __syncwarp();
         for (int jj = lane; jj < MOG_D; jj += 32) xs[jj] = bf1(xr[jj]);
         __syncwarp();
@@ -1086,9 +1102,7 @@ __global__ void __launch_bounds__(128) k_cent_prep(AssignJob jb) {
     const int u = blockIdx.y;
     const int *chg = jb.changed + (int64_t)u * jb.T;
     if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
-    const uint16_t *x;
-    int n, k;
-    job_unit(jb, u, x, n, k);
+    const int k = job_unit(jb, u).k;
     const int c = blockIdx.x * 8 + (threadIdx.x >> 4), q = threadIdx.x & 15;
     if (c >= tc_chunks(k) * TC_NC) return;
     float v[8];
@@ -1138,9 +1152,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_assign_tc(AssignJob jb, const
     const int u = blockIdx.y;
     const int *chg = jb.changed + (int64_t)u * jb.T;
     if (jb.t >= 2 && converged_by(chg, jb.t - 1)) return;
-    const uint16_t *x;
-    int n, k;
-    job_unit(jb, u, x, n, k);
+    const JobUnit ju = job_unit(jb, u);
+    const int n = ju.n, k = ju.k;
     const int ntile = (n + TC_M - 1) / TC_M;
     const int tile0 = blockIdx.x * tiles_per_cta;
     const int ntl = min(tiles_per_cta, ntile - tile0);
@@ -1413,6 +1426,9 @@ static AssignJob build_job(const Dev &dv, int t) {
     jb.sb = dv.sb;
     jb.sh = dv.sh;
     jb.sn = dv.sn;
+    jb.bt = dv.bt;
+    jb.pshift = dv.pshift;
+    jb.pps = dv.pps;
     jb.h_kv = dv.h_kv;
     jb.unit_info = dv.unit_info;
     jb.n_single = 0;
@@ -1523,7 +1539,8 @@ cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s, const Tr
     if (pl.n_mid_max > 0) {
         k_l1_init<<<dim3(pl.c_max, U), 128, 0, s>>>(dv);
         CUtensorMap kmap;
-        const bool tma = key_map(&kmap, dv.K, pl.n_cap, dv.h_kv, pl.batch, dv.sn, dv.sh, dv.sb);
+        // TMA tiles need contiguous rows: a paged cache takes the direct fp32 pass
+        const bool tma = !dv.bt && key_map(&kmap, dv.K, pl.n_cap, dv.h_kv, pl.batch, dv.sn, dv.sh, dv.sb);
         for (int t = 0; t < pl.T1; ++t) {
             AssignJob jb = build_job(dv, t);
             if (tr.l1c &&  // traced build: the centroids this step assigns to
@@ -1564,6 +1581,8 @@ cudaError_t launch_assign_l1(const uint16_t *x, int64_t ld, int n, const float *
     jb.K = x;
     jb.sb = jb.sh = 0;
     jb.sn = ld;
+    jb.bt = nullptr;
+    jb.pshift = jb.pps = 0;
     jb.h_kv = 1;
     jb.unit_info = nullptr;
     jb.n_single = n;

@@ -952,3 +952,154 @@ def test_bf16_summaries_follow_the_sliding_window():
     assert np.array_equal(sb16, as_bf(g["sub_ms"]))
     inj.summ = {k: ora.summaries_bf16(s) for k, s in inj.summ.items()}
     print("bf16 + sliding decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
+
+
+# -------------------------------------------------------------- periodic re-clustering
+
+@pytest.mark.parametrize("sliding", [0, 1])
+def test_recluster_equals_fresh_build_and_matches_oracle(sliding):
+    """mog_recluster after 40 appended tokens: the partition, the summaries and the window
+    equal a fresh mog_build over the grown sequences (with the build's C and L), bit for
+    bit -- also when the sliding window had moved keys into the clusters.  The statistics
+    and the decode then match the oracle on that partition."""
+    n0, steps = 3000, 40
+    w = small_workload(n0, batch=2, h_kv=2, h_q=8, top_c=5, top_s=3, n_recent=32, seed=36)
+    K, V, q, lens = wl.make_batch(w, n_cap=n0 + steps)
+    rng = np.random.default_rng(37)
+    prm = mog.make_params(2, 2, 8, n0 + steps, n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=5,
+                          top_s=3, n_sink=4, n_recent=32, sliding=sliding)
+    Kd, Vd = bf(K), bf(V)
+    h = mog.build(Kd, Vd, lens, prm)
+    for t in range(steps):
+        kn = wl.to_bf16(rng.standard_normal((2, 2, D)))
+        vn = wl.to_bf16(rng.standard_normal((2, 2, D)))
+        h.append(bf(kn), bf(vn))
+        K[:, :, n0 + t], V[:, :, n0 + t] = kn, vn
+    h.recluster()
+    fresh = mog.build(Kd, Vd, lens + steps, mog.make_params(
+        2, 2, 8, n0 + steps, n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=5, top_s=3, n_sink=4,
+        n_recent=32, sliding=sliding))
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0 and fresh.sync_status() == 0
+    lay = h.layout()
+    U, cm, lm = lay.units, lay.c_max, lay.l_max
+    for name, dt, shape in (("unit_info", torch.int32, (U, 8)), ("perm", torch.int32, (U, lay.n_cap)),
+                            ("sub_off", torch.int32, (U, lay.sub_off_stride)), ("cl_n", torch.int32, (U, cm)),
+                            ("cl_ms", torch.float32, (U, cm, 2, D)), ("cl_vbar", torch.float32, (U, cm, D)),
+                            ("sub_n", torch.int32, (U, cm * lm)), ("sub_ms", torch.float32, (U, cm * lm, 2, D)),
+                            ("sub_vbar", torch.float32, (U, cm * lm, D))):
+        a = h.array(name, dt, shape).cpu().numpy()
+        b = fresh.array(name, dt, shape).cpu().numpy()
+        info = h.array("unit_info", torch.int32, (U, 8)).cpu().numpy()
+        if name == "perm":   # only the mid region of each unit is defined
+            for u in range(U):
+                assert np.array_equal(a[u, :info[u, 3]], b[u, :info[u, 3]]), (name, u)
+        elif name == "sub_off":   # C*L + 1 offsets per unit (the row stride is padded)
+            for u in range(U):
+                used = info[u, 0] * info[u, 1] + 1
+                assert np.array_equal(a[u, :used], b[u, :used]), (name, u)
+        else:
+            assert np.array_equal(a, b), name
+    assert int(h.array("unit_info", torch.int32, (U, 8)).cpu().numpy()[0, 2]) == n0 + steps
+    # against the oracle, on the partition the GPU chose
+    w2 = wl.Workload("recluster", batch=2, h_kv=2, h_q=8, n=n0 + steps, centres=64, n_clusters=w.n_clusters,
+                     n_sub=w.n_sub, top_c=5, top_s=3, n_sink=4, n_recent=32, seed=36)
+    chk = type("Chk", (), {})()
+    chk.w, chk.h, chk.K, chk.V, chk.q, chk.qd = w2, h, K, V, q, bf(q)
+    chk.lens = lens + steps
+    chk.summ = {}
+    for u in range(U):
+        b, hh = divmod(u, 2)
+        Cn, L, nm, S, perm, off = _partition(h, u, n0 + steps, w2)
+        s = ora.stats(K[b, hh], V[b, hh], perm, off, Cn, L)
+        s.update(perm=perm, sub_off=off, C=Cn, L=L, n_build=n0 + steps, S=S, R=32)
+        chk.summ[(b, hh)] = s
+    chk.gpu_summaries = lambda: Injected.gpu_summaries(chk)
+    _check_stats(chk)
+    print("recluster decode", _check_decode(chk))
+
+
+# ------------------------------------------------------------------ paged KV cache
+
+def _paged_copy(K, V, page_rows, heads_first, seed):
+    """A paged copy of a contiguous cache [B, H, n_cap, d]: pages handed out in a random
+    order, plus spare pages, in either page layout; returns (PagedKV, block table)."""
+    B, H, n_cap, d = K.shape
+    pps = -(-n_cap // page_rows)
+    n_pages = B * pps + 5
+    order = np.random.default_rng(seed).permutation(n_pages)[:B * pps].reshape(B, pps).astype(np.int32)
+    shape = (n_pages, H, page_rows, d) if heads_first else (n_pages, page_rows, H, d)
+    Kp = np.zeros(shape, np.uint16)
+    Vp = np.zeros(shape, np.uint16)
+    for b in range(B):
+        for pg in range(pps):
+            lo, hi = pg * page_rows, min(n_cap, (pg + 1) * page_rows)
+            for h in range(H):
+                if heads_first:
+                    Kp[order[b, pg], h, :hi - lo], Vp[order[b, pg], h, :hi - lo] = K[b, h, lo:hi], V[b, h, lo:hi]
+                else:
+                    Kp[order[b, pg], :hi - lo, h], Vp[order[b, pg], :hi - lo, h] = K[b, h, lo:hi], V[b, h, lo:hi]
+    bt = torch.from_numpy(order).to(DEV)
+    return mog.PagedKV(bf(Kp), bf(Vp), bt, page_rows, heads_first=heads_first), order
+
+
+@pytest.mark.parametrize("page_rows,heads_first", [(64, True), (16, False)])
+def test_paged_cache_is_bit_identical_to_contiguous(page_rows, heads_first):
+    """The same cache stored contiguously and as scattered pages behind a block table:
+    build (the paged one without the tensor-core pass, which needs contiguous rows),
+    decode, append and dense_decode give bit-identical partitions, summaries, selections
+    and outputs."""
+    steps = 6
+    w = small_workload(2900, batch=2, h_kv=2, h_q=8, top_c=5, top_s=3, n_recent=32, seed=38)
+    K, V, q, lens = wl.make_batch(w, n_cap=2900 + steps)
+    lens = np.array([2900, 2750], np.int32)
+    K[1, :, 2750:] = 0
+    V[1, :, 2750:] = 0
+    prm = mog.make_params(2, 2, 8, 2900 + steps, n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=5,
+                          top_s=3, n_sink=4, n_recent=32)
+    Kd, Vd = bf(K), bf(V)
+    pk, order = _paged_copy(K, V, page_rows, heads_first, seed=39)
+    hc = mog.build(Kd, Vd, lens, prm)
+    hp = mog.build(pk, None, lens, prm)
+    qd = bf(q)
+    SW = 5 + 15
+    rng = np.random.default_rng(40)
+    for t in range(steps + 1):
+        sc = torch.empty((2 * 8, SW), dtype=torch.int32, device=DEV)
+        sp = torch.empty_like(sc)
+        oc = hc.decode(qd, sel_out=sc)
+        op = hp.decode(qd, sel_out=sp)
+        torch.cuda.synchronize()
+        assert torch.equal(sc, sp), t
+        assert torch.equal(oc, op), t
+        if t == 0:
+            lay = hc.layout()
+            info = hc.array("unit_info", torch.int32, (lay.units, 8)).cpu().numpy()
+            for u in range(lay.units):
+                a_p, b_p = (x.array("perm", torch.int32, (lay.units, lay.n_cap))[u, :info[u, 3]] for x in (hc, hp))
+                a_o, b_o = (x.array("sub_off", torch.int32, (lay.units, lay.sub_off_stride))[u, :info[u, 0] * info[u, 1] + 1]
+                            for x in (hc, hp))
+                assert torch.equal(a_p, b_p) and torch.equal(a_o, b_o), u
+            for name, dt, shape in (("cl_ms", torch.float32, (lay.units, lay.c_max, 2, D)),
+                                    ("sub_ms", torch.float32, (lay.units, lay.c_max * lay.l_max, 2, D)),
+                                    ("sub_vbar", torch.float32, (lay.units, lay.c_max * lay.l_max, D))):
+                assert torch.equal(hc.array(name, dt, shape), hp.array(name, dt, shape)), name
+        if t < steps:
+            kn = bf(wl.to_bf16(rng.standard_normal((2, 2, D))))
+            vn = bf(wl.to_bf16(rng.standard_normal((2, 2, D))))
+            hc.append(kn, vn)
+            hp.append(kn, vn)
+    ld = torch.tensor(lens + steps, dtype=torch.int32, device=DEV)
+    dc = mog.dense_decode(Kd, Vd, ld, int(lens.max()) + steps, qd)
+    dp = mog.dense_decode(pk, None, ld, int(lens.max()) + steps, qd)
+    assert torch.equal(dc, dp)
+    assert hc.sync_status() == 0 and hp.sync_status() == 0
+    # the appended rows went into the right pages
+    Kc = Kd.view(torch.int16).cpu().numpy().view(np.uint16)
+    Kp = pk.K.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b, n in enumerate(lens):
+        for t in range(steps):
+            pos = n + t
+            pg, r = order[b, pos // page_rows], pos % page_rows
+            row = Kp[pg, :, r] if heads_first else Kp[pg, r, :]
+            assert np.array_equal(row, Kc[b, :, pos])
