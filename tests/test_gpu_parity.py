@@ -1103,3 +1103,17 @@ def test_paged_cache_is_bit_identical_to_contiguous(page_rows, heads_first):
             pg, r = order[b, pos // page_rows], pos % page_rows
             row = Kp[pg, :, r] if heads_first else Kp[pg, r, :]
             assert np.array_equal(row, Kc[b, :, pos])
+
+
+@pytest.mark.parametrize("name,heads_per_unit", [("qwen3-14b-128k", (0, 4)), ("ctx-1m", (0, 3))])
+def test_full_layer_build_and_decode(name, heads_per_unit):
+    """A whole layer at full size, clustered by the library's own build: 4 sequences x 8 KV
+    heads at 131072 keys (362 x 17 groups), or 8 KV heads at 1048576 keys (1024 x 20).
+    Every head's statistics against the oracle's on the partition the GPU chose; selection
+    and decode on two query heads of every KV head."""
+    fb = FromBuildBatch(name)
+    worst_s = _check_stats(fb)
+    G = fb.w.group
+    heads = [u * G + g for u in range(fb.w.batch * fb.w.h_kv) for g in heads_per_unit]
+    ties, worst = _check_decode(fb, sample_heads=heads)
+    print(f"{name} full layer: stats worst {worst_s:.2e}, {ties} near-tie heads, decode worst {worst:.2e}")
