@@ -67,6 +67,9 @@ def args_():
     ap.add_argument("--group-select", action="store_true",
                     help="group-shared selection: the query heads of a KV head select once, "
                          "by the log-sum-exp of their scores")
+    ap.add_argument("--paged", type=int, default=0, metavar="ROWS",
+                    help="hold the cache as pages of ROWS rows (a power of two) in a random "
+                         "order behind a block table")
     ap.add_argument("--bf16-summaries", action="store_true",
                     help="selection scores and residual terms from the summaries rounded to bf16")
     ap.add_argument("--union-exact", action="store_true",
@@ -305,7 +308,24 @@ def run_gpu(a, w, rank, world):
         K, V = np.pad(K, pad), np.pad(V, pad)
     Kd, Vd, qd = bf(K), bf(V), bf(q)
     host_arrays = (K, V, q)  # kept for the oracle's timing sample (rank 0)
-    prm = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], n_clusters=w.n_clusters, n_sub=w.n_sub,
+    if a.paged:  # the same cache as pages in a random order behind a block table
+        pr = a.paged
+        B, H, ncap = Kd.shape[0], Kd.shape[1], Kd.shape[2]
+        pps = -(-ncap // pr)
+        order = torch.randperm(B * pps, generator=torch.Generator().manual_seed(5)).to(dev)
+        pools = []
+        for X in (Kd, Vd):
+            Xp = torch.nn.functional.pad(X, (0, 0, 0, pps * pr - ncap))
+            Xp = Xp.view(B, H, pps, pr, D).permute(0, 2, 1, 3, 4).reshape(B * pps, H, pr, D)
+            pool = torch.empty_like(Xp)
+            pool[order] = Xp
+            pools.append(pool)
+        del Xp
+        Kd = mog.PagedKV(pools[0], pools[1], order.view(B, pps).to(torch.int32).contiguous(), pr)
+        Vd = None
+        torch.cuda.empty_cache()
+    n_cap = K.shape[2]
+    prm = mog.make_params(w.batch, w.h_kv, w.h_q, n_cap, n_clusters=w.n_clusters, n_sub=w.n_sub,
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
                           union_exact=int(a.union_exact), sliding=int(a.sliding),
                           group_select=int(a.group_select), bf16_summaries=int(a.bf16_summaries))
@@ -384,7 +404,7 @@ def run_gpu(a, w, rank, world):
                       sliding=int(a.sliding), group_select=int(a.group_select),
                       bf16_summaries=int(a.bf16_summaries))
             kw.update(over)
-            pv = mog.make_params(w.batch, w.h_kv, w.h_q, Kd.shape[2], **kw)
+            pv = mog.make_params(w.batch, w.h_kv, w.h_q, n_cap, **kw)
             hv = mog.build(Kd, Vd, lens, pv, partition=(perm_t, off_t))
             sv = torch.empty_like(sel)
             ov = hv.decode(qd, sel_out=sv)
@@ -521,7 +541,8 @@ def run_gpu(a, w, rank, world):
                    "top_c": w.top_c, "top_s": w.top_s, "n_sink": w.n_sink, "n_recent": w.n_recent,
                    "mode": ("group-shared selection" if a.group_select else "per-head selection")
                            + (", union-exact" if a.union_exact else "")
-                           + (", bf16 summaries" if a.bf16_summaries else ""),
+                           + (", bf16 summaries" if a.bf16_summaries else "")
+                           + (f", paged cache ({a.paged}-row pages)" if a.paged else ""),
                    "recent_window": "sliding" if a.sliding else "growing",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
