@@ -320,6 +320,28 @@ def summaries_bf16(summ: dict) -> dict:
     return s
 
 
+def fp8_round(x) -> np.ndarray:
+    """x (float64) rounded to float32, then to fp8 e4m3 (3 mantissa bits, exponents -6..8,
+    subnormal steps of 2^-9), to nearest with ties to even, saturating at +-448; returned as
+    float64."""
+    f = np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
+    a = np.minimum(np.abs(f), 448.0)
+    e = np.clip(np.floor(np.log2(np.maximum(a, 2.0 ** -9))), -6, 8)
+    step = 2.0 ** (e - 3)
+    r = np.minimum(np.round(a / step) * step, 448.0)   # np.round: half to even
+    return np.copysign(r, f)
+
+
+def summaries_fp8(summ: dict) -> dict:
+    """The fp8-summary variant of this library (MOG_FLAG_FP8_SUMMARIES; the pages do not
+    fix the summaries' precision): every group's key mean, per-dimension variance and value
+    mean rounded as fp8_round does; counts, partition and everything else unchanged."""
+    s = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in summ.items()}
+    for k in ("cl_mu", "cl_var", "cl_vbar", "sub_mu", "sub_var", "sub_vbar"):
+        s[k] = fp8_round(s[k])
+    return s
+
+
 def group_selection(qs, summ: dict, top_c: int, top_s: int, score_mode: int = 0):
     """Group-shared selection (a variant of this library; the pages select per query head):
     the query heads qs[G][d] of one KV head select once.  A group's score is the log of the

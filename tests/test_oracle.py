@@ -709,3 +709,69 @@ def test_bf16_summaries_decode_matches_independent_mixture(ora):
     assert rel_l2(out, ref) < 1e-12
     full, _, _, _ = ora.mog_head(K, V, w.n, q[0], b, w.top_c, w.top_s)
     print("bf16 summaries vs fp64 summaries, rel-L2", rel_l2(out, full))
+
+
+# -------------------------------------------------------------- fp8 summaries (variant)
+
+def test_fp8_round_matches_torch_e4m3_and_saturates(ora):
+    """The fp8 summaries' rounding: float32, then e4m3 to nearest with ties to even --
+    torch's float32 -> float8_e4m3fn conversion on in-range values, subnormals included --
+    and saturation at +-448 beyond the range."""
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(42)
+    x = np.concatenate([g.standard_normal(4000) * 2.0 ** g.integers(-11, 8, 4000), [0.0, 1.0, -3.3]])
+    x = x[np.abs(x) <= 440.0]
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(ora.fp8_round(x), ref)
+    assert ora.fp8_round(1.0625) == 1.0 and ora.fp8_round(1.1875) == 1.25       # ties to even
+    assert ora.fp8_round(2.0 ** -10) == 0.0 and ora.fp8_round(3 * 2.0 ** -10) == 2.0 ** -8
+    assert ora.fp8_round(1000.0) == 448.0 and ora.fp8_round(-470.0) == -448.0
+
+
+def test_fp8_summaries_decode_matches_independent_mixture(ora):
+    """Decode on the fp8-rounded summaries against the numpy mixture with statistics rounded
+    by torch's e4m3 conversion, and a brute-force selection on the rounded scores."""
+    torch = pytest.importorskip("torch")
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    b = ora.build_unit(K, V, w.n, w.n_sink, w.n_recent, w.n_clusters, w.n_sub)
+    r = ora.summaries_fp8(b)
+    out, sel_c, sel_s, _ = ora.mog_head(K, V, w.n, q[0], r, w.top_c, w.top_s)
+    tq = lambda a: torch.from_numpy(np.asarray(a, np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    Kf, Vf, qf = f64(K), f64(V), f64(q[0])
+    perm, off, L = b["perm"], b["sub_off"], w.n_sub
+
+    def gstats(mem):
+        X = Kf[mem]
+        return tq(X.mean(0)), tq(X.var(0)), tq(Vf[mem].mean(0))
+
+    def score(mu, var, n):
+        return math.log(n) + TAU * (qf @ mu) + 0.5 * TAU ** 2 * float(qf ** 2 @ var)
+
+    cl = {c: perm[off[c * L]:off[(c + 1) * L]] for c in range(w.n_clusters)}
+    cs = {c: score(*gstats(m)[:2], m.size) for c, m in cl.items() if m.size}
+    chosen = [c for _, c in sorted((-v, c) for c, v in cs.items())][:w.top_c]
+    assert [int(c) for c in sel_c if c >= 0] == chosen
+    anchors = list(range(w.n_sink)) + list(range(w.n - w.n_recent, w.n))
+    logits = [TAU * (Kf[p] @ qf) for p in anchors]
+    rows = [Vf[p] for p in anchors]
+    for c in range(w.n_clusters):
+        if c not in chosen:
+            if cl[c].size:
+                mu, var, vb = gstats(cl[c])
+                logits.append(score(mu, var, cl[c].size))
+                rows.append(vb)
+            continue
+        subs = {l: perm[off[c * L + l]:off[c * L + l + 1]] for l in range(L)}
+        ss = {l: score(*gstats(m)[:2], m.size) for l, m in subs.items() if m.size}
+        top = [l for _, l in sorted((-v, l) for l, v in ss.items())][:w.top_s]
+        assert [int(l) for l in sel_s[chosen.index(c)] if l >= 0] == top
+        for l, m in subs.items():
+            if l in top:
+                logits += [TAU * (Kf[p] @ qf) for p in m]
+                rows += [Vf[p] for p in m]
+            elif m.size:
+                mu, var, vb = gstats(m)
+                logits.append(score(mu, var, m.size))
+                rows.append(vb)
+    assert rel_l2(out, softmax(np.array(logits)) @ np.array(rows)) < 1e-12
