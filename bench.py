@@ -72,6 +72,8 @@ def args_():
                          "order behind a block table")
     ap.add_argument("--bf16-summaries", action="store_true",
                     help="selection scores and residual terms from the summaries rounded to bf16")
+    ap.add_argument("--fp8-summaries", action="store_true",
+                    help="selection scores and residual terms from the summaries rounded to fp8 e4m3")
     ap.add_argument("--union-exact", action="store_true",
                     help="GQA union-exact mode: every query head attends the union of the "
                          "chosen subclusters of its KV group")
@@ -236,11 +238,18 @@ def oracle_decode_sample(w, budget_s, steps=None, warmup=0, arrays=None, dense_s
 
 # ------------------------------------------------------------------------ GPU path
 
-def bytes_from_selection(h, w, sel, lens, n_now, bf16s=False):
+def summary_bytes(a):
+    """Bytes per element of the summaries' means and variances the decode reads."""
+    return 1 if a.fp8_summaries else 2 if a.bf16_summaries else 4
+
+
+def bytes_from_selection(h, w, sel, lens, n_now, sb=4):
     """Algorithmic bytes of one decode step, per kernel: all cluster summaries and the
     subcluster summaries of each unit's union of selected clusters (selection); the K/V
     rows (+ index) of the union of selected subclusters, the anchors and the residual terms
-    (rows); the partials and the output (merge)."""
+    (rows); the partials and the output (merge).  sb: bytes per element of the summaries'
+    means and variances (4 fp32, 2 bf16, 1 fp8); the residual terms' value means take 4
+    (bf16 high and low parts) with fp32 summaries, else 2 (the high part)."""
     import torch
     lay = h.layout()
     U, cm, lm, G = lay.units, lay.c_max, lay.l_max, lay.group
@@ -267,7 +276,7 @@ def bytes_from_selection(h, w, sel, lens, n_now, bf16s=False):
         items = len(ucl) * L + Cn  # residual terms: the union's subclusters, then clusters
         gp = (G + 3) // 4 * 4
         P = h.splits()
-        sb = 2 if bf16s else 4  # bytes per summary element (mean, variance; value mean's high part)
+        vb = 4 if sb == 4 else 2  # bytes per value-mean element of a residual term
         # selection kernel: query, cluster summaries (mean, variance, count), the union's
         # subcluster summaries and offsets; writes the segments and the residual exponents
         tot["select"] += G * D * 2 + Cn * (2 * sb * D + 4) + len(ucl) * (L * (2 * sb * D + 8) + 4)
@@ -275,7 +284,7 @@ def bytes_from_selection(h, w, sel, lens, n_now, bf16s=False):
         # rows kernel: query, segments, perm index and K, V rows (bf16) of the chosen rows and
         # the anchors, the residual terms (bf16 high/low value means and exponents), partials
         tot["attend"] += G * D * 2 + len(usub) * 12 + Uk * 4 + (Uk + anchors) * 4 * D
-        tot["attend"] += items * (sb * D + gp * 4) + P * G * (D + 4) * 4
+        tot["attend"] += items * (vb * D + gp * 4) + P * G * (D + 4) * 4
         # merge kernel: partials in, the output (fp32) out
         tot["merge"] += P * G * (D + 4) * 4 + G * D * 4
         tot["rows"] += Uk + anchors
@@ -328,7 +337,8 @@ def run_gpu(a, w, rank, world):
     prm = mog.make_params(w.batch, w.h_kv, w.h_q, n_cap, n_clusters=w.n_clusters, n_sub=w.n_sub,
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
                           union_exact=int(a.union_exact), sliding=int(a.sliding),
-                          group_select=int(a.group_select), bf16_summaries=int(a.bf16_summaries))
+                          group_select=int(a.group_select), bf16_summaries=int(a.bf16_summaries),
+                          fp8_summaries=int(a.fp8_summaries))
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -361,7 +371,7 @@ def run_gpu(a, w, rank, world):
     h.decode(qd, out, sel_out=sel)
     torch.cuda.synchronize()
     n_now = [int(x) for x in lens]
-    by = bytes_from_selection(h, w, sel.cpu().numpy(), lens, n_now, a.bf16_summaries)
+    by = bytes_from_selection(h, w, sel.cpu().numpy(), lens, n_now, summary_bytes(a))
 
     clocks = Clocks(local)
     # ---- settle clocks, then dense_decode (the full scan) for comparison ----
@@ -402,7 +412,8 @@ def run_gpu(a, w, rank, world):
             kw = dict(n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s,
                       n_sink=w.n_sink, n_recent=w.n_recent, union_exact=int(a.union_exact),
                       sliding=int(a.sliding), group_select=int(a.group_select),
-                      bf16_summaries=int(a.bf16_summaries))
+                      bf16_summaries=int(a.bf16_summaries),
+                      fp8_summaries=int(a.fp8_summaries))
             kw.update(over)
             pv = mog.make_params(w.batch, w.h_kv, w.h_q, n_cap, **kw)
             hv = mog.build(Kd, Vd, lens, pv, partition=(perm_t, off_t))
@@ -411,7 +422,7 @@ def run_gpu(a, w, rank, world):
             torch.cuda.synchronize()
             assert hv.sync_status() == 0
             ev_ = ((ov.reshape(-1, D).double() - dn).norm(dim=1) / dn.norm(dim=1).clamp_min(1e-30)).cpu().numpy()
-            byv = bytes_from_selection(hv, w, sv.cpu().numpy(), lens, n_now, a.bf16_summaries)
+            byv = bytes_from_selection(hv, w, sv.cpu().numpy(), lens, n_now, summary_bytes(a))
             tv = []
             for i in range(3 + 20):
                 cold_l2()
@@ -464,7 +475,8 @@ def run_gpu(a, w, rank, world):
         sp = mog.make_params(1, w.h_kv, w.h_q, 4096, n_clusters=32, n_sub=sL, top_c=min(w.top_c, 16),
                              top_s=min(w.top_s, sL), n_sink=4, n_recent=64,
                              union_exact=int(a.union_exact), group_select=int(a.group_select),
-                             bf16_summaries=int(a.bf16_summaries))
+                             bf16_summaries=int(a.bf16_summaries),
+                             fp8_summaries=int(a.fp8_summaries))
         sKd, sVd, sqd = bf(sK), bf(sV), bf(sq)
         side = (mog.build(sKd, sVd, sl, sp), sqd, torch.empty(sqd.shape, dtype=torch.float32, device=dev))
     except Exception:
@@ -542,6 +554,7 @@ def run_gpu(a, w, rank, world):
                    "mode": ("group-shared selection" if a.group_select else "per-head selection")
                            + (", union-exact" if a.union_exact else "")
                            + (", bf16 summaries" if a.bf16_summaries else "")
+                           + (", fp8 summaries" if a.fp8_summaries else "")
                            + (f", paged cache ({a.paged}-row pages)" if a.paged else ""),
                    "recent_window": "sliding" if a.sliding else "growing",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",

@@ -66,7 +66,8 @@ typedef enum {
  *                      residual's own exponent); 1 = tau q.mu only.
  *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
  *  flags             : 0, or any of MOG_FLAG_UNION_EXACT, MOG_FLAG_SLIDING,
- *                      MOG_FLAG_GROUP_SELECT, MOG_FLAG_BF16_SUMMARIES.
+ *                      MOG_FLAG_GROUP_SELECT, and one of MOG_FLAG_BF16_SUMMARIES,
+ *                      MOG_FLAG_FP8_SUMMARIES.
  *
  * MOG_FLAG_UNION_EXACT (a variant of this library; the pages select per query head and do
  * not define it): each query head still makes its own selection, but every query head of a
@@ -107,6 +108,14 @@ typedef enum {
  * updates both.  The decode reads half the summary bytes.
  */
 #define MOG_FLAG_BF16_SUMMARIES 8
+/*
+ * MOG_FLAG_FP8_SUMMARIES (a variant of this library, exclusive with the bf16 one): the same
+ * with the summaries rounded from fp32 to fp8 e4m3 (nearest, ties to even, saturating at
+ * +-448); the build writes e4m3 copies of the means and variances (mog_layout.cl_ms8,
+ * sub_ms8: a quarter of the fp32 bytes) and the residual terms read the rounded value
+ * means (exact in bf16).
+ */
+#define MOG_FLAG_FP8_SUMMARIES 16
 typedef struct mog_params {
     int32_t batch, h_kv, h_q, d;
     int32_t n_cap;
@@ -167,6 +176,8 @@ typedef struct mog_layout {
     int64_t fallback;   /* int32 [units][iters_l1]: rows decided by the exact fp64 fallback */
     int64_t cl_ms16;    /* bf16  [units][c_max][2][d]: mean, variance (MOG_FLAG_BF16_SUMMARIES; else 0) */
     int64_t sub_ms16;   /* bf16  [units][c_max*l_max][2][d] (MOG_FLAG_BF16_SUMMARIES; else 0) */
+    int64_t cl_ms8;     /* e4m3  [units][c_max][2][d] (MOG_FLAG_FP8_SUMMARIES; else 0) */
+    int64_t sub_ms8;    /* e4m3  [units][c_max*l_max][2][d] (MOG_FLAG_FP8_SUMMARIES; else 0) */
 } mog_layout;
 
 /* Human-readable name of a status code.  Never NULL. */

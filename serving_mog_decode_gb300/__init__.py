@@ -22,6 +22,7 @@ FLAG_UNION_EXACT = 1  # MOG_FLAG_UNION_EXACT in mog.h
 FLAG_SLIDING = 2      # MOG_FLAG_SLIDING in mog.h
 FLAG_GROUP_SELECT = 4  # MOG_FLAG_GROUP_SELECT in mog.h
 FLAG_BF16_SUMMARIES = 8  # MOG_FLAG_BF16_SUMMARIES in mog.h
+FLAG_FP8_SUMMARIES = 16  # MOG_FLAG_FP8_SUMMARIES in mog.h
 STATUS = ["MOG_OK", "MOG_ERR_INVALID_ARG", "MOG_ERR_SHAPE", "MOG_ERR_ARENA_TOO_SMALL",
           "MOG_ERR_CUDA", "MOG_ERR_DEVICE_CHECK", "MOG_ERR_TIMEOUT", "MOG_ERR_NOT_IMPLEMENTED",
           "MOG_ERR_CAPACITY"]
@@ -79,7 +80,8 @@ class Layout(C.Structure):
                 [(n, C.c_int64) for n in ("unit_info", "n_now", "perm", "sub_off",
                                            "sub_off_stride", "cl_n", "cl_ms", "cl_vbar", "sub_n",
                                            "sub_ms", "sub_vbar", "l1_assign", "status",
-                                           "l1_steps", "fallback", "cl_ms16", "sub_ms16")])
+                                           "l1_steps", "fallback", "cl_ms16", "sub_ms16", "cl_ms8",
+                                           "sub_ms8")])
 
 
 class TraceLayout(C.Structure):
@@ -179,7 +181,7 @@ def _kv(K, V):
 
 def make_params(batch, h_kv, h_q, n_cap, *, d=128, n_clusters=0, n_sub=0, top_c=8, top_s=8,
                 n_sink=4, n_recent=256, iters_l1=10, iters_l2=10, score_mode=0, residual=1,
-                union_exact=0, sliding=0, group_select=0, bf16_summaries=0):
+                union_exact=0, sliding=0, group_select=0, bf16_summaries=0, fp8_summaries=0):
     """mog_params for a batch of `batch` sequences with h_kv KV heads and h_q query heads
     (d = 128), a KV cache of n_cap positions.  n_clusters / n_sub = 0 pick round(sqrt N)
     and ceil(log2 N) per sequence; top_c clusters and top_s subclusters per chosen cluster
@@ -187,12 +189,14 @@ def make_params(batch, h_kv, h_q, n_cap, *, d=128, n_clusters=0, n_sub=0, top_c=
     the variants: union_exact (every head of a KV group attends the union of the group's
     chosen rows), sliding (a fixed recent window whose leaving keys join the clusters),
     group_select (one selection per KV group by the log-sum-exp of its heads' scores),
-    bf16_summaries (scores and residual terms from the summaries rounded to bf16)."""
+    bf16_summaries or fp8_summaries (scores and residual terms from the summaries rounded to
+    bf16, or to fp8 e4m3; not both)."""
     return Params(batch, h_kv, h_q, d, n_cap, n_clusters, n_sub, top_c, top_s, n_sink,
                   n_recent, iters_l1, iters_l2, score_mode, residual,
                   (FLAG_UNION_EXACT if union_exact else 0) | (FLAG_SLIDING if sliding else 0)
                   | (FLAG_GROUP_SELECT if group_select else 0)
-                  | (FLAG_BF16_SUMMARIES if bf16_summaries else 0))
+                  | (FLAG_BF16_SUMMARIES if bf16_summaries else 0)
+                  | (FLAG_FP8_SUMMARIES if fp8_summaries else 0))
 
 
 def arena_bytes(params: Params, lengths_host) -> int:

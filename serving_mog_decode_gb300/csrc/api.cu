@@ -88,8 +88,10 @@ static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
 
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
-    const int known_flags =
-        MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT | MOG_FLAG_BF16_SUMMARIES;
+    const int known_flags = MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT |
+                            MOG_FLAG_BF16_SUMMARIES | MOG_FLAG_FP8_SUMMARIES;
+    if ((p->flags & MOG_FLAG_BF16_SUMMARIES) && (p->flags & MOG_FLAG_FP8_SUMMARIES))
+        return MOG_ERR_INVALID_ARG;
     if ((p->flags & ~known_flags) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
         p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
         p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
@@ -116,6 +118,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.sliding = (p->flags & MOG_FLAG_SLIDING) ? 1 : 0;
     P.group_select = (p->flags & MOG_FLAG_GROUP_SELECT) ? 1 : 0;
     P.bf16s = (p->flags & MOG_FLAG_BF16_SUMMARIES) ? 1 : 0;
+    P.fp8s = (p->flags & MOG_FLAG_FP8_SUMMARIES) ? 1 : 0;
     P.R = p->n_recent;
     P.c_max = P.l_max = 1;
     P.n_mid_max = 0;
@@ -163,6 +166,8 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_sub_vhl = take(2 * U * cm * lm * 2 * MOG_D);
     P.o_cl_ms16 = P.bf16s ? take(2 * U * cm * 2 * MOG_D) : 0;
     P.o_sub_ms16 = P.bf16s ? take(2 * U * cm * lm * 2 * MOG_D) : 0;
+    P.o_cl_ms8 = P.fp8s ? take(U * cm * 2 * MOG_D) : 0;
+    P.o_sub_ms8 = P.fp8s ? take(U * cm * lm * 2 * MOG_D) : 0;
     P.o_l1_assign = take(4 * U * nc);
     P.o_l1_steps = take(4 * U);
     P.o_cent = take(4 * U * cm * MOG_D);
@@ -249,6 +254,7 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.union_exact = P.union_exact;
     d.group_select = P.group_select;
     d.bf16s = P.bf16s;
+    d.fp8s = P.fp8s;
     d.P = P.P;
     d.nseg_max = P.nseg_max;
     d.cimg_ustride = P.cimg_ustride;
@@ -276,6 +282,10 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     if (P.bf16s) {
         PTR(cl_ms16, uint16_t);
         PTR(sub_ms16, uint16_t);
+    }
+    if (P.fp8s) {
+        PTR(cl_ms8, uint8_t);
+        PTR(sub_ms8, uint8_t);
     }
     PTR(cent, float);
     PTR(permA, int);
@@ -631,6 +641,8 @@ extern "C" int mog_get_layout(const mog_handle *h, mog_layout *o) {
     o->fallback = P.o_fb_cnt;
     o->cl_ms16 = P.o_cl_ms16;
     o->sub_ms16 = P.o_sub_ms16;
+    o->cl_ms8 = P.o_cl_ms8;
+    o->sub_ms8 = P.o_sub_ms8;
     return MOG_OK;
 }
 

@@ -1,6 +1,7 @@
 // common.cuh -- device helpers shared by libmog's kernels (sm_103a).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,6 +33,25 @@ __device__ __forceinline__ uint32_t cvt_bf2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// float -> fp8 e4m3 bits, nearest with ties to even, saturating at +-448
+__device__ __forceinline__ uint32_t f2e4m3(float f) {
+    uint16_t r;
+    asm("{\n.reg .b16 t;\ncvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\nmov.b16 %0, t;\n}" : "=h"(r) : "f"(0.f), "f"(f));
+    return r & 0xffu;
+}
+// four fp8 e4m3 values (bytes of w, lowest first) -> floats (exact)
+__device__ __forceinline__ float4 e4m3x4_to_float4(uint32_t w) {
+    uint32_t lo, hi;
+    asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %2;\ncvt.rn.f16x2.e4m3x2 %0, a;\ncvt.rn.f16x2.e4m3x2 %1, b;\n}"
+        : "=r"(lo), "=r"(hi) : "r"(w));
+    const __half2 h0 = *reinterpret_cast<const __half2 *>(&lo), h1 = *reinterpret_cast<const __half2 *>(&hi);
+    return make_float4(__low2float(h0), __high2float(h0), __low2float(h1), __high2float(h1));
+}
+// the float value of an e4m3 byte (exact)
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) { return e4m3x4_to_float4(b & 0xffu).x; }
+// x rounded to the nearest e4m3 value (ties to even, saturating), as a float
+__device__ __forceinline__ float e4m3_round(float x) { return e4m3_to_float(f2e4m3(x)); }
+
 // 2^x by the hardware approximation (flush-to-zero; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
     float r;

@@ -61,17 +61,20 @@ __device__ __forceinline__ void load_weights(float4 *w, const uint16_t *q, int G
 
 // Scores of one group by 4 cooperating lanes (lanes 4i..4i+3 of a warp): lane part q reads
 // the chunks k = q + 4i (dimensions 4k..4k+3) of the mean and of the variance, from the
-// fp32 summary ms or, when ms16 is given, from its bf16 copy.  For every head g < G
-// (G <= GT), emit(g, res, sel) is called on all 4 lanes with the log-mass exponent res
-// (the residual's) and the selection score sel.
+// fp32 summary ms or, when ms16 (ms8) is given, from its bf16 (fp8 e4m3) copy.  For every
+// head g < G (G <= GT), emit(g, res, sel) is called on all 4 lanes with the log-mass
+// exponent res (the residual's) and the selection score sel.
 template <int GT, class Emit>
-__device__ __forceinline__ void quad_scores(const float *ms, const uint16_t *ms16, int n, bool valid,
-                                            const float4 *w, int G, int mode, Emit &&emit) {
+__device__ __forceinline__ void quad_scores(const float *ms, const uint16_t *ms16, const uint8_t *ms8, int n,
+                                            bool valid, const float4 *w, int G, int mode, Emit &&emit) {
     const int q = threadIdx.x & 3;
     float4 mu[8], va[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        if (valid && ms16) {
+        if (valid && ms8) {
+            mu[i] = e4m3x4_to_float4(*reinterpret_cast<const uint32_t *>(ms8 + 4 * (q + 4 * i)));
+            va[i] = e4m3x4_to_float4(*reinterpret_cast<const uint32_t *>(ms8 + MOG_D + 4 * (q + 4 * i)));
+        } else if (valid && ms16) {
             const uint2 a = *reinterpret_cast<const uint2 *>(ms16 + 4 * (q + 4 * i));
             const uint2 b = *reinterpret_cast<const uint2 *>(ms16 + MOG_D + 4 * (q + 4 * i));
             mu[i] = make_float4(bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y));
@@ -302,9 +305,10 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     pdl_wait();
     pdl_trigger();
     {
-        const char *ms0 = dv.cl_ms16 ? reinterpret_cast<const char *>(dv.cl_ms16 + (ug + c0) * 2 * MOG_D)
-                                     : reinterpret_cast<const char *>(dv.cl_ms + (ug + c0) * 2 * MOG_D);
-        const int lines = ns * (dv.cl_ms16 ? 4 : 8);  // 128-byte lines of the slice's summaries
+        const char *ms0 = dv.cl_ms8    ? reinterpret_cast<const char *>(dv.cl_ms8 + (ug + c0) * 2 * MOG_D)
+                          : dv.cl_ms16 ? reinterpret_cast<const char *>(dv.cl_ms16 + (ug + c0) * 2 * MOG_D)
+                                       : reinterpret_cast<const char *>(dv.cl_ms + (ug + c0) * 2 * MOG_D);
+        const int lines = ns * (dv.cl_ms8 ? 2 : dv.cl_ms16 ? 4 : 8);  // 128-byte lines of the slice's summaries
         for (int e = tid; e < lines; e += NT) prefetch_l2(ms0 + 128 * (size_t)e);
         const char *n0 = reinterpret_cast<const char *>(dv.cl_n + ug + c0);
         if (tid * 128 < ns * 4) prefetch_l2(n0 + 128 * tid);
@@ -322,7 +326,8 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
         const bool wr = valid && (tid & 3) == 0;
         LogSumExp gsc;
         quad_scores<GT>(dv.cl_ms + (ug + c) * 2 * MOG_D,
-                        dv.cl_ms16 ? dv.cl_ms16 + (ug + c) * 2 * MOG_D : nullptr, n, valid, w, G, dv.score_mode,
+                        dv.cl_ms16 ? dv.cl_ms16 + (ug + c) * 2 * MOG_D : nullptr,
+                        dv.cl_ms8 ? dv.cl_ms8 + (ug + c) * 2 * MOG_D : nullptr, n, valid, w, G, dv.score_mode,
                     [&](int g, float res, float sl) {
                         if (wr) {
                             ckey[g * m.SLp + cl] = rank_key(sl, c);
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
         const bool wr = valid && (tid & 3) == 0;
         LogSumExp gsc;
         quad_scores<GT>(dv.sub_ms + gi * 2 * MOG_D, dv.sub_ms16 ? dv.sub_ms16 + gi * 2 * MOG_D : nullptr,
-                        valid ? dv.sub_n[gi] : 0, valid, w, G,
+                        dv.sub_ms8 ? dv.sub_ms8 + gi * 2 * MOG_D : nullptr, valid ? dv.sub_n[gi] : 0, valid, w, G,
                     dv.score_mode, [&](int g, float res, float sl) {
                         if (wr) {
                             sres[(s * G + g) * MOG_MAX_L + l] = res;
@@ -774,8 +779,9 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
                                  : dv.cl_vhl + (ug + (item - npi)) * 2 * MOG_D;
                 src += (r & 1) * MOG_D + ch * 8;
             }
-            // with bf16 summaries a term's value mean is its high part alone: the low row is zero
-            cp_async16(sv + swz(r, ch), src, ok && !(dv.bf16s && (r & 1)) ? 16 : 0);
+            // with bf16 or fp8 summaries a term's value mean is its high part alone (for fp8 the
+            // build writes the e4m3-rounded mean there, exact in bf16): the low row is zero
+            cp_async16(sv + swz(r, ch), src, ok && !((dv.bf16s | dv.fp8s) && (r & 1)) ? 16 : 0);
             if (ch == 0) smk[r] = ok ? allm : 0u;
         }
         float *E = reinterpret_cast<float *>(stg);  // [item][MOG_MAX_G] exponents

@@ -41,6 +41,7 @@ struct Dev {
     int union_exact;  // every head attends the union of the heads' chosen subclusters
     int group_select;  // one selection per KV head (log-sum-exp of the heads' scores)
     int bf16s;         // summaries read as bf16 (cl_ms16, sub_ms16, value means' high parts)
+    int fp8s;          // summaries read as fp8 e4m3 (cl_ms8, sub_ms8; value means rounded)
     int P, nchunks, nseg_max;
     int64_t sub_off_stride;
     float tau;
@@ -49,6 +50,7 @@ struct Dev {
     float *cl_ms, *cl_vbar, *sub_ms, *sub_vbar;
     uint16_t *cl_vhl, *sub_vhl;  // value means as bf16 high and low parts [item][2][d]
     uint16_t *cl_ms16, *sub_ms16;  // bf16 mean and variance [item][2][d], or null
+    uint8_t *cl_ms8, *sub_ms8;     // e4m3 mean and variance [item][2][d], or null
     // build workspace
     float *cent;
     int *permA, *changed, *fb_list, *fb_cnt, *hist, *offs, *ctot, *coff, *sub_assign;
@@ -90,10 +92,12 @@ struct TraceDev {
 // Host-side plan: sizes and byte offsets of every array in the arena.
 struct Plan {
     int batch, h_kv, h_q, G, d, n_cap, units, c_max, l_max, tc, ts, T1, T2;
-    int score_mode, residual, union_exact, group_select, sliding, bf16s, R, P, nchunks, n_mid_max, nseg_max;
+    int score_mode, residual, union_exact, group_select, sliding, bf16s, fp8s, R, P, nchunks, n_mid_max,
+        nseg_max;
     int64_t sub_off_stride;
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
-        o_sub_vbar, o_cl_vhl, o_sub_vhl, o_cl_ms16, o_sub_ms16, o_l1_assign, o_status, o_l1_steps;
+        o_sub_vbar, o_cl_vhl, o_sub_vhl, o_cl_ms16, o_sub_ms16, o_cl_ms8, o_sub_ms8, o_l1_assign, o_status,
+        o_l1_steps;
     int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
         o_sub_assign, o_rc_list, o_rc_cnt, o_cimg, o_cnorm, cimg_ustride, cn_ustride;
     int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask, o_resx, resx_stride;

@@ -984,12 +984,14 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
             const int64_t sg = sg0 + l;
             if (upper) {
                 dv.sub_vbar[sg * MOG_D + j] = mean;
-                const uint32_t hi = f2bf(mean);  // bf16 high and low parts, for the decode
+                // bf16 high and low parts, for the decode (fp8 summaries: the e4m3-rounded mean)
+                const uint32_t hi = f2bf(dv.fp8s ? e4m3_round(mean) : mean);
                 dv.sub_vhl[sg * 2 * MOG_D + j] = (uint16_t)hi;
                 dv.sub_vhl[sg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(mean - bf1((uint16_t)hi));
             } else {
                 dv.sub_ms[sg * 2 * MOG_D + j] = mean;
                 if (dv.sub_ms16) dv.sub_ms16[sg * 2 * MOG_D + j] = (uint16_t)f2bf(mean);
+                if (dv.sub_ms8) dv.sub_ms8[sg * 2 * MOG_D + j] = (uint8_t)f2e4m3(mean);
                 cs[l * MOG_D + j] = mean;
                 if (j == 0) dv.sub_n[sg] = ng;
             }
@@ -1012,12 +1014,13 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
         const float cmean = n > 0 ? tot.s / (float)n : 0.f;
         if (upper) {
             dv.cl_vbar[cg * MOG_D + j] = cmean;
-            const uint32_t hi = f2bf(cmean);
+            const uint32_t hi = f2bf(dv.fp8s ? e4m3_round(cmean) : cmean);
             dv.cl_vhl[cg * 2 * MOG_D + j] = (uint16_t)hi;
             dv.cl_vhl[cg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(cmean - bf1((uint16_t)hi));
         } else {
             dv.cl_ms[cg * 2 * MOG_D + j] = cmean;
             if (dv.cl_ms16) dv.cl_ms16[cg * 2 * MOG_D + j] = (uint16_t)f2bf(cmean);
+            if (dv.cl_ms8) dv.cl_ms8[cg * 2 * MOG_D + j] = (uint8_t)f2e4m3(cmean);
             s_cm[j] = cmean;
             if (j == 0) dv.cl_n[cg] = n;
         }
@@ -1033,6 +1036,7 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
                 const float var = ng > 0 ? q.s / (float)ng : 0.f;
                 dv.sub_ms[(sg0 + l) * 2 * MOG_D + MOG_D + j] = var;
                 if (dv.sub_ms16) dv.sub_ms16[(sg0 + l) * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(var);
+                if (dv.sub_ms8) dv.sub_ms8[(sg0 + l) * 2 * MOG_D + MOG_D + j] = (uint8_t)f2e4m3(var);
             }
             q.init();
             ++l;
@@ -1058,6 +1062,7 @@ __global__ void __launch_bounds__(L2_THREADS, 3) k_l2_stats(Dev dv, int do_kmean
             const float var = n > 0 ? q.s / (float)n : 0.f;
             dv.cl_ms[cg * 2 * MOG_D + MOG_D + j] = var;
             if (dv.cl_ms16) dv.cl_ms16[cg * 2 * MOG_D + MOG_D + j] = (uint16_t)f2bf(var);
+            if (dv.cl_ms8) dv.cl_ms8[cg * 2 * MOG_D + MOG_D + j] = (uint8_t)f2e4m3(var);
         } else {
             while (l < L) flush();
         }

@@ -193,10 +193,11 @@ __device__ int nearest_local(const float *ms, int ld, const int *cnt, int k, con
 }
 
 // Welford's update of one group (count n, mean and variance rows ms[0..d), ms[d..2d),
-// their bf16 copy ms16 (or null), value mean vb, its bf16 high/low copy vhl) by the key x
-// and value v (shared memory).  Threads j < d update key dimension j, threads d + j value
+// their bf16 copy ms16 and e4m3 copy ms8 (or null), value mean vb, its bf16 high/low copy
+// vhl, whose high part holds the e4m3-rounded mean when ms8 is given) by the key x and
+// value v (shared memory).  Threads j < d update key dimension j, threads d + j value
 // dimension j.
-__device__ __forceinline__ void welford(int n, float *ms, uint16_t *ms16, float *vb, uint16_t *vhl,
+__device__ __forceinline__ void welford(int n, float *ms, uint16_t *ms16, uint8_t *ms8, float *vb, uint16_t *vhl,
                                         const float *xs, const float *vs) {
     const int tid = threadIdx.x;
     const float n1 = (float)(n + 1);
@@ -212,11 +213,15 @@ __device__ __forceinline__ void welford(int n, float *ms, uint16_t *ms16, float 
             ms16[j] = (uint16_t)f2bf(mu_new);
             ms16[MOG_D + j] = (uint16_t)f2bf(var_new);
         }
+        if (ms8) {
+            ms8[j] = (uint8_t)f2e4m3(mu_new);
+            ms8[MOG_D + j] = (uint8_t)f2e4m3(var_new);
+        }
     } else if (tid < 2 * MOG_D) {
         const int j = tid - MOG_D;
         const float m = vb[j] + (vs[j] - vb[j]) / n1;
         vb[j] = m;
-        const uint32_t hi = f2bf(m);
+        const uint32_t hi = f2bf(ms8 ? e4m3_round(m) : m);
         vhl[j] = (uint16_t)hi;
         vhl[MOG_D + j] = (uint16_t)f2bf(m - bf1((uint16_t)hi));
     }
@@ -299,10 +304,11 @@ __global__ void __launch_bounds__(SL_THREADS) k_slide(Dev dv, int R) {
     csync();  // every CTA has chosen (c, l) from the means before they change
     if (rk == 0) {   // 3. Welford
         welford(ncl, dv.cl_ms + cgi * 2 * MOG_D, dv.cl_ms16 ? dv.cl_ms16 + cgi * 2 * MOG_D : nullptr,
-                dv.cl_vbar + cgi * MOG_D, dv.cl_vhl + cgi * 2 * MOG_D, xs, vs);
+                dv.cl_ms8 ? dv.cl_ms8 + cgi * 2 * MOG_D : nullptr, dv.cl_vbar + cgi * MOG_D,
+                dv.cl_vhl + cgi * 2 * MOG_D, xs, vs);
         welford(nsub, dv.sub_ms + sgi * 2 * MOG_D, dv.sub_ms16 ? dv.sub_ms16 + sgi * 2 * MOG_D : nullptr,
-                dv.sub_vbar + sgi * MOG_D, dv.sub_vhl + sgi * 2 * MOG_D, xs,
-                vs);
+                dv.sub_ms8 ? dv.sub_ms8 + sgi * 2 * MOG_D : nullptr, dv.sub_vbar + sgi * MOG_D,
+                dv.sub_vhl + sgi * 2 * MOG_D, xs, vs);
     }
     for (int bi = (CL - first + batch - 1) / batch - 1; bi >= 0; --bi) {
         const int base = first + bi * batch, top = min(CL, base + batch);

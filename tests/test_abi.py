@@ -54,14 +54,20 @@ def test_arena_size_query_and_validation(lib):
         mog.arena_bytes(mog.make_params(1, 1, 1, 100, n_sub=33), [100])  # L > 32
     with pytest.raises(mog.MogError, match="INVALID_ARG"):
         mog.arena_bytes(mog.make_params(1, 1, 1, 100, top_c=-1), [100])
-    # flags: the union-exact, sliding, group-select and bf16-summary bits are the only ones defined
+    # flags: the union-exact, sliding, group-select, bf16- and fp8-summary bits are the only ones defined
     u = mog.make_params(1, 8, 32, 32768, n_clusters=181, n_sub=15, top_c=8, top_s=8, union_exact=1)
     assert u.flags == mog.FLAG_UNION_EXACT and mog.arena_bytes(u, [32768]) == n
     assert mog.make_params(1, 1, 1, 100, sliding=1).flags == mog.FLAG_SLIDING
     assert mog.make_params(1, 1, 1, 100, group_select=1).flags == mog.FLAG_GROUP_SELECT
     bf = mog.make_params(1, 8, 32, 32768, n_clusters=181, n_sub=15, top_c=8, top_s=8, bf16_summaries=1)
     assert bf.flags == mog.FLAG_BF16_SUMMARIES and mog.arena_bytes(bf, [32768]) > n  # + the bf16 copies
-    u.flags = 16
+    f8 = mog.make_params(1, 8, 32, 32768, n_clusters=181, n_sub=15, top_c=8, top_s=8, fp8_summaries=1)
+    nb, n8 = mog.arena_bytes(bf, [32768]), mog.arena_bytes(f8, [32768])
+    assert f8.flags == mog.FLAG_FP8_SUMMARIES and n < n8 < nb  # + the e4m3 copies, half the bf16 ones
+    both = mog.make_params(1, 1, 1, 100, bf16_summaries=1, fp8_summaries=1)  # one rounding at most
+    with pytest.raises(mog.MogError, match="INVALID_ARG"):
+        mog.arena_bytes(both, [100])
+    u.flags = 32
     with pytest.raises(mog.MogError, match="INVALID_ARG"):
         mog.arena_bytes(u, [32768])
     # automatic C and L follow round(sqrt N) and ceil(log2 N)

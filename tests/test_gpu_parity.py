@@ -190,7 +190,7 @@ class Injected:
     each unit (small cases) or a rule applied to positions (large cases)."""
 
     def __init__(self, w, lens=None, mode="oracle", n_cap=None, union_exact=0, sliding=0,
-                 group_select=0, score_mode=0, residual=1, bf16_summaries=0):
+                 group_select=0, score_mode=0, residual=1, bf16_summaries=0, fp8_summaries=0):
         self.w = w
         self.score_mode, self.residual = score_mode, residual
         lens = wl.lengths(w) if lens is None else np.asarray(lens, np.int32)
@@ -205,7 +205,8 @@ class Injected:
                                    n_sub=w.n_sub, top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink,
                                    n_recent=w.n_recent, union_exact=union_exact, sliding=sliding,
                                    group_select=group_select, score_mode=score_mode,
-                                   residual=residual, bf16_summaries=bf16_summaries)
+                                   residual=residual, bf16_summaries=bf16_summaries,
+                                   fp8_summaries=fp8_summaries)
         stride = mog.sub_off_stride(self.prm, lens)
         perm_all = np.zeros((B * Hkv, self.n_cap), np.int32)
         off_all = np.zeros((B * Hkv, stride), np.int32)
@@ -952,6 +953,96 @@ def test_bf16_summaries_follow_the_sliding_window():
     assert np.array_equal(sb16, as_bf(g["sub_ms"]))
     inj.summ = {k: ora.summaries_bf16(s) for k, s in inj.summ.items()}
     print("bf16 + sliding decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
+
+
+# ------------------------------------------------------------- fp8 summaries (variant)
+
+def _e4m3_bits_to_f64(a):
+    """fp8 e4m3 bytes -> their values, decoded from the format's fields (sign, 4 exponent
+    bits with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals)."""
+    a = np.asarray(a).astype(np.uint8).astype(np.int64)
+    sgn = np.where(a & 0x80, -1.0, 1.0)
+    e, m = (a >> 3) & 0xF, a & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * 2.0 ** (e - 7))
+    return sgn * mag
+
+
+def _fp8_arrays(inj):
+    lay = inj.h.layout()
+    U, cm, lm = lay.units, lay.c_max, lay.l_max
+    cl8 = _e4m3_bits_to_f64(inj.h.array("cl_ms8", torch.uint8, (U, cm, 2, D)).cpu().numpy())
+    sb8 = _e4m3_bits_to_f64(inj.h.array("sub_ms8", torch.uint8, (U, cm * lm, 2, D)).cpu().numpy())
+    return cl8, sb8
+
+
+def _check_fp8_copies(inj):
+    """The GPU's e4m3 copies of the key means and variances against the oracle's rounding of
+    its own statistics: equal, except where the fp32 value sits on a rounding tie of e4m3
+    (the GPU's and the oracle's fp32 statistics may differ in their last bits); there the
+    GPU holds one of the tie's two neighbours."""
+    cl8, sb8 = _fp8_arrays(inj)
+    total, off_by_one = 0, 0
+    for (b, h), s in inj.summ.items():
+        u = b * inj.w.h_kv + h
+        Cn, L = s["C"], s["L"]
+        for gpu, ref, n in ((cl8[u, :Cn, 0], s["cl_mu"], s["cl_n"]), (cl8[u, :Cn, 1], s["cl_var"], s["cl_n"]),
+                            (sb8[u, :Cn * L, 0], s["sub_mu"], s["sub_n"]),
+                            (sb8[u, :Cn * L, 1], s["sub_var"], s["sub_n"])):
+            keep = n > 0
+            g, r = gpu[keep], ora.fp8_round(ref[keep])
+            total += g.size
+            bad = g != r
+            if bad.any():
+                mid = (g[bad] + r[bad]) / 2
+                f32 = ref[keep][bad].astype(np.float32).astype(np.float64)
+                assert np.all(np.abs(f32 - mid) <= np.abs(mid) * 2.0 ** -18), "not at a rounding tie"
+                lo, hi = ora.fp8_round(mid * (1 - 2.0 ** -10)), ora.fp8_round(mid * (1 + 2.0 ** -10))
+                assert np.all(((g[bad] == lo) & (r[bad] == hi)) | ((g[bad] == hi) & (r[bad] == lo))), \
+                    "not the tie's neighbours"
+                off_by_one += int(bad.sum())
+    assert total > 0 and off_by_one <= max(2, total // 10000), (off_by_one, total)
+    return total, off_by_one
+
+
+def test_fp8_summaries_match_oracle():
+    """MOG_FLAG_FP8_SUMMARIES on the oracle's partition: the fp32 summaries as usual, their
+    e4m3 copies against the oracle's rounding, then the selection and the decode (whose
+    residual terms read the rounded value means) against the oracle on the rounded
+    summaries."""
+    w = small_workload(3000, batch=2, h_kv=2, h_q=8, top_c=5, top_s=3, seed=36)
+    inj = Injected(w, fp8_summaries=1)
+    _check_stats(inj)
+    total, ob1 = _check_fp8_copies(inj)
+    lay = inj.h.layout()
+    assert lay.cl_ms16 == 0 and lay.sub_ms16 == 0
+    inj.summ = {k: ora.summaries_fp8(s) for k, s in inj.summ.items()}
+    ties, worst = _check_decode(inj)
+    print(f"fp8 summaries: {total} values, {ob1} off at ties; {ties} near-tie heads, decode worst {worst:.2e}")
+
+
+def test_fp8_summaries_full_size_qwen3_4b():
+    """The 32K workload at full size with fp8 summaries (position-rule partition)."""
+    w = wl.WORKLOADS["qwen3-4b-32k"]
+    inj = Injected(w, mode="rule", fp8_summaries=1)
+    _check_fp8_copies(inj)
+    inj.summ = {k: ora.summaries_fp8(s) for k, s in inj.summ.items()}
+    print("fp8 summaries 32K", _check_decode(inj))
+
+
+def test_fp8_summaries_follow_the_sliding_window():
+    """With the sliding window the Welford updates keep the e4m3 copies equal to the
+    rounding of the updated fp32 summaries (torch's e4m3 conversion, nearest-even)."""
+    steps, n0 = 12, 3000
+    w = small_workload(n0, batch=1, h_kv=2, h_q=4, n_recent=32, seed=85)
+    inj = Injected(w, n_cap=n0 + steps, sliding=1, fp8_summaries=1)
+    _slide_steps(inj, n0, steps, seed=13)
+    g = inj.gpu_summaries()
+    cl8, sb8 = _fp8_arrays(inj)
+    as_f8 = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(cl8, as_f8(np.clip(g["cl_ms"], -448, 448)))
+    assert np.array_equal(sb8, as_f8(np.clip(g["sub_ms"], -448, 448)))
+    inj.summ = {k: ora.summaries_fp8(s) for k, s in inj.summ.items()}
+    print("fp8 + sliding decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
 
 
 # -------------------------------------------------------------- periodic re-clustering
