@@ -48,7 +48,7 @@ def lib():
         build()
         l = C.CDLL(_LIB)
         for name in ("ora_assign", "ora_update", "ora_lloyd", "ora_stats", "ora_build",
-                     "ora_select", "ora_decode", "ora_dense"):
+                     "ora_select", "ora_decode", "ora_dense", "ora_pp_pick", "ora_kmeanspp"):
             getattr(l, name).restype = C.c_int
         _lib = l
     return _lib
@@ -116,6 +116,40 @@ def lloyd(x: np.ndarray, k: int, iters: int, rows=None, history: bool = False):
     return cent, asg, s, (hist[:s] if history else None)
 
 
+def _draws(draws, k):
+    u = np.ascontiguousarray(draws, np.float64).reshape(-1)
+    if u.shape[0] < k:
+        raise ValueError("one draw per seed")
+    return u
+
+
+def pp_pick(x: np.ndarray, seeds, u: float, rows=None) -> int:
+    """One k-means++ step (R28): the member index of the next seed after `seeds` (member
+    indices into x[rows]) for the uniform draw u."""
+    x = _u16(x)
+    d = x.shape[1]
+    rows = np.arange(x.shape[0], dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    sd = np.ascontiguousarray(seeds, np.int64).reshape(-1)
+    out = np.zeros(1, np.int64)
+    _check(lib().ora_pp_pick(_ptr(x), _i64(d), _ptr(rows), _i64(rows.shape[0]), _i64(d),
+                             _ptr(sd if sd.size else np.zeros(1, np.int64)), _i64(sd.size),
+                             C.c_double(float(u)), _ptr(out)), "pp_pick")
+    return int(out[0])
+
+
+def kmeanspp(x: np.ndarray, k: int, draws, rows=None) -> np.ndarray:
+    """k-means++ seeding (R28) of x[rows]: the k seeds' member indices, seed r drawn with
+    draws[r]."""
+    x = _u16(x)
+    d = x.shape[1]
+    rows = np.arange(x.shape[0], dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    u = _draws(draws, k)
+    out = np.zeros(k, np.int64)
+    _check(lib().ora_kmeanspp(_ptr(x), _i64(d), _ptr(rows), _i64(rows.shape[0]), _i64(k), _i64(d),
+                              _ptr(u), _ptr(out)), "kmeanspp")
+    return out
+
+
 def _summ_buffers(Cn: int, L: int, d: int):
     return dict(
         cl_n=np.zeros(Cn, np.int32), cl_mu=np.zeros((Cn, d)), cl_var=np.zeros((Cn, d)),
@@ -142,9 +176,10 @@ def stats(K: np.ndarray, V: np.ndarray, perm: np.ndarray, sub_off: np.ndarray, C
 
 
 def build_unit(K: np.ndarray, V: np.ndarray, n_build: int, S: int, R: int, Cn: int, L: int,
-               T1: int = 10, T2: int = 10):
+               T1: int = 10, T2: int = 10, draws=None):
     """The full two-level build of one KV head.  Returns a dict with ``perm``,
-    ``sub_off``, ``l1_assign``, ``steps`` and the summaries."""
+    ``sub_off``, ``l1_assign``, ``steps`` and the summaries.  draws (Cn uniforms in
+    [0, 1)): k-means++ seeds for the first level (R28) instead of strided ones."""
     K, V = _u16(K), _u16(V)
     d = K.shape[1]
     nm = max(0, n_build - R - S)
@@ -153,8 +188,9 @@ def build_unit(K: np.ndarray, V: np.ndarray, n_build: int, S: int, R: int, Cn: i
     sub_off = np.zeros(Cn * L + 1, np.int32)
     l1 = np.zeros(max(nm, 1), np.int32)
     steps = np.zeros(2, np.int64)
+    u = None if draws is None else _draws(draws, Cn)
     _check(lib().ora_build(_ptr(K), _ptr(V), _i64(d), _i64(n_build), _i64(d), _i64(S), _i64(R),
-                           _i64(Cn), _i64(L), _i64(T1), _i64(T2), _ptr(perm), _ptr(sub_off),
+                           _i64(Cn), _i64(L), _i64(T1), _i64(T2), _ptr(u), _ptr(perm), _ptr(sub_off),
                            *_summ_args(s), _ptr(l1), _ptr(steps)), "build")
     s.update(perm=perm[:nm], sub_off=sub_off, l1_assign=l1[:nm], steps=(int(steps[0]), int(steps[1])),
              C=Cn, L=L, n_build=n_build, S=S, R=R)

@@ -43,6 +43,15 @@
  *  R12 an unselected cluster contributes its cluster Gaussian; inside a selected cluster
  *      each unselected non-empty subcluster contributes its own Gaussian.
  *  R13 m is the maximum over exact logits and residual exponents.
+ *  R28 k-means++ seeding (a variant of the first level; the pages name no seeding): the
+ *      first seed is member floor(u_0 n); seed r >= 1 is member i with probability
+ *      D2_i / sum D2, D2_i the squared distance of member i to its nearest seed so far,
+ *      drawn by inversion with the given uniform u_r: the first i (in member order) whose
+ *      running sum of D2 exceeds u_r sum D2.  D2 is computed in fp32 (the difference,
+ *      its square and the running sum over the dimensions each rounded to fp32, in index
+ *      order), the precision of the library's kernel, because it decides an index; the
+ *      running sums over the members are fp64.  With sum D2 = 0 (every member on a seed)
+ *      the pick is floor(u_r n) again.
  *  Ranking order everywhere: score descending, then index ascending.
  *
  * Inputs are bf16 bit patterns (uint16) read as exact fp64 values.  Build with
@@ -151,6 +160,112 @@ int ora_update(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, co
     return ORA_OK;
 }
 
+/* ---------------------------------------------------------------------------------
+ * k-means++ seeding (R28)
+ * ------------------------------------------------------------------------------- */
+
+/* D2 of R28: fp32 squared distance of bf16 rows x and c, summed in index order. */
+static float sqdist32(const uint16_t *x, const uint16_t *c, int64_t d)
+{
+    float acc = 0.0f;
+    for (int64_t j = 0; j < d; ++j) {
+        float diff = (float)bf(x[j]) - (float)bf(c[j]);
+        float sq = diff * diff;
+        acc = acc + sq;
+    }
+    return acc;
+}
+
+/* The inversion pick of R28 over weights w[0..n) with uniform u. */
+static int64_t pp_draw(const float *w, int64_t n, double u)
+{
+    double total = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        total = total + (double)w[i];
+    if (!(total > 0.0)) {
+        int64_t j = (int64_t)floor(u * (double)n);
+        return j < n - 1 ? j : n - 1;
+    }
+    double target = u * total, run = 0.0;
+    int64_t last = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (w[i] > 0.0f)
+            last = i;
+        run = run + (double)w[i];
+        if (run > target)
+            return i;
+    }
+    return last; /* u * total rounded up to total: the last member of positive weight */
+}
+
+/*
+ * One k-means++ step (R28), on its own: given r seeds (member indices seeds[0..r)), the
+ * member picked as seed r with the uniform u.  r = 0 picks floor(u n).  For comparison
+ * with another implementation's seeding at any round.
+ */
+int ora_pp_pick(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, int64_t d,
+                const int64_t *seeds, int64_t r, double u, int64_t *pick)
+{
+    if (n <= 0 || d <= 0 || r < 0 || !(u >= 0.0 && u < 1.0))
+        return ORA_EINVAL;
+    for (int64_t i = 0; i < r; ++i)
+        if (seeds[i] < 0 || seeds[i] >= n)
+            return ORA_EINVAL;
+    float *w = malloc((size_t)n * sizeof(float));
+    if (!w)
+        return ORA_ENOMEM;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float best = 0.0f;
+        for (int64_t s = 0; s < r; ++s) {
+            float ds = sqdist32(x + rows[i] * ld, x + rows[seeds[s]] * ld, d);
+            if (s == 0 || ds < best)
+                best = ds;
+        }
+        w[i] = best;
+    }
+    if (r == 0) {
+        int64_t j = (int64_t)floor(u * (double)n);
+        *pick = j < n - 1 ? j : n - 1;
+    } else {
+        *pick = pp_draw(w, n, u);
+    }
+    free(w);
+    return ORA_OK;
+}
+
+/*
+ * k-means++ seeding (R28) of the rows listed in `rows`: seeds_out[r] (r < k) is the member
+ * index of seed r, drawn with draws[r].  D2 is kept as the minimum over the seeds so far,
+ * which equals its definition.
+ */
+int ora_kmeanspp(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, int64_t k,
+                 int64_t d, const double *draws, int64_t *seeds_out)
+{
+    if (n <= 0 || k <= 0 || d <= 0)
+        return ORA_EINVAL;
+    for (int64_t r = 0; r < k; ++r)
+        if (!(draws[r] >= 0.0 && draws[r] < 1.0))
+            return ORA_EINVAL;
+    float *w = malloc((size_t)n * sizeof(float));
+    if (!w)
+        return ORA_ENOMEM;
+    int64_t j = (int64_t)floor(draws[0] * (double)n);
+    seeds_out[0] = j < n - 1 ? j : n - 1;
+    for (int64_t r = 1; r < k; ++r) {
+        const uint16_t *c = x + rows[seeds_out[r - 1]] * ld;
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < n; ++i) {
+            float ds = sqdist32(x + rows[i] * ld, c, d);
+            if (r == 1 || ds < w[i])
+                w[i] = ds;
+        }
+        seeds_out[r] = pp_draw(w, n, draws[r]);
+    }
+    free(w);
+    return ORA_OK;
+}
+
 /*
  * Lloyd's algorithm over the rows listed in `rows` (ascending positions), k centroids,
  * at most `iters` assignment steps (R3, R4).
@@ -160,9 +275,22 @@ int ora_update(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, co
  *   steps_out         number of assignment steps taken
  * With n == 0 nothing is assigned and the centroids are left at zero.
  */
+static int lloyd_seeded(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n,
+                        int64_t k, int64_t d, int64_t iters, const int64_t *seeds,
+                        double *cent_out, int32_t *assign_out, double *hist, int64_t *steps_out);
+
 int ora_lloyd(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, int64_t k,
               int64_t d, int64_t iters, double *cent_out, int32_t *assign_out, double *hist,
               int64_t *steps_out)
+{
+    return lloyd_seeded(x, ld, rows, n, k, d, iters, NULL, cent_out, assign_out, hist, steps_out);
+}
+
+/* Lloyd's algorithm from the seeds seeds[0..k) (member indices), or strided (R3) when
+ * seeds is NULL. */
+static int lloyd_seeded(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n,
+                        int64_t k, int64_t d, int64_t iters, const int64_t *seeds,
+                        double *cent_out, int32_t *assign_out, double *hist, int64_t *steps_out)
 {
     if (n < 0 || k <= 0 || d <= 0 || iters <= 0)
         return ORA_EINVAL;
@@ -177,9 +305,9 @@ int ora_lloyd(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, int
         free(sum); free(cnt); free(prev);
         return ORA_ENOMEM;
     }
-    /* R3: strided seeding in position order */
+    /* R3: strided seeding in position order (R28: the k-means++ seeds instead) */
     for (int64_t c = 0; c < k; ++c) {
-        const uint16_t *xr = x + rows[(c * n) / k] * ld;
+        const uint16_t *xr = x + rows[seeds ? seeds[c] : (c * n) / k] * ld;
         for (int64_t j = 0; j < d; ++j)
             cent_out[c * d + j] = bf(xr[j]);
     }
@@ -273,9 +401,9 @@ int ora_stats(const uint16_t *K, const uint16_t *V, int64_t ld, int64_t d, const
  */
 int ora_build(const uint16_t *K, const uint16_t *V, int64_t ld, int64_t n_build, int64_t d,
               int64_t S, int64_t R, int64_t C, int64_t L, int64_t T1, int64_t T2,
-              int32_t *perm, int32_t *sub_off, int32_t *cl_n, double *cl_mu, double *cl_var,
-              double *cl_vbar, int32_t *sub_n, double *sub_mu, double *sub_var,
-              double *sub_vbar, int32_t *l1_assign, int64_t *steps)
+              const double *draws, int32_t *perm, int32_t *sub_off, int32_t *cl_n,
+              double *cl_mu, double *cl_var, double *cl_vbar, int32_t *sub_n, double *sub_mu,
+              double *sub_var, double *sub_vbar, int32_t *l1_assign, int64_t *steps)
 {
     if (n_build < 0 || d <= 0 || S < 0 || R < 0 || C <= 0 || L <= 0 || T1 <= 0 || T2 <= 0)
         return ORA_EINVAL;
@@ -297,8 +425,19 @@ int ora_build(const uint16_t *K, const uint16_t *V, int64_t ld, int64_t n_build,
     for (int64_t i = 0; i < nm; ++i)
         rows[i] = mid_lo + i;
     int64_t st1 = 0, st2max = 0;
-    if (nm > 0)
-        ora_lloyd(K, ld, rows, nm, C, d, T1, cent1, a1, NULL, &st1);
+    if (nm > 0) {
+        int64_t *seeds = NULL;
+        if (draws) { /* R28: k-means++ seeds for the first level */
+            seeds = malloc((size_t)C * sizeof(int64_t));
+            if (!seeds || ora_kmeanspp(K, ld, rows, nm, C, d, draws, seeds) != ORA_OK) {
+                free(seeds); free(rows); free(a1); free(a2); free(coff); free(cent1);
+                free(cent2); free(mem); free(scount);
+                return ORA_EINVAL;
+            }
+        }
+        lloyd_seeded(K, ld, rows, nm, C, d, T1, seeds, cent1, a1, NULL, &st1);
+        free(seeds);
+    }
     if (l1_assign)
         for (int64_t i = 0; i < nm; ++i)
             l1_assign[i] = a1[i];

@@ -226,6 +226,100 @@ def test_build_partition_is_consistent(ora):
     assert checked == int((b["cl_n"] > 0).sum())
 
 
+# ------------------------------------------------------------------ k-means++ seeding
+
+def _pp_set(n, seed, dup=None):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((n, D)) * rng.uniform(0.2, 3.0, (n, 1))
+    if dup is not None:
+        X = X[np.arange(n) % dup]
+    return wl.to_bf16(X)
+
+
+def _d2(X, seeds):
+    """Squared distance of every row to its nearest seed, by scipy (fp64)."""
+    return cdist(f64(X), f64(X[np.asarray(seeds)]), "sqeuclidean").min(axis=1)
+
+
+def test_pp_pick_hits_constructed_intervals(ora):
+    """A draw in the middle of member i's interval of the D2-weighted line picks i: the
+    inversion rule of k-means++ sampling, with D2 from scipy."""
+    X = _pp_set(40, 1)
+    for r in range(1, 6):
+        seeds = [7, 31, 2, 19, 25][:r]
+        d2 = _d2(X, seeds)
+        cum = np.concatenate([[0.0], np.cumsum(d2)])
+        for i in range(40):
+            if d2[i] == 0:
+                assert i in seeds
+                continue
+            u = (cum[i] + 0.5 * d2[i]) / cum[-1]
+            assert ora.pp_pick(X, seeds, u) == i, (r, i)
+    # the first seed: member floor(u n)
+    for i in range(40):
+        assert ora.pp_pick(X, [], (i + 0.5) / 40) == i
+    assert ora.pp_pick(X, [], 0.0) == 0
+
+
+def test_pp_pick_frequencies_follow_squared_distance(ora):
+    """Over uniform draws, member i is picked with probability D2_i / sum D2 (scipy D2);
+    every frequency lies within 5 binomial standard deviations."""
+    X = _pp_set(12, 2)
+    seeds = [3, 8]
+    p = _d2(X, seeds)
+    p = p / p.sum()
+    rng = np.random.default_rng(5)
+    m = 20000
+    picks = np.array([ora.pp_pick(X, seeds, u) for u in rng.random(m)])
+    f = np.bincount(picks, minlength=12) / m
+    assert f[3] == 0 and f[8] == 0
+    assert np.all(np.abs(f - p) <= 5 * np.sqrt(p * (1 - p) / m) + 1e-12), (f, p)
+
+
+def test_kmeanspp_special_cases(ora):
+    rng = np.random.default_rng(3)
+    # k = n distinct members: every member becomes a seed exactly once
+    X = _pp_set(30, 4)
+    s = ora.kmeanspp(X, 30, rng.random(30))
+    assert sorted(s.tolist()) == list(range(30))
+    # all members equal: sum D2 = 0 after the first seed, so every pick is floor(u n)
+    Xe = np.repeat(_pp_set(1, 5), 25, axis=0)
+    u = rng.random(6)
+    assert ora.kmeanspp(Xe, 6, u).tolist() == np.floor(u * 25).astype(int).tolist()
+    # two distinct points repeated: the second seed is always of the other point
+    X2 = _pp_set(40, 6, dup=2)
+    for _ in range(20):
+        s = ora.kmeanspp(X2, 2, rng.random(2))
+        assert s[0] % 2 != s[1] % 2
+    # the seeds of the full sequence are the one-step picks given the seeds before them
+    u = rng.random(12)
+    s = ora.kmeanspp(X, 12, u)
+    assert all(ora.pp_pick(X, s[:r], u[r]) == s[r] for r in range(12))
+    # a member already chosen is never drawn again while some distance is positive
+    assert len(set(s.tolist())) == 12
+    with pytest.raises(RuntimeError):
+        ora.kmeanspp(X, 3, [0.5, 1.0, 0.2])      # draws must lie in [0, 1)
+
+
+def test_build_with_kmeanspp_seeds_is_lloyd_from_them(ora):
+    """With draws, the first level is scipy's k-means started from the k-means++ seeds
+    (the rows the pick rule chooses), for the number of steps the oracle took; the rest of
+    the build is unchanged."""
+    w = wl.WORKLOADS["tiny-4k"]
+    K, V, q = wl.make_unit(w)
+    S, R, Cn, L = w.n_sink, w.n_recent, w.n_clusters, w.n_sub
+    nm = w.n - S - R
+    u = np.random.default_rng(8).random(Cn)
+    b = ora.build_unit(K, V, w.n, S, R, Cn, L, draws=u)
+    seeds = ora.kmeanspp(K[S:S + nm], Cn, u)
+    X = f64(K[S:S + nm])
+    _, lab = kmeans2(X, X[seeds], iter=b["steps"][0], minit="matrix", missing="warn")
+    assert np.array_equal(b["l1_assign"], lab)
+    assert np.array_equal(np.sort(b["perm"]), np.arange(S, S + nm))
+    # strided seeds give a different partition on these inputs
+    assert not np.array_equal(ora.build_unit(K, V, w.n, S, R, Cn, L)["l1_assign"], b["l1_assign"])
+
+
 # ----------------------------------------------------------------------------- estimator
 
 def _single_group(ora, K, V):
