@@ -72,6 +72,8 @@ def args_():
                          "order behind a block table")
     ap.add_argument("--bf16-summaries", action="store_true",
                     help="selection scores and residual terms from the summaries rounded to bf16")
+    ap.add_argument("--kmeanspp", action="store_true",
+                    help="first-level k-means++ seeds (draws from the input generator)")
     ap.add_argument("--fp8-summaries", action="store_true",
                     help="selection scores and residual terms from the summaries rounded to fp8 e4m3")
     ap.add_argument("--union-exact", action="store_true",
@@ -338,7 +340,11 @@ def run_gpu(a, w, rank, world):
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
                           union_exact=int(a.union_exact), sliding=int(a.sliding),
                           group_select=int(a.group_select), bf16_summaries=int(a.bf16_summaries),
-                          fp8_summaries=int(a.fp8_summaries))
+                          fp8_summaries=int(a.fp8_summaries), kmeanspp=int(a.kmeanspp))
+    draws = None
+    if a.kmeanspp:
+        tl = mog.trace_layout(prm, lens)
+        draws = torch.from_numpy(wl.seed_draws(tl.units, tl.c_max, w.seed + 100)).to(dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -354,7 +360,7 @@ def run_gpu(a, w, rank, world):
     torch.cuda.synchronize()
     b0, b1 = ev(), ev()
     b0.record()
-    h = mog.build(Kd, Vd, lens, prm)
+    h = mog.build(Kd, Vd, lens, prm, draws=draws)
     b1.record()
     torch.cuda.synchronize()
     build_ms = b0.elapsed_time(b1)
@@ -555,6 +561,7 @@ def run_gpu(a, w, rank, world):
                            + (", union-exact" if a.union_exact else "")
                            + (", bf16 summaries" if a.bf16_summaries else "")
                            + (", fp8 summaries" if a.fp8_summaries else "")
+                           + (", k-means++ seeds" if a.kmeanspp else "")
                            + (f", paged cache ({a.paged}-row pages)" if a.paged else ""),
                    "recent_window": "sliding" if a.sliding else "growing",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",
@@ -585,7 +592,10 @@ def run_gpu(a, w, rank, world):
         "approx_vs_dense_top_only": ablation["top_only"]["approx_vs_dense"] if ablation else None,
         "ablation": ablation,
         "build": {"ms": round(build_ms, 2), "l1_flop": l1_flop, "l2_flop": l2_flop,
-                  "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3)},
+                  "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3),
+                  # k-means++ reads every mid key once per seed (2 bytes x d each)
+                  "kmeanspp_key_bytes": (sum(float(info[u, 3]) * 2 * D * float(info[u, 0]) for u in range(lay.units))
+                                         if a.kmeanspp else None)},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",
                 "h2d_bytes_per_step": int(q_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 4)},
         "append": append,

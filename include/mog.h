@@ -66,8 +66,8 @@ typedef enum {
  *                      residual's own exponent); 1 = tau q.mu only.
  *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
  *  flags             : 0, or any of MOG_FLAG_UNION_EXACT, MOG_FLAG_SLIDING,
- *                      MOG_FLAG_GROUP_SELECT, and one of MOG_FLAG_BF16_SUMMARIES,
- *                      MOG_FLAG_FP8_SUMMARIES.
+ *                      MOG_FLAG_GROUP_SELECT, MOG_FLAG_KMEANSPP (mog_build_seeded only),
+ *                      and one of MOG_FLAG_BF16_SUMMARIES, MOG_FLAG_FP8_SUMMARIES.
  *
  * MOG_FLAG_UNION_EXACT (a variant of this library; the pages select per query head and do
  * not define it): each query head still makes its own selection, but every query head of a
@@ -116,6 +116,20 @@ typedef enum {
  * means (exact in bf16).
  */
 #define MOG_FLAG_FP8_SUMMARIES 16
+/*
+ * MOG_FLAG_KMEANSPP (a variant of this library; the pages name no seeding): the first
+ * level starts from k-means++ seeds instead of strided ones.  Seed 0 of a unit is mid key
+ * floor(u_0 n) (n mid keys in position order); seed r >= 1 is drawn with the uniform u_r
+ * from the mid keys with probability proportional to D2, the squared distance to the
+ * nearest seed so far: the first key (in position order) whose running sum of D2 exceeds
+ * u_r times the total.  D2 is computed in fp32 (each difference rounded to fp32, four
+ * partial sums, dimension j into sum j mod 4, by fused multiply-add in increasing j, then
+ * (s0 + s1) + (s2 + s3)), the running sums in fp64; if every key sits
+ * on a seed the pick is floor(u_r n).  The draws u are an input (mog_build_seeded); each
+ * round reads every mid key once, so the seeding costs about C_u passes over the keys.
+ * The second level keeps its strided seeds.
+ */
+#define MOG_FLAG_KMEANSPP 32
 typedef struct mog_params {
     int32_t batch, h_kv, h_q, d;
     int32_t n_cap;
@@ -178,6 +192,7 @@ typedef struct mog_layout {
     int64_t sub_ms16;   /* bf16  [units][c_max*l_max][2][d] (MOG_FLAG_BF16_SUMMARIES; else 0) */
     int64_t cl_ms8;     /* e4m3  [units][c_max][2][d] (MOG_FLAG_FP8_SUMMARIES; else 0) */
     int64_t sub_ms8;    /* e4m3  [units][c_max*l_max][2][d] (MOG_FLAG_FP8_SUMMARIES; else 0) */
+    int64_t pp_idx;     /* int32 [units][c_max]: seed r's mid-key index, -1 past C_u (MOG_FLAG_KMEANSPP; else 0) */
 } mog_layout;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -387,6 +402,23 @@ int mog_trace_layout_of(const mog_params *p, const int32_t *lengths_host, mog_tr
 int mog_build_traced(const mog_kv *kv, const int32_t *lengths_dev, const int32_t *lengths_host,
                      const mog_params *p, void *arena_dev, size_t arena_bytes, void *trace_dev,
                      size_t trace_bytes, void *stream, mog_handle **out);
+
+/*
+ * mog_build (or, with trace_dev non-NULL, mog_build_traced) with k-means++ seeds for the
+ * first level; p->flags must include MOG_FLAG_KMEANSPP, which mog_build and
+ * mog_build_traced reject with MOG_ERR_INVALID_ARG.
+ *  draws_dev : float64 [units][c_max] on the device, uniform draws in [0, 1); unit u's
+ *              seed r takes draws_dev[u*c_max + r] (c_max = mog_trace_layout_of().c_max,
+ *              the largest C_u).  Copied into the arena, so mog_recluster seeds from the
+ *              same draws.  A draw outside [0, 1) is clamped into it and sets the status
+ *              word (MOG_ERR_DEVICE_CHECK from mog_sync_status).
+ *  trace_dev, trace_bytes : as mog_build_traced, or NULL and 0.
+ * The seeds are exported in mog_layout.pp_idx.
+ */
+int mog_build_seeded(const mog_kv *kv, const int32_t *lengths_dev, const int32_t *lengths_host,
+                     const mog_params *p, const double *draws_dev, void *arena_dev,
+                     size_t arena_bytes, void *trace_dev, size_t trace_bytes, void *stream,
+                     mog_handle **out);
 
 /*
  * mog_build with the partition given instead of clustered: perm_dev int32 [units][n_cap]

@@ -47,11 +47,12 @@
  *      first seed is member floor(u_0 n); seed r >= 1 is member i with probability
  *      D2_i / sum D2, D2_i the squared distance of member i to its nearest seed so far,
  *      drawn by inversion with the given uniform u_r: the first i (in member order) whose
- *      running sum of D2 exceeds u_r sum D2.  D2 is computed in fp32 (the difference,
- *      its square and the running sum over the dimensions each rounded to fp32, in index
- *      order), the precision of the library's kernel, because it decides an index; the
- *      running sums over the members are fp64.  With sum D2 = 0 (every member on a seed)
- *      the pick is floor(u_r n) again.
+ *      running sum of D2 exceeds u_r sum D2.  D2 is computed in fp32, the precision of
+ *      the library's kernel, because it decides an index: each difference x_j - c_j is
+ *      rounded to fp32, four partial sums s_m (m = j mod 4) take its square by fused
+ *      multiply-add in increasing j, and D2 = (s_0 + s_1) + (s_2 + s_3), each sum
+ *      rounded to fp32.  The running sums over the members are fp64.  With sum D2 = 0
+ *      (every member on a seed) the pick is floor(u_r n) again.
  *  Ranking order everywhere: score descending, then index ascending.
  *
  * Inputs are bf16 bit patterns (uint16) read as exact fp64 values.  Build with
@@ -164,16 +165,18 @@ int ora_update(const uint16_t *x, int64_t ld, const int64_t *rows, int64_t n, co
  * k-means++ seeding (R28)
  * ------------------------------------------------------------------------------- */
 
-/* D2 of R28: fp32 squared distance of bf16 rows x and c, summed in index order. */
+/* D2 of R28: fp32 squared distance of bf16 rows x and c (d a multiple of 4): four
+ * interleaved partial sums by fused multiply-add, then (s0 + s1) + (s2 + s3). */
 static float sqdist32(const uint16_t *x, const uint16_t *c, int64_t d)
 {
-    float acc = 0.0f;
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     for (int64_t j = 0; j < d; ++j) {
         float diff = (float)bf(x[j]) - (float)bf(c[j]);
-        float sq = diff * diff;
-        acc = acc + sq;
+        s[j % 4] = fmaf(diff, diff, s[j % 4]);
     }
-    return acc;
+    float a = s[0] + s[1];
+    float b = s[2] + s[3];
+    return a + b;
 }
 
 /* The inversion pick of R28 over weights w[0..n) with uniform u. */

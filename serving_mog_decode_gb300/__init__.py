@@ -23,6 +23,7 @@ FLAG_SLIDING = 2      # MOG_FLAG_SLIDING in mog.h
 FLAG_GROUP_SELECT = 4  # MOG_FLAG_GROUP_SELECT in mog.h
 FLAG_BF16_SUMMARIES = 8  # MOG_FLAG_BF16_SUMMARIES in mog.h
 FLAG_FP8_SUMMARIES = 16  # MOG_FLAG_FP8_SUMMARIES in mog.h
+FLAG_KMEANSPP = 32       # MOG_FLAG_KMEANSPP in mog.h
 STATUS = ["MOG_OK", "MOG_ERR_INVALID_ARG", "MOG_ERR_SHAPE", "MOG_ERR_ARENA_TOO_SMALL",
           "MOG_ERR_CUDA", "MOG_ERR_DEVICE_CHECK", "MOG_ERR_TIMEOUT", "MOG_ERR_NOT_IMPLEMENTED",
           "MOG_ERR_CAPACITY"]
@@ -81,7 +82,7 @@ class Layout(C.Structure):
                                            "sub_off_stride", "cl_n", "cl_ms", "cl_vbar", "sub_n",
                                            "sub_ms", "sub_vbar", "l1_assign", "status",
                                            "l1_steps", "fallback", "cl_ms16", "sub_ms16", "cl_ms8",
-                                           "sub_ms8")])
+                                           "sub_ms8", "pp_idx")])
 
 
 class TraceLayout(C.Structure):
@@ -101,6 +102,7 @@ _SIGS = {
     "mog_sub_off_stride": (C.c_int, [_P, _P, _P]),
     "mog_trace_layout_of": (C.c_int, [_P, _P, _P]),
     "mog_build_traced": (C.c_int, [_P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, _P]),
+    "mog_build_seeded": (C.c_int, [_P, _P, _P, _P, _P, _P, C.c_size_t, _P, C.c_size_t, _P, _P]),
     "mog_decode": (C.c_int, [_P, _P, _P, _P]),
     "mog_decode_ex": (C.c_int, [_P, _P, _P, _P, _P, _P]),
     "mog_decode_phased": (C.c_int, [_P, _P, _P, _P, _P, _P, _P]),
@@ -181,7 +183,8 @@ def _kv(K, V):
 
 def make_params(batch, h_kv, h_q, n_cap, *, d=128, n_clusters=0, n_sub=0, top_c=8, top_s=8,
                 n_sink=4, n_recent=256, iters_l1=10, iters_l2=10, score_mode=0, residual=1,
-                union_exact=0, sliding=0, group_select=0, bf16_summaries=0, fp8_summaries=0):
+                union_exact=0, sliding=0, group_select=0, bf16_summaries=0, fp8_summaries=0,
+                kmeanspp=0):
     """mog_params for a batch of `batch` sequences with h_kv KV heads and h_q query heads
     (d = 128), a KV cache of n_cap positions.  n_clusters / n_sub = 0 pick round(sqrt N)
     and ceil(log2 N) per sequence; top_c clusters and top_s subclusters per chosen cluster
@@ -190,13 +193,15 @@ def make_params(batch, h_kv, h_q, n_cap, *, d=128, n_clusters=0, n_sub=0, top_c=
     chosen rows), sliding (a fixed recent window whose leaving keys join the clusters),
     group_select (one selection per KV group by the log-sum-exp of its heads' scores),
     bf16_summaries or fp8_summaries (scores and residual terms from the summaries rounded to
-    bf16, or to fp8 e4m3; not both)."""
+    bf16, or to fp8 e4m3; not both), kmeanspp (first-level k-means++ seeds; build() then
+    needs the draws)."""
     return Params(batch, h_kv, h_q, d, n_cap, n_clusters, n_sub, top_c, top_s, n_sink,
                   n_recent, iters_l1, iters_l2, score_mode, residual,
                   (FLAG_UNION_EXACT if union_exact else 0) | (FLAG_SLIDING if sliding else 0)
                   | (FLAG_GROUP_SELECT if group_select else 0)
                   | (FLAG_BF16_SUMMARIES if bf16_summaries else 0)
-                  | (FLAG_FP8_SUMMARIES if fp8_summaries else 0))
+                  | (FLAG_FP8_SUMMARIES if fp8_summaries else 0)
+                  | (FLAG_KMEANSPP if kmeanspp else 0))
 
 
 def arena_bytes(params: Params, lengths_host) -> int:
@@ -318,10 +323,11 @@ def trace_layout(params: Params, lengths_host) -> TraceLayout:
     return lay
 
 
-def build(K, V, lengths, params: Params, stream=None, partition=None, trace=False):
+def build(K, V, lengths, params: Params, stream=None, partition=None, trace=False, draws=None):
     """mog_build (or mog_build_from_partition when partition=(perm, sub_off) is given, or
     mog_build_traced when trace=True, which returns (handle, Trace)).  `lengths` is a host
-    sequence of int; a device copy is made."""
+    sequence of int; a device copy is made.  With the k-means++ flag, draws (float64
+    [units, c_max] uniforms in [0, 1), c_max from trace_layout) go to mog_build_seeded."""
     import numpy as np
     torch = _torch()
     lh = np.ascontiguousarray(lengths, np.int32)
@@ -332,6 +338,20 @@ def build(K, V, lengths, params: Params, stream=None, partition=None, trace=Fals
     arena = arena[off:off + nbytes]
     kv = _kv(K, V)
     h = _P()
+    if params.flags & FLAG_KMEANSPP:
+        if draws is None:
+            raise ValueError("k-means++ seeding needs draws (float64 [units, c_max] in [0, 1))")
+        lay = trace_layout(params, lh)
+        dr = torch.as_tensor(draws, dtype=torch.float64, device=K.device).contiguous()
+        if dr.numel() != lay.units * lay.c_max:
+            raise ValueError(f"k-means++ needs draws of shape [{lay.units}, {lay.c_max}]")
+        tbuf = torch.empty(lay.bytes, dtype=torch.uint8, device=K.device) if trace else None
+        rc = lib().mog_build_seeded(C.byref(kv), _ptr(ld), lh.ctypes.data_as(_P), C.byref(params),
+                                    _ptr(dr), _ptr(arena), nbytes, _ptr(tbuf),
+                                    lay.bytes if trace else 0, _stream(stream), C.byref(h))
+        _check(rc, "mog_build_seeded")
+        hd = Handle(h, arena, params, K, V, ld, lh)
+        return (hd, Trace(tbuf, lay)) if trace else hd
     if trace:
         lay = trace_layout(params, lh)
         tbuf = torch.empty(lay.bytes, dtype=torch.uint8, device=K.device)

@@ -89,7 +89,7 @@ static int64_t al(int64_t x) { return (x + 255) & ~(int64_t)255; }
 int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (!p || !lengths_host || !pl) return MOG_ERR_INVALID_ARG;
     const int known_flags = MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING | MOG_FLAG_GROUP_SELECT |
-                            MOG_FLAG_BF16_SUMMARIES | MOG_FLAG_FP8_SUMMARIES;
+                            MOG_FLAG_BF16_SUMMARIES | MOG_FLAG_FP8_SUMMARIES | MOG_FLAG_KMEANSPP;
     if ((p->flags & MOG_FLAG_BF16_SUMMARIES) && (p->flags & MOG_FLAG_FP8_SUMMARIES))
         return MOG_ERR_INVALID_ARG;
     if ((p->flags & ~known_flags) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
@@ -119,6 +119,7 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.group_select = (p->flags & MOG_FLAG_GROUP_SELECT) ? 1 : 0;
     P.bf16s = (p->flags & MOG_FLAG_BF16_SUMMARIES) ? 1 : 0;
     P.fp8s = (p->flags & MOG_FLAG_FP8_SUMMARIES) ? 1 : 0;
+    P.kpp = (p->flags & MOG_FLAG_KMEANSPP) ? 1 : 0;
     P.R = p->n_recent;
     P.c_max = P.l_max = 1;
     P.n_mid_max = 0;
@@ -196,6 +197,13 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     // residual items per unit: union pairs, then clusters; G exponents each (16-byte rows)
     P.resx_stride = (std::min<int64_t>(cm, G * std::max(P.tc, 1)) * lm + cm) * ((G + 3) & ~3LL);
     P.o_resx = take(4 * U * P.resx_stride);
+    // k-means++ seeding: one CTA per PP_ROWS mid keys of the longest mid region a
+    // re-clustering can see
+    P.pp_nblk = P.kpp ? (int)ceil_div64(std::max<int64_t>(1, nc), PP_ROWS) : 0;
+    P.o_pp_draw = P.kpp ? take(8 * U * cm) : 0;
+    P.o_pp_idx = P.kpp ? take(4 * U * cm) : 0;
+    P.o_pp_d2 = P.kpp ? take(4 * 2 * U * nc) : 0;
+    P.o_pp_part = P.kpp ? take(8 * 2 * U * (int64_t)P.pp_nblk) : 0;
     P.total = o;
     return MOG_OK;
 }
@@ -255,6 +263,8 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     d.group_select = P.group_select;
     d.bf16s = P.bf16s;
     d.fp8s = P.fp8s;
+    d.kpp = P.kpp;
+    d.pp_nblk = P.pp_nblk;
     d.P = P.P;
     d.nseg_max = P.nseg_max;
     d.cimg_ustride = P.cimg_ustride;
@@ -286,6 +296,12 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     if (P.fp8s) {
         PTR(cl_ms8, uint8_t);
         PTR(sub_ms8, uint8_t);
+    }
+    if (P.kpp) {
+        PTR(pp_draw, double);
+        PTR(pp_idx, int);
+        PTR(pp_d2, float);
+        PTR(pp_part, double);
     }
     PTR(cent, float);
     PTR(permA, int);
@@ -410,6 +426,8 @@ static cudaError_t reset_build_state(mog_handle *h, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaMemsetAsync(a + pl.o_cl_n, 0, 4 * (size_t)pl.units * pl.c_max, s);
     if (e == cudaSuccess)
         e = cudaMemsetAsync(a + pl.o_sub_n, 0, 4 * (size_t)pl.units * pl.c_max * pl.l_max, s);
+    if (e == cudaSuccess && pl.kpp)  // seeds past a unit's C stay -1
+        e = cudaMemsetAsync(a + pl.o_pp_idx, 0xff, 4 * (size_t)pl.units * pl.c_max, s);
     return e;
 }
 
@@ -453,6 +471,7 @@ static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
 extern "C" int mog_build(const mog_kv *kv, const int32_t *lengths_dev, const int32_t *lengths_host,
                          const mog_params *p, void *arena_dev, size_t arena_bytes, void *stream,
                          mog_handle **out) {
+    if (p && (p->flags & MOG_FLAG_KMEANSPP)) return MOG_ERR_INVALID_ARG;  // draws: mog_build_seeded
     mog_handle *h = nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int st = common_build(kv, lengths_dev, lengths_host, p, arena_dev, arena_bytes, s, out, &h);
@@ -476,33 +495,64 @@ extern "C" int mog_trace_layout_of(const mog_params *p, const int32_t *lengths_h
     return MOG_OK;
 }
 
+static int build_traced_or_seeded(const mog_kv *kv, const int32_t *lengths_dev,
+                                  const int32_t *lengths_host, const mog_params *p,
+                                  const double *draws, void *arena_dev, size_t arena_bytes,
+                                  void *trace_dev, size_t trace_bytes, void *stream, mog_handle **out);
+
 extern "C" int mog_build_traced(const mog_kv *kv, const int32_t *lengths_dev,
                                 const int32_t *lengths_host, const mog_params *p, void *arena_dev,
                                 size_t arena_bytes, void *trace_dev, size_t trace_bytes,
                                 void *stream, mog_handle **out) {
-    if (!trace_dev || !aligned16(trace_dev)) return MOG_ERR_INVALID_ARG;
+    if (!trace_dev) return MOG_ERR_INVALID_ARG;
+    if (p && (p->flags & MOG_FLAG_KMEANSPP)) return MOG_ERR_INVALID_ARG;  // draws: mog_build_seeded
+    return build_traced_or_seeded(kv, lengths_dev, lengths_host, p, nullptr, arena_dev, arena_bytes,
+                                  trace_dev, trace_bytes, stream, out);
+}
+
+extern "C" int mog_build_seeded(const mog_kv *kv, const int32_t *lengths_dev,
+                                const int32_t *lengths_host, const mog_params *p,
+                                const double *draws_dev, void *arena_dev, size_t arena_bytes,
+                                void *trace_dev, size_t trace_bytes, void *stream, mog_handle **out) {
+    if (!p || !(p->flags & MOG_FLAG_KMEANSPP) || !draws_dev || ((uintptr_t)draws_dev & 7))
+        return MOG_ERR_INVALID_ARG;
+    return build_traced_or_seeded(kv, lengths_dev, lengths_host, p, draws_dev, arena_dev, arena_bytes,
+                                  trace_dev, trace_bytes, stream, out);
+}
+
+static int build_traced_or_seeded(const mog_kv *kv, const int32_t *lengths_dev,
+                                  const int32_t *lengths_host, const mog_params *p,
+                                  const double *draws, void *arena_dev, size_t arena_bytes,
+                                  void *trace_dev, size_t trace_bytes, void *stream, mog_handle **out) {
+    if (trace_dev && !aligned16(trace_dev)) return MOG_ERR_INVALID_ARG;
     if (out) *out = nullptr;
     mog_trace_layout tl;
     int st = mog_trace_layout_of(p, lengths_host, &tl);
     if (st != MOG_OK) return st;
-    if (trace_bytes < (size_t)tl.bytes) return MOG_ERR_ARENA_TOO_SMALL;
+    if (trace_dev && trace_bytes < (size_t)tl.bytes) return MOG_ERR_ARENA_TOO_SMALL;
     mog_handle *h = nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = common_build(kv, lengths_dev, lengths_host, p, arena_dev, arena_bytes, s, out, &h);
     if (st != MOG_OK) return st;
-    char *tr = static_cast<char *>(trace_dev);
-    TraceDev td;
-    td.l1c = reinterpret_cast<float *>(tr + tl.l1_cent);
-    td.l1a = reinterpret_cast<int *>(tr + tl.l1_assign);
-    td.l2c = reinterpret_cast<float *>(tr + tl.l2_cent);
-    td.l2a = reinterpret_cast<int *>(tr + tl.l2_assign);
-    td.l2s = reinterpret_cast<int *>(tr + tl.l2_steps);
-    td.nm = tl.n_mid;
-    cudaError_t e = cudaMemsetAsync(trace_dev, 0, (size_t)tl.bytes, s);
+    TraceDev td{};
+    cudaError_t e = cudaSuccess;
+    if (trace_dev) {
+        char *tr = static_cast<char *>(trace_dev);
+        td.l1c = reinterpret_cast<float *>(tr + tl.l1_cent);
+        td.l1a = reinterpret_cast<int *>(tr + tl.l1_assign);
+        td.l2c = reinterpret_cast<float *>(tr + tl.l2_cent);
+        td.l2a = reinterpret_cast<int *>(tr + tl.l2_assign);
+        td.l2s = reinterpret_cast<int *>(tr + tl.l2_steps);
+        td.nm = tl.n_mid;
+        e = cudaMemsetAsync(trace_dev, 0, (size_t)tl.bytes, s);
+    }
+    if (e == cudaSuccess && draws)
+        e = cudaMemcpyAsync(h->dev.pp_draw, draws, 8 * (size_t)h->plan.units * h->plan.c_max,
+                            cudaMemcpyDeviceToDevice, s);
     if (e == cudaSuccess) e = launch_build(h->dev, h->plan, s, td);
     if (e != cudaSuccess) {
         delete h;
-        return cuda_fail(e, "mog_build_traced launch");
+        return cuda_fail(e, "mog_build launch");
     }
     *out = h;
     return MOG_OK;
@@ -643,6 +693,7 @@ extern "C" int mog_get_layout(const mog_handle *h, mog_layout *o) {
     o->sub_ms16 = P.o_sub_ms16;
     o->cl_ms8 = P.o_cl_ms8;
     o->sub_ms8 = P.o_sub_ms8;
+    o->pp_idx = P.o_pp_idx;
     return MOG_OK;
 }
 

@@ -27,6 +27,8 @@ constexpr int PLAN_START = 8;
 constexpr int PLAN_UCL = PLAN_START + MAX_SPLITS;
 constexpr int PLAN_W = PLAN_UCL + MOG_MAX_UNION;  // ints, whole 16-byte chunks
 constexpr int MAX_C = 4096;        // clusters per unit supported
+constexpr int PP_THREADS = 256, PP_PER = 4;  // k-means++ seeding: keys per thread
+constexpr int PP_ROWS = PP_THREADS * PP_PER;  // ... and per CTA
 
 // Typed view of an arena, passed by value to every kernel.
 struct Dev {
@@ -42,6 +44,7 @@ struct Dev {
     int group_select;  // one selection per KV head (log-sum-exp of the heads' scores)
     int bf16s;         // summaries read as bf16 (cl_ms16, sub_ms16, value means' high parts)
     int fp8s;          // summaries read as fp8 e4m3 (cl_ms8, sub_ms8; value means rounded)
+    int kpp;           // first-level k-means++ seeds (pp_*)
     int P, nchunks, nseg_max;
     int64_t sub_off_stride;
     float tau;
@@ -58,6 +61,12 @@ struct Dev {
     uint16_t *cimg;         // centroid images for the tensor cores [unit][cimg_ustride]
     float *cnorm;           // |c|^2 [unit][cn_ustride]
     int64_t cimg_ustride, cn_ustride;
+    // k-means++ seeding: draws [unit][c_max], seeds [unit][c_max], D2 [2][unit][n_cap]
+    // (round parity), per-CTA D2 sums [2][unit][pp_nblk]
+    double *pp_draw, *pp_part;
+    int *pp_idx;
+    float *pp_d2;
+    int pp_nblk;
     // decode workspace
     float *partials;  // [units][PART_SLOTS][G][PART_W]
     int *sel;         // [units][G][tc + tc*ts] selection of the last step
@@ -92,8 +101,8 @@ struct TraceDev {
 // Host-side plan: sizes and byte offsets of every array in the arena.
 struct Plan {
     int batch, h_kv, h_q, G, d, n_cap, units, c_max, l_max, tc, ts, T1, T2;
-    int score_mode, residual, union_exact, group_select, sliding, bf16s, fp8s, R, P, nchunks, n_mid_max,
-        nseg_max;
+    int score_mode, residual, union_exact, group_select, sliding, bf16s, fp8s, kpp, R, P, nchunks,
+        n_mid_max, nseg_max, pp_nblk;
     int64_t sub_off_stride;
     int64_t o_unit_info, o_n_now, o_perm, o_sub_off, o_cl_n, o_cl_ms, o_cl_vbar, o_sub_n, o_sub_ms,
         o_sub_vbar, o_cl_vhl, o_sub_vhl, o_cl_ms16, o_sub_ms16, o_cl_ms8, o_sub_ms8, o_l1_assign, o_status,
@@ -101,6 +110,7 @@ struct Plan {
     int64_t o_cent, o_permA, o_changed, o_fb_list, o_fb_cnt, o_hist, o_offs, o_ctot, o_coff,
         o_sub_assign, o_rc_list, o_rc_cnt, o_cimg, o_cnorm, cimg_ustride, cn_ustride;
     int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask, o_resx, resx_stride;
+    int64_t o_pp_draw, o_pp_idx, o_pp_d2, o_pp_part;
     int64_t total;
 };
 

@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "exact.cuh"
@@ -505,13 +506,234 @@ __global__ void __launch_bounds__(256) k_l1_update(Dev dv, int t) {
     }
 }
 
+// ------------------------------------------------------------------------------------
+// k-means++ seeding of the first level (a variant).  Two launches per seed r:
+//  k_pp_pick (one CTA per unit) draws seed r from the squared distances D2 left by round
+//    r - 1;
+//  k_pp_update (CTAs over the mid keys) lowers each key's D2 to its distance to seed r and
+//    writes each CTA's sum of D2.  Every round reads every mid key once.
+// Both are launched as programmatic dependents, each waiting for its predecessor before
+// it reads what that one wrote.  D2 and the CTA sums alternate between two buffers by the
+// parity of r.
+// ------------------------------------------------------------------------------------
+
+// fp32 squared distance of a bf16 key row to c (fp32, shared memory): each difference
+// rounded to fp32, four partial sums (dimension j into sum j mod 4) by fused multiply-add
+// in increasing j, then (s0 + s1) + (s2 + s3).  Four chains instead of one keep the
+// dependent adds from limiting the kernel.
+__device__ __forceinline__ float pp_dist(const uint16_t *x, const float *c) {
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+    uint4 rv[16];  // the row's loads issued together: each 32-byte sector by consecutive loads
+#pragma unroll
+    for (int q = 0; q < 16; ++q) rv[q] = xv[q];
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const uint4 v = rv[q];
+        const float *cq = c + 8 * q;
+        float d;
+        d = __fsub_rn(bf_lo(v.x), cq[0]); s0 = __fmaf_rn(d, d, s0);
+        d = __fsub_rn(bf_hi(v.x), cq[1]); s1 = __fmaf_rn(d, d, s1);
+        d = __fsub_rn(bf_lo(v.y), cq[2]); s2 = __fmaf_rn(d, d, s2);
+        d = __fsub_rn(bf_hi(v.y), cq[3]); s3 = __fmaf_rn(d, d, s3);
+        d = __fsub_rn(bf_lo(v.z), cq[4]); s0 = __fmaf_rn(d, d, s0);
+        d = __fsub_rn(bf_hi(v.z), cq[5]); s1 = __fmaf_rn(d, d, s1);
+        d = __fsub_rn(bf_lo(v.w), cq[6]); s2 = __fmaf_rn(d, d, s2);
+        d = __fsub_rn(bf_hi(v.w), cq[7]); s3 = __fmaf_rn(d, d, s3);
+    }
+    return __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
+}
+
+// Prefix over the CTA of one double per thread, in one fixed order (shuffles within the
+// warps, then the warps' sums in index order): the thread's exclusive prefix and the total.
+struct PPScan {
+    double excl, total;
+};
+__device__ __forceinline__ PPScan pp_scan(double v, double *s_w) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    double inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    double ex = __shfl_up_sync(0xffffffffu, inc, 1);
+    if (lane == 0) ex = 0.0;
+    if (lane == 31) s_w[warp] = inc;
+    __syncthreads();
+    double base = 0.0, tot = 0.0;
+    for (int w = 0; w < PP_THREADS / 32; ++w) {
+        if (w == warp) base = tot;
+        tot += s_w[w];
+    }
+    __syncthreads();  // s_w is reused by the next scan
+    return {base + ex, tot};
+}
+
+__global__ void __launch_bounds__(PP_THREADS) k_pp_pick(Dev dv, int r) {
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int C = ui[UI_C], n = ui[UI_NMID];
+    if (r >= C || n == 0) return;
+    pdl_wait();  // D2 and the CTA sums of round r - 1 are written
+    pdl_trigger();
+    const int nb = (n + PP_ROWS - 1) / PP_ROWS;
+    __shared__ double s_w[PP_THREADS / 32];
+    __shared__ int s_blk, s_pick, s_lastpos;
+    __shared__ double s_pre;
+    if (tid == 0) {
+        s_blk = s_pick = INT_MAX;
+        s_lastpos = -1;
+    }
+    const int64_t U = dv.units, cm = dv.c_max;
+    double ur = dv.pp_draw[u * cm + r];
+    if (!(ur >= 0.0 && ur < 1.0)) {  // outside [0, 1) (or NaN): clamp and report
+        if (tid == 0) flag_error(dv.status, ST_BAD_INDEX);
+        ur = ur >= 1.0 ? 0x1.fffffffffffffp-1 : 0.0;
+    }
+    const int pr = (r + 1) & 1;
+    const float *d2p = dv.pp_d2 + ((int64_t)pr * U + u) * dv.n_cap;
+    const double *partp = dv.pp_part + ((int64_t)pr * U + u) * dv.pp_nblk;
+
+    int j = min((int)floor(ur * (double)n), n - 1);  // seed 0, or every key on a seed
+    if (r > 0) {
+        // the CTA sums of round r - 1: the first CTA whose running sum exceeds ur * total
+        const int per = (nb + PP_THREADS - 1) / PP_THREADS;
+        const int e0 = min(nb, tid * per), e1 = min(nb, e0 + per);
+        double loc = 0.0;
+        for (int e = e0; e < e1; ++e) loc += partp[e];
+        const PPScan sc = pp_scan(loc, s_w);
+        if (sc.total > 0.0) {
+            const double target = ur * sc.total;
+            double run = sc.excl;
+            for (int e = e0; e < e1; ++e) {
+                const double nx = run + partp[e];
+                if (nx > target) {
+                    atomicMin(&s_blk, e);
+                    break;
+                }
+                run = nx;
+            }
+            __syncthreads();
+            int B = s_blk;
+            if (B != INT_MAX) {
+                if (B >= e0 && B < e1) {  // its owner: the running sum before it
+                    double pre = sc.excl;
+                    for (int e = e0; e < B; ++e) pre += partp[e];
+                    s_pre = pre;
+                }
+            } else {  // ur * total rounded up to the total: the last CTA with a positive sum
+                for (int e = e1 - 1; e >= e0; --e)
+                    if (partp[e] > 0.0) {
+                        atomicMax(&s_lastpos, e);
+                        break;
+                    }
+            }
+            __syncthreads();
+            const bool found = B != INT_MAX;
+            if (!found) B = max(s_lastpos, 0);
+            __syncthreads();
+            if (tid == 0) s_lastpos = -1;
+            // inside CTA B, keys in position order, PP_PER consecutive keys a thread (the
+            // order in which k_pp_update summed them)
+            const int i0 = B * PP_ROWS + tid * PP_PER;
+            double l2 = 0.0;
+            for (int k = 0; k < PP_PER; ++k)
+                if (i0 + k < n) l2 += (double)d2p[i0 + k];
+            const PPScan s2 = pp_scan(l2, s_w);  // (its barrier also orders s_lastpos)
+            if (found) {
+                double rr = s_pre + s2.excl;
+                for (int k = 0; k < PP_PER && i0 + k < n; ++k) {
+                    const double nx = rr + (double)d2p[i0 + k];
+                    if (nx > target) {
+                        atomicMin(&s_pick, i0 + k);
+                        break;
+                    }
+                    rr = nx;
+                }
+            }
+            __syncthreads();
+            if (s_pick == INT_MAX) {  // no crossing (rounding): the last key with D2 > 0
+                for (int k = PP_PER - 1; k >= 0; --k)
+                    if (i0 + k < n && d2p[i0 + k] > 0.f) {
+                        atomicMax(&s_lastpos, i0 + k);
+                        break;
+                    }
+                __syncthreads();
+                j = s_lastpos >= 0 ? s_lastpos : B * PP_ROWS;
+            } else {
+                j = s_pick;
+            }
+        }
+    }
+    if (tid == 0) dv.pp_idx[u * cm + r] = j;
+}
+
+// One CTA per PP_ROWS mid keys, PP_PER a thread (consecutive keys across the threads, so
+// that a warp's loads cover 32 adjacent rows).  Each thread reads its own rows from global
+// memory: measured faster here than staging tiles in shared memory by cp.async (the
+// per-SM limit on outstanding copies) or by one bulk copy per row.
+__global__ void __launch_bounds__(PP_THREADS) k_pp_update(Dev dv, int r) {
+    const int u = blockIdx.y, blk = blockIdx.x, tid = threadIdx.x;
+    const int *ui = dv.unit_info + u * UI_STRIDE;
+    const int C = ui[UI_C], n = ui[UI_NMID];
+    const int nb = (n + PP_ROWS - 1) / PP_ROWS;
+    if (r >= C - 1 || n == 0 || blk >= nb) return;
+    __shared__ double s_w[PP_THREADS / 32];
+    __shared__ float s_c[MOG_D];
+    __shared__ float s_d2[PP_ROWS];
+    const int64_t U = dv.units, cm = dv.c_max;
+    const int pr = (r + 1) & 1, cr = r & 1;
+    const int b = ui[UI_B], h = u % dv.h_kv, S = ui[UI_S];
+    pdl_wait();  // seed r is picked, D2 of round r - 1 is written
+    pdl_trigger();
+    const float *d2p = dv.pp_d2 + ((int64_t)pr * U + u) * dv.n_cap;
+    float *d2c = dv.pp_d2 + ((int64_t)cr * U + u) * dv.n_cap;
+    const int j = dv.pp_idx[u * cm + r];
+    if (tid < MOG_D) s_c[tid] = bf1(dv.krow(b, h, S + j)[tid]);
+    __syncthreads();
+    const int base = blk * PP_ROWS;
+#pragma unroll 1
+    for (int k = 0; k < PP_PER; ++k) {
+        const int i = base + k * PP_THREADS + tid;
+        float v = 0.f;
+        if (i < n) {
+            const float dd = pp_dist(dv.krow(b, h, S + i), s_c);
+            v = r == 0 ? dd : fminf(d2p[i], dd);
+            d2c[i] = v;
+        }
+        s_d2[k * PP_THREADS + tid] = v;
+    }
+    __syncthreads();
+    double loc = 0.0;  // summed in the order in which k_pp_pick scans this CTA's keys
+    for (int q = 0; q < PP_PER; ++q) loc += (double)s_d2[tid * PP_PER + q];
+    const PPScan sc = pp_scan(loc, s_w);
+    if (tid == 0) dv.pp_part[((int64_t)cr * U + u) * dv.pp_nblk + blk] = sc.total;
+}
+
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl_km(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __global__ void k_l1_init(Dev dv) {
     const int u = blockIdx.y, c = blockIdx.x;
     const int *ui = dv.unit_info + u * UI_STRIDE;
     const int C = ui[UI_C], n = ui[UI_NMID];
     if (c >= C || n == 0) return;
     const int b = ui[UI_B], h = u % dv.h_kv;
-    const int64_t pos = ui[UI_S] + (int64_t)c * n / C;
+    // strided seeds, or the k-means++ seeds
+    const int64_t pos = ui[UI_S] + (dv.kpp ? (int64_t)dv.pp_idx[(int64_t)u * dv.c_max + c] : (int64_t)c * n / C);
     const uint16_t *row = dv.krow(b, h, pos);
     for (int j = threadIdx.x; j < MOG_D; j += blockDim.x)
         dv.cent[((int64_t)u * dv.c_max + c) * MOG_D + j] = bf1(row[j]);
@@ -1542,6 +1764,14 @@ cudaError_t launch_build(const Dev &dv, const Plan &pl, cudaStream_t s, const Tr
     if ((e = set_smem((const void *)k_sort_scatter, pl.c_max * sizeof(int))) != cudaSuccess) return e;
     const int U = pl.units;
     if (pl.n_mid_max > 0) {
+        if (dv.kpp) {
+            for (int r = 0; r < pl.c_max && e == cudaSuccess; ++r) {
+                e = launch_pdl_km(k_pp_pick, dim3(U), dim3(PP_THREADS), 0, s, dv, r);
+                if (e == cudaSuccess && r + 1 < pl.c_max)
+                    e = launch_pdl_km(k_pp_update, dim3(pl.pp_nblk, U), dim3(PP_THREADS), 0, s, dv, r);
+            }
+            if (e != cudaSuccess) return e;
+        }
         k_l1_init<<<dim3(pl.c_max, U), 128, 0, s>>>(dv);
         CUtensorMap kmap;
         // TMA tiles need contiguous rows: a paged cache takes the direct fp32 pass

@@ -94,6 +94,13 @@ def clusters_for(w: Workload, n: int) -> tuple[int, int]:
     return max(c, 1), max(l, 1)
 
 
+def seed_draws(units: int, c_max: int, seed: int) -> np.ndarray:
+    """Uniform draws in [0, 1), float64 [units, c_max]: the random input of k-means++
+    seeding (one draw per unit and seed)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(1 << 21,))))
+    return rng.random((units, c_max))
+
+
 def to_bf16(x: np.ndarray) -> np.ndarray:
     """float64 -> float32 (RNE) -> bf16 (RNE) bit patterns as uint16."""
     b = np.ascontiguousarray(x, np.float32).view(np.uint32)

@@ -54,7 +54,7 @@ def test_arena_size_query_and_validation(lib):
         mog.arena_bytes(mog.make_params(1, 1, 1, 100, n_sub=33), [100])  # L > 32
     with pytest.raises(mog.MogError, match="INVALID_ARG"):
         mog.arena_bytes(mog.make_params(1, 1, 1, 100, top_c=-1), [100])
-    # flags: the union-exact, sliding, group-select, bf16- and fp8-summary bits are the only ones defined
+    # flags: the union-exact, sliding, group-select, bf16- and fp8-summary and k-means++ bits are the only ones defined
     u = mog.make_params(1, 8, 32, 32768, n_clusters=181, n_sub=15, top_c=8, top_s=8, union_exact=1)
     assert u.flags == mog.FLAG_UNION_EXACT and mog.arena_bytes(u, [32768]) == n
     assert mog.make_params(1, 1, 1, 100, sliding=1).flags == mog.FLAG_SLIDING
@@ -67,7 +67,7 @@ def test_arena_size_query_and_validation(lib):
     both = mog.make_params(1, 1, 1, 100, bf16_summaries=1, fp8_summaries=1)  # one rounding at most
     with pytest.raises(mog.MogError, match="INVALID_ARG"):
         mog.arena_bytes(both, [100])
-    u.flags = 32
+    u.flags = 64
     with pytest.raises(mog.MogError, match="INVALID_ARG"):
         mog.arena_bytes(u, [32768])
     # automatic C and L follow round(sqrt N) and ceil(log2 N)
@@ -84,6 +84,17 @@ def test_null_arguments_are_rejected_before_any_gpu_work(lib):
     assert rc == 1
     assert lib.mog_decode(None, None, None, None) == 1
     assert lib.mog_append(None, None, None, None) == 1
+    # k-means++ seeding needs its draws: mog_build and mog_build_traced refuse the flag,
+    # mog_build_seeded refuses it missing or the draws missing
+    pk = mog.make_params(1, 1, 1, 128, kmeanspp=1)
+    assert pk.flags == mog.FLAG_KMEANSPP
+    lp = lens.ctypes.data_as(C.c_void_p)
+    assert lib.mog_build(None, None, lp, C.byref(pk), None, 0, None, C.byref(out)) == 1
+    assert lib.mog_build_traced(None, None, lp, C.byref(pk), None, 0, C.c_void_p(256), 1 << 20, None,
+                                C.byref(out)) == 1
+    assert lib.mog_build_seeded(None, None, lp, C.byref(pk), None, None, 0, None, 0, None, C.byref(out)) == 1
+    assert lib.mog_build_seeded(None, None, lp, C.byref(p), C.c_void_p(256), None, 0, None, 0, None,
+                                C.byref(out)) == 1
     sz = C.c_size_t()
     assert lib.dense_decode_scratch_bytes(1, 2, 3, 128, 100, C.byref(sz)) == 2
     assert lib.dense_decode_scratch_bytes(1, 2, 8, 128, 100, C.byref(sz)) == 0 and sz.value > 0

@@ -4,7 +4,9 @@ of each head are split into clusters and each cluster into subclusters after pre
 
 mog_build_traced records the centroids every step assigned to and the assignment it made,
 at both levels.  For every step the tests check, on the GPU's own trajectory:
-  (i)   the seeds are the member rows at floor(j n / k), bit for bit;
+  (i)   the seeds are the member rows at floor(j n / k), bit for bit (with k-means++ seeding
+        of the first level: the rows the oracle's k-means++ draws pick with the same
+        uniforms, every round or sampled rounds);
   (ii)  the GPU's assignment equals the oracle's assignment to the GPU's centroids of that
         step, bit for bit (all rows, or a seeded sample of rows at 128K and 1M keys);
   (iii) the GPU's next centroids are the oracle's mean of the GPU's members within 1e-5
@@ -42,8 +44,9 @@ def bf(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(DEV)
 
 
-def traced_head(name, b=0, h=0):
-    """One KV head of a workload, built by mog_build_traced."""
+def traced_head(name, b=0, h=0, kpp=False):
+    """One KV head of a workload, built by mog_build_traced (with kpp: k-means++ seeds from
+    the input generator's draws, returned as the last item)."""
     w = wl.WORKLOADS[name]
     n = int(wl.lengths(w)[b])
     u = wl.UnitDraw(w, b, h, n)
@@ -52,11 +55,12 @@ def traced_head(name, b=0, h=0):
     u.keys_values(K[0, 0], V[0, 0])
     Cn, L = wl.clusters_for(w, n)
     prm = mog.make_params(1, 1, w.group, n, n_clusters=Cn, n_sub=L, top_c=w.top_c, top_s=w.top_s,
-                          n_sink=w.n_sink, n_recent=w.n_recent)
-    hd, tr = mog.build(bf(K), bf(V), [n], prm, trace=True)
+                          n_sink=w.n_sink, n_recent=w.n_recent, kmeanspp=int(kpp))
+    draws = wl.seed_draws(1, Cn, w.seed + 100) if kpp else None
+    hd, tr = mog.build(bf(K), bf(V), [n], prm, trace=True, draws=draws)
     torch.cuda.synchronize()
     assert hd.sync_status() == 0
-    return w, K[0, 0], n, Cn, L, hd, tr
+    return w, K[0, 0], n, Cn, L, hd, tr, draws
 
 
 def _updates_close(gpu_next, ref, prev, counts):
@@ -83,8 +87,10 @@ def _expected_steps(labels, T):
     return T
 
 
-def lockstep(name, l1_sample=None, l2_clusters=None, seed=0):
-    w, K, n, Cn, L, hd, tr = traced_head(name)
+def lockstep(name, l1_sample=None, l2_clusters=None, seed=0, kpp=False, pp_rounds=None):
+    """pp_rounds (with kpp): the k-means++ rounds checked one by one against the oracle's
+    step given the GPU's earlier seeds; None checks the whole seed sequence at once."""
+    w, K, n, Cn, L, hd, tr, draws = traced_head(name, kpp=kpp)
     S, R = w.n_sink, w.n_recent
     nm = n - S - R
     T1, T2 = tr.layout.iters_l1, tr.layout.iters_l2
@@ -98,7 +104,18 @@ def lockstep(name, l1_sample=None, l2_clusters=None, seed=0):
     rows = (np.arange(nm) if l1_sample is None or l1_sample >= nm
             else np.sort(rng.choice(nm, size=l1_sample, replace=False)))
     # ------------------------------------------------------------ first level
-    assert np.array_equal(l1c[0], X[(np.arange(Cn) * nm) // Cn])                      # (i)
+    if kpp:
+        pp = hd.array("pp_idx", torch.int32, (1, lay.c_max)).cpu().numpy()[0, :Cn].astype(np.int64)
+        if pp_rounds is None:
+            assert np.array_equal(pp, ora.kmeanspp(Kmid, Cn, draws[0])), "k-means++ seeds"
+        else:
+            for r in pp_rounds:
+                assert ora.pp_pick(Kmid, pp[:r], draws[0, r]) == pp[r], ("k-means++ round", r)
+        nd = len(set(pp.tolist()))   # distinct, unless every key already sits on a seed
+        assert nd == Cn or nd == len(np.unique(Kmid, axis=0)), nd
+        assert np.array_equal(l1c[0], X[pp])                                             # (i)
+    else:
+        assert np.array_equal(l1c[0], X[(np.arange(Cn) * nm) // Cn])                  # (i)
     worst1 = 0.0
     for t in range(steps1):
         cent = l1c[t].astype(np.float64)
@@ -178,3 +195,29 @@ def test_lockstep_1m_head_1024_clusters():
     sampled rows per step, every first-level update in full, every cluster's second level
     in full."""
     print("1M lockstep", lockstep("ctx-1m", l1_sample=16384, seed=4))
+
+
+# ------------------------------------------------------------- k-means++ seeding (variant)
+
+def test_kmeanspp_lockstep_tiny():
+    """k-means++ seeds equal the oracle's for the same draws, then the whole lockstep."""
+    r = lockstep("tiny-4k", kpp=True)
+    print("tiny k-means++ lockstep", r)
+
+
+def test_kmeanspp_lockstep_qwen3_4b_full_head():
+    """A full 32K-key head: all 181 seeds against the oracle, every row at every step."""
+    print("32K k-means++ lockstep", lockstep("qwen3-4b-32k", kpp=True))
+
+
+def test_kmeanspp_lockstep_qwen3_14b_head():
+    """A 131072-key head: all 362 seeds against the oracle; the Lloyd steps on 16384 sampled
+    rows, every cluster's second level in full."""
+    print("128K k-means++ lockstep", lockstep("qwen3-14b-128k", l1_sample=16384, seed=5, kpp=True))
+
+
+def test_kmeanspp_lockstep_1m_head_sampled_rounds():
+    """A 1M-key head: rounds 0-3, 17, 64 and 255 of the seeding, each against the oracle's
+    step from the GPU's earlier seeds; the Lloyd steps on 16384 sampled rows."""
+    print("1M k-means++ lockstep", lockstep("ctx-1m", l1_sample=16384, seed=6, kpp=True,
+                                            pp_rounds=[0, 1, 2, 3, 17, 64, 255]))

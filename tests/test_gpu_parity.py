@@ -1045,10 +1045,58 @@ def test_fp8_summaries_follow_the_sliding_window():
     print("fp8 + sliding decode", _check_decode(inj, n_now=[n0 + steps] * w.batch))
 
 
+# ------------------------------------------------------------ k-means++ seeding (variant)
+
+def test_kmeanspp_ragged_batch_paged_and_bad_draws():
+    """k-means++ seeding over a ragged batch (units of different lengths and numbers of
+    clusters): every unit's seeds equal the oracle's with that unit's draws; a paged copy
+    of the cache gives the same seeds and partition bit for bit; a draw outside [0, 1) is
+    reported by the status word."""
+    w = small_workload(0, batch=2, h_kv=2, h_q=8, centres=48, n_clusters=0, n_sub=0, top_c=3,
+                       top_s=2, n_recent=40, n_range=(2500, 3100), seed=22)
+    K, V, q, lens = wl.make_batch(w)
+    n_cap = K.shape[2]
+    prm = mog.make_params(2, 2, 8, n_cap, top_c=3, top_s=2, n_sink=4, n_recent=40, kmeanspp=1)
+    tl = mog.trace_layout(prm, lens)
+    draws = wl.seed_draws(tl.units, tl.c_max, 23)
+    h = mog.build(bf(K), bf(V), lens, prm, draws=draws)
+    torch.cuda.synchronize()
+    assert h.sync_status() == 0
+    lay = h.layout()
+    U = lay.units
+    pp = h.array("pp_idx", torch.int32, (U, lay.c_max)).cpu().numpy()
+    info = h.array("unit_info", torch.int32, (U, 8)).cpu().numpy()
+    assert len(set(info[:, 0].tolist())) == 2          # two numbers of clusters
+    for u in range(U):
+        b, hh = divmod(u, 2)
+        Cn, nm, S = int(info[u, 0]), int(info[u, 3]), int(info[u, 4])
+        ref = ora.kmeanspp(K[b, hh, S:S + nm], Cn, draws[u])
+        assert np.array_equal(pp[u, :Cn], ref), u
+    pk, _ = _paged_copy(K, V, 64, True, seed=24)
+    hp = mog.build(pk, None, lens, prm, draws=draws)
+    torch.cuda.synchronize()
+    assert hp.sync_status() == 0
+    ppp = hp.array("pp_idx", torch.int32, (U, lay.c_max)).cpu().numpy()
+    assert np.array_equal(pp, ppp)                      # (entries past a unit's C stay -1)
+    assert all(np.all(pp[u, info[u, 0]:] == -1) for u in range(U))
+    for u in range(U):
+        nm, used = int(info[u, 3]), int(info[u, 0] * info[u, 1] + 1)
+        for name, width in (("perm", nm), ("sub_off", used)):
+            stride = lay.n_cap if name == "perm" else lay.sub_off_stride
+            a, c = (x.array(name, torch.int32, (U, stride))[u, :width] for x in (h, hp))
+            assert torch.equal(a, c), (name, u)
+    bad = draws.copy()
+    bad[1, 3] = 1.5
+    hb = mog.build(bf(K), bf(V), lens, prm, draws=bad)
+    assert hb.sync_status() == 5                        # MOG_ERR_DEVICE_CHECK
+    with pytest.raises(ValueError):
+        mog.build(bf(K), bf(V), lens, prm)               # the draws are required
+
+
 # -------------------------------------------------------------- periodic re-clustering
 
-@pytest.mark.parametrize("sliding", [0, 1])
-def test_recluster_equals_fresh_build_and_matches_oracle(sliding):
+@pytest.mark.parametrize("sliding,kpp", [(0, 0), (1, 0), (0, 1)])
+def test_recluster_equals_fresh_build_and_matches_oracle(sliding, kpp):
     """mog_recluster after 40 appended tokens: the partition, the summaries and the window
     equal a fresh mog_build over the grown sequences (with the build's C and L), bit for
     bit -- also when the sliding window had moved keys into the clusters.  The statistics
@@ -1058,9 +1106,10 @@ def test_recluster_equals_fresh_build_and_matches_oracle(sliding):
     K, V, q, lens = wl.make_batch(w, n_cap=n0 + steps)
     rng = np.random.default_rng(37)
     prm = mog.make_params(2, 2, 8, n0 + steps, n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=5,
-                          top_s=3, n_sink=4, n_recent=32, sliding=sliding)
+                          top_s=3, n_sink=4, n_recent=32, sliding=sliding, kmeanspp=kpp)
     Kd, Vd = bf(K), bf(V)
-    h = mog.build(Kd, Vd, lens, prm)
+    draws = wl.seed_draws(4, w.n_clusters, 38) if kpp else None   # k-means++: reused by recluster
+    h = mog.build(Kd, Vd, lens, prm, draws=draws)
     for t in range(steps):
         kn = wl.to_bf16(rng.standard_normal((2, 2, D)))
         vn = wl.to_bf16(rng.standard_normal((2, 2, D)))
@@ -1069,7 +1118,7 @@ def test_recluster_equals_fresh_build_and_matches_oracle(sliding):
     h.recluster()
     fresh = mog.build(Kd, Vd, lens + steps, mog.make_params(
         2, 2, 8, n0 + steps, n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=5, top_s=3, n_sink=4,
-        n_recent=32, sliding=sliding))
+        n_recent=32, sliding=sliding, kmeanspp=kpp), draws=draws)
     torch.cuda.synchronize()
     assert h.sync_status() == 0 and fresh.sync_status() == 0
     lay = h.layout()
