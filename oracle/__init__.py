@@ -48,7 +48,8 @@ def lib():
         build()
         l = C.CDLL(_LIB)
         for name in ("ora_assign", "ora_update", "ora_lloyd", "ora_stats", "ora_build",
-                     "ora_select", "ora_decode", "ora_dense", "ora_pp_pick", "ora_kmeanspp"):
+                     "ora_select", "ora_decode", "ora_dense", "ora_pp_pick", "ora_kmeanspp",
+                     "ora_decode_fm", "ora_fm_sums"):
             getattr(l, name).restype = C.c_int
         _lib = l
     return _lib
@@ -239,6 +240,44 @@ def decode(K: np.ndarray, V: np.ndarray, n_now: int, q: np.ndarray, summ: dict,
                             _i64(ts), C.c_int(1 if residual else 0), _ptr(out), _ptr(diag)),
            "decode")
     return out, diag
+
+
+def decode_fm(K: np.ndarray, V: np.ndarray, n_now: int, q: np.ndarray, summ: dict,
+              sel_c: np.ndarray, sel_s: np.ndarray, omega: np.ndarray):
+    """Decode of one query head with the feature-map residual (R29): exact attention over
+    the anchors and the selected subclusters' members, the random-feature estimate with
+    the rows of `omega` [m, d] for every other mid key.  Returns (out[d], diag[4])."""
+    K, V, q = _u16(K), _u16(V), _u16(q)
+    d = K.shape[1]
+    om = np.ascontiguousarray(omega, np.float64)
+    tc = int(np.asarray(sel_c).shape[0])
+    ts = int(np.asarray(sel_s).reshape(tc, -1).shape[1]) if tc else 0
+    sc = np.ascontiguousarray(sel_c, np.int32).reshape(-1)
+    ss = np.ascontiguousarray(sel_s, np.int32).reshape(-1)
+    out = np.zeros(d)
+    diag = np.zeros(4)
+    _check(lib().ora_decode_fm(_ptr(K), _ptr(V), _i64(d), _i64(d), _i64(n_now), _i64(summ["n_build"]),
+                               _i64(summ["S"]), _i64(summ["R"]), _ptr(q), _dbl(tau_of(d)),
+                               _i64(summ["C"]), _i64(summ["L"]), _ptr(summ["perm"]),
+                               _ptr(summ["sub_off"]), _ptr(sc if sc.size else np.zeros(1, np.int32)),
+                               _ptr(ss if ss.size else np.zeros(1, np.int32)), _i64(tc), _i64(ts),
+                               _ptr(om), _i64(om.shape[0]), _ptr(out), _ptr(diag)), "decode_fm")
+    return out, diag
+
+
+def fm_sums(K: np.ndarray, V: np.ndarray, summ: dict, omega: np.ndarray) -> np.ndarray:
+    """Unscaled feature sums of every subcluster (R29): [C*L, m, d+1], the value-weighted
+    sums in [..., :d] and the plain sums in [..., d]."""
+    K, V = _u16(K), _u16(V)
+    d = K.shape[1]
+    om = np.ascontiguousarray(omega, np.float64)
+    m = om.shape[0]
+    Cn, L = summ["C"], summ["L"]
+    z = np.zeros((Cn * L, m, d + 1))
+    _check(lib().ora_fm_sums(_ptr(K), _ptr(V), _i64(d), _i64(d), _ptr(summ["perm"]),
+                             _ptr(summ["sub_off"]), _i64(Cn), _i64(L), _dbl(tau_of(d)), _ptr(om),
+                             _i64(m), _ptr(z)), "fm_sums")
+    return z
 
 
 def dense(K: np.ndarray, V: np.ndarray, n: int, q: np.ndarray) -> np.ndarray:

@@ -53,6 +53,14 @@
  *      multiply-add in increasing j, and D2 = (s_0 + s_1) + (s_2 + s_3), each sum
  *      rounded to fp32.  The running sums over the members are fp64.  With sum D2 = 0
  *      (every member on a seed) the pick is floor(u_r n) again.
+ *  R29 the feature-map residual (a second estimator, [RC]: a fixed-size feature-map
+ *      summary of the mid region, built at prefill, estimates the numerator and
+ *      denominator of the keys not retrieved): positive random features of the softmax
+ *      kernel, phi_i(x) = m^(-1/2) exp(w_i.x - |x|^2/2) for i < m with w_i drawn N(0, I_d)
+ *      (an input), so that E[phi(x).phi(y)] = exp(x.y).  With q~ = sqrt(tau) q and
+ *      k~ = sqrt(tau) k, every mid key k that is not attended exactly adds
+ *      phi(q~).phi(k~) [v_k, 1] to the numerator and denominator; the exact part is the
+ *      same as ora_decode's; one normalisation.
  *  Ranking order everywhere: score descending, then index ascending.
  *
  * Inputs are bf16 bit patterns (uint16) read as exact fp64 values.  Build with
@@ -715,6 +723,167 @@ int ora_decode(const uint16_t *K, const uint16_t *V, int64_t ld, int64_t d, int6
         diag[2] = (double)ne;
     }
     free(q); free(csel); free(ssel); free(epos); free(elog); free(rgrp); free(rexp);
+    return ORA_OK;
+}
+
+/* ---------------------------------------------------------------------------------
+ * The feature-map residual (R29, [RC])
+ * ------------------------------------------------------------------------------- */
+
+/* log(phi(q~).phi(k~)): log of (1/m) sum_i exp(w_i.q~ - |q~|^2/2 + w_i.k~ - |k~|^2/2),
+ * summed with the largest term factored out. */
+static double log_feature_kernel(const double *qt, const double *kt, const double *omega,
+                                 int64_t m, int64_t d, double *tmp)
+{
+    double qq = 0.0, kk = 0.0;
+    for (int64_t j = 0; j < d; ++j) {
+        qq = qq + qt[j] * qt[j];
+        kk = kk + kt[j] * kt[j];
+    }
+    double mx = -INFINITY;
+    for (int64_t i = 0; i < m; ++i) {
+        double a = 0.0, b = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+            a = a + omega[i * d + j] * qt[j];
+            b = b + omega[i * d + j] * kt[j];
+        }
+        tmp[i] = a - 0.5 * qq + b - 0.5 * kk;
+        if (tmp[i] > mx)
+            mx = tmp[i];
+    }
+    double acc = 0.0;
+    for (int64_t i = 0; i < m; ++i)
+        acc = acc + exp(tmp[i] - mx);
+    return mx + log(acc) - log((double)m);
+}
+
+/*
+ * Decode of one query head with the feature-map residual (R29): the exact part over the
+ * anchors and the members of the selected subclusters (sel_c, sel_s as ora_decode), and
+ * the estimate phi(q~).phi(k~) for every other mid key; omega [m][d].
+ *   out[d]; diag (or NULL): [max log-weight, denominator, exact rows, estimated keys]
+ */
+int ora_decode_fm(const uint16_t *K, const uint16_t *V, int64_t ld, int64_t d, int64_t n_now,
+                  int64_t n_build, int64_t S, int64_t R, const uint16_t *q_bf16, double tau,
+                  int64_t C, int64_t L, const int32_t *perm, const int32_t *sub_off,
+                  const int32_t *sel_c, const int32_t *sel_s, int64_t tc, int64_t ts,
+                  const double *omega, int64_t m, double *out, double *diag)
+{
+    if (d <= 0 || n_now < n_build || L <= 0 || C < 0 || m <= 0)
+        return ORA_EINVAL;
+    int64_t mid_lo = S, mid_hi = n_build - R > S ? n_build - R : S;
+    double *q = malloc((size_t)d * sizeof(double));
+    double *qt = malloc((size_t)d * sizeof(double));
+    double *kt = malloc((size_t)d * sizeof(double));
+    double *tmp = malloc((size_t)m * sizeof(double));
+    char *exact = calloc((size_t)(n_now > 0 ? n_now : 1), 1);
+    double *lw = malloc((size_t)(n_now > 0 ? n_now : 1) * sizeof(double)); /* log-weights */
+    if (!q || !qt || !kt || !tmp || !exact || !lw) {
+        free(q); free(qt); free(kt); free(tmp); free(exact); free(lw);
+        return ORA_ENOMEM;
+    }
+    bf_vec(q_bf16, d, q);
+    double st = sqrt(tau);
+    for (int64_t j = 0; j < d; ++j)
+        qt[j] = st * q[j];
+    /* R1: anchors; then the members of the selected subclusters */
+    for (int64_t p = 0; p < (S < n_now ? S : n_now); ++p)
+        exact[p] = 1;
+    for (int64_t p = mid_hi; p < n_now; ++p)
+        exact[p] = 1;
+    for (int64_t i = 0; i < tc; ++i) {
+        if (sel_c[i] < 0)
+            continue;
+        for (int64_t r = 0; r < ts; ++r) {
+            if (sel_s[i * ts + r] < 0)
+                continue;
+            int64_t g = sel_c[i] * L + sel_s[i * ts + r];
+            for (int64_t t = sub_off[g]; t < sub_off[g + 1]; ++t)
+                exact[perm[t]] = 1;
+        }
+    }
+    int64_t ne = 0, nf = 0;
+    double mx = -INFINITY;
+    for (int64_t p = 0; p < n_now; ++p) {
+        const uint16_t *kr = K + p * ld;
+        if (exact[p]) {
+            double dot = 0.0;
+            for (int64_t j = 0; j < d; ++j)
+                dot = dot + q[j] * bf(kr[j]);
+            lw[p] = tau * dot;
+            ++ne;
+        } else if (p >= mid_lo && p < mid_hi) {
+            for (int64_t j = 0; j < d; ++j)
+                kt[j] = st * bf(kr[j]);
+            lw[p] = log_feature_kernel(qt, kt, omega, m, d, tmp);
+            ++nf;
+        } else {
+            lw[p] = -INFINITY; /* beyond the build's mid region and not an anchor: none */
+        }
+        if (lw[p] > mx)
+            mx = lw[p];
+    }
+    double den = 0.0;
+    for (int64_t j = 0; j < d; ++j)
+        out[j] = 0.0;
+    for (int64_t p = 0; p < n_now; ++p) {
+        if (lw[p] == -INFINITY)
+            continue;
+        double w = exp(lw[p] - mx);
+        const uint16_t *vr = V + p * ld;
+        den = den + w;
+        for (int64_t j = 0; j < d; ++j)
+            out[j] = out[j] + w * bf(vr[j]);
+    }
+    for (int64_t j = 0; j < d; ++j)
+        out[j] = den > 0.0 ? out[j] / den : 0.0;
+    if (diag) {
+        diag[0] = mx;
+        diag[1] = den;
+        diag[2] = (double)ne;
+        diag[3] = (double)nf;
+    }
+    free(q); free(qt); free(kt); free(tmp); free(exact); free(lw);
+    return ORA_OK;
+}
+
+/*
+ * The feature sums of every subcluster (R29), unscaled: for subcluster g and feature i,
+ * z[(g*m + i)*(d+1) + j] = sum over its members k of exp(w_i.k~ - |k~|^2/2) v_kj for j < d,
+ * and the same sum of exp(...) alone at j = d.
+ */
+int ora_fm_sums(const uint16_t *K, const uint16_t *V, int64_t ld, int64_t d, const int32_t *perm,
+                const int32_t *sub_off, int64_t C, int64_t L, double tau, const double *omega,
+                int64_t m, double *z)
+{
+    if (d <= 0 || C < 0 || L <= 0 || m <= 0)
+        return ORA_EINVAL;
+    double *kt = malloc((size_t)d * sizeof(double));
+    if (!kt)
+        return ORA_ENOMEM;
+    double st = sqrt(tau);
+    memset(z, 0, (size_t)(C * L * m * (d + 1)) * sizeof(double));
+    for (int64_t g = 0; g < C * L; ++g) {
+        for (int64_t t = sub_off[g]; t < sub_off[g + 1]; ++t) {
+            const uint16_t *kr = K + (int64_t)perm[t] * ld, *vr = V + (int64_t)perm[t] * ld;
+            double kk = 0.0;
+            for (int64_t j = 0; j < d; ++j) {
+                kt[j] = st * bf(kr[j]);
+                kk = kk + kt[j] * kt[j];
+            }
+            for (int64_t i = 0; i < m; ++i) {
+                double a = 0.0;
+                for (int64_t j = 0; j < d; ++j)
+                    a = a + omega[i * d + j] * kt[j];
+                double f = exp(a - 0.5 * kk);
+                double *zr = z + (g * m + i) * (d + 1);
+                for (int64_t j = 0; j < d; ++j)
+                    zr[j] = zr[j] + f * bf(vr[j]);
+                zr[d] = zr[d] + f;
+            }
+        }
+    }
+    free(kt);
     return ORA_OK;
 }
 

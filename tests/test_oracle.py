@@ -320,6 +320,105 @@ def test_build_with_kmeanspp_seeds_is_lloyd_from_them(ora):
     assert not np.array_equal(ora.build_unit(K, V, w.n, S, R, Cn, L)["l1_assign"], b["l1_assign"])
 
 
+# -------------------------------------------------------- feature-map residual (R29)
+
+def _fm_case(n=300, scale=1.0, seed=9):
+    rng = np.random.default_rng(seed)
+    K = wl.to_bf16(rng.standard_normal((n, D)) * scale)
+    V = wl.to_bf16(rng.standard_normal((n, D)))
+    q = wl.to_bf16(rng.standard_normal(D) * scale)
+    return K, V, q
+
+
+def _np_feature_weights(K, q, omega):
+    """phi(q~).phi(k~) for every row of K, written with numpy matrix products (fp64)."""
+    st = math.sqrt(TAU)
+    qt, kt = st * f64(q), st * f64(K)
+    a = omega @ qt - 0.5 * qt @ qt                      # [m]
+    b = kt @ omega.T - 0.5 * np.sum(kt * kt, axis=1)[:, None]   # [n, m]
+    return np.exp(a[None, :] + b).mean(axis=1)
+
+
+def test_fm_identity_random_features_estimate_the_softmax_kernel():
+    """E over w ~ N(0, I) of exp(w.x - |x|^2/2) exp(w.y - |y|^2/2) = exp(x.y): the sample
+    mean over 400,000 draws lies within 5 standard errors (the identity R29 rests on)."""
+    rng = np.random.default_rng(1)
+    x, y = rng.standard_normal(D) * 0.06, rng.standard_normal(D) * 0.06
+    w = rng.standard_normal((400000, D))
+    f = np.exp(w @ x - 0.5 * x @ x + w @ y - 0.5 * y @ y)
+    assert abs(f.mean() - math.exp(x @ y)) <= 5 * f.std() / math.sqrt(f.size)
+
+
+def test_fm_decode_matches_brute_force_and_special_cases(ora):
+    K, V, q = _fm_case()
+    S, R, Cn, L = 4, 16, 4, 3
+    n = K.shape[0]
+    b = ora.build_unit(K, V, n, S, R, Cn, L)
+    omega = np.random.default_rng(2).standard_normal((64, D))
+    # nothing selected: anchors exact, every mid key estimated
+    sc = np.full(2, -1, np.int32)
+    ss = np.full((2, 2), -1, np.int32)
+    out, diag = ora.decode_fm(K, V, n, q, b, sc, ss, omega)
+    w_exact = np.exp(TAU * (f64(K) @ f64(q)))
+    anchors = np.r_[0:S, n - R:n]
+    mid = np.arange(S, n - R)
+    w = np.zeros(n)
+    w[anchors] = w_exact[anchors]
+    w[mid] = _np_feature_weights(K[mid], q, omega)
+    ref = w @ f64(V) / w.sum()
+    assert rel_l2(out, ref) < 1e-12 and diag[2] == S + R and diag[3] == n - S - R
+    # two subclusters selected: their members move to the exact part
+    sc = np.array([1, 3], np.int32)
+    ss = np.array([[0, 2], [1, -1]], np.int32)
+    out, diag = ora.decode_fm(K, V, n, q, b, sc, ss, omega)
+    off, perm = b["sub_off"], b["perm"]
+    chosen = np.concatenate([perm[off[c * L + l]:off[c * L + l + 1]] for c, l in ((1, 0), (1, 2), (3, 1))])
+    w2 = w.copy()
+    w2[chosen] = w_exact[chosen]
+    assert rel_l2(out, w2 @ f64(V) / w2.sum()) < 1e-12 and diag[2] == S + R + chosen.size
+    # everything selected: the dense softmax, no key estimated
+    sc = np.arange(Cn, dtype=np.int32)
+    ss = np.tile(np.arange(L, dtype=np.int32), (Cn, 1))
+    out, diag = ora.decode_fm(K, V, n, q, b, sc, ss, omega)
+    assert rel_l2(out, dense_ref(K, V, n, q)) < 1e-12 and diag[3] == 0
+
+
+def test_fm_decode_converges_to_dense_with_more_features(ora):
+    """Nothing selected, small keys (the estimator's variance is then small) and values
+    with mean 1: the output approaches the dense softmax as the number of features grows,
+    the error falling about as 1 / sqrt(m)."""
+    rng = np.random.default_rng(10)
+    n = 300
+    K = wl.to_bf16(rng.standard_normal((n, D)) * 0.3)
+    V = wl.to_bf16(rng.standard_normal((n, D)) + 1.0)
+    q = wl.to_bf16(rng.standard_normal(D) * 0.3)
+    b = ora.build_unit(K, V, n, 4, 16, 4, 3)
+    sc = np.full(1, -1, np.int32)
+    ss = np.full((1, 1), -1, np.int32)
+    ref = dense_ref(K, V, n, q)
+    rng = np.random.default_rng(3)
+    errs = [rel_l2(ora.decode_fm(K, V, n, q, b, sc, ss, rng.standard_normal((m, D)))[0], ref)
+            for m in (64, 1024, 16384)]
+    assert errs[2] < 0.003 and errs[2] < errs[1] / 2 < errs[0] / 4, errs
+
+
+def test_fm_sums_are_the_per_subcluster_feature_sums(ora):
+    K, V, q = _fm_case(seed=11)
+    S, R, Cn, L = 4, 16, 4, 3
+    n = K.shape[0]
+    b = ora.build_unit(K, V, n, S, R, Cn, L)
+    omega = np.random.default_rng(4).standard_normal((16, D))
+    z = ora.fm_sums(K, V, b, omega)
+    st = math.sqrt(TAU)
+    off, perm = b["sub_off"], b["perm"]
+    for g in range(Cn * L):
+        rows = perm[off[g]:off[g + 1]]
+        kt = st * f64(K[rows])
+        e = np.exp(kt @ omega.T - 0.5 * np.sum(kt * kt, axis=1)[:, None])   # [rows, m]
+        assert np.allclose(z[g, :, D], e.sum(axis=0), rtol=1e-12, atol=0)
+        assert np.allclose(z[g, :, :D], e.T @ f64(V[rows]), rtol=1e-10, atol=1e-300)
+
+
 # ----------------------------------------------------------------------------- estimator
 
 def _single_group(ora, K, V):
