@@ -72,6 +72,8 @@ def args_():
                          "order behind a block table")
     ap.add_argument("--bf16-summaries", action="store_true",
                     help="selection scores and residual terms from the summaries rounded to bf16")
+    ap.add_argument("--fm-residual", action="store_true",
+                    help="the feature-map residual (random features) instead of the Gaussian one")
     ap.add_argument("--kmeanspp", action="store_true",
                     help="first-level k-means++ seeds (draws from the input generator)")
     ap.add_argument("--fp8-summaries", action="store_true",
@@ -245,13 +247,16 @@ def summary_bytes(a):
     return 1 if a.fp8_summaries else 2 if a.bf16_summaries else 4
 
 
-def bytes_from_selection(h, w, sel, lens, n_now, sb=4):
+def bytes_from_selection(h, w, sel, lens, n_now, sb=4, resid=1):
     """Algorithmic bytes of one decode step, per kernel: all cluster summaries and the
     subcluster summaries of each unit's union of selected clusters (selection); the K/V
     rows (+ index) of the union of selected subclusters, the anchors and the residual terms
     (rows); the partials and the output (merge).  sb: bytes per element of the summaries'
     means and variances (4 fp32, 2 bf16, 1 fp8); the residual terms' value means take 4
-    (bf16 high and low parts) with fp32 summaries, else 2 (the high part)."""
+    (bf16 high and low parts) with fp32 summaries, else 2 (the high part).  resid: 1 the
+    Gaussian residual's terms (rows kernel), 0 none, 2 the feature-map residual (its own
+    kernel: per head the unit's total and the chosen subclusters' feature sums, 32 x 132
+    floats each, and FM_NCH + 1 vectors out, which the merge reads)."""
     import torch
     lay = h.layout()
     U, cm, lm, G = lay.units, lay.c_max, lay.l_max, lay.group
@@ -259,7 +264,9 @@ def bytes_from_selection(h, w, sel, lens, n_now, sb=4):
     off = h.array("sub_off", torch.int32, (U, lay.sub_off_stride)).cpu().numpy()
     tc, ts = w.top_c, w.top_s
     sel = sel.reshape(U, G, -1)
-    tot = dict(select=0, attend=0, merge=0, rows=0)
+    tot = dict(select=0, attend=0, merge=0, rows=0, fm=0)
+    fm_row = 32 * 132 * 4   # one feature sum (all features), bytes
+    fm_vec = 33 * 132 * 4   # the vectors one head's CTAs write
     for u in range(U):
         Cn, L, nb, S, rlo, b = info[u, 0], info[u, 1], info[u, 2], info[u, 4], info[u, 5], info[u, 6]
         ucl, usub = set(), set()
@@ -286,11 +293,19 @@ def bytes_from_selection(h, w, sel, lens, n_now, sb=4):
         # rows kernel: query, segments, perm index and K, V rows (bf16) of the chosen rows and
         # the anchors, the residual terms (bf16 high/low value means and exponents), partials
         tot["attend"] += G * D * 2 + len(usub) * 12 + Uk * 4 + (Uk + anchors) * 4 * D
-        tot["attend"] += items * (vb * D + gp * 4) + P * G * (D + 4) * 4
+        if resid == 1:
+            tot["attend"] += items * (vb * D + gp * 4)
+        tot["attend"] += P * G * (D + 4) * 4
+        if resid == 2:
+            for g in range(G):
+                nsel = sum(1 for i in range(tc) if sel[u, g, i] >= 0
+                           for r in range(ts) if sel[u, g, tc + i * ts + r] >= 0)
+                tot["fm"] += D * 2 + 4 * (tc + tc * ts) + (1 + nsel) * fm_row + fm_vec
+                tot["merge"] += fm_vec + 4
         # merge kernel: partials in, the output (fp32) out
         tot["merge"] += P * G * (D + 4) * 4 + G * D * 4
         tot["rows"] += Uk + anchors
-    tot["step"] = tot["select"] + tot["attend"] + tot["merge"]
+    tot["step"] = tot["select"] + tot["attend"] + tot["merge"] + tot["fm"]
     return tot
 
 
@@ -340,7 +355,10 @@ def run_gpu(a, w, rank, world):
                           top_c=w.top_c, top_s=w.top_s, n_sink=w.n_sink, n_recent=w.n_recent,
                           union_exact=int(a.union_exact), sliding=int(a.sliding),
                           group_select=int(a.group_select), bf16_summaries=int(a.bf16_summaries),
-                          fp8_summaries=int(a.fp8_summaries), kmeanspp=int(a.kmeanspp))
+                          fp8_summaries=int(a.fp8_summaries), kmeanspp=int(a.kmeanspp),
+                          residual=2 if a.fm_residual else 1)
+    omega = (torch.from_numpy(wl.fm_omega(mog.FM_FEATURES, D, w.seed + 200)).to(torch.float32).to(dev)
+             if a.fm_residual else None)
     draws = None
     if a.kmeanspp:
         tl = mog.trace_layout(prm, lens)
@@ -364,6 +382,13 @@ def run_gpu(a, w, rank, world):
     b1.record()
     torch.cuda.synchronize()
     build_ms = b0.elapsed_time(b1)
+    fm_ms = None
+    if a.fm_residual:   # the feature-map summary, also at prefill time
+        b0.record()
+        h.feature_map(omega)
+        b1.record()
+        torch.cuda.synchronize()
+        fm_ms = b0.elapsed_time(b1)
     assert h.sync_status() == 0
     lay = h.layout()
     steps1 = h.array("l1_steps", torch.int32, (lay.units,)).cpu().numpy()
@@ -377,7 +402,7 @@ def run_gpu(a, w, rank, world):
     h.decode(qd, out, sel_out=sel)
     torch.cuda.synchronize()
     n_now = [int(x) for x in lens]
-    by = bytes_from_selection(h, w, sel.cpu().numpy(), lens, n_now, summary_bytes(a))
+    by = bytes_from_selection(h, w, sel.cpu().numpy(), lens, n_now, summary_bytes(a), prm.residual)
 
     clocks = Clocks(local)
     # ---- settle clocks, then dense_decode (the full scan) for comparison ----
@@ -421,14 +446,17 @@ def run_gpu(a, w, rank, world):
                       bf16_summaries=int(a.bf16_summaries),
                       fp8_summaries=int(a.fp8_summaries))
             kw.update(over)
+            kw.setdefault("residual", 2 if a.fm_residual else 1)
             pv = mog.make_params(w.batch, w.h_kv, w.h_q, n_cap, **kw)
             hv = mog.build(Kd, Vd, lens, pv, partition=(perm_t, off_t))
+            if pv.residual == 2:
+                hv.feature_map(omega)
             sv = torch.empty_like(sel)
             ov = hv.decode(qd, sel_out=sv)
             torch.cuda.synchronize()
             assert hv.sync_status() == 0
             ev_ = ((ov.reshape(-1, D).double() - dn).norm(dim=1) / dn.norm(dim=1).clamp_min(1e-30)).cpu().numpy()
-            byv = bytes_from_selection(hv, w, sv.cpu().numpy(), lens, n_now, summary_bytes(a))
+            byv = bytes_from_selection(hv, w, sv.cpu().numpy(), lens, n_now, summary_bytes(a), pv.residual)
             tv = []
             for i in range(3 + 20):
                 cold_l2()
@@ -482,9 +510,12 @@ def run_gpu(a, w, rank, world):
                              top_s=min(w.top_s, sL), n_sink=4, n_recent=64,
                              union_exact=int(a.union_exact), group_select=int(a.group_select),
                              bf16_summaries=int(a.bf16_summaries),
-                             fp8_summaries=int(a.fp8_summaries))
+                             fp8_summaries=int(a.fp8_summaries), residual=prm.residual)
         sKd, sVd, sqd = bf(sK), bf(sV), bf(sq)
-        side = (mog.build(sKd, sVd, sl, sp), sqd, torch.empty(sqd.shape, dtype=torch.float32, device=dev))
+        sh = mog.build(sKd, sVd, sl, sp)
+        if sp.residual == 2:
+            sh.feature_map(omega)
+        side = (sh, sqd, torch.empty(sqd.shape, dtype=torch.float32, device=dev))
     except Exception:
         side = None
     phase = [[], [], []]
@@ -562,6 +593,7 @@ def run_gpu(a, w, rank, world):
                            + (", bf16 summaries" if a.bf16_summaries else "")
                            + (", fp8 summaries" if a.fp8_summaries else "")
                            + (", k-means++ seeds" if a.kmeanspp else "")
+                           + (", feature-map residual" if a.fm_residual else "")
                            + (f", paged cache ({a.paged}-row pages)" if a.paged else ""),
                    "recent_window": "sliding" if a.sliding else "growing",
                    "l2": "cold before every timed step (256 MB write, then 256 MB read)",
@@ -595,7 +627,8 @@ def run_gpu(a, w, rank, world):
                   "TFLOPs": round((l1_flop + l2_flop) / (build_ms * 1e-3) / 1e12, 3),
                   # k-means++ reads every mid key once per seed (2 bytes x d each)
                   "kmeanspp_key_bytes": (sum(float(info[u, 3]) * 2 * D * float(info[u, 0]) for u in range(lay.units))
-                                         if a.kmeanspp else None)},
+                                         if a.kmeanspp else None),
+                  "feature_map_ms": round(fm_ms, 2) if fm_ms is not None else None},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",
                 "h2d_bytes_per_step": int(q_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 4)},
         "append": append,

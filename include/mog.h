@@ -64,7 +64,8 @@ typedef enum {
  *                      early once a step changes no assignment.
  *  score_mode        : 0 = log-mass score ln n + tau q.mu + tau^2/2 sum q^2 sigma2 (the
  *                      residual's own exponent); 1 = tau q.mu only.
- *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation.
+ *  residual          : 1 = add the Gaussian residual (default), 0 = top-only ablation,
+ *                      2 = the feature-map residual (MOG_RESIDUAL_FEATURE_MAP) instead.
  *  flags             : 0, or any of MOG_FLAG_UNION_EXACT, MOG_FLAG_SLIDING,
  *                      MOG_FLAG_GROUP_SELECT, MOG_FLAG_KMEANSPP (mog_build_seeded only),
  *                      and one of MOG_FLAG_BF16_SUMMARIES, MOG_FLAG_FP8_SUMMARIES.
@@ -77,6 +78,20 @@ typedef enum {
  * clusters no head chose.  The bytes read are those of the default mode.
  */
 #define MOG_FLAG_UNION_EXACT 1
+/*
+ * MOG_RESIDUAL_FEATURE_MAP (mog_params.residual = 2; the retrieval-completion page on
+ * newx.sg, Abstract and AI Summary: a fixed-size feature-map summary of the mid region,
+ * built at prefill, estimates the numerator and denominator of the keys that are not
+ * retrieved, added to the exact part unnormalised before one normalisation): instead of
+ * the groups' Gaussians, every mid key that a head does not attend exactly contributes
+ * phi(q~).phi(k~) [v, 1], phi_i(x) = m^(-1/2) exp(w_i.x - |x|^2/2) for the
+ * m = MOG_FM_FEATURES caller-given frequencies w_i (drawn N(0, I_d); mog_feature_map),
+ * q~ = sqrt(tau) q, k~ = sqrt(tau) k.  The build keeps every subcluster's feature sums;
+ * a decode subtracts the head's chosen subclusters' sums from the unit's total.  Not
+ * with MOG_FLAG_UNION_EXACT or MOG_FLAG_SLIDING (MOG_ERR_INVALID_ARG).
+ */
+#define MOG_RESIDUAL_FEATURE_MAP 2
+#define MOG_FM_FEATURES 32
 /*
  * MOG_FLAG_SLIDING (a variant of this library; the pages keep a recent window but do not
  * say what happens to a key leaving it): the recent anchors stay the last n_recent keys.
@@ -193,6 +208,11 @@ typedef struct mog_layout {
     int64_t cl_ms8;     /* e4m3  [units][c_max][2][d] (MOG_FLAG_FP8_SUMMARIES; else 0) */
     int64_t sub_ms8;    /* e4m3  [units][c_max*l_max][2][d] (MOG_FLAG_FP8_SUMMARIES; else 0) */
     int64_t pp_idx;     /* int32 [units][c_max]: seed r's mid-key index, -1 past C_u (MOG_FLAG_KMEANSPP; else 0) */
+    /* MOG_RESIDUAL_FEATURE_MAP (else 0): f32 [units][c_max*l_max][MOG_FM_FEATURES][d+4]
+     * feature sums of every subcluster, row i holding sum over members of
+     * exp(w_i.k~ - |k~|^2/2 - M_i) v_k in [0, d) and the same sum without v at d, scaled
+     * by M_i = |w_i|^2/2 - 40; and f32 [units][MOG_FM_FEATURES][d+4] their sum per unit */
+    int64_t fm_z, fm_t;
 } mog_layout;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -258,6 +278,17 @@ int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev, const int32_
  * be run concurrently with a decode on the same handle.
  */
 int mog_append(mog_handle *h, const void *k_new_dev, const void *v_new_dev, void *stream);
+
+/*
+ * The feature-map summary (MOG_RESIDUAL_FEATURE_MAP; the retrieval-completion page's
+ * prefill-time summary): copies the frequencies omega_dev (f32 [MOG_FM_FEATURES][d],
+ * device, 4-byte aligned; rows drawn N(0, I_d) by the caller) into the arena and computes
+ * every subcluster's feature sums and the units' totals for the handle's partition.
+ * Required once after the build before a decode with residual = 2 (MOG_ERR_INVALID_ARG
+ * otherwise, also when the handle was built with another residual); mog_recluster redoes
+ * the sums for the new partition.  Enqueued on `stream`.
+ */
+int mog_feature_map(mog_handle *h, const float *omega_dev, void *stream);
 
 /*
  * Periodic re-clustering during long generation ([IA]'s post-prefill partition, redone

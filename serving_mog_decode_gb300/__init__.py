@@ -24,6 +24,8 @@ FLAG_GROUP_SELECT = 4  # MOG_FLAG_GROUP_SELECT in mog.h
 FLAG_BF16_SUMMARIES = 8  # MOG_FLAG_BF16_SUMMARIES in mog.h
 FLAG_FP8_SUMMARIES = 16  # MOG_FLAG_FP8_SUMMARIES in mog.h
 FLAG_KMEANSPP = 32       # MOG_FLAG_KMEANSPP in mog.h
+RESIDUAL_FEATURE_MAP = 2  # MOG_RESIDUAL_FEATURE_MAP in mog.h
+FM_FEATURES = 32          # MOG_FM_FEATURES in mog.h
 STATUS = ["MOG_OK", "MOG_ERR_INVALID_ARG", "MOG_ERR_SHAPE", "MOG_ERR_ARENA_TOO_SMALL",
           "MOG_ERR_CUDA", "MOG_ERR_DEVICE_CHECK", "MOG_ERR_TIMEOUT", "MOG_ERR_NOT_IMPLEMENTED",
           "MOG_ERR_CAPACITY"]
@@ -82,7 +84,7 @@ class Layout(C.Structure):
                                            "sub_off_stride", "cl_n", "cl_ms", "cl_vbar", "sub_n",
                                            "sub_ms", "sub_vbar", "l1_assign", "status",
                                            "l1_steps", "fallback", "cl_ms16", "sub_ms16", "cl_ms8",
-                                           "sub_ms8", "pp_idx")])
+                                           "sub_ms8", "pp_idx", "fm_z", "fm_t")])
 
 
 class TraceLayout(C.Structure):
@@ -108,6 +110,7 @@ _SIGS = {
     "mog_decode_phased": (C.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "mog_append": (C.c_int, [_P, _P, _P, _P]),
     "mog_recluster": (C.c_int, [_P, _P]),
+    "mog_feature_map": (C.c_int, [_P, _P, _P]),
     "mog_get_layout": (C.c_int, [_P, _P]),
     "mog_sync_status": (C.c_int, [_P, _P]),
     "mog_decode_splits": (C.c_int, [_P, _P]),
@@ -265,6 +268,16 @@ class Handle:
     def recluster(self, stream=None):
         """Rebuild the partition and summaries over the grown sequences (mog_recluster)."""
         _check(lib().mog_recluster(self._h, _stream(stream)), "mog_recluster")
+
+    def feature_map(self, omega, stream=None):
+        """The feature-map summary for residual = 2 (mog_feature_map): omega, float32
+        [FM_FEATURES, 128] frequencies drawn N(0, I), on the cache's device."""
+        torch = _torch()
+        om = torch.as_tensor(omega, dtype=torch.float32, device=self.arena.device).contiguous()
+        if tuple(om.shape) != (FM_FEATURES, 128):
+            raise ValueError(f"omega must be [{FM_FEATURES}, 128]")
+        self._omega = om   # kept alive until the copy has run
+        _check(lib().mog_feature_map(self._h, _ptr(om), _stream(stream)), "mog_feature_map")
 
     def splits(self) -> int:
         v = C.c_int32(0)

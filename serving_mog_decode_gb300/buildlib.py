@@ -11,7 +11,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmog.so")
-SOURCES = ["api.cu", "kmeans.cu", "decode.cu", "dense.cu", "slide.cu"]
+SOURCES = ["api.cu", "kmeans.cu", "decode.cu", "dense.cu", "slide.cu", "fmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -25,6 +25,7 @@ struct mog_handle {
     std::vector<int32_t> lengths;
     std::vector<int32_t> info;  // host copy of unit_info
     int appended;
+    bool fm_ready;  // mog_feature_map has run (the feature-map residual can decode)
 };
 
 static thread_local char g_err[256] = "";
@@ -95,7 +96,11 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if ((p->flags & ~known_flags) != 0 || p->batch <= 0 || p->h_kv <= 0 || p->h_q <= 0 || p->n_cap <= 0 ||
         p->top_c < 0 || p->top_s < 0 || p->n_sink < 0 || p->n_recent < 0 || p->iters_l1 < 0 ||
         p->iters_l2 < 0 || p->n_clusters < 0 || p->n_sub < 0 ||
-        (p->score_mode != 0 && p->score_mode != 1) || (p->residual != 0 && p->residual != 1))
+        (p->score_mode != 0 && p->score_mode != 1) || p->residual < 0 || p->residual > 2)
+        return MOG_ERR_INVALID_ARG;
+    // the feature-map residual subtracts each head's own chosen subclusters from fixed sums:
+    // neither the union's rows nor keys moved by the sliding window are in those sums
+    if (p->residual == MOG_RESIDUAL_FEATURE_MAP && (p->flags & (MOG_FLAG_UNION_EXACT | MOG_FLAG_SLIDING)))
         return MOG_ERR_INVALID_ARG;
     if (p->d != MOG_D || p->h_q % p->h_kv != 0 || p->h_q / p->h_kv > MOG_MAX_G)
         return MOG_ERR_SHAPE;
@@ -204,6 +209,14 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     P.o_pp_idx = P.kpp ? take(4 * U * cm) : 0;
     P.o_pp_d2 = P.kpp ? take(4 * 2 * U * nc) : 0;
     P.o_pp_part = P.kpp ? take(8 * 2 * U * (int64_t)P.pp_nblk) : 0;
+    const bool fm = P.residual == MOG_RESIDUAL_FEATURE_MAP;
+    P.o_fm_omega = fm ? take(4 * FM_M * MOG_D) : 0;
+    P.o_fm_mi = fm ? take(4 * FM_M) : 0;
+    P.o_fm_z = fm ? take(4 * U * cm * lm * FM_M * FM_W) : 0;
+    P.o_fm_zc = fm ? take(4 * U * cm * FM_M * FM_W) : 0;
+    P.o_fm_t = fm ? take(4 * U * FM_M * FM_W) : 0;
+    P.o_fm_vec = fm ? take(4 * U * G * (FM_NCH + 1) * FM_W) : 0;
+    P.o_fm_mref = fm ? take(4 * U * G) : 0;
     P.total = o;
     return MOG_OK;
 }
@@ -296,6 +309,15 @@ Dev make_dev(const Plan &P, void *arena, const mog_kv *kv) {
     if (P.fp8s) {
         PTR(cl_ms8, uint8_t);
         PTR(sub_ms8, uint8_t);
+    }
+    if (P.residual == MOG_RESIDUAL_FEATURE_MAP) {
+        PTR(fm_omega, float);
+        PTR(fm_mi, float);
+        PTR(fm_z, float);
+        PTR(fm_zc, float);
+        PTR(fm_t, float);
+        PTR(fm_vec, float);
+        PTR(fm_mref, float);
     }
     if (P.kpp) {
         PTR(pp_draw, double);
@@ -449,6 +471,7 @@ static int common_build(const mog_kv *kv, const int32_t *lengths_dev,
     h->dev = make_dev(pl, arena, kv);
     h->lengths.assign(lengths_host, lengths_host + p->batch);
     h->appended = 0;
+    h->fm_ready = false;
     h->info.assign((size_t)pl.units * UI_STRIDE, 0);
     for (int u = 0; u < pl.units; ++u) {
         const int b = u / p->h_kv;
@@ -601,6 +624,7 @@ extern "C" int mog_build_from_partition(const mog_kv *kv, const int32_t *lengths
 extern "C" int mog_decode_ex(mog_handle *h, const void *q_dev, float *out_dev,
                              const int32_t *sel_in_dev, int32_t *sel_out_dev, void *stream) {
     if (!h || !q_dev || !out_dev) return MOG_ERR_INVALID_ARG;
+    if (h->plan.residual == MOG_RESIDUAL_FEATURE_MAP && !h->fm_ready) return MOG_ERR_INVALID_ARG;
     if (!aligned16(q_dev) || !aligned16(out_dev)) return MOG_ERR_INVALID_ARG;
     cudaError_t e = launch_decode(h->dev, h->plan, q_dev, out_dev, sel_in_dev, sel_out_dev,
                                   static_cast<cudaStream_t>(stream));
@@ -612,6 +636,7 @@ extern "C" int mog_decode_phased(mog_handle *h, const void *q_dev, float *out_de
                                  const int32_t *sel_in_dev, int32_t *sel_out_dev,
                                  void *const *events, void *stream) {
     if (!h || !q_dev || !out_dev || !events) return MOG_ERR_INVALID_ARG;
+    if (h->plan.residual == MOG_RESIDUAL_FEATURE_MAP && !h->fm_ready) return MOG_ERR_INVALID_ARG;
     for (int i = 0; i < 4; ++i)
         if (!events[i]) return MOG_ERR_INVALID_ARG;
     if (!aligned16(q_dev) || !aligned16(out_dev)) return MOG_ERR_INVALID_ARG;
@@ -658,7 +683,20 @@ extern "C" int mog_recluster(mog_handle *h, void *stream) {
     h->plan.n_mid_max = nmid;
     cudaError_t e = reset_build_state(h, s);
     if (e == cudaSuccess) e = launch_build(h->dev, h->plan, s);
+    if (e == cudaSuccess && h->fm_ready) e = launch_fm_build(h->dev, h->plan, s);  // the new partition's sums
     if (e != cudaSuccess) return cuda_fail(e, "mog_recluster");
+    return MOG_OK;
+}
+
+extern "C" int mog_feature_map(mog_handle *h, const float *omega_dev, void *stream) {
+    if (!h || !omega_dev || ((uintptr_t)omega_dev & 3)) return MOG_ERR_INVALID_ARG;
+    if (h->plan.residual != MOG_RESIDUAL_FEATURE_MAP) return MOG_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(h->dev.fm_omega, omega_dev, 4 * (size_t)FM_M * MOG_D,
+                                    cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = launch_fm_build(h->dev, h->plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mog_feature_map");
+    h->fm_ready = true;
     return MOG_OK;
 }
 
@@ -694,6 +732,8 @@ extern "C" int mog_get_layout(const mog_handle *h, mog_layout *o) {
     o->cl_ms8 = P.o_cl_ms8;
     o->sub_ms8 = P.o_sub_ms8;
     o->pp_idx = P.o_pp_idx;
+    o->fm_z = P.o_fm_z;
+    o->fm_t = P.o_fm_t;
     return MOG_OK;
 }
 

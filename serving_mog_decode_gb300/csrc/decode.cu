@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
     const size_t usg = (size_t)u * dv.c_max * dv.l_max;   // subcluster index base
     const uint16_t *qg = a.q + (size_t)u * G * MOG_D;
     int *selu = dv.sel + (size_t)u * G * a.SW;
-    const bool resid = dv.residual != 0;
+    const bool resid = dv.residual == 1;  // the Gaussian residual's terms (not the feature map's)
     const bool uex = dv.union_exact != 0;  // every head attends the union's subclusters
     const bool grp = dv.group_select != 0;  // one selection per KV head, by log-sum-exp
     const int GS = grp ? 1 : G;             // selection lists
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     // rows (bf16 high and low parts of its value mean) with its exponents from the
     // selection kernel.
     const int Uc = s_plan[5], L = s_plan[6], C = s_plan[7];
-    const int npi = Uc * L, I = dv.residual ? npi + C : 0;
+    const int npi = Uc * L, I = dv.residual == 1 ? npi + C : 0;
     const int ia = (int)((int64_t)I * p / P), ib = (int)((int64_t)I * (p + 1) / P);
     const int nr = dry ? 1 : (ib - ia + AT_ROWS / 2 - 1) / (AT_ROWS / 2);
     const float *rx = dv.resx + (size_t)u * dv.resx_stride;
@@ -860,7 +860,8 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
 constexpr int MG_THREADS = 4 * MOG_D;
 constexpr int MG_PARTS = MG_THREADS / MOG_D;
 __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials, int P, int G,
-                                                          float *out, int warm) {
+                                                          float *out, int warm, const float *fmv,
+                                                          const float *fmm) {
     const int g = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
     const int j = tid % MOG_D, part = tid / MOG_D;
     __shared__ float s_m[MAX_SPLITS], s_l[MAX_SPLITS];
@@ -885,8 +886,22 @@ __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials,
         s_m[tid] = __ldcg(src(tid));
         s_l[tid] = __ldcg(src(tid) + 1);
     }
+    // the feature-map residual (fmv non-null): one more state, T's vector minus the vectors
+    // of the head's chosen subclusters, at the head's largest feature exponent
+    float fden = 0.f, fnum = 0.f, fm2 = -INFINITY;
+    if (fmv) {
+        const float *fv = fmv + ((size_t)u * G + g) * (FM_NCH + 1) * FM_W;
+        fden = __ldcg(fv + FM_NCH * FM_W + MOG_D);
+        fnum = __ldcg(fv + FM_NCH * FM_W + j);
+#pragma unroll 8
+        for (int c = 0; c < FM_NCH; ++c) {
+            fden -= __ldcg(fv + c * FM_W + MOG_D);
+            fnum -= __ldcg(fv + c * FM_W + j);
+        }
+        if (fden > 0.f) fm2 = __ldcg(fmm + (size_t)u * G + g) * LOG2E;
+    }
     __syncthreads();
-    float mx = -INFINITY;
+    float mx = fm2;
     for (int i = 0; i < P; ++i) mx = fmaxf(mx, s_m[i]);
     float l = 0.f, v = 0.f;
     if (mx != -INFINITY) {
@@ -896,6 +911,10 @@ __global__ void __launch_bounds__(MG_THREADS) k_mog_merge(const float *partials,
         for (int q = 0; q < MAX_SPLITS / MG_PARTS; ++q) {
             const int i = part + q * MG_PARTS;
             if (i < P && s_m[i] != -INFINITY) v += exp2f(s_m[i] - mx) * av[q];
+        }
+        if (fm2 != -INFINITY) {
+            l += exp2f(fm2 - mx) * fden;
+            if (part == 0) v += exp2f(fm2 - mx) * fnum;
         }
     }
     s_acc[part][j] = v;
@@ -1030,6 +1049,8 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
         cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[1], s)) != cudaSuccess) return e;
+    const bool fm = dv.residual == MOG_RESIDUAL_FEATURE_MAP;
+    if (fm && (e = launch_fm_resid(dv, a.q, a.SW, s)) != cudaSuccess) return e;  // (timed with the rows)
     const void *rows_fn = dv.bt ? (const void *)k_mog_rows<GT, true> : (const void *)k_mog_rows<GT, false>;
     if ((e = ensure_smem(rows_fn, AT_SMEM)) != cudaSuccess) return e;
     if (dv.bt)
@@ -1039,7 +1060,9 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_mog_merge, dim3(dv.G, dv.units), dim3(MG_THREADS), 0, s,
-                        (const float *)dv.partials, dv.P, dv.G, a.out, a.warm)) != cudaSuccess)
+                        (const float *)dv.partials, dv.P, dv.G, a.out, a.warm,
+                        (const float *)(fm ? dv.fm_vec : nullptr), (const float *)(fm ? dv.fm_mref : nullptr))) !=
+        cudaSuccess)
         return e;
     if (events && (e = cudaEventRecord(events[3], s)) != cudaSuccess) return e;
     return cudaSuccess;

@@ -29,6 +29,9 @@ constexpr int PLAN_W = PLAN_UCL + MOG_MAX_UNION;  // ints, whole 16-byte chunks
 constexpr int MAX_C = 4096;        // clusters per unit supported
 constexpr int PP_THREADS = 256, PP_PER = 4;  // k-means++ seeding: keys per thread
 constexpr int PP_ROWS = PP_THREADS * PP_PER;  // ... and per CTA
+constexpr int FM_M = MOG_FM_FEATURES;  // feature-map residual: features
+constexpr int FM_W = MOG_D + 4;        // floats per feature row of a sum: d values, the plain sum, padding
+constexpr int FM_NCH = 32;             // decode: CTAs per head over its chosen subclusters
 
 // Typed view of an arena, passed by value to every kernel.
 struct Dev {
@@ -67,6 +70,10 @@ struct Dev {
     int *pp_idx;
     float *pp_d2;
     int pp_nblk;
+    // feature-map residual: frequencies [FM_M][d], M_i [FM_M], sums per subcluster
+    // [unit][c_max*l_max][FM_M][FM_W], per cluster [unit][c_max][FM_M][FM_W], per unit
+    // [unit][FM_M][FM_W]; decode: per-head vectors [unit][G][FM_NCH+1][FM_W], maxima [unit][G]
+    float *fm_omega, *fm_mi, *fm_z, *fm_zc, *fm_t, *fm_vec, *fm_mref;
     // decode workspace
     float *partials;  // [units][PART_SLOTS][G][PART_W]
     int *sel;         // [units][G][tc + tc*ts] selection of the last step
@@ -111,6 +118,7 @@ struct Plan {
         o_sub_assign, o_rc_list, o_rc_cnt, o_cimg, o_cnorm, cimg_ustride, cn_ustride;
     int64_t o_partials, o_sel, o_plan, o_segrow, o_segoff, o_segmask, o_resx, resx_stride;
     int64_t o_pp_draw, o_pp_idx, o_pp_d2, o_pp_part;
+    int64_t o_fm_omega, o_fm_mi, o_fm_z, o_fm_zc, o_fm_t, o_fm_vec, o_fm_mref;
     int64_t total;
 };
 
@@ -131,6 +139,8 @@ cudaError_t launch_decode(const Dev &dv, const Plan &pl, const void *q, float *o
 cudaError_t launch_append(const Dev &dv, const Plan &pl, const void *k_new, const void *v_new,
                           cudaStream_t s);
 cudaError_t launch_slide(const Dev &dv, const Plan &pl, cudaStream_t s);
+cudaError_t launch_fm_build(const Dev &dv, const Plan &pl, cudaStream_t s);
+cudaError_t launch_fm_resid(const Dev &dv, const uint16_t *q, int SW, cudaStream_t s);
 cudaError_t launch_dense(const mog_kv *kv, const int32_t *lengths, int n_max, int batch, int h_kv,
                          int G, const void *q, float *out, float *scratch, int splits,
                          cudaStream_t s);

@@ -101,6 +101,13 @@ def seed_draws(units: int, c_max: int, seed: int) -> np.ndarray:
     return rng.random((units, c_max))
 
 
+def fm_omega(m: int, d: int, seed: int) -> np.ndarray:
+    """Random-feature frequencies, float64 [m, d] drawn N(0, 1): the random input of the
+    feature-map residual."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(1 << 22,))))
+    return rng.standard_normal((m, d))
+
+
 def to_bf16(x: np.ndarray) -> np.ndarray:
     """float64 -> float32 (RNE) -> bf16 (RNE) bit patterns as uint16."""
     b = np.ascontiguousarray(x, np.float32).view(np.uint32)

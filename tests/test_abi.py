@@ -67,6 +67,14 @@ def test_arena_size_query_and_validation(lib):
     both = mog.make_params(1, 1, 1, 100, bf16_summaries=1, fp8_summaries=1)  # one rounding at most
     with pytest.raises(mog.MogError, match="INVALID_ARG"):
         mog.arena_bytes(both, [100])
+    # the feature-map residual: accepted alone, refused with union-exact or sliding
+    assert mog.arena_bytes(mog.make_params(1, 8, 32, 32768, n_clusters=181, n_sub=15, top_c=8, top_s=8,
+                                           residual=2), [32768]) > n
+    for kw in (dict(union_exact=1), dict(sliding=1)):
+        with pytest.raises(mog.MogError, match="INVALID_ARG"):
+            mog.arena_bytes(mog.make_params(1, 1, 1, 100, residual=2, **kw), [100])
+    with pytest.raises(mog.MogError, match="INVALID_ARG"):
+        mog.arena_bytes(mog.make_params(1, 1, 1, 100, residual=3), [100])
     u.flags = 64
     with pytest.raises(mog.MogError, match="INVALID_ARG"):
         mog.arena_bytes(u, [32768])
@@ -83,6 +91,7 @@ def test_null_arguments_are_rejected_before_any_gpu_work(lib):
     rc = lib.mog_build(None, None, lens.ctypes.data_as(C.c_void_p), C.byref(p), None, 0, None, C.byref(out))
     assert rc == 1
     assert lib.mog_decode(None, None, None, None) == 1
+    assert lib.mog_feature_map(None, None, None) == 1
     assert lib.mog_append(None, None, None, None) == 1
     # k-means++ seeding needs its draws: mog_build and mog_build_traced refuse the flag,
     # mog_build_seeded refuses it missing or the draws missing

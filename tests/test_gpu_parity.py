@@ -1093,6 +1093,137 @@ def test_kmeanspp_ragged_batch_paged_and_bad_draws():
         mog.build(bf(K), bf(V), lens, prm)               # the draws are required
 
 
+# ---------------------------------------------------- feature-map residual (variant)
+
+FM_M = mog.FM_FEATURES
+
+
+def _omega(seed):
+    """The frequencies as the GPU holds them (float32), and as float64 for the oracle."""
+    om32 = wl.fm_omega(FM_M, D, seed).astype(np.float32)
+    return om32, om32.astype(np.float64)
+
+
+def _check_fm_sums(inj, om64):
+    """The GPU's per-subcluster feature sums (scaled by exp(-(|w_i|^2/2 - 40))) against the
+    oracle's unscaled sums, feature row by feature row; and the unit totals against the
+    oracle's sums over all subclusters."""
+    lay = inj.h.layout()
+    U, cm, lm = lay.units, lay.c_max, lay.l_max
+    z = inj.h.array("fm_z", torch.float32, (U, cm * lm, FM_M, D + 4)).cpu().numpy().astype(np.float64)
+    t = inj.h.array("fm_t", torch.float32, (U, FM_M, D + 4)).cpu().numpy().astype(np.float64)
+    mi = 0.5 * np.sum(om64 * om64, axis=1) - 40.0
+    scale = np.exp(mi)[None, :, None]
+    worst = 0.0
+    for (b, h), s in inj.summ.items():
+        u = b * inj.w.h_kv + h
+        Cn, L = s["C"], s["L"]
+        ref = ora.fm_sums(inj.K[b, h], inj.V[b, h], s, om64)           # [C*L, m, d+1]
+        gz = z[u, :Cn * L, :, :D + 1] * scale
+        for g in range(Cn * L):
+            if s["sub_n"][g] == 0:
+                assert np.all(gz[g] == 0), g
+                continue
+            e = np.abs(gz[g] - ref[g]).max(axis=1) / np.abs(ref[g]).max(axis=1)
+            worst = max(worst, float(e.max()))
+        tot = ref.sum(axis=0)
+        e = np.abs(t[u, :, :D + 1] * scale[0] - tot).max(axis=1) / np.abs(tot).max(axis=1)
+        worst = max(worst, float(e.max()))
+    assert worst < 2e-4, worst
+    return worst
+
+
+def _check_decode_fm(inj, om64, sample_heads=None):
+    """Outputs under the oracle's selection against the oracle's decode with the
+    feature-map residual."""
+    w, G = inj.w, inj.w.group
+    SW = w.top_c + w.top_c * w.top_s
+    U = w.batch * w.h_kv
+    heads = range(U * G) if sample_heads is None else sample_heads
+    sel_ref, ties = _selection_vs_oracle(inj, heads)
+    out = inj.h.decode(inj.qd, sel_in=torch.from_numpy(sel_ref).to(DEV)).cpu().numpy().reshape(U * G, D)
+    worst = 0.0
+    for hq in heads:
+        u, g = hq // G, hq % G
+        b, h = u // w.h_kv, u % w.h_kv
+        ref, diag = ora.decode_fm(inj.K[b, h], inj.V[b, h], int(inj.lens[b]), inj.q[b, h * G + g], inj.summ[(b, h)],
+                                  sel_ref[hq, :w.top_c], sel_ref[hq, w.top_c:SW].reshape(w.top_c, w.top_s), om64)
+        e = rel(out[hq], ref)
+        worst = max(worst, e)
+        assert e <= OUT_TOL, (hq, e)
+    assert inj.h.sync_status() == 0
+    return ties, worst
+
+
+def test_fm_residual_sums_and_decode_match_oracle():
+    """residual = 2 on the oracle's partition: every subcluster's feature sums and the unit
+    totals against the oracle's, then the decode against the oracle's feature-map decode."""
+    w = small_workload(3000, batch=2, h_kv=2, h_q=8, top_c=5, top_s=3, seed=41)
+    inj = Injected(w, residual=2)
+    om32, om64 = _omega(42)
+    with pytest.raises(mog.MogError, match="INVALID_ARG"):
+        inj.h.decode(inj.qd)                       # the summary is not built yet
+    inj.h.feature_map(om32)
+    print("fm sums worst", _check_fm_sums(inj, om64))
+    print("fm decode (near-ties, worst)", _check_decode_fm(inj, om64))
+
+
+def test_fm_residual_full_size_qwen3_4b():
+    """The 32K workload at full size (position-rule partition): sums and every head."""
+    w = wl.WORKLOADS["qwen3-4b-32k"]
+    inj = Injected(w, mode="rule", residual=2)
+    om32, om64 = _omega(43)
+    inj.h.feature_map(om32)
+    print("fm sums 32K worst", _check_fm_sums(inj, om64))
+    print("fm decode 32K", _check_decode_fm(inj, om64))
+
+
+def test_fm_residual_paged_recluster_and_misuse():
+    """A paged copy gives bit-identical sums and outputs; re-clustering redoes the sums for
+    the new partition (equal to a fresh build's); the summary is refused for another
+    residual mode."""
+    n0, steps = 3000, 8
+    w = small_workload(n0, batch=2, h_kv=2, h_q=8, top_c=5, top_s=3, n_recent=32, seed=44)
+    K, V, q, lens = wl.make_batch(w, n_cap=n0 + steps)
+    prm = mog.make_params(2, 2, 8, n0 + steps, n_clusters=w.n_clusters, n_sub=w.n_sub, top_c=5, top_s=3,
+                          n_sink=4, n_recent=32, residual=2)
+    om32, _ = _omega(45)
+    Kd, Vd, qd = bf(K), bf(V), bf(q)
+    hc = mog.build(Kd, Vd, lens, prm)
+    hc.feature_map(om32)
+    pk, _ = _paged_copy(K, V, 64, False, seed=46)
+    hp = mog.build(pk, None, lens, prm)
+    hp.feature_map(om32)
+    lay = hc.layout()
+    U, cm, lm = lay.units, lay.c_max, lay.l_max
+    zc = hc.array("fm_z", torch.float32, (U, cm * lm, FM_M, D + 4))[..., :D + 1]
+    zp = hp.array("fm_z", torch.float32, (U, cm * lm, FM_M, D + 4))[..., :D + 1]
+    assert torch.equal(zc, zp)
+    assert torch.equal(hc.decode(qd), hp.decode(qd))
+    rng = np.random.default_rng(47)
+    for t in range(steps):
+        kn = wl.to_bf16(rng.standard_normal((2, 2, D)))
+        vn = wl.to_bf16(rng.standard_normal((2, 2, D)))
+        hc.append(bf(kn), bf(vn))
+        K[:, :, n0 + t], V[:, :, n0 + t] = kn, vn
+    hc.recluster()
+    fresh = mog.build(Kd, Vd, lens + steps, prm)
+    fresh.feature_map(om32)
+    torch.cuda.synchronize()
+    zr = hc.array("fm_z", torch.float32, (U, cm * lm, FM_M, D + 4))[..., :D + 1]
+    zf = fresh.array("fm_z", torch.float32, (U, cm * lm, FM_M, D + 4))[..., :D + 1]
+    info = hc.array("unit_info", torch.int32, (U, 8)).cpu().numpy()
+    for u in range(U):
+        used = int(info[u, 0] * info[u, 1])
+        assert torch.equal(zr[u, :used], zf[u, :used]), u
+    assert torch.equal(hc.decode(qd), fresh.decode(qd))
+    g = mog.build(Kd, Vd, lens, mog.make_params(2, 2, 8, n0 + steps, n_clusters=w.n_clusters, n_sub=w.n_sub,
+                                                top_c=5, top_s=3, n_sink=4, n_recent=32))
+    with pytest.raises(mog.MogError, match="INVALID_ARG"):
+        g.feature_map(om32)
+    assert hc.sync_status() == 0 and hp.sync_status() == 0
+
+
 # -------------------------------------------------------------- periodic re-clustering
 
 @pytest.mark.parametrize("sliding,kpp", [(0, 0), (1, 0), (0, 1)])
