@@ -281,10 +281,11 @@ __global__ void __launch_bounds__(FB_THREADS) k_assign_fallback(AssignJob jb) {
         __syncwarp();
         for (int jj = lane; jj < MOG_D; jj += 32) xs[jj] = bf1(xr[jj]);
         __syncwarp();
-        // fp32 distance in index order: difference, fused square-add
+        // fp32 distance: difference, fused square-add into four partial sums (only a
+        // filter: its threshold's margin is far above the rounding of any summation order)
         auto dist32 = [&](int c) {
             const float *cc = cent + (int64_t)c * MOG_D;
-            float acc = 0.f;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
             if (vec) {
                 const float4 *c4 = reinterpret_cast<const float4 *>(cc);
                 const float4 *x4 = reinterpret_cast<const float4 *>(xs);
@@ -292,22 +293,28 @@ __global__ void __launch_bounds__(FB_THREADS) k_assign_fallback(AssignJob jb) {
                 for (int v = 0; v < MOG_D / 4; ++v) {
                     const float4 cv = __ldg(c4 + v), xv = x4[v];
                     float df = __fsub_rn(xv.x, cv.x);
-                    acc = __fmaf_rn(df, df, acc);
+                    a0 = __fmaf_rn(df, df, a0);
                     df = __fsub_rn(xv.y, cv.y);
-                    acc = __fmaf_rn(df, df, acc);
+                    a1 = __fmaf_rn(df, df, a1);
                     df = __fsub_rn(xv.z, cv.z);
-                    acc = __fmaf_rn(df, df, acc);
+                    a2 = __fmaf_rn(df, df, a2);
                     df = __fsub_rn(xv.w, cv.w);
-                    acc = __fmaf_rn(df, df, acc);
+                    a3 = __fmaf_rn(df, df, a3);
                 }
             } else {
 #pragma unroll 8
-                for (int jj = 0; jj < MOG_D; ++jj) {
-                    const float df = __fsub_rn(xs[jj], __ldg(cc + jj));
-                    acc = __fmaf_rn(df, df, acc);
+                for (int jj = 0; jj < MOG_D; jj += 4) {
+                    float df = __fsub_rn(xs[jj], __ldg(cc + jj));
+                    a0 = __fmaf_rn(df, df, a0);
+                    df = __fsub_rn(xs[jj + 1], __ldg(cc + jj + 1));
+                    a1 = __fmaf_rn(df, df, a1);
+                    df = __fsub_rn(xs[jj + 2], __ldg(cc + jj + 2));
+                    a2 = __fmaf_rn(df, df, a2);
+                    df = __fsub_rn(xs[jj + 3], __ldg(cc + jj + 3));
+                    a3 = __fmaf_rn(df, df, a3);
                 }
             }
-            return acc;
+            return (a0 + a1) + (a2 + a3);
         };
         float b32 = INFINITY;
         for (int c = lane; c < k; c += 32) b32 = fminf(b32, dist32(c));
@@ -380,10 +387,19 @@ __global__ void k_sort_colscan(Dev dv, int t) {
     const int nch = (int)ceil_div64(n, SORT_CHUNK);
     const int *h = dv.hist + (int64_t)u * dv.nchunks * dv.c_max + c;
     int *o = dv.offs + (int64_t)u * dv.nchunks * dv.c_max + c;
+    // the chunks' counts are loaded CS_BATCH at a time, so that their latencies overlap
+    constexpr int CS_BATCH = 16;
     int run = 0;
-    for (int k = 0; k < nch; ++k) {
-        o[(int64_t)k * dv.c_max] = run;
-        run += h[(int64_t)k * dv.c_max];
+    for (int k0 = 0; k0 < nch; k0 += CS_BATCH) {
+        int v[CS_BATCH];
+#pragma unroll
+        for (int j = 0; j < CS_BATCH; ++j) v[j] = k0 + j < nch ? h[(int64_t)(k0 + j) * dv.c_max] : 0;
+#pragma unroll
+        for (int j = 0; j < CS_BATCH; ++j)
+            if (k0 + j < nch) {
+                o[(int64_t)(k0 + j) * dv.c_max] = run;
+                run += v[j];
+            }
     }
     dv.ctot[(int64_t)u * dv.c_max + c] = run;
 }
@@ -481,13 +497,21 @@ __global__ void __launch_bounds__(256) k_l1_update(Dev dv, int t) {
     Kahan acc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q].init();
-    for (int m = m0; m < m1; ++m) {
-        const uint16_t *row = dv.krow(b, h, perm[m]);
-        uint2 wv = *reinterpret_cast<const uint2 *>(row + lane * 4);
-        acc[0].add(bf_lo(wv.x));
-        acc[1].add(bf_hi(wv.x));
-        acc[2].add(bf_lo(wv.y));
-        acc[3].add(bf_hi(wv.y));
+    // members are loaded UP_BATCH at a time (their latencies overlap) and added in order
+    constexpr int UP_BATCH = 8;
+    for (int m = m0; m < m1; m += UP_BATCH) {
+        uint2 wv[UP_BATCH];
+#pragma unroll
+        for (int j = 0; j < UP_BATCH; ++j)
+            if (m + j < m1) wv[j] = *reinterpret_cast<const uint2 *>(dv.krow(b, h, perm[m + j]) + lane * 4);
+#pragma unroll
+        for (int j = 0; j < UP_BATCH; ++j)
+            if (m + j < m1) {
+                acc[0].add(bf_lo(wv[j].x));
+                acc[1].add(bf_hi(wv[j].x));
+                acc[2].add(bf_lo(wv[j].y));
+                acc[3].add(bf_hi(wv[j].y));
+            }
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
