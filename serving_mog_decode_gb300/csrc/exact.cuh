@@ -32,4 +32,38 @@ __device__ __forceinline__ double exact_dist(const uint16_t *x, const float *c) 
     return acc;
 }
 
+// A double-float evaluation of D(x, c) (x fp32 values of bf16 keys, c fp32): each
+// difference is split exactly into hi + lo (two-sum), its square into the exact product
+// dh^2 (the fused multiply-add's residual) plus 2 dh dl (dl^2 < 2^-48 dh^2 is dropped), and
+// the terms are summed in a (hi, lo) pair.  The low word gathers at most 4 * 2^-24 of
+// each term; its own rounding is at most 2^9 * 2^-48 of D a step, so over d = 128 terms
+// the pair is within 2^-31 D of the exact sum (kDfRel carries a safety factor of 20 over
+// that).  The fp64 rule of D sums exact squares (the differences of fp32 values and
+// their squares fit in 53 bits) with 127 roundings, within 2^-46 D of the exact sum: a
+// best candidate whose double-float value is below every other by more than both bounds
+// is the fp64 argmin.
+constexpr double kDfRel = 1e-8;
+
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ double df_dist(const float *x, const float *c) {
+    float sh = 0.f, sl = 0.f;
+    for (int j = 0; j < MOG_D; ++j) {
+        float dh, dl;
+        two_sum(x[j], -c[j], dh, dl);
+        const float ph = __fmul_rn(dh, dh);
+        float pl = __fmaf_rn(dh, dh, -ph);
+        pl = __fmaf_rn(__fmul_rn(2.f, dh), dl, pl);
+        float s, e;
+        two_sum(sh, ph, s, e);
+        sh = s;
+        sl = __fadd_rn(sl, __fadd_rn(e, pl));
+    }
+    return __dadd_rn((double)sh, (double)sl);
+}
+
 }  // namespace mog

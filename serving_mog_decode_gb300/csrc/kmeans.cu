@@ -261,6 +261,8 @@ __global__ void __launch_bounds__(AS_THREADS) k_assign_l1(AssignJob jb) {
 constexpr int FB_THREADS = 256;
 constexpr int FB_CTAS = 64;  // CTAs per unit
 
+constexpr int FB_KEEP = 32;  // fp32 distances a lane keeps in registers (k <= 1024)
+
 __global__ void __launch_bounds__(FB_THREADS) k_assign_fallback(AssignJob jb) {
     __shared__ __align__(16) float xs_all[FB_THREADS / 32][MOG_D];
     const int u = blockIdx.y;
@@ -316,29 +318,79 @@ __global__ void __launch_bounds__(FB_THREADS) k_assign_fallback(AssignJob jb) {
             }
             return (a0 + a1) + (a2 + a3);
         };
+        // fp32 distances to every centroid, kept in registers when k <= FB_KEEP * 32
+        float dk[FB_KEEP];
+        const bool keep = k <= FB_KEEP * 32;
         float b32 = INFINITY;
-        for (int c = lane; c < k; c += 32) b32 = fminf(b32, dist32(c));
+        if (keep) {
+#pragma unroll
+            for (int i = 0; i < FB_KEEP; ++i) {
+                const int c = lane + 32 * i;
+                dk[i] = c < k ? dist32(c) : INFINITY;
+                b32 = fminf(b32, dk[i]);
+            }
+        } else {
+            for (int c = lane; c < k; c += 32) b32 = fminf(b32, dist32(c));
+        }
         b32 = warp_min(b32);
         // every centroid whose exact distance can be the smallest (kCertRel is above the
         // relative fp32 error on each side)
         const float thr = b32 * (1.f + 2.5f * kCertRel);
-        double best = INFINITY;
-        int bi = 0x7fffffff;
-        for (int c = lane; c < k; c += 32) {
-            if (dist32(c) > thr) continue;
-            double dd = exact_dist(xr, cent + (int64_t)c * MOG_D);
-            if (dd < best) {
-                best = dd;
-                bi = c;
+        auto d32 = [&](int i, int c) { return keep ? dk[i] : dist32(c); };
+        // the candidates' double-float distances: the best and the runner-up over the warp
+        double v1 = INFINITY, v2 = INFINITY;
+        int i1 = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < FB_KEEP; ++i) {
+            for (int c = lane + 32 * i; c < k; c += 32 * FB_KEEP) {  // (one pass when kept)
+                if (d32(i, c) > thr) continue;
+                const double v = df_dist(xs, cent + (int64_t)c * MOG_D);
+                if (v < v1) {
+                    v2 = v1;
+                    v1 = v;
+                    i1 = c;
+                } else if (v < v2) {
+                    v2 = v;
+                }
             }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            double ob = __shfl_xor_sync(0xffffffffu, best, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ob < best || (ob == best && oi < bi)) {
-                best = ob;
-                bi = oi;
+            const double ov1 = __shfl_xor_sync(0xffffffffu, v1, o), ov2 = __shfl_xor_sync(0xffffffffu, v2, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, i1, o);
+            if (ov1 < v1 || (ov1 == v1 && oi < i1)) {
+                v2 = fmin(v1, ov2);
+                v1 = ov1;
+                i1 = oi;
+            } else {
+                v2 = fmin(v2, ov1);
+            }
+        }
+        double best = v1;
+        int bi = i1;
+        const double win = 2.0 * kDfRel * v2 + 1e-300;  // both values' bounds, and zero
+        if (v2 != INFINITY && !(v2 - v1 > win)) {  // (a single candidate is the argmin)
+            // not separated: the fp64 rule over every candidate that may be the smallest
+            best = INFINITY;
+            bi = 0x7fffffff;
+            const double lim = v1 + win;  // the fp64 argmin's double-float value is below this
+            for (int c = lane; c < k; c += 32) {
+                if (dist32(c) > thr) continue;  // (rare: recomputed)
+                if (df_dist(xs, cent + (int64_t)c * MOG_D) > lim) continue;
+                const double dd = exact_dist(xr, cent + (int64_t)c * MOG_D);
+                if (dd < best) {
+                    best = dd;
+                    bi = c;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ob < best || (ob == best && oi < bi)) {
+                    best = ob;
+                    bi = oi;
+                }
             }
         }
         if (lane == 0) {
