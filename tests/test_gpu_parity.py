@@ -648,10 +648,10 @@ def test_sliding_window_union_exact_ragged_batch():
     print("sliding + union-exact: stats", _check_stats(inj), "decode", _check_decode_union(inj))
 
 
-def _check_decode_group(inj):
+def _check_decode_group(inj, om64=None):
     """Group-shared selection: the GPU's selection against the oracle's group selection
     (differences only at near-ties), repeated for every head; then every head's output
-    under the oracle's group selection."""
+    under the oracle's group selection (with om64: the oracle's feature-map decode)."""
     w, G = inj.w, inj.w.group
     tc, ts, SW = w.top_c, w.top_s, w.top_c + w.top_c * w.top_s
     U = w.batch * w.h_kv
@@ -688,8 +688,9 @@ def _check_decode_group(inj):
         b, h = u // w.h_kv, u % w.h_kv
         s = inj.summ[(b, h)]
         for g in range(G):
-            ref, _ = ora.decode(inj.K[b, h], inj.V[b, h], int(inj.lens[b]), inj.q[b, h * G + g], s,
-                                sel_ref[u * G + g, :tc], sel_ref[u * G + g, tc:].reshape(tc, ts))
+            args = (inj.K[b, h], inj.V[b, h], int(inj.lens[b]), inj.q[b, h * G + g], s,
+                    sel_ref[u * G + g, :tc], sel_ref[u * G + g, tc:].reshape(tc, ts))
+            ref, _ = ora.decode(*args) if om64 is None else ora.decode_fm(*args, om64)
             e = rel(out[u * G + g], ref)
             worst = max(worst, e)
             assert e <= OUT_TOL, (u, g, e)
@@ -1166,6 +1167,17 @@ def test_fm_residual_sums_and_decode_match_oracle():
     inj.h.feature_map(om32)
     print("fm sums worst", _check_fm_sums(inj, om64))
     print("fm decode (near-ties, worst)", _check_decode_fm(inj, om64))
+
+
+def test_fm_residual_with_group_selection():
+    """residual = 2 with the group-shared selection: every head subtracts the group's chosen
+    subclusters; outputs against the oracle's feature-map decode under the group's
+    selection."""
+    w = small_workload(2500, batch=2, h_kv=2, h_q=8, top_c=5, top_s=3, seed=48)
+    inj = Injected(w, group_select=1, residual=2)
+    om32, om64 = _omega(49)
+    inj.h.feature_map(om32)
+    print("fm + group-shared decode", _check_decode_group(inj, om64))
 
 
 def test_fm_residual_full_size_qwen3_4b():
