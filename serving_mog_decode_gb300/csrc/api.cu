@@ -141,10 +141,10 @@ int make_plan(const mog_params *p, const int32_t *lengths_host, Plan *pl) {
     if (std::min(P.c_max, P.G * P.tc) > MOG_MAX_UNION || P.tc > MOG_MAX_UNION) return MOG_ERR_SHAPE;
     if (slot_smem_bytes(P.G, P.c_max, P.l_max, P.tc) > 226 * 1024) return MOG_ERR_SHAPE;  // decode shared memory
     const int sms = num_sms();
-    // rows kernel: one wave of two CTAs per SM; with so many units that a wave gives each
+    // rows kernel: one wave of three CTAs per SM; with so many units that a wave gives each
     // fewer than four CTAs, four per unit over several waves, which the CTA scheduler
     // balances across units of different lengths
-    P.P = std::min(MAX_SPLITS, std::max(4, 2 * sms / P.units));
+    P.P = std::min(MAX_SPLITS, std::max(4, 3 * sms / P.units));
     // the sort workspace covers the longest mid region a later re-clustering can see
     P.nchunks = std::max(1, (int)ceil_div64(std::max(P.n_mid_max, p->n_cap - p->n_recent - p->n_sink),
                                             SORT_CHUNK));

@@ -612,10 +612,15 @@ __global__ void __launch_bounds__(md_warps(GT) * 32, md_min_blocks(GT)) k_mog_de
 constexpr int RW_SUPER = 256;                  // row positions per batch in the rows kernel
 constexpr int RW_TPB = RW_SUPER / AT_ROWS;     // tiles per batch
 constexpr int RW_PER = RW_SUPER / AT_THREADS;  // positions a thread fetches per batch
-constexpr int RW_SEGW = 512;                   // row segments held in shared memory
-static_assert(RW_TPB >= AT_STAGES - 1, "the first batch must cover the pipeline's prologue");
+constexpr int RW_SEGW = 256;                   // row segments held in shared memory
+// Two tile stages (one copy in flight while the other is computed) keep a CTA at 74.6 KB
+// of shared memory, so three CTAs fit on an SM: more warps to hide the tile computation's
+// latencies, and more copies in flight per SM than two CTAs with three stages.
+constexpr int RW_STAGES = 2;
+constexpr int RW_SMEM = RW_STAGES * AT_STAGE_BYTES;
+static_assert(RW_TPB >= RW_STAGES - 1, "the first batch must cover the pipeline's prologue");
 
-// Kernel B: grid (P, units), 4 warps, two CTAs per SM.  Rows [p*T/P, (p+1)*T/P) of the
+// Kernel B: grid (P, units), 4 warps, three CTAs per SM.  Rows [p*T/P, (p+1)*T/P) of the
 // unit's exact list (anchors, then the chosen subclusters' rows, segment by segment)
 // through the 64-row tile engine.  A window of segments sits in shared memory; a row's
 // position is read from the partition (perm) at its segment's offset.  Positions are
@@ -739,7 +744,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     };
     auto issue = [&](int t) {  // (the warm-up tile is zero-filled: no rows are read)
         const int buf = (t / RW_TPB) & 1, rb = (t % RW_TPB) * AT_ROWS;
-        issue_tile(tile + (t % AT_STAGES) * AT_STAGE_BYTES, dry ? 0 : min(AT_ROWS, nrow - t * AT_ROWS), kb, vb,
+        issue_tile(tile + (t % RW_STAGES) * AT_STAGE_BYTES, dry ? 0 : min(AT_ROWS, nrow - t * AT_ROWS), kb, vb,
                    ra, [&](int r, int64_t &pos, uint32_t &mk) {
                        int pp = s_pos[buf][rb + r];
                        uint32_t mm = s_mk[buf][rb + r];
@@ -763,7 +768,7 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     const float *rx = dv.resx + (size_t)u * dv.resx_stride;
     const size_t ug = (size_t)u * dv.c_max, usg = ug * dv.l_max;
     auto issue_terms = [&](int t, int tr) {  // tile t of the stream = terms tile tr
-        uint8_t *stg = tile + (t % AT_STAGES) * AT_STAGE_BYTES;
+        uint8_t *stg = tile + (t % RW_STAGES) * AT_STAGE_BYTES;
         const int i0 = ia + tr * (AT_ROWS / 2), cnt = min(AT_ROWS / 2, ib - i0);
         const uint32_t sv = smem_u32(stg) + AT_TILE_BYTES;
         uint32_t *smk = reinterpret_cast<uint32_t *>(stg + 2 * AT_TILE_BYTES);
@@ -804,14 +809,14 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
     }
     __syncthreads();
 #pragma unroll
-    for (int s2 = 0; s2 < AT_STAGES - 1; ++s2) {
+    for (int s2 = 0; s2 < RW_STAGES - 1; ++s2) {
         if (s2 < nt) issue(s2);
         cp_async_commit();
     }
     for (int t = 0; t < nt; ++t) {
-        cp_async_wait<AT_STAGES - 2>();
+        cp_async_wait<RW_STAGES - 2>();
         __syncthreads();
-        const int ti = t + AT_STAGES - 1;
+        const int ti = t + RW_STAGES - 1;
         int next = -1;  // batch whose positions are fetched after this tile's compute
         if (ti < nt) {
             if (ti % RW_TPB == 0) {  // first tile of a batch: its positions go to shared memory
@@ -823,23 +828,23 @@ __global__ void __launch_bounds__(AT_THREADS) k_mog_rows(DecArgs a) {
             issue(ti);
         }
         cp_async_commit();
-        compute_tile(acc, qf, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
+        compute_tile(acc, qf, tile + (t % RW_STAGES) * AT_STAGE_BYTES, scale2);
         if (next >= 0) fetch(next);
     }
     cp_async_wait<0>();
     __syncthreads();
     // the residual terms: the same pipeline over nr tiles of given logits
 #pragma unroll
-    for (int s2 = 0; s2 < AT_STAGES - 1; ++s2) {
+    for (int s2 = 0; s2 < RW_STAGES - 1; ++s2) {
         if (s2 < nr) issue_terms(s2, s2);
         cp_async_commit();
     }
     for (int t = 0; t < nr; ++t) {
-        cp_async_wait<AT_STAGES - 2>();
+        cp_async_wait<RW_STAGES - 2>();
         __syncthreads();
-        if (t + AT_STAGES - 1 < nr) issue_terms(t + AT_STAGES - 1, t + AT_STAGES - 1);
+        if (t + RW_STAGES - 1 < nr) issue_terms(t + RW_STAGES - 1, t + RW_STAGES - 1);
         cp_async_commit();
-        compute_tile<NB, true>(acc, qf, tile + (t % AT_STAGES) * AT_STAGE_BYTES, scale2);
+        compute_tile<NB, true>(acc, qf, tile + (t % RW_STAGES) * AT_STAGE_BYTES, scale2);
     }
     cp_async_wait<0>();
     __syncthreads();
@@ -1052,11 +1057,11 @@ static cudaError_t launch_steps(const DecArgs &a, cudaStream_t s, cudaEvent_t co
     const bool fm = dv.residual == MOG_RESIDUAL_FEATURE_MAP;
     if (fm && (e = launch_fm_resid(dv, a.q, a.SW, s)) != cudaSuccess) return e;  // (timed with the rows)
     const void *rows_fn = dv.bt ? (const void *)k_mog_rows<GT, true> : (const void *)k_mog_rows<GT, false>;
-    if ((e = ensure_smem(rows_fn, AT_SMEM)) != cudaSuccess) return e;
+    if ((e = ensure_smem(rows_fn, RW_SMEM)) != cudaSuccess) return e;
     if (dv.bt)
-        e = launch_pdl(k_mog_rows<GT, true>, dim3(dv.P, dv.units), dim3(AT_THREADS), AT_SMEM, s, a);
+        e = launch_pdl(k_mog_rows<GT, true>, dim3(dv.P, dv.units), dim3(AT_THREADS), RW_SMEM, s, a);
     else
-        e = launch_pdl(k_mog_rows<GT, false>, dim3(dv.P, dv.units), dim3(AT_THREADS), AT_SMEM, s, a);
+        e = launch_pdl(k_mog_rows<GT, false>, dim3(dv.P, dv.units), dim3(AT_THREADS), RW_SMEM, s, a);
     if (e != cudaSuccess) return e;
     if (events && (e = cudaEventRecord(events[2], s)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_mog_merge, dim3(dv.G, dv.units), dim3(MG_THREADS), 0, s,
