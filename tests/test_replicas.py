@@ -118,3 +118,15 @@ def test_bench_counts_algorithmic_bytes_from_the_selection():
     assert by["attend"] == 512 + 3 * 12 + 10 * 4 + 24 * 512 + 7 * (512 + 16) + 4 * 2 * 132 * 4
     assert by["merge"] == 4 * 2 * 132 * 4 + 2 * 128 * 4
     assert by["step"] == by["select"] + by["attend"] + by["merge"]
+    # fp8 summaries: 1 byte a mean or variance element, the terms' value means' high parts
+    b8 = bench.bytes_from_selection(H(), W(), sel, np.array([100]), [100], sb=1)
+    assert b8["select"] == 512 + 3 * (2 * 128 + 4) + 2 * (2 * (2 * 128 + 8) + 4) + 3 * 12 + 7 * 16
+    assert b8["attend"] == 512 + 3 * 12 + 10 * 4 + 24 * 512 + 7 * (256 + 16) + 4 * 2 * 132 * 4
+    # the feature-map residual: no Gaussian terms in the rows kernel; per head the unit's
+    # feature sums and those of its chosen subclusters (32 x 132 floats each), 33 vectors out
+    bf = bench.bytes_from_selection(H(), W(), sel, np.array([100]), [100], resid=2)
+    row, vec = 32 * 132 * 4, 33 * 132 * 4
+    assert bf["attend"] == 512 + 3 * 12 + 10 * 4 + 24 * 512 + 4 * 2 * 132 * 4
+    assert bf["fm"] == (256 + 4 * 4 + 3 * row + vec) + (256 + 4 * 4 + 2 * row + vec)
+    assert bf["merge"] == 4 * 2 * 132 * 4 + 2 * 128 * 4 + 2 * (vec + 4)
+    assert bf["step"] == bf["select"] + bf["attend"] + bf["merge"] + bf["fm"]
