@@ -211,7 +211,7 @@ typedef struct mog_layout {
     /* MOG_RESIDUAL_FEATURE_MAP (else 0): f32 [units][c_max*l_max][MOG_FM_FEATURES][d+4]
      * feature sums of every subcluster, row i holding sum over members of
      * exp(w_i.k~ - |k~|^2/2 - M_i) v_k in [0, d) and the same sum without v at d (entries
-     * d+1 .. d+3 unused), scaled by M_i = |w_i|^2/2 - 40; and f32
+     * d+1 .. d+3 zero), scaled by M_i = |w_i|^2/2 - 40; and f32
      * [units][MOG_FM_FEATURES][d+4] their sum per unit */
     int64_t fm_z, fm_t;
 } mog_layout;

@@ -120,12 +120,14 @@ __global__ void __launch_bounds__(FM_THREADS) k_fm_stats(Dev dv) {
             cacc[q] += acc[q];
         }
         if (fj == 0) z[MOG_D] = den;
+        if (fj < FM_W - MOG_D - 1) z[MOG_D + 1 + fj] = 0.f;  // the row's padding
         cden += den;
     }
     float *zc = dv.fm_zc + (((int64_t)u * dv.c_max + c) * FM_M + fi) * FM_W;
 #pragma unroll
     for (int q = 0; q < MOG_D / 8; ++q) zc[fj + 8 * q] = cacc[q];
     if (fj == 0) zc[MOG_D] = cden;
+    if (fj < FM_W - MOG_D - 1) zc[MOG_D + 1 + fj] = 0.f;
 }
 
 // T[u] = the sum of the unit's cluster sums, in cluster order: one thread per entry.
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(FM_THREADS) k_fm_resid(Dev dv, const uint16_t 
         s_qq = s;
     }
     __syncthreads();
-    // a_i: warp w takes features 4w .. 4w + 3
+    // a_i: warp w takes features FM_M / 8 at a time (4w .. 4w + 3)
     for (int f = 0; f < FM_M / (FM_THREADS / 32); ++f) {
         const int i = warp * (FM_M / (FM_THREADS / 32)) + f;
         float s = 0.f;
