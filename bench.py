@@ -632,7 +632,8 @@ def run_gpu(a, w, rank, world):
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / world, 3), "unit": "us/step/layer",
                 "h2d_bytes_per_step": int(q_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 4)},
         "append": append,
-        "gpu_launches": 3 * a.steps,  # selection, rows and merge kernels per step
+        # selection, rows and merge kernels per step (and the feature-map kernel with it)
+        "gpu_launches": (4 if a.fm_residual else 3) * a.steps,
         "clocks": clk,
     }
     if rank == 0 and a.cpu_seconds <= 0:   # timing experiments only: no CPU baseline
